@@ -1,0 +1,562 @@
+"""Plain fp64 CPU oracle of the Prism hot path.  TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+reference leg of ``bench.py`` may import this module.  The CUDA path shares no
+code with it and never calls it.
+
+"Prism" below is the paper *Prism: Dynamic Sparse Attention for Native 2K
+Joint Video-Audio Generation Model Training* (arXiv 2610.05416) as printed on
+its abstract, figure and table pages.  The pages give the method only in prose
+(Abstract; Fig. 2 caption) and table captions (Tables 7, 9, 10, 11, 12); the
+equations they refer to (Eq. 1, Eq. 7) are not printed.  Where a step is left
+open, the plainest reading is taken and marked READING.
+
+Steps, in the order the pages give them:
+  1. zone statistics            -- ``zone_stats``
+  2. block shape per zone       -- ``assign_shapes``
+     and the token permutation  -- ``build_permutation`` / ``permute``
+  3. block-mean Q/K, scores     -- ``pool``, ``block_scores``
+  4. hybrid Top-k / Top-p       -- ``hybrid_select_row`` / ``select_blocks``
+  5. block-sparse attention     -- ``attn_fwd_row`` / ``attn_bwd``
+     and the inverse permutation-- ``unpermute``
+plus two independent references used as pins: ``dense_attention`` (plain
+softmax attention in the original token order) and ``masked_attention``
+(explicit N x N token mask, original order, forward and VJP).
+
+Everything is computed in float64 from the bf16-rounded inputs.
+Parity pinned by the tests in tests/test_oracle_*.py, except the reading of the
+unprinted Eq. 1 / Eq. 7 / gate / combination, which is parity unpinned: the
+pages do not print them, so only their special cases can be checked.
+"""
+from __future__ import annotations
+
+import math
+from typing import List, Sequence, Tuple
+
+import numpy as np
+
+f64 = np.float64
+
+
+# --------------------------------------------------------------------------
+# geometry
+# --------------------------------------------------------------------------
+
+def padded_grid(T: int, Hg: int, W: int, zone: Sequence[int]) -> Tuple[int, int, int]:
+    """READING (Prism, Abstract: macro-zones tile the token grid): each axis is
+    padded up to a multiple of the zone extent; padded tokens are not real."""
+    zT, zH, zW = zone
+    return (-(-T // zT) * zT, -(-Hg // zH) * zH, -(-W // zW) * zW)
+
+
+def admissible_shapes(menu: Sequence[Sequence[int]], zone: Sequence[int]) -> List[int]:
+    """READING: a menu shape (bT, bH, bW) may be given to a zone only when it
+    tiles the zone exactly, i.e. each block extent divides the zone extent."""
+    return [k for k, b in enumerate(menu)
+            if zone[0] % b[0] == 0 and zone[1] % b[1] == 0 and zone[2] % b[2] == 0]
+
+
+def _grid_views(x: np.ndarray, w, C: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Scatter a real-token array x [N, C] onto the padded grid and view it as
+    [Zt, zT, Zh, zH, Zw, zW, C]; also return the matching validity mask."""
+    Tp, Hp, Wp = padded_grid(w.T, w.Hg, w.W, w.zone)
+    zT, zH, zW = w.zone
+    g = np.zeros((Tp, Hp, Wp, C), dtype=f64)
+    g[: w.T, : w.Hg, : w.W] = x.reshape(w.T, w.Hg, w.W, C)
+    m = np.zeros((Tp, Hp, Wp), dtype=bool)
+    m[: w.T, : w.Hg, : w.W] = True
+    g = g.reshape(Tp // zT, zT, Hp // zH, zH, Wp // zW, zW, C)
+    m = m.reshape(Tp // zT, zT, Hp // zH, zH, Wp // zW, zW)
+    return g, m
+
+
+# --------------------------------------------------------------------------
+# step 1: zone statistics
+# --------------------------------------------------------------------------
+
+def line_variance(g: np.ndarray, m: np.ndarray, axis: int) -> np.ndarray:
+    """Directional variance of every zone along one grid axis.
+
+    g: [Zt, zT, Zh, zH, Zw, zW, C] values, m: the validity mask without C.
+    axis: 0 = T, 1 = H, 2 = W.
+    READING of Prism's per-channel variance (Table 9 caption, "Eq. 1", not
+    printed): a line along an axis is the set of valid tokens of a zone that
+    share the other two coordinates.  For each line with at least two valid
+    tokens and each channel, take the population variance of the values on the
+    line; the zone's statistic is the plain mean of those over all such lines
+    and all channels.  Returns [Zt, Zh, Zw]; 0 where no line qualifies.
+    """
+    inner = (1, 3, 5)[axis]
+    mf = m.astype(f64)[..., None]
+    n = mf.sum(axis=inner, keepdims=True)                      # valid tokens per line
+    mean = (g * mf).sum(axis=inner, keepdims=True) / np.maximum(n, 1.0)
+    var = (mf * (g - mean) ** 2).sum(axis=inner, keepdims=True) / np.maximum(n, 1.0)
+    ok = (n >= 2.0)                                            # qualifying lines
+    var = np.where(ok, var, 0.0)
+    # mean over the lines (the other two in-zone axes) and the channels
+    other = tuple(a for a in (1, 3, 5) if a != inner)
+    num = var.sum(axis=(inner,) + other + (6,))
+    cnt = ok.astype(f64).sum(axis=(inner,) + other) * g.shape[6]
+    cnt = cnt[..., 0] if cnt.ndim == num.ndim + 1 else cnt
+    return np.where(cnt > 0, num / np.maximum(cnt, 1.0), 0.0)
+
+
+def zone_stats(w, V: np.ndarray, a2v: np.ndarray) -> np.ndarray:
+    """Per (b, h, zone) statistics, [B, H, Z, 8] float64:
+    (var_v_T, var_v_H, var_v_W, var_n_T, var_n_H, var_n_W, nbar, n_valid).
+
+    * var_v_d: directional variance of the VALUE features of head h
+      (Prism, Table 9 caption: the default uses value features; the query/key
+      variants are ablations) -- ``line_variance`` along d.
+    * n_i = ||a2v_i||_2: per-token norm of the audio-to-video cross-attention
+      output (Prism, Abstract: feature norms from the A2V cross-attention).
+      var_n_d: the same directional variance of the scalar map n (READING of
+      the audio directional variance v_hat_{a,d} of Table 9's caption).
+      nbar: mean of n over the zone's valid tokens (READING of the audio
+      coupling gate's input, Table 9 caption).
+    V: [B, N, H, d], a2v: [B, N, Ca] (any float dtype; used as float64).
+    """
+    B, N, H, d = V.shape
+    out = []
+    for b in range(B):
+        n_tok = np.sqrt((a2v[b].astype(f64) ** 2).sum(axis=-1))          # [N]
+        gn, m = _grid_views(n_tok[:, None], w, 1)
+        sn = np.stack([line_variance(gn, m, a) for a in range(3)], -1)    # [Zt,Zh,Zw,3]
+        mf = m.astype(f64)
+        cnt = mf.sum(axis=(1, 3, 5))
+        nbar = np.where(cnt > 0, (gn[..., 0] * mf).sum(axis=(1, 3, 5)) / np.maximum(cnt, 1), 0.0)
+        per_h = []
+        for h in range(H):
+            gv, _ = _grid_views(V[b, :, h, :].astype(f64), w, d)
+            sv = np.stack([line_variance(gv, m, a) for a in range(3)], -1)
+            st = np.concatenate([sv, sn, nbar[..., None], cnt[..., None]], -1)
+            per_h.append(st.reshape(-1, 8))
+        out.append(np.stack(per_h))
+    return np.stack(out)
+
+
+# --------------------------------------------------------------------------
+# step 2: block shape per zone (Eq. 7) and token permutation
+# --------------------------------------------------------------------------
+
+def guidance(w, st: np.ndarray, nbar_max: float) -> np.ndarray:
+    """g_d for one zone from its statistics row st[8].
+
+    READING (Prism, Table 9 caption names r_{v,d}, a_bar and v_hat_{a,d};
+    Table 12 ablates each guidance):
+      r_{v,d}     = var_v_d / sum_d var_v_d      (1/3 each when the sum is 0)
+      v_hat_{a,d} = var_n_d / sum_d var_n_d      (1/3 each when the sum is 0)
+      a_bar       = nbar / max over zones of nbar (0 when that max is 0)
+      g_d = u_v r_{v,d} + u_a a_bar v_hat_{a,d} + eps
+    with u_v, u_a the video/audio guidance switches.
+    """
+    sv, sn = st[0:3], st[3:6]
+    r = sv / sv.sum() if sv.sum() > 0 else np.full(3, 1.0 / 3.0)
+    vh = sn / sn.sum() if sn.sum() > 0 else np.full(3, 1.0 / 3.0)
+    abar = st[6] / nbar_max if nbar_max > 0 else 0.0
+    uv = 1.0 if w.use_video else 0.0
+    ua = 1.0 if w.use_audio else 0.0
+    return uv * r + ua * abar * vh + w.eps
+
+
+def shape_costs(w, g: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Eq. 7 (Prism, Table 10 caption: b*_d is proportional to g_d^-alpha).
+
+    READING: with the token count fixed at S = bT bH bW, the continuous optimum
+    is log2 b*_d = log2(S)/3 + alpha (mean_d log2 g_d - log2 g_d).  Each
+    admissible menu shape is scored by sum_d (log2 b_d - log2 b*_d)^2.
+    Returns (costs over the admissible shapes, their menu indices)."""
+    S = w.block
+    lg = np.log2(g)
+    lstar = math.log2(S) / 3.0 + w.alpha * (lg.mean() - lg)
+    idx = admissible_shapes(w.menu, w.zone)
+    costs = np.array([sum((math.log2(w.menu[k][dd]) - lstar[dd]) ** 2 for dd in range(3))
+                      for k in idx], dtype=f64)
+    return costs, np.array(idx)
+
+
+SHAPE_TIE = 1e-4
+
+
+def assign_shapes(w, stats: np.ndarray):
+    """Shape id per (b, h, zone) -> (shape_id [B,H,Z] int, near_tie [B,H,Z] bool).
+
+    The admissible shape of least cost wins; an exact tie goes to the lowest
+    menu index.  A zone whose best and second-best costs differ by less than
+    SHAPE_TIE is flagged as a near tie (either shape is then accepted).
+    With per_head False, the video statistics are averaged over heads first and
+    every head gets the same shape (Prism, Table 10 caption ablates per-head
+    shapes)."""
+    B, H, Z, _ = stats.shape
+    if not admissible_shapes(w.menu, w.zone):
+        raise ValueError("no admissible shape for this zone")
+    sid = np.zeros((B, H, Z), dtype=np.int64)
+    tie = np.zeros((B, H, Z), dtype=bool)
+    for b in range(B):
+        for h in range(H):
+            st_h = stats[b, h] if w.per_head else stats[b].mean(axis=0)
+            nmax = st_h[:, 6].max()
+            for z in range(Z):
+                costs, idx = shape_costs(w, guidance(w, st_h[z], nmax))
+                k = int(np.argmin(costs))            # first minimum = lowest menu index
+                sid[b, h, z] = idx[k]
+                if len(costs) > 1:
+                    srt = np.sort(costs)
+                    tie[b, h, z] = (srt[1] - srt[0]) < SHAPE_TIE
+    return sid, tie
+
+
+def build_permutation(w, shape_id: np.ndarray):
+    """Token order for every (b, h): zones in raster (zt, zh, zw) order, the
+    zone's blocks in raster order of its chosen shape, and inside a block its
+    valid tokens first in (t, h, w) raster order, then its padding slots.
+
+    READING (Prism, Abstract: tokens inside a block stay together; the pages do
+    not give an order).  Returns perm [B,H,Np] (slot -> real token, -1 for a
+    padding slot), inv [B,H,N] (token -> slot), n_valid [B,H,nb]."""
+    B, H, Z = shape_id.shape
+    Tp, Hp, Wp = padded_grid(w.T, w.Hg, w.W, w.zone)
+    zT, zH, zW = w.zone
+    nzT, nzH, nzW = Tp // zT, Hp // zH, Wp // zW
+    S = w.block
+    Np = Tp * Hp * Wp
+    nb = Np // S
+    perm = np.full((B, H, Np), -1, dtype=np.int64)
+    inv = np.full((B, H, w.N), -1, dtype=np.int64)
+    nvalid = np.zeros((B, H, nb), dtype=np.int64)
+    for b in range(B):
+        for h in range(H):
+            slot = 0
+            blk = 0
+            for z in range(Z):
+                zt, zh, zw = z // (nzH * nzW), (z // nzW) % nzH, z % nzW
+                bT, bH, bW = w.menu[int(shape_id[b, h, z])]
+                for it in range(zT // bT):
+                    for ih in range(zH // bH):
+                        for iw in range(zW // bW):
+                            toks = []
+                            for t in range(bT):
+                                for y in range(bH):
+                                    for x in range(bW):
+                                        tt = zt * zT + it * bT + t
+                                        yy = zh * zH + ih * bH + y
+                                        xx = zw * zW + iw * bW + x
+                                        if tt < w.T and yy < w.Hg and xx < w.W:
+                                            toks.append((tt * w.Hg + yy) * w.W + xx)
+                            for k, n in enumerate(toks):
+                                perm[b, h, slot + k] = n
+                                inv[b, h, n] = slot + k
+                            nvalid[b, h, blk] = len(toks)
+                            slot += S
+                            blk += 1
+    return perm, inv, nvalid
+
+
+def permute(X: np.ndarray, perm: np.ndarray) -> np.ndarray:
+    """X [B, N, H, d] -> Xp [B, H, Np, d] in block order; padding slots are 0."""
+    B, N, H, d = X.shape
+    Np = perm.shape[2]
+    Xp = np.zeros((B, H, Np, d), dtype=f64)
+    for b in range(B):
+        for h in range(H):
+            ok = perm[b, h] >= 0
+            Xp[b, h, ok] = X[b, perm[b, h, ok], h].astype(f64)
+    return Xp
+
+
+def unpermute(Xp: np.ndarray, inv: np.ndarray) -> np.ndarray:
+    """Inverse of ``permute``: Xp [B, H, Np, d] -> X [B, N, H, d]."""
+    B, H, Np, d = Xp.shape
+    N = inv.shape[2]
+    X = np.zeros((B, N, H, d), dtype=f64)
+    for b in range(B):
+        for h in range(H):
+            X[b, :, h] = Xp[b, h, inv[b, h]]
+    return X
+
+
+# --------------------------------------------------------------------------
+# step 3: block-level features and scores
+# --------------------------------------------------------------------------
+
+def pool(Xp: np.ndarray, n_valid: np.ndarray, S: int) -> np.ndarray:
+    """Block-level feature = mean of the block's valid tokens (READING of the
+    pages' block-level features, Prism Abstract; valid slots come first in a
+    block).  Xp [B,H,Np,d], n_valid [B,H,nb] -> [B,H,nb,d]; 0 for empty blocks."""
+    B, H, Np, d = Xp.shape
+    nb = Np // S
+    out = np.zeros((B, H, nb, d), dtype=f64)
+    blocks = Xp.reshape(B, H, nb, S, d)
+    for b in range(B):
+        for h in range(H):
+            for i in range(nb):
+                nv = int(n_valid[b, h, i])
+                if nv > 0:
+                    out[b, h, i] = blocks[b, h, i, :nv].sum(axis=0) / nv
+    return out
+
+
+def block_scores(Qbar: np.ndarray, Kbar: np.ndarray, d: int) -> np.ndarray:
+    """Query-block x key-block score Qbar Kbar^T / sqrt(d) for one (b, h)
+    (Prism, Fig. 2 caption: block-sparse attention over block scores; READING:
+    the usual 1/sqrt(d) scale, no bias)."""
+    return (Qbar @ Kbar.T) / math.sqrt(d)
+
+
+# --------------------------------------------------------------------------
+# step 4: hybrid Top-k / Top-p selection
+# --------------------------------------------------------------------------
+
+TIE_SCORE = 1e-6
+TIE_MASS = 1e-6
+
+
+def topp_count(probs_sorted: np.ndarray, p: float) -> int:
+    """Top-p (Prism, Table 7 caption): the smallest number of key blocks, taken
+    in decreasing weight, whose cumulative weight is strictly greater than p;
+    all of them when no prefix gets there.  READING: for p >= 1 no prefix can
+    exceed p (the weights sum to 1), so every candidate is kept; this is
+    stated explicitly so that rounding of the running sum cannot end early."""
+    if p >= 1.0:
+        return len(probs_sorted)
+    acc = 0.0
+    for m, q in enumerate(probs_sorted, start=1):
+        acc += q
+        if acc > p:
+            return m
+    return len(probs_sorted)
+
+
+def hybrid_select_probs(probs: np.ndarray, order: np.ndarray, kf: int, p: float) -> int:
+    """Number of blocks kept for one query block given its candidates'
+    probabilities and their ranking: at least the Top-k floor (capped at the
+    candidate count) and at least the Top-p count (READING of Prism's hybrid
+    rule, Abstract and Fig. 2 caption: the count varies per query block)."""
+    nv = len(order)
+    mp = topp_count(probs[order], p)
+    return max(min(kf, nv), mp)
+
+
+def hybrid_select_row(scores: np.ndarray, valid: np.ndarray, kf: int, p: float):
+    """Selection for one query block.
+
+    scores: [nb] block scores, valid: [nb] bool (key block has valid tokens).
+    Candidates are ranked by (score descending, block index ascending); their
+    weights are the softmax of the scores over the candidates.
+    Returns (ascending list of selected block ids, near_tie flag)."""
+    cand = np.nonzero(valid)[0]
+    if cand.size == 0:
+        return np.zeros(0, dtype=np.int64), False
+    s = scores[cand]
+    order = np.lexsort((cand, -s))                    # primary -s, secondary index
+    e = np.exp(s - s.max())
+    probs = e / e.sum()
+    m = hybrid_select_probs(probs, order, kf, p)
+    sel = np.sort(cand[order[:m]])
+    # near tie: the boundary scores are within TIE_SCORE, or a cumulative mass
+    # at the Top-p boundary is within TIE_MASS of p
+    flag = False
+    if m < cand.size:
+        a, b = s[order[m - 1]], s[order[m]]
+        flag |= abs(a - b) <= TIE_SCORE * max(1.0, abs(a))
+    cum = np.cumsum(probs[order])
+    mp = topp_count(probs[order], p)
+    flag |= abs(cum[mp - 1] - p) <= TIE_MASS
+    if mp >= 2:
+        flag |= abs(cum[mp - 2] - p) <= TIE_MASS
+    return sel, bool(flag)
+
+
+def select_blocks(w, Qbar: np.ndarray, Kbar: np.ndarray, n_valid: np.ndarray, heads=None,
+                  rows=None):
+    """Hybrid selection for every (b, h, query block).
+
+    Returns (lists, flags): lists[(b, h)][i] = ascending selected key blocks
+    (empty for an empty query block), flags[(b, h)][i] = near-tie flag.
+    ``heads`` / ``rows`` restrict the work to a sample."""
+    B, H, nb, d = Qbar.shape
+    lists, flags = {}, {}
+    for b in range(B):
+        for h in (range(H) if heads is None else heads):
+            S = block_scores(Qbar[b, h], Kbar[b, h], d)
+            valid = n_valid[b, h] > 0
+            L, F = [None] * nb, [False] * nb
+            for i in (range(nb) if rows is None else rows):
+                if not valid[i]:
+                    L[i] = np.zeros(0, dtype=np.int64)
+                    continue
+                L[i], F[i] = hybrid_select_row(S[i], valid, w.topk_floor, w.topp)
+            lists[(b, h)], flags[(b, h)] = L, F
+    return lists, flags
+
+
+# --------------------------------------------------------------------------
+# step 5: block-sparse attention, forward and backward
+# --------------------------------------------------------------------------
+
+def _gather_keys(Xp_bh: np.ndarray, n_valid_bh: np.ndarray, sel, S: int) -> np.ndarray:
+    """Valid rows of the selected key blocks, concatenated in list order."""
+    return np.concatenate([Xp_bh[j * S: j * S + int(n_valid_bh[j])] for j in sel], axis=0)
+
+
+def attn_fwd_row(Qp_bh, Kp_bh, Vp_bh, n_valid_bh, i: int, sel, S: int, scale: float):
+    """Exact softmax attention of query block i over the valid tokens of its
+    selected key blocks (Prism, Fig. 2 caption; READING: bidirectional, no
+    dropout, no correction for the dropped blocks).
+    Returns (O rows [S, d] with padding rows 0, natural-log LSE [S])."""
+    d = Qp_bh.shape[1]
+    q = Qp_bh[i * S:(i + 1) * S].astype(f64)
+    k = _gather_keys(Kp_bh, n_valid_bh, sel, S).astype(f64)
+    v = _gather_keys(Vp_bh, n_valid_bh, sel, S).astype(f64)
+    s = (q @ k.T) * scale
+    mx = s.max(axis=1, keepdims=True)
+    e = np.exp(s - mx)
+    l = e.sum(axis=1, keepdims=True)
+    o = (e / l) @ v
+    lse = (mx + np.log(l))[:, 0]
+    nv = int(n_valid_bh[i])
+    o[nv:] = 0.0
+    lse[nv:] = 0.0
+    return o, lse
+
+
+def attn_fwd(w, Qp, Kp, Vp, n_valid, lists, scale):
+    """Forward over every (b, h, query block) present in ``lists``."""
+    B, H, Np, d = Qp.shape
+    S = w.block
+    Op = np.zeros((B, H, Np, d), dtype=f64)
+    lse = np.zeros((B, H, Np), dtype=f64)
+    for (b, h), L in lists.items():
+        for i, sel in enumerate(L):
+            if sel is None or len(sel) == 0:
+                continue
+            o, l = attn_fwd_row(Qp[b, h], Kp[b, h], Vp[b, h], n_valid[b, h], i, sel, S, scale)
+            Op[b, h, i * S:(i + 1) * S] = o
+            lse[b, h, i * S:(i + 1) * S] = l
+    return Op, lse
+
+
+def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale):
+    """VJP of ``attn_fwd_row`` (Prism trains through this attention: Table 2
+    caption -- it replaces video self-attention during training).  Gradients
+    flow only through the attention; the discrete steps are constants.
+    Returns (dq [S, d], dk [rows, d], dv [rows, d]) with dk/dv in the order of
+    ``_gather_keys``."""
+    q = Qp_bh[i * S:(i + 1) * S].astype(f64)
+    k = _gather_keys(Kp_bh, n_valid_bh, sel, S).astype(f64)
+    v = _gather_keys(Vp_bh, n_valid_bh, sel, S).astype(f64)
+    do = dOp_bh[i * S:(i + 1) * S].astype(f64).copy()
+    nv = int(n_valid_bh[i])
+    do[nv:] = 0.0                                     # padding query rows carry no gradient
+    s = (q @ k.T) * scale
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    P = e / e.sum(axis=1, keepdims=True)
+    o = P @ v
+    dv = P.T @ do
+    dP = do @ v.T
+    Dr = (do * o).sum(axis=1, keepdims=True)
+    dS = P * (dP - Dr)
+    dq = (dS @ k) * scale
+    dk = (dS.T @ q) * scale
+    dq[nv:] = 0.0
+    return dq, dk, dv
+
+
+def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None):
+    """Backward over every (b, h, query block) in ``lists``; returns permuted
+    dQp, dKp, dVp [B, H, Np, d] (float64).  ``rows_only`` restricts the query
+    blocks that are processed (dK/dV then hold partial sums)."""
+    B, H, Np, d = Qp.shape
+    S = w.block
+    dQ = np.zeros((B, H, Np, d), dtype=f64)
+    dK = np.zeros((B, H, Np, d), dtype=f64)
+    dV = np.zeros((B, H, Np, d), dtype=f64)
+    for (b, h), L in lists.items():
+        for i, sel in enumerate(L):
+            if sel is None or len(sel) == 0:
+                continue
+            if rows_only is not None and i not in rows_only:
+                continue
+            dq, dk, dv = attn_bwd_row(Qp[b, h], Kp[b, h], Vp[b, h], dOp[b, h], n_valid[b, h],
+                                      i, sel, S, scale)
+            dQ[b, h, i * S:(i + 1) * S] += dq
+            off = 0
+            for j in sel:
+                nv = int(n_valid[b, h, j])
+                dK[b, h, j * S: j * S + nv] += dk[off: off + nv]
+                dV[b, h, j * S: j * S + nv] += dv[off: off + nv]
+                off += nv
+    return dQ, dK, dV
+
+
+def csc_from_lists(L, nb: int):
+    """Key block -> ascending list of the query blocks that selected it."""
+    cols = [[] for _ in range(nb)]
+    for i, sel in enumerate(L):
+        if sel is None:
+            continue
+        for j in sel:
+            cols[int(j)].append(i)
+    return [np.array(c, dtype=np.int64) for c in cols]
+
+
+# --------------------------------------------------------------------------
+# independent references (pins)
+# --------------------------------------------------------------------------
+
+def dense_attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    """Plain softmax attention in the original token order, one query at a
+    time: Q, K, V [N, d] -> O [N, d]."""
+    N = Q.shape[0]
+    O = np.zeros_like(Q, dtype=f64)
+    for n in range(N):
+        s = K.astype(f64) @ Q[n].astype(f64) * scale
+        e = np.exp(s - s.max())
+        O[n] = (e[:, None] * V.astype(f64)).sum(axis=0) / e.sum()
+    return O
+
+
+def masked_attention(Q, K, V, mask, scale, dO=None):
+    """Softmax attention of every query over the keys its row of ``mask``
+    allows (original token order), and its VJP when dO is given.
+    Q, K, V, dO [N, d]; mask [N, N] bool.  Returns O or (O, dQ, dK, dV)."""
+    Q, K, V = Q.astype(f64), K.astype(f64), V.astype(f64)
+    s = np.where(mask, (Q @ K.T) * scale, -np.inf)
+    mx = s.max(axis=1, keepdims=True)
+    e = np.where(mask, np.exp(s - mx), 0.0)
+    P = e / e.sum(axis=1, keepdims=True)
+    O = P @ V
+    if dO is None:
+        return O
+    dO = dO.astype(f64)
+    dV = P.T @ dO
+    dP = dO @ V.T
+    dS = P * (dP - (dO * O).sum(axis=1, keepdims=True))
+    return O, (dS @ K) * scale, (dS.T @ Q) * scale, dV
+
+
+# --------------------------------------------------------------------------
+# whole path
+# --------------------------------------------------------------------------
+
+def run(w, Q, K, V, a2v, dO=None, heads=None):
+    """The whole hot path on one batch, every step in the pages' order.
+    Inputs in [B, N, H, d] / [B, N, Ca] (any float dtype); returns a dict of
+    every intermediate and output in float64 / int64."""
+    stats = zone_stats(w, V, a2v)
+    sid, stie = assign_shapes(w, stats)
+    perm, inv, nval = build_permutation(w, sid)
+    Qp, Kp, Vp = permute(Q, perm), permute(K, perm), permute(V, perm)
+    Qb, Kb = pool(Qp, nval, w.block), pool(Kp, nval, w.block)
+    lists, flags = select_blocks(w, Qb, Kb, nval, heads=heads)
+    scale = 1.0 / math.sqrt(w.d)
+    Op, lse = attn_fwd(w, Qp, Kp, Vp, nval, lists, scale)
+    res = dict(stats=stats, shape_id=sid, shape_tie=stie, perm=perm, inv=inv, n_valid=nval,
+               Qp=Qp, Kp=Kp, Vp=Vp, Qbar=Qb, Kbar=Kb, lists=lists, flags=flags, Op=Op, lse=lse,
+               O=unpermute(Op, inv), scale=scale)
+    if dO is not None:
+        dOp = permute(dO, perm)
+        dQp, dKp, dVp = attn_bwd(w, Qp, Kp, Vp, dOp, nval, lists, scale)
+        res.update(dOp=dOp, dQp=dQp, dKp=dKp, dVp=dVp, dQ=unpermute(dQp, inv),
+                   dK=unpermute(dKp, inv), dV=unpermute(dVp, inv))
+    return res

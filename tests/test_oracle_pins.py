@@ -1,0 +1,420 @@
+"""Pins of the CPU oracle against what the Prism pages and plain mathematics fix.
+
+Each test checks the oracle against something other than itself: printed
+values (Table 11's shape names), closed forms, invariants, special cases that
+reduce to a textbook routine, and brute force on tiny inputs.
+"""
+import itertools
+import math
+import os
+import statistics
+
+import numpy as np
+import pytest
+import torch
+
+from content_adaptive_block_02_b300 import synth
+from oracle import prism_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _small(**kw):
+    """A small padded workload: 5x7x9 grid, 2x4x4 zones, 16-token blocks."""
+    base = synth.WORKLOADS["tiny"].with_(T=5, Hg=7, W=9, H=2, d=8, Ca=8, Na=4)
+    return base.with_(**kw)
+
+
+# ---------------------------------------------------------------- menu ------
+
+def test_table11_shape_names_have_class_token_count():
+    """Prism Table 11: every printed shape bT bH bW multiplies to its class."""
+    n = 0
+    with open(os.path.join(GOLDEN, "table11_shape_names.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            cls, *names = line.split()
+            for s in names:
+                assert int(s[0]) * int(s[1]) * int(s[2]) == int(cls)
+                n += 1
+    assert n == 16
+
+
+@pytest.mark.parametrize("menu,S", [(synth.MENU_TINY, 16), (synth.MENU_128, 128)])
+def test_menus_have_equal_token_count(menu, S):
+    assert all(a * b * c == S for a, b, c in menu)
+
+
+def test_admissible_shapes():
+    assert orc.admissible_shapes(synth.MENU_128, (3, 16, 16)) == [0, 1]
+    assert orc.admissible_shapes(synth.MENU_128, (4, 16, 16)) == list(range(7))
+    assert orc.admissible_shapes(synth.MENU_TINY, (2, 4, 4)) == [0, 1, 2]
+
+
+def test_geometry_matches_2k_token_count():
+    """Table 5 caption: 10 s of 2K video at 24 fps is about 870K tokens;
+    the 2K-like frame is 90 x 160 latent tokens (61 latent frames)."""
+    w = synth.WORKLOADS["2k"]
+    assert abs(61 * w.Hg * w.W - 870_000) / 870_000 < 0.01
+    assert w.Np == 322_560 and w.n_zones == 420 and w.n_blocks == 2520
+
+
+# ----------------------------------------------------------- statistics -----
+
+def _grid(w, fn, C):
+    x = np.zeros((w.T, w.Hg, w.W, C))
+    for t, y, z in itertools.product(range(w.T), range(w.Hg), range(w.W)):
+        x[t, y, z] = fn(t, y, z)
+    return x.reshape(w.N, C)
+
+
+@pytest.mark.parametrize("axis", [0, 1, 2])
+def test_line_variance_linear_ramp_closed_form(axis):
+    """A ramp of slope s along one axis over n tokens has population variance
+    s^2 (n^2 - 1) / 12 on every full line of that axis, and none across."""
+    w = synth.WORKLOADS["tiny"].with_(H=1, d=3)        # 4x8x8 grid, zones 2x4x4, no padding
+    slopes = np.array([0.5, -1.25, 3.0])
+    x = _grid(w, lambda t, y, z: slopes * (t, y, z)[axis], 3)
+    g, m = orc._grid_views(x, w, 3)
+    n = w.zone[axis]
+    for a in range(3):
+        got = orc.line_variance(g, m, a)
+        want = (slopes ** 2).mean() * (n * n - 1) / 12.0 if a == axis else 0.0
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_line_variance_constant_field_is_zero():
+    w = _small()
+    x = np.full((w.N, 4), 2.75)
+    g, m = orc._grid_views(x, w, 4)
+    for a in range(3):
+        assert np.all(orc.line_variance(g, m, a) == 0.0)
+
+
+def test_line_variance_brute_force_with_padding():
+    """Explicit per-line loop with statistics.pvariance on a padded grid."""
+    w = _small()
+    rng = np.random.default_rng(5)
+    C = 3
+    x = rng.normal(size=(w.N, C))
+    g, m = orc._grid_views(x, w, C)
+    Tp, Hp, Wp = orc.padded_grid(w.T, w.Hg, w.W, w.zone)
+    zT, zH, zW = w.zone
+    xs = x.reshape(w.T, w.Hg, w.W, C)
+    for axis in range(3):
+        got = orc.line_variance(g, m, axis)
+        for zt, zh, zw in itertools.product(range(Tp // zT), range(Hp // zH), range(Wp // zW)):
+            vals = []
+            ext = (zT, zH, zW)
+            others = [a for a in range(3) if a != axis]
+            for u in range(ext[others[0]]):
+                for v in range(ext[others[1]]):
+                    coords = []
+                    for s in range(ext[axis]):
+                        c = [0, 0, 0]
+                        c[axis], c[others[0]], c[others[1]] = s, u, v
+                        tt, yy, xx = zt * zT + c[0], zh * zH + c[1], zw * zW + c[2]
+                        if tt < w.T and yy < w.Hg and xx < w.W:
+                            coords.append((tt, yy, xx))
+                    if len(coords) >= 2:
+                        for ch in range(C):
+                            vals.append(statistics.pvariance([xs[p][ch] for p in coords]))
+            want = sum(vals) / len(vals) if vals else 0.0
+            assert abs(got[zt, zh, zw] - want) < 1e-12
+
+
+def test_zone_stats_audio_fields():
+    """Constant-norm A2V output: nbar is that norm, no directional variance;
+    n_valid counts the zone's real tokens."""
+    w = _small()
+    rng = np.random.default_rng(1)
+    a2v = rng.normal(size=(1, w.N, w.Ca))
+    a2v /= np.linalg.norm(a2v, axis=-1, keepdims=True) / 3.0
+    V = rng.normal(size=(1, w.N, w.H, w.d))
+    st = orc.zone_stats(w, V, a2v)
+    assert st.shape == (1, w.H, w.n_zones, 8)
+    np.testing.assert_allclose(st[..., 6], 3.0, rtol=1e-12)
+    np.testing.assert_allclose(st[..., 3:6], 0.0, atol=1e-12)
+    assert st[0, 0, :, 7].sum() == w.N
+    # zone 0 is a full 2x4x4 zone
+    assert st[0, 0, 0, 7] == 32
+
+
+# ----------------------------------------------------------- shape rule -----
+
+def test_shape_rule_exact_inverse_guidance_has_zero_cost():
+    """g_d proportional to 1/b_d for a menu shape b makes b the continuous
+    optimum of Eq. 7 with alpha = 1, so it is chosen with cost 0."""
+    w = synth.WORKLOADS["2k"].with_(zone=(4, 16, 16))
+    for k, b in enumerate(w.menu):
+        g = 0.37 / np.array(b, dtype=float)
+        costs, idx = orc.shape_costs(w, g)
+        j = int(np.argmin(costs))
+        assert idx[j] == k and costs[j] < 1e-24
+
+
+def test_shape_rule_equal_guidance_takes_lowest_index():
+    w = synth.WORKLOADS["2k"]
+    costs, idx = orc.shape_costs(w, np.ones(3))
+    assert costs[0] == costs[1] and idx[int(np.argmin(costs))] == 0
+    w4 = w.with_(zone=(4, 16, 16))
+    costs, idx = orc.shape_costs(w4, np.ones(3))
+    # (4,4,8) and (4,8,4) sit nearest to the cube root of 128 and tie
+    assert idx[int(np.argmin(costs))] == 3 and abs(costs[3] - costs[4]) < 1e-15
+
+
+def test_shape_rule_dominant_axis_gets_finest_extent():
+    w = synth.WORKLOADS["2k"].with_(zone=(4, 16, 16))
+    for axis in range(3):
+        g = np.full(3, 1e-3)
+        g[axis] = 10.0
+        costs, idx = orc.shape_costs(w, g)
+        best = w.menu[idx[int(np.argmin(costs))]]
+        assert best[axis] == min(s[axis] for s in w.menu)
+
+
+def test_guidance_zero_statistics_is_isotropic():
+    w = synth.WORKLOADS["2k"]
+    g = orc.guidance(w, np.zeros(8), 0.0)
+    np.testing.assert_allclose(g, 1.0 / 3.0 + w.eps)
+    g = orc.guidance(w.with_(use_video=False), np.array([1, 2, 3, 0, 0, 4, 2.0, 5]), 4.0)
+    np.testing.assert_allclose(g, 0.5 * np.array([0, 0, 1.0]) + w.eps)
+
+
+def test_assign_shapes_follow_directional_variance():
+    """A zone whose values vary only along W must get the finer W extent."""
+    w = synth.WORKLOADS["2k"].with_(T=3, Hg=16, W=32, H=1, d=4, use_audio=False)
+    x = _grid(w, lambda t, y, z: np.array([z, -z, 2 * z, z]) if z < 16 else
+              np.array([y, y, -y, 3 * y]), 4)
+    a2v = np.ones((1, w.N, 4))
+    st = orc.zone_stats(w, x[None, :, None, :], a2v)
+    sid, tie = orc.assign_shapes(w, st)
+    assert w.menu[sid[0, 0, 0]] == (1, 16, 8)          # fine along W
+    assert w.menu[sid[0, 0, 1]] == (1, 8, 16)          # fine along H
+    assert not tie.any()
+
+
+# ------------------------------------------------------------ permutation ---
+
+def _random_shapes(w, seed):
+    rng = np.random.default_rng(seed)
+    adm = orc.admissible_shapes(w.menu, w.zone)
+    return rng.choice(adm, size=(w.B, w.H, w.n_zones))
+
+
+def test_permutation_is_a_blockwise_bijection():
+    w = _small()
+    sid = _random_shapes(w, 3)
+    perm, inv, nval = orc.build_permutation(w, sid)
+    S = w.block
+    for h in range(w.H):
+        p = perm[0, h]
+        real = p[p >= 0]
+        assert sorted(real.tolist()) == list(range(w.N))
+        assert np.all(p[inv[0, h]] == np.arange(w.N))
+        for blk in range(w.n_blocks):
+            seg = p[blk * S:(blk + 1) * S]
+            nv = int(nval[0, h, blk])
+            assert np.all(seg[:nv] >= 0) and np.all(seg[nv:] == -1)
+            if nv == 0:
+                continue
+            t, r = np.divmod(seg[:nv], w.Hg * w.W)
+            y, x = np.divmod(r, w.W)
+            # one zone, and inside the box of the zone's chosen shape
+            z = set(zip(t // w.zone[0], y // w.zone[1], x // w.zone[2]))
+            assert len(z) == 1
+            zt, zh, zw = z.pop()
+            Z = ((zt * (orc.padded_grid(w.T, w.Hg, w.W, w.zone)[1] // w.zone[1]) + zh)
+                 * (orc.padded_grid(w.T, w.Hg, w.W, w.zone)[2] // w.zone[2]) + zw)
+            bT, bH, bW = w.menu[sid[0, h, Z]]
+            assert t.max() - t.min() < bT and y.max() - y.min() < bH and x.max() - x.min() < bW
+            # valid tokens in raster order
+            assert np.all(np.diff(seg[:nv]) > 0)
+
+
+def test_permute_unpermute_identity():
+    w = _small()
+    sid = _random_shapes(w, 4)
+    perm, inv, _ = orc.build_permutation(w, sid)
+    X = np.random.default_rng(0).normal(size=(1, w.N, w.H, w.d))
+    Xp = orc.permute(X, perm)
+    assert np.all(Xp[perm < 0] == 0.0)
+    np.testing.assert_array_equal(orc.unpermute(Xp, inv), X)
+
+
+def test_pool_is_mean_of_the_blocks_tokens():
+    w = _small()
+    sid = _random_shapes(w, 5)
+    perm, inv, nval = orc.build_permutation(w, sid)
+    X = np.random.default_rng(2).normal(size=(1, w.N, w.H, w.d))
+    Xb = orc.pool(orc.permute(X, perm), nval, w.block)
+    for h in range(w.H):
+        for blk in range(w.n_blocks):
+            toks = [n for n in perm[0, h, blk * w.block:(blk + 1) * w.block] if n >= 0]
+            if toks:
+                want = np.mean([X[0, n, h] for n in toks], axis=0)
+                np.testing.assert_allclose(Xb[0, h, blk], want, rtol=1e-13, atol=1e-15)
+            else:
+                assert np.all(Xb[0, h, blk] == 0)
+
+
+# -------------------------------------------------------------- selection ---
+
+def test_topp_strictly_exceeds():
+    """Table 7 caption: the set's cumulative weight must exceed p."""
+    pr = np.array([0.5, 0.25, 0.125, 0.125])
+    assert orc.topp_count(pr, 0.75) == 3      # 0.75 does not exceed 0.75
+    assert orc.topp_count(pr, 0.74) == 2
+    assert orc.topp_count(pr, 0.0) == 1
+    assert orc.topp_count(pr, 0.875) == 4
+    assert orc.topp_count(pr, 1.0) == 4
+
+
+def test_topp_is_the_smallest_exceeding_set_brute_force():
+    rng = np.random.default_rng(7)
+    for trial in range(200):
+        n = int(rng.integers(1, 8))
+        pr = rng.dirichlet(np.ones(n) * 0.7)
+        p = float(rng.uniform(0, 0.999))
+        best = min(len(c) for r in range(1, n + 1) for c in itertools.combinations(range(n), r)
+                   if sum(pr[list(c)]) > p)
+        assert orc.topp_count(np.sort(pr)[::-1], p) == best
+
+
+def test_select_p0_is_topk_by_score():
+    rng = np.random.default_rng(9)
+    for trial in range(50):
+        nb = int(rng.integers(3, 40))
+        s = rng.normal(size=nb) * 3
+        s[rng.integers(0, nb)] = s[0]                   # a duplicated score
+        valid = rng.random(nb) > 0.2
+        valid[0] = True
+        kf = int(rng.integers(1, 6))
+        sel, _ = orc.hybrid_select_row(s, valid, kf, 0.0)
+        cand = [j for j in range(nb) if valid[j]]
+        want = sorted(sorted(cand, key=lambda j: (-s[j], j))[:min(kf, len(cand))])
+        assert sel.tolist() == want
+
+
+def test_select_p1_keeps_every_valid_block():
+    rng = np.random.default_rng(10)
+    s = rng.normal(size=30) * 40                        # very peaked softmax
+    valid = np.ones(30, bool)
+    valid[[3, 17]] = False
+    sel, _ = orc.hybrid_select_row(s, valid, 2, 1.0)
+    assert sel.tolist() == [j for j in range(30) if valid[j]]
+
+
+def test_select_hybrid_is_max_of_floor_and_topp():
+    s = np.log(np.array([0.5, 0.25, 0.125, 0.0625, 0.0625]))
+    valid = np.ones(5, bool)
+    sel, _ = orc.hybrid_select_row(s, valid, 1, 0.7)   # Top-p needs 2
+    assert sel.tolist() == [0, 1]
+    sel, _ = orc.hybrid_select_row(s, valid, 4, 0.7)   # floor 4 wins
+    assert sel.tolist() == [0, 1, 2, 3]
+    sel, _ = orc.hybrid_select_row(s, valid, 9, 0.7)   # floor capped at the candidates
+    assert sel.tolist() == [0, 1, 2, 3, 4]
+
+
+def test_select_flags_near_ties():
+    s = np.array([1.0, 0.5, 0.5 + 1e-9, -3.0])
+    sel, flag = orc.hybrid_select_row(s, np.ones(4, bool), 2, 0.0)
+    assert flag and sel.tolist() == [0, 2]
+    sel, flag = orc.hybrid_select_row(np.array([2.0, 0.0, -2.0]), np.ones(3, bool), 1, 0.1)
+    assert not flag
+
+
+# -------------------------------------------------------------- attention ---
+
+def _tiny_inputs(w, seed=0):
+    torch.manual_seed(seed)
+    d = synth.generate(w, "cpu")
+    return {k: (v.float().numpy().astype(np.float64) if torch.is_tensor(v) else v)
+            for k, v in d.items()}
+
+
+def test_dense_special_case_equals_plain_attention():
+    """Top-p = 1 keeps every block, so the path is plain softmax attention."""
+    w = synth.WORKLOADS["tiny"].with_(topp=1.0)
+    x = _tiny_inputs(w)
+    r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"])
+    for h in range(w.H):
+        ref = orc.dense_attention(x["Q"][0, :, h], x["K"][0, :, h], x["V"][0, :, h], r["scale"])
+        assert np.abs(r["O"][0, :, h] - ref).max() <= 1e-12
+    w2 = synth.WORKLOADS["tiny"].with_(topk_floor=10 ** 6)
+    r2 = orc.run(w2, x["Q"], x["K"], x["V"], x["a2v"])
+    assert np.abs(r2["O"] - r["O"]).max() <= 1e-12
+
+
+def _token_mask(w, r, b, h):
+    S = w.block
+    perm, L = r["perm"][b, h], r["lists"][(b, h)]
+    mask = np.zeros((w.N, w.N), bool)
+    for i, sel in enumerate(L):
+        qs = [n for n in perm[i * S:(i + 1) * S] if n >= 0]
+        ks = [n for j in sel for n in perm[j * S:(j + 1) * S] if n >= 0]
+        for q in qs:
+            mask[q, ks] = True
+    return mask
+
+
+def test_block_sparse_equals_brute_force_masked_attention():
+    """Permuted block-sparse forward and backward equal masked attention with
+    the explicit N x N token mask, in the original order."""
+    w = synth.WORKLOADS["tiny"]
+    x = _tiny_inputs(w)
+    r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"], dO=x["dO"])
+    sparsity = []
+    for h in range(w.H):
+        mask = _token_mask(w, r, 0, h)
+        sparsity.append(1 - mask.mean())
+        O, dQ, dK, dV = orc.masked_attention(x["Q"][0, :, h], x["K"][0, :, h], x["V"][0, :, h],
+                                             mask, r["scale"], dO=x["dO"][0, :, h])
+        assert np.abs(O - r["O"][0, :, h]).max() <= 1e-12
+        assert np.abs(dQ - r["dQ"][0, :, h]).max() <= 1e-11
+        assert np.abs(dK - r["dK"][0, :, h]).max() <= 1e-11
+        assert np.abs(dV - r["dV"][0, :, h]).max() <= 1e-11
+    assert max(sparsity) > 0.2                          # the case is genuinely sparse
+
+
+def test_gradients_match_central_finite_differences():
+    """d<O, dO>/dX by central differences with the selection held fixed."""
+    w = _small(H=1, d=6, Ca=6, topp=0.6, topk_floor=1)
+    x = _tiny_inputs(w, seed=3)
+    r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"], dO=x["dO"])
+    rng = np.random.default_rng(0)
+    perm, inv, nval = r["perm"], r["inv"], r["n_valid"]
+
+    def objective(Q, K, V):
+        Qp, Kp, Vp = orc.permute(Q, perm), orc.permute(K, perm), orc.permute(V, perm)
+        Op, _ = orc.attn_fwd(w, Qp, Kp, Vp, nval, r["lists"], r["scale"])
+        return float((orc.unpermute(Op, inv) * x["dO"]).sum())
+
+    eps = 1e-6
+    for name, grad in (("Q", r["dQ"]), ("K", r["dK"]), ("V", r["dV"])):
+        for _ in range(6):
+            n, c = int(rng.integers(0, w.N)), int(rng.integers(0, w.d))
+            args = {k: x[k].copy() for k in ("Q", "K", "V")}
+            args[name][0, n, 0, c] += eps
+            fp = objective(args["Q"], args["K"], args["V"])
+            args[name][0, n, 0, c] -= 2 * eps
+            fm = objective(args["Q"], args["K"], args["V"])
+            fd = (fp - fm) / (2 * eps)
+            assert abs(fd - grad[0, n, 0, c]) <= 1e-6 * max(1.0, abs(fd))
+
+
+def test_lse_is_log_sum_exp_of_selected_scores():
+    w = synth.WORKLOADS["tiny"]
+    x = _tiny_inputs(w)
+    r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"])
+    S = w.block
+    h = 1
+    mask = _token_mask(w, r, 0, h)
+    q, k = x["Q"][0, :, h], x["K"][0, :, h]
+    for n in range(0, w.N, 37):
+        s = [math.fsum([q[n, c] * k[m, c] for c in range(w.d)]) * r["scale"]
+             for m in range(w.N) if mask[n, m]]
+        want = max(s) + math.log(math.fsum(math.exp(v - max(s)) for v in s))
+        slot = r["inv"][0, h, n]
+        assert abs(r["lse"][0, h, slot] - want) < 1e-12
