@@ -1,0 +1,296 @@
+// The C ABI of libprism: plan validation, workspace layout and the entry
+// points declared in include/prism.h.  Every entry point checks its
+// arguments on the host, then enqueues kernels on the caller's stream.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "prism_internal.cuh"
+
+using prism::Plan;
+
+struct prism_plan {
+  Plan p;
+};
+
+namespace prism {
+cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp, float* D,
+                           float* dQacc, cudaStream_t st);
+cudaError_t launch_attn_fwd_simt(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                 const uint16_t* Vp, const int32_t* n_valid,
+                                 const int32_t* row_ptr, const int32_t* col_idx, float scale,
+                                 uint16_t* Op, float* lse, cudaStream_t st);
+cudaError_t launch_attn_bwd_simt(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                 const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                                 const float* D, const int32_t* n_valid,
+                                 const int32_t* col_ptr, const int32_t* row_idx, float scale,
+                                 float* dQacc, uint16_t* dKp, uint16_t* dVp, cudaStream_t st);
+cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                               const uint16_t* Vp, const int32_t* n_valid, const int32_t* row_ptr,
+                               const int32_t* col_idx, float scale, uint16_t* Op, float* lse,
+                               uint8_t* ws, cudaStream_t st);
+cudaError_t launch_attn_bwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                               const float* D, const int32_t* n_valid, const int32_t* col_ptr,
+                               const int32_t* row_idx, float scale, float* dQacc, uint16_t* dKp,
+                               uint16_t* dVp, uint8_t* ws, cudaStream_t st);
+}  // namespace prism
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+inline int ilog2_exact(int v) {
+  int r = 0;
+  while ((1 << r) < v) ++r;
+  return (1 << r) == v ? r : -1;
+}
+
+#define PRISM_CHECK_PTR(p)                 \
+  do {                                     \
+    if ((p) == nullptr) return PRISM_ERR_ARG; \
+    if (!aligned16(p)) return PRISM_ERR_ALIGN; \
+  } while (0)
+
+#define PRISM_CUDA(call)                      \
+  do {                                        \
+    if ((call) != cudaSuccess) return PRISM_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* prism_strerror(int code) {
+  switch (code) {
+    case PRISM_OK: return "ok";
+    case PRISM_ERR_ARG: return "invalid argument";
+    case PRISM_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case PRISM_ERR_UNSUPPORTED: return "configuration not supported by the kernels";
+    case PRISM_ERR_NO_ADMISSIBLE_SHAPE: return "no menu shape tiles the macro-zone";
+    case PRISM_ERR_CUDA: return "CUDA runtime error";
+    case PRISM_ERR_DEVICE_TIMEOUT: return "a device-side wait exceeded its bound";
+    case PRISM_ERR_DEVICE_BOUNDS: return "a device-side index check failed";
+    default: return "unknown error";
+  }
+}
+
+int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
+  if (cfg == nullptr || out == nullptr) return PRISM_ERR_ARG;
+  *out = nullptr;
+  const prism_config_t& c = *cfg;
+  if (c.B < 1 || c.H < 1 || c.d < 1 || c.T < 1 || c.Hg < 1 || c.W < 1 || c.zT < 1 ||
+      c.zH < 1 || c.zW < 1 || c.block_tokens < 1 || c.Ca < 1 || c.topk_floor < 0 ||
+      !(c.topp >= 0.f) || c.n_shapes < 1 || c.n_shapes > PRISM_MAX_SHAPES ||
+      !(c.alpha == c.alpha) || !(c.eps >= 0.0))
+    return PRISM_ERR_ARG;
+  if (c.d % 32 != 0 || c.d > 128) return PRISM_ERR_UNSUPPORTED;
+  const int lS = ilog2_exact(c.block_tokens);
+  if (lS < 2 || c.block_tokens > 128) return PRISM_ERR_UNSUPPORTED;
+  if (c.d * c.block_tokens > 16384) return PRISM_ERR_UNSUPPORTED;
+  for (int k = 0; k < c.n_shapes; ++k) {
+    const int* s = c.shapes[k];
+    if (s[0] < 1 || s[1] < 1 || s[2] < 1) return PRISM_ERR_ARG;
+    if (s[0] * s[1] * s[2] != c.block_tokens) return PRISM_ERR_UNSUPPORTED;
+  }
+  const long long vol = static_cast<long long>(c.zT) * c.zH * c.zW;
+  if (vol > 3072) return PRISM_ERR_UNSUPPORTED;
+  Plan p;
+  memset(&p, 0, sizeof(p));
+  p.cfg = c;
+  prism_sizes_t& z = p.sz;
+  z.nzT = (c.T + c.zT - 1) / c.zT;
+  z.nzH = (c.Hg + c.zH - 1) / c.zH;
+  z.nzW = (c.W + c.zW - 1) / c.zW;
+  z.Tp = z.nzT * c.zT;
+  z.Hp = z.nzH * c.zH;
+  z.Wp = z.nzW * c.zW;
+  z.Z = z.nzT * z.nzH * z.nzW;
+  z.N = static_cast<long long>(c.T) * c.Hg * c.W;
+  z.Np = static_cast<long long>(z.Tp) * z.Hp * z.Wp;
+  for (int k = 0; k < c.n_shapes; ++k) {
+    const int* s = c.shapes[k];
+    if (c.zT % s[0] == 0 && c.zH % s[1] == 0 && c.zW % s[2] == 0)
+      z.admissible[z.n_admissible++] = k;
+  }
+  if (z.n_admissible == 0) return PRISM_ERR_NO_ADMISSIBLE_SHAPE;
+  z.blocks_per_zone = static_cast<int>(vol / c.block_tokens);
+  const long long nb = z.Np / c.block_tokens;
+  if (nb > 8192 || z.Np >= (1LL << 31) || z.N >= (1LL << 31)) return PRISM_ERR_UNSUPPORTED;
+  z.nb = static_cast<int>(nb);
+  const long long rows = static_cast<long long>(c.B) * c.H * nb;
+  z.max_pairs = rows * nb;
+  if (z.max_pairs >= (1LL << 31)) return PRISM_ERR_UNSUPPORTED;
+  z.tensor_core_path = 0;
+  for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
+    for (int a = 0; a < 3; ++a) {
+      const int e = k < c.n_shapes ? c.shapes[k][a] : 1;
+      const int l = ilog2_exact(e);
+      p.log2_ext[k][a] = l >= 0 ? static_cast<double>(l) : log2(static_cast<double>(e));
+    }
+  p.log2_S = static_cast<double>(lS);
+  // workspace layout
+  const int nwords = (z.nb + 31) / 32;
+  size_t off = 256;
+  p.off_rowcnt = off; off = align256(off + rows * 4);
+  p.off_colcnt = off; off = align256(off + rows * 4);
+  p.off_amb = off; off = align256(off + rows * 4);
+  p.off_qn = off; off = align256(off + 2 * rows * 4);
+  p.off_bitmask = off; off = align256(off + rows * nwords * 4);
+  p.off_scores = off; off = align256(off + rows * nb * 4);
+  p.off_D = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
+  p.off_dq = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * c.d * 4);
+  z.ws_bytes = off;
+  prism_plan* h = static_cast<prism_plan*>(malloc(sizeof(prism_plan)));
+  if (h == nullptr) return PRISM_ERR_ARG;
+  h->p = p;
+  *out = h;
+  return PRISM_OK;
+}
+
+void prism_plan_destroy(prism_plan_t* plan) { free(plan); }
+
+int prism_plan_query(const prism_plan_t* plan, prism_sizes_t* out) {
+  if (plan == nullptr || out == nullptr) return PRISM_ERR_ARG;
+  *out = plan->p.sz;
+  return PRISM_OK;
+}
+
+int prism_ws_init(const prism_plan_t* plan, void* ws, void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(ws);
+  PRISM_CUDA(cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)));
+  return PRISM_OK;
+}
+
+int prism_device_status(const prism_plan_t* plan, const void* ws, void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(ws);
+  uint32_t word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PRISM_CUDA(cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st));
+  PRISM_CUDA(cudaStreamSynchronize(st));
+  if (word == prism::DEV_ERR_TIMEOUT) return PRISM_ERR_DEVICE_TIMEOUT;
+  if (word != 0) return PRISM_ERR_DEVICE_BOUNDS;
+  return PRISM_OK;
+}
+
+int prism_zone_stats(const prism_plan_t* plan, const uint16_t* V, const uint16_t* a2v,
+                     float* stats, void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(V);
+  PRISM_CHECK_PTR(a2v);
+  PRISM_CHECK_PTR(stats);
+  PRISM_CUDA(prism::launch_zone_stats(plan->p, V, a2v, stats, static_cast<cudaStream_t>(stream)));
+  return PRISM_OK;
+}
+
+int prism_assign_and_permute(const prism_plan_t* plan, const float* stats, const uint16_t* Q,
+                             const uint16_t* K, const uint16_t* V, uint8_t* shape_id,
+                             uint8_t* shape_tie, int32_t* perm, int32_t* inv, uint16_t* Qp,
+                             uint16_t* Kp, uint16_t* Vp, float* Qbar, float* Qbar_lo,
+                             float* Kbar, float* Kbar_lo, int32_t* n_valid, void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(stats);
+  PRISM_CHECK_PTR(Q); PRISM_CHECK_PTR(K); PRISM_CHECK_PTR(V);
+  PRISM_CHECK_PTR(shape_id); PRISM_CHECK_PTR(shape_tie);
+  PRISM_CHECK_PTR(perm); PRISM_CHECK_PTR(inv);
+  PRISM_CHECK_PTR(Qp); PRISM_CHECK_PTR(Kp); PRISM_CHECK_PTR(Vp);
+  PRISM_CHECK_PTR(Qbar); PRISM_CHECK_PTR(Qbar_lo);
+  PRISM_CHECK_PTR(Kbar); PRISM_CHECK_PTR(Kbar_lo);
+  PRISM_CHECK_PTR(n_valid);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PRISM_CUDA(prism::launch_assign(plan->p, stats, shape_id, shape_tie, st));
+  PRISM_CUDA(prism::launch_permute_pool(plan->p, shape_id, Q, K, V, perm, inv, Qp, Kp, Vp, Qbar,
+                                        Qbar_lo, Kbar, Kbar_lo, n_valid, st));
+  return PRISM_OK;
+}
+
+int prism_block_select(const prism_plan_t* plan, const float* Qbar, const float* Qbar_lo,
+                       const float* Kbar, const float* Kbar_lo, const int32_t* n_valid,
+                       int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr, int32_t* row_idx,
+                       uint8_t* sel_tie, void* ws, void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(Qbar); PRISM_CHECK_PTR(Qbar_lo);
+  PRISM_CHECK_PTR(Kbar); PRISM_CHECK_PTR(Kbar_lo);
+  PRISM_CHECK_PTR(n_valid);
+  PRISM_CHECK_PTR(row_ptr); PRISM_CHECK_PTR(col_idx);
+  PRISM_CHECK_PTR(col_ptr); PRISM_CHECK_PTR(row_idx);
+  PRISM_CHECK_PTR(sel_tie); PRISM_CHECK_PTR(ws);
+  PRISM_CUDA(prism::launch_select(plan->p, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid, sel_tie,
+                                  row_ptr, col_idx, col_ptr, row_idx,
+                                  static_cast<uint8_t*>(ws), static_cast<cudaStream_t>(stream)));
+  return PRISM_OK;
+}
+
+int prism_sparse_attn_fwd(const prism_plan_t* plan, const uint16_t* Qp, const uint16_t* Kp,
+                          const uint16_t* Vp, const int32_t* n_valid, const int32_t* row_ptr,
+                          const int32_t* col_idx, float scale, uint16_t* Op, float* lse,
+                          void* ws, void* stream) {
+  if (plan == nullptr || !(scale > 0.f)) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(Qp); PRISM_CHECK_PTR(Kp); PRISM_CHECK_PTR(Vp);
+  PRISM_CHECK_PTR(n_valid); PRISM_CHECK_PTR(row_ptr); PRISM_CHECK_PTR(col_idx);
+  PRISM_CHECK_PTR(Op); PRISM_CHECK_PTR(lse); PRISM_CHECK_PTR(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Plan& p = plan->p;
+  if (p.sz.tensor_core_path) {
+    PRISM_CUDA(prism::launch_attn_fwd_tc(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op, lse,
+                                         static_cast<uint8_t*>(ws), st));
+  } else {
+    PRISM_CUDA(prism::launch_attn_fwd_simt(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op,
+                                           lse, st));
+  }
+  return PRISM_OK;
+}
+
+int prism_permute(const prism_plan_t* plan, const int32_t* perm, const uint16_t* X, uint16_t* Xp,
+                  void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(perm); PRISM_CHECK_PTR(X); PRISM_CHECK_PTR(Xp);
+  PRISM_CUDA(prism::launch_permute(plan->p, perm, X, Xp, static_cast<cudaStream_t>(stream)));
+  return PRISM_OK;
+}
+
+int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const uint16_t* Kp,
+                          const uint16_t* Vp, const uint16_t* Op, const uint16_t* dOp,
+                          const float* lse, const int32_t* n_valid, const int32_t* row_ptr,
+                          const int32_t* col_idx, const int32_t* col_ptr, const int32_t* row_idx,
+                          float scale, uint16_t* dQp, uint16_t* dKp, uint16_t* dVp, void* ws,
+                          void* stream) {
+  if (plan == nullptr || !(scale > 0.f)) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(Qp); PRISM_CHECK_PTR(Kp); PRISM_CHECK_PTR(Vp);
+  PRISM_CHECK_PTR(Op); PRISM_CHECK_PTR(dOp); PRISM_CHECK_PTR(lse);
+  PRISM_CHECK_PTR(n_valid); PRISM_CHECK_PTR(row_ptr); PRISM_CHECK_PTR(col_idx);
+  PRISM_CHECK_PTR(col_ptr); PRISM_CHECK_PTR(row_idx);
+  PRISM_CHECK_PTR(dQp); PRISM_CHECK_PTR(dKp); PRISM_CHECK_PTR(dVp); PRISM_CHECK_PTR(ws);
+  (void)row_ptr;
+  (void)col_idx;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Plan& p = plan->p;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* D = reinterpret_cast<float*>(w + p.off_D);
+  float* dq = reinterpret_cast<float*>(w + p.off_dq);
+  PRISM_CUDA(prism::launch_bwd_pre(p, Op, dOp, D, dq, st));
+  if (p.sz.tensor_core_path) {
+    PRISM_CUDA(prism::launch_attn_bwd_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx,
+                                         scale, dq, dKp, dVp, w, st));
+  } else {
+    PRISM_CUDA(prism::launch_attn_bwd_simt(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx,
+                                           scale, dq, dKp, dVp, st));
+  }
+  // dQ in block order, bf16, scaled
+  PRISM_CUDA(prism::launch_dq_convert(p, dq, scale, dQp, st));
+  return PRISM_OK;
+}
+
+int prism_unpermute(const prism_plan_t* plan, const int32_t* inv, const uint16_t* Xp, uint16_t* X,
+                    void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(inv); PRISM_CHECK_PTR(Xp); PRISM_CHECK_PTR(X);
+  PRISM_CUDA(prism::launch_unpermute(plan->p, inv, Xp, X, static_cast<cudaStream_t>(stream)));
+  return PRISM_OK;
+}
+
+}  // extern "C"

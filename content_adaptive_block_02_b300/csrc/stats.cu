@@ -1,0 +1,347 @@
+// Zone statistics and block-shape assignment.
+//
+// Prism (arXiv 2610.05416), Abstract: each spatiotemporal macro-zone is
+// described by the variance of the video features along each axis and by
+// the norms of the audio-to-video (A2V) cross-attention output; Table 9
+// caption names the three signals (per-channel variance of the value
+// features r_{v,d}, audio coupling gate a_bar, audio directional variance
+// v_hat_{a,d}); Table 10 caption gives the Eq. 7 quantisation
+// b*_d ~ g_d^-alpha with alpha = 1 the best setting.
+//
+// zone_stats: one CTA per (zone, head) for the value variance and one CTA
+// per zone for the A2V norm statistics.  The zone's real tokens are staged in
+// shared memory 32 channels at a time (cp.async, 16-byte rows pieces, two
+// stages so the next chunk loads while this one is reduced), then every line
+// along every axis is reduced exactly with a two-pass mean / variance.
+#include "prism_internal.cuh"
+
+namespace prism {
+namespace {
+
+constexpr int kStatsThreads = 256;
+constexpr int kChunk = 32;  // channels per smem stage (64 bytes of bf16)
+
+struct ZoneGeom {
+  int t0, y0, x0;  // zone origin on the padded grid
+  int vt, vy, vx;  // real extents inside the zone (>= 1 each)
+};
+
+__device__ __forceinline__ ZoneGeom zone_geom(const prism_config_t& c, int nzH, int nzW, int z) {
+  ZoneGeom g;
+  int zt = z / (nzH * nzW), zh = (z / nzW) % nzH, zw = z % nzW;
+  g.t0 = zt * c.zT;
+  g.y0 = zh * c.zH;
+  g.x0 = zw * c.zW;
+  g.vt = min(c.zT, c.T - g.t0);
+  g.vy = min(c.zH, c.Hg - g.y0);
+  g.vx = min(c.zW, c.W - g.x0);
+  return g;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+
+// Sum over the CTA, fixed order (deterministic).
+template <int NV>
+__device__ __forceinline__ void block_sum(float (&v)[NV], float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+  }
+  __syncthreads();
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) red[warp * NV + k] = v[k];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int nw = blockDim.x >> 5;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      float s = 0.f;
+      for (int w = 0; w < nw; ++w) s += red[w * NV + k];
+      v[k] = s;
+    }
+  }
+}
+
+// Accumulate, over the lines along one axis, the population variance of
+// every channel pair held in a [vt][vy][vx][kChunk] bf16 smem tile.
+// `len` tokens per line with stride `step` (in tokens); lines are indexed by
+// (a, b) over extents (na, nb) with strides (sa, sb).
+__device__ __forceinline__ float lines_variance(const uint32_t* tile, int na, int nb, int sa,
+                                                int sb, int len, int step) {
+  float acc = 0.f;
+  if (len < 2) return 0.f;
+  const int pairs = kChunk / 2;
+  const int items = na * nb * pairs;
+  const float inv = 1.f / static_cast<float>(len);
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    const int cp = it % pairs;
+    const int ln = it / pairs;
+    const int base = (ln / nb) * sa + (ln % nb) * sb;
+    float m0 = 0.f, m1 = 0.f;
+    for (int k = 0; k < len; ++k) {
+      uint32_t u = tile[(base + k * step) * pairs + cp];
+      m0 += bf16_lo(u);
+      m1 += bf16_hi(u);
+    }
+    m0 *= inv;
+    m1 *= inv;
+    float s0 = 0.f, s1 = 0.f;
+    for (int k = 0; k < len; ++k) {
+      uint32_t u = tile[(base + k * step) * pairs + cp];
+      float a = bf16_lo(u) - m0, b = bf16_hi(u) - m1;
+      s0 = fmaf(a, a, s0);
+      s1 = fmaf(b, b, s1);
+    }
+    acc += (s0 + s1) * inv;
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
+    prism_config_t c, int nzH, int nzW, int Z, const uint16_t* __restrict__ V,
+    const uint16_t* __restrict__ a2v, float* __restrict__ stats) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float red[32 * 4];
+  const int z = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const ZoneGeom g = zone_geom(c, nzH, nzW, z);
+  const int vol = g.vt * g.vy * g.vx;
+  const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
+
+  if (h < c.H) {
+    // ---- directional variance of the value features of head h ----
+    const int nchunk = c.d / kChunk;
+    const size_t stage_bytes = static_cast<size_t>(vol) * kChunk * 2;
+    auto load_chunk = [&](int ch, int stage) {
+      uint8_t* dst = smem + stage * stage_bytes;
+      const int pieces = vol * (kChunk / 8);
+      for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+        const int li = i >> 2, q = i & 3;
+        const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
+        const long long n =
+            (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
+        const uint16_t* src = V + ((static_cast<long long>(b) * N + n) * c.H + h) * c.d +
+                              ch * kChunk + q * 8;
+        cp_async16(dst + static_cast<size_t>(li) * kChunk * 2 + q * 16, src);
+      }
+      cp_async_commit();
+    };
+    float acc[3] = {0.f, 0.f, 0.f};
+    load_chunk(0, 0);
+    for (int ch = 0; ch < nchunk; ++ch) {
+      if (ch + 1 < nchunk) {
+        load_chunk(ch + 1, (ch + 1) & 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      const uint32_t* tile = reinterpret_cast<const uint32_t*>(smem + (ch & 1) * stage_bytes);
+      // token index li = (t*vy + y)*vx + x
+      acc[0] += lines_variance(tile, g.vy, g.vx, g.vx, 1, g.vt, g.vy * g.vx);  // along T
+      acc[1] += lines_variance(tile, g.vt, g.vx, g.vy * g.vx, 1, g.vy, g.vx);  // along H
+      acc[2] += lines_variance(tile, g.vt, g.vy, g.vy * g.vx, g.vx, g.vx, 1);  // along W
+      __syncthreads();
+    }
+    block_sum<3>(acc, red);
+    if (threadIdx.x == 0) {
+      const float nl[3] = {static_cast<float>(g.vy * g.vx), static_cast<float>(g.vt * g.vx),
+                           static_cast<float>(g.vt * g.vy)};
+      const int len[3] = {g.vt, g.vy, g.vx};
+      float* o = stats + ((static_cast<long long>(b) * c.H + h) * Z + z) * 8;
+      for (int a = 0; a < 3; ++a)
+        o[a] = len[a] >= 2 ? acc[a] / (nl[a] * static_cast<float>(c.d)) : 0.f;
+    }
+  } else {
+    // ---- A2V norm map of the zone: n_i = ||a2v_i||_2 ----
+    float* nmap = reinterpret_cast<float*>(smem);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int li = warp; li < vol; li += nw) {
+      const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
+      const long long n =
+          (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
+      const uint16_t* row = a2v + (static_cast<long long>(b) * N + n) * c.Ca;
+      float s = 0.f;
+      for (int k = lane; k < c.Ca; k += 32) {
+        float v = bf16_to_f(row[k]);
+        s = fmaf(v, v, s);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) nmap[li] = sqrtf(s);
+    }
+    __syncthreads();
+    // line variances of the scalar map, thread per line
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int nlT = g.vy * g.vx, nlH = g.vt * g.vx, nlW = g.vt * g.vy;
+    for (int ln = threadIdx.x; ln < nlT + nlH + nlW; ln += blockDim.x) {
+      int base, len, step, axis;
+      if (ln < nlT) {
+        axis = 0; base = ln; len = g.vt; step = g.vy * g.vx;
+      } else if (ln < nlT + nlH) {
+        const int l = ln - nlT;
+        axis = 1; base = (l / g.vx) * g.vy * g.vx + (l % g.vx); len = g.vy; step = g.vx;
+      } else {
+        const int l = ln - nlT - nlH;
+        axis = 2; base = l * g.vx; len = g.vx; step = 1;
+      }
+      if (len < 2) continue;
+      float m = 0.f;
+      for (int k = 0; k < len; ++k) m += nmap[base + k * step];
+      m /= static_cast<float>(len);
+      float s = 0.f;
+      for (int k = 0; k < len; ++k) {
+        float e = nmap[base + k * step] - m;
+        s = fmaf(e, e, s);
+      }
+      acc[axis] += s / static_cast<float>(len);
+    }
+    for (int li = threadIdx.x; li < vol; li += blockDim.x) acc[3] += nmap[li];
+    block_sum<4>(acc, red);
+    if (threadIdx.x == 0) {
+      const float nl[3] = {static_cast<float>(nlT), static_cast<float>(nlH),
+                           static_cast<float>(nlW)};
+      const int len[3] = {g.vt, g.vy, g.vx};
+      float out[5];
+      for (int a = 0; a < 3; ++a) out[a] = len[a] >= 2 ? acc[a] / nl[a] : 0.f;
+      out[3] = acc[3] / static_cast<float>(vol);
+      out[4] = static_cast<float>(vol);
+      for (int hh = 0; hh < c.H; ++hh) {
+        float* o = stats + ((static_cast<long long>(b) * c.H + hh) * Z + z) * 8;
+        for (int k = 0; k < 5; ++k) o[3 + k] = out[k];
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ assign ------
+
+struct MenuConst {
+  double log2_ext[PRISM_MAX_SHAPES][3];
+  int adm[PRISM_MAX_SHAPES];
+  int n_adm;
+  double log2_S;
+};
+
+// Eq. 7 (Table 10 caption) in log space: with bT*bH*bW = S fixed, the
+// continuous optimum of b_d ~ g_d^-alpha is
+//   log2 b*_d = log2(S)/3 + alpha * (mean_d log2 g_d - log2 g_d)
+// and each admissible menu shape is scored by sum_d (log2 b_d - log2 b*_d)^2.
+// Guidance g_d = u_v r_{v,d} + u_a a_bar v_hat_{a,d} + eps, with
+// r_{v,d} = var_v_d / sum var_v, v_hat_{a,d} = var_n_d / sum var_n (1/3 each
+// when the sum is 0) and a_bar = nbar / max over the zones of nbar.
+__global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, MenuConst menu,
+                                                     const float* __restrict__ stats,
+                                                     uint8_t* __restrict__ shape_id,
+                                                     uint8_t* __restrict__ shape_tie) {
+  __shared__ double red[32];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const float* sb = stats + static_cast<long long>(b) * c.H * Z * 8;
+  const float* sh = sb + static_cast<long long>(h) * Z * 8;
+  // max over zones of nbar (the audio statistics are the same for every head)
+  double mx = 0.0;
+  for (int z = threadIdx.x; z < Z; z += blockDim.x) mx = fmax(mx, static_cast<double>(sh[z * 8 + 6]));
+  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double m = 0.0;
+    for (int w = 0; w < (blockDim.x >> 5); ++w) m = fmax(m, red[w]);
+    red[0] = m;
+  }
+  __syncthreads();
+  const double nmax = red[0];
+  for (int z = threadIdx.x; z < Z; z += blockDim.x) {
+    double sv[3], sn[3], nbar;
+    if (c.per_head) {
+      for (int a = 0; a < 3; ++a) sv[a] = sh[z * 8 + a];
+    } else {
+      for (int a = 0; a < 3; ++a) {
+        double s = 0.0;
+        for (int hh = 0; hh < c.H; ++hh) s += static_cast<double>(sb[(static_cast<long long>(hh) * Z + z) * 8 + a]);
+        sv[a] = s / c.H;
+      }
+    }
+    for (int a = 0; a < 3; ++a) sn[a] = sh[z * 8 + 3 + a];
+    nbar = sh[z * 8 + 6];
+    const double ssv = sv[0] + sv[1] + sv[2];
+    const double ssn = sn[0] + sn[1] + sn[2];
+    const double abar = nmax > 0.0 ? nbar / nmax : 0.0;
+    const double uv = c.use_video ? 1.0 : 0.0, ua = c.use_audio ? 1.0 : 0.0;
+    double lg[3];
+    for (int a = 0; a < 3; ++a) {
+      const double r = ssv > 0.0 ? sv[a] / ssv : 1.0 / 3.0;
+      const double vh = ssn > 0.0 ? sn[a] / ssn : 1.0 / 3.0;
+      const double gd = uv * r + ua * abar * vh + c.eps;
+      lg[a] = log2(gd);
+    }
+    const double mean = (lg[0] + lg[1] + lg[2]) / 3.0;
+    double lstar[3];
+    for (int a = 0; a < 3; ++a) lstar[a] = menu.log2_S / 3.0 + c.alpha * (mean - lg[a]);
+    double best = 1e300, second = 1e300;
+    int bk = menu.adm[0];
+    for (int q = 0; q < menu.n_adm; ++q) {
+      const int k = menu.adm[q];
+      double cost = 0.0;
+      for (int a = 0; a < 3; ++a) {
+        const double e = menu.log2_ext[k][a] - lstar[a];
+        cost += e * e;
+      }
+      if (cost < best) {
+        second = best;
+        best = cost;
+        bk = k;
+      } else if (cost < second) {
+        second = cost;
+      }
+    }
+    const long long o = (static_cast<long long>(b) * c.H + h) * Z + z;
+    shape_id[o] = static_cast<uint8_t>(bk);
+    shape_tie[o] = (menu.n_adm > 1 && (second - best) < 1e-4) ? 1 : 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* a2v,
+                              float* stats, cudaStream_t st) {
+  const prism_config_t& c = p.cfg;
+  const int vol = c.zT * c.zH * c.zW;
+  const size_t smem_video = 2ull * vol * kChunk * 2;
+  const size_t smem_audio = static_cast<size_t>(vol) * sizeof(float);
+  const size_t smem = smem_video > smem_audio ? smem_video : smem_audio;
+  cudaError_t e = cudaFuncSetAttribute(zone_stats_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.sz.Z, c.H + 1, c.B);
+  zone_stats_kernel<<<grid, kStatsThreads, smem, st>>>(c, p.sz.nzH, p.sz.nzW, p.sz.Z, V, a2v,
+                                                      stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assign(const Plan& p, const float* stats, uint8_t* shape_id,
+                          uint8_t* shape_tie, cudaStream_t st) {
+  MenuConst m;
+  for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
+    for (int a = 0; a < 3; ++a) m.log2_ext[k][a] = p.log2_ext[k][a];
+  for (int q = 0; q < PRISM_MAX_SHAPES; ++q) m.adm[q] = p.sz.admissible[q];
+  m.n_adm = p.sz.n_admissible;
+  m.log2_S = p.log2_S;
+  assign_kernel<<<dim3(p.cfg.H, p.cfg.B), 256, 0, st>>>(p.cfg, p.sz.Z, m, stats, shape_id,
+                                                        shape_tie);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

@@ -1,0 +1,199 @@
+/*
+ * prism.h -- C ABI of the B300 (sm_103a) Prism block-sparse attention path.
+ *
+ * Prism: Dynamic Sparse Attention for Native 2K Joint Video-Audio Generation
+ * Model Training (arXiv 2610.05416).  The pages state the method in the
+ * Abstract and the Fig. 2 caption: the latent token grid is cut into
+ * spatiotemporal macro-zones; each zone gets a block shape from the
+ * directional variance of the video features and the norms of the
+ * audio-to-video cross-attention output; tokens are regrouped so that every
+ * block is contiguous; block-level (pooled) features give block scores; a
+ * hybrid Top-k / Top-p rule picks key blocks per query block; block-sparse
+ * attention runs over the picked blocks, forward and backward.
+ *
+ * Conventions shared by every entry point
+ *   - All device pointers are owned by the caller.  The library never
+ *     allocates device memory; it allocates only the host-side plan.
+ *   - Every call is asynchronous on the caller's stream `stream`
+ *     (a cudaStream_t passed as void*; NULL = legacy default stream) and
+ *     returns once the work is enqueued.  Argument errors are detected on
+ *     the host before anything is enqueued.
+ *   - Token layout of model-side tensors (Q, K, V, dO, O, dQ, dK, dV):
+ *     [B, N, H, d] row-major bf16, token n = (t * Hg + y) * W + x over the
+ *     real grid (T, Hg, W).  a2v: [B, N, Ca] bf16.
+ *   - Permuted ("block order") tensors Xp: [B, H, Np, d] row-major; slot
+ *     s of head h belongs to block s / S.  Padding slots hold zeros.
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Device pointers must be 16-byte aligned; d must be a multiple of 8.
+ *   - Return value: PRISM_OK (0) or a negative PRISM_ERR_* code.  Errors
+ *     raised inside a kernel (a bounded wait that ran out, an index out of
+ *     range) are recorded in the status word of the workspace and read
+ *     with prism_device_status().
+ */
+#ifndef PRISM_H_
+#define PRISM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PRISM_MAX_SHAPES 16
+
+enum {
+  PRISM_OK = 0,
+  PRISM_ERR_ARG = -1,            /* null pointer, bad size or inconsistent configuration */
+  PRISM_ERR_ALIGN = -2,          /* a device pointer is not 16-byte aligned */
+  PRISM_ERR_UNSUPPORTED = -3,    /* d, block size or menu outside what the kernels handle */
+  PRISM_ERR_NO_ADMISSIBLE_SHAPE = -4, /* no menu shape tiles the macro-zone */
+  PRISM_ERR_CUDA = -5,           /* a CUDA runtime call failed (launch, copy, attribute) */
+  PRISM_ERR_DEVICE_TIMEOUT = -6, /* a device-side wait exceeded its bound; results are invalid */
+  PRISM_ERR_DEVICE_BOUNDS = -7   /* a device-side index check failed; results are invalid */
+};
+
+/* Problem statement (Prism Abstract; Fig. 2 caption; Tables 7, 9, 10, 12). */
+typedef struct prism_config {
+  int B, H, d;            /* batch, heads, head dim (multiple of 8, <= 128)          */
+  int T, Hg, W;           /* real latent grid (frames, height, width) in tokens     */
+  int zT, zH, zW;         /* macro-zone extents; the grid is zero-padded up to      */
+                          /* multiples of them                                      */
+  int block_tokens;       /* S: tokens per block; every menu shape has bT*bH*bW==S  */
+  int n_shapes;           /* menu size, 1..PRISM_MAX_SHAPES                         */
+  int shapes[PRISM_MAX_SHAPES][3]; /* menu of (bT, bH, bW) block shapes            */
+  int Ca;                 /* channels of the audio-to-video cross-attention output  */
+  double alpha;           /* Eq. 7 exponent: b*_d proportional to g_d^-alpha        */
+  double eps;             /* floor added to the guidance g_d                        */
+  int per_head;           /* 1: shapes per head; 0: one shape per zone for all heads */
+  int use_video;          /* 1: video variance guidance on (Table 12 ablates it)    */
+  int use_audio;          /* 1: audio guidance on (Table 12 ablates it)             */
+  int topk_floor;         /* Top-k: minimum number of key blocks per query block    */
+  float topp;             /* Top-p: cumulative block weight that must be exceeded   */
+  unsigned long long timeout_cycles; /* bound on any device wait; 0 = default (~2 s) */
+} prism_config_t;
+
+/* Derived sizes of a plan. */
+typedef struct prism_sizes {
+  int Tp, Hp, Wp;         /* padded grid */
+  int nzT, nzH, nzW;      /* zones per axis */
+  int Z;                  /* zones = nzT * nzH * nzW */
+  int nb;                 /* blocks per (b, h) = Np / S */
+  int blocks_per_zone;
+  long long N, Np;        /* real and padded tokens */
+  int n_admissible;       /* menu shapes that tile the zone */
+  int admissible[PRISM_MAX_SHAPES];
+  long long max_pairs;    /* capacity needed for col_idx / row_idx: B*H*nb*nb */
+  size_t ws_bytes;        /* workspace bytes needed by prism_block_select,
+                             prism_sparse_attn_fwd and prism_sparse_attn_bwd */
+  int tensor_core_path;   /* 1 when the attention runs on the tcgen05 kernels */
+} prism_sizes_t;
+
+typedef struct prism_plan prism_plan_t;
+
+/* Validate `cfg` and build a host plan.  Errors: PRISM_ERR_ARG (sizes),
+ * PRISM_ERR_UNSUPPORTED (menu with unequal token counts, d, S),
+ * PRISM_ERR_NO_ADMISSIBLE_SHAPE (no menu shape divides the zone). */
+int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out);
+void prism_plan_destroy(prism_plan_t* plan);
+int prism_plan_query(const prism_plan_t* plan, prism_sizes_t* out);
+
+/* Clear the device status word at the start of the workspace (async). */
+int prism_ws_init(const prism_plan_t* plan, void* ws, void* stream);
+/* Wait for `stream`, read the status word; returns PRISM_OK or the first
+ * device error (PRISM_ERR_DEVICE_TIMEOUT / PRISM_ERR_DEVICE_BOUNDS). */
+int prism_device_status(const prism_plan_t* plan, const void* ws, void* stream);
+const char* prism_strerror(int code);
+
+/* Step 1 -- zone statistics (Prism Abstract: video feature variance along
+ * each axis and A2V feature norms; Table 9 caption: per-channel variance of
+ * the value features r_{v,d}, audio coupling gate a_bar, audio directional
+ * variance v_hat_{a,d}).
+ *   V      [B, N, H, d] bf16     value features (post-projection)
+ *   a2v    [B, N, Ca]  bf16      audio-to-video cross-attention output
+ *   stats  [B, H, Z, 8] fp32 out (var_v_T, var_v_H, var_v_W,
+ *                                 var_n_T, var_n_H, var_n_W, nbar, n_valid)
+ * var_*_d: mean over the zone's lines along d (lines with >= 2 real tokens)
+ * and over channels of the population variance on the line; n = ||a2v||_2. */
+int prism_zone_stats(const prism_plan_t* plan, const uint16_t* V, const uint16_t* a2v,
+                     float* stats, void* stream);
+
+/* Step 2 -- block shape per zone (Eq. 7 quantisation, Table 10 caption) and
+ * the token permutation into zone / block order, fused with block pooling.
+ *   stats      [B, H, Z, 8] fp32 in
+ *   Q, K, V    [B, N, H, d] bf16 in
+ *   shape_id   [B, H, Z] uint8 out: menu index of the zone's shape
+ *   shape_tie  [B, H, Z] uint8 out: 1 when the best two costs differ < 1e-4
+ *   perm       [B, H, Np] int32 out: slot -> token, -1 for a padding slot
+ *   inv        [B, H, N]  int32 out: token -> slot
+ *   Qp, Kp, Vp [B, H, Np, d] bf16 out
+ *   Qbar, Qbar_lo, Kbar, Kbar_lo [B, H, nb, d] fp32 out: mean over the
+ *              block's real tokens as a double-float pair: Qbar is the fp32
+ *              rounding of the mean and Qbar_lo the fp32 rounding of the rest
+ *              (Qbar + Qbar_lo carries about 46 significant bits); 0 for a
+ *              block without real tokens
+ *   n_valid    [B, H, nb] int32 out: real tokens in the block (first in it) */
+int prism_assign_and_permute(const prism_plan_t* plan, const float* stats,
+                             const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                             uint8_t* shape_id, uint8_t* shape_tie, int32_t* perm,
+                             int32_t* inv, uint16_t* Qp, uint16_t* Kp, uint16_t* Vp,
+                             float* Qbar, float* Qbar_lo, float* Kbar, float* Kbar_lo,
+                             int32_t* n_valid, void* stream);
+
+/* Step 3+4 -- block scores Qbar Kbar^T / sqrt(d) and hybrid Top-k / Top-p
+ * selection (Table 7 caption; Abstract: per-query sparsity), then the
+ * block lists in both directions.
+ *   Qbar, Qbar_lo, Kbar, Kbar_lo [B, H, nb, d] fp32 in (as written above)
+ *   n_valid     [B, H, nb] int32 in
+ *   row_ptr     [B*H*nb + 1] int32 out: CSR offsets over all (b, h, i)
+ *   col_idx     [max_pairs] int32 out: key blocks of each query block, ascending
+ *   col_ptr     [B*H*nb + 1] int32 out: CSC offsets over all (b, h, j)
+ *   row_idx     [max_pairs] int32 out: query blocks of each key block, ascending
+ *   sel_tie     [B, H, nb] uint8 out: 1 where the decision sat within 1e-6 of
+ *               a boundary (score gap or cumulative mass)
+ *   ws          workspace of ws_bytes
+ * Query blocks with no real token select nothing; candidates are the key
+ * blocks with at least one real token. */
+int prism_block_select(const prism_plan_t* plan, const float* Qbar, const float* Qbar_lo,
+                       const float* Kbar, const float* Kbar_lo, const int32_t* n_valid,
+                       int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
+                       int32_t* row_idx, uint8_t* sel_tie, void* ws, void* stream);
+
+/* Step 5a -- block-sparse attention forward (Fig. 2 caption).
+ * For every query block i and every key block j in its list, exact softmax
+ * over the real tokens of the listed key blocks, scale `scale`.
+ *   Qp, Kp, Vp [B, H, Np, d] bf16 in; n_valid, row_ptr, col_idx as above
+ *   Op  [B, H, Np, d] bf16 out (padding rows 0)
+ *   lse [B, H, Np] fp32 out: natural-log log-sum-exp per row (padding 0) */
+int prism_sparse_attn_fwd(const prism_plan_t* plan, const uint16_t* Qp, const uint16_t* Kp,
+                          const uint16_t* Vp, const int32_t* n_valid, const int32_t* row_ptr,
+                          const int32_t* col_idx, float scale, uint16_t* Op, float* lse,
+                          void* ws, void* stream);
+
+/* Gather a model-side tensor into block order: Xp[b,h,s] = X[b,perm[s],h]
+ * (zeros where perm[s] < 0).  X [B, N, H, d] bf16 -> Xp [B, H, Np, d] bf16. */
+int prism_permute(const prism_plan_t* plan, const int32_t* perm, const uint16_t* X,
+                  uint16_t* Xp, void* stream);
+
+/* Step 5b -- backward of step 5a (Prism trains through this attention; it
+ * replaces video self-attention during training, Table 2 caption).  The
+ * selection and the permutation are constants.
+ *   dOp [B, H, Np, d] bf16 in (padding rows must be 0, as prism_permute writes)
+ *   dQp, dKp, dVp [B, H, Np, d] bf16 out (padding rows 0) */
+int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const uint16_t* Kp,
+                          const uint16_t* Vp, const uint16_t* Op, const uint16_t* dOp,
+                          const float* lse, const int32_t* n_valid, const int32_t* row_ptr,
+                          const int32_t* col_idx, const int32_t* col_ptr,
+                          const int32_t* row_idx, float scale, uint16_t* dQp, uint16_t* dKp,
+                          uint16_t* dVp, void* ws, void* stream);
+
+/* Inverse permutation: X[b,n,h] = Xp[b,h,inv[n]].  Xp [B, H, Np, d] bf16 ->
+ * X [B, N, H, d] bf16. */
+int prism_unpermute(const prism_plan_t* plan, const int32_t* inv, const uint16_t* Xp,
+                    uint16_t* X, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRISM_H_ */

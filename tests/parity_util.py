@@ -1,0 +1,222 @@
+"""Step-by-step comparison of the CUDA path (through the C ABI) with the CPU
+oracle on the same seeded inputs.
+
+Contract (checked per step):
+  * zone statistics: relative 2e-5 of the column's scale (fp32 vs fp64);
+  * shape ids: identical, except zones the oracle flags as near ties (either
+    shape is then accepted and the CUDA choice is carried into the oracle);
+  * perm / inv / n_valid and the permuted Q, K, V: bit-exact;
+  * block means: |(hi + lo) - oracle| <= 1e-11 max(1, |mean|);
+  * block lists: identical per query block, except rows the oracle flags as
+    near ties (then the CUDA list is carried into the oracle);
+  * CSC lists: exactly the transpose of the CSR lists;
+  * attention: max|gpu - ref| / max|ref| per head <= 2e-2 for O and <= 5e-2
+    for dQ, dK, dV (bf16 tensor-core arithmetic against fp64).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from content_adaptive_block_02_b300 import prism, synth
+from oracle import prism_oracle as orc
+
+O_TOL = 2e-2
+G_TOL = 5e-2
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(w, inputs):
+    dev = torch.device("cuda")
+    x = {k: inputs[k].to(dev) for k in ("Q", "K", "V", "a2v", "dO")}
+    att = prism.PrismAttention(w, dev)
+    O = att.forward(x["Q"], x["K"], x["V"], x["a2v"])
+    dQ, dK, dV = att.backward(x["dO"])
+    torch.cuda.synchronize()
+    assert att.status() == 0, "device status word set"
+    g = {k: v.cpu() for k, v in att.perm_out.items()}
+    g.update({k: v.cpu() for k, v in att.lists.items()})
+    g.update(stats=att.stats.cpu(), Op=att.Op.cpu(), lse=att.lse.cpu(), O=O.cpu(),
+             dQ=dQ.cpu(), dK=dK.cpu(), dV=dV.cpu(), dQp=att.dQp.cpu(), dKp=att.dKp.cpu(),
+             dVp=att.dVp.cpu(), dOp=att.dOp.cpu())
+    return att, g
+
+
+def gpu_lists(w, g, nb):
+    """CSR lists of every (b, h) as python lists of ascending arrays."""
+    rp = g["row_ptr"].numpy()
+    ci = g["col_idx"].numpy()
+    out = {}
+    for b in range(w.B):
+        for h in range(w.H):
+            L = []
+            for i in range(nb):
+                r = (b * w.H + h) * nb + i
+                L.append(ci[rp[r]:rp[r + 1]].astype(np.int64))
+            out[(b, h)] = L
+    return out
+
+
+def rel_err(a, b):
+    den = np.abs(b).max()
+    return np.abs(a - b).max() / (den if den > 0 else 1.0)
+
+
+def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=None):
+    """Run both sides on the seeded inputs of `w`; assert the contract.
+    heads / rows / key_blocks restrict the oracle's attention work (a sample
+    of the (b, h), query blocks and key blocks)."""
+    inputs = synth.generate(w, "cpu")
+    att, g = run_gpu(w, inputs)
+    nb = att.plan.nb
+    X = {k: f64(inputs[k]) for k in ("Q", "K", "V", "a2v", "dO")}
+    rep = {} if report is None else report
+    hs = list(range(w.H)) if heads is None else list(heads)
+
+    # ---- step 1: zone statistics ----
+    Vs = X["V"][:, :, hs, :]
+    w_h = w.with_(H=len(hs))
+    st_o = orc.zone_stats(w_h, Vs, X["a2v"])
+    st_g = f64(g["stats"])[:, hs]
+    for k in range(8):
+        scale = max(1e-30, np.abs(st_o[..., k]).max())
+        err = np.abs(st_g[..., k] - st_o[..., k]).max() / scale
+        assert err <= 2e-5, (k, err)
+    if not w.per_head:
+        st_o = orc.zone_stats(w, X["V"], X["a2v"])
+
+    # ---- step 2: shapes, permutation, pooling ----
+    if w.per_head:
+        sid_o, tie_o = orc.assign_shapes(w_h, st_o)
+    else:
+        sid_o, tie_o = orc.assign_shapes(w, st_o)
+        sid_o, tie_o = sid_o[:, hs], tie_o[:, hs]
+    sid_g = g["shape_id"].numpy().astype(np.int64)[:, hs]
+    mism = sid_g != sid_o
+    assert not (mism & ~tie_o).any(), "shape id differs on a zone that is not a near tie"
+    rep["shape_ties_taken"] = int(mism.sum())
+    sid_use = np.where(mism, sid_g, sid_o)
+    perm_o, inv_o, nval_o = orc.build_permutation(w_h, sid_use)
+    assert np.array_equal(g["perm"].numpy()[:, hs], perm_o)
+    assert np.array_equal(g["inv"].numpy()[:, hs], inv_o)
+    assert np.array_equal(g["n_valid"].numpy()[:, hs], nval_o)
+    Qp_o = orc.permute(X["Q"][:, :, hs], perm_o)
+    Kp_o = orc.permute(X["K"][:, :, hs], perm_o)
+    Vp_o = orc.permute(X["V"][:, :, hs], perm_o)
+    assert np.array_equal(f64(g["Qp"])[:, hs], Qp_o)
+    assert np.array_equal(f64(g["Kp"])[:, hs], Kp_o)
+    assert np.array_equal(f64(g["Vp"])[:, hs], Vp_o)
+    Qb_o = orc.pool(Qp_o, nval_o, w.block)
+    Kb_o = orc.pool(Kp_o, nval_o, w.block)
+    Qb_g = (f64(g["Qbar"]) + f64(g["Qbar_lo"]))[:, hs]
+    Kb_g = (f64(g["Kbar"]) + f64(g["Kbar_lo"]))[:, hs]
+    assert np.abs(Qb_g - Qb_o).max() <= 1e-11 * max(1.0, np.abs(Qb_o).max())
+    assert np.abs(Kb_g - Kb_o).max() <= 1e-11 * max(1.0, np.abs(Kb_o).max())
+
+    # ---- step 3+4: selection ----
+    Lg_all = gpu_lists(w, g, nb)
+    Lo, Fo = orc.select_blocks(w_h, Qb_o, Kb_o, nval_o, rows=rows)
+    diff_rows = 0
+    flagged = 0
+    # The CUDA lists (equal to the oracle's on every unflagged row checked
+    # here) are the ones the attention steps of both sides use.
+    L_use = {(b, hi): Lg_all[(b, h)] for b in range(w.B) for hi, h in enumerate(hs)}
+    for b in range(w.B):
+        for hi, h in enumerate(hs):
+            Lg = Lg_all[(b, h)]
+            lo_, fo = Lo[(b, hi)], Fo[(b, hi)]
+            for i in range(nb):
+                if lo_[i] is None:
+                    continue
+                flagged += int(fo[i])
+                if not np.array_equal(Lg[i], lo_[i]):
+                    assert fo[i], f"list differs on an unflagged row (b={b}, h={h}, i={i})"
+                    diff_rows += 1
+    L_fwd = {k: [L[i] if (rows is None or i in rows) else None for i in range(nb)]
+             for k, L in L_use.items()}
+    rep["select_rows_differing_on_near_ties"] = diff_rows
+    rep["select_rows_flagged"] = flagged
+    # CSC = transpose of CSR (exact)
+    cp = g["col_ptr"].numpy()
+    ri = g["row_idx"].numpy()
+    for b in range(w.B):
+        for h in hs:
+            cols = orc.csc_from_lists(Lg_all[(b, h)], nb)
+            for j in range(nb):
+                r = (b * w.H + h) * nb + j
+                assert np.array_equal(ri[cp[r]:cp[r + 1]], cols[j]), (b, h, j)
+
+    # ---- step 5: attention forward ----
+    scale = 1.0 / math.sqrt(w.d)
+    Op_o, lse_o = orc.attn_fwd(w_h, Qp_o, Kp_o, Vp_o, nval_o, L_fwd, scale)
+    Op_g = f64(g["Op"])[:, hs]
+    lse_g = f64(g["lse"])[:, hs]
+    row_mask = np.zeros(w.Np, bool)
+    for i in (range(nb) if rows is None else rows):
+        row_mask[i * w.block:(i + 1) * w.block] = True
+    errs = []
+    for b in range(w.B):
+        for hi in range(len(hs)):
+            e = rel_err(Op_g[b, hi, row_mask], Op_o[b, hi, row_mask])
+            errs.append(e)
+            assert e <= O_TOL, ("O", b, hs[hi], e)
+            assert np.abs(lse_g[b, hi, row_mask] - lse_o[b, hi, row_mask]).max() <= 2e-2
+    rep["O_max_rel"] = max(errs)
+    if rows is None and heads is None:
+        O_o = orc.unpermute(Op_o, inv_o)
+        assert rel_err(f64(g["O"]), O_o) <= O_TOL
+
+    if not check_bwd:
+        return rep
+    # ---- step 5b: backward ----
+    dOp_o = orc.permute(X["dO"][:, :, hs], perm_o)
+    assert np.array_equal(f64(g["dOp"])[:, hs], dOp_o)
+    if key_blocks is None and rows is None:
+        dQ_o, dK_o, dV_o = orc.attn_bwd(w_h, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, L_use, scale)
+        for name, got, ref in (("dQ", g["dQp"], dQ_o), ("dK", g["dKp"], dK_o),
+                               ("dV", g["dVp"], dV_o)):
+            got = f64(got)[:, hs]
+            e = max(rel_err(got[b, hi], ref[b, hi]) for b in range(w.B) for hi in range(len(hs)))
+            rep[name + "_max_rel"] = e
+            assert e <= G_TOL, (name, e)
+        if heads is None:
+            for name, ref in (("dQ", dQ_o), ("dK", dK_o), ("dV", dV_o)):
+                assert rel_err(f64(g[name]), orc.unpermute(ref, inv_o)) <= G_TOL, name
+    else:
+        # dQ on the sampled rows, dK / dV on the sampled key blocks (all the
+        # query blocks that selected them contribute)
+        S = w.block
+        if rows is not None:
+            dQ_o, _, _ = orc.attn_bwd(w_h, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, L_use, scale,
+                                      rows_only=set(rows))
+            got = f64(g["dQp"])[:, hs]
+            e = 0.0
+            for b in range(w.B):
+                for hi in range(len(hs)):
+                    e = max(e, rel_err(got[b, hi, row_mask], dQ_o[b, hi, row_mask]))
+            rep["dQ_max_rel"] = e
+            assert e <= G_TOL, ("dQ", e)
+        if key_blocks:
+            ek = 0.0
+            for b in range(w.B):
+                for hi in range(len(hs)):
+                    cols = orc.csc_from_lists(L_use[(b, hi)], nb)
+                    for j in key_blocks:
+                        qs = set(int(i) for i in cols[j])
+                        _, dK_o, dV_o = orc.attn_bwd(
+                            w_h, Qp_o[b:b + 1, hi:hi + 1], Kp_o[b:b + 1, hi:hi + 1],
+                            Vp_o[b:b + 1, hi:hi + 1], dOp_o[b:b + 1, hi:hi + 1],
+                            nval_o[b:b + 1, hi:hi + 1], {(0, 0): L_use[(b, hi)]}, scale,
+                            rows_only=qs)
+                        sl = slice(j * S, (j + 1) * S)
+                        for nm, ref in (("dKp", dK_o), ("dVp", dV_o)):
+                            got = f64(g[nm])[b, hs[hi], sl]
+                            ek = max(ek, rel_err(got, ref[0, 0, sl]))
+            rep["dKV_sampled_max_rel"] = ek
+            assert ek <= G_TOL, ("dK/dV", ek)
+    return rep

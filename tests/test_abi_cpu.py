@@ -1,0 +1,80 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the header declares, and validates configurations and sizes
+on the host exactly as the oracle's geometry says."""
+import ctypes
+
+import pytest
+
+from content_adaptive_block_02_b300 import build, prism, synth
+from oracle import prism_oracle as orc
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return prism.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = prism.declared_functions()
+    assert len(names) == 13
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_strerror_names_every_code(L):
+    for code in range(0, -8, -1):
+        s = L.prism_strerror(code).decode()
+        assert s and s != "unknown error"
+    assert L.prism_strerror(-99).decode() == "unknown error"
+
+
+@pytest.mark.parametrize("name", ["tiny", "720p", "1080p", "2k", "2k_long"])
+def test_plan_sizes_match_oracle_geometry(L, name):
+    w = synth.WORKLOADS[name]
+    p = prism.Plan(w)
+    Tp, Hp, Wp = orc.padded_grid(w.T, w.Hg, w.W, w.zone)
+    assert (p.sz.Tp, p.sz.Hp, p.sz.Wp) == (Tp, Hp, Wp)
+    assert p.sz.N == w.N and p.sz.Np == Tp * Hp * Wp == w.Np
+    assert p.sz.Z == w.n_zones and p.sz.nb == w.n_blocks
+    assert list(p.sz.admissible[: p.sz.n_admissible]) == orc.admissible_shapes(w.menu, w.zone)
+    assert p.sz.max_pairs == w.B * w.H * w.n_blocks ** 2
+    assert p.sz.ws_bytes > 0
+
+
+def test_2k_sizes_are_the_documented_ones(L):
+    p = prism.Plan(synth.WORKLOADS["2k"])
+    assert (p.sz.Np, p.sz.Z, p.sz.nb) == (322_560, 420, 2520)
+    assert p.sz.tensor_core_path in (0, 1)
+
+
+def _err(w):
+    with pytest.raises(prism.PrismError) as e:
+        prism.Plan(w)
+    return e.value.code
+
+
+def test_plan_rejects_bad_configurations(L):
+    base = synth.WORKLOADS["tiny"]
+    assert _err(base.with_(B=0)) == -1                         # PRISM_ERR_ARG
+    assert _err(base.with_(topk_floor=-1)) == -1
+    assert _err(base.with_(topp=float("nan"))) == -1
+    assert _err(base.with_(d=48)) == -3                        # not a multiple of 32
+    assert _err(base.with_(menu=((1, 4, 4), (2, 2, 2)))) == -3  # unequal token counts
+    assert _err(base.with_(zone=(3, 3, 3))) == -4              # nothing tiles the zone
+    assert _err(base.with_(block=12, menu=((1, 3, 4),))) == -3  # block size not a power of 2
+
+
+def test_null_pointers_are_rejected_before_any_launch(L):
+    p = prism.Plan(synth.WORKLOADS["tiny"])
+    assert L.prism_zone_stats(p.h, None, None, None, None) == -1
+    assert L.prism_unpermute(p.h, None, None, None, None) == -1
+    assert L.prism_plan_query(None, None) == -1
+
+
+def test_misaligned_pointers_are_rejected_before_any_launch(L):
+    p = prism.Plan(synth.WORKLOADS["tiny"])
+    bad = ctypes.c_void_p(0x1008)     # never dereferenced: the host check rejects it
+    good = ctypes.c_void_p(0x1000)
+    assert L.prism_zone_stats(p.h, bad, good, good, None) == -2
+    assert L.prism_permute(p.h, good, good, bad, None) == -2

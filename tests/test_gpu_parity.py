@@ -1,0 +1,56 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle,
+step by step, on seeded synthetic inputs.  The contract is stated in
+tests/parity_util.py."""
+import pytest
+import torch
+
+from content_adaptive_block_02_b300 import build, synth
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def test_tiny_full_pipeline():
+    """16-token blocks, d = 64: the whole path, every step."""
+    rep = pu.compare(synth.WORKLOADS["tiny"])
+    assert rep["O_max_rel"] <= pu.O_TOL
+
+
+def test_small_ragged_grid_with_padding():
+    """5 x 7 x 9 grid: padding on every axis, partially real blocks."""
+    w = synth.WORKLOADS["tiny"].with_(T=5, Hg=7, W=9, H=3, name="ragged")
+    pu.compare(w)
+
+
+@pytest.mark.parametrize("kw", [dict(per_head=False), dict(use_video=False),
+                                dict(use_audio=False), dict(topp=0.5, topk_floor=1),
+                                dict(topp=0.99), dict(topk_floor=0, topp=0.0)])
+def test_tiny_variants(kw):
+    w = synth.WORKLOADS["tiny"].with_(**kw)
+    pu.compare(w)
+
+
+def test_topp_one_is_dense_attention():
+    """Top-p = 1 keeps every block: the path is plain softmax attention."""
+    import numpy as np
+    from oracle import prism_oracle as orc
+    w = synth.WORKLOADS["tiny"].with_(topp=1.0)
+    pu.compare(w)
+    inputs = synth.generate(w, "cpu")
+    att, g = pu.run_gpu(w, inputs)
+    nv = g["n_valid"].numpy()
+    for (b, h), L in pu.gpu_lists(w, g, att.plan.nb).items():
+        allv = np.nonzero(nv[b, h] > 0)[0]
+        for i, sel in enumerate(L):
+            assert np.array_equal(sel, allv if nv[b, h, i] > 0 else allv[:0])
+    X = {k: pu.f64(inputs[k]) for k in ("Q", "K", "V")}
+    for h in range(w.H):
+        ref = orc.dense_attention(X["Q"][0, :, h], X["K"][0, :, h], X["V"][0, :, h],
+                                  1 / np.sqrt(w.d))
+        assert pu.rel_err(pu.f64(g["O"])[0, :, h], ref) <= pu.O_TOL
