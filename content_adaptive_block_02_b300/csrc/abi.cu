@@ -123,7 +123,12 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   const long long rows = static_cast<long long>(c.B) * c.H * nb;
   z.max_pairs = rows * nb;
   if (z.max_pairs >= (1LL << 31)) return PRISM_ERR_UNSUPPORTED;
-  z.tensor_core_path = 0;
+  {
+    const bool tc_shape = c.block_tokens == 128 && c.d == 128 && c.attn_kernel == 0;
+    z.tensor_core_fwd = tc_shape ? 1 : 0;
+    z.tensor_core_bwd = 0;
+  }
+  if (c.attn_kernel < 0 || c.attn_kernel > 1) return PRISM_ERR_ARG;
   for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
     for (int a = 0; a < 3; ++a) {
       const int e = k < c.n_shapes ? c.shapes[k][a] : 1;
@@ -235,7 +240,7 @@ int prism_sparse_attn_fwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
   PRISM_CHECK_PTR(Op); PRISM_CHECK_PTR(lse); PRISM_CHECK_PTR(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Plan& p = plan->p;
-  if (p.sz.tensor_core_path) {
+  if (p.sz.tensor_core_fwd) {
     PRISM_CUDA(prism::launch_attn_fwd_tc(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op, lse,
                                          static_cast<uint8_t*>(ws), st));
   } else {
@@ -273,7 +278,7 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
   float* D = reinterpret_cast<float*>(w + p.off_D);
   float* dq = reinterpret_cast<float*>(w + p.off_dq);
   PRISM_CUDA(prism::launch_bwd_pre(p, Op, dOp, D, dq, st));
-  if (p.sz.tensor_core_path) {
+  if (p.sz.tensor_core_bwd) {
     PRISM_CUDA(prism::launch_attn_bwd_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx,
                                          scale, dq, dKp, dVp, w, st));
   } else {

@@ -1,16 +1,444 @@
-// Placeholder for the tcgen05 attention kernels (filled in next).
-#include "prism_internal.cuh"
+// Block-sparse attention forward on the 5th-generation tensor cores
+// (tcgen05 + tensor memory), 128-token blocks, head dim 128, bf16 in, fp32
+// accumulation.
+//
+// Prism (arXiv 2610.05416), Fig. 2 caption: each query block attends only to
+// the key blocks selected for it.  Reading used here: exact softmax over the
+// real tokens of the selected key blocks, scale `scale`, natural-log LSE.
+//
+// Design (one persistent CTA per SM, 192 threads, warp-specialised):
+//   warp 4  producer: takes the next query block from a global work counter,
+//           publishes it in a 2-slot work ring, and streams the K and V tiles
+//           of its selected key blocks into two 3-stage shared-memory rings
+//           with TMA (128-byte swizzle, 2 boxes of 64 x 128 per tile).
+//   warp 5  MMA issuer (one thread): S = Q K^T with Q held in tensor memory
+//           (A from TMEM, B = K tile from smem), then O += P V with P in
+//           tensor memory (A from TMEM, B = V tile, MN-major).  Order per
+//           query block: S_0, S_1, PV_0, S_2, PV_1, ... so the next score tile
+//           is on the tensor pipe while the softmax warps work on this one.
+//   warps 0-3  softmax (thread = query row = TMEM lane): Q row -> TMEM; per
+//           key block: S row from TMEM to registers, online softmax in the
+//           log2 domain with lazy rescaling (O in TMEM is rescaled only when
+//           the running max grows by more than 2^8), P (bf16) -> TMEM; at the
+//           end O / l -> bf16 rows of Op, LSE.
+// Tensor memory (512 columns): S [0,128), O [128,256), Q [256,320),
+// P0 [320,384), P1 [384,448).
+// Every wait is bounded: on expiry the CTA raises a flag, records the error in
+// the workspace status word, and every role stops issuing and leaves.
+#include <cudaTypedefs.h>
+
+#include "tc_common.cuh"
 
 namespace prism {
-cudaError_t launch_attn_fwd_tc(const Plan&, const uint16_t*, const uint16_t*, const uint16_t*,
-                               const int32_t*, const int32_t*, const int32_t*, float, uint16_t*,
-                               float*, uint8_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+using namespace tc;
+
+constexpr int kS = 128;
+constexpr int kD = 128;
+constexpr int kTile = kS * kD * 2;  // 32 KB
+constexpr int kStages = 3;
+constexpr int kFwdThreads = 192;
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_Q = 256, TM_P0 = 320, TM_P1 = 384;
+
+struct FwdShared {
+  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t s_full, s_free, p_full[2], o_full, q_ready, final_bar;
+  uint64_t work_full[2], work_empty[2];
+  int work_row[2], work_beg[2], work_end[2], work_nvq[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct FwdParams {
+  const uint16_t* Qp;
+  const int32_t* n_valid;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  uint16_t* Op;
+  float* lse;
+  uint32_t* status;
+  long long rows;
+  long long Np;
+  int nb;
+  float scale_log2;
+  unsigned long long limit;
+};
+
+__device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity,
+                                         unsigned long long limit) {
+  const unsigned long long t0 = clock64();
+  while (!mbar_try(bar, parity))
+    if (clock64() - t0 > limit) return false;
+  return true;
 }
+
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, FwdParams P) {
+  extern __shared__ uint8_t dsm_raw[];
+  __shared__ FwdShared sm;
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  uint8_t* kbuf = dsm;
+  uint8_t* vbuf = dsm + kStages * kTile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_free, 128);
+    mbar_init(&sm.p_full[0], 128);
+    mbar_init(&sm.p_full[1], 128);
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.q_ready, 128);
+    mbar_init(&sm.final_bar, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.work_full[s], 1);
+      mbar_init(&sm.work_empty[s], 129);
+    }
+    sm.abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const Waiter W{&sm.abort, P.status, P.limit};
+  uint32_t* queue = P.status + WS_FWD_QUEUE;
+
+  if (warp == 4) {
+    // ------------------------------------------------------ producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kuse = 0, vuse = 0;
+      for (uint32_t it = 0;; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_empty[ws], ((it >> 1) & 1) ^ 1, 1)) break;
+        const long long row = atomicAdd(queue, 1u);
+        if (row >= P.rows) {
+          sm.work_row[ws] = -1;
+          mbar_arrive(&sm.work_full[ws]);
+          break;
+        }
+        const int beg = P.row_ptr[row], end = P.row_ptr[row + 1];
+        const int nvq = P.n_valid[row];
+        sm.work_row[ws] = static_cast<int>(row);
+        sm.work_beg[ws] = beg;
+        sm.work_end[ws] = nvq > 0 ? end : beg;
+        sm.work_nvq[ws] = nvq;
+        mbar_arrive(&sm.work_full[ws]);
+        if (nvq == 0) continue;
+        const long long bh = row / P.nb;
+        bool ok = true;
+        for (int t = beg; t < end && ok; ++t) {
+          const int j = P.col_idx[t];
+          const int y = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
+          const int ks = kuse % kStages;
+          if (!W.wait(&sm.k_empty[ks], ((kuse / kStages) & 1) ^ 1, 2)) { ok = false; break; }
+          mbar_expect_tx(&sm.k_full[ks], kTile);
+          tma_load_2d(kbuf + ks * kTile, &tmK, &sm.k_full[ks], 0, y);
+          tma_load_2d(kbuf + ks * kTile + kTile / 2, &tmK, &sm.k_full[ks], 64, y);
+          ++kuse;
+          const int vs = vuse % kStages;
+          if (!W.wait(&sm.v_empty[vs], ((vuse / kStages) & 1) ^ 1, 3)) { ok = false; break; }
+          mbar_expect_tx(&sm.v_full[vs], kTile);
+          tma_load_2d(vbuf + vs * kTile, &tmV, &sm.v_full[vs], 0, y);
+          tma_load_2d(vbuf + vs * kTile + kTile / 2, &tmV, &sm.v_full[vs], 64, y);
+          ++vuse;
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------ MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);   // A = Q (TMEM), B = K, K-major
+      constexpr uint32_t idPV = idesc_bf16(128, 128, 0, 1);  // A = P (TMEM), B = V, MN-major
+      uint32_t kuse = 0, vuse = 0, sidx = 0, pidx = 0, qcnt = 0;
+      bool ok = true;
+      auto issue_pv = [&](bool first) -> bool {
+        const uint32_t pb = pidx & 1;
+        if (!W.wait(&sm.p_full[pb], (pidx >> 1) & 1, 7)) return false;
+        const int vs = vuse % kStages;
+        if (!W.wait(&sm.v_full[vs], (vuse / kStages) & 1, 8)) return false;
+        fence_after();
+        const uint32_t vb = smem_u32(vbuf + vs * kTile);
+        const uint32_t pa = tmem + (pb ? TM_P1 : TM_P0);
+#pragma unroll
+        for (int kk = 0; kk < kS / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTile / 2, 1024);
+          mma_ts(tmem + TM_O, pa + kk * 8, bd, idPV, (!first || kk > 0) ? 1u : 0u);
+        }
+        commit(&sm.o_full);
+        commit(&sm.v_empty[vs]);
+        ++vuse;
+        ++pidx;
+        return true;
+      };
+      for (uint32_t it = 0; ok; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 4)) break;
+        const int row = sm.work_row[ws];
+        if (row < 0) break;
+        const int n = sm.work_end[ws] - sm.work_beg[ws];
+        if (n > 0) {
+          if (!W.wait(&sm.q_ready, qcnt & 1, 5)) break;
+          ++qcnt;
+          fence_after();
+          for (int jj = 0; jj < n && ok; ++jj) {
+            if (jj > 0 && !W.wait(&sm.s_free, (sidx - 1) & 1, 6)) { ok = false; break; }
+            const int ks = kuse % kStages;
+            if (!W.wait(&sm.k_full[ks], (kuse / kStages) & 1, 9)) { ok = false; break; }
+            fence_after();
+            const uint32_t kb = smem_u32(kbuf + ks * kTile);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * (kTile / 2) + (kk & 3) * 32, 16, 1024);
+              mma_ts(tmem + TM_S, tmem + TM_Q + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
+            }
+            commit(&sm.s_full);
+            commit(&sm.k_empty[ks]);
+            ++kuse;
+            ++sidx;
+            if (jj > 0 && !issue_pv(jj == 1)) { ok = false; break; }
+          }
+          if (ok && !issue_pv(n == 1)) ok = false;
+        }
+        if (ok) mbar_arrive(&sm.work_empty[ws]);
+      }
+      commit(&sm.final_bar);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ softmax ----
+    const int r = threadIdx.x;  // query row of the block == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base + TM_S, tO = tmem + lane_base + TM_O;
+    uint32_t sidx = 0, pidx = 0, qcnt = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int ws = it & 1;
+      if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 10)) break;
+      const int row = sm.work_row[ws];
+      if (row < 0) break;
+      const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg, nvq = sm.work_nvq[ws];
+      const long long bh = row / P.nb;
+      const int i = row % P.nb;
+      const long long grow = bh * P.Np + static_cast<long long>(i) * kS + r;
+      uint4* orow = reinterpret_cast<uint4*>(P.Op + grow * kD);
+      if (n == 0) {
+#pragma unroll
+        for (int q = 0; q < kD / 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
+        P.lse[grow] = 0.f;
+        mbar_arrive(&sm.work_empty[ws]);
+        continue;
+      }
+      {
+        // this row of Q -> tensor memory (bf16 pairs, 64 columns)
+        const uint4* qrow = reinterpret_cast<const uint4*>(P.Qp + grow * kD);
+        uint32_t a[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = ldg_nc_v4(qrow + h * 8 + q);
+            a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_base + TM_Q + h * 32, a);
+        }
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&sm.q_ready);
+        ++qcnt;
+      }
+      const uint32_t pv_base = pidx;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int jj = 0; jj < n; ++jj) {
+        const int j = P.col_idx[beg + jj];
+        const int nvk = P.n_valid[bh * P.nb + j];
+        if (!W.wait(&sm.s_full, sidx & 1, 11)) { ok = false; break; }
+        fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+        tmem_ld_wait();
+        fence_before();
+        mbar_arrive(&sm.s_free);
+        ++sidx;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < nvk) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+        mx *= P.scale_log2;
+        const bool resc = mx > m + 8.f;
+        const float m_new = resc ? mx : m;
+        const float corr = resc ? ex2(m - m_new) : 1.f;
+        if (jj > 0 && __any_sync(0xffffffffu, resc)) {
+          const uint32_t g = pv_base + jj - 1;  // PV of the previous key block
+          if (!W.wait(&sm.o_full, g & 1, 12)) { ok = false; break; }
+          fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+        l *= corr;
+        m = m_new;
+        float lsum = 0.f;
+        const uint32_t tP = tmem + lane_base + ((pidx & 1) ? TM_P1 : TM_P0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int c0 = h * 64 + 2 * e;
+            const float x0 = __uint_as_float(s[c0 >> 5][c0 & 31]);
+            const float x1 = __uint_as_float(s[(c0 + 1) >> 5][(c0 + 1) & 31]);
+            const float p0 = c0 < nvk ? ex2(fmaf(x0, P.scale_log2, -m)) : 0.f;
+            const float p1 = c0 + 1 < nvk ? ex2(fmaf(x1, P.scale_log2, -m)) : 0.f;
+            lsum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tP + h * 32, pk);
+        }
+        l += lsum;
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&sm.p_full[pidx & 1]);
+        ++pidx;
+      }
+      if (!ok) break;
+      // epilogue: wait for the last PV, normalise, write the row
+      if (!W.wait(&sm.o_full, (pidx - 1) & 1, 13)) break;
+      fence_after();
+      const bool real = r < nvq;
+      const float inv = real ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          orow[c * 4 + q] = v;
+        }
+      }
+      P.lse[grow] = real ? (m + log2f(l)) * 0.69314718055994531f : 0.f;
+      fence_before();
+      mbar_arrive(&sm.work_empty[ws]);
+    }
+  }
+
+  // ---------------------------------------------------------- teardown ----
+  __syncthreads();
+  if (warp == 0) {
+    // every MMA this CTA issued has completed before the columns are freed
+    if (!wait_raw(&sm.final_bar, 0, P.limit) && lane == 0)
+      dev_error(P.status, DEV_ERR_TIMEOUT, 99, 0);
+    fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a [rows, 128] bf16 matrix, box 64 x 128 (128-byte rows),
+// 128-byte swizzle: one box is one half (64 channels) of a 128-row tile.
+bool make_tile_map(CUtensorMap* m, const void* base, long long rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kS)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                               const uint16_t* Vp, const int32_t* n_valid, const int32_t* row_ptr,
+                               const int32_t* col_idx, float scale, uint16_t* Op, float* lse,
+                               uint8_t* ws, cudaStream_t st) {
+  const prism_config_t& c = p.cfg;
+  const long long rows_total = static_cast<long long>(c.B) * c.H * p.sz.Np;
+  CUtensorMap tmK, tmV;
+  if (!make_tile_map(&tmK, Kp, rows_total) || !make_tile_map(&tmV, Vp, rows_total))
+    return cudaErrorInvalidValue;
+  FwdParams a;
+  a.Qp = Qp;
+  a.n_valid = n_valid;
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.Op = Op;
+  a.lse = lse;
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.rows = static_cast<long long>(c.B) * c.H * p.sz.nb;
+  a.Np = p.sz.Np;
+  a.nb = p.sz.nb;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
+  cudaError_t e = cudaMemsetAsync(a.status + WS_FWD_QUEUE, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  const size_t smem = 2ull * kStages * kTile + 1024;
+  e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long g = a.rows < sm_count() ? a.rows : sm_count();
+  attn_fwd_tc_kernel<<<static_cast<unsigned>(g), kFwdThreads, smem, st>>>(tmK, tmV, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd_tc(const Plan&, const uint16_t*, const uint16_t*, const uint16_t*,
                                const uint16_t*, const float*, const float*, const int32_t*,
                                const int32_t*, const int32_t*, float, float*, uint16_t*,
                                uint16_t*, uint8_t*, cudaStream_t) {
   return cudaErrorNotSupported;
 }
+
 }  // namespace prism

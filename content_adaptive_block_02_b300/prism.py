@@ -48,7 +48,7 @@ class Config(ctypes.Structure):
         ("alpha", ctypes.c_double), ("eps", ctypes.c_double),
         ("per_head", ctypes.c_int), ("use_video", ctypes.c_int), ("use_audio", ctypes.c_int),
         ("topk_floor", ctypes.c_int), ("topp", ctypes.c_float),
-        ("timeout_cycles", ctypes.c_ulonglong),
+        ("timeout_cycles", ctypes.c_ulonglong), ("attn_kernel", ctypes.c_int),
     ]
 
 
@@ -60,7 +60,7 @@ class Sizes(ctypes.Structure):
         ("N", ctypes.c_longlong), ("Np", ctypes.c_longlong),
         ("n_admissible", ctypes.c_int), ("admissible", ctypes.c_int * MAX_SHAPES),
         ("max_pairs", ctypes.c_longlong), ("ws_bytes", ctypes.c_size_t),
-        ("tensor_core_path", ctypes.c_int),
+        ("tensor_core_fwd", ctypes.c_int), ("tensor_core_bwd", ctypes.c_int),
     ]
 
 
@@ -132,7 +132,7 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def make_config(w, timeout_cycles: int = 0) -> Config:
+def make_config(w, timeout_cycles: int = 0, attn_kernel: int = 0) -> Config:
     """Config from a workload description (``synth.Workload``-like object)."""
     c = Config()
     c.B, c.H, c.d = w.B, w.H, w.d
@@ -150,15 +150,16 @@ def make_config(w, timeout_cycles: int = 0) -> Config:
     c.topk_floor = w.topk_floor
     c.topp = w.topp
     c.timeout_cycles = timeout_cycles
+    c.attn_kernel = attn_kernel
     return c
 
 
 class Plan:
     """Host plan of one problem size (prism_plan_create / prism_plan_query)."""
 
-    def __init__(self, w, timeout_cycles: int = 0):
+    def __init__(self, w, timeout_cycles: int = 0, attn_kernel: int = 0):
         self.w = w
-        self.cfg = make_config(w, timeout_cycles)
+        self.cfg = make_config(w, timeout_cycles, attn_kernel)
         h = ctypes.c_void_p()
         _check(lib().prism_plan_create(ctypes.byref(self.cfg), ctypes.byref(h)), "prism_plan_create")
         self.h = h
@@ -296,9 +297,9 @@ class PrismAttention:
     (dQ, dK, dV) in the same layout.  Buffers are allocated once per plan and
     reused across calls."""
 
-    def __init__(self, w, device="cuda"):
+    def __init__(self, w, device="cuda", attn_kernel: int = 0):
         self.w = w
-        self.plan = Plan(w)
+        self.plan = Plan(w, attn_kernel=attn_kernel)
         self.device = torch.device(device)
         self.scale = 1.0 / math.sqrt(w.d)
         self.ws = self.plan.ws(self.device)

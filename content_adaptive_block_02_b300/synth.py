@@ -104,7 +104,7 @@ MENU_128 = ((1, 8, 16), (1, 16, 8), (2, 8, 8), (4, 4, 8), (4, 8, 4), (2, 4, 16),
 
 # Block-mean field gain: chosen once so that the 720p-like grid at Top-p 0.9,
 # Top-k floor 8 lands in the 85-90 % block-sparsity band.
-GAMMA = 1.0
+GAMMA = 1.95
 
 WORKLOADS = {
     "tiny": Workload("tiny", B=1, H=2, d=64, T=4, Hg=8, W=8, zone=(2, 4, 4), block=16,

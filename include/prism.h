@@ -71,6 +71,9 @@ typedef struct prism_config {
   int topk_floor;         /* Top-k: minimum number of key blocks per query block    */
   float topp;             /* Top-p: cumulative block weight that must be exceeded   */
   unsigned long long timeout_cycles; /* bound on any device wait; 0 = default (~2 s) */
+  int attn_kernel;        /* 0: tensor-core (tcgen05) attention where supported
+                             (S = 128, d = 128), CUDA-core kernels otherwise;
+                             1: CUDA-core kernels always                         */
 } prism_config_t;
 
 /* Derived sizes of a plan. */
@@ -86,7 +89,8 @@ typedef struct prism_sizes {
   long long max_pairs;    /* capacity needed for col_idx / row_idx: B*H*nb*nb */
   size_t ws_bytes;        /* workspace bytes needed by prism_block_select,
                              prism_sparse_attn_fwd and prism_sparse_attn_bwd */
-  int tensor_core_path;   /* 1 when the attention runs on the tcgen05 kernels */
+  int tensor_core_fwd;    /* 1 when the forward attention runs on tcgen05 kernels */
+  int tensor_core_bwd;    /* 1 when the backward attention runs on tcgen05 kernels */
 } prism_sizes_t;
 
 typedef struct prism_plan prism_plan_t;

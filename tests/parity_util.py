@@ -31,10 +31,10 @@ def f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(w, inputs):
+def run_gpu(w, inputs, attn_kernel=0):
     dev = torch.device("cuda")
     x = {k: inputs[k].to(dev) for k in ("Q", "K", "V", "a2v", "dO")}
-    att = prism.PrismAttention(w, dev)
+    att = prism.PrismAttention(w, dev, attn_kernel=attn_kernel)
     O = att.forward(x["Q"], x["K"], x["V"], x["a2v"])
     dQ, dK, dV = att.backward(x["dO"])
     torch.cuda.synchronize()
@@ -67,12 +67,13 @@ def rel_err(a, b):
     return np.abs(a - b).max() / (den if den > 0 else 1.0)
 
 
-def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=None):
+def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=None,
+            attn_kernel=0):
     """Run both sides on the seeded inputs of `w`; assert the contract.
     heads / rows / key_blocks restrict the oracle's attention work (a sample
     of the (b, h), query blocks and key blocks)."""
     inputs = synth.generate(w, "cpu")
-    att, g = run_gpu(w, inputs)
+    att, g = run_gpu(w, inputs, attn_kernel)
     nb = att.plan.nb
     X = {k: f64(inputs[k]) for k in ("Q", "K", "V", "a2v", "dO")}
     rep = {} if report is None else report

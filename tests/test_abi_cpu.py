@@ -45,7 +45,10 @@ def test_plan_sizes_match_oracle_geometry(L, name):
 def test_2k_sizes_are_the_documented_ones(L):
     p = prism.Plan(synth.WORKLOADS["2k"])
     assert (p.sz.Np, p.sz.Z, p.sz.nb) == (322_560, 420, 2520)
-    assert p.sz.tensor_core_path in (0, 1)
+    assert p.sz.tensor_core_fwd == 1
+    p1 = prism.Plan(synth.WORKLOADS["2k"], attn_kernel=1)
+    assert p1.sz.tensor_core_fwd == 0 and p1.sz.tensor_core_bwd == 0
+    assert prism.Plan(synth.WORKLOADS["tiny"]).sz.tensor_core_fwd == 0
 
 
 def _err(w):

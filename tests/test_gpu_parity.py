@@ -54,3 +54,27 @@ def test_topp_one_is_dense_attention():
         ref = orc.dense_attention(X["Q"][0, :, h], X["K"][0, :, h], X["V"][0, :, h],
                                   1 / np.sqrt(w.d))
         assert pu.rel_err(pu.f64(g["O"])[0, :, h], ref) <= pu.O_TOL
+
+
+def _w128(**kw):
+    """6 x 40 x 48 grid (padded to 6 x 48 x 48), 3 x 16 x 16 zones, 128-token
+    blocks, d = 128: 108 blocks per head, several tiles and ragged padding."""
+    base = synth.WORKLOADS["720p"].with_(T=6, Hg=40, W=48, H=2, n_src=1, name="small128")
+    return base.with_(**kw)
+
+
+@pytest.mark.parametrize("attn_kernel", [0, 1])
+def test_128_blocks_both_kernels(attn_kernel):
+    rep = pu.compare(_w128(), attn_kernel=attn_kernel)
+    assert rep["O_max_rel"] <= pu.O_TOL
+
+
+def test_128_blocks_full_menu_zone():
+    """4 x 16 x 16 zones admit every shape of the 128-token menu."""
+    pu.compare(_w128(zone=(4, 16, 16), T=8))
+
+
+@pytest.mark.parametrize("kw", [dict(topp=0.5), dict(topp=0.99), dict(topk_floor=40),
+                                dict(topp=1.0)])
+def test_128_blocks_selection_settings(kw):
+    pu.compare(_w128(**kw))
