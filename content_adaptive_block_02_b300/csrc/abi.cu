@@ -126,7 +126,7 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   {
     const bool tc_shape = c.block_tokens == 128 && c.d == 128 && c.attn_kernel == 0;
     z.tensor_core_fwd = tc_shape ? 1 : 0;
-    z.tensor_core_bwd = 0;
+    z.tensor_core_bwd = tc_shape ? 1 : 0;
   }
   if (c.attn_kernel < 0 || c.attn_kernel > 1) return PRISM_ERR_ARG;
   for (int k = 0; k < PRISM_MAX_SHAPES; ++k)

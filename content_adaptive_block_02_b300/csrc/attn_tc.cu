@@ -64,14 +64,6 @@ struct FwdParams {
   unsigned long long limit;
 };
 
-__device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity,
-                                         unsigned long long limit) {
-  const unsigned long long t0 = clock64();
-  while (!mbar_try(bar, parity))
-    if (clock64() - t0 > limit) return false;
-  return true;
-}
-
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, FwdParams P) {
@@ -361,6 +353,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
@@ -399,8 +393,6 @@ int sm_count() {
   return n;
 }
 
-}  // namespace
-
 cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
                                const uint16_t* Vp, const int32_t* n_valid, const int32_t* row_ptr,
                                const int32_t* col_idx, float scale, uint16_t* Op, float* lse,
@@ -434,11 +426,20 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_tc(const Plan&, const uint16_t*, const uint16_t*, const uint16_t*,
-                               const uint16_t*, const float*, const float*, const int32_t*,
-                               const int32_t*, const int32_t*, float, float*, uint16_t*,
-                               uint16_t*, uint8_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t launch_attn_bwd_tc_impl(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                    const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                                    const float* D, const int32_t* n_valid,
+                                    const int32_t* col_ptr, const int32_t* row_idx, float scale,
+                                    float* dQacc, uint16_t* dKp, uint16_t* dVp, uint8_t* ws,
+                                    cudaStream_t st);
+
+cudaError_t launch_attn_bwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                               const float* D, const int32_t* n_valid, const int32_t* col_ptr,
+                               const int32_t* row_idx, float scale, float* dQacc, uint16_t* dKp,
+                               uint16_t* dVp, uint8_t* ws, cudaStream_t st) {
+  return launch_attn_bwd_tc_impl(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx, scale,
+                                 dQacc, dKp, dVp, ws, st);
 }
 
 }  // namespace prism

@@ -1,0 +1,496 @@
+// Block-sparse attention backward on the tcgen05 tensor cores, 128-token
+// blocks, head dim 128.
+//
+// Prism (arXiv 2610.05416) trains through its sparse attention (Table 2
+// caption: trainable methods replace video self-attention during training).
+// The backward is the softmax-attention VJP restricted to the selected
+// (query block, key block) pairs; the selection itself is a constant.
+//
+// Work item = one key block j of one (b, h) with the ascending list of query
+// blocks i that selected it (CSC).  For each i, five 128x128x128 products:
+//   (1) S^T  = K_j Q_i^T           A = K_j (smem),  B = Q_i (smem)   -> TMEM S
+//   (2) dP^T = V_j dO_i^T          A = V_j (smem),  B = dO_i (smem)  -> TMEM dP
+//       P^T = exp(S^T * scale - LSE_i)     (row = key, column = query)
+//       dS^T = P^T * (dP^T - D_i)
+//   (3) dV  += P^T dO_i            A = P^T (TMEM, written over S), B = dO_i (MN-major)
+//   (4) dK  += dS^T Q_i            A = dS^T (smem, K-major), B = Q_i (MN-major)
+//   (5) dQ_i = dS K_j              A = dS^T (smem, read MN-major), B = K_j (MN-major)
+//                                  -> TMEM, over dP once dP^T has been read
+// and the dQ_i tile is added to an fp32 accumulator with vector reductions.
+//
+// Roles (320 threads, one persistent CTA per SM):
+//   warps 0-3  compute: thread = key row = TMEM lane; P^T, dS^T, epilogue
+//              dK * scale, dV -> bf16.
+//   warps 4-7  dQ drain: thread = query row; TMEM -> registers -> red.add.v4.
+//   warp 8     producer: work counter, TMA loads of K_j, V_j (once per item)
+//              and of Q_i, dO_i, LSE_i, D_i (2-stage ring).
+//   warp 9     MMA issuer.  Tensor-pipe order per step i (steady state):
+//              4_i 5_i | 3_{i+1} | 2_{i+1} | 1_{i+2}
+//              so the P / dS work of the compute warps and the dQ drain both
+//              overlap tensor work.
+// Tensor memory: S/P [0,128), dP/dQ [128,256), dV [256,384), dK [384,512).
+#include "tc_common.cuh"
+
+namespace prism {
+namespace {
+using namespace tc;
+
+constexpr int kS = 128, kD = 128;
+constexpr int kTile = kS * kD * 2;           // 32 KB
+constexpr int kStage = 2 * kTile + 1024;     // Q, dO, LSE (512 B), D (512 B)
+constexpr int kThreads = 320;
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
+constexpr int kOffV = kTile, kOffStage = 2 * kTile, kOffDS = 2 * kTile + 2 * kStage;
+constexpr int kOffBar = kOffDS + kTile;
+
+struct BwdBars {
+  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready, ds_empty, dq_full, dq_drained;
+  uint64_t kv_done, kv_free, final_bar;
+  uint64_t work_full[2], work_empty[2];
+  int work_col[2], work_beg[2], work_end[2], work_nvk[2];
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kSmemBytes = kOffBar + sizeof(BwdBars);
+
+struct BwdParams {
+  const uint16_t* Qp;
+  const float* lse;
+  const float* D;
+  const int32_t* n_valid;
+  const int32_t* col_ptr;
+  const int32_t* row_idx;
+  float* dQacc;
+  uint16_t* dKp;
+  uint16_t* dVp;
+  uint32_t* status;
+  long long cols;  // B*H*nb work items
+  long long Np;
+  int nb;
+  float scale, scale_log2;
+  unsigned long long limit;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmdO, BwdParams P) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  BwdBars& sm = *reinterpret_cast<BwdBars*>(dsm + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(dsm) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) dev_error(P.status, DEV_ERR_BOUNDS, 0xA11, smem_u32(dsm));
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.qdo_full[s], 1);
+      mbar_init(&sm.qdo_empty[s], 1);
+      mbar_init(&sm.work_full[s], 1);
+      mbar_init(&sm.work_empty[s], 1 + 128 + 128);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.p_ready, 128);
+    mbar_init(&sm.ds_ready, 128);
+    mbar_init(&sm.ds_empty, 1);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_drained, 128);
+    mbar_init(&sm.kv_done, 1);
+    mbar_init(&sm.kv_free, 128);
+    mbar_init(&sm.final_bar, 1);
+    sm.abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const Waiter W{&sm.abort, P.status, P.limit};
+  uint8_t* kbuf = dsm;
+  uint8_t* vbuf = dsm + kOffV;
+  uint8_t* dsbuf = dsm + kOffDS;
+  auto stage = [&](int s) { return dsm + kOffStage + s * kStage; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------ producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      uint32_t use = 0, items = 0;
+      bool ok = true;
+      for (uint32_t it = 0; ok; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_empty[ws], ((it >> 1) & 1) ^ 1, 21)) break;
+        const long long col = atomicAdd(P.status + WS_BWD_QUEUE, 1u);
+        if (col >= P.cols) {
+          sm.work_col[ws] = -1;
+          mbar_arrive(&sm.work_full[ws]);
+          break;
+        }
+        const int beg = P.col_ptr[col], end = P.col_ptr[col + 1];
+        sm.work_col[ws] = static_cast<int>(col);
+        sm.work_beg[ws] = beg;
+        sm.work_end[ws] = end;
+        sm.work_nvk[ws] = P.n_valid[col];
+        mbar_arrive(&sm.work_full[ws]);
+        if (end == beg) continue;
+        const long long bh = col / P.nb;
+        const int j = static_cast<int>(col % P.nb);
+        const int yk = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
+        if (!W.wait(&sm.kv_empty, (items & 1) ^ 1, 22)) break;
+        ++items;
+        mbar_expect_tx(&sm.kv_full, 2 * kTile);
+        tma_load_2d(kbuf, &tmK, &sm.kv_full, 0, yk);
+        tma_load_2d(kbuf + kTile / 2, &tmK, &sm.kv_full, 64, yk);
+        tma_load_2d(vbuf, &tmV, &sm.kv_full, 0, yk);
+        tma_load_2d(vbuf + kTile / 2, &tmV, &sm.kv_full, 64, yk);
+        for (int t = beg; t < end; ++t) {
+          const int i = P.row_idx[t];
+          const long long yq = bh * P.Np + static_cast<long long>(i) * kS;
+          const int s = use & 1;
+          if (!W.wait(&sm.qdo_empty[s], ((use >> 1) & 1) ^ 1, 23)) { ok = false; break; }
+          uint8_t* st = stage(s);
+          mbar_expect_tx(&sm.qdo_full[s], 2 * kTile + 1024);
+          tma_load_2d(st, &tmQ, &sm.qdo_full[s], 0, static_cast<int>(yq));
+          tma_load_2d(st + kTile / 2, &tmQ, &sm.qdo_full[s], 64, static_cast<int>(yq));
+          tma_load_2d(st + kTile, &tmdO, &sm.qdo_full[s], 0, static_cast<int>(yq));
+          tma_load_2d(st + kTile + kTile / 2, &tmdO, &sm.qdo_full[s], 64, static_cast<int>(yq));
+          bulk_load(st + 2 * kTile, P.lse + yq, 512, &sm.qdo_full[s]);
+          bulk_load(st + 2 * kTile + 512, P.D + yq, 512, &sm.qdo_full[s]);
+          ++use;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------ MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // A K-major, B K-major
+      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // A K-major, B MN-major
+      constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // A MN-major, B MN-major
+      const uint32_t kb = smem_u32(kbuf), vb = smem_u32(vbuf), db = smem_u32(dsbuf);
+      uint32_t use = 0, items = 0, pcnt = 0, dscnt = 0, dqcnt = 0, kvcnt = 0;
+      bool ok = true;
+      // (1) and (2): K-major A (key rows) times K-major B (query rows)
+      auto mma_kt = [&](uint32_t a_base, uint32_t b_base, uint32_t d) {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile / 2) + (kk & 3) * 32;
+          mma_ss(tmem + d, sdesc_sw128(a_base + off, 16, 1024),
+                 sdesc_sw128(b_base + off, 16, 1024), id_kk, kk > 0 ? 1u : 0u);
+        }
+      };
+      for (uint32_t it = 0; ok; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 31)) break;
+        const int col = sm.work_col[ws];
+        if (col < 0) break;
+        const int n = sm.work_end[ws] - sm.work_beg[ws];
+        if (n > 0) {
+          if (!W.wait(&sm.kv_full, items & 1, 32)) break;
+          ++items;
+          // the previous item's dK / dV have been read out
+          if (kvcnt > 0 && !W.wait(&sm.kv_free, (kvcnt - 1) & 1, 33)) break;
+          fence_after();
+          const uint32_t u0 = use;
+          auto st_q = [&](uint32_t k) { return smem_u32(stage((u0 + k) & 1)); };
+          auto wait_qdo = [&](uint32_t k) {
+            return W.wait(&sm.qdo_full[(u0 + k) & 1], ((u0 + k) >> 1) & 1, 34);
+          };
+          // prologue: 1_0, 2_0, 3_0, 1_1
+          if (!wait_qdo(0)) break;
+          fence_after();
+          mma_kt(kb, st_q(0), TM_S);
+          commit(&sm.s_full);
+          // the dP region may still hold the previous item's last dQ tile
+          if (dqcnt > 0 && !W.wait(&sm.dq_drained, (dqcnt - 1) & 1, 35)) break;
+          fence_after();
+          mma_kt(vb, st_q(0) + kTile, TM_DP);
+          commit(&sm.dp_full);
+          auto issue_dv = [&](uint32_t k) -> bool {
+            if (!W.wait(&sm.p_ready, pcnt & 1, 36)) return false;
+            ++pcnt;
+            fence_after();
+            const uint32_t dob = st_q(k) + kTile;
+#pragma unroll
+            for (int kk = 0; kk < kS / 16; ++kk)
+              mma_ts(tmem + TM_DV, tmem + TM_S + kk * 8, sdesc_sw128(dob + kk * 2048, kTile / 2, 1024),
+                     id_kn, (k > 0 || kk > 0) ? 1u : 0u);
+            return true;
+          };
+          if (!issue_dv(0)) break;
+          if (n > 1) {
+            if (!wait_qdo(1)) break;
+            fence_after();
+            mma_kt(kb, st_q(1), TM_S);
+            commit(&sm.s_full);
+          }
+          for (int k = 0; k < n && ok; ++k) {
+            // 4_k, 5_k
+            if (!W.wait(&sm.ds_ready, dscnt & 1, 37)) { ok = false; break; }
+            ++dscnt;
+            fence_after();
+            const uint32_t qb = st_q(k);
+#pragma unroll
+            for (int kk = 0; kk < kS / 16; ++kk) {
+              const uint32_t aoff = (kk >> 2) * (kTile / 2) + (kk & 3) * 32;
+              mma_ss(tmem + TM_DK, sdesc_sw128(db + aoff, 16, 1024),
+                     sdesc_sw128(qb + kk * 2048, kTile / 2, 1024), id_kn, (k > 0 || kk > 0) ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kS / 16; ++kk)
+              mma_ss(tmem + TM_DP, sdesc_sw128(db + kk * 2048, kTile / 2, 1024),
+                     sdesc_sw128(kb + kk * 2048, kTile / 2, 1024), id_nn, kk > 0 ? 1u : 0u);
+            commit(&sm.dq_full);
+            commit(&sm.ds_empty);
+            commit(&sm.qdo_empty[(u0 + k) & 1]);
+            ++dqcnt;
+            if (k + 1 < n) {
+              if (!issue_dv(k + 1)) { ok = false; break; }
+              // 2_{k+1} once dQ_k has left the dP region
+              if (!W.wait(&sm.dq_drained, (dqcnt - 1) & 1, 38)) { ok = false; break; }
+              fence_after();
+              mma_kt(vb, st_q(k + 1) + kTile, TM_DP);
+              commit(&sm.dp_full);
+              if (k + 2 < n) {
+                if (!wait_qdo(k + 2)) { ok = false; break; }
+                fence_after();
+                mma_kt(kb, st_q(k + 2), TM_S);
+                commit(&sm.s_full);
+              }
+            }
+          }
+          if (!ok) break;
+          use = u0 + n;
+          commit(&sm.kv_done);
+          commit(&sm.kv_empty);
+          ++kvcnt;
+        }
+        mbar_arrive(&sm.work_empty[ws]);
+      }
+      commit(&sm.final_bar);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------ compute ----
+    const int r = threadIdx.x;  // key row == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t use = 0, scnt = 0, dpcnt = 0, dsidx = 0, kvcnt = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int ws = it & 1;
+      if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 41)) break;
+      const int col = sm.work_col[ws];
+      if (col < 0) break;
+      const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg, nvk = sm.work_nvk[ws];
+      const long long bh = col / P.nb;
+      const int j = static_cast<int>(col % P.nb);
+      const long long krow = bh * P.Np + static_cast<long long>(j) * kS + r;
+      uint4* dkrow = reinterpret_cast<uint4*>(P.dKp + krow * kD);
+      uint4* dvrow = reinterpret_cast<uint4*>(P.dVp + krow * kD);
+      if (n == 0) {
+#pragma unroll
+        for (int q = 0; q < kD / 8; ++q) dkrow[q] = dvrow[q] = make_uint4(0, 0, 0, 0);
+        mbar_arrive(&sm.work_empty[ws]);
+        continue;
+      }
+      bool ok = true;
+      for (int k = 0; k < n; ++k) {
+        const int i = P.row_idx[beg + k];
+        const int nvq = P.n_valid[bh * P.nb + i];
+        const float* lsed = reinterpret_cast<const float*>(stage((use + k) & 1) + 2 * kTile);
+        // LSE_i and D_i arrive with Q_i / dO_i on the stage's barrier
+        if (!W.wait(&sm.qdo_full[(use + k) & 1], ((use + k) >> 1) & 1, 40)) { ok = false; break; }
+        // ---- P^T = exp(S^T * scale - LSE) ----
+        if (!W.wait(&sm.s_full, scnt & 1, 42)) { ok = false; break; }
+        ++scnt;
+        fence_after();
+        float p[128];
+        {
+          uint32_t s[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + TM_S + c * 32, s[c]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int q = c * 32 + e;
+              const float x = fmaf(__uint_as_float(s[c][e]), P.scale_log2,
+                                   -lsed[q] * 1.4426950408889634f);
+              p[q] = (r < nvk && q < nvq) ? ex2(x) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[h * 64 + 2 * e], p[h * 64 + 2 * e + 1]);
+          tmem_st32(tmem + lb + TM_S + h * 32, pk);
+        }
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&sm.p_ready);
+        // ---- dS^T = P^T * (dP^T - D) -> smem (128-byte swizzled, K-major) ----
+        if (!W.wait(&sm.dp_full, dpcnt & 1, 43)) { ok = false; break; }
+        ++dpcnt;
+        if (dsidx > 0 && !W.wait(&sm.ds_empty, (dsidx - 1) & 1, 44)) { ok = false; break; }
+        ++dsidx;
+        fence_after();
+        const float* Dv = lsed + 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dp[32];
+          tmem_ld32(tmem + lb + TM_DP + c * 32, dp);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
+            const int q0 = c * 32 + g * 8;
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int qa = q0 + 2 * e, qb2 = qa + 1;
+              const float da = p[qa] * (__uint_as_float(dp[g * 8 + 2 * e]) - Dv[qa]);
+              const float db = p[qb2] * (__uint_as_float(dp[g * 8 + 2 * e + 1]) - Dv[qb2]);
+              w4[e] = pack_bf16x2(da, db);
+            }
+            const int panel = q0 >> 6, chunk = (q0 & 63) >> 3;
+            const uint32_t off = panel * (kTile / 2) + r * 128 + ((chunk ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        fence_proxy_async();
+        fence_before();
+        mbar_arrive(&sm.ds_ready);
+      }
+      if (!ok) break;
+      use += n;
+      // ---- epilogue: dV, dK * scale -> bf16 rows ----
+      if (!W.wait(&sm.kv_done, kvcnt & 1, 45)) break;
+      ++kvcnt;
+      fence_after();
+      const bool real = r < nvk;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        uint4* dst = which ? dkrow : dvrow;
+        const float mul = real ? (which ? P.scale : 1.f) : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lb + (which ? TM_DK : TM_DV) + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * mul, __uint_as_float(o[8 * q + 1]) * mul);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * mul, __uint_as_float(o[8 * q + 3]) * mul);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * mul, __uint_as_float(o[8 * q + 5]) * mul);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * mul, __uint_as_float(o[8 * q + 7]) * mul);
+            dst[c * 4 + q] = v;
+          }
+        }
+      }
+      fence_before();
+      mbar_arrive(&sm.kv_free);
+      mbar_arrive(&sm.work_empty[ws]);
+    }
+  } else {
+    // ------------------------------------------------------ dQ drain ----
+    const int q = threadIdx.x - 128;  // query row == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    uint32_t dqcnt = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int ws = it & 1;
+      if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 51)) break;
+      const int col = sm.work_col[ws];
+      if (col < 0) break;
+      const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg;
+      const long long bh = col / P.nb;
+      bool ok = true;
+      for (int k = 0; k < n; ++k) {
+        const int i = P.row_idx[beg + k];
+        const int nvq = P.n_valid[bh * P.nb + i];
+        if (!W.wait(&sm.dq_full, dqcnt & 1, 52)) { ok = false; break; }
+        ++dqcnt;
+        fence_after();
+        uint32_t v[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + TM_DP + c * 32, v[c]);
+        tmem_ld_wait();
+        fence_before();
+        mbar_arrive(&sm.dq_drained);
+        if (q < nvq) {
+          float* dst = P.dQacc + (bh * P.Np + static_cast<long long>(i) * kS + q) * kD;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add_v4(dst + c * 32 + e, __uint_as_float(v[c][e]), __uint_as_float(v[c][e + 1]),
+                         __uint_as_float(v[c][e + 2]), __uint_as_float(v[c][e + 3]));
+        }
+      }
+      if (!ok) break;
+      mbar_arrive(&sm.work_empty[ws]);
+    }
+  }
+
+  // ---------------------------------------------------------- teardown ----
+  __syncthreads();
+  if (warp == 0) {
+    if (!wait_raw(&sm.final_bar, 0, P.limit) && lane == 0)
+      dev_error(P.status, DEV_ERR_TIMEOUT, 199, 0);
+    fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc_impl(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                    const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                                    const float* D, const int32_t* n_valid,
+                                    const int32_t* col_ptr, const int32_t* row_idx, float scale,
+                                    float* dQacc, uint16_t* dKp, uint16_t* dVp, uint8_t* ws,
+                                    cudaStream_t st) {
+  const prism_config_t& c = p.cfg;
+  const long long rows_total = static_cast<long long>(c.B) * c.H * p.sz.Np;
+  CUtensorMap tmQ, tmK, tmV, tmdO;
+  if (!make_tile_map(&tmQ, Qp, rows_total) || !make_tile_map(&tmK, Kp, rows_total) ||
+      !make_tile_map(&tmV, Vp, rows_total) || !make_tile_map(&tmdO, dOp, rows_total))
+    return cudaErrorInvalidValue;
+  BwdParams a;
+  a.Qp = Qp;
+  a.lse = lse;
+  a.D = D;
+  a.n_valid = n_valid;
+  a.col_ptr = col_ptr;
+  a.row_idx = row_idx;
+  a.dQacc = dQacc;
+  a.dKp = dKp;
+  a.dVp = dVp;
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.cols = static_cast<long long>(c.B) * c.H * p.sz.nb;
+  a.Np = p.sz.Np;
+  a.nb = p.sz.nb;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
+  cudaError_t e = cudaMemsetAsync(a.status + WS_BWD_QUEUE, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const long long g = a.cols < sm_count() ? a.cols : sm_count();
+  attn_bwd_tc_kernel<<<static_cast<unsigned>(g), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO,
+                                                                            a);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

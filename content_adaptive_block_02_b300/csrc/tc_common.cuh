@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "prism_internal.cuh"
@@ -183,5 +184,42 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity,
+                                         unsigned long long limit) {
+  const unsigned long long t0 = clock64();
+  while (!mbar_try(bar, parity))
+    if (clock64() - t0 > limit) return false;
+  return true;
+}
+
+// 1-D bulk copy global -> shared, completing on an mbarrier (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (TMA, tcgen05.mma) before a barrier hands them over.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 }  // namespace tc
+
+// Host helpers shared by the tensor-core launchers.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
+bool make_tile_map(CUtensorMap* m, const void* base, long long rows);
+int sm_count();
+
 }  // namespace prism
