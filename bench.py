@@ -1,0 +1,373 @@
+"""Benchmark of the Prism block-sparse attention hot path (forward + backward).
+
+One step = the whole path on one batch of the seeded synthetic 2K-like grid
+(21 x 90 x 160 latent tokens, 24 heads, d = 128, bf16, 3 x 16 x 16 zones,
+128-token blocks, Top-k floor 8, Top-p 0.9), every stage through the C ABI:
+zone statistics -> shapes + permutation + pooling -> block selection ->
+sparse attention forward -> inverse permutation of O -> permutation of dO ->
+sparse attention backward -> inverse permutation of dQ, dK, dV.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`value` is effective TFLOP/s: the attention flops of the selected
+(query block, key block) pairs, 4 S^2 d forward + 10 S^2 d backward per pair,
+divided by the whole step time.  Multi-GPU runs are independent replicas
+(every head of every batch is independent; no data-path collective).
+`--impl reference` times the CPU oracle (fp64 numpy) on a bounded sample of
+the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from content_adaptive_block_02_b300 import build, prism, synth  # noqa: E402
+
+METRIC = "sparse-attn fwd+bwd ms & effective TFLOP/s at 2K grid; % of bf16 tensor peak"
+FWD_PAIR_FLOP = 4 * 128 * 128 * 128          # S = QK^T and O = PV per 128x128 pair
+BWD_PAIR_FLOP = 10 * 128 * 128 * 128         # S, dP, dV, dK, dQ
+KERNELS_PER_STEP = 22
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(bf16=m["bf16_tflops"], bf16_sus=m["bf16_tflops_sustained"],
+                    hbm=m["hbm_gbs"], src="measured")
+    except Exception:
+        return dict(bf16=1800.0, bf16_sus=1400.0, hbm=6400.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.idx = dev_index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "out", "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- ours ----
+
+def run_ours(args, w):
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    build.build()
+    wr = w.with_(seed_base=w.seed_base + 100 * rank)     # an independent problem per replica
+    x = synth.generate(wr, dev)
+    att = prism.PrismAttention(wr, dev)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(tk=None):
+        att.plan.zone_stats(x["V"], x["a2v"], att.stats)
+        att.plan.assign_and_permute(att.stats, x["Q"], x["K"], x["V"], att.perm_out)
+        o = att.perm_out
+        att.plan.block_select(o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"], o["n_valid"],
+                              att.ws, att.lists)
+        if tk is not None:
+            tk[0].record(stream)
+        att.plan.sparse_attn_fwd(o["Qp"], o["Kp"], o["Vp"], o["n_valid"], att.lists["row_ptr"],
+                                 att.lists["col_idx"], att.scale, att.ws, att.Op, att.lse)
+        if tk is not None:
+            tk[1].record(stream)
+        att.plan.unpermute(o["inv"], att.Op, att.O)
+        att.plan.permute(o["perm"], x["dO"], att.dOp)
+        if tk is not None:
+            tk[2].record(stream)
+        att.plan.sparse_attn_bwd(o["Qp"], o["Kp"], o["Vp"], att.Op, att.dOp, att.lse, o["n_valid"],
+                                 att.lists, att.scale, att.ws, att.dQp, att.dKp, att.dVp)
+        if tk is not None:
+            tk[3].record(stream)
+        att.plan.unpermute(o["inv"], att.dQp, att.dQ)
+        att.plan.unpermute(o["inv"], att.dKp, att.dK)
+        att.plan.unpermute(o["inv"], att.dVp, att.dV)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = att.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    pairs = int(att.lists["row_ptr"][-1].item())
+    amb = int(att.ws[4:8].view(torch.int32).item())
+    flop = pairs * (FWD_PAIR_FLOP + BWD_PAIR_FLOP)
+
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    marks = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = ev(), ev()
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for k in range(args.steps):
+            step(marks[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    fwd_ms = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
+    bwd_ms = statistics.mean(m[2].elapsed_time(m[3]) for m in marks)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        f = torch.tensor([float(flop)], device=dev)
+        torch.distributed.all_reduce(f)
+        flop_all = float(f.item())
+    else:
+        flop_all = float(flop)
+    st = att.status()
+
+    # ---- end to end through host buffers (pinned), H2D inputs, D2H outputs ----
+    names_in = ["Q", "K", "V", "a2v", "dO"]
+    host_in = {k: x[k].cpu().pin_memory() for k in names_in}
+    host_out = {k: torch.empty(x["Q"].shape, dtype=torch.bfloat16).pin_memory()
+                for k in ("O", "dQ", "dK", "dV")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e_steps = max(1, min(args.steps, 3))
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e_steps):
+        for k in names_in:
+            x[k].copy_(host_in[k], non_blocking=True)
+        step()
+        for k, src in (("O", att.O), ("dQ", att.dQ), ("dK", att.dK), ("dV", att.dV)):
+            host_out[k].copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    if ws > 1:
+        t = torch.tensor([e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(t.item())
+
+    pk = peaks()
+    bwd_achieved = pairs * BWD_PAIR_FLOP / (bwd_ms * 1e-3) / 1e12
+    fwd_achieved = pairs * FWD_PAIR_FLOP / (fwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(flop_all / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.T}x{w.Hg}x{w.W} grid, {w.H} heads, d={w.d}, "
+                               f"zones {w.zone}, {w.block}-token blocks, top-k {w.topk_floor}, "
+                               f"top-p {w.topp}",
+                   "global_batch": w.B * ws, "tokens": w.N, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "selected_pairs": pairs,
+                   "block_density": round(pairs / (w.B * w.H * w.n_blocks ** 2), 4),
+                   "rows_decided_exactly": amb},
+        "attn_ms": {"fwd": round(fwd_ms, 3), "bwd": round(bwd_ms, 3),
+                    "other": round(ms - fwd_ms - bwd_ms, 3)},
+        "attn_tflops": {"fwd": round(fwd_achieved, 1), "bwd": round(bwd_achieved, 1)},
+        "dense_equiv_tflops": round(w.B * w.H * (w.n_blocks ** 2) *
+                                    (FWD_PAIR_FLOP + BWD_PAIR_FLOP) / (ms * 1e-3) / 1e12 * ws, 1),
+        "roofline": {"bound": "tensor", "kernel": "attn_bwd_tc (events around prism_sparse_attn_bwd)",
+                     "achieved": round(bwd_achieved, 1), "peak": pk["bf16_sus"],
+                     "peak_kind": f"bf16 sustained ({pk['src']})", "unit": "TFLOP/s",
+                     "frac": round(bwd_achieved / pk["bf16_sus"], 4),
+                     "frac_burst": round(bwd_achieved / pk["bf16"], 4), "traffic": None},
+        "e2e": {"value": round(flop_all / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+        "device_status": st,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return line if rank == 0 else None
+
+
+# ------------------------------------------------------------ oracle leg ----
+
+def _threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, inputs_f64, rows_sample=8, head=0):
+    """Time the fp64 oracle on one head (statistics, shapes, permutation,
+    pooling, selection) and on `rows_sample` query blocks of attention
+    forward + backward; extrapolate to the whole workload.  Returns
+    (seconds for the whole workload, pair flop of the whole workload,
+    description)."""
+    from oracle import prism_oracle as orc
+    X = inputs_f64
+    w1 = w.with_(H=1)
+    t0 = time.perf_counter()
+    st = orc.zone_stats(w1, X["V"], X["a2v"])
+    sid, _ = orc.assign_shapes(w1, st)
+    perm, inv, nval = orc.build_permutation(w1, sid)
+    Qp, Kp, Vp = orc.permute(X["Q"], perm), orc.permute(X["K"], perm), orc.permute(X["V"], perm)
+    Qb, Kb = orc.pool(Qp, nval, w.block), orc.pool(Kp, nval, w.block)
+    lists, _ = orc.select_blocks(w1, Qb, Kb, nval)
+    t1 = time.perf_counter()
+    L = lists[(0, 0)]
+    pairs_head = sum(len(s) for s in L if s is not None)
+    rng = np.random.default_rng(0)
+    cand = [i for i in range(len(L)) if L[i] is not None and len(L[i]) > 0]
+    rows = rng.choice(cand, size=min(rows_sample, len(cand)), replace=False)
+    dOp = orc.permute(X["dO"], perm)
+    scale = 1.0 / math.sqrt(w.d)
+    t2 = time.perf_counter()
+    sp = 0
+    for i in rows:
+        orc.attn_fwd_row(Qp[0, 0], Kp[0, 0], Vp[0, 0], nval[0, 0], int(i), L[i], w.block, scale)
+        orc.attn_bwd_row(Qp[0, 0], Kp[0, 0], Vp[0, 0], dOp[0, 0], nval[0, 0], int(i), L[i],
+                         w.block, scale)
+        sp += len(L[i])
+    t3 = time.perf_counter()
+    per_pair = (t3 - t2) / max(sp, 1)
+    pairs_all = pairs_head * w.H * w.B
+    total = (t1 - t0) * w.H * w.B + per_pair * pairs_all
+    desc = (f"oracle on head {head}: steps 1-4 timed in full ({t1 - t0:.1f} s, x{w.H * w.B} heads); "
+            f"attention fwd+bwd timed on {len(rows)} query blocks ({sp} pairs, {t3 - t2:.1f} s), "
+            f"extrapolated per pair to the oracle's {pairs_all} pairs")
+    return total, pairs_all * (FWD_PAIR_FLOP + BWD_PAIR_FLOP), desc, (t3 - t0)
+
+
+def _head_inputs(x, head=0):
+    f = lambda t: t.detach().float().cpu().numpy().astype(np.float64)
+    return {"Q": f(x["Q"][:, :, head:head + 1]), "K": f(x["K"][:, :, head:head + 1]),
+            "V": f(x["V"][:, :, head:head + 1]), "dO": f(x["dO"][:, :, head:head + 1]),
+            "a2v": f(x["a2v"])}
+
+
+def cpu_baseline(w, x):
+    X = _head_inputs(x)
+    total, flop, desc, spent = oracle_sample(w, X)
+    return {"value": round(flop / total / 1e12, 6), "unit": "TFLOP/s", "cores": _threads(),
+            "kind": "oracle", "sample": desc, "seconds_spent": round(spent, 1),
+            "extrapolated_s_per_step": round(total, 1)}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    x = synth.generate(w, "cpu")
+    X = _head_inputs(x)
+    for _ in range(args.warmup):
+        oracle_sample(w, X, rows_sample=2)
+    vals, descs, spent = [], [], 0.0
+    for _ in range(args.steps):
+        total, flop, desc, s = oracle_sample(w, X, rows_sample=2)
+        vals.append(total)
+        descs.append(desc)
+        spent += s
+    total = statistics.mean(vals)
+    v = flop / total / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.T}x{w.Hg}x{w.W} grid, {w.H} heads, d={w.d}",
+                       "global_batch": w.B, "tokens": w.N},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": _threads(),
+                             "kind": "oracle", "sample": descs[-1]},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "seconds_spent": round(spent, 1)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="2k", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

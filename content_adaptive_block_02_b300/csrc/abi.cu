@@ -142,9 +142,8 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   p.off_rowcnt = off; off = align256(off + rows * 4);
   p.off_colcnt = off; off = align256(off + rows * 4);
   p.off_amb = off; off = align256(off + rows * 4);
-  p.off_qn = off; off = align256(off + 2 * rows * 4);
   p.off_bitmask = off; off = align256(off + rows * nwords * 4);
-  p.off_scores = off; off = align256(off + rows * nb * 4);
+  p.off_scores = off; off = align256(off + 2 * rows * nb * 4);
   p.off_D = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
   p.off_dq = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * c.d * 4);
   z.ws_bytes = off;

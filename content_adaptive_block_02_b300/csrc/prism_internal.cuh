@@ -18,7 +18,7 @@ struct Plan {
   double log2_ext[PRISM_MAX_SHAPES][3];  // log2 of every menu extent
   double log2_S;
   // workspace offsets (bytes), each region 256-aligned
-  size_t off_rowcnt, off_colcnt, off_amb, off_qn, off_bitmask, off_scores, off_D, off_dq;
+  size_t off_rowcnt, off_colcnt, off_amb, off_bitmask, off_scores, off_D, off_dq;
 };
 
 // Workspace layout (bytes from the start of ws, each region 256-aligned):
@@ -26,9 +26,8 @@ struct Plan {
 //   off_rowcnt      int32 [B*H*nb]       selected key blocks per query block
 //   off_colcnt      int32 [B*H*nb]       query blocks that selected each key block
 //   off_amb         int32 [B*H*nb]       rows whose fp32 decision was ambiguous
-//   off_qn          fp32  [2*B*H*nb]     norms of the block means (Q then K)
 //   off_bitmask     u32   [B*H*nb*nw]    selection bitmask, nw = ceil(nb/32)
-//   off_scores      fp32  [B*H*nb*nb]    fp32 block scores (unscaled dots)
+//   off_scores      fp32  [2*B*H*nb*nb]  block scores (unscaled dots), hi then lo
 //   off_D           fp32  [B*H*Np]       rowsum(dO * O) for the backward
 //   off_dq          fp32  [B*H*Np*d]     dQ accumulator for the backward
 enum : int {

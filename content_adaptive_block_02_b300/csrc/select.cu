@@ -12,14 +12,16 @@
 // where m_p is the smallest prefix whose weight is strictly above p (all
 // candidates when none is, or when p >= 1).
 //
-// Precision.  The block lists must not depend on rounding, so the decision is
-// certified: the fast path computes fp32 scores (tiled SGEMM) and runs the
-// selection on them, together with a rigorous bound delta on the score error
-// ((d + 5) u ||q|| ||k_max|| / sqrt(d), u = 2^-24).  A row whose decision sits
-// within that bound of a boundary (score gap at the cut, or cumulative mass
-// near p) is re-done from the double-float block means (hi + lo fp32 pairs)
-// with compensated (Dot2, Ogita-Rump-Oishi 2005) scores accurate to ~1e-13, a
-// full sort and an fp64 cumulative sum -- the same decision as an fp64 reading.
+// Precision.  The block lists must not depend on rounding.  Scores are
+// computed for every pair in double-float arithmetic (hi + lo fp32 pairs,
+// compensated dot product Dot2 of Ogita, Rump and Oishi, SIAM J. Sci. Comput.
+// 2005) from the double-float block means, which puts their error near 1e-9.
+// The selection then runs on those scores with fp32 weights exp(s - max)
+// (CUDA expf, 2 ulp) and compensated sums, so every cumulative weight carries
+// an error below 4e-7.  A query block whose decision lies within 1e-6 of a
+// boundary (cumulative weight near p, or a score gap at the cut) is decided
+// again by an exact pass: full sort of the double-float scores and fp64
+// weights and running sums.
 #include <float.h>
 
 #include "prism_internal.cuh"
@@ -37,82 +39,85 @@ __device__ __forceinline__ float fkey_inv(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// ------------------------------------------------------------- norms -------
-__global__ void norms_kernel(long long rows, int d, const float* __restrict__ Qb,
-                             const float* __restrict__ Kb, float* __restrict__ qn,
-                             float* __restrict__ kn) {
-  const int lane = threadIdx.x & 31;
-  const long long w = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
-  if (w >= 2 * rows) return;
-  const float* src = w < rows ? Qb + w * d : Kb + (w - rows) * d;
-  float s = 0.f;
-  for (int c = lane; c < d; c += 32) s = fmaf(src[c], src[c], s);
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) {
-    // round the norm up a little so that it bounds the exact norm
-    const float r = sqrtf(s) * (1.f + 1e-6f);
-    if (w < rows) qn[w] = r; else kn[w - rows] = r;
-  }
-}
+// ------------------------------------------------ Dot2 score GEMM ---------
+// S[bh][i][j] = Qbar_i . Kbar_j (unscaled) in double-float: for every term the
+// product hi*hi is split exactly (TwoProduct by FMA), the cross terms
+// hi*lo + lo*hi are added in fp32, and the running sum is kept as an
+// unevaluated pair with TwoSum.  Tile 64 (i) x 128 (j) per CTA, 256 threads
+// with a 4 x 8 register tile, channels staged 16 at a time (transposed).
+constexpr int kTI = 64, kTJ = 128, kBK = 16;
 
-// ---------------------------------------------------- score SGEMM ----------
-// S[bh][i][j] = sum_c Q[bh][i][c] * K[bh][j][c] in fp32 (ragged edges zero
-// filled).  128 x 128 tile per CTA, 256 threads with an 8 x 8 register tile
-// each, K-dimension staged 16 channels at a time (transposed in smem).
-constexpr int kTile = 128, kBK = 16;
-
-__global__ void __launch_bounds__(256) score_gemm_kernel(int nb, int d,
-                                                         const float* __restrict__ Qb,
-                                                         const float* __restrict__ Kb,
-                                                         float* __restrict__ S) {
-  __shared__ __align__(16) float As[kBK][kTile + 4];
-  __shared__ __align__(16) float Bs[kBK][kTile + 4];
+__global__ void __launch_bounds__(256) score_dot2_kernel(int nb, int d,
+                                                         const float* __restrict__ Qh,
+                                                         const float* __restrict__ Ql,
+                                                         const float* __restrict__ Kh,
+                                                         const float* __restrict__ Kl,
+                                                         float* __restrict__ Shi,
+                                                         float* __restrict__ Slo) {
+  __shared__ __align__(16) float Ah[kBK][kTI + 4], Al[kBK][kTI + 4];
+  __shared__ __align__(16) float Bh[kBK][kTJ + 4], Bl[kBK][kTJ + 4];
   const int bh = blockIdx.z;
-  const int i0 = blockIdx.y * kTile, j0 = blockIdx.x * kTile;
-  const float* A = Qb + static_cast<long long>(bh) * nb * d;
-  const float* B = Kb + static_cast<long long>(bh) * nb * d;
+  const int i0 = blockIdx.y * kTI, j0 = blockIdx.x * kTJ;
+  const long long ob = static_cast<long long>(bh) * nb * d;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[8][8];
+  float sh[4][8], sc[4][8];
 #pragma unroll
-  for (int a = 0; a < 8; ++a)
+  for (int a = 0; a < 4; ++a)
 #pragma unroll
-    for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+    for (int b = 0; b < 8; ++b) sh[a][b] = sc[a][b] = 0.f;
   for (int c0 = 0; c0 < d; c0 += kBK) {
-    // 128 rows x 16 channels per operand = 2048 floats, 8 per thread
-    for (int e = threadIdx.x; e < kTile * kBK; e += 256) {
-      const int r = e / kBK, cc = e % kBK;
-      const int gi = i0 + r, gj = j0 + r, c = c0 + cc;
-      As[cc][r] = (gi < nb && c < d) ? A[static_cast<long long>(gi) * d + c] : 0.f;
-      Bs[cc][r] = (gj < nb && c < d) ? B[static_cast<long long>(gj) * d + c] : 0.f;
+    for (int e = threadIdx.x; e < kTI * kBK; e += 256) {
+      const int r = e / kBK, cc = e % kBK, gi = i0 + r;
+      const bool ok = gi < nb;
+      const long long o = ob + static_cast<long long>(gi) * d + c0 + cc;
+      Ah[cc][r] = ok ? Qh[o] : 0.f;
+      Al[cc][r] = ok ? Ql[o] : 0.f;
+    }
+    for (int e = threadIdx.x; e < kTJ * kBK; e += 256) {
+      const int r = e / kBK, cc = e % kBK, gj = j0 + r;
+      const bool ok = gj < nb;
+      const long long o = ob + static_cast<long long>(gj) * d + c0 + cc;
+      Bh[cc][r] = ok ? Kh[o] : 0.f;
+      Bl[cc][r] = ok ? Kl[o] : 0.f;
     }
     __syncthreads();
-#pragma unroll
+#pragma unroll 4
     for (int cc = 0; cc < kBK; ++cc) {
-      float a[8], b[8];
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[cc][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[cc][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cc][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cc][64 + tx * 4]);
-      a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-      a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
-      b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
-      b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+      const float4 ah4 = *reinterpret_cast<const float4*>(&Ah[cc][ty * 4]);
+      const float4 al4 = *reinterpret_cast<const float4*>(&Al[cc][ty * 4]);
+      const float4 bh0 = *reinterpret_cast<const float4*>(&Bh[cc][tx * 4]);
+      const float4 bh1 = *reinterpret_cast<const float4*>(&Bh[cc][64 + tx * 4]);
+      const float4 bl0 = *reinterpret_cast<const float4*>(&Bl[cc][tx * 4]);
+      const float4 bl1 = *reinterpret_cast<const float4*>(&Bl[cc][64 + tx * 4]);
+      const float ah[4] = {ah4.x, ah4.y, ah4.z, ah4.w}, al[4] = {al4.x, al4.y, al4.z, al4.w};
+      const float bhv[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
+      const float blv[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
 #pragma unroll
-      for (int x = 0; x < 8; ++x)
+      for (int x = 0; x < 4; ++x)
 #pragma unroll
-        for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(a[x], b[y], acc[x][y]);
+        for (int y = 0; y < 8; ++y) {
+          const float p = __fmul_rn(ah[x], bhv[y]);
+          const float pe = fmaf(ah[x], bhv[y], -p);
+          const float cross = fmaf(ah[x], blv[y], __fmul_rn(al[x], bhv[y]));
+          const df t = two_sum(sh[x][y], p);
+          sh[x][y] = t.hi;
+          sc[x][y] = __fadd_rn(sc[x][y], __fadd_rn(t.lo, __fadd_rn(pe, cross)));
+        }
     }
     __syncthreads();
   }
-  float* out = S + static_cast<long long>(bh) * nb * nb;
+  const long long os = static_cast<long long>(bh) * nb * nb;
 #pragma unroll
-  for (int x = 0; x < 8; ++x) {
-    const int gi = i0 + (x < 4 ? ty * 4 + x : 64 + ty * 4 + x - 4);
+  for (int x = 0; x < 4; ++x) {
+    const int gi = i0 + ty * 4 + x;
     if (gi >= nb) continue;
 #pragma unroll
     for (int y = 0; y < 8; ++y) {
       const int gj = j0 + (y < 4 ? tx * 4 + y : 64 + tx * 4 + y - 4);
-      if (gj < nb) out[static_cast<long long>(gi) * nb + gj] = acc[x][y];
+      if (gj >= nb) continue;
+      const df r = fast_two_sum(sh[x][y], sc[x][y]);
+      Shi[os + static_cast<long long>(gi) * nb + gj] = r.hi;
+      Slo[os + static_cast<long long>(gi) * nb + gj] = r.lo;
     }
   }
 }
@@ -121,13 +126,13 @@ __global__ void __launch_bounds__(256) score_gemm_kernel(int nb, int d,
 constexpr int kEPL = 40;  // score elements held per lane
 
 struct SelParams {
-  int nb, nwords, d, topk;
+  int nb, nwords, topk;
   long long rows;  // B*H*nb
-  float topp, inv_sqrt_d, u_scale;
-  const float* S;
+  float topp;
+  df inv_sqrt_d;
+  const float* Shi;
+  const float* Slo;
   const int32_t* n_valid;
-  const float* qn;
-  const float* kn;
   uint32_t* bitmask;
   int32_t* rowcnt;
   uint8_t* tie;
@@ -140,7 +145,7 @@ struct SelParams {
 template <int R>
 struct Group {
   int grp, wig, lane;
-  float* scratch;  // [R * 4] floats (viewed as any 32-bit type)
+  float* scratch;  // 4 slots of R 32-bit words (a double-float uses two slots)
   int slot;
   __device__ __forceinline__ void sync() const {
     if (R > 1) asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(R * 32) : "memory");
@@ -165,11 +170,10 @@ struct Group {
       df w;
       w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
       w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
-      // combine in a fixed lane-independent order: lower lane first
-      v = (lane & o) ? df_add(w, v) : df_add(v, w);
+      v = (lane & o) ? df_add(w, v) : df_add(v, w);  // lower lane first: deterministic
     }
     if (R == 1) return v;
-    float* s = scratch + slot * R * 2;  // uses two slots
+    float* s = scratch + slot * R;  // slots slot and slot+1
     if (lane == 0) {
       s[2 * wig] = v.hi;
       s[2 * wig + 1] = v.lo;
@@ -183,9 +187,14 @@ struct Group {
   }
 };
 
+constexpr float kBand = 1e-6f;    // decision margin on cumulative weights
+constexpr float kGapAbs = 1e-7f;  // decision margin on the score gap at the cut
+
+// One row group (R warps) per query block.  Lane l of warp w holds the
+// candidates j = w*32 + l + k*R*32, k < kEPL.
 template <int R>
 __global__ void __launch_bounds__(256) select_fast_kernel(SelParams P) {
-  __shared__ float scratch_all[8][4 * 8 * 2];
+  __shared__ float scratch_all[8][4 * 8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_per_cta = (blockDim.x >> 5) / R;
   Group<R> G;
@@ -199,8 +208,7 @@ __global__ void __launch_bounds__(256) select_fast_kernel(SelParams P) {
   const long long bh = row / P.nb;
   const int nb = P.nb;
   uint32_t* bm = P.bitmask + row * P.nwords;
-  const int nv_i = P.n_valid[row];
-  if (nv_i == 0) {
+  if (P.n_valid[row] == 0) {
     for (int w = G.wig * 32 + lane; w < P.nwords; w += R * 32) bm[w] = 0u;
     if (G.wig == 0 && lane == 0) {
       P.rowcnt[row] = 0;
@@ -208,50 +216,51 @@ __global__ void __launch_bounds__(256) select_fast_kernel(SelParams P) {
     }
     return;
   }
-  // ---- load the row: key (0 = not a candidate), value, weight ----
-  const float* srow = P.S + row * nb;
+  // ---- the row: key of the hi part (0 = not a candidate), scaled scores ----
+  const float* shr = P.Shi + row * nb;
+  const float* slr = P.Slo + row * nb;
   const int32_t* nvk = P.n_valid + bh * nb;
-  const float* knr = P.kn + bh * nb;
   uint32_t key[kEPL];
-  float e[kEPL];
-  float mx = -FLT_MAX, kmax = 0.f;
+  float sl[kEPL];  // lo part of the scaled score, later the weight
+  float mx = -FLT_MAX;
   int ncand = 0;
 #pragma unroll
   for (int k = 0; k < kEPL; ++k) {
     const int j = G.wig * 32 + lane + k * R * 32;
     key[k] = 0u;
-    e[k] = 0.f;
+    sl[k] = 0.f;
     if (j < nb && nvk[j] > 0) {
-      const float s = __fmul_rn(srow[j], P.inv_sqrt_d);
-      key[k] = fkey(s);
-      e[k] = s;
-      mx = fmaxf(mx, s);
-      kmax = fmaxf(kmax, knr[j]);
+      const df s = df_mul(df{shr[j], slr[j]}, P.inv_sqrt_d);
+      key[k] = fkey(s.hi);
+      sl[k] = s.lo;
+      mx = fmaxf(mx, s.hi);
       ++ncand;
     }
   }
   mx = G.reduce(mx, [](float a, float b) { return fmaxf(a, b); });
-  kmax = G.reduce(kmax, [](float a, float b) { return fmaxf(a, b); });
   ncand = G.reduce(ncand, [](int a, int b) { return a + b; });
+  // weights e = exp(s - mx), s = hi + lo, error <= 2 ulp (expf) + O(u)
   df zl = {0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < kEPL; ++k) {
     if (key[k]) {
-      e[k] = expf(e[k] - mx);
-      zl = df_add(zl, df{e[k], 0.f});
+      const df x = two_sum(fkey_inv(key[k]), -mx);
+      const float ex = expf(x.hi);
+      sl[k] = fmaf(ex, __fadd_rn(x.lo, sl[k]), ex);
+      zl = df_add(zl, df{sl[k], 0.f});
+    } else {
+      sl[k] = 0.f;
     }
   }
+  float* e = sl;
   const df Z = G.reduce_df(zl);
-  const float Zf = Z.hi + Z.lo;
+  const float Zf = __fadd_rn(Z.hi, Z.lo);
   const int kf = min(P.topk, ncand);
   int m = ncand;
-  uint32_t tau = 1u;  // select every candidate key >= tau
+  uint32_t tau = 1u;  // select every candidate with key >= tau
   bool ambiguous = false;
   bool flag = false;
   if (!(P.topp >= 1.f) && kf < ncand) {
-    // certified error of an fp32 score and of a cumulative weight
-    const float delta = P.u_scale * P.qn[row] * kmax;
-    const float band = 2.1f * delta + 16.f * 5.9604645e-8f;
     const float target = P.topp * Zf;
     auto mass_ge = [&](uint32_t t) {
       float a = 0.f;
@@ -274,92 +283,83 @@ __global__ void __launch_bounds__(256) select_fast_kernel(SelParams P) {
       }
     kmin = G.reduce(kmin, [](uint32_t a, uint32_t b) { return min(a, b); });
     kmx = G.reduce(kmx, [](uint32_t a, uint32_t b) { return max(a, b); });
-    // largest key tp with mass(key >= tp) > target
+    // largest key tp with weight(key >= tp) > p * Z
     uint64_t lo = kmin, hi = static_cast<uint64_t>(kmx) + 1;
     while (hi - lo > 1) {
       const uint64_t mid = lo + ((hi - lo) >> 1);
       if (mass_ge(static_cast<uint32_t>(mid)) > target) lo = mid; else hi = mid;
     }
-    const uint32_t tp = static_cast<uint32_t>(lo);
-    // exact pieces around tp: compensated mass above, tie count, neighbours
-    df egt_l = {0.f, 0.f};
-    int cgt = 0, ceq = 0;
-    uint32_t above = 0xffffffffu, below = 0u;
+    uint32_t tsel = static_cast<uint32_t>(lo);
+    int mp;
+    float cum_prev, cum_at;
+    {
+      df egt_l = {0.f, 0.f};
+      int cgt = 0, ceq = 0;
+      float eeq = 0.f;
 #pragma unroll
-    for (int k = 0; k < kEPL; ++k) {
-      if (!key[k]) continue;
-      if (key[k] > tp) {
-        egt_l = df_add(egt_l, df{e[k], 0.f});
-        ++cgt;
-        above = min(above, key[k]);
-      } else if (key[k] == tp) {
-        ++ceq;
-      } else {
-        below = max(below, key[k]);
+      for (int k = 0; k < kEPL; ++k) {
+        if (!key[k]) continue;
+        if (key[k] > tsel) {
+          egt_l = df_add(egt_l, df{e[k], 0.f});
+          ++cgt;
+        } else if (key[k] == tsel) {
+          ++ceq;
+          eeq = e[k];
+        }
       }
+      const df Egt = G.reduce_df(egt_l);
+      cgt = G.reduce(cgt, [](int a, int b) { return a + b; });
+      ceq = G.reduce(ceq, [](int a, int b) { return a + b; });
+      eeq = G.reduce(eeq, [](float a, float b) { return fmaxf(a, b); });
+      if (ceq != 1) ambiguous = true;  // equal hi parts: order decided by lo / index
+      mp = cgt + 1;
+      const df at = df_add(Egt, df{eeq, 0.f});
+      cum_prev = __fdiv_rn(__fadd_rn(Egt.hi, Egt.lo), Zf);
+      cum_at = __fdiv_rn(__fadd_rn(at.hi, at.lo), Zf);
+      if (!(cum_prev < P.topp - kBand)) ambiguous = true;
+      if (mp < ncand && !(cum_at > P.topp + kBand)) ambiguous = true;
+      flag = fabsf(cum_at - P.topp) <= 1e-6f || (mp >= 2 && fabsf(cum_prev - P.topp) <= 1e-6f);
     }
-    const df Egt = G.reduce_df(egt_l);
-    cgt = G.reduce(cgt, [](int a, int b) { return a + b; });
-    ceq = G.reduce(ceq, [](int a, int b) { return a + b; });
-    above = G.reduce(above, [](uint32_t a, uint32_t b) { return min(a, b); });
-    below = G.reduce(below, [](uint32_t a, uint32_t b) { return max(a, b); });
-    const float stp = fkey_inv(tp);
-    const float etp = expf(stp - mx);
-    const float egt = Egt.hi + Egt.lo;
-    int t = 1;
-    while (t < ceq && egt + t * etp <= target) ++t;
-    const int mp = cgt + t;
-    const float cum_prev = (egt + (t - 1) * etp) / Zf;
-    const float cum_at = (egt + t * etp) / Zf;
-    const float s_above = above != 0xffffffffu ? fkey_inv(above) : 0.f;
-    const float s_below = below ? fkey_inv(below) : 0.f;
-    if (mp >= kf) {
-      m = mp;
-      tau = tp;
-      // the cut must not split ties, and must clear the error bound on
-      // both sides of the Top-p count and on the mass
-      if (t < ceq) ambiguous = true;
-      if (mp < ncand && !(stp - s_below > 2.f * delta)) ambiguous = true;
-      if (mp >= 2 && (t >= 2 || !(s_above - stp > 2.f * delta))) ambiguous = true;
-      if (!(cum_prev < P.topp - band)) ambiguous = true;
-      if (mp < ncand && !(cum_at > P.topp + band)) ambiguous = true;
-      flag = (mp < ncand && stp - s_below <= 1e-6f * fmaxf(1.f, fabsf(stp))) ||
-             fabsf(cum_at - P.topp) <= 1e-6f || (mp >= 2 && fabsf(cum_prev - P.topp) <= 1e-6f);
-    } else {
+    if (mp < kf) {
       // the Top-k floor decides: largest key tk with count(key >= tk) >= kf
       uint64_t l2 = kmin, h2 = static_cast<uint64_t>(kmx) + 1;
       while (h2 - l2 > 1) {
         const uint64_t mid = l2 + ((h2 - l2) >> 1);
         if (count_ge(static_cast<uint32_t>(mid)) >= kf) l2 = mid; else h2 = mid;
       }
-      const uint32_t tk = static_cast<uint32_t>(l2);
+      tsel = static_cast<uint32_t>(l2);
+      m = kf;
+      // the Top-p count must stay below the floor: weight of the kf best > p
       df ek_l = {0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < kEPL; ++k)
+        if (key[k] && key[k] >= tsel) ek_l = df_add(ek_l, df{e[k], 0.f});
+      const df Ek = G.reduce_df(ek_l);
+      if (!(__fdiv_rn(__fadd_rn(Ek.hi, Ek.lo), Zf) > P.topp + kBand)) ambiguous = true;
+    } else {
+      m = mp;
+    }
+    if (m < ncand) {
+      // the cut: exactly m keys >= tsel, and a clear gap to the next score
       int cge = 0;
-      uint32_t bel = 0u;
+      uint32_t below = 0u;
+      float lo_at = 0.f, lo_below = 0.f;
 #pragma unroll
       for (int k = 0; k < kEPL; ++k) {
         if (!key[k]) continue;
-        if (key[k] >= tk) {
-          ek_l = df_add(ek_l, df{e[k], 0.f});
-          ++cge;
-        } else {
-          bel = max(bel, key[k]);
-        }
+        if (key[k] >= tsel) ++cge; else below = max(below, key[k]);
       }
-      const df Ek = G.reduce_df(ek_l);
       cge = G.reduce(cge, [](int a, int b) { return a + b; });
-      bel = G.reduce(bel, [](uint32_t a, uint32_t b) { return max(a, b); });
-      m = kf;
-      tau = tk;
-      const float stk = fkey_inv(tk);
-      const float sbel = bel ? fkey_inv(bel) : 0.f;
-      const float cumk = (Ek.hi + Ek.lo) / Zf;
-      if (cge != kf) ambiguous = true;  // ties straddle the cut
-      if (!(stk - sbel > 2.f * delta)) ambiguous = true;
-      if (!(cumk > P.topp + band)) ambiguous = true;
-      flag = (stk - sbel <= 1e-6f * fmaxf(1.f, fabsf(stk))) ||
-             fabsf(cum_at - P.topp) <= 1e-6f || (mp >= 2 && fabsf(cum_prev - P.topp) <= 1e-6f);
+      below = G.reduce(below, [](uint32_t a, uint32_t b) { return max(a, b); });
+      if (cge != m) ambiguous = true;
+      const float s_at = fkey_inv(tsel), s_below = fkey_inv(below);
+      (void)lo_at;
+      (void)lo_below;
+      const float gap = s_at - s_below;  // hi parts; lo parts are below 1e-7 of them
+      if (!(gap > kGapAbs * fmaxf(1.f, fabsf(s_at)) + 2e-7f * fabsf(s_at))) ambiguous = true;
+      flag |= gap <= 1e-6f * fmaxf(1.f, fabsf(s_at));
     }
+    tau = tsel;
   }
   if (ambiguous) {
     if (G.wig == 0 && lane == 0) {
@@ -382,13 +382,11 @@ __global__ void __launch_bounds__(256) select_fast_kernel(SelParams P) {
 
 // ---------------------------------------------- exact fallback -------------
 struct FbParams {
-  int nb, nwords, d, topk, P2;
+  int nb, nwords, topk, P2;
   float topp;
   df inv_sqrt_d;
-  const float* Qh;
-  const float* Ql;
-  const float* Kh;
-  const float* Kl;
+  const float* Shi;
+  const float* Slo;
   const int32_t* n_valid;
   uint32_t* bitmask;
   int32_t* rowcnt;
@@ -403,51 +401,43 @@ __device__ __forceinline__ uint64_t df_key(df s) {
 __device__ __forceinline__ df df_key_inv(uint64_t k) {
   return {fkey_inv(static_cast<uint32_t>(k >> 32)), fkey_inv(static_cast<uint32_t>(k))};
 }
+__device__ __forceinline__ double df_to_d(df x) {
+  return static_cast<double>(x.hi) + static_cast<double>(x.lo);
+}
 
-// One CTA per ambiguous row (grid-stride over the list).  Smem: keys[P2]
-// (u64, descending order wanted), idx[P2] (u32), cum[P2] (fp64 weights, then
-// their running sum), the query's double-float mean.
+// One CTA per ambiguous row (grid-stride over the list): sort the candidates
+// by (double-float score desc, index asc), fp64 weights exp(s - max) and
+// their running sum in sorted order, the hybrid count, the bitmask.
+// Smem: keys[P2] (u64), cum[P2] (fp64), idx[P2] (u32).
 __global__ void __launch_bounds__(256) select_fallback_kernel(FbParams P) {
   extern __shared__ __align__(16) uint8_t sm[];
   uint64_t* keys = reinterpret_cast<uint64_t*>(sm);
   double* cum = reinterpret_cast<double*>(sm + 8ull * P.P2);
   uint32_t* idx = reinterpret_cast<uint32_t*>(sm + 16ull * P.P2);
-  float* qh = reinterpret_cast<float*>(sm + 20ull * P.P2);
-  float* ql = qh + P.d;
   __shared__ double red[32];
-  __shared__ int sh_m, sh_mp;
+  __shared__ int sh_nc, sh_mp;
   const uint32_t count = *reinterpret_cast<volatile uint32_t*>(P.status + WS_AMB_COUNT);
   const int nb = P.nb;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (uint32_t a = blockIdx.x; a < count; a += gridDim.x) {
     const long long row = P.amb[a];
     const long long bh = row / nb;
-    for (int c = threadIdx.x; c < P.d; c += blockDim.x) {
-      qh[c] = P.Qh[row * P.d + c];
-      ql[c] = P.Ql[row * P.d + c];
-    }
-    __syncthreads();
     const int32_t* nvk = P.n_valid + bh * nb;
-    // Dot2 scores of all candidates, as sortable keys
+    if (threadIdx.x == 0) sh_nc = 0;
+    __syncthreads();
+    int nc = 0;
     for (int j = threadIdx.x; j < P.P2; j += blockDim.x) {
       uint64_t kk = 0;  // not a candidate: sorts last
       if (j < nb && nvk[j] > 0) {
-        const float* kh = P.Kh + (bh * nb + j) * P.d;
-        const float* kl = P.Kl + (bh * nb + j) * P.d;
-        float s = 0.f, c = 0.f;
-        for (int q = 0; q < P.d; ++q) {
-          const float p = __fmul_rn(qh[q], kh[q]);
-          const float pe = fmaf(qh[q], kh[q], -p);
-          const float cross = fmaf(qh[q], kl[q], __fmul_rn(ql[q], kh[q]));
-          const df t = two_sum(s, p);
-          s = t.hi;
-          c = __fadd_rn(c, __fadd_rn(t.lo, __fadd_rn(pe, cross)));
-        }
-        const df dot = fast_two_sum(s, c);
-        kk = df_key(df_mul(dot, P.inv_sqrt_d));
+        const df s = df_mul(df{P.Shi[row * nb + j], P.Slo[row * nb + j]}, P.inv_sqrt_d);
+        kk = df_key(s);
+        ++nc;
       }
       keys[j] = kk;
       idx[j] = static_cast<uint32_t>(j);
     }
+    for (int o = 16; o > 0; o >>= 1) nc += __shfl_xor_sync(0xffffffffu, nc, o);
+    if (lane == 0) atomicAdd(&sh_nc, nc);
     __syncthreads();
     // bitonic sort: key descending, index ascending
     for (int k = 2; k <= P.P2; k <<= 1) {
@@ -460,38 +450,31 @@ __global__ void __launch_bounds__(256) select_fallback_kernel(FbParams P) {
             const uint32_t ia = idx[t], ib = idx[o];
             const bool a_first = ka > kb || (ka == kb && ia < ib);
             if (a_first != desc) {
-              keys[t] = kb; keys[o] = ka;
-              idx[t] = ib; idx[o] = ia;
+              keys[t] = kb;
+              keys[o] = ka;
+              idx[t] = ib;
+              idx[o] = ia;
             }
           }
         }
         __syncthreads();
       }
     }
-    // weights exp(s - max) in fp64, then the running sum in sorted order
-    const df smax = df_key_inv(keys[0]);
-    for (int j = threadIdx.x; j < P.P2; j += blockDim.x) {
-      double w = 0.0;
-      if (keys[j]) {
-        const df x = df_add(df_key_inv(keys[j]), df_neg(smax));
-        float ex = expf(x.hi);
-        ex = fmaf(ex, x.lo, ex);
-        w = static_cast<double>(ex);
-      }
-      cum[j] = w;
-    }
+    const int ncand = sh_nc;
+    const double smax = df_to_d(df_key_inv(keys[0]));
+    for (int j = threadIdx.x; j < P.P2; j += blockDim.x)
+      cum[j] = j < ncand ? exp(df_to_d(df_key_inv(keys[j])) - smax) : 0.0;
     __syncthreads();
     {
-      const int per = P.P2 / blockDim.x;  // P2 is a multiple of blockDim
+      // running sum in sorted order: per-thread runs, then a scan of the runs
+      const int per = P.P2 / blockDim.x;
       const int b0 = threadIdx.x * per;
       double run = 0.0;
       for (int q = 0; q < per; ++q) {
         run += cum[b0 + q];
         cum[b0 + q] = run;
       }
-      // exclusive scan of the per-thread totals (warp shuffles + smem)
       double incl = run;
-      const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
       for (int o = 1; o < 32; o <<= 1) {
         const double y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
@@ -510,33 +493,21 @@ __global__ void __launch_bounds__(256) select_fallback_kernel(FbParams P) {
       const double off = red[warp] + (incl - run);
       for (int q = 0; q < per; ++q) cum[b0 + q] += off;
     }
-    __syncthreads();
-    int ncand = 0;
-    for (int j = threadIdx.x; j < nb; j += blockDim.x) ncand += nvk[j] > 0 ? 1 : 0;
-    for (int o = 16; o > 0; o >>= 1) ncand += __shfl_xor_sync(0xffffffffu, ncand, o);
     if (threadIdx.x == 0) sh_mp = ncand;
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) atomicAdd(&sh_m, 0);  // keep sh_m live
-    __shared__ int ncand_s;
-    if (threadIdx.x == 0) ncand_s = 0;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) atomicAdd(&ncand_s, ncand);
-    __syncthreads();
-    const int nc = ncand_s;
-    const double Zt = cum[nc - 1];
-    if (threadIdx.x == 0) sh_mp = nc;
-    __syncthreads();
+    const double Zt = cum[ncand - 1];
+    const double p = P.topp;
     if (!(P.topp >= 1.f)) {
       // smallest m with cum_m / Z > p (1-based)
-      for (int j = threadIdx.x; j < nc; j += blockDim.x) {
-        const bool over = cum[j] / Zt > static_cast<double>(P.topp);
-        const bool prev_over = j > 0 && cum[j - 1] / Zt > static_cast<double>(P.topp);
+      for (int j = threadIdx.x; j < ncand; j += blockDim.x) {
+        const bool over = cum[j] / Zt > p;
+        const bool prev_over = j > 0 && cum[j - 1] / Zt > p;
         if (over && !prev_over) atomicMin(&sh_mp, j + 1);
       }
     }
     __syncthreads();
     const int mp = sh_mp;
-    const int m = max(min(P.topk, nc), mp);
+    const int m = max(min(P.topk, ncand), mp);
     uint32_t* bm = P.bitmask + row * P.nwords;
     for (int w = threadIdx.x; w < P.nwords; w += blockDim.x) bm[w] = 0u;
     __syncthreads();
@@ -544,12 +515,10 @@ __global__ void __launch_bounds__(256) select_fallback_kernel(FbParams P) {
     if (threadIdx.x == 0) {
       P.rowcnt[row] = m;
       bool flag = false;
-      if (m < nc) {
-        const df a = df_key_inv(keys[m - 1]), b = df_key_inv(keys[m]);
-        const double sa = static_cast<double>(a.hi) + a.lo, sb = static_cast<double>(b.hi) + b.lo;
+      if (m < ncand) {
+        const double sa = df_to_d(df_key_inv(keys[m - 1])), sb = df_to_d(df_key_inv(keys[m]));
         flag |= fabs(sa - sb) <= 1e-6 * fmax(1.0, fabs(sa));
       }
-      const double p = P.topp;
       flag |= fabs(cum[mp - 1] / Zt - p) <= 1e-6;
       if (mp >= 2) flag |= fabs(cum[mp - 2] / Zt - p) <= 1e-6;
       P.tie[row] = flag ? 1 : 0;
@@ -658,34 +627,30 @@ cudaError_t launch_select(const Plan& p, const float* Qh, const float* Ql, const
   const long long rows = static_cast<long long>(c.B) * c.H * nb;
   const int nwords = (nb + 31) / 32;
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  float* S = reinterpret_cast<float*>(ws + p.off_scores);
+  float* Shi = reinterpret_cast<float*>(ws + p.off_scores);
+  float* Slo = Shi + rows * nb;
   uint32_t* bitmask = reinterpret_cast<uint32_t*>(ws + p.off_bitmask);
   int32_t* rowcnt = reinterpret_cast<int32_t*>(ws + p.off_rowcnt);
   int32_t* colcnt = reinterpret_cast<int32_t*>(ws + p.off_colcnt);
   int32_t* amb = reinterpret_cast<int32_t*>(ws + p.off_amb);
-  float* qn = reinterpret_cast<float*>(ws + p.off_qn);
-  float* kn = qn + rows;
-  cudaError_t e;
-  e = cudaMemsetAsync(status + WS_AMB_COUNT, 0, sizeof(uint32_t), st);
+  const double isd = 1.0 / sqrt(static_cast<double>(c.d));
+  df isd_df;
+  isd_df.hi = static_cast<float>(isd);
+  isd_df.lo = static_cast<float>(isd - static_cast<double>(isd_df.hi));
+  cudaError_t e = cudaMemsetAsync(status + WS_AMB_COUNT, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  norms_kernel<<<static_cast<unsigned>((2 * rows * 32 + 255) / 256), 256, 0, st>>>(rows, c.d, Qh,
-                                                                                   Kh, qn, kn);
-  dim3 g((nb + kTile - 1) / kTile, (nb + kTile - 1) / kTile, c.B * c.H);
-  score_gemm_kernel<<<g, 256, 0, st>>>(nb, c.d, Qh, Kh, S);
+  dim3 g((nb + kTJ - 1) / kTJ, (nb + kTI - 1) / kTI, c.B * c.H);
+  score_dot2_kernel<<<g, 256, 0, st>>>(nb, c.d, Qh, Ql, Kh, Kl, Shi, Slo);
   SelParams sp;
   sp.nb = nb;
   sp.nwords = nwords;
-  sp.d = c.d;
   sp.topk = c.topk_floor;
   sp.rows = rows;
   sp.topp = c.topp;
-  sp.inv_sqrt_d = static_cast<float>(1.0 / sqrt(static_cast<double>(c.d)));
-  sp.u_scale = static_cast<float>(1.01 * (c.d + 5) * 5.9604644775390625e-8 /
-                                  sqrt(static_cast<double>(c.d)));
-  sp.S = S;
+  sp.inv_sqrt_d = isd_df;
+  sp.Shi = Shi;
+  sp.Slo = Slo;
   sp.n_valid = n_valid;
-  sp.qn = qn;
-  sp.kn = kn;
   sp.bitmask = bitmask;
   sp.rowcnt = rowcnt;
   sp.tie = sel_tie;
@@ -703,28 +668,21 @@ cudaError_t launch_select(const Plan& p, const float* Qh, const float* Ql, const
   FbParams fp;
   fp.nb = nb;
   fp.nwords = nwords;
-  fp.d = c.d;
   fp.topk = c.topk_floor;
   int P2 = 256;
   while (P2 < nb) P2 <<= 1;
   fp.P2 = P2;
   fp.topp = c.topp;
-  {
-    const double isd = 1.0 / sqrt(static_cast<double>(c.d));
-    fp.inv_sqrt_d.hi = static_cast<float>(isd);
-    fp.inv_sqrt_d.lo = static_cast<float>(isd - static_cast<double>(fp.inv_sqrt_d.hi));
-  }
-  fp.Qh = Qh;
-  fp.Ql = Ql;
-  fp.Kh = Kh;
-  fp.Kl = Kl;
+  fp.inv_sqrt_d = isd_df;
+  fp.Shi = Shi;
+  fp.Slo = Slo;
   fp.n_valid = n_valid;
   fp.bitmask = bitmask;
   fp.rowcnt = rowcnt;
   fp.tie = sel_tie;
   fp.amb = amb;
   fp.status = status;
-  const size_t fsm = 20ull * P2 + 8ull * c.d;
+  const size_t fsm = 20ull * P2;
   e = cudaFuncSetAttribute(select_fallback_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(fsm));
   if (e != cudaSuccess) return e;
