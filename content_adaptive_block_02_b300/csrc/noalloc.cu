@@ -1,0 +1,111 @@
+// Backward entry point that allocates nothing and takes no workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// backward: code that runs inside a memory-pool arena it does not own, or
+// inside a runtime that forbids cudaMalloc / cudaFree after start-up.  For
+// them the backward's scratch -- the per-row rowsum D, the fp32 dQ
+// accumulator and the small status / work-counter words -- lives in one
+// fixed-size array that is part of this library (below), instead of in a
+// caller-provided workspace.
+//
+// The array is kNoAllocScratchBytes (32 MiB) on every GPU that loads the
+// library and is held until the process exits.  All calls share it and it
+// keeps the last call's contents; everything that must start at zero is
+// cleared at the start of each call.  Two calls whose kernels overlap on the
+// GPU (different streams, or different threads without ordering) race on the
+// array and give wrong results.  Device-side wait timeouts of this variant are
+// recorded only in the array's own status word and are not reported back.
+#include <mutex>
+
+#include "prism_internal.cuh"
+
+namespace prism {
+cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp, float* D,
+                           float* dQacc, cudaStream_t st);
+cudaError_t launch_attn_bwd_simt(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                 const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                                 const float* D, const int32_t* n_valid,
+                                 const int32_t* col_ptr, const int32_t* row_idx, float scale,
+                                 float* dQacc, uint16_t* dKp, uint16_t* dVp, cudaStream_t st);
+cudaError_t launch_attn_bwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                               const float* D, const int32_t* n_valid, const int32_t* col_ptr,
+                               const int32_t* row_idx, float scale, float* dQacc, uint16_t* dKp,
+                               uint16_t* dVp, uint8_t* ws, cudaStream_t st);
+}  // namespace prism
+
+struct prism_plan {
+  prism::Plan p;
+};
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 32ull << 20;
+
+// The scratch itself.  In host code `g_noalloc_scratch` names a host-side
+// stand-in, not device memory: its device address comes from
+// cudaGetSymbolAddress, taken once per device below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (set up on the first
+// call on that device).
+cudaError_t scratch_address(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(g_addr[dev]);
+  return cudaSuccess;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int prism_sparse_attn_bwd_noalloc(
+    const prism_plan_t* plan, const uint16_t* Qp, const uint16_t* Kp, const uint16_t* Vp,
+    const uint16_t* Op, const uint16_t* dOp, const float* lse, const int32_t* n_valid,
+    const int32_t* col_ptr, const int32_t* row_idx, float scale, uint16_t* dQp, uint16_t* dKp,
+    uint16_t* dVp, void* stream) {
+  if (plan == nullptr || !(scale > 0.f)) return PRISM_ERR_ARG;
+  const void* ptrs[] = {Qp, Kp, Vp, Op, dOp, lse, n_valid, col_ptr, row_idx, dQp, dKp, dVp};
+  for (const void* q : ptrs) {
+    if (q == nullptr) return PRISM_ERR_ARG;
+    if (!al16(q)) return PRISM_ERR_ALIGN;
+  }
+  const prism::Plan& p = plan->p;
+  // layout inside the scratch: status words, D, dQ accumulator
+  const size_t rows = static_cast<size_t>(p.cfg.B) * p.cfg.H * p.sz.Np;
+  const size_t off_D = 256;
+  const size_t off_dq = off_D + ((rows * 4 + 255) & ~static_cast<size_t>(255));
+  const size_t need = off_dq + rows * p.cfg.d * 4;
+  if (need > kNoAllocScratchBytes) return PRISM_ERR_UNSUPPORTED;  // problem too large for it
+  uint8_t* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return PRISM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* D = reinterpret_cast<float*>(base + off_D);
+  float* dq = reinterpret_cast<float*>(base + off_dq);
+  if (cudaMemsetAsync(base, 0, 256, st) != cudaSuccess) return PRISM_ERR_CUDA;
+  if (prism::launch_bwd_pre(p, Op, dOp, D, dq, st) != cudaSuccess) return PRISM_ERR_CUDA;
+  cudaError_t e;
+  if (p.sz.tensor_core_bwd)
+    e = prism::launch_attn_bwd_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx, scale,
+                                  dq, dKp, dVp, base, st);
+  else
+    e = prism::launch_attn_bwd_simt(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx, scale,
+                                    dq, dKp, dVp, st);
+  if (e != cudaSuccess) return PRISM_ERR_CUDA;
+  if (prism::launch_dq_convert(p, dq, scale, dQp, st) != cudaSuccess) return PRISM_ERR_CUDA;
+  return PRISM_OK;
+}

@@ -191,6 +191,25 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
                           const int32_t* row_idx, float scale, uint16_t* dQp, uint16_t* dKp,
                           uint16_t* dVp, void* ws, void* stream);
 
+/* Backward without a workspace, for callers that cannot allocate device
+ * memory when they run it (for example code confined to a memory pool it does
+ * not own, or a runtime that forbids cudaMalloc / cudaFree after start-up).
+ * The paper has no counterpart: this is a library convenience.  Arguments and
+ * results are those of prism_sparse_attn_bwd minus row_ptr, col_idx and ws;
+ * the scratch (rowsum D and the fp32 dQ accumulator, B*H*Np*(d+1)*4 bytes plus
+ * 256) lives in a 32 MiB array inside the library, held on every GPU that
+ * loads the library until the process exits.  Larger problems return
+ * PRISM_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
+ * device looks the array's address up (make that first call before any stream
+ * capture).  All calls share the array: calls whose kernels overlap on the GPU
+ * race and give wrong results.  Device-side wait timeouts are not reported by
+ * this variant. */
+int prism_sparse_attn_bwd_noalloc(const prism_plan_t* plan, const uint16_t* Qp,
+                                  const uint16_t* Kp, const uint16_t* Vp, const uint16_t* Op,
+                                  const uint16_t* dOp, const float* lse, const int32_t* n_valid,
+                                  const int32_t* col_ptr, const int32_t* row_idx, float scale,
+                                  uint16_t* dQp, uint16_t* dKp, uint16_t* dVp, void* stream);
+
 /* Inverse permutation: X[b,n,h] = Xp[b,h,inv[n]].  Xp [B, H, Np, d] bf16 ->
  * X [B, N, H, d] bf16. */
 int prism_unpermute(const prism_plan_t* plan, const int32_t* inv, const uint16_t* Xp,
