@@ -6,21 +6,24 @@
 // the key blocks selected for it.  Reading used here: exact softmax over the
 // real tokens of the selected key blocks, scale `scale`, natural-log LSE.
 //
-// Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 4  producer: takes the next query block from a global work counter,
+// Design (one persistent CTA per SM, 320 threads, warp-specialised):
+//   warp 8  producer: takes the next query block from a global work counter,
 //           publishes it in a 2-slot work ring, and streams the K and V tiles
 //           of its selected key blocks into two 3-stage shared-memory rings
 //           with TMA (128-byte swizzle, 2 boxes of 64 x 128 per tile).
-//   warp 5  MMA issuer (one thread): S = Q K^T with Q held in tensor memory
+//   warp 9  MMA issuer (one thread): S = Q K^T with Q held in tensor memory
 //           (A from TMEM, B = K tile from smem), then O += P V with P in
 //           tensor memory (A from TMEM, B = V tile, MN-major).  Order per
 //           query block: S_0, S_1, PV_0, S_2, PV_1, ... so the next score tile
 //           is on the tensor pipe while the softmax warps work on this one.
-//   warps 0-3  softmax (thread = query row = TMEM lane): Q row -> TMEM; per
-//           key block: S row from TMEM to registers, online softmax in the
-//           log2 domain with lazy rescaling (O in TMEM is rescaled only when
-//           the running max grows by more than 2^8), P (bf16) -> TMEM; at the
-//           end O / l -> bf16 rows of Op, LSE.
+//   warps 0-7  softmax, two warpgroups: warps w and w+4 share the query rows
+//           of TMEM lane quarter w%4 (thread = query row) and split the 128
+//           key columns (and the 128 O columns) in halves.  Per key block: the
+//           half row of S from TMEM to registers, the half maxima exchanged
+//           through shared memory (one 64-thread named barrier per lane
+//           quarter), online softmax in the log2 domain with lazy rescaling
+//           (O in TMEM is rescaled only when the running max grows by more
+//           than 2^8), P (bf16) -> TMEM; at the end O / l -> bf16, LSE.
 // Tensor memory (512 columns): S [0,128), O [128,256), Q [256,320),
 // P0 [320,384), P1 [384,448).
 // Every wait is bounded: on expiry the CTA raises a flag, records the error in
@@ -37,7 +40,8 @@ constexpr int kS = 128;
 constexpr int kD = 128;
 constexpr int kTile = kS * kD * 2;  // 32 KB
 constexpr int kStages = 3;
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 320;
+constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_Q = 256, TM_P0 = 320, TM_P1 = 384;
 
 struct FwdShared {
@@ -45,6 +49,8 @@ struct FwdShared {
   uint64_t s_full, s_free, p_full[2], o_full, q_ready, final_bar;
   uint64_t work_full[2], work_empty[2];
   int work_row[2], work_beg[2], work_end[2], work_nvq[2];
+  float xmax[2][2][128];  // [tile parity][column half][row]: half-row maxima
+  float xsum[2][128];     // [column half][row]: half-row sums at the end
   uint32_t tmem_base;
   int abort;
 };
@@ -83,15 +89,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&sm.v_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 128);
-    mbar_init(&sm.p_full[0], 128);
-    mbar_init(&sm.p_full[1], 128);
+    mbar_init(&sm.s_free, kSoftmaxThreads);
+    mbar_init(&sm.p_full[0], kSoftmaxThreads);
+    mbar_init(&sm.p_full[1], kSoftmaxThreads);
     mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.q_ready, 128);
+    mbar_init(&sm.q_ready, kSoftmaxThreads);
     mbar_init(&sm.final_bar, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.work_full[s], 1);
-      mbar_init(&sm.work_empty[s], 129);
+      mbar_init(&sm.work_empty[s], 1 + kSoftmaxThreads);
     }
     sm.abort = 0;
     mbar_init_fence();
@@ -104,7 +110,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const Waiter W{&sm.abort, P.status, P.limit};
   uint32_t* queue = P.status + WS_FWD_QUEUE;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------ producer ----
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer ----
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);   // A = Q (TMEM), B = K, K-major
@@ -211,10 +217,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------ softmax ----
-    const int r = threadIdx.x;  // query row of the block == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base + TM_S, tO = tmem + lane_base + TM_O;
-    uint32_t sidx = 0, pidx = 0, qcnt = 0;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // query row of the block == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + TM_S + half * 64;
+    const uint32_t tO = tmem + lane_base + TM_O + half * 64;
+    const int c0 = half * 64;  // first key column (and O column) of this half
+    auto pair_sync = [&]() {
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+    };
+    uint32_t sidx = 0, pidx = 0, tile = 0;
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
       if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 10)) break;
@@ -224,31 +236,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const long long bh = row / P.nb;
       const int i = row % P.nb;
       const long long grow = bh * P.Np + static_cast<long long>(i) * kS + r;
-      uint4* orow = reinterpret_cast<uint4*>(P.Op + grow * kD);
+      uint4* orow = reinterpret_cast<uint4*>(P.Op + grow * kD) + half * 8;
       if (n == 0) {
 #pragma unroll
-        for (int q = 0; q < kD / 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
-        P.lse[grow] = 0.f;
+        for (int q = 0; q < 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
+        if (half == 0) P.lse[grow] = 0.f;
         mbar_arrive(&sm.work_empty[ws]);
         continue;
       }
       {
-        // this row of Q -> tensor memory (bf16 pairs, 64 columns)
-        const uint4* qrow = reinterpret_cast<const uint4*>(P.Qp + grow * kD);
+        // this half of the row of Q -> tensor memory (bf16 pairs, 32 columns)
+        const uint4* qrow = reinterpret_cast<const uint4*>(P.Qp + grow * kD) + half * 8;
         uint32_t a[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 v = ldg_nc_v4(qrow + h * 8 + q);
-            a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
-          }
-          tmem_st32(tmem + lane_base + TM_Q + h * 32, a);
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = ldg_nc_v4(qrow + q);
+          a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
         }
+        tmem_st32(tmem + lane_base + TM_Q + half * 32, a);
         tmem_st_wait();
         fence_before();
         mbar_arrive(&sm.q_ready);
-        ++qcnt;
       }
       const uint32_t pv_base = pidx;
       float m = -INFINITY, l = 0.f;
@@ -256,22 +264,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int jj = 0; jj < n; ++jj) {
         const int j = P.col_idx[beg + jj];
         const int nvk = P.n_valid[bh * P.nb + j];
+        const int lim = nvk - c0;  // columns of this half that hold real keys
         if (!W.wait(&sm.s_full, sidx & 1, 11)) { ok = false; break; }
         fence_after();
-        uint32_t s[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+        uint32_t s[2][32];
+        tmem_ld32(tS, s[0]);
+        tmem_ld32(tS + 32, s[1]);
         tmem_ld_wait();
         fence_before();
         mbar_arrive(&sm.s_free);
         ++sidx;
         float mx = -INFINITY;
+        if (lim >= 64) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < nvk) mx = fmaxf(mx, __uint_as_float(s[c][e]));
-        mx *= P.scale_log2;
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+        }
+        const int par = tile & 1;
+        ++tile;
+        sm.xmax[par][half][r] = mx;
+        pair_sync();
+        mx = fmaxf(mx, sm.xmax[par][half ^ 1][r]) * P.scale_log2;
         const bool resc = mx > m + 8.f;
         const float m_new = resc ? mx : m;
         const float corr = resc ? ex2(m - m_new) : 1.f;
@@ -280,7 +300,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!W.wait(&sm.o_full, g & 1, 12)) { ok = false; break; }
           fence_after();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
             tmem_ld_wait();
@@ -293,22 +313,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l *= corr;
         m = m_new;
         float lsum = 0.f;
-        const uint32_t tP = tmem + lane_base + ((pidx & 1) ? TM_P1 : TM_P0);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+        uint32_t pk[32];
+        if (lim >= 64) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int c0 = h * 64 + 2 * e;
-            const float x0 = __uint_as_float(s[c0 >> 5][c0 & 31]);
-            const float x1 = __uint_as_float(s[(c0 + 1) >> 5][(c0 + 1) & 31]);
-            const float p0 = c0 < nvk ? ex2(fmaf(x0, P.scale_log2, -m)) : 0.f;
-            const float p1 = c0 + 1 < nvk ? ex2(fmaf(x1, P.scale_log2, -m)) : 0.f;
+            const int k0 = 2 * e;
+            const float p0 = ex2(fmaf(__uint_as_float(s[k0 >> 5][k0 & 31]), P.scale_log2, -m));
+            const float p1 = ex2(fmaf(__uint_as_float(s[(k0 + 1) >> 5][(k0 + 1) & 31]), P.scale_log2, -m));
             lsum += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
-          tmem_st32(tP + h * 32, pk);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int k0 = 2 * e;
+            const float p0 = k0 < lim ? ex2(fmaf(__uint_as_float(s[k0 >> 5][k0 & 31]), P.scale_log2, -m)) : 0.f;
+            const float p1 = k0 + 1 < lim ? ex2(fmaf(__uint_as_float(s[(k0 + 1) >> 5][(k0 + 1) & 31]), P.scale_log2, -m)) : 0.f;
+            lsum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
         }
+        tmem_st32(tmem + lane_base + ((pidx & 1) ? TM_P1 : TM_P0) + half * 32, pk);
         l += lsum;
         tmem_st_wait();
         fence_before();
@@ -316,13 +341,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++pidx;
       }
       if (!ok) break;
-      // epilogue: wait for the last PV, normalise, write the row
+      // epilogue: row sum over both halves, wait for the last PV, write the row
+      sm.xsum[half][r] = l;
+      pair_sync();
+      const float lt = sm.xsum[0][r] + sm.xsum[1][r];
       if (!W.wait(&sm.o_full, (pidx - 1) & 1, 13)) break;
       fence_after();
       const bool real = r < nvq;
-      const float inv = real ? 1.f / l : 0.f;
+      const float inv = real ? 1.f / lt : 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait();
@@ -336,7 +364,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           orow[c * 4 + q] = v;
         }
       }
-      P.lse[grow] = real ? (m + log2f(l)) * 0.69314718055994531f : 0.f;
+      if (half == 0) P.lse[grow] = real ? (m + log2f(lt)) * 0.69314718055994531f : 0.f;
+      // both halves have read xsum before either writes it for the next block
+      pair_sync();
       fence_before();
       mbar_arrive(&sm.work_empty[ws]);
     }

@@ -18,13 +18,16 @@
 //                                  -> TMEM, over dP once dP^T has been read
 // and the dQ_i tile is added to an fp32 accumulator with vector reductions.
 //
-// Roles (320 threads, one persistent CTA per SM):
-//   warps 0-3  compute: thread = key row = TMEM lane; P^T, dS^T, epilogue
-//              dK * scale, dV -> bf16.
-//   warps 4-7  dQ drain: thread = query row; TMEM -> registers -> red.add.v4.
-//   warp 8     producer: work counter, TMA loads of K_j, V_j (once per item)
-//              and of Q_i, dO_i, LSE_i, D_i (2-stage ring).
-//   warp 9     MMA issuer.  Tensor-pipe order per step i (steady state):
+// Roles (448 threads, one persistent CTA per SM):
+//   warps 0-7  compute, two warpgroups: warps w and w+4 own the key rows of
+//              TMEM lane quarter w%4 (thread = key row) and split the 128
+//              query columns in halves; P^T, dS^T, epilogue dK * scale, dV
+//              -> bf16 (the halves split the 128 channels there).
+//   warps 8-11 dQ drain: thread = query row; TMEM -> registers -> red.add.v4.
+//   warp 12    producer: work counter, TMA loads of K_j, V_j (once per item)
+//              and of Q_i, dO_i, LSE_i, D_i (2-stage ring) plus the stage's
+//              query-block index and real-token count.
+//   warp 13    MMA issuer.  Tensor-pipe order per step i (steady state):
 //              4_i 5_i | 3_{i+1} | 2_{i+1} | 1_{i+2}
 //              so the P / dS work of the compute warps and the dQ drain both
 //              overlap tensor work.
@@ -38,7 +41,8 @@ using namespace tc;
 constexpr int kS = 128, kD = 128;
 constexpr int kTile = kS * kD * 2;           // 32 KB
 constexpr int kStage = 2 * kTile + 1024;     // Q, dO, LSE (512 B), D (512 B)
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kCompute = 256;
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
 constexpr int kOffV = kTile, kOffStage = 2 * kTile, kOffDS = 2 * kTile + 2 * kStage;
 constexpr int kOffBar = kOffDS + kTile;
@@ -49,6 +53,7 @@ struct BwdBars {
   uint64_t kv_done, kv_free, final_bar;
   uint64_t work_full[2], work_empty[2];
   int work_col[2], work_beg[2], work_end[2], work_nvk[2];
+  int stage_i[2], stage_nvq[2];  // query block of each Q / dO stage and its real rows
   uint32_t tmem_base;
   int abort;
 };
@@ -72,6 +77,7 @@ struct BwdParams {
   unsigned long long limit;
 };
 
+// 14 warps: 3-4 per SM sub-partition, so at most 128 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -91,17 +97,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.qdo_full[s], 1);
       mbar_init(&sm.qdo_empty[s], 1);
       mbar_init(&sm.work_full[s], 1);
-      mbar_init(&sm.work_empty[s], 1 + 128 + 128);
+      mbar_init(&sm.work_empty[s], 1 + kCompute + 128);
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.p_ready, 128);
-    mbar_init(&sm.ds_ready, 128);
+    mbar_init(&sm.p_ready, kCompute);
+    mbar_init(&sm.ds_ready, kCompute);
     mbar_init(&sm.ds_empty, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_drained, 128);
     mbar_init(&sm.kv_done, 1);
-    mbar_init(&sm.kv_free, 128);
+    mbar_init(&sm.kv_free, kCompute);
     mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
     mbar_init_fence();
@@ -117,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* dsbuf = dsm + kOffDS;
   auto stage = [&](int s) { return dsm + kOffStage + s * kStage; };
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------ producer ----
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -158,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = use & 1;
           if (!W.wait(&sm.qdo_empty[s], ((use >> 1) & 1) ^ 1, 23)) { ok = false; break; }
           uint8_t* st = stage(s);
+          sm.stage_i[s] = i;
+          sm.stage_nvq[s] = P.n_valid[bh * P.nb + i];
           mbar_expect_tx(&sm.qdo_full[s], 2 * kTile + 1024);
           tma_load_2d(st, &tmQ, &sm.qdo_full[s], 0, static_cast<int>(yq));
           tma_load_2d(st + kTile / 2, &tmQ, &sm.qdo_full[s], 64, static_cast<int>(yq));
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------ MMA issuer ----
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // A K-major, B K-major
@@ -279,10 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       commit(&sm.final_bar);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------ compute ----
-    const int r = threadIdx.x;  // key row == TMEM lane
-    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // key row == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
+    const int q0 = half * 64;  // first query column (and first channel) of this half
+    auto pair_sync = [&]() {
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+    };
     uint32_t use = 0, scnt = 0, dpcnt = 0, dsidx = 0, kvcnt = 0;
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
@@ -293,76 +306,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long bh = col / P.nb;
       const int j = static_cast<int>(col % P.nb);
       const long long krow = bh * P.Np + static_cast<long long>(j) * kS + r;
-      uint4* dkrow = reinterpret_cast<uint4*>(P.dKp + krow * kD);
-      uint4* dvrow = reinterpret_cast<uint4*>(P.dVp + krow * kD);
+      uint4* dkrow = reinterpret_cast<uint4*>(P.dKp + krow * kD) + half * 8;
+      uint4* dvrow = reinterpret_cast<uint4*>(P.dVp + krow * kD) + half * 8;
       if (n == 0) {
 #pragma unroll
-        for (int q = 0; q < kD / 8; ++q) dkrow[q] = dvrow[q] = make_uint4(0, 0, 0, 0);
+        for (int q = 0; q < 8; ++q) dkrow[q] = dvrow[q] = make_uint4(0, 0, 0, 0);
         mbar_arrive(&sm.work_empty[ws]);
         continue;
       }
       bool ok = true;
       for (int k = 0; k < n; ++k) {
-        const int i = P.row_idx[beg + k];
-        const int nvq = P.n_valid[bh * P.nb + i];
-        const float* lsed = reinterpret_cast<const float*>(stage((use + k) & 1) + 2 * kTile);
-        // LSE_i and D_i arrive with Q_i / dO_i on the stage's barrier
-        if (!W.wait(&sm.qdo_full[(use + k) & 1], ((use + k) >> 1) & 1, 40)) { ok = false; break; }
-        // ---- P^T = exp(S^T * scale - LSE) ----
+        const int s_ = (use + k) & 1;
+        if (!W.wait(&sm.qdo_full[s_], ((use + k) >> 1) & 1, 40)) { ok = false; break; }
+        const int lim = (r < nvk) ? sm.stage_nvq[s_] - q0 : 0;  // real query columns here
+        const float4* lse4 = reinterpret_cast<const float4*>(stage(s_) + 2 * kTile) + half * 16;
+        const float4* D4 = lse4 + 32;
+        // ---- P^T = exp(S^T * scale - LSE) on this half of the queries ----
         if (!W.wait(&sm.s_full, scnt & 1, 42)) { ok = false; break; }
         ++scnt;
         fence_after();
-        float p[128];
-        {
-          uint32_t s[4][32];
+        float p[64];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + TM_S + c * 32, s[c]);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(tmem + lb + TM_S + q0 + c * 32, sv);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int g = 0; g < 8; ++g) {
+            const float4 L = lse4[c * 8 + g];
+            const float lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int q = c * 32 + e;
-              const float x = fmaf(__uint_as_float(s[c][e]), P.scale_log2,
-                                   -lsed[q] * 1.4426950408889634f);
-              p[q] = (r < nvk && q < nvq) ? ex2(x) : 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const int q = c * 32 + g * 4 + e;
+              const float x = fmaf(__uint_as_float(sv[g * 4 + e]), P.scale_log2,
+                                   -lv[e] * 1.4426950408889634f);
+              p[q] = q < lim ? ex2(x) : 0.f;
             }
+          }
         }
+        // both halves have read S^T before P^T (half as wide) is written over it
+        pair_sync();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[h * 64 + 2 * e], p[h * 64 + 2 * e + 1]);
-          tmem_st32(tmem + lb + TM_S + h * 32, pk);
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[h * 32 + 2 * e], p[h * 32 + 2 * e + 1]);
+          tmem_st16(tmem + lb + TM_S + half * 32 + h * 16, pk);
         }
         tmem_st_wait();
         fence_before();
         mbar_arrive(&sm.p_ready);
-        // ---- dS^T = P^T * (dP^T - D) -> smem (128-byte swizzled, K-major) ----
+        // ---- dS^T = P^T * (dP^T - D) -> smem panel `half` (128-byte swizzle) ----
         if (!W.wait(&sm.dp_full, dpcnt & 1, 43)) { ok = false; break; }
         ++dpcnt;
         if (dsidx > 0 && !W.wait(&sm.ds_empty, (dsidx - 1) & 1, 44)) { ok = false; break; }
         ++dsidx;
         fence_after();
-        const float* Dv = lsed + 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t dp[32];
-          tmem_ld32(tmem + lb + TM_DP + c * 32, dp);
+          tmem_ld32(tmem + lb + TM_DP + q0 + c * 32, dp);
           tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
-            const int q0 = c * 32 + g * 8;
+            const int ql = c * 32 + g * 8;  // local query index in this half
+            const float4 da = D4[ql / 4], db4 = D4[ql / 4 + 1];
+            const float dv[8] = {da.x, da.y, da.z, da.w, db4.x, db4.y, db4.z, db4.w};
             uint32_t w4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int qa = q0 + 2 * e, qb2 = qa + 1;
-              const float da = p[qa] * (__uint_as_float(dp[g * 8 + 2 * e]) - Dv[qa]);
-              const float db = p[qb2] * (__uint_as_float(dp[g * 8 + 2 * e + 1]) - Dv[qb2]);
-              w4[e] = pack_bf16x2(da, db);
+              const float x0 = p[ql + 2 * e] * (__uint_as_float(dp[g * 8 + 2 * e]) - dv[2 * e]);
+              const float x1 =
+                  p[ql + 2 * e + 1] * (__uint_as_float(dp[g * 8 + 2 * e + 1]) - dv[2 * e + 1]);
+              w4[e] = pack_bf16x2(x0, x1);
             }
-            const int panel = q0 >> 6, chunk = (q0 & 63) >> 3;
-            const uint32_t off = panel * (kTile / 2) + r * 128 + ((chunk ^ (r & 7)) << 4);
+            const int chunk = ql >> 3;
+            const uint32_t off = half * (kTile / 2) + r * 128 + ((chunk ^ (r & 7)) << 4);
             *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
@@ -372,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       use += n;
-      // ---- epilogue: dV, dK * scale -> bf16 rows ----
+      // ---- epilogue: dV, dK * scale -> bf16, this half of the channels ----
       if (!W.wait(&sm.kv_done, kvcnt & 1, 45)) break;
       ++kvcnt;
       fence_after();
@@ -382,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4* dst = which ? dkrow : dvrow;
         const float mul = real ? (which ? P.scale : 1.f) : 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tmem_ld32(tmem + lb + (which ? TM_DK : TM_DV) + c * 32, o);
+          tmem_ld32(tmem + lb + (which ? TM_DK : TM_DV) + q0 + c * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -403,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------ dQ drain ----
-    const int q = threadIdx.x - 128;  // query row == TMEM lane
-    const uint32_t lb = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const int q = threadIdx.x - 256;  // query row == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>((warp - 8) * 32) << 16;
     uint32_t dqcnt = 0;
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
@@ -420,20 +439,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!W.wait(&sm.dq_full, dqcnt & 1, 52)) { ok = false; break; }
         ++dqcnt;
         fence_after();
-        uint32_t v[4][32];
+        float* dst = P.dQacc + (bh * P.Np + static_cast<long long>(i) * kS + q) * kD;
+        const bool real = q < nvq;
+        // two columns halves: the second load ends this thread's use of the
+        // dP / dQ columns, which are then handed back before the last reductions
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lb + TM_DP + c * 32, v[c]);
-        tmem_ld_wait();
-        fence_before();
-        mbar_arrive(&sm.dq_drained);
-        if (q < nvq) {
-          float* dst = P.dQacc + (bh * P.Np + static_cast<long long>(i) * kS + q) * kD;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[2][32];
+          tmem_ld32(tmem + lb + TM_DP + hh * 64, v[0]);
+          tmem_ld32(tmem + lb + TM_DP + hh * 64 + 32, v[1]);
+          tmem_ld_wait();
+          if (hh == 1) {
+            fence_before();
+            mbar_arrive(&sm.dq_drained);
+          }
+          if (real) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4(dst + c * 32 + e, __uint_as_float(v[c][e]), __uint_as_float(v[c][e + 1]),
-                         __uint_as_float(v[c][e + 2]), __uint_as_float(v[c][e + 3]));
+              for (int e = 0; e < 32; e += 4)
+                red_add_v4(dst + hh * 64 + c * 32 + e, __uint_as_float(v[c][e]),
+                           __uint_as_float(v[c][e + 1]), __uint_as_float(v[c][e + 2]),
+                           __uint_as_float(v[c][e + 3]));
+          }
         }
       }
       if (!ok) break;
