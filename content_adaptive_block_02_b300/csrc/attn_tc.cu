@@ -261,9 +261,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t pv_base = pidx;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
+      const int32_t* nvb = P.n_valid + bh * P.nb;
+      int nvk_next = nvb[P.col_idx[beg]];
       for (int jj = 0; jj < n; ++jj) {
-        const int j = P.col_idx[beg + jj];
-        const int nvk = P.n_valid[bh * P.nb + j];
+        const int nvk = nvk_next;
+        if (jj + 1 < n) nvk_next = nvb[P.col_idx[beg + jj + 1]];  // ahead of its use
         const int lim = nvk - c0;  // columns of this half that hold real keys
         if (!W.wait(&sm.s_full, sidx & 1, 11)) { ok = false; break; }
         fence_after();

@@ -422,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------ dQ drain ----
-    const int q = threadIdx.x - 256;  // query row == TMEM lane
-    const uint32_t lb = static_cast<uint32_t>((warp - 8) * 32) << 16;
+    const int qw = warp - 8;  // TMEM lane quarter of this warp (query rows 32qw..)
+    const uint32_t lb = static_cast<uint32_t>(qw * 32) << 16;
     uint32_t dqcnt = 0;
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
@@ -433,34 +433,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg;
       const long long bh = col / P.nb;
       bool ok = true;
+      int i_next = n > 0 ? P.row_idx[beg] : 0;
+      int nvq_next = n > 0 ? P.n_valid[bh * P.nb + i_next] : 0;
       for (int k = 0; k < n; ++k) {
-        const int i = P.row_idx[beg + k];
-        const int nvq = P.n_valid[bh * P.nb + i];
+        const int i = i_next, nvq = nvq_next;
+        if (k + 1 < n) {  // ahead of its use
+          i_next = P.row_idx[beg + k + 1];
+          nvq_next = P.n_valid[bh * P.nb + i_next];
+        }
         if (!W.wait(&sm.dq_full, dqcnt & 1, 52)) { ok = false; break; }
         ++dqcnt;
         fence_after();
-        float* dst = P.dQacc + (bh * P.Np + static_cast<long long>(i) * kS + q) * kD;
-        const bool real = q < nvq;
-        // two columns halves: the second load ends this thread's use of the
-        // dP / dQ columns, which are then handed back before the last reductions
+        // 16-lane halves of this warp's quarter in the 16x256b shape: four
+        // consecutive threads hold one 32-byte run of a row, so every v2
+        // reduction of a warp covers whole sectors
+        float* tile = P.dQacc + (bh * P.Np + static_cast<long long>(i) * kS) * kD;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v[2][32];
-          tmem_ld32(tmem + lb + TM_DP + hh * 64, v[0]);
-          tmem_ld32(tmem + lb + TM_DP + hh * 64 + 32, v[1]);
+          uint32_t v[64];
+          tmem_ld_16x256b_x16(tmem + lb + (static_cast<uint32_t>(hh * 16) << 16) + TM_DP, v);
           tmem_ld_wait();
           if (hh == 1) {
             fence_before();
             mbar_arrive(&sm.dq_drained);
           }
-          if (real) {
+          const int ra = qw * 32 + hh * 16 + (lane >> 2), rb = ra + 8;
+          const int cc = 2 * (lane & 3);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                red_add_v4(dst + hh * 64 + c * 32 + e, __uint_as_float(v[c][e]),
-                           __uint_as_float(v[c][e + 1]), __uint_as_float(v[c][e + 2]),
-                           __uint_as_float(v[c][e + 3]));
+          for (int k = 0; k < 16; ++k) {
+            if (ra < nvq)
+              red_add_v2(tile + ra * kD + 8 * k + cc, __uint_as_float(v[4 * k]),
+                         __uint_as_float(v[4 * k + 1]));
+            if (rb < nvq)
+              red_add_v2(tile + rb * kD + 8 * k + cc, __uint_as_float(v[4 * k + 2]),
+                         __uint_as_float(v[4 * k + 3]));
           }
         }
       }
