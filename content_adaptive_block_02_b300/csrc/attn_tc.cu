@@ -6,16 +6,20 @@
 // the key blocks selected for it.  Reading used here: exact softmax over the
 // real tokens of the selected key blocks, scale `scale`, natural-log LSE.
 //
-// Design (one persistent CTA per SM, 320 threads, warp-specialised):
+// Design (one persistent CTA per SM, 352 threads, warp-specialised):
 //   warp 8  producer: takes the next query block from a global work counter,
 //           publishes it in a 2-slot work ring, and streams the K and V tiles
-//           of its selected key blocks into two 3-stage shared-memory rings
-//           with TMA (128-byte swizzle, 2 boxes of 64 x 128 per tile).
-//   warp 9  MMA issuer (one thread): S = Q K^T with Q held in tensor memory
-//           (A from TMEM, B = K tile from smem), then O += P V with P in
-//           tensor memory (A from TMEM, B = V tile, MN-major).  Order per
-//           query block: S_0, S_1, PV_0, S_2, PV_1, ... so the next score tile
-//           is on the tensor pipe while the softmax warps work on this one.
+//           of its selected key blocks into a 3-stage shared-memory ring (one
+//           K + V pair per stage) with TMA (128-byte swizzle, 2 boxes of
+//           64 x 128 per tile).
+//   warp 9  S issuer (one thread): S = Q K^T with Q held in tensor memory
+//           (A from TMEM, B = K tile from smem), as soon as the softmax warps
+//           have read the previous S tile, so the next score tile is on the
+//           tensor pipe while they work on this one.
+//   warp 10 PV issuer (one thread): O += P V with P in tensor memory (A from
+//           TMEM, B = V tile, MN-major).  Two issuing threads keep the tensor
+//           pipe fed: a tcgen05.mma issue blocks while the pipe's queue is full,
+//           and each issuer's barrier waits overlap the other's MMAs.
 //   warps 0-7  softmax, two warpgroups: warps w and w+4 share the query rows
 //           of TMEM lane quarter w%4 (thread = query row) and split the 128
 //           key columns (and the 128 O columns) in halves.  Per key block: the
@@ -40,17 +44,18 @@ constexpr int kS = 128;
 constexpr int kD = 128;
 constexpr int kTile = kS * kD * 2;  // 32 KB
 constexpr int kStages = 3;
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_Q = 256, TM_P0 = 320, TM_P1 = 384;
 
 struct FwdShared {
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full, s_free, p_full[2], o_full, q_ready, final_bar;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full, s_free, p_full[2], p_empty[2], q_ready, final_bar;
   uint64_t work_full[2], work_empty[2];
   int work_row[2], work_beg[2], work_end[2], work_nvq[2];
   float xmax[2][2][128];  // [tile parity][column half][row]: half-row maxima
   float xsum[2][128];     // [column half][row]: half-row sums at the end
+  int xok[2][2][4];       // [exchange parity][column half][lane quarter]: still on track
   uint32_t tmem_base;
   int abort;
 };
@@ -77,27 +82,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __shared__ FwdShared sm;
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* kbuf = dsm;
-  uint8_t* vbuf = dsm + kStages * kTile;
+  uint8_t* kvbuf = dsm;  // stage s: K at s * 2 * kTile, V right after
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
-      mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 2);  // released by the S and the PV issuer
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, kSoftmaxThreads);
     mbar_init(&sm.p_full[0], kSoftmaxThreads);
     mbar_init(&sm.p_full[1], kSoftmaxThreads);
-    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.p_empty[0], 1);
+    mbar_init(&sm.p_empty[1], 1);
     mbar_init(&sm.q_ready, kSoftmaxThreads);
-    mbar_init(&sm.final_bar, 1);
+    mbar_init(&sm.final_bar, 2);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.work_full[s], 1);
-      mbar_init(&sm.work_empty[s], 1 + kSoftmaxThreads);
+      mbar_init(&sm.work_empty[s], 2 + kSoftmaxThreads);
     }
     sm.abort = 0;
     mbar_init_fence();
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t kuse = 0, vuse = 0;
+      uint32_t use = 0;
       for (uint32_t it = 0;; ++it) {
         const int ws = it & 1;
         if (!W.wait(&sm.work_empty[ws], ((it >> 1) & 1) ^ 1, 1)) break;
@@ -135,80 +138,92 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (nvq == 0) continue;
         const long long bh = row / P.nb;
         bool ok = true;
-        for (int t = beg; t < end && ok; ++t) {
+        for (int t = beg; t < end; ++t) {
           const int j = P.col_idx[t];
           const int y = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
-          const int ks = kuse % kStages;
-          if (!W.wait(&sm.k_empty[ks], ((kuse / kStages) & 1) ^ 1, 2)) { ok = false; break; }
-          mbar_expect_tx(&sm.k_full[ks], kTile);
-          tma_load_2d(kbuf + ks * kTile, &tmK, &sm.k_full[ks], 0, y);
-          tma_load_2d(kbuf + ks * kTile + kTile / 2, &tmK, &sm.k_full[ks], 64, y);
-          ++kuse;
-          const int vs = vuse % kStages;
-          if (!W.wait(&sm.v_empty[vs], ((vuse / kStages) & 1) ^ 1, 3)) { ok = false; break; }
-          mbar_expect_tx(&sm.v_full[vs], kTile);
-          tma_load_2d(vbuf + vs * kTile, &tmV, &sm.v_full[vs], 0, y);
-          tma_load_2d(vbuf + vs * kTile + kTile / 2, &tmV, &sm.v_full[vs], 64, y);
-          ++vuse;
+          const int st = use % kStages;
+          if (!W.wait(&sm.kv_empty[st], ((use / kStages) & 1) ^ 1, 2)) { ok = false; break; }
+          uint8_t* kb = kvbuf + st * 2 * kTile;
+          mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
+          tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
+          tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
+          tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
+          tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+          ++use;
         }
         if (!ok) break;
       }
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ------------------------------------------------------ MMA issuer ----
+    // ------------------------------------------------------ S issuer ----
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);   // A = Q (TMEM), B = K, K-major
-      constexpr uint32_t idPV = idesc_bf16(128, 128, 0, 1);  // A = P (TMEM), B = V, MN-major
-      uint32_t kuse = 0, vuse = 0, sidx = 0, pidx = 0, qcnt = 0;
+      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);  // A = Q (TMEM), B = K, K-major
+      uint32_t use = 0, sidx = 0, qcnt = 0;
       bool ok = true;
-      auto issue_pv = [&](bool first) -> bool {
-        const uint32_t pb = pidx & 1;
-        if (!W.wait(&sm.p_full[pb], (pidx >> 1) & 1, 7)) return false;
-        const int vs = vuse % kStages;
-        if (!W.wait(&sm.v_full[vs], (vuse / kStages) & 1, 8)) return false;
-        fence_after();
-        const uint32_t vb = smem_u32(vbuf + vs * kTile);
-        const uint32_t pa = tmem + (pb ? TM_P1 : TM_P0);
-#pragma unroll
-        for (int kk = 0; kk < kS / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, kTile / 2, 1024);
-          mma_ts(tmem + TM_O, pa + kk * 8, bd, idPV, (!first || kk > 0) ? 1u : 0u);
-        }
-        commit(&sm.o_full);
-        commit(&sm.v_empty[vs]);
-        ++vuse;
-        ++pidx;
-        return true;
-      };
       for (uint32_t it = 0; ok; ++it) {
         const int ws = it & 1;
         if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 4)) break;
-        const int row = sm.work_row[ws];
-        if (row < 0) break;
+        if (sm.work_row[ws] < 0) break;
         const int n = sm.work_end[ws] - sm.work_beg[ws];
         if (n > 0) {
           if (!W.wait(&sm.q_ready, qcnt & 1, 5)) break;
           ++qcnt;
-          fence_after();
-          for (int jj = 0; jj < n && ok; ++jj) {
+          for (int jj = 0; jj < n; ++jj) {
             if (jj > 0 && !W.wait(&sm.s_free, (sidx - 1) & 1, 6)) { ok = false; break; }
-            const int ks = kuse % kStages;
-            if (!W.wait(&sm.k_full[ks], (kuse / kStages) & 1, 9)) { ok = false; break; }
+            const int st = use % kStages;
+            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 9)) { ok = false; break; }
             fence_after();
-            const uint32_t kb = smem_u32(kbuf + ks * kTile);
+            const uint64_t kd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile), 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint64_t bd = sdesc_sw128(kb + (kk >> 2) * (kTile / 2) + (kk & 3) * 32, 16, 1024);
-              mma_ts(tmem + TM_S, tmem + TM_Q + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ts(tmem + TM_S, tmem + TM_Q + kk * 8,
+                     kd + static_cast<uint64_t>(((kk >> 2) * (kTile / 2) + (kk & 3) * 32) >> 4), idS,
+                     kk > 0 ? 1u : 0u);
             commit(&sm.s_full);
-            commit(&sm.k_empty[ks]);
-            ++kuse;
+            commit(&sm.kv_empty[st]);
+            ++use;
             ++sidx;
-            if (jj > 0 && !issue_pv(jj == 1)) { ok = false; break; }
           }
-          if (ok && !issue_pv(n == 1)) ok = false;
+        }
+        if (ok) mbar_arrive(&sm.work_empty[ws]);
+      }
+      commit(&sm.final_bar);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------ PV issuer ----
+    if (lane == 0) {
+      constexpr uint32_t idPV = idesc_bf16(128, 128, 0, 1);  // A = P (TMEM), B = V, MN-major
+      uint32_t use = 0, pidx = 0, qcnt = 0;
+      bool ok = true;
+      for (uint32_t it = 0; ok; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 14)) break;
+        if (sm.work_row[ws] < 0) break;
+        const int n = sm.work_end[ws] - sm.work_beg[ws];
+        if (n > 0) {
+          // the first PV overwrites O: the previous block's epilogue has read it
+          if (!W.wait(&sm.q_ready, qcnt & 1, 15)) break;
+          ++qcnt;
+          for (int jj = 0; jj < n; ++jj) {
+            const uint32_t pb = pidx & 1;
+            if (!W.wait(&sm.p_full[pb], (pidx >> 1) & 1, 7)) { ok = false; break; }
+            const int st = use % kStages;
+            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 8)) { ok = false; break; }
+            fence_after();
+            const uint64_t vd =
+                sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile + kTile), kTile / 2, 1024);
+            const uint32_t pa = tmem + (pb ? TM_P1 : TM_P0);
+#pragma unroll
+            for (int kk = 0; kk < kS / 16; ++kk)
+              mma_ts(tmem + TM_O, pa + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idPV,
+                     (jj > 0 || kk > 0) ? 1u : 0u);
+            commit(&sm.p_empty[pb]);
+            commit(&sm.kv_empty[st]);
+            ++use;
+            ++pidx;
+          }
         }
         if (ok) mbar_arrive(&sm.work_empty[ws]);
       }
@@ -217,19 +232,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------ softmax ----
+    // Warps w and w+4 meet at a named barrier (64 threads) once per key block
+    // and twice per query block.  A named barrier has no time limit, so the
+    // two never leave a loop on their own: every bounded wait only clears
+    // `ok`, the flags are exchanged at each meeting, and both warps leave
+    // together at the first meeting after either of them failed.
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;  // query row of the block == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + TM_S + half * 64;
     const uint32_t tO = tmem + lane_base + TM_O + half * 64;
     const int c0 = half * 64;  // first key column (and O column) of this half
-    auto pair_sync = [&]() {
+    uint32_t xpar = 0;         // parity of the flag slots of the next meeting
+    auto meet = [&](bool mine) -> bool {  // pair barrier, returns both flags ANDed
+      const int slot = xpar & 1;
+      ++xpar;
+      if (lane == 0) sm.xok[slot][half][quarter] = mine ? 1 : 0;
       asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+      return mine && sm.xok[slot][half ^ 1][quarter] != 0;
+    };
+    // wait until the PV that used P buffer (g & 1) for key block g is done
+    auto pv_done = [&](uint32_t g, uint32_t where) {
+      return W.wait(&sm.p_empty[g & 1], (g >> 1) & 1, where);
     };
     uint32_t sidx = 0, pidx = 0, tile = 0;
+    bool ok = true;
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
-      if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 10)) break;
+      ok = meet(ok && W.wait(&sm.work_full[ws], (it >> 1) & 1, 10));
+      if (!ok) break;
       const int row = sm.work_row[ws];
       if (row < 0) break;
       const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg, nvq = sm.work_nvq[ws];
@@ -258,59 +289,61 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         fence_before();
         mbar_arrive(&sm.q_ready);
       }
-      const uint32_t pv_base = pidx;
       float m = -INFINITY, l = 0.f;
-      bool ok = true;
       const int32_t* nvb = P.n_valid + bh * P.nb;
       int nvk_next = nvb[P.col_idx[beg]];
       for (int jj = 0; jj < n; ++jj) {
         const int nvk = nvk_next;
         if (jj + 1 < n) nvk_next = nvb[P.col_idx[beg + jj + 1]];  // ahead of its use
         const int lim = nvk - c0;  // columns of this half that hold real keys
-        if (!W.wait(&sm.s_full, sidx & 1, 11)) { ok = false; break; }
-        fence_after();
+        ok = ok && W.wait(&sm.s_full, sidx & 1, 11);
         uint32_t s[2][32];
-        tmem_ld32(tS, s[0]);
-        tmem_ld32(tS + 32, s[1]);
-        tmem_ld_wait();
-        fence_before();
-        mbar_arrive(&sm.s_free);
-        ++sidx;
         float mx = -INFINITY;
-        if (lim >= 64) {
+        if (ok) {
+          fence_after();
+          tmem_ld32(tS, s[0]);
+          tmem_ld32(tS + 32, s[1]);
+          tmem_ld_wait();
+          fence_before();
+          mbar_arrive(&sm.s_free);
+          if (lim >= 64) {
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
-        } else {
+              for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+          } else {
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+              for (int e = 0; e < 32; ++e)
+                if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+          }
         }
+        ++sidx;
         const int par = tile & 1;
         ++tile;
         sm.xmax[par][half][r] = mx;
-        pair_sync();
+        ok = meet(ok);
+        if (!ok) break;
         mx = fmaxf(mx, sm.xmax[par][half ^ 1][r]) * P.scale_log2;
         const bool resc = mx > m + 8.f;
         const float m_new = resc ? mx : m;
         const float corr = resc ? ex2(m - m_new) : 1.f;
         if (jj > 0 && __any_sync(0xffffffffu, resc)) {
-          const uint32_t g = pv_base + jj - 1;  // PV of the previous key block
-          if (!W.wait(&sm.o_full, g & 1, 12)) { ok = false; break; }
-          fence_after();
+          ok = ok && pv_done(pidx - 1, 12);  // the previous key block's PV
+          if (ok) {
+            fence_after();
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait();
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-            tmem_st32(tO + c * 32, o);
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+              tmem_st32(tO + c * 32, o);
+            }
+            tmem_st_wait();
           }
-          tmem_st_wait();
         }
         l *= corr;
         m = m_new;
@@ -335,40 +368,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             pk[e] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st32(tmem + lane_base + ((pidx & 1) ? TM_P1 : TM_P0) + half * 32, pk);
         l += lsum;
-        tmem_st_wait();
-        fence_before();
-        mbar_arrive(&sm.p_full[pidx & 1]);
+        // the PV issued two key blocks ago has finished reading this P buffer
+        if (pidx >= 2) ok = ok && pv_done(pidx - 2, 16);
+        if (ok) {
+          fence_after();
+          tmem_st32(tmem + lane_base + ((pidx & 1) ? TM_P1 : TM_P0) + half * 32, pk);
+          tmem_st_wait();
+          fence_before();
+          mbar_arrive(&sm.p_full[pidx & 1]);
+        }
         ++pidx;
       }
-      if (!ok) break;
       // epilogue: row sum over both halves, wait for the last PV, write the row
       sm.xsum[half][r] = l;
-      pair_sync();
+      ok = meet(ok);
+      if (!ok) break;
       const float lt = sm.xsum[0][r] + sm.xsum[1][r];
-      if (!W.wait(&sm.o_full, (pidx - 1) & 1, 13)) break;
-      fence_after();
-      const bool real = r < nvq;
-      const float inv = real ? 1.f / lt : 0.f;
+      ok = ok && pv_done(pidx - 1, 13);
+      if (ok) {
+        fence_after();
+        const bool real = r < nvq;
+        const float inv = real ? 1.f / lt : 0.f;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        tmem_ld_wait();
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-          orow[c * 4 + q] = v;
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            orow[c * 4 + q] = v;
+          }
         }
+        if (half == 0) P.lse[grow] = real ? (m + log2f(lt)) * 0.69314718055994531f : 0.f;
       }
-      if (half == 0) P.lse[grow] = real ? (m + log2f(lt)) * 0.69314718055994531f : 0.f;
       // both halves have read xsum before either writes it for the next block
-      pair_sync();
+      ok = meet(ok);
+      if (!ok) break;
       fence_before();
       mbar_arrive(&sm.work_empty[ws]);
     }
@@ -449,7 +490,7 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
   cudaError_t e = cudaMemsetAsync(a.status + WS_FWD_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  const size_t smem = 2ull * kStages * kTile + 1024;
+  const size_t smem = 2ull * kStages * kTile + 1024;  // K + V per stage
   e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -54,6 +54,7 @@ struct BwdBars {
   uint64_t work_full[2], work_empty[2];
   int work_col[2], work_beg[2], work_end[2], work_nvk[2];
   int stage_i[2], stage_nvq[2];  // query block of each Q / dO stage and its real rows
+  int xok[2][2][4];  // [meeting parity][column half][lane quarter]: still on track
   uint32_t tmem_base;
   int abort;
 };
@@ -293,13 +294,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // key row == TMEM lane
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
     const int q0 = half * 64;  // first query column (and first channel) of this half
-    auto pair_sync = [&]() {
+    // Warps w and w+4 meet at a named barrier (64 threads) once per query
+    // block and once per work item.  A named barrier has no time limit, so
+    // the two never leave a loop on their own: every bounded wait only clears
+    // `ok`, the flags are exchanged at each meeting, and both warps leave
+    // together at the first meeting after either of them failed.
+    uint32_t xpar = 0;
+    auto meet = [&](bool mine) -> bool {
+      const int slot = xpar & 1;
+      ++xpar;
+      if (lane == 0) sm.xok[slot][half][quarter] = mine ? 1 : 0;
       asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+      return mine && sm.xok[slot][half ^ 1][quarter] != 0;
     };
     uint32_t use = 0, scnt = 0, dpcnt = 0, dsidx = 0, kvcnt = 0;
+    bool ok = true;
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
-      if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 41)) break;
+      ok = meet(ok && W.wait(&sm.work_full[ws], (it >> 1) & 1, 41));
+      if (!ok) break;
       const int col = sm.work_col[ws];
       if (col < 0) break;
       const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg, nvk = sm.work_nvk[ws];
@@ -314,38 +327,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sm.work_empty[ws]);
         continue;
       }
-      bool ok = true;
       for (int k = 0; k < n; ++k) {
         const int s_ = (use + k) & 1;
-        if (!W.wait(&sm.qdo_full[s_], ((use + k) >> 1) & 1, 40)) { ok = false; break; }
+        // LSE_i and D_i arrive with Q_i / dO_i on the stage's barrier
+        ok = ok && W.wait(&sm.qdo_full[s_], ((use + k) >> 1) & 1, 40);
         const int lim = (r < nvk) ? sm.stage_nvq[s_] - q0 : 0;  // real query columns here
         const float4* lse4 = reinterpret_cast<const float4*>(stage(s_) + 2 * kTile) + half * 16;
         const float4* D4 = lse4 + 32;
         // ---- P^T = exp(S^T * scale - LSE) on this half of the queries ----
-        if (!W.wait(&sm.s_full, scnt & 1, 42)) { ok = false; break; }
+        ok = ok && W.wait(&sm.s_full, scnt & 1, 42);
         ++scnt;
-        fence_after();
         float p[64];
+        if (ok) {
+          fence_after();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32];
-          tmem_ld32(tmem + lb + TM_S + q0 + c * 32, sv);
-          tmem_ld_wait();
+          for (int c = 0; c < 2; ++c) {
+            uint32_t sv[32];
+            tmem_ld32(tmem + lb + TM_S + q0 + c * 32, sv);
+            tmem_ld_wait();
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const float4 L = lse4[c * 8 + g];
-            const float lv[4] = {L.x, L.y, L.z, L.w};
+            for (int g = 0; g < 8; ++g) {
+              const float4 L = lse4[c * 8 + g];
+              const float lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int q = c * 32 + g * 4 + e;
-              const float x = fmaf(__uint_as_float(sv[g * 4 + e]), P.scale_log2,
-                                   -lv[e] * 1.4426950408889634f);
-              p[q] = q < lim ? ex2(x) : 0.f;
+              for (int e = 0; e < 4; ++e) {
+                const int q = c * 32 + g * 4 + e;
+                const float x = fmaf(__uint_as_float(sv[g * 4 + e]), P.scale_log2,
+                                     -lv[e] * 1.4426950408889634f);
+                p[q] = q < lim ? ex2(x) : 0.f;
+              }
             }
           }
         }
         // both halves have read S^T before P^T (half as wide) is written over it
-        pair_sync();
+        ok = meet(ok);
+        if (!ok) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[16];
@@ -357,43 +373,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_before();
         mbar_arrive(&sm.p_ready);
         // ---- dS^T = P^T * (dP^T - D) -> smem panel `half` (128-byte swizzle) ----
-        if (!W.wait(&sm.dp_full, dpcnt & 1, 43)) { ok = false; break; }
+        ok = ok && W.wait(&sm.dp_full, dpcnt & 1, 43);
         ++dpcnt;
-        if (dsidx > 0 && !W.wait(&sm.ds_empty, (dsidx - 1) & 1, 44)) { ok = false; break; }
+        if (dsidx > 0) ok = ok && W.wait(&sm.ds_empty, (dsidx - 1) & 1, 44);
         ++dsidx;
-        fence_after();
+        if (ok) {
+          fence_after();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t dp[32];
-          tmem_ld32(tmem + lb + TM_DP + q0 + c * 32, dp);
-          tmem_ld_wait();
+          for (int c = 0; c < 2; ++c) {
+            uint32_t dp[32];
+            tmem_ld32(tmem + lb + TM_DP + q0 + c * 32, dp);
+            tmem_ld_wait();
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
-            const int ql = c * 32 + g * 8;  // local query index in this half
-            const float4 da = D4[ql / 4], db4 = D4[ql / 4 + 1];
-            const float dv[8] = {da.x, da.y, da.z, da.w, db4.x, db4.y, db4.z, db4.w};
-            uint32_t w4[4];
+            for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
+              const int ql = c * 32 + g * 8;  // local query index in this half
+              const float4 da = D4[ql / 4], db4 = D4[ql / 4 + 1];
+              const float dv[8] = {da.x, da.y, da.z, da.w, db4.x, db4.y, db4.z, db4.w};
+              uint32_t w4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float x0 = p[ql + 2 * e] * (__uint_as_float(dp[g * 8 + 2 * e]) - dv[2 * e]);
-              const float x1 =
-                  p[ql + 2 * e + 1] * (__uint_as_float(dp[g * 8 + 2 * e + 1]) - dv[2 * e + 1]);
-              w4[e] = pack_bf16x2(x0, x1);
+              for (int e = 0; e < 4; ++e) {
+                const float x0 = p[ql + 2 * e] * (__uint_as_float(dp[g * 8 + 2 * e]) - dv[2 * e]);
+                const float x1 =
+                    p[ql + 2 * e + 1] * (__uint_as_float(dp[g * 8 + 2 * e + 1]) - dv[2 * e + 1]);
+                w4[e] = pack_bf16x2(x0, x1);
+              }
+              const int chunk = ql >> 3;
+              const uint32_t off = half * (kTile / 2) + r * 128 + ((chunk ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            const int chunk = ql >> 3;
-            const uint32_t off = half * (kTile / 2) + r * 128 + ((chunk ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
+          fence_proxy_async();
+          fence_before();
+          mbar_arrive(&sm.ds_ready);
         }
-        fence_proxy_async();
-        fence_before();
-        mbar_arrive(&sm.ds_ready);
       }
-      if (!ok) break;
+      // a failure in the last query block is caught at the next meeting
       use += n;
       // ---- epilogue: dV, dK * scale -> bf16, this half of the channels ----
-      if (!W.wait(&sm.kv_done, kvcnt & 1, 45)) break;
+      ok = ok && W.wait(&sm.kv_done, kvcnt & 1, 45);
       ++kvcnt;
+      if (!ok) continue;  // both halves leave at the next meeting
       fence_after();
       const bool real = r < nvk;
 #pragma unroll

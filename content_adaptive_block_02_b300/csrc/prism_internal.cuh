@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/prism.h"
+#include "prism.h"
 
 namespace prism {
 
