@@ -27,10 +27,12 @@
 //   warp 12    producer: work counter, TMA loads of K_j, V_j (once per item)
 //              and of Q_i, dO_i, LSE_i, D_i (2-stage ring) plus the stage's
 //              query-block index and real-token count.
-//   warp 13    MMA issuer.  Tensor-pipe order per step i (steady state):
-//              4_i 5_i | 3_{i+1} | 2_{i+1} | 1_{i+2}
-//              so the P / dS work of the compute warps and the dQ drain both
-//              overlap tensor work.
+//   warp 13    issuer A: (1) and (3), which share the S/P columns, in the
+//              order 1_0 3_0 1_1 3_1 ...
+//   warp 14    issuer B: (2), (5), (4) in the order 2_0 5_0 4_0 2_1 5_1 4_1 ...
+//              (dQ first, so that the drain starts while dK is computed).
+//   A tcgen05.mma issue blocks while the tensor pipe's queue is full; with two
+//   issuing threads, one thread's barrier waits overlap the other's MMAs.
 // Tensor memory: S/P [0,128), dP/dQ [128,256), dV [256,384), dK [384,512).
 #include "tc_common.cuh"
 
@@ -41,7 +43,7 @@ using namespace tc;
 constexpr int kS = 128, kD = 128;
 constexpr int kTile = kS * kD * 2;           // 32 KB
 constexpr int kStage = 2 * kTile + 1024;     // Q, dO, LSE (512 B), D (512 B)
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kCompute = 256;
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
 constexpr int kOffV = kTile, kOffStage = 2 * kTile, kOffDS = 2 * kTile + 2 * kStage;
@@ -93,12 +95,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
-    mbar_init(&sm.kv_empty, 1);
+    mbar_init(&sm.kv_empty, 2);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.qdo_full[s], 1);
-      mbar_init(&sm.qdo_empty[s], 1);
+      mbar_init(&sm.qdo_empty[s], 2);  // issuers A and B
       mbar_init(&sm.work_full[s], 1);
-      mbar_init(&sm.work_empty[s], 1 + kCompute + 128);
+      mbar_init(&sm.work_empty[s], 2 + kCompute + 128);
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
@@ -107,9 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.ds_empty, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_drained, 128);
-    mbar_init(&sm.kv_done, 1);
+    mbar_init(&sm.kv_done, 2);
     mbar_init(&sm.kv_free, kCompute);
-    mbar_init(&sm.final_bar, 1);
+    mbar_init(&sm.final_bar, 2);
     sm.abort = 0;
     mbar_init_fence();
   }
@@ -179,29 +181,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 13) {
-    // ------------------------------------------------------ MMA issuer ----
+  } else if (warp == 13 || warp == 14) {
+    // ------------------------------------------------------ MMA issuers ----
     if (lane == 0) {
+      const bool is_a = warp == 13;
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // A K-major, B K-major
       constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // A K-major, B MN-major
       constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // A MN-major, B MN-major
-      const uint32_t kb = smem_u32(kbuf), vb = smem_u32(vbuf), db = smem_u32(dsbuf);
+      const uint64_t kd_k = sdesc_sw128(smem_u32(kbuf), 16, 1024);          // K, K-major
+      const uint64_t vd_k = sdesc_sw128(smem_u32(vbuf), 16, 1024);          // V, K-major
+      const uint64_t kd_n = sdesc_sw128(smem_u32(kbuf), kTile / 2, 1024);   // K, MN-major
+      const uint64_t dsd_k = sdesc_sw128(smem_u32(dsbuf), 16, 1024);        // dS^T, K-major
+      const uint64_t dsd_n = sdesc_sw128(smem_u32(dsbuf), kTile / 2, 1024); // dS, MN-major
+      auto koff = [](int kk) {  // K-major 16-element step inside two 64-column panels
+        return static_cast<uint64_t>(((kk >> 2) * (kTile / 2) + (kk & 3) * 32) >> 4);
+      };
+      auto noff = [](int kk) {  // MN-major 16-row step
+        return static_cast<uint64_t>((kk * 2048) >> 4);
+      };
       uint32_t use = 0, items = 0, pcnt = 0, dscnt = 0, dqcnt = 0, kvcnt = 0;
       bool ok = true;
-      // (1) and (2): K-major A (key rows) times K-major B (query rows)
-      auto mma_kt = [&](uint32_t a_base, uint32_t b_base, uint32_t d) {
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile / 2) + (kk & 3) * 32;
-          mma_ss(tmem + d, sdesc_sw128(a_base + off, 16, 1024),
-                 sdesc_sw128(b_base + off, 16, 1024), id_kk, kk > 0 ? 1u : 0u);
-        }
-      };
       for (uint32_t it = 0; ok; ++it) {
         const int ws = it & 1;
         if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 31)) break;
-        const int col = sm.work_col[ws];
-        if (col < 0) break;
+        if (sm.work_col[ws] < 0) break;
         const int n = sm.work_end[ws] - sm.work_beg[ws];
         if (n > 0) {
           if (!W.wait(&sm.kv_full, items & 1, 32)) break;
@@ -209,76 +212,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the previous item's dK / dV have been read out
           if (kvcnt > 0 && !W.wait(&sm.kv_free, (kvcnt - 1) & 1, 33)) break;
           fence_after();
-          const uint32_t u0 = use;
-          auto st_q = [&](uint32_t k) { return smem_u32(stage((u0 + k) & 1)); };
-          auto wait_qdo = [&](uint32_t k) {
-            return W.wait(&sm.qdo_full[(u0 + k) & 1], ((u0 + k) >> 1) & 1, 34);
-          };
-          // prologue: 1_0, 2_0, 3_0, 1_1
-          if (!wait_qdo(0)) break;
-          fence_after();
-          mma_kt(kb, st_q(0), TM_S);
-          commit(&sm.s_full);
-          // the dP region may still hold the previous item's last dQ tile
-          if (dqcnt > 0 && !W.wait(&sm.dq_drained, (dqcnt - 1) & 1, 35)) break;
-          fence_after();
-          mma_kt(vb, st_q(0) + kTile, TM_DP);
-          commit(&sm.dp_full);
-          auto issue_dv = [&](uint32_t k) -> bool {
-            if (!W.wait(&sm.p_ready, pcnt & 1, 36)) return false;
-            ++pcnt;
+          for (int k = 0; k < n; ++k) {
+            const int st = (use + k) & 1;
+            if (!W.wait(&sm.qdo_full[st], ((use + k) >> 1) & 1, 34)) { ok = false; break; }
             fence_after();
-            const uint32_t dob = st_q(k) + kTile;
+            const uint64_t qd_k = sdesc_sw128(smem_u32(stage(st)), 16, 1024);
+            const uint64_t qd_n = sdesc_sw128(smem_u32(stage(st)), kTile / 2, 1024);
+            const uint64_t dod_k = sdesc_sw128(smem_u32(stage(st) + kTile), 16, 1024);
+            const uint64_t dod_n = sdesc_sw128(smem_u32(stage(st) + kTile), kTile / 2, 1024);
+            if (is_a) {
+              // (1) S^T = K Q^T
 #pragma unroll
-            for (int kk = 0; kk < kS / 16; ++kk)
-              mma_ts(tmem + TM_DV, tmem + TM_S + kk * 8, sdesc_sw128(dob + kk * 2048, kTile / 2, 1024),
-                     id_kn, (k > 0 || kk > 0) ? 1u : 0u);
-            return true;
-          };
-          if (!issue_dv(0)) break;
-          if (n > 1) {
-            if (!wait_qdo(1)) break;
-            fence_after();
-            mma_kt(kb, st_q(1), TM_S);
-            commit(&sm.s_full);
-          }
-          for (int k = 0; k < n && ok; ++k) {
-            // 4_k, 5_k
-            if (!W.wait(&sm.ds_ready, dscnt & 1, 37)) { ok = false; break; }
-            ++dscnt;
-            fence_after();
-            const uint32_t qb = st_q(k);
-#pragma unroll
-            for (int kk = 0; kk < kS / 16; ++kk) {
-              const uint32_t aoff = (kk >> 2) * (kTile / 2) + (kk & 3) * 32;
-              mma_ss(tmem + TM_DK, sdesc_sw128(db + aoff, 16, 1024),
-                     sdesc_sw128(qb + kk * 2048, kTile / 2, 1024), id_kn, (k > 0 || kk > 0) ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < kS / 16; ++kk)
-              mma_ss(tmem + TM_DP, sdesc_sw128(db + kk * 2048, kTile / 2, 1024),
-                     sdesc_sw128(kb + kk * 2048, kTile / 2, 1024), id_nn, kk > 0 ? 1u : 0u);
-            commit(&sm.dq_full);
-            commit(&sm.ds_empty);
-            commit(&sm.qdo_empty[(u0 + k) & 1]);
-            ++dqcnt;
-            if (k + 1 < n) {
-              if (!issue_dv(k + 1)) { ok = false; break; }
-              // 2_{k+1} once dQ_k has left the dP region
-              if (!W.wait(&sm.dq_drained, (dqcnt - 1) & 1, 38)) { ok = false; break; }
+              for (int kk = 0; kk < kD / 16; ++kk)
+                mma_ss(tmem + TM_S, kd_k + koff(kk), qd_k + koff(kk), id_kk, kk > 0 ? 1u : 0u);
+              commit(&sm.s_full);
+              // (3) dV += P^T dO, once P^T has replaced S^T
+              if (!W.wait(&sm.p_ready, pcnt & 1, 36)) { ok = false; break; }
+              ++pcnt;
               fence_after();
-              mma_kt(vb, st_q(k + 1) + kTile, TM_DP);
+#pragma unroll
+              for (int kk = 0; kk < kS / 16; ++kk)
+                mma_ts(tmem + TM_DV, tmem + TM_S + kk * 8, dod_n + noff(kk), id_kn,
+                       (k > 0 || kk > 0) ? 1u : 0u);
+              commit(&sm.qdo_empty[st]);
+            } else {
+              // (2) dP^T = V dO^T, once the previous dQ tile has left the dP columns
+              if (dqcnt > 0 && !W.wait(&sm.dq_drained, (dqcnt - 1) & 1, 35)) { ok = false; break; }
+              fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kD / 16; ++kk)
+                mma_ss(tmem + TM_DP, vd_k + koff(kk), dod_k + koff(kk), id_kk, kk > 0 ? 1u : 0u);
               commit(&sm.dp_full);
-              if (k + 2 < n) {
-                if (!wait_qdo(k + 2)) { ok = false; break; }
-                fence_after();
-                mma_kt(kb, st_q(k + 2), TM_S);
-                commit(&sm.s_full);
-              }
+              // (5) dQ = dS K into the dP columns, then (4) dK += dS^T Q
+              if (!W.wait(&sm.ds_ready, dscnt & 1, 37)) { ok = false; break; }
+              ++dscnt;
+              fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kS / 16; ++kk)
+                mma_ss(tmem + TM_DP, dsd_n + noff(kk), kd_n + noff(kk), id_nn, kk > 0 ? 1u : 0u);
+              commit(&sm.dq_full);
+              ++dqcnt;
+#pragma unroll
+              for (int kk = 0; kk < kS / 16; ++kk)
+                mma_ss(tmem + TM_DK, dsd_k + koff(kk), qd_n + noff(kk), id_kn,
+                       (k > 0 || kk > 0) ? 1u : 0u);
+              commit(&sm.ds_empty);
+              commit(&sm.qdo_empty[st]);
             }
           }
           if (!ok) break;
-          use = u0 + n;
+          use += n;
           commit(&sm.kv_done);
           commit(&sm.kv_empty);
           ++kvcnt;
