@@ -14,8 +14,9 @@ struct prism_plan {
 };
 
 namespace prism {
-cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp, float* D,
-                           float* dQacc, cudaStream_t st);
+cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp,
+                           const float* lse, float* D, float* lse2, float* dQacc,
+                           cudaStream_t st);
 cudaError_t launch_attn_fwd_simt(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
                                  const uint16_t* Vp, const int32_t* n_valid,
                                  const int32_t* row_ptr, const int32_t* col_idx, float scale,
@@ -29,11 +30,16 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
                                const uint16_t* Vp, const int32_t* n_valid, const int32_t* row_ptr,
                                const int32_t* col_idx, float scale, uint16_t* Op, float* lse,
                                uint8_t* ws, cudaStream_t st);
-cudaError_t launch_attn_bwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
-                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
-                               const float* D, const int32_t* n_valid, const int32_t* col_ptr,
-                               const int32_t* row_idx, float scale, float* dQacc, uint16_t* dKp,
-                               uint16_t* dVp, uint8_t* ws, cudaStream_t st);
+cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
+                                const float* D, const int32_t* n_valid, const int32_t* col_ptr,
+                                const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
+                                uint8_t* ws, cudaStream_t st);
+cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                              const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                              const float* D, const int32_t* n_valid, const int32_t* row_ptr,
+                              const int32_t* col_idx, float scale, uint16_t* dQp, uint8_t* ws,
+                              cudaStream_t st);
 }  // namespace prism
 
 namespace {
@@ -145,6 +151,7 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   p.off_bitmask = off; off = align256(off + rows * nwords * 4);
   p.off_scores = off; off = align256(off + 2 * rows * nb * 4);
   p.off_D = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
+  p.off_lse2 = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
   p.off_dq = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * c.d * 4);
   z.ws_bytes = off;
   prism_plan* h = static_cast<prism_plan*>(malloc(sizeof(prism_plan)));
@@ -269,23 +276,26 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
   PRISM_CHECK_PTR(n_valid); PRISM_CHECK_PTR(row_ptr); PRISM_CHECK_PTR(col_idx);
   PRISM_CHECK_PTR(col_ptr); PRISM_CHECK_PTR(row_idx);
   PRISM_CHECK_PTR(dQp); PRISM_CHECK_PTR(dKp); PRISM_CHECK_PTR(dVp); PRISM_CHECK_PTR(ws);
-  (void)row_ptr;
-  (void)col_idx;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Plan& p = plan->p;
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* D = reinterpret_cast<float*>(w + p.off_D);
-  float* dq = reinterpret_cast<float*>(w + p.off_dq);
-  PRISM_CUDA(prism::launch_bwd_pre(p, Op, dOp, D, dq, st));
   if (p.sz.tensor_core_bwd) {
-    PRISM_CUDA(prism::launch_attn_bwd_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx,
-                                         scale, dq, dKp, dVp, w, st));
+    // dK, dV over the key blocks' lists; dQ over the query blocks' lists
+    float* lse2 = reinterpret_cast<float*>(w + p.off_lse2);
+    PRISM_CUDA(prism::launch_bwd_pre(p, Op, dOp, lse, D, lse2, nullptr, st));
+    PRISM_CUDA(prism::launch_attn_dkdv_tc(p, Qp, Kp, Vp, dOp, lse2, D, n_valid, col_ptr, row_idx,
+                                          scale, dKp, dVp, w, st));
+    PRISM_CUDA(prism::launch_attn_dq_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx,
+                                        scale, dQp, w, st));
   } else {
+    float* dq = reinterpret_cast<float*>(w + p.off_dq);
+    PRISM_CUDA(prism::launch_bwd_pre(p, Op, dOp, lse, D, nullptr, dq, st));
     PRISM_CUDA(prism::launch_attn_bwd_simt(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx,
                                            scale, dq, dKp, dVp, st));
+    // dQ in block order, bf16, scaled
+    PRISM_CUDA(prism::launch_dq_convert(p, dq, scale, dQp, st));
   }
-  // dQ in block order, bf16, scaled
-  PRISM_CUDA(prism::launch_dq_convert(p, dq, scale, dQp, st));
   return PRISM_OK;
 }
 

@@ -223,10 +223,12 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
 
 }  // namespace
 
-// D[b,h,s] = sum_c dOp * Op (fp32), and the dQ accumulator cleared.  One warp
-// per row of d channels.
+// D[b,h,s] = sum_c dOp * Op (fp32); when lse2 is given, also
+// lse2 = lse * log2(e); when dQacc is given, that row of the accumulator is
+// cleared.  One warp per row of d channels.
 __global__ void bwd_pre_kernel(long long rows, int d, const uint16_t* __restrict__ Op,
-                               const uint16_t* __restrict__ dOp, float* __restrict__ D,
+                               const uint16_t* __restrict__ dOp, const float* __restrict__ lse,
+                               float* __restrict__ D, float* __restrict__ lse2,
                                float* __restrict__ dQacc) {
   const int lane = threadIdx.x & 31;
   const long long row = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
@@ -241,19 +243,25 @@ __global__ void bwd_pre_kernel(long long rows, int d, const uint16_t* __restrict
       s = fmaf(bf16_lo(ow[k]), bf16_lo(gw[k]), s);
       s = fmaf(bf16_hi(ow[k]), bf16_hi(gw[k]), s);
     }
-    float4* dq = reinterpret_cast<float4*>(dQacc + row * d + q * 8);
-    dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dQacc != nullptr) {
+      float4* dq = reinterpret_cast<float4*>(dQacc + row * d + q * 8);
+      dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) D[row] = s;
+  if (lane == 0) {
+    D[row] = s;
+    if (lse2 != nullptr) lse2[row] = lse[row] * 1.4426950408889634f;
+  }
 }
 
-cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp, float* D,
-                           float* dQacc, cudaStream_t st) {
+cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp,
+                           const float* lse, float* D, float* lse2, float* dQacc,
+                           cudaStream_t st) {
   const long long rows = static_cast<long long>(p.cfg.B) * p.cfg.H * p.sz.Np;
-  bwd_pre_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(rows, p.cfg.d,
-                                                                                 Op, dOp, D, dQacc);
+  bwd_pre_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(
+      rows, p.cfg.d, Op, dOp, lse, D, lse2, dQacc);
   return cudaGetLastError();
 }
 

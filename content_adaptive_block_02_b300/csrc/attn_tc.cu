@@ -499,20 +499,4 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_tc_impl(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
-                                    const uint16_t* Vp, const uint16_t* dOp, const float* lse,
-                                    const float* D, const int32_t* n_valid,
-                                    const int32_t* col_ptr, const int32_t* row_idx, float scale,
-                                    float* dQacc, uint16_t* dKp, uint16_t* dVp, uint8_t* ws,
-                                    cudaStream_t st);
-
-cudaError_t launch_attn_bwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
-                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
-                               const float* D, const int32_t* n_valid, const int32_t* col_ptr,
-                               const int32_t* row_idx, float scale, float* dQacc, uint16_t* dKp,
-                               uint16_t* dVp, uint8_t* ws, cudaStream_t st) {
-  return launch_attn_bwd_tc_impl(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx, scale,
-                                 dQacc, dKp, dVp, ws, st);
-}
-
 }  // namespace prism

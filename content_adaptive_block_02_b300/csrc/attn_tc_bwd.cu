@@ -1,39 +1,36 @@
-// Block-sparse attention backward on the tcgen05 tensor cores, 128-token
-// blocks, head dim 128.
+// dK and dV of the block-sparse attention on the tcgen05 tensor cores,
+// 128-token blocks, head dim 128.
 //
 // Prism (arXiv 2610.05416) trains through its sparse attention (Table 2
 // caption: trainable methods replace video self-attention during training).
 // The backward is the softmax-attention VJP restricted to the selected
-// (query block, key block) pairs; the selection itself is a constant.
+// (query block, key block) pairs; the selection itself is a constant.  dQ
+// runs in its own kernel (attn_tc_dq.cu), so that no partial sum leaves an SM.
 //
 // Work item = one key block j of one (b, h) with the ascending list of query
-// blocks i that selected it (CSC).  For each i, five 128x128x128 products:
+// blocks i that selected it (CSC).  For each i, four 128x128x128 products:
 //   (1) S^T  = K_j Q_i^T           A = K_j (smem),  B = Q_i (smem)   -> TMEM S
 //   (2) dP^T = V_j dO_i^T          A = V_j (smem),  B = dO_i (smem)  -> TMEM dP
 //       P^T = exp(S^T * scale - LSE_i)     (row = key, column = query)
 //       dS^T = P^T * (dP^T - D_i)
 //   (3) dV  += P^T dO_i            A = P^T (TMEM, written over S), B = dO_i (MN-major)
 //   (4) dK  += dS^T Q_i            A = dS^T (smem, K-major), B = Q_i (MN-major)
-//   (5) dQ_i = dS K_j              A = dS^T (smem, read MN-major), B = K_j (MN-major)
-//                                  -> TMEM, over dP once dP^T has been read
-// and the dQ_i tile is added to an fp32 accumulator with vector reductions.
 //
-// Roles (448 threads, one persistent CTA per SM):
+// Roles (352 threads, one persistent CTA per SM):
 //   warps 0-7  compute, two warpgroups: warps w and w+4 own the key rows of
 //              TMEM lane quarter w%4 (thread = key row) and split the 128
 //              query columns in halves; P^T, dS^T, epilogue dK * scale, dV
 //              -> bf16 (the halves split the 128 channels there).
-//   warps 8-11 dQ drain: thread = query row; TMEM -> registers -> red.add.v4.
-//   warp 12    producer: work counter, TMA loads of K_j, V_j (once per item)
-//              and of Q_i, dO_i, LSE_i, D_i (2-stage ring) plus the stage's
-//              query-block index and real-token count.
-//   warp 13    issuer A: (1) and (3), which share the S/P columns, in the
+//   warp 8     producer: work counter, TMA loads of K_j, V_j (once per item)
+//              and of Q_i, dO_i, LSE_i * log2 e, D_i (2-stage ring) plus the
+//              stage's query-block real-token count.
+//   warp 9     issuer A: (1) and (3), which share the S/P columns, in the
 //              order 1_0 3_0 1_1 3_1 ...
-//   warp 14    issuer B: (2), (5), (4) in the order 2_0 5_0 4_0 2_1 5_1 4_1 ...
-//              (dQ first, so that the drain starts while dK is computed).
+//   warp 10    issuer B: (2) and (4); dP^T of the next query block is issued
+//              as soon as the compute warps have read this one.
 //   A tcgen05.mma issue blocks while the tensor pipe's queue is full; with two
 //   issuing threads, one thread's barrier waits overlap the other's MMAs.
-// Tensor memory: S/P [0,128), dP/dQ [128,256), dV [256,384), dK [384,512).
+// Tensor memory: S/P [0,128), dP [128,256), dV [256,384), dK [384,512).
 #include "tc_common.cuh"
 
 namespace prism {
@@ -43,7 +40,7 @@ using namespace tc;
 constexpr int kS = 128, kD = 128;
 constexpr int kTile = kS * kD * 2;           // 32 KB
 constexpr int kStage = 2 * kTile + 1024;     // Q, dO, LSE (512 B), D (512 B)
-constexpr int kThreads = 480;
+constexpr int kThreads = 352;
 constexpr int kCompute = 256;
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
 constexpr int kOffV = kTile, kOffStage = 2 * kTile, kOffDS = 2 * kTile + 2 * kStage;
@@ -51,7 +48,7 @@ constexpr int kOffBar = kOffDS + kTile;
 
 struct BwdBars {
   uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2];
-  uint64_t s_full, dp_full, p_ready, ds_ready, ds_empty, dq_full, dq_drained;
+  uint64_t s_full, dp_full, dp_free, p_ready, ds_ready, ds_empty;
   uint64_t kv_done, kv_free, final_bar;
   uint64_t work_full[2], work_empty[2];
   int work_col[2], work_beg[2], work_end[2], work_nvk[2];
@@ -63,13 +60,11 @@ struct BwdBars {
 constexpr size_t kSmemBytes = kOffBar + sizeof(BwdBars);
 
 struct BwdParams {
-  const uint16_t* Qp;
-  const float* lse;
+  const float* lse2;  // LSE * log2(e)
   const float* D;
   const int32_t* n_valid;
   const int32_t* col_ptr;
   const int32_t* row_idx;
-  float* dQacc;
   uint16_t* dKp;
   uint16_t* dVp;
   uint32_t* status;
@@ -100,15 +95,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.qdo_full[s], 1);
       mbar_init(&sm.qdo_empty[s], 2);  // issuers A and B
       mbar_init(&sm.work_full[s], 1);
-      mbar_init(&sm.work_empty[s], 2 + kCompute + 128);
+      mbar_init(&sm.work_empty[s], 2 + kCompute);
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.dp_free, kCompute);
     mbar_init(&sm.p_ready, kCompute);
     mbar_init(&sm.ds_ready, kCompute);
     mbar_init(&sm.ds_empty, 1);
-    mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_drained, 128);
     mbar_init(&sm.kv_done, 2);
     mbar_init(&sm.kv_free, kCompute);
     mbar_init(&sm.final_bar, 2);
@@ -126,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* dsbuf = dsm + kOffDS;
   auto stage = [&](int s) { return dsm + kOffStage + s * kStage; };
 
-  if (warp == 12) {
+  if (warp == 8) {
     // ------------------------------------------------------ producer ----
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -174,32 +168,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(st + kTile / 2, &tmQ, &sm.qdo_full[s], 64, static_cast<int>(yq));
           tma_load_2d(st + kTile, &tmdO, &sm.qdo_full[s], 0, static_cast<int>(yq));
           tma_load_2d(st + kTile + kTile / 2, &tmdO, &sm.qdo_full[s], 64, static_cast<int>(yq));
-          bulk_load(st + 2 * kTile, P.lse + yq, 512, &sm.qdo_full[s]);
+          bulk_load(st + 2 * kTile, P.lse2 + yq, 512, &sm.qdo_full[s]);
           bulk_load(st + 2 * kTile + 512, P.D + yq, 512, &sm.qdo_full[s]);
           ++use;
         }
       }
     }
     __syncwarp();
-  } else if (warp == 13 || warp == 14) {
+  } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------ MMA issuers ----
     if (lane == 0) {
-      const bool is_a = warp == 13;
+      const bool is_a = warp == 9;
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // A K-major, B K-major
       constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // A K-major, B MN-major
-      constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // A MN-major, B MN-major
       const uint64_t kd_k = sdesc_sw128(smem_u32(kbuf), 16, 1024);          // K, K-major
       const uint64_t vd_k = sdesc_sw128(smem_u32(vbuf), 16, 1024);          // V, K-major
-      const uint64_t kd_n = sdesc_sw128(smem_u32(kbuf), kTile / 2, 1024);   // K, MN-major
       const uint64_t dsd_k = sdesc_sw128(smem_u32(dsbuf), 16, 1024);        // dS^T, K-major
-      const uint64_t dsd_n = sdesc_sw128(smem_u32(dsbuf), kTile / 2, 1024); // dS, MN-major
       auto koff = [](int kk) {  // K-major 16-element step inside two 64-column panels
         return static_cast<uint64_t>(((kk >> 2) * (kTile / 2) + (kk & 3) * 32) >> 4);
       };
       auto noff = [](int kk) {  // MN-major 16-row step
         return static_cast<uint64_t>((kk * 2048) >> 4);
       };
-      uint32_t use = 0, items = 0, pcnt = 0, dscnt = 0, dqcnt = 0, kvcnt = 0;
+      uint32_t use = 0, items = 0, pcnt = 0, dscnt = 0, dpcnt = 0, kvcnt = 0;
       bool ok = true;
       for (uint32_t it = 0; ok; ++it) {
         const int ws = it & 1;
@@ -218,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_after();
             const uint64_t qd_k = sdesc_sw128(smem_u32(stage(st)), 16, 1024);
             const uint64_t qd_n = sdesc_sw128(smem_u32(stage(st)), kTile / 2, 1024);
-            const uint64_t dod_k = sdesc_sw128(smem_u32(stage(st) + kTile), 16, 1024);
             const uint64_t dod_n = sdesc_sw128(smem_u32(stage(st) + kTile), kTile / 2, 1024);
             if (is_a) {
               // (1) S^T = K Q^T
@@ -236,22 +226,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (k > 0 || kk > 0) ? 1u : 0u);
               commit(&sm.qdo_empty[st]);
             } else {
-              // (2) dP^T = V dO^T, once the previous dQ tile has left the dP columns
-              if (dqcnt > 0 && !W.wait(&sm.dq_drained, (dqcnt - 1) & 1, 35)) { ok = false; break; }
-              fence_after();
+              // (2) dP^T of this query block was issued in the previous step
+              // (or just below for the first one); (2) of the next one goes
+              // out as soon as the compute warps have read this dP^T
+              auto issue_dp = [&](uint32_t kq) -> bool {
+                const int sq = (use + kq) & 1;
+                if (kq > 0 && !W.wait(&sm.qdo_full[sq], ((use + kq) >> 1) & 1, 35)) return false;
+                if (dpcnt > 0 && !W.wait(&sm.dp_free, (dpcnt - 1) & 1, 38)) return false;
+                fence_after();
+                const uint64_t dd = sdesc_sw128(smem_u32(stage(sq) + kTile), 16, 1024);
 #pragma unroll
-              for (int kk = 0; kk < kD / 16; ++kk)
-                mma_ss(tmem + TM_DP, vd_k + koff(kk), dod_k + koff(kk), id_kk, kk > 0 ? 1u : 0u);
-              commit(&sm.dp_full);
-              // (5) dQ = dS K into the dP columns, then (4) dK += dS^T Q
+                for (int kk = 0; kk < kD / 16; ++kk)
+                  mma_ss(tmem + TM_DP, vd_k + koff(kk), dd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
+                commit(&sm.dp_full);
+                ++dpcnt;
+                return true;
+              };
+              if (k == 0 && !issue_dp(0)) { ok = false; break; }
+              if (k + 1 < n && !issue_dp(k + 1)) { ok = false; break; }
+              // (4) dK += dS^T Q
               if (!W.wait(&sm.ds_ready, dscnt & 1, 37)) { ok = false; break; }
               ++dscnt;
               fence_after();
-#pragma unroll
-              for (int kk = 0; kk < kS / 16; ++kk)
-                mma_ss(tmem + TM_DP, dsd_n + noff(kk), kd_n + noff(kk), id_nn, kk > 0 ? 1u : 0u);
-              commit(&sm.dq_full);
-              ++dqcnt;
 #pragma unroll
               for (int kk = 0; kk < kS / 16; ++kk)
                 mma_ss(tmem + TM_DK, dsd_k + koff(kk), qd_n + noff(kk), id_kn,
@@ -335,8 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int q = c * 32 + g * 4 + e;
-                const float x = fmaf(__uint_as_float(sv[g * 4 + e]), P.scale_log2,
-                                     -lv[e] * 1.4426950408889634f);
+                const float x = fmaf(__uint_as_float(sv[g * 4 + e]), P.scale_log2, -lv[e]);
                 p[q] = q < lim ? ex2(x) : 0.f;
               }
             }
@@ -367,6 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t dp[32];
             tmem_ld32(tmem + lb + TM_DP + q0 + c * 32, dp);
             tmem_ld_wait();
+            if (c == 1) {
+              fence_before();
+              mbar_arrive(&sm.dp_free);  // issuer B may start the next dP^T
+            }
 #pragma unroll
             for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
               const int ql = c * 32 + g * 8;  // local query index in this half
@@ -422,59 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sm.kv_free);
       mbar_arrive(&sm.work_empty[ws]);
     }
-  } else {
-    // ------------------------------------------------------ dQ drain ----
-    const int qw = warp - 8;  // TMEM lane quarter of this warp (query rows 32qw..)
-    const uint32_t lb = static_cast<uint32_t>(qw * 32) << 16;
-    uint32_t dqcnt = 0;
-    for (uint32_t it = 0;; ++it) {
-      const int ws = it & 1;
-      if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 51)) break;
-      const int col = sm.work_col[ws];
-      if (col < 0) break;
-      const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg;
-      const long long bh = col / P.nb;
-      bool ok = true;
-      int i_next = n > 0 ? P.row_idx[beg] : 0;
-      int nvq_next = n > 0 ? P.n_valid[bh * P.nb + i_next] : 0;
-      for (int k = 0; k < n; ++k) {
-        const int i = i_next, nvq = nvq_next;
-        if (k + 1 < n) {  // ahead of its use
-          i_next = P.row_idx[beg + k + 1];
-          nvq_next = P.n_valid[bh * P.nb + i_next];
-        }
-        if (!W.wait(&sm.dq_full, dqcnt & 1, 52)) { ok = false; break; }
-        ++dqcnt;
-        fence_after();
-        // 16-lane halves of this warp's quarter in the 16x256b shape: four
-        // consecutive threads hold one 32-byte run of a row, so every v2
-        // reduction of a warp covers whole sectors
-        float* tile = P.dQacc + (bh * P.Np + static_cast<long long>(i) * kS) * kD;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v[64];
-          tmem_ld_16x256b_x16(tmem + lb + (static_cast<uint32_t>(hh * 16) << 16) + TM_DP, v);
-          tmem_ld_wait();
-          if (hh == 1) {
-            fence_before();
-            mbar_arrive(&sm.dq_drained);
-          }
-          const int ra = qw * 32 + hh * 16 + (lane >> 2), rb = ra + 8;
-          const int cc = 2 * (lane & 3);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            if (ra < nvq)
-              red_add_v2(tile + ra * kD + 8 * k + cc, __uint_as_float(v[4 * k]),
-                         __uint_as_float(v[4 * k + 1]));
-            if (rb < nvq)
-              red_add_v2(tile + rb * kD + 8 * k + cc, __uint_as_float(v[4 * k + 2]),
-                         __uint_as_float(v[4 * k + 3]));
-          }
-        }
-      }
-      if (!ok) break;
-      mbar_arrive(&sm.work_empty[ws]);
-    }
   }
 
   // ---------------------------------------------------------- teardown ----
@@ -489,12 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_tc_impl(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
-                                    const uint16_t* Vp, const uint16_t* dOp, const float* lse,
-                                    const float* D, const int32_t* n_valid,
-                                    const int32_t* col_ptr, const int32_t* row_idx, float scale,
-                                    float* dQacc, uint16_t* dKp, uint16_t* dVp, uint8_t* ws,
-                                    cudaStream_t st) {
+cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
+                                const float* D, const int32_t* n_valid, const int32_t* col_ptr,
+                                const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
+                                uint8_t* ws, cudaStream_t st) {
   const prism_config_t& c = p.cfg;
   const long long rows_total = static_cast<long long>(c.B) * c.H * p.sz.Np;
   CUtensorMap tmQ, tmK, tmV, tmdO;
@@ -502,13 +447,11 @@ cudaError_t launch_attn_bwd_tc_impl(const Plan& p, const uint16_t* Qp, const uin
       !make_tile_map(&tmV, Vp, rows_total) || !make_tile_map(&tmdO, dOp, rows_total))
     return cudaErrorInvalidValue;
   BwdParams a;
-  a.Qp = Qp;
-  a.lse = lse;
+  a.lse2 = lse2;
   a.D = D;
   a.n_valid = n_valid;
   a.col_ptr = col_ptr;
   a.row_idx = row_idx;
-  a.dQacc = dQacc;
   a.dKp = dKp;
   a.dVp = dVp;
   a.status = reinterpret_cast<uint32_t*>(ws);

@@ -1,0 +1,405 @@
+// dQ of the block-sparse attention on the tcgen05 tensor cores, 128-token
+// blocks, head dim 128.
+//
+// Prism (arXiv 2610.05416) trains through its sparse attention (Table 2
+// caption).  dQ_i = scale * sum over the key blocks j selected by query
+// block i of dS_ij K_j, with P_ij = exp(Q_i K_j^T * scale - LSE_i) and
+// dS_ij = P_ij * (dO_i V_j^T - D_i).  The key-block side (dK, dV) runs in a
+// separate kernel, so no partial sum of dQ ever leaves the SM: dQ is summed
+// in tensor memory and written once, in bf16, deterministically.
+//
+// Work item = one query block (b, h, i) with its ascending list of key
+// blocks (CSR).  Per key block j, three 128x128x128 products:
+//   S  = Q_i K_j^T     A = Q_i (smem),  B = K_j (smem)        -> TMEM S
+//   dP = dO_i V_j^T    A = dO_i (smem), B = V_j (smem)        -> TMEM dP
+//   dQ += dS K_j       A = dS (TMEM, bf16), B = K_j (MN-major) -> TMEM dQ
+// Roles (352 threads, one persistent CTA per SM):
+//   warps 0-7  compute: thread = query row; warps w and w+4 split the key
+//              columns in halves.  P = exp2(S*c - LSE*log2 e), dS = P (dP - D)
+//              -> bf16 pairs in TMEM (two buffers); epilogue dQ * scale -> bf16.
+//              No exchange between the halves is needed: LSE and D are known.
+//   warp 8     producer: work counter, TMA loads of Q_i and dO_i (once per
+//              item) and of K_j, V_j (2-stage ring).
+//   warp 9     issuer A: S_j then dP_j, as soon as the compute warps have
+//              read the previous S / dP tiles.
+//   warp 10    issuer B: dQ += dS_j K_j.
+// Tensor memory: S [0,128), dP [128,256), dQ [256,384), dS0 [384,448),
+// dS1 [448,512).
+#include "tc_common.cuh"
+
+namespace prism {
+namespace {
+using namespace tc;
+
+constexpr int kS = 128, kD = 128;
+constexpr int kTile = kS * kD * 2;  // 32 KB
+constexpr int kStages = 2;
+constexpr int kThreads = 352;
+constexpr int kCompute = 256;
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_DS0 = 384, TM_DS1 = 448;
+constexpr int kOffQ = 0, kOffDO = kTile, kOffKV = 2 * kTile;
+constexpr int kOffBar = kOffKV + kStages * 2 * kTile;
+
+struct DqBars {
+  uint64_t qd_full, qd_empty, kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full, dp_full, s_free, dp_free, ds_ready[2], ds_empty[2];
+  uint64_t dq_done, dq_free, final_bar;
+  uint64_t work_full[2], work_empty[2];
+  int work_row[2], work_beg[2], work_end[2], work_nvq[2];
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kSmemBytes = kOffBar + sizeof(DqBars);
+
+struct DqParams {
+  const float* lse;
+  const float* D;
+  const int32_t* n_valid;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  uint16_t* dQp;
+  uint32_t* status;
+  long long rows;  // B*H*nb work items
+  long long Np;
+  int nb;
+  float scale, scale_log2;
+  unsigned long long limit;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmdO, DqParams P) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  DqBars& sm = *reinterpret_cast<DqBars*>(dsm + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(dsm) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) dev_error(P.status, DEV_ERR_BOUNDS, 0xA12, smem_u32(dsm));
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.qd_full, 1);
+    mbar_init(&sm.qd_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 2);  // K is read by both issuers
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.s_free, kCompute);
+    mbar_init(&sm.dp_free, kCompute);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.ds_ready[b], kCompute);
+      mbar_init(&sm.ds_empty[b], 1);
+      mbar_init(&sm.work_full[b], 1);
+      mbar_init(&sm.work_empty[b], 2 + kCompute);
+    }
+    mbar_init(&sm.dq_done, 1);
+    mbar_init(&sm.dq_free, kCompute);
+    mbar_init(&sm.final_bar, 2);
+    sm.abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(&sm.tmem_base, 512);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const Waiter W{&sm.abort, P.status, P.limit};
+  uint8_t* kvbuf = dsm + kOffKV;  // stage s: K at s * 2 * kTile, V right after
+
+  if (warp == 8) {
+    // ------------------------------------------------------ producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      uint32_t use = 0, items = 0;
+      bool ok = true;
+      for (uint32_t it = 0; ok; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_empty[ws], ((it >> 1) & 1) ^ 1, 61)) break;
+        const long long row = atomicAdd(P.status + WS_DQ_QUEUE, 1u);
+        if (row >= P.rows) {
+          sm.work_row[ws] = -1;
+          mbar_arrive(&sm.work_full[ws]);
+          break;
+        }
+        const int beg = P.row_ptr[row], end = P.row_ptr[row + 1];
+        const int nvq = P.n_valid[row];
+        sm.work_row[ws] = static_cast<int>(row);
+        sm.work_beg[ws] = beg;
+        sm.work_end[ws] = nvq > 0 ? end : beg;
+        sm.work_nvq[ws] = nvq;
+        mbar_arrive(&sm.work_full[ws]);
+        if (nvq == 0 || end == beg) continue;
+        const long long bh = row / P.nb;
+        const int i = static_cast<int>(row % P.nb);
+        const int yq = static_cast<int>(bh * P.Np + static_cast<long long>(i) * kS);
+        // Q_i, dO_i once the previous item's S / dP products are done
+        if (!W.wait(&sm.qd_empty, (items & 1) ^ 1, 62)) break;
+        ++items;
+        mbar_expect_tx(&sm.qd_full, 2 * kTile);
+        tma_load_2d(dsm + kOffQ, &tmQ, &sm.qd_full, 0, yq);
+        tma_load_2d(dsm + kOffQ + kTile / 2, &tmQ, &sm.qd_full, 64, yq);
+        tma_load_2d(dsm + kOffDO, &tmdO, &sm.qd_full, 0, yq);
+        tma_load_2d(dsm + kOffDO + kTile / 2, &tmdO, &sm.qd_full, 64, yq);
+        for (int t = beg; t < end; ++t) {
+          const int j = P.col_idx[t];
+          const int y = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
+          const int st = use % kStages;
+          if (!W.wait(&sm.kv_empty[st], ((use / kStages) & 1) ^ 1, 63)) { ok = false; break; }
+          uint8_t* kb = kvbuf + st * 2 * kTile;
+          mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
+          tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
+          tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
+          tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
+          tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+          ++use;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------ issuer A: S, dP ----
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);
+      const uint64_t qd = sdesc_sw128(smem_u32(dsm + kOffQ), 16, 1024);
+      const uint64_t dod = sdesc_sw128(smem_u32(dsm + kOffDO), 16, 1024);
+      auto koff = [](int kk) {
+        return static_cast<uint64_t>(((kk >> 2) * (kTile / 2) + (kk & 3) * 32) >> 4);
+      };
+      uint32_t use = 0, items = 0, sidx = 0;
+      bool ok = true;
+      for (uint32_t it = 0; ok; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 64)) break;
+        if (sm.work_row[ws] < 0) break;
+        const int n = sm.work_end[ws] - sm.work_beg[ws];
+        if (n > 0) {
+          if (!W.wait(&sm.qd_full, items & 1, 65)) break;
+          ++items;
+          for (int jj = 0; jj < n; ++jj) {
+            const int st = use % kStages;
+            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 66)) { ok = false; break; }
+            const uint64_t kd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile), 16, 1024);
+            const uint64_t vd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile + kTile), 16, 1024);
+            if (sidx > 0 && !W.wait(&sm.s_free, (sidx - 1) & 1, 67)) { ok = false; break; }
+            fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ss(tmem + TM_S, qd + koff(kk), kd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
+            commit(&sm.s_full);
+            if (sidx > 0 && !W.wait(&sm.dp_free, (sidx - 1) & 1, 68)) { ok = false; break; }
+            fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ss(tmem + TM_DP, dod + koff(kk), vd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
+            commit(&sm.dp_full);
+            commit(&sm.kv_empty[st]);
+            ++use;
+            ++sidx;
+          }
+          if (ok) commit(&sm.qd_empty);
+        }
+        if (ok) mbar_arrive(&sm.work_empty[ws]);
+      }
+      commit(&sm.final_bar);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------ issuer B: dQ ----
+    if (lane == 0) {
+      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // A = dS (TMEM), B = K MN-major
+      uint32_t use = 0, gidx = 0, items = 0;
+      bool ok = true;
+      for (uint32_t it = 0; ok; ++it) {
+        const int ws = it & 1;
+        if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 71)) break;
+        if (sm.work_row[ws] < 0) break;
+        const int n = sm.work_end[ws] - sm.work_beg[ws];
+        if (n > 0) {
+          // the previous item's dQ has been read out before it is overwritten
+          if (items > 0 && !W.wait(&sm.dq_free, (items - 1) & 1, 72)) break;
+          ++items;
+          for (int jj = 0; jj < n; ++jj) {
+            const uint32_t b = gidx & 1;
+            if (!W.wait(&sm.ds_ready[b], (gidx >> 1) & 1, 73)) { ok = false; break; }
+            const int st = use % kStages;
+            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 74)) { ok = false; break; }
+            fence_after();
+            const uint64_t kd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile), kTile / 2, 1024);
+            const uint32_t a = tmem + (b ? TM_DS1 : TM_DS0);
+#pragma unroll
+            for (int kk = 0; kk < kS / 16; ++kk)
+              mma_ts(tmem + TM_DQ, a + kk * 8, kd + static_cast<uint64_t>((kk * 2048) >> 4), id_kn,
+                     (jj > 0 || kk > 0) ? 1u : 0u);
+            commit(&sm.ds_empty[b]);
+            commit(&sm.kv_empty[st]);
+            ++use;
+            ++gidx;
+          }
+          if (ok) commit(&sm.dq_done);
+        }
+        if (ok) mbar_arrive(&sm.work_empty[ws]);
+      }
+      commit(&sm.final_bar);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------ compute ----
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // query row == TMEM lane
+    const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
+    const int c0 = half * 64;  // first key column (and dQ channel) of this half
+    uint32_t sidx = 0, gidx = 0, items = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int ws = it & 1;
+      if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 81)) break;
+      const int row = sm.work_row[ws];
+      if (row < 0) break;
+      const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg, nvq = sm.work_nvq[ws];
+      const long long bh = row / P.nb;
+      const int i = row % P.nb;
+      const long long grow = bh * P.Np + static_cast<long long>(i) * kS + r;
+      uint4* drow = reinterpret_cast<uint4*>(P.dQp + grow * kD) + half * 8;
+      if (n == 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) drow[q] = make_uint4(0, 0, 0, 0);
+        mbar_arrive(&sm.work_empty[ws]);
+        continue;
+      }
+      const bool real = r < nvq;
+      const float lse2 = P.lse[grow] * 1.4426950408889634f;
+      const float Dr = P.D[grow];
+      const int32_t* nvb = P.n_valid + bh * P.nb;
+      int nvk_next = nvb[P.col_idx[beg]];
+      bool ok = true;
+      for (int jj = 0; jj < n; ++jj) {
+        const int nvk = nvk_next;
+        if (jj + 1 < n) nvk_next = nvb[P.col_idx[beg + jj + 1]];  // ahead of its use
+        const int lim = real ? nvk - c0 : 0;  // real key columns of this half
+        if (!W.wait(&sm.s_full, sidx & 1, 82)) { ok = false; break; }
+        fence_after();
+        uint32_t sv[2][32], dp[2][32];
+        tmem_ld32(tmem + lb + TM_S + c0, sv[0]);
+        tmem_ld32(tmem + lb + TM_S + c0 + 32, sv[1]);
+        tmem_ld_wait();
+        fence_before();
+        mbar_arrive(&sm.s_free);
+        if (!W.wait(&sm.dp_full, sidx & 1, 83)) { ok = false; break; }
+        fence_after();
+        tmem_ld32(tmem + lb + TM_DP + c0, dp[0]);
+        tmem_ld32(tmem + lb + TM_DP + c0 + 32, dp[1]);
+        tmem_ld_wait();
+        fence_before();
+        mbar_arrive(&sm.dp_free);
+        ++sidx;
+        uint32_t pk[32];
+        if (lim >= 64) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int k0 = 2 * e, k1 = k0 + 1;
+            const float p0 = ex2(fmaf(__uint_as_float(sv[k0 >> 5][k0 & 31]), P.scale_log2, -lse2));
+            const float p1 = ex2(fmaf(__uint_as_float(sv[k1 >> 5][k1 & 31]), P.scale_log2, -lse2));
+            pk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[k0 >> 5][k0 & 31]) - Dr),
+                                p1 * (__uint_as_float(dp[k1 >> 5][k1 & 31]) - Dr));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int k0 = 2 * e, k1 = k0 + 1;
+            const float p0 = k0 < lim ? ex2(fmaf(__uint_as_float(sv[k0 >> 5][k0 & 31]), P.scale_log2, -lse2)) : 0.f;
+            const float p1 = k1 < lim ? ex2(fmaf(__uint_as_float(sv[k1 >> 5][k1 & 31]), P.scale_log2, -lse2)) : 0.f;
+            pk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[k0 >> 5][k0 & 31]) - Dr),
+                                p1 * (__uint_as_float(dp[k1 >> 5][k1 & 31]) - Dr));
+          }
+        }
+        // the dQ product that read this dS buffer two key blocks ago is done
+        const uint32_t b = gidx & 1;
+        if (gidx >= 2 && !W.wait(&sm.ds_empty[b], ((gidx >> 1) - 1) & 1, 84)) { ok = false; break; }
+        fence_after();
+        tmem_st32(tmem + lb + (b ? TM_DS1 : TM_DS0) + half * 32, pk);
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&sm.ds_ready[b]);
+        ++gidx;
+      }
+      if (!ok) break;
+      // epilogue: dQ * scale -> bf16, this half of the channels
+      if (!W.wait(&sm.dq_done, items & 1, 85)) break;
+      ++items;
+      fence_after();
+      const float mul = real ? P.scale : 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lb + TM_DQ + c0 + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * mul, __uint_as_float(o[8 * q + 1]) * mul);
+          v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * mul, __uint_as_float(o[8 * q + 3]) * mul);
+          v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * mul, __uint_as_float(o[8 * q + 5]) * mul);
+          v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * mul, __uint_as_float(o[8 * q + 7]) * mul);
+          drow[c * 4 + q] = v;
+        }
+      }
+      fence_before();
+      mbar_arrive(&sm.dq_free);
+      mbar_arrive(&sm.work_empty[ws]);
+    }
+  }
+
+  // ---------------------------------------------------------- teardown ----
+  __syncthreads();
+  if (warp == 0) {
+    if (!wait_raw(&sm.final_bar, 0, P.limit) && lane == 0)
+      dev_error(P.status, DEV_ERR_TIMEOUT, 299, 0);
+    fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                              const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                              const float* D, const int32_t* n_valid, const int32_t* row_ptr,
+                              const int32_t* col_idx, float scale, uint16_t* dQp, uint8_t* ws,
+                              cudaStream_t st) {
+  const prism_config_t& c = p.cfg;
+  const long long rows_total = static_cast<long long>(c.B) * c.H * p.sz.Np;
+  CUtensorMap tmQ, tmK, tmV, tmdO;
+  if (!make_tile_map(&tmQ, Qp, rows_total) || !make_tile_map(&tmK, Kp, rows_total) ||
+      !make_tile_map(&tmV, Vp, rows_total) || !make_tile_map(&tmdO, dOp, rows_total))
+    return cudaErrorInvalidValue;
+  DqParams a;
+  a.lse = lse;
+  a.D = D;
+  a.n_valid = n_valid;
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.dQp = dQp;
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.rows = static_cast<long long>(c.B) * c.H * p.sz.nb;
+  a.Np = p.sz.Np;
+  a.nb = p.sz.nb;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
+  cudaError_t e = cudaMemsetAsync(a.status + WS_DQ_QUEUE, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const long long g = a.rows < sm_count() ? a.rows : sm_count();
+  attn_dq_tc_kernel<<<static_cast<unsigned>(g), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO,
+                                                                             a);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

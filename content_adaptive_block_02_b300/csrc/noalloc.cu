@@ -20,18 +20,24 @@
 #include "prism_internal.cuh"
 
 namespace prism {
-cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp, float* D,
-                           float* dQacc, cudaStream_t st);
+cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp,
+                           const float* lse, float* D, float* lse2, float* dQacc,
+                           cudaStream_t st);
 cudaError_t launch_attn_bwd_simt(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
                                  const uint16_t* Vp, const uint16_t* dOp, const float* lse,
                                  const float* D, const int32_t* n_valid,
                                  const int32_t* col_ptr, const int32_t* row_idx, float scale,
                                  float* dQacc, uint16_t* dKp, uint16_t* dVp, cudaStream_t st);
-cudaError_t launch_attn_bwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
-                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
-                               const float* D, const int32_t* n_valid, const int32_t* col_ptr,
-                               const int32_t* row_idx, float scale, float* dQacc, uint16_t* dKp,
-                               uint16_t* dVp, uint8_t* ws, cudaStream_t st);
+cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                                const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
+                                const float* D, const int32_t* n_valid, const int32_t* col_ptr,
+                                const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
+                                uint8_t* ws, cudaStream_t st);
+cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
+                              const uint16_t* Vp, const uint16_t* dOp, const float* lse,
+                              const float* D, const int32_t* n_valid, const int32_t* row_ptr,
+                              const int32_t* col_idx, float scale, uint16_t* dQp, uint8_t* ws,
+                              cudaStream_t st);
 }  // namespace prism
 
 struct prism_plan {
@@ -76,36 +82,46 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 extern "C" int prism_sparse_attn_bwd_noalloc(
     const prism_plan_t* plan, const uint16_t* Qp, const uint16_t* Kp, const uint16_t* Vp,
     const uint16_t* Op, const uint16_t* dOp, const float* lse, const int32_t* n_valid,
-    const int32_t* col_ptr, const int32_t* row_idx, float scale, uint16_t* dQp, uint16_t* dKp,
-    uint16_t* dVp, void* stream) {
+    const int32_t* row_ptr, const int32_t* col_idx, const int32_t* col_ptr,
+    const int32_t* row_idx, float scale, uint16_t* dQp, uint16_t* dKp, uint16_t* dVp,
+    void* stream) {
   if (plan == nullptr || !(scale > 0.f)) return PRISM_ERR_ARG;
-  const void* ptrs[] = {Qp, Kp, Vp, Op, dOp, lse, n_valid, col_ptr, row_idx, dQp, dKp, dVp};
+  const void* ptrs[] = {Qp,      Kp,      Vp,      Op,  dOp, lse, n_valid, row_ptr,
+                        col_idx, col_ptr, row_idx, dQp, dKp, dVp};
   for (const void* q : ptrs) {
     if (q == nullptr) return PRISM_ERR_ARG;
     if (!al16(q)) return PRISM_ERR_ALIGN;
   }
   const prism::Plan& p = plan->p;
-  // layout inside the scratch: status words, D, dQ accumulator
+  // layout inside the scratch: status words, D, then LSE * log2(e) for the
+  // tensor-core kernels or the fp32 dQ accumulator for the CUDA-core ones
   const size_t rows = static_cast<size_t>(p.cfg.B) * p.cfg.H * p.sz.Np;
   const size_t off_D = 256;
-  const size_t off_dq = off_D + ((rows * 4 + 255) & ~static_cast<size_t>(255));
-  const size_t need = off_dq + rows * p.cfg.d * 4;
+  const size_t off_x = off_D + ((rows * 4 + 255) & ~static_cast<size_t>(255));
+  const size_t need = off_x + rows * 4 * (p.sz.tensor_core_bwd ? 1 : p.cfg.d);
   if (need > kNoAllocScratchBytes) return PRISM_ERR_UNSUPPORTED;  // problem too large for it
   uint8_t* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return PRISM_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* D = reinterpret_cast<float*>(base + off_D);
-  float* dq = reinterpret_cast<float*>(base + off_dq);
+  float* x = reinterpret_cast<float*>(base + off_x);
   if (cudaMemsetAsync(base, 0, 256, st) != cudaSuccess) return PRISM_ERR_CUDA;
-  if (prism::launch_bwd_pre(p, Op, dOp, D, dq, st) != cudaSuccess) return PRISM_ERR_CUDA;
-  cudaError_t e;
-  if (p.sz.tensor_core_bwd)
-    e = prism::launch_attn_bwd_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx, scale,
-                                  dq, dKp, dVp, base, st);
-  else
-    e = prism::launch_attn_bwd_simt(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx, scale,
-                                    dq, dKp, dVp, st);
-  if (e != cudaSuccess) return PRISM_ERR_CUDA;
-  if (prism::launch_dq_convert(p, dq, scale, dQp, st) != cudaSuccess) return PRISM_ERR_CUDA;
+  if (p.sz.tensor_core_bwd) {
+    if (prism::launch_bwd_pre(p, Op, dOp, lse, D, x, nullptr, st) != cudaSuccess)
+      return PRISM_ERR_CUDA;
+    if (prism::launch_attn_dkdv_tc(p, Qp, Kp, Vp, dOp, x, D, n_valid, col_ptr, row_idx, scale,
+                                   dKp, dVp, base, st) != cudaSuccess)
+      return PRISM_ERR_CUDA;
+    if (prism::launch_attn_dq_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx, scale,
+                                 dQp, base, st) != cudaSuccess)
+      return PRISM_ERR_CUDA;
+  } else {
+    if (prism::launch_bwd_pre(p, Op, dOp, lse, D, nullptr, x, st) != cudaSuccess)
+      return PRISM_ERR_CUDA;
+    if (prism::launch_attn_bwd_simt(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx, scale,
+                                    x, dKp, dVp, st) != cudaSuccess)
+      return PRISM_ERR_CUDA;
+    if (prism::launch_dq_convert(p, x, scale, dQp, st) != cudaSuccess) return PRISM_ERR_CUDA;
+  }
   return PRISM_OK;
 }

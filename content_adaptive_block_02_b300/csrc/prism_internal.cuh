@@ -18,7 +18,7 @@ struct Plan {
   double log2_ext[PRISM_MAX_SHAPES][3];  // log2 of every menu extent
   double log2_S;
   // workspace offsets (bytes), each region 256-aligned
-  size_t off_rowcnt, off_colcnt, off_amb, off_bitmask, off_scores, off_D, off_dq;
+  size_t off_rowcnt, off_colcnt, off_amb, off_bitmask, off_scores, off_D, off_lse2, off_dq;
 };
 
 // Workspace layout (bytes from the start of ws, each region 256-aligned):
@@ -29,13 +29,15 @@ struct Plan {
 //   off_bitmask     u32   [B*H*nb*nw]    selection bitmask, nw = ceil(nb/32)
 //   off_scores      fp32  [2*B*H*nb*nb]  block scores (unscaled dots), hi then lo
 //   off_D           fp32  [B*H*Np]       rowsum(dO * O) for the backward
-//   off_dq          fp32  [B*H*Np*d]     dQ accumulator for the backward
+//   off_lse2        fp32  [B*H*Np]       LSE * log2(e) for the backward
+//   off_dq          fp32  [B*H*Np*d]     dQ accumulator of the CUDA-core backward
 enum : int {
   WS_STATUS = 0,      // uint32: first device error code (0 = none)
   WS_AMB_COUNT = 1,   // uint32: number of ambiguous rows appended by the select kernel
   WS_FWD_QUEUE = 2,   // uint32: next work item of the persistent forward
   WS_BWD_QUEUE = 3,   // uint32: next work item of the persistent backward
   WS_ERR_INFO = 4,    // uint32 x4: where a device error was raised
+  WS_DQ_QUEUE = 8,    // uint32: next work item of the persistent dQ kernel
 };
 
 enum : uint32_t { DEV_ERR_TIMEOUT = 1, DEV_ERR_BOUNDS = 2 };

@@ -195,10 +195,11 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
  * memory when they run it (for example code confined to a memory pool it does
  * not own, or a runtime that forbids cudaMalloc / cudaFree after start-up).
  * The paper has no counterpart: this is a library convenience.  Arguments and
- * results are those of prism_sparse_attn_bwd minus row_ptr, col_idx and ws;
- * the scratch (rowsum D and the fp32 dQ accumulator, B*H*Np*(d+1)*4 bytes plus
- * 256) lives in a 32 MiB array inside the library, held on every GPU that
- * loads the library until the process exits.  Larger problems return
+ * results are those of prism_sparse_attn_bwd minus ws; the scratch (rowsum D
+ * and LSE * log2 e, 8*B*H*Np bytes plus 512, on the tensor-core path; D and the
+ * fp32 dQ accumulator, 4*B*H*Np*(d+1) bytes plus 512, on the CUDA-core path)
+ * lives in a 32 MiB array inside the library, held on every GPU that loads
+ * the library until the process exits.  Larger problems return
  * PRISM_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
  * device looks the array's address up (make that first call before any stream
  * capture).  All calls share the array: calls whose kernels overlap on the GPU
@@ -207,6 +208,7 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
 int prism_sparse_attn_bwd_noalloc(const prism_plan_t* plan, const uint16_t* Qp,
                                   const uint16_t* Kp, const uint16_t* Vp, const uint16_t* Op,
                                   const uint16_t* dOp, const float* lse, const int32_t* n_valid,
+                                  const int32_t* row_ptr, const int32_t* col_idx,
                                   const int32_t* col_ptr, const int32_t* row_idx, float scale,
                                   uint16_t* dQp, uint16_t* dKp, uint16_t* dVp, void* stream);
 

@@ -21,7 +21,7 @@ P = ctypes.c_void_p
 def _fn():
     build.build()
     fn = prism.lib().prism_sparse_attn_bwd_noalloc
-    fn.argtypes = [P] * 10 + [ctypes.c_float] + [P] * 4
+    fn.argtypes = [P] * 12 + [ctypes.c_float] + [P] * 4
     fn.restype = ctypes.c_int
     return fn
 
@@ -46,7 +46,8 @@ def test_noalloc_backward_matches_workspace_backward(w):
     for _ in range(2):
         got = [torch.full_like(t, float("nan")) for t in want]
         rc = fn(att.plan.h, ptr(o["Qp"]), ptr(o["Kp"]), ptr(o["Vp"]), ptr(att.Op), ptr(att.dOp),
-                ptr(att.lse), ptr(o["n_valid"]), ptr(att.lists["col_ptr"]),
+                ptr(att.lse), ptr(o["n_valid"]), ptr(att.lists["row_ptr"]),
+                ptr(att.lists["col_idx"]), ptr(att.lists["col_ptr"]),
                 ptr(att.lists["row_idx"]), att.scale, ptr(got[0]), ptr(got[1]), ptr(got[2]),
                 prism._stream())
         assert rc == 0, prism.ERRORS.get(rc, rc)
@@ -59,5 +60,5 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     fn = _fn()
     plan = prism.Plan(synth.WORKLOADS["2k"])
     fake = P(0x1000)  # aligned, never dereferenced: the size check comes first
-    rc = fn(plan.h, *([fake] * 9), 0.1, fake, fake, fake, None)
+    rc = fn(plan.h, *([fake] * 11), 0.1, fake, fake, fake, None)
     assert rc == -3  # PRISM_ERR_UNSUPPORTED
