@@ -164,26 +164,30 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
         o[a] = len[a] >= 2 ? acc[a] / (nl[a] * static_cast<float>(c.d)) : 0.f;
     }
   } else {
-    // ---- A2V norm map of the zone: n_i = ||a2v_i||_2 ----
-    float* nmap = reinterpret_cast<float*>(smem);
+    // ---- A2V norm map of the zone: n_i = ||a2v_i||_2, in fp64 ----
+    // The audio directional variance is a ratio of variances that can be
+    // tiny (a norm map that is nearly constant over the zone), so it is
+    // computed in fp64 throughout: 768 norms and ~350 lines per zone.
+    double* nmap = reinterpret_cast<double*>(smem);
+    __shared__ double dred[32 * 4];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     for (int li = warp; li < vol; li += nw) {
       const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
       const long long n =
           (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
       const uint16_t* row = a2v + (static_cast<long long>(b) * N + n) * c.Ca;
-      float s = 0.f;
+      double s = 0.0;
       for (int k = lane; k < c.Ca; k += 32) {
-        float v = bf16_to_f(row[k]);
-        s = fmaf(v, v, s);
+        const double v = bf16_to_f(row[k]);
+        s = fma(v, v, s);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) nmap[li] = sqrtf(s);
+      if (lane == 0) nmap[li] = sqrt(s);
     }
     __syncthreads();
     // line variances of the scalar map, thread per line
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    double acc[4] = {0.0, 0.0, 0.0, 0.0};
     const int nlT = g.vy * g.vx, nlH = g.vt * g.vx, nlW = g.vt * g.vy;
     for (int ln = threadIdx.x; ln < nlT + nlH + nlW; ln += blockDim.x) {
       int base, len, step, axis;
@@ -197,25 +201,38 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
         axis = 2; base = l * g.vx; len = g.vx; step = 1;
       }
       if (len < 2) continue;
-      float m = 0.f;
+      double m = 0.0;
       for (int k = 0; k < len; ++k) m += nmap[base + k * step];
-      m /= static_cast<float>(len);
-      float s = 0.f;
+      m /= static_cast<double>(len);
+      double s = 0.0;
       for (int k = 0; k < len; ++k) {
-        float e = nmap[base + k * step] - m;
-        s = fmaf(e, e, s);
+        const double e = nmap[base + k * step] - m;
+        s = fma(e, e, s);
       }
-      acc[axis] += s / static_cast<float>(len);
+      acc[axis] += s / static_cast<double>(len);
     }
     for (int li = threadIdx.x; li < vol; li += blockDim.x) acc[3] += nmap[li];
-    block_sum<4>(acc, red);
+    // fixed-order reduction (deterministic)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+    __syncthreads();
+    if (lane == 0)
+      for (int k = 0; k < 4; ++k) dred[warp * 4 + k] = acc[k];
+    __syncthreads();
     if (threadIdx.x == 0) {
-      const float nl[3] = {static_cast<float>(nlT), static_cast<float>(nlH),
-                           static_cast<float>(nlW)};
+      for (int k = 0; k < 4; ++k) {
+        double s = 0.0;
+        for (int q = 0; q < nw; ++q) s += dred[q * 4 + k];
+        acc[k] = s;
+      }
+      const double nl[3] = {static_cast<double>(nlT), static_cast<double>(nlH),
+                            static_cast<double>(nlW)};
       const int len[3] = {g.vt, g.vy, g.vx};
       float out[5];
-      for (int a = 0; a < 3; ++a) out[a] = len[a] >= 2 ? acc[a] / nl[a] : 0.f;
-      out[3] = acc[3] / static_cast<float>(vol);
+      for (int a = 0; a < 3; ++a) out[a] = len[a] >= 2 ? static_cast<float>(acc[a] / nl[a]) : 0.f;
+      out[3] = static_cast<float>(acc[3] / static_cast<double>(vol));
       out[4] = static_cast<float>(vol);
       for (int hh = 0; hh < c.H; ++hh) {
         float* o = stats + ((static_cast<long long>(b) * c.H + hh) * Z + z) * 8;
@@ -277,12 +294,15 @@ __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, Me
     nbar = sh[z * 8 + 6];
     const double ssv = sv[0] + sv[1] + sv[2];
     const double ssn = sn[0] + sn[1] + sn[2];
+    // no audio direction when the norm map's variance is round-off (a
+    // constant map): at most 1e-20 nbar^2
+    const bool no_var = !(ssn > 1e-20 * nbar * nbar);
     const double abar = nmax > 0.0 ? nbar / nmax : 0.0;
     const double uv = c.use_video ? 1.0 : 0.0, ua = c.use_audio ? 1.0 : 0.0;
     double lg[3];
     for (int a = 0; a < 3; ++a) {
       const double r = ssv > 0.0 ? sv[a] / ssv : 1.0 / 3.0;
-      const double vh = ssn > 0.0 ? sn[a] / ssn : 1.0 / 3.0;
+      const double vh = no_var ? 1.0 / 3.0 : sn[a] / ssn;
       const double gd = uv * r + ua * abar * vh + c.eps;
       lg[a] = log2(gd);
     }
@@ -319,7 +339,7 @@ cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* 
   const prism_config_t& c = p.cfg;
   const int vol = c.zT * c.zH * c.zW;
   const size_t smem_video = 2ull * vol * kChunk * 2;
-  const size_t smem_audio = static_cast<size_t>(vol) * sizeof(float);
+  const size_t smem_audio = static_cast<size_t>(vol) * sizeof(double);
   const size_t smem = smem_video > smem_audio ? smem_video : smem_audio;
   cudaError_t e = cudaFuncSetAttribute(zone_stats_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -139,20 +139,30 @@ def zone_stats(w, V: np.ndarray, a2v: np.ndarray) -> np.ndarray:
 # step 2: block shape per zone (Eq. 7) and token permutation
 # --------------------------------------------------------------------------
 
+# A2V norm maps that are constant over a zone (e.g. a zone where one audio
+# token dominates the cross-attention) have no directional variance; what any
+# arithmetic returns for them is round-off, and its ratios are meaningless.
+# A directional variance whose sum is at most AUDIO_VAR_FLOOR * nbar^2 counts
+# as zero (round-off of a constant map is ~1e-30 nbar^2 in fp64).
+AUDIO_VAR_FLOOR = 1e-20
+
+
 def guidance(w, st: np.ndarray, nbar_max: float) -> np.ndarray:
     """g_d for one zone from its statistics row st[8].
 
     READING (Prism, Table 9 caption names r_{v,d}, a_bar and v_hat_{a,d};
     Table 12 ablates each guidance):
       r_{v,d}     = var_v_d / sum_d var_v_d      (1/3 each when the sum is 0)
-      v_hat_{a,d} = var_n_d / sum_d var_n_d      (1/3 each when the sum is 0)
+      v_hat_{a,d} = var_n_d / sum_d var_n_d      (1/3 each when there is no
+                    variance: sum <= AUDIO_VAR_FLOOR * nbar^2)
       a_bar       = nbar / max over zones of nbar (0 when that max is 0)
       g_d = u_v r_{v,d} + u_a a_bar v_hat_{a,d} + eps
     with u_v, u_a the video/audio guidance switches.
     """
     sv, sn = st[0:3], st[3:6]
     r = sv / sv.sum() if sv.sum() > 0 else np.full(3, 1.0 / 3.0)
-    vh = sn / sn.sum() if sn.sum() > 0 else np.full(3, 1.0 / 3.0)
+    no_var = not (sn.sum() > AUDIO_VAR_FLOOR * st[6] * st[6])
+    vh = np.full(3, 1.0 / 3.0) if no_var else sn / sn.sum()
     abar = st[6] / nbar_max if nbar_max > 0 else 0.0
     uv = 1.0 if w.use_video else 0.0
     ua = 1.0 if w.use_audio else 0.0

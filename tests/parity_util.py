@@ -221,3 +221,124 @@ def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=No
             rep["dKV_sampled_max_rel"] = ek
             assert ek <= G_TOL, ("dK/dV", ek)
     return rep
+
+
+def compare_sampled(w, heads, n_rows=6, n_key_blocks=1, seed=0, report=None):
+    """Full-size check on a sample.  Inputs are generated on the device; for
+    each sampled head the oracle runs every step of that head (statistics,
+    shapes, permutation, pooling), the selection on `n_rows` sampled query
+    blocks (always including one partially real block when there is one),
+    attention forward and dQ on those rows, and dK / dV on `n_key_blocks`
+    sampled key blocks (every query block that selected them contributes).
+    Only the sampled slices are copied to the host."""
+    assert w.per_head, "sampled comparison needs per-head shapes"
+    rep = {} if report is None else report
+    dev = torch.device("cuda")
+    x = synth.generate(w, dev)
+    att = prism.PrismAttention(w, dev)
+    att.forward(x["Q"], x["K"], x["V"], x["a2v"])
+    att.backward(x["dO"])
+    torch.cuda.synchronize()
+    assert att.status() == 0, "device status word set"
+    nb, S = att.plan.nb, w.block
+    w1 = w.with_(H=1)
+    scale = 1.0 / math.sqrt(w.d)
+    rng = np.random.default_rng(seed)
+    a2v = f64(x["a2v"])
+    o, L = att.perm_out, att.lists
+    rp_all = L["row_ptr"].cpu().numpy()
+    cp_all = L["col_ptr"].cpu().numpy()
+    errs = dict(O=0.0, dQ=0.0, dKV=0.0)
+    for b in range(w.B):
+        for h in heads:
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            X = {k: f64(x[k][b:b + 1, :, h:h + 1]) for k in ("Q", "K", "V", "dO")}
+            # ---- statistics, shapes, permutation, pooling (whole head) ----
+            st_o = orc.zone_stats(w1, X["V"], a2v[b:b + 1])
+            st_g = f64(att.stats[sl])
+            for k in range(8):
+                sc = max(1e-30, np.abs(st_o[..., k]).max())
+                assert np.abs(st_g[..., k] - st_o[..., k]).max() / sc <= 2e-5, ("stats", k)
+            sid_o, tie_o = orc.assign_shapes(w1, st_o)
+            sid_g = o["shape_id"][sl].cpu().numpy().astype(np.int64)
+            mism = sid_g != sid_o
+            assert not (mism & ~tie_o).any(), "shape id differs on a zone that is not a near tie"
+            sid_use = np.where(mism, sid_g, sid_o)
+            perm_o, inv_o, nval_o = orc.build_permutation(w1, sid_use)
+            assert np.array_equal(o["perm"][sl].cpu().numpy(), perm_o)
+            assert np.array_equal(o["inv"][sl].cpu().numpy(), inv_o)
+            assert np.array_equal(o["n_valid"][sl].cpu().numpy(), nval_o)
+            Qp_o, Kp_o = orc.permute(X["Q"], perm_o), orc.permute(X["K"], perm_o)
+            Vp_o, dOp_o = orc.permute(X["V"], perm_o), orc.permute(X["dO"], perm_o)
+            for nm, ref in (("Qp", Qp_o), ("Kp", Kp_o), ("Vp", Vp_o)):
+                assert np.array_equal(f64(o[nm][sl]), ref), nm
+            assert np.array_equal(f64(att.dOp[sl]), dOp_o)
+            Qb_o, Kb_o = orc.pool(Qp_o, nval_o, S), orc.pool(Kp_o, nval_o, S)
+            Qb_g = f64(o["Qbar"][sl]) + f64(o["Qbar_lo"][sl])
+            Kb_g = f64(o["Kbar"][sl]) + f64(o["Kbar_lo"][sl])
+            assert np.abs(Qb_g - Qb_o).max() <= 1e-11 * max(1.0, np.abs(Qb_o).max())
+            assert np.abs(Kb_g - Kb_o).max() <= 1e-11 * max(1.0, np.abs(Kb_o).max())
+            # ---- the head's CSR lists from the device ----
+            base = (b * w.H + h) * nb
+            lo_, hi_ = int(rp_all[base]), int(rp_all[base + nb])
+            ci = L["col_idx"][lo_:hi_].cpu().numpy().astype(np.int64)
+            Lg = [ci[int(rp_all[base + i]) - lo_:int(rp_all[base + i + 1]) - lo_] for i in range(nb)]
+            c_lo, c_hi = int(cp_all[base]), int(cp_all[base + nb])
+            ri = L["row_idx"][c_lo:c_hi].cpu().numpy().astype(np.int64)
+            cols = orc.csc_from_lists(Lg, nb)
+            for j in range(nb):
+                got = ri[int(cp_all[base + j]) - c_lo:int(cp_all[base + j + 1]) - c_lo]
+                assert np.array_equal(got, cols[j]), ("csc", j)
+            # ---- sampled query blocks: selection, O, LSE, dQ ----
+            realq = np.nonzero(nval_o[0, 0] > 0)[0]
+            partial = [i for i in realq if nval_o[0, 0, i] < S]
+            rows = list(rng.choice(realq, size=min(n_rows, len(realq)), replace=False))
+            if partial and not any(i in partial for i in rows):
+                rows[0] = int(rng.choice(partial))
+            rows = sorted(int(i) for i in rows)
+            Lo, Fo = orc.select_blocks(w1, Qb_o, Kb_o, nval_o, rows=rows)
+            for i in rows:
+                if not np.array_equal(Lg[i], Lo[(0, 0)][i]):
+                    assert Fo[(0, 0)][i], f"list differs on an unflagged row (b={b}, h={h}, i={i})"
+            Lfull = {(0, 0): Lg}
+            Lrows = {(0, 0): [Lg[i] if i in rows else None for i in range(nb)]}
+            Op_o, lse_o = orc.attn_fwd(w1, Qp_o, Kp_o, Vp_o, nval_o, Lrows, scale)
+            dQ_o, _, _ = orc.attn_bwd(w1, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, Lfull, scale,
+                                      rows_only=set(rows))
+            Op_g, lse_g, dQp_g = f64(att.Op[sl]), f64(att.lse[sl]), f64(att.dQp[sl])
+            # the contract is per tensor (per head): max |err| / max |ref|; on a
+            # sample the maxima run over the sampled rows (a smaller, stricter
+            # denominator than the whole head's)
+            rr = np.concatenate([np.arange(i * S, (i + 1) * S) for i in rows])
+            eo = rel_err(Op_g[0, 0, rr], Op_o[0, 0, rr])
+            eq = rel_err(dQp_g[0, 0, rr], dQ_o[0, 0, rr])
+            assert eo <= O_TOL, ("O", b, h, eo)
+            assert eq <= G_TOL, ("dQ", b, h, eq)
+            assert np.abs(lse_g[0, 0, rr] - lse_o[0, 0, rr]).max() <= 2e-2
+            errs["O"], errs["dQ"] = max(errs["O"], eo), max(errs["dQ"], eq)
+            for i in rows:  # per-block figures, reported only
+                r = slice(i * S, (i + 1) * S)
+                rep.setdefault("dQ_worst_block_rel", 0.0)
+                rep["dQ_worst_block_rel"] = max(rep["dQ_worst_block_rel"],
+                                                rel_err(dQp_g[0, 0, r], dQ_o[0, 0, r]))
+                # model order: the unpermuted outputs carry the same rows
+                toks = perm_o[0, 0, r]
+                real = toks >= 0
+                for nm, got in (("O", Op_g), ("dQ", dQp_g)):
+                    mo = f64(getattr(att, nm)[b:b + 1, :, h:h + 1])
+                    assert np.array_equal(mo[0, toks[real], 0], got[0, 0, r][real]), nm
+            # ---- sampled key blocks: dK, dV over every query block that selected them ----
+            realk = [j for j in range(nb) if len(cols[j]) > 0]
+            for j in rng.choice(realk, size=min(n_key_blocks, len(realk)), replace=False):
+                j = int(j)
+                _, dK_o, dV_o = orc.attn_bwd(w1, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, Lfull, scale,
+                                             rows_only=set(int(i) for i in cols[j]))
+                r = slice(j * S, (j + 1) * S)
+                for nm, ref in (("dKp", dK_o), ("dVp", dV_o)):
+                    got = f64(getattr(att, nm)[sl])[0, 0, r]
+                    e = rel_err(got, ref[0, 0, r])  # one key block: its own maximum
+                    assert e <= G_TOL, (nm, b, h, j, e)
+                    errs["dKV"] = max(errs["dKV"], e)
+    rep.update(errs)
+    rep["block_density"] = float(rp_all[-1]) / (w.B * w.H * nb * nb)
+    return rep

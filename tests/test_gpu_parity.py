@@ -78,3 +78,14 @@ def test_128_blocks_full_menu_zone():
                                 dict(topp=1.0)])
 def test_128_blocks_selection_settings(kw):
     pu.compare(_w128(**kw))
+
+
+# --------------------------------------------------------------------------
+# full-size workloads, in the launch configuration of bench.py, on samples
+# the oracle can compute one by one
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,heads", [("720p", [0, 13]), ("1080p", [5]), ("2k", [7])])
+def test_full_size_sampled(name, heads):
+    rep = pu.compare_sampled(synth.WORKLOADS[name], heads)
+    assert rep["O"] <= pu.O_TOL and rep["dQ"] <= pu.G_TOL and rep["dKV"] <= pu.G_TOL

@@ -182,6 +182,20 @@ def test_guidance_zero_statistics_is_isotropic():
     np.testing.assert_allclose(g, 0.5 * np.array([0, 0, 1.0]) + w.eps)
 
 
+def test_audio_guidance_of_a_constant_norm_map_is_isotropic():
+    """A zone whose A2V norms are all equal has no audio direction: round-off
+    variances (any size up to 1e-20 nbar^2) give v_hat = 1/3 each, while a
+    small real variance keeps its direction."""
+    w = synth.WORKLOADS["2k"]
+    for noise in ([3e-30, 1e-31, 0.0], [0.0, 9e-13 / 1e9, 0.0]):
+        st = np.array([1.0, 2.0, 3.0] + noise + [11.0, 768.0])
+        g = orc.guidance(w, st, 11.0)
+        np.testing.assert_allclose(g, np.array([1, 2, 3]) / 6.0 + 1.0 / 3.0 + w.eps)
+    st = np.array([1.0, 2.0, 3.0, 1e-8, 0.0, 3e-8, 11.0, 768.0])
+    g = orc.guidance(w, st, 11.0)
+    np.testing.assert_allclose(g, np.array([1, 2, 3]) / 6.0 + np.array([0.25, 0, 0.75]) + w.eps)
+
+
 def test_assign_shapes_follow_directional_variance():
     """A zone whose values vary only along W must get the finer W extent."""
     w = synth.WORKLOADS["2k"].with_(T=3, Hg=16, W=32, H=1, d=4, use_audio=False)
