@@ -11,6 +11,7 @@ using prism::Plan;
 
 struct prism_plan {
   Plan p;
+  cudaEvent_t trace[2 * PRISM_TRACE_SLOTS];  // optional timing marks, caller-owned
 };
 
 namespace prism {
@@ -63,6 +64,19 @@ inline int ilog2_exact(int v) {
 #define PRISM_CUDA(call)                      \
   do {                                        \
     if ((call) != cudaSuccess) return PRISM_ERR_CUDA; \
+  } while (0)
+
+// Record the begin (end = 0) or end (end = 1) mark of a trace slot, if set.
+inline cudaError_t trace_mark(const prism_plan* plan, int slot, int end, cudaStream_t st) {
+  cudaEvent_t e = plan->trace[2 * slot + end];
+  return e == nullptr ? cudaSuccess : cudaEventRecord(e, st);
+}
+
+#define PRISM_TRACED(slot, call)                            \
+  do {                                                      \
+    PRISM_CUDA(trace_mark(plan, (slot), 0, st));            \
+    PRISM_CUDA(call);                                       \
+    PRISM_CUDA(trace_mark(plan, (slot), 1, st));            \
   } while (0)
 
 }  // namespace
@@ -157,6 +171,7 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   prism_plan* h = static_cast<prism_plan*>(malloc(sizeof(prism_plan)));
   if (h == nullptr) return PRISM_ERR_ARG;
   h->p = p;
+  for (int i = 0; i < 2 * PRISM_TRACE_SLOTS; ++i) h->trace[i] = nullptr;
   *out = h;
   return PRISM_OK;
 }
@@ -247,11 +262,13 @@ int prism_sparse_attn_fwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Plan& p = plan->p;
   if (p.sz.tensor_core_fwd) {
-    PRISM_CUDA(prism::launch_attn_fwd_tc(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op, lse,
-                                         static_cast<uint8_t*>(ws), st));
+    PRISM_TRACED(PRISM_TRACE_ATTN_FWD,
+                 prism::launch_attn_fwd_tc(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op,
+                                           lse, static_cast<uint8_t*>(ws), st));
   } else {
-    PRISM_CUDA(prism::launch_attn_fwd_simt(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op,
-                                           lse, st));
+    PRISM_TRACED(PRISM_TRACE_ATTN_FWD,
+                 prism::launch_attn_fwd_simt(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op,
+                                             lse, st));
   }
   return PRISM_OK;
 }
@@ -283,19 +300,31 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
   if (p.sz.tensor_core_bwd) {
     // dK, dV over the key blocks' lists; dQ over the query blocks' lists
     float* lse2 = reinterpret_cast<float*>(w + p.off_lse2);
-    PRISM_CUDA(prism::launch_bwd_pre(p, Op, dOp, lse, D, lse2, nullptr, st));
-    PRISM_CUDA(prism::launch_attn_dkdv_tc(p, Qp, Kp, Vp, dOp, lse2, D, n_valid, col_ptr, row_idx,
-                                          scale, dKp, dVp, w, st));
-    PRISM_CUDA(prism::launch_attn_dq_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx,
-                                        scale, dQp, w, st));
+    PRISM_TRACED(PRISM_TRACE_BWD_PRE,
+                 prism::launch_bwd_pre(p, Op, dOp, lse, D, lse2, nullptr, st));
+    PRISM_TRACED(PRISM_TRACE_ATTN_DKDV,
+                 prism::launch_attn_dkdv_tc(p, Qp, Kp, Vp, dOp, lse2, D, n_valid, col_ptr,
+                                            row_idx, scale, dKp, dVp, w, st));
+    PRISM_TRACED(PRISM_TRACE_ATTN_DQ,
+                 prism::launch_attn_dq_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx,
+                                          scale, dQp, w, st));
   } else {
     float* dq = reinterpret_cast<float*>(w + p.off_dq);
-    PRISM_CUDA(prism::launch_bwd_pre(p, Op, dOp, lse, D, nullptr, dq, st));
-    PRISM_CUDA(prism::launch_attn_bwd_simt(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr, row_idx,
-                                           scale, dq, dKp, dVp, st));
+    PRISM_TRACED(PRISM_TRACE_BWD_PRE,
+                 prism::launch_bwd_pre(p, Op, dOp, lse, D, nullptr, dq, st));
+    PRISM_TRACED(PRISM_TRACE_ATTN_DKDV,
+                 prism::launch_attn_bwd_simt(p, Qp, Kp, Vp, dOp, lse, D, n_valid, col_ptr,
+                                             row_idx, scale, dq, dKp, dVp, st));
     // dQ in block order, bf16, scaled
-    PRISM_CUDA(prism::launch_dq_convert(p, dq, scale, dQp, st));
+    PRISM_TRACED(PRISM_TRACE_ATTN_DQ, prism::launch_dq_convert(p, dq, scale, dQp, st));
   }
+  return PRISM_OK;
+}
+
+int prism_plan_set_trace_events(prism_plan_t* plan, void* const* events) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  for (int i = 0; i < 2 * PRISM_TRACE_SLOTS; ++i)
+    plan->trace[i] = events == nullptr ? nullptr : static_cast<cudaEvent_t>(events[i]);
   return PRISM_OK;
 }
 

@@ -77,7 +77,7 @@ struct BwdParams {
 
 // 14 warps: 3-4 per SM sub-partition, so at most 128 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+    attn_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmdO, BwdParams P) {
@@ -463,11 +463,11 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
   cudaError_t e = cudaMemsetAsync(a.status + WS_BWD_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const long long g = a.cols < sm_count() ? a.cols : sm_count();
-  attn_bwd_tc_kernel<<<static_cast<unsigned>(g), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO,
+  attn_dkdv_tc_kernel<<<static_cast<unsigned>(g), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO,
                                                                             a);
   return cudaGetLastError();
 }

@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
         "prism_permute": [P, P, P, P, P],
         "prism_sparse_attn_bwd": [P] + [P] * 11 + [ctypes.c_float] + [P] * 5,
         "prism_unpermute": [P, P, P, P, P],
+        "prism_plan_set_trace_events": [P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -194,6 +195,29 @@ class Plan:
 
     def device_status(self, ws: torch.Tensor) -> int:
         return lib().prism_device_status(self.h, _ptr(ws), _stream())
+
+    TRACE_SLOTS = ("attn_fwd", "bwd_pre", "attn_dkdv", "attn_dq")
+
+    def set_trace_events(self, events=None):
+        """prism_plan_set_trace_events: `events` maps a slot name of
+        TRACE_SLOTS to a (begin, end) pair of torch.cuda.Event(enable_timing=True),
+        or is None to clear every slot.  Each event is recorded once here on
+        the current stream so that its CUDA handle exists."""
+        if events is None:
+            _check(lib().prism_plan_set_trace_events(self.h, None), "prism_plan_set_trace_events")
+            self._trace_keep = None
+            return
+        arr = (ctypes.c_void_p * (2 * len(self.TRACE_SLOTS)))()
+        for i, name in enumerate(self.TRACE_SLOTS):
+            pair = events.get(name)
+            if pair is None:
+                continue
+            for j, e in enumerate(pair):
+                if e.cuda_event == 0:
+                    e.record(torch.cuda.current_stream())
+                arr[2 * i + j] = e.cuda_event
+        self._trace_keep = events
+        _check(lib().prism_plan_set_trace_events(self.h, arr), "prism_plan_set_trace_events")
 
     def zone_stats(self, V, a2v, stats=None):
         w = self.w

@@ -17,7 +17,7 @@ def L():
 
 def test_exports_every_declared_function(L):
     names = prism.declared_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     for n in names:
         assert hasattr(L, n), n
 
@@ -81,3 +81,13 @@ def test_misaligned_pointers_are_rejected_before_any_launch(L):
     good = ctypes.c_void_p(0x1000)
     assert L.prism_zone_stats(p.h, bad, good, good, None) == -2
     assert L.prism_permute(p.h, good, good, bad, None) == -2
+
+
+def test_trace_events_can_be_set_and_cleared_without_a_gpu(L):
+    # recording only happens when an attention entry point runs; setting and
+    # clearing the handles touches no device
+    p = prism.Plan(synth.WORKLOADS["tiny"])
+    arr = (ctypes.c_void_p * (2 * len(prism.Plan.TRACE_SLOTS)))()
+    assert L.prism_plan_set_trace_events(p.h, arr) == 0
+    assert L.prism_plan_set_trace_events(p.h, None) == 0
+    assert L.prism_plan_set_trace_events(None, None) == -1
