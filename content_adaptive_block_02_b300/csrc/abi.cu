@@ -104,7 +104,8 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   if (c.B < 1 || c.H < 1 || c.d < 1 || c.T < 1 || c.Hg < 1 || c.W < 1 || c.zT < 1 ||
       c.zH < 1 || c.zW < 1 || c.block_tokens < 1 || c.Ca < 1 || c.topk_floor < 0 ||
       !(c.topp >= 0.f) || c.n_shapes < 1 || c.n_shapes > PRISM_MAX_SHAPES ||
-      !(c.alpha == c.alpha) || !(c.eps >= 0.0))
+      !(c.alpha == c.alpha) || !(c.eps >= 0.0) ||
+      (c.fault_inject != 0 && c.fault_inject != PRISM_FAULT_STARVE_LOADS))
     return PRISM_ERR_ARG;
   if (c.d % 32 != 0 || c.d > 128) return PRISM_ERR_UNSUPPORTED;
   const int lS = ilog2_exact(c.block_tokens);

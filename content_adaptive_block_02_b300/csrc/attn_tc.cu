@@ -73,6 +73,7 @@ struct FwdParams {
   int nb;
   float scale_log2;
   unsigned long long limit;
+  int starve;  // fault injection (test only): the producer issues no loads
 };
 
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -144,11 +145,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int st = use % kStages;
           if (!W.wait(&sm.kv_empty[st], ((use / kStages) & 1) ^ 1, 2)) { ok = false; break; }
           uint8_t* kb = kvbuf + st * 2 * kTile;
-          mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
-          tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
-          tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
-          tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
-          tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+          if (!P.starve) {  // fault injection: no loads, consumers time out
+            mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
+            tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
+            tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
+            tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
+            tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+          }
           ++use;
         }
         if (!ok) break;
@@ -488,6 +491,7 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   a.nb = p.sz.nb;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
+  a.starve = c.fault_inject == PRISM_FAULT_STARVE_LOADS ? 1 : 0;
   cudaError_t e = cudaMemsetAsync(a.status + WS_FWD_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   const size_t smem = 2ull * kStages * kTile + 1024;  // K + V per stage

@@ -73,6 +73,7 @@ struct BwdParams {
   int nb;
   float scale, scale_log2;
   unsigned long long limit;
+  int starve;  // fault injection (test only): the producer issues no loads
 };
 
 // 14 warps: 3-4 per SM sub-partition, so at most 128 registers per thread.
@@ -150,11 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int yk = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
         if (!W.wait(&sm.kv_empty, (items & 1) ^ 1, 22)) break;
         ++items;
-        mbar_expect_tx(&sm.kv_full, 2 * kTile);
-        tma_load_2d(kbuf, &tmK, &sm.kv_full, 0, yk);
-        tma_load_2d(kbuf + kTile / 2, &tmK, &sm.kv_full, 64, yk);
-        tma_load_2d(vbuf, &tmV, &sm.kv_full, 0, yk);
-        tma_load_2d(vbuf + kTile / 2, &tmV, &sm.kv_full, 64, yk);
+        if (!P.starve) {  // fault injection: no loads, consumers time out
+          mbar_expect_tx(&sm.kv_full, 2 * kTile);
+          tma_load_2d(kbuf, &tmK, &sm.kv_full, 0, yk);
+          tma_load_2d(kbuf + kTile / 2, &tmK, &sm.kv_full, 64, yk);
+          tma_load_2d(vbuf, &tmV, &sm.kv_full, 0, yk);
+          tma_load_2d(vbuf + kTile / 2, &tmV, &sm.kv_full, 64, yk);
+        }
         for (int t = beg; t < end; ++t) {
           const int i = P.row_idx[t];
           const long long yq = bh * P.Np + static_cast<long long>(i) * kS;
@@ -163,13 +166,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = stage(s);
           sm.stage_i[s] = i;
           sm.stage_nvq[s] = P.n_valid[bh * P.nb + i];
-          mbar_expect_tx(&sm.qdo_full[s], 2 * kTile + 1024);
-          tma_load_2d(st, &tmQ, &sm.qdo_full[s], 0, static_cast<int>(yq));
-          tma_load_2d(st + kTile / 2, &tmQ, &sm.qdo_full[s], 64, static_cast<int>(yq));
-          tma_load_2d(st + kTile, &tmdO, &sm.qdo_full[s], 0, static_cast<int>(yq));
-          tma_load_2d(st + kTile + kTile / 2, &tmdO, &sm.qdo_full[s], 64, static_cast<int>(yq));
-          bulk_load(st + 2 * kTile, P.lse2 + yq, 512, &sm.qdo_full[s]);
-          bulk_load(st + 2 * kTile + 512, P.D + yq, 512, &sm.qdo_full[s]);
+          if (!P.starve) {  // fault injection: no loads, consumers time out
+            mbar_expect_tx(&sm.qdo_full[s], 2 * kTile + 1024);
+            tma_load_2d(st, &tmQ, &sm.qdo_full[s], 0, static_cast<int>(yq));
+            tma_load_2d(st + kTile / 2, &tmQ, &sm.qdo_full[s], 64, static_cast<int>(yq));
+            tma_load_2d(st + kTile, &tmdO, &sm.qdo_full[s], 0, static_cast<int>(yq));
+            tma_load_2d(st + kTile + kTile / 2, &tmdO, &sm.qdo_full[s], 64, static_cast<int>(yq));
+            bulk_load(st + 2 * kTile, P.lse2 + yq, 512, &sm.qdo_full[s]);
+            bulk_load(st + 2 * kTile + 512, P.D + yq, 512, &sm.qdo_full[s]);
+          }
           ++use;
         }
       }
@@ -461,6 +466,7 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
+  a.starve = c.fault_inject == PRISM_FAULT_STARVE_LOADS ? 1 : 0;
   cudaError_t e = cudaMemsetAsync(a.status + WS_BWD_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

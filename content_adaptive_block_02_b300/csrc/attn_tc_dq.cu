@@ -64,6 +64,7 @@ struct DqParams {
   int nb;
   float scale, scale_log2;
   unsigned long long limit;
+  int starve;  // fault injection (test only): the producer issues no loads
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -141,22 +142,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Q_i, dO_i once the previous item's S / dP products are done
         if (!W.wait(&sm.qd_empty, (items & 1) ^ 1, 62)) break;
         ++items;
-        mbar_expect_tx(&sm.qd_full, 2 * kTile);
-        tma_load_2d(dsm + kOffQ, &tmQ, &sm.qd_full, 0, yq);
-        tma_load_2d(dsm + kOffQ + kTile / 2, &tmQ, &sm.qd_full, 64, yq);
-        tma_load_2d(dsm + kOffDO, &tmdO, &sm.qd_full, 0, yq);
-        tma_load_2d(dsm + kOffDO + kTile / 2, &tmdO, &sm.qd_full, 64, yq);
+        if (!P.starve) {  // fault injection: no loads, consumers time out
+          mbar_expect_tx(&sm.qd_full, 2 * kTile);
+          tma_load_2d(dsm + kOffQ, &tmQ, &sm.qd_full, 0, yq);
+          tma_load_2d(dsm + kOffQ + kTile / 2, &tmQ, &sm.qd_full, 64, yq);
+          tma_load_2d(dsm + kOffDO, &tmdO, &sm.qd_full, 0, yq);
+          tma_load_2d(dsm + kOffDO + kTile / 2, &tmdO, &sm.qd_full, 64, yq);
+        }
         for (int t = beg; t < end; ++t) {
           const int j = P.col_idx[t];
           const int y = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
           const int st = use % kStages;
           if (!W.wait(&sm.kv_empty[st], ((use / kStages) & 1) ^ 1, 63)) { ok = false; break; }
           uint8_t* kb = kvbuf + st * 2 * kTile;
-          mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
-          tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
-          tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
-          tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
-          tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+          if (!P.starve) {  // fault injection: no loads, consumers time out
+            mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
+            tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
+            tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
+            tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
+            tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+          }
           ++use;
         }
       }
@@ -391,6 +396,7 @@ cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t*
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
+  a.starve = c.fault_inject == PRISM_FAULT_STARVE_LOADS ? 1 : 0;
   cudaError_t e = cudaMemsetAsync(a.status + WS_DQ_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -49,7 +49,14 @@ class Config(ctypes.Structure):
         ("per_head", ctypes.c_int), ("use_video", ctypes.c_int), ("use_audio", ctypes.c_int),
         ("topk_floor", ctypes.c_int), ("topp", ctypes.c_float),
         ("timeout_cycles", ctypes.c_ulonglong), ("attn_kernel", ctypes.c_int),
+        ("fault_inject", ctypes.c_int),
     ]
+
+
+FAULT_STARVE_LOADS = 1   # PRISM_FAULT_STARVE_LOADS: failure-detection tests only
+PRISM_OK = 0
+PRISM_ERR_DEVICE_TIMEOUT = -6
+PRISM_ERR_DEVICE_BOUNDS = -7
 
 
 class Sizes(ctypes.Structure):
@@ -133,7 +140,8 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def make_config(w, timeout_cycles: int = 0, attn_kernel: int = 0) -> Config:
+def make_config(w, timeout_cycles: int = 0, attn_kernel: int = 0,
+                fault_inject: int = 0) -> Config:
     """Config from a workload description (``synth.Workload``-like object)."""
     c = Config()
     c.B, c.H, c.d = w.B, w.H, w.d
@@ -152,15 +160,16 @@ def make_config(w, timeout_cycles: int = 0, attn_kernel: int = 0) -> Config:
     c.topp = w.topp
     c.timeout_cycles = timeout_cycles
     c.attn_kernel = attn_kernel
+    c.fault_inject = fault_inject
     return c
 
 
 class Plan:
     """Host plan of one problem size (prism_plan_create / prism_plan_query)."""
 
-    def __init__(self, w, timeout_cycles: int = 0, attn_kernel: int = 0):
+    def __init__(self, w, timeout_cycles: int = 0, attn_kernel: int = 0, fault_inject: int = 0):
         self.w = w
-        self.cfg = make_config(w, timeout_cycles, attn_kernel)
+        self.cfg = make_config(w, timeout_cycles, attn_kernel, fault_inject)
         h = ctypes.c_void_p()
         _check(lib().prism_plan_create(ctypes.byref(self.cfg), ctypes.byref(h)), "prism_plan_create")
         self.h = h
@@ -192,6 +201,10 @@ class Plan:
         t = torch.empty(self.sz.ws_bytes, dtype=torch.uint8, device=device)
         _check(lib().prism_ws_init(self.h, _ptr(t), _stream()), "prism_ws_init")
         return t
+
+    def ws_init(self, ws: torch.Tensor):
+        """prism_ws_init: clear the status word of an existing workspace."""
+        _check(lib().prism_ws_init(self.h, _ptr(ws), _stream()), "prism_ws_init")
 
     def device_status(self, ws: torch.Tensor) -> int:
         return lib().prism_device_status(self.h, _ptr(ws), _stream())
@@ -321,9 +334,11 @@ class PrismAttention:
     (dQ, dK, dV) in the same layout.  Buffers are allocated once per plan and
     reused across calls."""
 
-    def __init__(self, w, device="cuda", attn_kernel: int = 0):
+    def __init__(self, w, device="cuda", attn_kernel: int = 0, timeout_cycles: int = 0,
+                 fault_inject: int = 0):
         self.w = w
-        self.plan = Plan(w, attn_kernel=attn_kernel)
+        self.plan = Plan(w, timeout_cycles=timeout_cycles, attn_kernel=attn_kernel,
+                         fault_inject=fault_inject)
         self.device = torch.device(device)
         self.scale = 1.0 / math.sqrt(w.d)
         self.ws = self.plan.ws(self.device)

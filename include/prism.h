@@ -74,7 +74,16 @@ typedef struct prism_config {
   int attn_kernel;        /* 0: tensor-core (tcgen05) attention where supported
                              (S = 128, d = 128), CUDA-core kernels otherwise;
                              1: CUDA-core kernels always                         */
+  int fault_inject;       /* 0 in normal use.  PRISM_FAULT_STARVE_LOADS (tests of
+                             failure detection only): the producer warps of the
+                             tensor-core attention kernels issue no loads, so the
+                             first bounded wait of their consumers runs out; the
+                             kernels free their tensor memory and return, and the
+                             status word reads PRISM_ERR_DEVICE_TIMEOUT.  No copy
+                             is in flight when they return.                       */
 } prism_config_t;
+
+#define PRISM_FAULT_STARVE_LOADS 1
 
 /* Derived sizes of a plan. */
 typedef struct prism_sizes {

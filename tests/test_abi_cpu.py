@@ -91,3 +91,11 @@ def test_trace_events_can_be_set_and_cleared_without_a_gpu(L):
     assert L.prism_plan_set_trace_events(p.h, arr) == 0
     assert L.prism_plan_set_trace_events(p.h, None) == 0
     assert L.prism_plan_set_trace_events(None, None) == -1
+
+
+def test_unknown_fault_injection_setting_is_rejected(L):
+    w = synth.WORKLOADS["tiny"]
+    assert prism.Plan(w, fault_inject=prism.FAULT_STARVE_LOADS).cfg.fault_inject == 1
+    with pytest.raises(prism.PrismError) as e:
+        prism.Plan(w, fault_inject=7)
+    assert e.value.code == -1
