@@ -109,6 +109,89 @@ __device__ __forceinline__ float lines_variance(const uint32_t* tile, int na, in
   return acc;
 }
 
+// A2V norm map of one zone: n_i = ||a2v_i||_2 and its directional
+// statistics, in fp64.  The audio directional variance is a ratio of
+// variances that can be tiny (a norm map that is nearly constant over the
+// zone), so it is computed in fp64 throughout: 768 norms and ~350 lines per
+// zone.  Written to slots 3..7 of every head's record.
+__device__ void audio_zone_stats(const prism_config_t& c, const ZoneGeom& g, int b, int z, int Z,
+                                 const uint16_t* __restrict__ a2v, float* __restrict__ stats,
+                                 uint8_t* smem) {
+  const int vol = g.vt * g.vy * g.vx;
+  const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
+  double* nmap = reinterpret_cast<double*>(smem);
+  __shared__ double dred[32 * 4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int li = warp; li < vol; li += nw) {
+    const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
+    const long long n =
+        (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
+    const uint16_t* row = a2v + (static_cast<long long>(b) * N + n) * c.Ca;
+    double s = 0.0;
+    for (int k = lane; k < c.Ca; k += 32) {
+      const double v = bf16_to_f(row[k]);
+      s = fma(v, v, s);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) nmap[li] = sqrt(s);
+  }
+  __syncthreads();
+  // line variances of the scalar map, thread per line
+  double acc[4] = {0.0, 0.0, 0.0, 0.0};
+  const int nlT = g.vy * g.vx, nlH = g.vt * g.vx, nlW = g.vt * g.vy;
+  for (int ln = threadIdx.x; ln < nlT + nlH + nlW; ln += blockDim.x) {
+    int base, len, step, axis;
+    if (ln < nlT) {
+      axis = 0; base = ln; len = g.vt; step = g.vy * g.vx;
+    } else if (ln < nlT + nlH) {
+      const int l = ln - nlT;
+      axis = 1; base = (l / g.vx) * g.vy * g.vx + (l % g.vx); len = g.vy; step = g.vx;
+    } else {
+      const int l = ln - nlT - nlH;
+      axis = 2; base = l * g.vx; len = g.vx; step = 1;
+    }
+    if (len < 2) continue;
+    double m = 0.0;
+    for (int k = 0; k < len; ++k) m += nmap[base + k * step];
+    m /= static_cast<double>(len);
+    double s = 0.0;
+    for (int k = 0; k < len; ++k) {
+      const double e = nmap[base + k * step] - m;
+      s = fma(e, e, s);
+    }
+    acc[axis] += s / static_cast<double>(len);
+  }
+  for (int li = threadIdx.x; li < vol; li += blockDim.x) acc[3] += nmap[li];
+  // fixed-order reduction (deterministic)
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+  __syncthreads();
+  if (lane == 0)
+    for (int k = 0; k < 4; ++k) dred[warp * 4 + k] = acc[k];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < 4; ++k) {
+      double s = 0.0;
+      for (int q = 0; q < nw; ++q) s += dred[q * 4 + k];
+      acc[k] = s;
+    }
+    const double nl[3] = {static_cast<double>(nlT), static_cast<double>(nlH),
+                          static_cast<double>(nlW)};
+    const int len[3] = {g.vt, g.vy, g.vx};
+    float out[5];
+    for (int a = 0; a < 3; ++a) out[a] = len[a] >= 2 ? static_cast<float>(acc[a] / nl[a]) : 0.f;
+    out[3] = static_cast<float>(acc[3] / static_cast<double>(vol));
+    out[4] = static_cast<float>(vol);
+    for (int hh = 0; hh < c.H; ++hh) {
+      float* o = stats + ((static_cast<long long>(b) * c.H + hh) * Z + z) * 8;
+      for (int k = 0; k < 5; ++k) o[3 + k] = out[k];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
     prism_config_t c, int nzH, int nzW, int Z, const uint16_t* __restrict__ V,
     const uint16_t* __restrict__ a2v, float* __restrict__ stats) {
@@ -164,81 +247,149 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
         o[a] = len[a] >= 2 ? acc[a] / (nl[a] * static_cast<float>(c.d)) : 0.f;
     }
   } else {
-    // ---- A2V norm map of the zone: n_i = ||a2v_i||_2, in fp64 ----
-    // The audio directional variance is a ratio of variances that can be
-    // tiny (a norm map that is nearly constant over the zone), so it is
-    // computed in fp64 throughout: 768 norms and ~350 lines per zone.
-    double* nmap = reinterpret_cast<double*>(smem);
-    __shared__ double dred[32 * 4];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int li = warp; li < vol; li += nw) {
+    audio_zone_stats(c, g, b, z, Z, a2v, stats, smem);
+  }
+}
+
+// Zones of at most kPT x kPH x kPW tokens (the 3 x 16 x 16 zones of the
+// latent grids, and smaller ones).  One CTA per (head, zone), heads fastest
+// so that the heads of one zone read the same token rows at the same time.
+// The zone is staged 32 channels at a time (two cp.async stages); each token
+// row (t, y) of the stage is padded by 64 bytes so that both register
+// passes below are free of bank conflicts.  Thread (cp, j): cp = channel
+// pair of the stage (16), j = y in pass A and x in pass B (16).
+//   pass A holds the pencil (t, y = j, all x): lines along W (over x) and
+//          along T (over t) are reduced in registers;
+//   pass B holds the pencil (t, all y, x = j): lines along H (over y).
+// Every line is reduced with a two-pass mean / variance in fp32, so each
+// staged element is read from shared memory twice in all.
+constexpr int kPT = 4, kPH = 16, kPW = 16;
+
+__device__ __forceinline__ float line_ss(const float (&v)[kPW], int n) {
+  // sum of squared deviations from the mean of v[0..n)
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < kPW; ++k)
+    if (k < n) m += v[k];
+  m *= 1.f / static_cast<float>(n);
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < kPW; ++k)
+    if (k < n) {
+      const float e = v[k] - m;
+      s = fmaf(e, e, s);
+    }
+  return s;
+}
+
+__global__ void __launch_bounds__(kStatsThreads, 2) zone_stats_pencil_kernel(
+    prism_config_t c, int nzH, int nzW, int Z, const uint16_t* __restrict__ V,
+    const uint16_t* __restrict__ a2v, float* __restrict__ stats) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float red[32 * 4];
+  const int h = blockIdx.x, z = blockIdx.y, b = blockIdx.z;
+  const ZoneGeom g = zone_geom(c, nzH, nzW, z);
+  if (h == c.H) {
+    audio_zone_stats(c, g, b, z, Z, a2v, stats, smem);
+    return;
+  }
+  const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
+  const int vol = g.vt * g.vy * g.vx;
+  const int rs = g.vx * (kChunk / 2) + 16;  // words per padded token row (t, y)
+  const size_t stage_words = static_cast<size_t>(c.zT) * c.zH * (c.zW * (kChunk / 2) + 16);
+  uint32_t* st0 = reinterpret_cast<uint32_t*>(smem);
+  const int nchunk = c.d / kChunk;
+  auto load_chunk = [&](int ch, int stage) {
+    uint32_t* dst = st0 + stage * stage_words;
+    const int pieces = vol * (kChunk / 8);
+    for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+      const int li = i >> 2, q = i & 3;
       const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
-      const long long n =
-          (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
-      const uint16_t* row = a2v + (static_cast<long long>(b) * N + n) * c.Ca;
-      double s = 0.0;
-      for (int k = lane; k < c.Ca; k += 32) {
-        const double v = bf16_to_f(row[k]);
-        s = fma(v, v, s);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) nmap[li] = sqrt(s);
+      const long long n = (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
+      const uint16_t* src =
+          V + ((static_cast<long long>(b) * N + n) * c.H + h) * c.d + ch * kChunk + q * 8;
+      cp_async16(dst + (t * g.vy + y) * rs + x * (kChunk / 2) + q * 4, src);
+    }
+    cp_async_commit();
+  };
+  const int cp = threadIdx.x & 15, j = threadIdx.x >> 4;
+  float acc[3] = {0.f, 0.f, 0.f};  // sums of line variances along T, H, W
+  load_chunk(0, 0);
+  for (int ch = 0; ch < nchunk; ++ch) {
+    if (ch + 1 < nchunk) {
+      load_chunk(ch + 1, (ch + 1) & 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    // line variances of the scalar map, thread per line
-    double acc[4] = {0.0, 0.0, 0.0, 0.0};
-    const int nlT = g.vy * g.vx, nlH = g.vt * g.vx, nlW = g.vt * g.vy;
-    for (int ln = threadIdx.x; ln < nlT + nlH + nlW; ln += blockDim.x) {
-      int base, len, step, axis;
-      if (ln < nlT) {
-        axis = 0; base = ln; len = g.vt; step = g.vy * g.vx;
-      } else if (ln < nlT + nlH) {
-        const int l = ln - nlT;
-        axis = 1; base = (l / g.vx) * g.vy * g.vx + (l % g.vx); len = g.vy; step = g.vx;
-      } else {
-        const int l = ln - nlT - nlH;
-        axis = 2; base = l * g.vx; len = g.vx; step = 1;
-      }
-      if (len < 2) continue;
-      double m = 0.0;
-      for (int k = 0; k < len; ++k) m += nmap[base + k * step];
-      m /= static_cast<double>(len);
-      double s = 0.0;
-      for (int k = 0; k < len; ++k) {
-        const double e = nmap[base + k * step] - m;
-        s = fma(e, e, s);
-      }
-      acc[axis] += s / static_cast<double>(len);
-    }
-    for (int li = threadIdx.x; li < vol; li += blockDim.x) acc[3] += nmap[li];
-    // fixed-order reduction (deterministic)
+    const uint32_t* tile = st0 + (ch & 1) * stage_words;
+    uint32_t w[kPT][kPW];
+    if (j < g.vy) {
+      // ---- pass A: pencil (t, y = j, x) ----
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+      for (int t = 0; t < kPT; ++t)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
-    __syncthreads();
-    if (lane == 0)
-      for (int k = 0; k < 4; ++k) dred[warp * 4 + k] = acc[k];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int k = 0; k < 4; ++k) {
-        double s = 0.0;
-        for (int q = 0; q < nw; ++q) s += dred[q * 4 + k];
-        acc[k] = s;
+        for (int x = 0; x < kPW; ++x)
+          w[t][x] = (t < g.vt && x < g.vx) ? tile[(t * g.vy + j) * rs + x * (kChunk / 2) + cp] : 0u;
+      if (g.vx >= 2) {
+        const float inv = 1.f / static_cast<float>(g.vx);
+#pragma unroll
+        for (int t = 0; t < kPT; ++t) {
+          if (t < g.vt) {
+            float lo[kPW], hi[kPW];
+#pragma unroll
+            for (int x = 0; x < kPW; ++x) {
+              lo[x] = bf16_lo(w[t][x]);
+              hi[x] = bf16_hi(w[t][x]);
+            }
+            acc[2] += (line_ss(lo, g.vx) + line_ss(hi, g.vx)) * inv;
+          }
+        }
       }
-      const double nl[3] = {static_cast<double>(nlT), static_cast<double>(nlH),
-                            static_cast<double>(nlW)};
-      const int len[3] = {g.vt, g.vy, g.vx};
-      float out[5];
-      for (int a = 0; a < 3; ++a) out[a] = len[a] >= 2 ? static_cast<float>(acc[a] / nl[a]) : 0.f;
-      out[3] = static_cast<float>(acc[3] / static_cast<double>(vol));
-      out[4] = static_cast<float>(vol);
-      for (int hh = 0; hh < c.H; ++hh) {
-        float* o = stats + ((static_cast<long long>(b) * c.H + hh) * Z + z) * 8;
-        for (int k = 0; k < 5; ++k) o[3 + k] = out[k];
+      if (g.vt >= 2) {
+        const float inv = 1.f / static_cast<float>(g.vt);
+#pragma unroll
+        for (int x = 0; x < kPW; ++x) {
+          if (x < g.vx) {
+            float lo[kPW], hi[kPW];
+#pragma unroll
+            for (int t = 0; t < kPW; ++t) {
+              lo[t] = t < kPT ? bf16_lo(w[t < kPT ? t : 0][x]) : 0.f;
+              hi[t] = t < kPT ? bf16_hi(w[t < kPT ? t : 0][x]) : 0.f;
+            }
+            acc[0] += (line_ss(lo, g.vt) + line_ss(hi, g.vt)) * inv;
+          }
+        }
       }
     }
+    if (j < g.vx && g.vy >= 2) {
+      // ---- pass B: pencil (t, y, x = j), lines along H ----
+      const float inv = 1.f / static_cast<float>(g.vy);
+#pragma unroll
+      for (int t = 0; t < kPT; ++t) {
+        if (t < g.vt) {
+          float lo[kPW], hi[kPW];
+#pragma unroll
+          for (int y = 0; y < kPH; ++y) {
+            const uint32_t u = y < g.vy ? tile[(t * g.vy + y) * rs + j * (kChunk / 2) + cp] : 0u;
+            lo[y] = bf16_lo(u);
+            hi[y] = bf16_hi(u);
+          }
+          acc[1] += (line_ss(lo, g.vy) + line_ss(hi, g.vy)) * inv;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  block_sum<3>(acc, red);
+  if (threadIdx.x == 0) {
+    const float nl[3] = {static_cast<float>(g.vy * g.vx), static_cast<float>(g.vt * g.vx),
+                         static_cast<float>(g.vt * g.vy)};
+    const int len[3] = {g.vt, g.vy, g.vx};
+    float* o = stats + ((static_cast<long long>(b) * c.H + h) * Z + z) * 8;
+    for (int a = 0; a < 3; ++a)
+      o[a] = len[a] >= 2 ? acc[a] / (nl[a] * static_cast<float>(c.d)) : 0.f;
   }
 }
 
@@ -341,6 +492,18 @@ cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* 
   const size_t smem_video = 2ull * vol * kChunk * 2;
   const size_t smem_audio = static_cast<size_t>(vol) * sizeof(double);
   const size_t smem = smem_video > smem_audio ? smem_video : smem_audio;
+  if (c.zT <= kPT && c.zH <= kPH && c.zW <= kPW && p.sz.Z <= 65535) {
+    const size_t stage_words = static_cast<size_t>(c.zT) * c.zH * (c.zW * (kChunk / 2) + 16);
+    const size_t sv = 2 * stage_words * 4;
+    const size_t sm = sv > smem_audio ? sv : smem_audio;
+    cudaError_t e = cudaFuncSetAttribute(zone_stats_pencil_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sm));
+    if (e != cudaSuccess) return e;
+    zone_stats_pencil_kernel<<<dim3(c.H + 1, p.sz.Z, c.B), kStatsThreads, sm, st>>>(
+        c, p.sz.nzH, p.sz.nzW, p.sz.Z, V, a2v, stats);
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaFuncSetAttribute(zone_stats_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

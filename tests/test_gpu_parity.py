@@ -69,6 +69,12 @@ def test_128_blocks_both_kernels(attn_kernel):
     assert rep["O_max_rel"] <= pu.O_TOL
 
 
+def test_128_blocks_wide_zone():
+    """3 x 8 x 32 zones: wider than the register-pencil statistics kernel
+    handles (16 tokens per line), so the general statistics kernel runs."""
+    pu.compare(_w128(zone=(3, 8, 32)))
+
+
 def test_128_blocks_full_menu_zone():
     """4 x 16 x 16 zones admit every shape of the 128-token menu."""
     pu.compare(_w128(zone=(4, 16, 16), T=8))
