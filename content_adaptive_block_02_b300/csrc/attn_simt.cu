@@ -225,32 +225,52 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
 
 // D[b,h,s] = sum_c dOp * Op (fp32); when lse2 is given, also
 // lse2 = lse * log2(e); when dQacc is given, that row of the accumulator is
-// cleared.  One warp per row of d channels.
+// cleared.  Four lanes per row of d channels (d <= 128: at most four 16-byte
+// pieces of O and of dO per lane, all loads issued before the first use).
 __global__ void bwd_pre_kernel(long long rows, int d, const uint16_t* __restrict__ Op,
                                const uint16_t* __restrict__ dOp, const float* __restrict__ lse,
                                float* __restrict__ D, float* __restrict__ lse2,
                                float* __restrict__ dQacc) {
-  const int lane = threadIdx.x & 31;
-  const long long row = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
-  if (row >= rows) return;
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long row = tid >> 2;
+  const int sub = static_cast<int>(tid & 3);
+  const bool live = row < rows;  // no early return: the row's lanes shuffle below
+  const int P = d / 8;           // 16-byte pieces per row
   float s = 0.f;
-  const int P = d / 8;
-  for (int q = lane; q < P; q += 32) {
-    const uint4 o = ldg_nc_v4(Op + row * d + q * 8), g = ldg_nc_v4(dOp + row * d + q * 8);
-    const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+  if (live) {
+    const uint16_t* orow = Op + row * d;
+    const uint16_t* grow = dOp + row * d;
+    uint4 ov[4], gv[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      s = fmaf(bf16_lo(ow[k]), bf16_lo(gw[k]), s);
-      s = fmaf(bf16_hi(ow[k]), bf16_hi(gw[k]), s);
+      const int q = sub + 4 * k;
+      if (q < P) {
+        ov[k] = ldg_nc_v4(orow + q * 8);
+        gv[k] = ldg_nc_v4(grow + q * 8);
+      }
     }
-    if (dQacc != nullptr) {
-      float4* dq = reinterpret_cast<float4*>(dQacc + row * d + q * 8);
-      dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = sub + 4 * k;
+      if (q < P) {
+        const uint32_t ow[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+        const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s = fmaf(bf16_lo(ow[e]), bf16_lo(gw[e]), s);
+          s = fmaf(bf16_hi(ow[e]), bf16_hi(gw[e]), s);
+        }
+        if (dQacc != nullptr) {
+          float4* dq = reinterpret_cast<float4*>(dQacc + row * d + q * 8);
+          dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
     }
   }
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) {
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  if (live && sub == 0) {
     D[row] = s;
     if (lse2 != nullptr) lse2[row] = lse[row] * 1.4426950408889634f;
   }
@@ -260,7 +280,7 @@ cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dO
                            const float* lse, float* D, float* lse2, float* dQacc,
                            cudaStream_t st) {
   const long long rows = static_cast<long long>(p.cfg.B) * p.cfg.H * p.sz.Np;
-  bwd_pre_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(
+  bwd_pre_kernel<<<static_cast<unsigned>((rows * 4 + 255) / 256), 256, 0, st>>>(
       rows, p.cfg.d, Op, dOp, lse, D, lse2, dQacc);
   return cudaGetLastError();
 }

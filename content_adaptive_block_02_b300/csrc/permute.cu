@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
     uint16_t* __restrict__ Vp, float* __restrict__ Qh, float* __restrict__ Ql,
     float* __restrict__ Kh, float* __restrict__ Kl, int32_t* __restrict__ n_valid) {
   extern __shared__ __align__(16) float2 red2[];
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;  // heads fastest: the heads
+                                                                 // of a block share token rows
   const int S = c.block_tokens, d = c.d, P = d / 8;
   const int G = kPermThreads / P;  // tokens handled per pass
   const int q = threadIdx.x % P, grp = threadIdx.x / P;
@@ -79,34 +80,49 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
 #pragma unroll
   for (int k = 0; k < 8; ++k) sq[k] = sk[k] = df{0.f, 0.f};
   const long long slot0 = static_cast<long long>(blk) * S;
-  for (int k = grp; k < S; k += G) {
-    const long long dst = (bh * Np + slot0 + k) * d + q * 8;
-    uint4 vq = make_uint4(0, 0, 0, 0), vk = vq, vv = vq;
-    if (k < nv) {
-      const long long n = slot_token(c, g, k);
-      const long long src = ((static_cast<long long>(b) * N + n) * c.H + h) * d + q * 8;
-      vq = ldg_nc_v4(Q + src);
-      vk = ldg_nc_v4(K + src);
-      vv = ldg_nc_v4(V + src);
-      const uint32_t wq[4] = {vq.x, vq.y, vq.z, vq.w};
-      const uint32_t wk[4] = {vk.x, vk.y, vk.z, vk.w};
+  constexpr int U = 4;  // tokens per thread in flight
+  for (int k0 = grp; k0 < S; k0 += U * G) {
+    uint4 vq[U], vk[U], vv[U];
+    long long nn[U];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        sq[2 * j] = df_add(sq[2 * j], df{bf16_lo(wq[j]), 0.f});
-        sq[2 * j + 1] = df_add(sq[2 * j + 1], df{bf16_hi(wq[j]), 0.f});
-        sk[2 * j] = df_add(sk[2 * j], df{bf16_lo(wk[j]), 0.f});
-        sk[2 * j + 1] = df_add(sk[2 * j + 1], df{bf16_hi(wk[j]), 0.f});
+    for (int u = 0; u < U; ++u) {
+      const int k = k0 + u * G;
+      vq[u] = vk[u] = vv[u] = make_uint4(0, 0, 0, 0);
+      nn[u] = -1;
+      if (k < nv) {  // nv <= S
+        nn[u] = slot_token(c, g, k);
+        const long long src = ((static_cast<long long>(b) * N + nn[u]) * c.H + h) * d + q * 8;
+        vq[u] = ldg_nc_v4(Q + src);
+        vk[u] = ldg_nc_v4(K + src);
+        vv[u] = ldg_nc_v4(V + src);
       }
-      if (q == 0) {
-        perm[bh * Np + slot0 + k] = static_cast<int32_t>(n);
-        inv[bh * N + n] = static_cast<int32_t>(slot0 + k);
-      }
-    } else if (q == 0) {
-      perm[bh * Np + slot0 + k] = -1;
     }
-    *reinterpret_cast<uint4*>(Qp + dst) = vq;
-    *reinterpret_cast<uint4*>(Kp + dst) = vk;
-    *reinterpret_cast<uint4*>(Vp + dst) = vv;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = k0 + u * G;
+      if (k >= S) break;
+      const long long dst = (bh * Np + slot0 + k) * d + q * 8;
+      if (nn[u] >= 0) {
+        const uint32_t wq[4] = {vq[u].x, vq[u].y, vq[u].z, vq[u].w};
+        const uint32_t wk[4] = {vk[u].x, vk[u].y, vk[u].z, vk[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          sq[2 * j] = df_add(sq[2 * j], df{bf16_lo(wq[j]), 0.f});
+          sq[2 * j + 1] = df_add(sq[2 * j + 1], df{bf16_hi(wq[j]), 0.f});
+          sk[2 * j] = df_add(sk[2 * j], df{bf16_lo(wk[j]), 0.f});
+          sk[2 * j + 1] = df_add(sk[2 * j + 1], df{bf16_hi(wk[j]), 0.f});
+        }
+        if (q == 0) {
+          perm[bh * Np + slot0 + k] = static_cast<int32_t>(nn[u]);
+          inv[bh * N + nn[u]] = static_cast<int32_t>(slot0 + k);
+        }
+      } else if (q == 0) {
+        perm[bh * Np + slot0 + k] = -1;
+      }
+      *reinterpret_cast<uint4*>(Qp + dst) = vq[u];
+      *reinterpret_cast<uint4*>(Kp + dst) = vk[u];
+      *reinterpret_cast<uint4*>(Vp + dst) = vv[u];
+    }
   }
   // cross-group reduction of the channel sums, fixed order
   float2* rq = red2;
@@ -218,7 +234,8 @@ cudaError_t launch_permute_pool(const Plan& p, const uint8_t* shape_id, const ui
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(p.sz.nb, c.H, c.B);
+  if (p.sz.nb > 65535) return cudaErrorInvalidValue;
+  dim3 grid(c.H, p.sz.nb, c.B);
   permute_pool_kernel<<<grid, kPermThreads, smem, st>>>(
       c, p.sz.nzH, p.sz.nzW, p.sz.blocks_per_zone, p.sz.Z, p.sz.nb, p.sz.Np, m, shape_id, Q, K,
       V, perm, inv, Qp, Kp, Vp, Qh, Ql, Kh, Kl, n_valid);

@@ -110,10 +110,11 @@ __device__ __forceinline__ float lines_variance(const uint32_t* tile, int na, in
 }
 
 // A2V norm map of one zone: n_i = ||a2v_i||_2 and its directional
-// statistics, in fp64.  The audio directional variance is a ratio of
-// variances that can be tiny (a norm map that is nearly constant over the
-// zone), so it is computed in fp64 throughout: 768 norms and ~350 lines per
-// zone.  Written to slots 3..7 of every head's record.
+// statistics.  The audio directional variance is a ratio of variances that
+// can be tiny (a norm map that is nearly constant over the zone), so the
+// norms are accurate to ~1e-11 and the line statistics run in fp64: 768
+// norms and ~350 lines per zone.  Written to slots 3..7 of every head's
+// record.
 __device__ void audio_zone_stats(const prism_config_t& c, const ZoneGeom& g, int b, int z, int Z,
                                  const uint16_t* __restrict__ a2v, float* __restrict__ stats,
                                  uint8_t* smem) {
@@ -122,19 +123,38 @@ __device__ void audio_zone_stats(const prism_config_t& c, const ZoneGeom& g, int
   double* nmap = reinterpret_cast<double*>(smem);
   __shared__ double dred[32 * 4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int li = warp; li < vol; li += nw) {
+  // one token per thread: the squares of bf16 values are exact in fp32 and
+  // are summed as a double-float (TwoSum), so n^2 carries ~1e-11 relative
+  // error before the fp64 square root -- far below the 1e-20 nbar^2 floor on
+  // the directional variance, at FP32 rather than FP64 throughput
+  const bool vec = (c.Ca % 8) == 0;
+  for (int li = threadIdx.x; li < vol; li += blockDim.x) {
     const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
     const long long n =
         (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
     const uint16_t* row = a2v + (static_cast<long long>(b) * N + n) * c.Ca;
-    double s = 0.0;
-    for (int k = lane; k < c.Ca; k += 32) {
-      const double v = bf16_to_f(row[k]);
-      s = fma(v, v, s);
-    }
+    float hi = 0.f, lo = 0.f;
+    auto add = [&](float v) {
+      const float p = v * v;
+      const float s2 = hi + p, bb = s2 - hi;
+      lo += (hi - (s2 - bb)) + (p - bb);
+      hi = s2;
+    };
+    if (vec) {
+      const uint4* r4 = reinterpret_cast<const uint4*>(row);
+      for (int k = 0; k < c.Ca / 8; ++k) {
+        const uint4 q = __ldg(r4 + k);
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) nmap[li] = sqrt(s);
+        for (int e = 0; e < 4; ++e) {
+          add(bf16_lo(u[e]));
+          add(bf16_hi(u[e]));
+        }
+      }
+    } else {
+      for (int k = 0; k < c.Ca; ++k) add(bf16_to_f(row[k]));
+    }
+    nmap[li] = sqrt(static_cast<double>(hi) + static_cast<double>(lo));
   }
   __syncthreads();
   // line variances of the scalar map, thread per line
@@ -265,21 +285,89 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
 // staged element is read from shared memory twice in all.
 constexpr int kPT = 4, kPH = 16, kPW = 16;
 
-__device__ __forceinline__ float line_ss(const float (&v)[kPW], int n) {
-  // sum of squared deviations from the mean of v[0..n)
+// sum of squared deviations from the mean of v[0..n); with n a compile-time
+// constant (full zones) every predicate folds away
+template <int M>
+__device__ __forceinline__ float line_ss(const float (&v)[M], int n) {
   float m = 0.f;
 #pragma unroll
-  for (int k = 0; k < kPW; ++k)
+  for (int k = 0; k < M; ++k)
     if (k < n) m += v[k];
   m *= 1.f / static_cast<float>(n);
   float s = 0.f;
 #pragma unroll
-  for (int k = 0; k < kPW; ++k)
+  for (int k = 0; k < M; ++k)
     if (k < n) {
       const float e = v[k] - m;
       s = fmaf(e, e, s);
     }
   return s;
+}
+
+// One staged chunk (32 channels) of one zone.  MT x MH x MW bound the zone's
+// real extents; with EXACT the extents are exactly those (a full zone) and
+// the runtime extents are ignored.
+template <int MT, int MH, int MW, bool EXACT>
+__device__ __forceinline__ void pencil_chunk(const uint32_t* __restrict__ tile, int rs, int vt_,
+                                             int vy_, int vx_, int cp, int j, float (&acc)[3]) {
+  const int vt = EXACT ? MT : vt_, vy = EXACT ? MH : vy_, vx = EXACT ? MW : vx_;
+  constexpr int P = kChunk / 2;  // words per token in a stage
+  if (j < vy) {
+    // ---- pass A: pencil (t, y = j, all x): lines along W and along T ----
+    uint32_t w[MT][MW];
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int x = 0; x < MW; ++x)
+        w[t][x] = (t < vt && x < vx) ? tile[(t * vy + j) * rs + x * P + cp] : 0u;
+    if (vx >= 2) {
+      const float inv = 1.f / static_cast<float>(vx);
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        if (t < vt) {
+          float lo[MW], hi[MW];
+#pragma unroll
+          for (int x = 0; x < MW; ++x) {
+            lo[x] = bf16_lo(w[t][x]);
+            hi[x] = bf16_hi(w[t][x]);
+          }
+          acc[2] += (line_ss(lo, vx) + line_ss(hi, vx)) * inv;
+        }
+      }
+    }
+    if (vt >= 2) {
+      const float inv = 1.f / static_cast<float>(vt);
+#pragma unroll
+      for (int x = 0; x < MW; ++x) {
+        if (x < vx) {
+          float lo[MT], hi[MT];
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            lo[t] = bf16_lo(w[t][x]);
+            hi[t] = bf16_hi(w[t][x]);
+          }
+          acc[0] += (line_ss(lo, vt) + line_ss(hi, vt)) * inv;
+        }
+      }
+    }
+  }
+  if (j < vx && vy >= 2) {
+    // ---- pass B: pencil (t, all y, x = j): lines along H ----
+    const float inv = 1.f / static_cast<float>(vy);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      if (t < vt) {
+        float lo[MH], hi[MH];
+#pragma unroll
+        for (int y = 0; y < MH; ++y) {
+          const uint32_t u = y < vy ? tile[(t * vy + y) * rs + j * P + cp] : 0u;
+          lo[y] = bf16_lo(u);
+          hi[y] = bf16_hi(u);
+        }
+        acc[1] += (line_ss(lo, vy) + line_ss(hi, vy)) * inv;
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kStatsThreads, 2) zone_stats_pencil_kernel(
@@ -324,62 +412,12 @@ __global__ void __launch_bounds__(kStatsThreads, 2) zone_stats_pencil_kernel(
     }
     __syncthreads();
     const uint32_t* tile = st0 + (ch & 1) * stage_words;
-    uint32_t w[kPT][kPW];
-    if (j < g.vy) {
-      // ---- pass A: pencil (t, y = j, x) ----
-#pragma unroll
-      for (int t = 0; t < kPT; ++t)
-#pragma unroll
-        for (int x = 0; x < kPW; ++x)
-          w[t][x] = (t < g.vt && x < g.vx) ? tile[(t * g.vy + j) * rs + x * (kChunk / 2) + cp] : 0u;
-      if (g.vx >= 2) {
-        const float inv = 1.f / static_cast<float>(g.vx);
-#pragma unroll
-        for (int t = 0; t < kPT; ++t) {
-          if (t < g.vt) {
-            float lo[kPW], hi[kPW];
-#pragma unroll
-            for (int x = 0; x < kPW; ++x) {
-              lo[x] = bf16_lo(w[t][x]);
-              hi[x] = bf16_hi(w[t][x]);
-            }
-            acc[2] += (line_ss(lo, g.vx) + line_ss(hi, g.vx)) * inv;
-          }
-        }
-      }
-      if (g.vt >= 2) {
-        const float inv = 1.f / static_cast<float>(g.vt);
-#pragma unroll
-        for (int x = 0; x < kPW; ++x) {
-          if (x < g.vx) {
-            float lo[kPW], hi[kPW];
-#pragma unroll
-            for (int t = 0; t < kPW; ++t) {
-              lo[t] = t < kPT ? bf16_lo(w[t < kPT ? t : 0][x]) : 0.f;
-              hi[t] = t < kPT ? bf16_hi(w[t < kPT ? t : 0][x]) : 0.f;
-            }
-            acc[0] += (line_ss(lo, g.vt) + line_ss(hi, g.vt)) * inv;
-          }
-        }
-      }
-    }
-    if (j < g.vx && g.vy >= 2) {
-      // ---- pass B: pencil (t, y, x = j), lines along H ----
-      const float inv = 1.f / static_cast<float>(g.vy);
-#pragma unroll
-      for (int t = 0; t < kPT; ++t) {
-        if (t < g.vt) {
-          float lo[kPW], hi[kPW];
-#pragma unroll
-          for (int y = 0; y < kPH; ++y) {
-            const uint32_t u = y < g.vy ? tile[(t * g.vy + y) * rs + j * (kChunk / 2) + cp] : 0u;
-            lo[y] = bf16_lo(u);
-            hi[y] = bf16_hi(u);
-          }
-          acc[1] += (line_ss(lo, g.vy) + line_ss(hi, g.vy)) * inv;
-        }
-      }
-    }
+    if (g.vt == 3 && g.vy == 16 && g.vx == 16)
+      pencil_chunk<3, 16, 16, true>(tile, rs, 3, 16, 16, cp, j, acc);
+    else if (g.vt == 4 && g.vy == 16 && g.vx == 16)
+      pencil_chunk<4, 16, 16, true>(tile, rs, 4, 16, 16, cp, j, acc);
+    else
+      pencil_chunk<kPT, kPH, kPW, false>(tile, rs, g.vt, g.vy, g.vx, cp, j, acc);
     __syncthreads();
   }
   block_sum<3>(acc, red);
