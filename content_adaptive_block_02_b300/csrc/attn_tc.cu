@@ -310,10 +310,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           fence_before();
           mbar_arrive(&sm.s_free);
           if (lim >= 64) {
+            // four independent chains of three-input maxima (depth 8, not 64)
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
-              for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[c][e]));
+              for (int e = 0; e < 32; e += 2) {
+                float& a = m4[c * 2 + ((e >> 4) & 1)];
+                a = fmax3(a, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+              }
+            mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
           } else {
 #pragma unroll
             for (int c = 0; c < 2; ++c)
@@ -350,17 +356,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         l *= corr;
         m = m_new;
+        // early, non-blocking look at the release of the P buffer this key
+        // block will write (its PV two blocks back); consumed at the store
+        const bool p_free_early =
+            pidx < 2 || mbar_test(&sm.p_empty[pidx & 1], ((pidx - 2) >> 1) & 1);
         float lsum = 0.f;
         uint32_t pk[32];
         if (lim >= 64) {
+          float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int k0 = 2 * e;
             const float p0 = ex2(fmaf(__uint_as_float(s[k0 >> 5][k0 & 31]), P.scale_log2, -m));
             const float p1 = ex2(fmaf(__uint_as_float(s[(k0 + 1) >> 5][(k0 + 1) & 31]), P.scale_log2, -m));
-            lsum += p0 + p1;
+            ls4[e & 3] += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
+          lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -373,7 +385,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         l += lsum;
         // the PV issued two key blocks ago has finished reading this P buffer
-        if (pidx >= 2) ok = ok && pv_done(pidx - 2, 16);
+        if (!p_free_early) ok = ok && pv_done(pidx - 2, 16);
         if (ok) {
           fence_after();
           tmem_st32(tmem + lane_base + ((pidx & 1) ? TM_P1 : TM_P0) + half * 32, pk);

@@ -285,23 +285,64 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
 // staged element is read from shared memory twice in all.
 constexpr int kPT = 4, kPH = 16, kPW = 16;
 
-// sum of squared deviations from the mean of v[0..n); with n a compile-time
-// constant (full zones) every predicate folds away
+// Packed pairs of fp32 (the two channels of a bf16x2 word) for the fp32x2
+// add / sub / fma of sm_100-class SMs: one instruction for both channels,
+// each rounded exactly as the scalar operation would be.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 unpack2(uint32_t u) {  // bf16x2 -> (lo, hi) fp32
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(u << 16), "r"(u & 0xffff0000u));
+  return r;
+}
+__device__ __forceinline__ f32x2 splat2(float a) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(a));
+  return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ float hsum2(f32x2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return lo + hi;
+}
+
+// Sum over both channels of the squared deviations from the line mean of
+// v[0..n) (two-pass); with n a compile-time constant (full zones) every
+// predicate folds away.
 template <int M>
-__device__ __forceinline__ float line_ss(const float (&v)[M], int n) {
-  float m = 0.f;
+__device__ __forceinline__ float line_ss(const f32x2 (&v)[M], int n) {
+  f32x2 m = 0ull;
 #pragma unroll
   for (int k = 0; k < M; ++k)
-    if (k < n) m += v[k];
-  m *= 1.f / static_cast<float>(n);
-  float s = 0.f;
+    if (k < n) m = add2(m, v[k]);
+  m = mul2(m, splat2(1.f / static_cast<float>(n)));
+  f32x2 s = 0ull;
 #pragma unroll
   for (int k = 0; k < M; ++k)
     if (k < n) {
-      const float e = v[k] - m;
-      s = fmaf(e, e, s);
+      const f32x2 e = sub2(v[k], m);
+      s = fma2(e, e, s);
     }
-  return s;
+  return hsum2(s);
 }
 
 // One staged chunk (32 channels) of one zone.  MT x MH x MW bound the zone's
@@ -325,13 +366,10 @@ __device__ __forceinline__ void pencil_chunk(const uint32_t* __restrict__ tile, 
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         if (t < vt) {
-          float lo[MW], hi[MW];
+          f32x2 v[MW];
 #pragma unroll
-          for (int x = 0; x < MW; ++x) {
-            lo[x] = bf16_lo(w[t][x]);
-            hi[x] = bf16_hi(w[t][x]);
-          }
-          acc[2] += (line_ss(lo, vx) + line_ss(hi, vx)) * inv;
+          for (int x = 0; x < MW; ++x) v[x] = unpack2(w[t][x]);
+          acc[2] += line_ss(v, vx) * inv;
         }
       }
     }
@@ -340,13 +378,10 @@ __device__ __forceinline__ void pencil_chunk(const uint32_t* __restrict__ tile, 
 #pragma unroll
       for (int x = 0; x < MW; ++x) {
         if (x < vx) {
-          float lo[MT], hi[MT];
+          f32x2 v[MT];
 #pragma unroll
-          for (int t = 0; t < MT; ++t) {
-            lo[t] = bf16_lo(w[t][x]);
-            hi[t] = bf16_hi(w[t][x]);
-          }
-          acc[0] += (line_ss(lo, vt) + line_ss(hi, vt)) * inv;
+          for (int t = 0; t < MT; ++t) v[t] = unpack2(w[t][x]);
+          acc[0] += line_ss(v, vt) * inv;
         }
       }
     }
@@ -357,14 +392,11 @@ __device__ __forceinline__ void pencil_chunk(const uint32_t* __restrict__ tile, 
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       if (t < vt) {
-        float lo[MH], hi[MH];
+        f32x2 v[MH];
 #pragma unroll
-        for (int y = 0; y < MH; ++y) {
-          const uint32_t u = y < vy ? tile[(t * vy + y) * rs + j * P + cp] : 0u;
-          lo[y] = bf16_lo(u);
-          hi[y] = bf16_hi(u);
-        }
-        acc[1] += (line_ss(lo, vy) + line_ss(hi, vy)) * inv;
+        for (int y = 0; y < MH; ++y)
+          v[y] = unpack2(y < vy ? tile[(t * vy + y) * rs + j * P + cp] : 0u);
+        acc[1] += line_ss(v, vy) * inv;
       }
     }
   }
