@@ -16,20 +16,25 @@
 //           (A from TMEM, B = K tile from smem), as soon as the softmax warps
 //           have read the previous S tile, so the next score tile is on the
 //           tensor pipe while they work on this one.
-//   warp 10 PV issuer (one thread): O += P V with P in tensor memory (A from
-//           TMEM, B = V tile, MN-major).  Two issuing threads keep the tensor
-//           pipe fed: a tcgen05.mma issue blocks while the pipe's queue is full,
-//           and each issuer's barrier waits overlap the other's MMAs.
-//   warps 0-7  softmax, two warpgroups: warps w and w+4 share the query rows
-//           of TMEM lane quarter w%4 (thread = query row) and split the 128
-//           key columns (and the 128 O columns) in halves.  Per key block: the
-//           half row of S from TMEM to registers, the half maxima exchanged
-//           through shared memory (one 64-thread named barrier per lane
-//           quarter), online softmax in the log2 domain with lazy rescaling
-//           (O in TMEM is rescaled only when the running max grows by more
-//           than 2^8), P (bf16) -> TMEM; at the end O / l -> bf16, LSE.
-// Tensor memory (512 columns): S [0,128), O [128,256), Q [256,320),
-// P0 [320,384), P1 [384,448).
+//   warp 10 PV issuer (one thread): O_h += P_h V_h for each column half h
+//           (keys 64h..64h+63; A = P from TMEM, B = V rows from smem,
+//           MN-major), as soon as that half's P is in.  Two issuing threads
+//           keep the tensor pipe fed: a tcgen05.mma issue blocks while the
+//           pipe's queue is full, and each issuer's waits overlap the other's
+//           MMAs.
+//   warps 0-7  softmax, two independent halves: warps w and w+4 share the
+//           query rows of TMEM lane quarter w%4 (thread = query row) and split
+//           the 128 key columns.  Each half keeps its own running max m_h,
+//           row sum l_h and output accumulator O_h = sum_j P_h V_h (all 128
+//           channels), so the halves never wait for each other inside a query
+//           block and the exp work of one overlaps the loads, maxima and
+//           waits of the other.  Online softmax in the log2 domain with lazy
+//           rescaling (O_h is rescaled only when m_h grows by more than 2^8).
+//           At the end of the query block the halves meet once and combine:
+//           O = (O_0 2^(m_0-M) + O_1 2^(m_1-M)) / (l_0 2^(m_0-M) + l_1 2^(m_1-M)),
+//           M = max(m_0, m_1); each half writes 64 of the output channels.
+// Tensor memory (512 columns): S [0,128), O_0 [128,256), O_1 [256,384),
+// Q [384,448), P [448,512) (half h: [448+32h, 480+32h)).
 // Every wait is bounded: on expiry the CTA raises a flag, records the error in
 // the workspace status word, and every role stops issuing and leaves.
 #include <cudaTypedefs.h>
@@ -46,15 +51,15 @@ constexpr int kTile = kS * kD * 2;  // 32 KB
 constexpr int kStages = 3;
 constexpr int kFwdThreads = 352;
 constexpr int kSoftmaxThreads = 256;
-constexpr uint32_t TM_S = 0, TM_O = 128, TM_Q = 256, TM_P0 = 320, TM_P1 = 384;
+constexpr uint32_t TM_S = 0, TM_O0 = 128, TM_O1 = 256, TM_Q = 384, TM_P = 448;
 
 struct FwdShared {
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full, s_free, p_full[2], p_empty[2], q_ready, final_bar;
+  uint64_t s_full, s_free, p_full[2], p_empty[2], q_ready, final_bar;  // p_*: per column half
   uint64_t work_full[2], work_empty[2];
   int work_row[2], work_beg[2], work_end[2], work_nvq[2];
-  float xmax[2][2][128];  // [tile parity][column half][row]: half-row maxima
-  float xsum[2][128];     // [column half][row]: half-row sums at the end
+  float xm[2][128];       // [column half][row]: running max at the end of a query block
+  float xl[2][128];       // [column half][row]: row sum at the end of a query block
   int xok[2][2][4];       // [exchange parity][column half][lane quarter]: still on track
   uint32_t tmem_base;
   int abort;
@@ -93,8 +98,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, kSoftmaxThreads);
-    mbar_init(&sm.p_full[0], kSoftmaxThreads);
-    mbar_init(&sm.p_full[1], kSoftmaxThreads);
+    mbar_init(&sm.p_full[0], kSoftmaxThreads / 2);
+    mbar_init(&sm.p_full[1], kSoftmaxThreads / 2);
     mbar_init(&sm.p_empty[0], 1);
     mbar_init(&sm.p_empty[1], 1);
     mbar_init(&sm.q_ready, kSoftmaxThreads);
@@ -206,23 +211,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (sm.work_row[ws] < 0) break;
         const int n = sm.work_end[ws] - sm.work_beg[ws];
         if (n > 0) {
-          // the first PV overwrites O: the previous block's epilogue has read it
+          // the first PV overwrites O_h: the previous block's epilogue has read it
           if (!W.wait(&sm.q_ready, qcnt & 1, 15)) break;
           ++qcnt;
           for (int jj = 0; jj < n; ++jj) {
-            const uint32_t pb = pidx & 1;
-            if (!W.wait(&sm.p_full[pb], (pidx >> 1) & 1, 7)) { ok = false; break; }
             const int st = use % kStages;
-            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 8)) { ok = false; break; }
-            fence_after();
             const uint64_t vd =
                 sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile + kTile), kTile / 2, 1024);
-            const uint32_t pa = tmem + (pb ? TM_P1 : TM_P0);
+            for (int h = 0; h < 2; ++h) {
+              if (!W.wait(&sm.p_full[h], pidx & 1, 7)) { ok = false; break; }
+              if (h == 0 && !W.wait(&sm.kv_full[st], (use / kStages) & 1, 8)) { ok = false; break; }
+              fence_after();
+              const uint32_t o = tmem + (h ? TM_O1 : TM_O0);
 #pragma unroll
-            for (int kk = 0; kk < kS / 16; ++kk)
-              mma_ts(tmem + TM_O, pa + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idPV,
-                     (jj > 0 || kk > 0) ? 1u : 0u);
-            commit(&sm.p_empty[pb]);
+              for (int k4 = 0; k4 < kS / 32; ++k4) {
+                const int kk = h * (kS / 32) + k4;  // 16-key step: keys 16kk .. 16kk+15
+                mma_ts(o, tmem + TM_P + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idPV,
+                       (jj > 0 || k4 > 0) ? 1u : 0u);
+              }
+              commit(&sm.p_empty[h]);
+            }
+            if (!ok) break;
             commit(&sm.kv_empty[st]);
             ++use;
             ++pidx;
@@ -235,17 +244,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------ softmax ----
-    // Warps w and w+4 meet at a named barrier (64 threads) once per key block
-    // and twice per query block.  A named barrier has no time limit, so the
-    // two never leave a loop on their own: every bounded wait only clears
-    // `ok`, the flags are exchanged at each meeting, and both warps leave
-    // together at the first meeting after either of them failed.
+    // Warps w and w+4 meet at a named barrier (64 threads) three times per
+    // query block: at its start, before the epilogue and after it.  A named
+    // barrier has no time limit, so the two never leave a loop on their own:
+    // every bounded wait only clears `ok`, the flags are exchanged at each
+    // meeting, and both warps leave together at the first meeting after
+    // either of them failed.  (A half that stops inside the key-block loop
+    // stops arriving at s_free; the S issuer's bounded wait then runs out and
+    // the other half's next wait sees the abort flag.)
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;  // query row of the block == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + TM_S + half * 64;
-    const uint32_t tO = tmem + lane_base + TM_O + half * 64;
-    const int c0 = half * 64;  // first key column (and O column) of this half
+    const uint32_t tO = tmem + lane_base + (half ? TM_O1 : TM_O0);  // this half's accumulator
+    const uint32_t tP = tmem + lane_base + TM_P + half * 32;
+    const int c0 = half * 64;  // first key column (and output channel) of this half
     uint32_t xpar = 0;         // parity of the flag slots of the next meeting
     auto meet = [&](bool mine) -> bool {  // pair barrier, returns both flags ANDed
       const int slot = xpar & 1;
@@ -254,11 +267,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
       return mine && sm.xok[slot][half ^ 1][quarter] != 0;
     };
-    // wait until the PV that used P buffer (g & 1) for key block g is done
-    auto pv_done = [&](uint32_t g, uint32_t where) {
-      return W.wait(&sm.p_empty[g & 1], (g >> 1) & 1, where);
+    // wait until column half h's PV of key block g (CTA-local count) is done
+    auto pv_done = [&](int h, uint32_t g, uint32_t where) {
+      return W.wait(&sm.p_empty[h], g & 1, where);
     };
-    uint32_t sidx = 0, pidx = 0, tile = 0;
+    uint32_t sidx = 0, pidx = 0;
     bool ok = true;
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
@@ -292,58 +305,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         fence_before();
         mbar_arrive(&sm.q_ready);
       }
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;  // this half's running max (log2 units) and row sum
       const int32_t* nvb = P.n_valid + bh * P.nb;
       int nvk_next = nvb[P.col_idx[beg]];
       for (int jj = 0; jj < n; ++jj) {
         const int nvk = nvk_next;
         if (jj + 1 < n) nvk_next = nvb[P.col_idx[beg + jj + 1]];  // ahead of its use
         const int lim = nvk - c0;  // columns of this half that hold real keys
-        ok = ok && W.wait(&sm.s_full, sidx & 1, 11);
+        // wait results are made warp-uniform: the TMEM loads and stores
+        // below are warp-collective
+        ok = __all_sync(0xffffffffu, ok && W.wait(&sm.s_full, sidx & 1, 11));
+        ++sidx;
+        if (!ok) break;
         uint32_t s[2][32];
         float mx = -INFINITY;
-        if (ok) {
-          fence_after();
-          tmem_ld32(tS, s[0]);
-          tmem_ld32(tS + 32, s[1]);
-          tmem_ld_wait();
-          fence_before();
-          mbar_arrive(&sm.s_free);
-          if (lim >= 64) {
-            // four independent chains of three-input maxima (depth 8, not 64)
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        fence_after();
+        tmem_ld32(tS, s[0]);
+        tmem_ld32(tS + 32, s[1]);
+        tmem_ld_wait();
+        fence_before();
+        mbar_arrive(&sm.s_free);
+        if (lim >= 64) {
+          // four independent chains of three-input maxima (depth 8, not 64)
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                float& a = m4[c * 2 + ((e >> 4) & 1)];
-                a = fmax3(a, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
-              }
-            mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-          } else {
+            for (int e = 0; e < 32; e += 2) {
+              float& a = m4[c * 2 + ((e >> 4) & 1)];
+              a = fmax3(a, __uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1]));
+            }
+          mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+        } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(s[c][e]));
-          }
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(s[c][e]));
         }
-        ++sidx;
-        const int par = tile & 1;
-        ++tile;
-        sm.xmax[par][half][r] = mx;
-        ok = meet(ok);
-        if (!ok) break;
-        mx = fmaxf(mx, sm.xmax[par][half ^ 1][r]) * P.scale_log2;
+        mx *= P.scale_log2;
         const bool resc = mx > m + 8.f;
         const float m_new = resc ? mx : m;
         const float corr = resc ? ex2(m - m_new) : 1.f;
+        // this half's P buffer and O_h are free once its previous PV is done
+        bool pv_prev = pidx == 0 || mbar_test(&sm.p_empty[half], (pidx - 1) & 1);
         if (jj > 0 && __any_sync(0xffffffffu, resc)) {
-          ok = ok && pv_done(pidx - 1, 12);  // the previous key block's PV
+          if (!pv_prev) ok = ok && pv_done(half, pidx - 1, 12);
+          ok = __all_sync(0xffffffffu, ok);
+          pv_prev = true;
           if (ok) {
             fence_after();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kD / 32; ++c) {
               uint32_t o[32];
               tmem_ld32(tO + c * 32, o);
               tmem_ld_wait();
@@ -356,10 +369,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         l *= corr;
         m = m_new;
-        // early, non-blocking look at the release of the P buffer this key
-        // block will write (its PV two blocks back); consumed at the store
-        const bool p_free_early =
-            pidx < 2 || mbar_test(&sm.p_empty[pidx & 1], ((pidx - 2) >> 1) & 1);
         float lsum = 0.f;
         uint32_t pk[32];
         if (lim >= 64) {
@@ -384,45 +393,55 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         l += lsum;
-        // the PV issued two key blocks ago has finished reading this P buffer
-        if (!p_free_early) ok = ok && pv_done(pidx - 2, 16);
-        if (ok) {
-          fence_after();
-          tmem_st32(tmem + lane_base + ((pidx & 1) ? TM_P1 : TM_P0) + half * 32, pk);
-          tmem_st_wait();
-          fence_before();
-          mbar_arrive(&sm.p_full[pidx & 1]);
-        }
+        if (!pv_prev) ok = ok && pv_done(half, pidx - 1, 16);
+        ok = __all_sync(0xffffffffu, ok);
         ++pidx;
+        if (!ok) break;
+        fence_after();
+        tmem_st32(tP, pk);
+        tmem_st_wait();
+        fence_before();
+        mbar_arrive(&sm.p_full[half]);
       }
-      // epilogue: row sum over both halves, wait for the last PV, write the row
-      sm.xsum[half][r] = l;
+      // epilogue: both halves' last PV done, then combine the two halves
+      sm.xm[half][r] = m;
+      sm.xl[half][r] = l;
       ok = meet(ok);
       if (!ok) break;
-      const float lt = sm.xsum[0][r] + sm.xsum[1][r];
-      ok = ok && pv_done(pidx - 1, 13);
+      ok = __all_sync(0xffffffffu, ok && pv_done(0, pidx - 1, 13) && pv_done(1, pidx - 1, 17));
       if (ok) {
         fence_after();
+        const float m0 = sm.xm[0][r], m1 = sm.xm[1][r];
+        const float M = fmaxf(m0, m1);  // finite: half 0 holds a real key of every block
+        const float a0 = ex2(m0 - M), a1 = ex2(m1 - M);
+        const float lt = sm.xl[0][r] * a0 + sm.xl[1][r] * a1;
         const bool real = r < nvq;
         const float inv = real ? 1.f / lt : 0.f;
+        const float w0 = a0 * inv, w1 = a1 * inv;
+        const uint32_t tO0 = tmem + lane_base + TM_O0 + c0, tO1 = tmem + lane_base + TM_O1 + c0;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO0 + c * 32, o0);
+          tmem_ld32(tO1 + c * 32, o1);
           tmem_ld_wait();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-            orow[c * 4 + q] = v;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              v[e] = fmaf(__uint_as_float(o0[8 * q + e]), w0, __uint_as_float(o1[8 * q + e]) * w1);
+            uint4 u;
+            u.x = pack_bf16x2(v[0], v[1]);
+            u.y = pack_bf16x2(v[2], v[3]);
+            u.z = pack_bf16x2(v[4], v[5]);
+            u.w = pack_bf16x2(v[6], v[7]);
+            orow[c * 4 + q] = u;
           }
         }
-        if (half == 0) P.lse[grow] = real ? (m + log2f(lt)) * 0.69314718055994531f : 0.f;
+        if (half == 0) P.lse[grow] = real ? (M + log2f(lt)) * 0.69314718055994531f : 0.f;
       }
-      // both halves have read xsum before either writes it for the next block
+      // both halves have read O_0, O_1, xm and xl before either moves on
       ok = meet(ok);
       if (!ok) break;
       fence_before();
