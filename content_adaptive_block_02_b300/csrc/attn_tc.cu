@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     };
     uint32_t sidx = 0, pidx = 0;
     bool ok = true;
+    bool s_ready = false;  // early look at the next S tile, taken after the last P store
     for (uint32_t it = 0;; ++it) {
       const int ws = it & 1;
       ok = meet(ok && W.wait(&sm.work_full[ws], (it >> 1) & 1, 10));
@@ -306,15 +307,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive(&sm.q_ready);
       }
       float m = -INFINITY, l = 0.f;  // this half's running max (log2 units) and row sum
+      // real-token counts of the listed key blocks, fetched ahead of use:
+      // the block index two key blocks ahead, its count one block ahead
       const int32_t* nvb = P.n_valid + bh * P.nb;
-      int nvk_next = nvb[P.col_idx[beg]];
+      const int32_t* cols = P.col_idx + beg;
+      int nvk_next = nvb[cols[0]];
+      int j_next2 = n > 1 ? cols[1] : 0;
       for (int jj = 0; jj < n; ++jj) {
         const int nvk = nvk_next;
-        if (jj + 1 < n) nvk_next = nvb[P.col_idx[beg + jj + 1]];  // ahead of its use
+        if (jj + 1 < n) nvk_next = nvb[j_next2];
+        if (jj + 2 < n) j_next2 = cols[jj + 2];
         const int lim = nvk - c0;  // columns of this half that hold real keys
         // wait results are made warp-uniform: the TMEM loads and stores
         // below are warp-collective
-        ok = __all_sync(0xffffffffu, ok && W.wait(&sm.s_full, sidx & 1, 11));
+        ok = __all_sync(0xffffffffu, ok && (s_ready || W.wait(&sm.s_full, sidx & 1, 11)));
         ++sidx;
         if (!ok) break;
         uint32_t s[2][32];
@@ -402,6 +408,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st_wait();
         fence_before();
         mbar_arrive(&sm.p_full[half]);
+        s_ready = mbar_test(&sm.s_full, sidx & 1);  // the next S tile, most often done
       }
       // epilogue: both halves' last PV done, then combine the two halves
       sm.xm[half][r] = m;

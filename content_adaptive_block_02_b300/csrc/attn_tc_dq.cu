@@ -279,12 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool real = r < nvq;
       const float lse2 = P.lse[grow] * 1.4426950408889634f;
       const float Dr = P.D[grow];
+      // real-token counts of the listed key blocks, fetched ahead of use:
+      // the block index two key blocks ahead, its count one block ahead
       const int32_t* nvb = P.n_valid + bh * P.nb;
-      int nvk_next = nvb[P.col_idx[beg]];
+      const int32_t* cols = P.col_idx + beg;
+      int nvk_next = nvb[cols[0]];
+      int j_next2 = n > 1 ? cols[1] : 0;
       bool ok = true;
       for (int jj = 0; jj < n; ++jj) {
         const int nvk = nvk_next;
-        if (jj + 1 < n) nvk_next = nvb[P.col_idx[beg + jj + 1]];  // ahead of its use
+        if (jj + 1 < n) nvk_next = nvb[j_next2];
+        if (jj + 2 < n) j_next2 = cols[jj + 2];
         const int lim = real ? nvk - c0 : 0;  // real key columns of this half
         if (!W.wait(&sm.s_full, sidx & 1, 82)) { ok = false; break; }
         fence_after();
