@@ -231,7 +231,26 @@ int prism_assign_and_permute(const prism_plan_t* plan, const float* stats, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   PRISM_CUDA(prism::launch_assign(plan->p, stats, shape_id, shape_tie, st));
   PRISM_CUDA(prism::launch_permute_pool(plan->p, shape_id, Q, K, V, perm, inv, Qp, Kp, Vp, Qbar,
-                                        Qbar_lo, Kbar, Kbar_lo, n_valid, st));
+                                        Qbar_lo, Kbar, Kbar_lo, n_valid, nullptr, st));
+  return PRISM_OK;
+}
+
+int prism_permute_shapes(const prism_plan_t* plan, const uint8_t* shape_id, const uint16_t* Q,
+                         const uint16_t* K, const uint16_t* V, int32_t* perm, int32_t* inv,
+                         uint16_t* Qp, uint16_t* Kp, uint16_t* Vp, float* Qbar, float* Qbar_lo,
+                         float* Kbar, float* Kbar_lo, int32_t* n_valid, void* ws, void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(Q); PRISM_CHECK_PTR(K); PRISM_CHECK_PTR(V);
+  PRISM_CHECK_PTR(shape_id);
+  PRISM_CHECK_PTR(perm); PRISM_CHECK_PTR(inv);
+  PRISM_CHECK_PTR(Qp); PRISM_CHECK_PTR(Kp); PRISM_CHECK_PTR(Vp);
+  PRISM_CHECK_PTR(Qbar); PRISM_CHECK_PTR(Qbar_lo);
+  PRISM_CHECK_PTR(Kbar); PRISM_CHECK_PTR(Kbar_lo);
+  PRISM_CHECK_PTR(n_valid); PRISM_CHECK_PTR(ws);
+  PRISM_CUDA(prism::launch_permute_pool(plan->p, shape_id, Q, K, V, perm, inv, Qp, Kp, Vp, Qbar,
+                                        Qbar_lo, Kbar, Kbar_lo, n_valid,
+                                        static_cast<uint32_t*>(ws),
+                                        static_cast<cudaStream_t>(stream)));
   return PRISM_OK;
 }
 

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int c0 = half * 64;  // first key column (and output channel) of this half
     uint32_t xpar = 0;         // parity of the flag slots of the next meeting
     auto meet = [&](bool mine) -> bool {  // pair barrier, returns both flags ANDed
+      mine = __all_sync(0xffffffffu, mine);  // one flag per warp
       const int slot = xpar & 1;
       ++xpar;
       if (lane == 0) sm.xok[slot][half][quarter] = mine ? 1 : 0;

@@ -285,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // together at the first meeting after either of them failed.
     uint32_t xpar = 0;
     auto meet = [&](bool mine) -> bool {
+      mine = __all_sync(0xffffffffu, mine);  // one flag per warp
       const int slot = xpar & 1;
       ++xpar;
       if (lane == 0) sm.xok[slot][half][quarter] = mine ? 1 : 0;
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* lse4 = reinterpret_cast<const float4*>(stage(s_) + 2 * kTile) + half * 16;
         const float4* D4 = lse4 + 32;
         // ---- P^T = exp(S^T * scale - LSE) on this half of the queries ----
-        ok = ok && W.wait(&sm.s_full, scnt & 1, 42);
+        ok = __all_sync(0xffffffffu, ok && W.wait(&sm.s_full, scnt & 1, 42));
         ++scnt;
         float p[64];
         if (ok) {
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ok && W.wait(&sm.dp_full, dpcnt & 1, 43);
         ++dpcnt;
         if (dsidx > 0) ok = ok && W.wait(&sm.ds_empty, (dsidx - 1) & 1, 44);
+        ok = __all_sync(0xffffffffu, ok);
         ++dsidx;
         if (ok) {
           fence_after();
@@ -397,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a failure in the last query block is caught at the next meeting
       use += n;
       // ---- epilogue: dV, dK * scale -> bf16, this half of the channels ----
-      ok = ok && W.wait(&sm.kv_done, kvcnt & 1, 45);
+      ok = __all_sync(0xffffffffu, ok && W.wait(&sm.kv_done, kvcnt & 1, 45));
       ++kvcnt;
       if (!ok) continue;  // both halves leave at the next meeting
       fence_after();

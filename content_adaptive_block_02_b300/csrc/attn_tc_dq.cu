@@ -291,7 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj + 1 < n) nvk_next = nvb[j_next2];
         if (jj + 2 < n) j_next2 = cols[jj + 2];
         const int lim = real ? nvk - c0 : 0;  // real key columns of this half
-        if (!W.wait(&sm.s_full, sidx & 1, 82)) { ok = false; break; }
+        // wait results are made warp-uniform: TMEM loads and stores are
+        // warp-collective
+        if (!__all_sync(0xffffffffu, W.wait(&sm.s_full, sidx & 1, 82))) { ok = false; break; }
         fence_after();
         uint32_t sv[2][32], dp[2][32];
         tmem_ld32(tmem + lb + TM_S + c0, sv[0]);
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         fence_before();
         mbar_arrive(&sm.s_free);
-        if (!W.wait(&sm.dp_full, sidx & 1, 83)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, W.wait(&sm.dp_full, sidx & 1, 83))) { ok = false; break; }
         fence_after();
         tmem_ld32(tmem + lb + TM_DP + c0, dp[0]);
         tmem_ld32(tmem + lb + TM_DP + c0 + 32, dp[1]);
@@ -329,7 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the dQ product that read this dS buffer two key blocks ago is done
         const uint32_t b = gidx & 1;
-        if (gidx >= 2 && !W.wait(&sm.ds_empty[b], ((gidx >> 1) - 1) & 1, 84)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, gidx < 2 || W.wait(&sm.ds_empty[b], ((gidx >> 1) - 1) & 1, 84))) {
+          ok = false;
+          break;
+        }
         fence_after();
         tmem_st32(tmem + lb + (b ? TM_DS1 : TM_DS0) + half * 32, pk);
         tmem_st_wait();
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: dQ * scale -> bf16, this half of the channels
-      if (!W.wait(&sm.dq_done, items & 1, 85)) break;
+      if (!__all_sync(0xffffffffu, W.wait(&sm.dq_done, items & 1, 85))) break;
       ++items;
       fence_after();
       const float mul = real ? P.scale : 0.f;

@@ -19,6 +19,8 @@ namespace {
 
 struct Menu {
   int ext[PRISM_MAX_SHAPES][3];
+  uint32_t adm_mask;  // bit k: menu shape k tiles the zone
+  int first_adm;      // lowest admissible menu index
 };
 
 struct BlockGeom {
@@ -64,7 +66,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
     const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, uint16_t* __restrict__ Qp, uint16_t* __restrict__ Kp,
     uint16_t* __restrict__ Vp, float* __restrict__ Qh, float* __restrict__ Ql,
-    float* __restrict__ Kh, float* __restrict__ Kl, int32_t* __restrict__ n_valid) {
+    float* __restrict__ Kh, float* __restrict__ Kl, int32_t* __restrict__ n_valid,
+    uint32_t* __restrict__ status) {
   extern __shared__ __align__(16) float2 red2[];
   const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;  // heads fastest: the heads
                                                                  // of a block share token rows
@@ -73,7 +76,13 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
   const int q = threadIdx.x % P, grp = threadIdx.x / P;
   const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
   const long long bh = static_cast<long long>(b) * c.H + h;
-  const int sid = shape_id[bh * Z + blk / bpz];
+  int sid = shape_id[bh * Z + blk / bpz];
+  if (sid >= PRISM_MAX_SHAPES || !((menu.adm_mask >> sid) & 1u)) {
+    // a caller-given shape that does not tile the zone: report, fall back
+    if (status != nullptr && threadIdx.x == 0 && blk % bpz == 0)
+      dev_error(status, DEV_ERR_BOUNDS, 0x5A1, static_cast<uint32_t>(sid));
+    sid = menu.first_adm;
+  }
   const BlockGeom g = block_geom(c, nzH, nzW, bpz, menu, sid, blk);
   const int nv = g.et * g.ey * g.ex;
   df sq[8], sk[8];
@@ -223,11 +232,14 @@ cudaError_t launch_permute_pool(const Plan& p, const uint8_t* shape_id, const ui
                                 const uint16_t* K, const uint16_t* V, int32_t* perm,
                                 int32_t* inv, uint16_t* Qp, uint16_t* Kp, uint16_t* Vp,
                                 float* Qh, float* Ql, float* Kh, float* Kl, int32_t* n_valid,
-                                cudaStream_t st) {
+                                uint32_t* status, cudaStream_t st) {
   const prism_config_t& c = p.cfg;
   Menu m;
   for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
     for (int a = 0; a < 3; ++a) m.ext[k][a] = k < c.n_shapes ? c.shapes[k][a] : 1;
+  m.adm_mask = 0;
+  for (int q = 0; q < p.sz.n_admissible; ++q) m.adm_mask |= 1u << p.sz.admissible[q];
+  m.first_adm = p.sz.admissible[0];
   const int G = kPermThreads / (c.d / 8);
   const size_t smem = 2ull * G * c.d * sizeof(float2);
   cudaError_t e = cudaFuncSetAttribute(permute_pool_kernel,
@@ -238,7 +250,7 @@ cudaError_t launch_permute_pool(const Plan& p, const uint8_t* shape_id, const ui
   dim3 grid(c.H, p.sz.nb, c.B);
   permute_pool_kernel<<<grid, kPermThreads, smem, st>>>(
       c, p.sz.nzH, p.sz.nzW, p.sz.blocks_per_zone, p.sz.Z, p.sz.nb, p.sz.Np, m, shape_id, Q, K,
-      V, perm, inv, Qp, Kp, Vp, Qh, Ql, Kh, Kl, n_valid);
+      V, perm, inv, Qp, Kp, Vp, Qh, Ql, Kh, Kl, n_valid, status);
   return cudaGetLastError();
 }
 

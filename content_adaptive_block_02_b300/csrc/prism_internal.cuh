@@ -49,11 +49,13 @@ cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* 
                               float* stats, cudaStream_t st);
 cudaError_t launch_assign(const Plan& p, const float* stats, uint8_t* shape_id,
                           uint8_t* shape_tie, cudaStream_t st);
+// status: when not null, a shape id that is not admissible is recorded there
+// (DEV_ERR_BOUNDS); such a zone always falls back to the first admissible shape.
 cudaError_t launch_permute_pool(const Plan& p, const uint8_t* shape_id, const uint16_t* Q,
                                 const uint16_t* K, const uint16_t* V, int32_t* perm,
                                 int32_t* inv, uint16_t* Qp, uint16_t* Kp, uint16_t* Vp,
                                 float* Qh, float* Ql, float* Kh, float* Kl, int32_t* n_valid,
-                                cudaStream_t st);
+                                uint32_t* status, cudaStream_t st);
 cudaError_t launch_permute(const Plan& p, const int32_t* perm, const uint16_t* X, uint16_t* Xp,
                            cudaStream_t st);
 cudaError_t launch_unpermute(const Plan& p, const int32_t* inv, const uint16_t* Xp, uint16_t* X,

@@ -104,6 +104,7 @@ def lib() -> ctypes.CDLL:
         "prism_sparse_attn_bwd": [P] + [P] * 11 + [ctypes.c_float] + [P] * 5,
         "prism_unpermute": [P, P, P, P, P],
         "prism_plan_set_trace_events": [P, P],
+        "prism_permute_shapes": [P] * 17,
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -267,6 +268,20 @@ class Plan:
             _ptr(o["Kbar_lo"]), _ptr(o["n_valid"]), _stream()), "prism_assign_and_permute")
         return o
 
+    def permute_shapes(self, shape_id, Q, K, V, ws, out=None):
+        """prism_permute_shapes: step 2 with caller-given shape ids
+        ([B, H, Z] uint8 menu indices) instead of Eq. 7; the ids are copied
+        into ``out["shape_id"]``."""
+        o = out if out is not None else self.alloc_permuted(Q.device)
+        o["shape_id"].copy_(shape_id)
+        o["shape_tie"].zero_()
+        _check(lib().prism_permute_shapes(
+            self.h, _ptr(o["shape_id"]), _ptr(Q), _ptr(K), _ptr(V), _ptr(o["perm"]),
+            _ptr(o["inv"]), _ptr(o["Qp"]), _ptr(o["Kp"]), _ptr(o["Vp"]), _ptr(o["Qbar"]),
+            _ptr(o["Qbar_lo"]), _ptr(o["Kbar"]), _ptr(o["Kbar_lo"]), _ptr(o["n_valid"]),
+            _ptr(ws), _stream()), "prism_permute_shapes")
+        return o
+
     def alloc_lists(self, device):
         w = self.w
         rows = w.B * w.H * self.nb
@@ -352,10 +367,16 @@ class PrismAttention:
         self.dQp, self.dKp, self.dVp = (torch.empty_like(self.Op) for _ in range(3))
         self.dQ, self.dK, self.dV = (torch.empty_like(self.O) for _ in range(3))
 
-    def forward(self, Q, K, V, a2v):
+    def forward(self, Q, K, V, a2v, shape_id=None):
+        """``shape_id`` ([B, H, Z] uint8, optional): block shapes given by the
+        caller (fixed / random baselines) instead of the zone statistics and
+        Eq. 7; ``a2v`` is then unused."""
         p, o = self.plan, self.perm_out
-        p.zone_stats(V, a2v, self.stats)
-        p.assign_and_permute(self.stats, Q, K, V, o)
+        if shape_id is None:
+            p.zone_stats(V, a2v, self.stats)
+            p.assign_and_permute(self.stats, Q, K, V, o)
+        else:
+            p.permute_shapes(shape_id, Q, K, V, self.ws, o)
         p.block_select(o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"], o["n_valid"], self.ws,
                        self.lists)
         p.sparse_attn_fwd(o["Qp"], o["Kp"], o["Vp"], o["n_valid"], self.lists["row_ptr"],

@@ -177,6 +177,22 @@ int prism_assign_and_permute(const prism_plan_t* plan, const float* stats,
                              float* Qbar, float* Qbar_lo, float* Kbar, float* Kbar_lo,
                              int32_t* n_valid, void* stream);
 
+/* Step 2 with the block shapes given by the caller instead of Eq. 7: the
+ * fixed-shape and random-shape baselines of the block-shape ablation (Prism,
+ * Table 9: "Random Shape", "Fixed 4^3", ...) run through the same
+ * permutation, pooling, selection and attention kernels.
+ *   shape_id   [B, H, Z] uint8 in: menu index of each zone's shape; it must
+ *              be admissible for the zone (prism_sizes_t.admissible)
+ *   ws         workspace (for the status word)
+ *   other arguments as for prism_assign_and_permute.
+ * A shape id that is not admissible is recorded as PRISM_ERR_DEVICE_BOUNDS
+ * in the status word (read it with prism_device_status) and that zone uses
+ * the first admissible shape instead, so every access stays in bounds. */
+int prism_permute_shapes(const prism_plan_t* plan, const uint8_t* shape_id, const uint16_t* Q,
+                         const uint16_t* K, const uint16_t* V, int32_t* perm, int32_t* inv,
+                         uint16_t* Qp, uint16_t* Kp, uint16_t* Vp, float* Qbar, float* Qbar_lo,
+                         float* Kbar, float* Kbar_lo, int32_t* n_valid, void* ws, void* stream);
+
 /* Step 3+4 -- block scores Qbar Kbar^T / sqrt(d) and hybrid Top-k / Top-p
  * selection (Table 7 caption; Abstract: per-query sparsity), then the
  * block lists in both directions.

@@ -31,11 +31,12 @@ def f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(w, inputs, attn_kernel=0):
+def run_gpu(w, inputs, attn_kernel=0, shape_id=None):
     dev = torch.device("cuda")
     x = {k: inputs[k].to(dev) for k in ("Q", "K", "V", "a2v", "dO")}
     att = prism.PrismAttention(w, dev, attn_kernel=attn_kernel)
-    O = att.forward(x["Q"], x["K"], x["V"], x["a2v"])
+    sid = None if shape_id is None else torch.as_tensor(shape_id, dtype=torch.uint8).to(dev)
+    O = att.forward(x["Q"], x["K"], x["V"], x["a2v"], shape_id=sid)
     dQ, dK, dV = att.backward(x["dO"])
     torch.cuda.synchronize()
     assert att.status() == 0, "device status word set"
@@ -68,20 +69,27 @@ def rel_err(a, b):
 
 
 def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=None,
-            attn_kernel=0):
+            attn_kernel=0, shape_id=None):
     """Run both sides on the seeded inputs of `w`; assert the contract.
     heads / rows / key_blocks restrict the oracle's attention work (a sample
-    of the (b, h), query blocks and key blocks)."""
+    of the (b, h), query blocks and key blocks).  shape_id ([B, H, Z] ints):
+    block shapes given to both sides instead of the statistics and Eq. 7."""
     inputs = synth.generate(w, "cpu")
-    att, g = run_gpu(w, inputs, attn_kernel)
+    att, g = run_gpu(w, inputs, attn_kernel, shape_id)
     nb = att.plan.nb
     X = {k: f64(inputs[k]) for k in ("Q", "K", "V", "a2v", "dO")}
     rep = {} if report is None else report
     hs = list(range(w.H)) if heads is None else list(heads)
 
+    w_h = w.with_(H=len(hs))
+    if shape_id is not None:
+        sid_use = np.asarray(shape_id, dtype=np.int64)[:, hs]
+        assert np.array_equal(g["shape_id"].numpy().astype(np.int64)[:, hs], sid_use)
+        return _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd,
+                                    rep, heads)
+
     # ---- step 1: zone statistics ----
     Vs = X["V"][:, :, hs, :]
-    w_h = w.with_(H=len(hs))
     st_o = orc.zone_stats(w_h, Vs, X["a2v"])
     st_g = f64(g["stats"])[:, hs]
     for k in range(8):
@@ -102,6 +110,13 @@ def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=No
     assert not (mism & ~tie_o).any(), "shape id differs on a zone that is not a near tie"
     rep["shape_ties_taken"] = int(mism.sum())
     sid_use = np.where(mism, sid_g, sid_o)
+    return _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd, rep,
+                                heads)
+
+
+def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd, rep,
+                         heads):
+    """Steps 2 (permutation, pooling) to 5b of ``compare`` for given shapes."""
     perm_o, inv_o, nval_o = orc.build_permutation(w_h, sid_use)
     assert np.array_equal(g["perm"].numpy()[:, hs], perm_o)
     assert np.array_equal(g["inv"].numpy()[:, hs], inv_o)

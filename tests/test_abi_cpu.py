@@ -17,7 +17,7 @@ def L():
 
 def test_exports_every_declared_function(L):
     names = prism.declared_functions()
-    assert len(names) == 15
+    assert len(names) == 16
     for n in names:
         assert hasattr(L, n), n
 
@@ -99,3 +99,9 @@ def test_unknown_fault_injection_setting_is_rejected(L):
     with pytest.raises(prism.PrismError) as e:
         prism.Plan(w, fault_inject=7)
     assert e.value.code == -1
+
+
+def test_permute_shapes_rejects_null_pointers(L):
+    p = prism.Plan(synth.WORKLOADS["tiny"])
+    args = [p.h] + [None] * 16
+    assert L.prism_permute_shapes(*args) == -1

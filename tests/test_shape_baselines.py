@@ -1,0 +1,76 @@
+"""Block-shape baselines of the shape ablation (Prism, Table 9: "Random
+Shape", "Fixed 4^3"): the zones' block shapes are given by the caller
+(prism_permute_shapes) and the rest of the path -- permutation, pooling,
+selection, attention forward and backward -- runs through the same kernels.
+Both sides get the same shapes; the contract is that of the other parity
+tests."""
+import numpy as np
+import pytest
+import torch
+
+from content_adaptive_block_02_b300 import build, prism, synth
+from oracle import prism_oracle as orc
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+def _w_menu128(**kw):
+    """4 x 16 x 16 zones admit every shape of the 128-token menu."""
+    base = synth.WORKLOADS["720p"].with_(T=8, Hg=40, W=48, H=2, n_src=1, zone=(4, 16, 16),
+                                         name="menu128")
+    return base.with_(**kw)
+
+
+def _random_shapes(w, seed):
+    adm = orc.admissible_shapes(w.menu, w.zone)
+    rng = np.random.default_rng(seed)
+    return rng.choice(adm, size=(w.B, w.H, w.n_zones)).astype(np.uint8)
+
+
+def test_random_shapes_128_token_menu():
+    w = _w_menu128()
+    sid = _random_shapes(w, 7)
+    assert len(set(sid.ravel().tolist())) >= 4
+    rep = pu.compare(w, shape_id=sid)
+    assert rep["O_max_rel"] <= pu.O_TOL
+
+
+@pytest.mark.parametrize("k", [2, 5])  # (2, 8, 8) and (2, 4, 16) everywhere
+def test_fixed_shape_128_token_menu(k):
+    w = _w_menu128()
+    pu.compare(w, shape_id=np.full((w.B, w.H, w.n_zones), k, np.uint8))
+
+
+def test_fixed_4cubed_64_token_blocks():
+    """Fixed 4^3: the single 64-token shape (4, 4, 4) on 4 x 16 x 16 zones
+    (64-token blocks run on the CUDA-core attention kernels)."""
+    w = synth.WORKLOADS["720p"].with_(T=8, Hg=32, W=48, H=2, n_src=1, zone=(4, 16, 16),
+                                      block=64, menu=((4, 4, 4),), name="fixed4")
+    assert prism.Plan(w).sz.tensor_core_fwd == 0
+    pu.compare(w, shape_id=np.zeros((w.B, w.H, w.n_zones), np.uint8))
+
+
+def test_shape_that_does_not_tile_the_zone_is_reported():
+    """3 x 16 x 16 zones admit only (1, 8, 16) and (1, 16, 8); a given
+    (2, 8, 8) or an index past the menu is reported in the status word and
+    the zone falls back to the first admissible shape."""
+    build.build()
+    w = synth.WORKLOADS["720p"].with_(T=6, Hg=40, W=48, H=2, n_src=1, name="small128")
+    assert orc.admissible_shapes(w.menu, w.zone) == [0, 1]
+    dev = torch.device("cuda", 0)
+    x = synth.generate(w, dev)
+    for bad in (2, 200):
+        att = prism.PrismAttention(w, dev)
+        sid = torch.zeros(w.B, w.H, w.n_zones, dtype=torch.uint8, device=dev)
+        sid[0, 1, 3] = bad
+        att.forward(x["Q"], x["K"], x["V"], x["a2v"], shape_id=sid)
+        assert att.status() == prism.PRISM_ERR_DEVICE_BOUNDS
+        info = att.ws[16:32].view(torch.int32).tolist()
+        assert info[0] == 0x5A1 and info[1] == bad, info
+        # the fallback equals giving shape 0 there
+        ref = prism.PrismAttention(w, dev)
+        ref.forward(x["Q"], x["K"], x["V"], x["a2v"], shape_id=torch.zeros_like(sid))
+        assert ref.status() == 0
+        assert torch.equal(att.perm_out["perm"], ref.perm_out["perm"])
+        assert torch.equal(att.O, ref.O)
