@@ -1,10 +1,12 @@
 """Parity of the CUDA path (called through the C ABI) with the CPU oracle,
 step by step, on seeded synthetic inputs.  The contract is stated in
 tests/parity_util.py."""
+import numpy as np
 import pytest
 import torch
 
-from content_adaptive_block_02_b300 import build, synth
+from content_adaptive_block_02_b300 import build, prism, synth
+from oracle import prism_oracle as orc
 from tests import parity_util as pu
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +32,8 @@ def test_small_ragged_grid_with_padding():
 
 @pytest.mark.parametrize("kw", [dict(per_head=False), dict(use_video=False),
                                 dict(use_audio=False), dict(topp=0.5, topk_floor=1),
-                                dict(topp=0.99), dict(topk_floor=0, topp=0.0)])
+                                dict(topp=0.99), dict(topk_floor=0, topp=0.0),
+                                dict(alpha=1.0 / 3.0), dict(alpha=2.0)])
 def test_tiny_variants(kw):
     w = synth.WORKLOADS["tiny"].with_(**kw)
     pu.compare(w)
@@ -95,3 +98,20 @@ def test_128_blocks_selection_settings(kw):
 def test_full_size_sampled(name, heads):
     rep = pu.compare_sampled(synth.WORKLOADS[name], heads)
     assert rep["O"] <= pu.O_TOL and rep["dQ"] <= pu.G_TOL and rep["dKV"] <= pu.G_TOL
+
+
+def test_key_feature_variance_variant():
+    """Table 9 caption: the variance can be taken on query / key features
+    instead of value features; the statistics step takes any [B, N, H, d]
+    tensor, here K, and matches the oracle's statistics of K."""
+    w = synth.WORKLOADS["720p"].with_(T=6, Hg=40, W=48, H=2, n_src=1, name="small128")
+    x = synth.generate(w, "cpu")
+    dev = torch.device("cuda", 0)
+    plan = prism.Plan(w)
+    st = plan.zone_stats(x["K"].to(dev), x["a2v"].to(dev))
+    torch.cuda.synchronize()
+    ref = orc.zone_stats(w, pu.f64(x["K"]), pu.f64(x["a2v"]))
+    got = pu.f64(st.cpu())
+    for k in range(8):
+        scale = max(1e-30, np.abs(ref[..., k]).max())
+        assert np.abs(got[..., k] - ref[..., k]).max() / scale <= 2e-5, k

@@ -154,6 +154,23 @@ def test_shape_rule_exact_inverse_guidance_has_zero_cost():
         assert idx[j] == k and costs[j] < 1e-24
 
 
+@pytest.mark.parametrize("alpha", [1.0 / 3.0, 2.0])
+def test_shape_rule_exponent_alpha(alpha):
+    """The shape-mapping ablation's exponents (Table 10: alpha = 1/3, 2): with
+    b*_d proportional to g_d^-alpha, guidance g_d proportional to
+    b_d^(-1/alpha) makes the menu shape b the exact optimum (cost 0)."""
+    w = synth.WORKLOADS["2k"].with_(zone=(4, 16, 16), alpha=alpha)
+    for k, b in enumerate(w.menu):
+        g = 0.37 * np.array(b, dtype=float) ** (-1.0 / alpha)
+        costs, idx = orc.shape_costs(w, g)
+        j = int(np.argmin(costs))
+        assert idx[j] == k and costs[j] < 1e-24
+    # and alpha scales the deviation of log2 b* from the cube root linearly
+    g = np.array([1.0, 2.0, 8.0])
+    c1, _ = orc.shape_costs(w.with_(alpha=1.0), g)
+    assert not np.allclose(orc.shape_costs(w, g)[0], c1)
+
+
 def test_shape_rule_equal_guidance_takes_lowest_index():
     w = synth.WORKLOADS["2k"]
     costs, idx = orc.shape_costs(w, np.ones(3))
