@@ -379,31 +379,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float lsum = 0.f;
         uint32_t pk[32];
         if (lim >= 64) {
-          // pairs of columns in packed fp32x2 arithmetic; 12 of the 32 pairs
-          // take 2^x on the FMA pipe (exp2_poly2), the rest on the MUFU unit,
-          // which balances the two
-          const f32x2 sc2 = splat2(P.scale_log2), nm2 = splat2(-m);
-          f32x2 ls2[2] = {0ull, 0ull};  // independent partial sums
+          float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int k0 = 2 * e;
-            const f32x2 x = fma2(pair2(__uint_as_float(s[k0 >> 5][k0 & 31]),
-                                       __uint_as_float(s[(k0 + 1) >> 5][(k0 + 1) & 31])),
-                                 sc2, nm2);
-            f32x2 p;
-            if ((e & 7) < 3) {
-              p = exp2_poly2(x);
-            } else {
-              float x0, x1;
-              split2(x, x0, x1);
-              p = pair2(ex2(x0), ex2(x1));
-            }
-            ls2[e & 1] = add2(ls2[e & 1], p);
-            float p0, p1;
-            split2(p, p0, p1);
+            const float p0 = ex2(fmaf(__uint_as_float(s[k0 >> 5][k0 & 31]), P.scale_log2, -m));
+            const float p1 = ex2(fmaf(__uint_as_float(s[(k0 + 1) >> 5][(k0 + 1) & 31]), P.scale_log2, -m));
+            ls4[e & 3] += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
-          lsum = hsum2(add2(ls2[0], ls2[1]));
+          lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {

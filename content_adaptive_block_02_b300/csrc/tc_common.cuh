@@ -222,38 +222,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x for two lanes on the FMA pipe instead of the MUFU unit (whose 16
-// results per clock and SM bound the softmax), for x <= 0.  Cody-Waite style
-// range reduction: x = n + f with n = rint(x) (adding 1.5 * 2^23 rounds x to
-// an integer held in the low mantissa bits), f in [-1/2, 1/2]; 2^f by a
-// degree-4 polynomial whose coefficients were fitted to 2^f by weighted least
-// squares on Chebyshev nodes of [-1/2, 1/2] (max relative error 2.7e-6 in
-// fp32 evaluation); 2^n by adding n to the exponent field.  x is clamped at
-// -126 first, so the exponent never wraps (2^-126 stands in for anything
-// smaller, against 1 for the row maximum).
-constexpr float kExp2C0 = 0.9999992847442627f, kExp2C1 = 0.6931217908859253f,
-                kExp2C2 = 0.240247443318367f, kExp2C3 = 0.05591785907745361f,
-                kExp2C4 = 0.0095701077952981f;
-__device__ __forceinline__ f32x2 exp2_poly2(f32x2 x) {
-  float x0, x1;
-  split2(x, x0, x1);
-  x = pair2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-  const f32x2 magic = splat2(12582912.f);  // 1.5 * 2^23
-  const f32x2 t = add2(x, magic);
-  const f32x2 f = sub2(x, sub2(t, magic));
-  f32x2 p = fma2(splat2(kExp2C4), f, splat2(kExp2C3));
-  p = fma2(p, f, splat2(kExp2C2));
-  p = fma2(p, f, splat2(kExp2C1));
-  p = fma2(p, f, splat2(kExp2C0));
-  float p0, p1, t0, t1;
-  split2(p, p0, p1);
-  split2(t, t0, t1);
-  // the low bits of t hold n (two's complement); n << 23 lands in the exponent
-  const uint32_t r0 = __float_as_uint(p0) + (__float_as_uint(t0) << 23);
-  const uint32_t r1 = __float_as_uint(p1) + (__float_as_uint(t1) << 23);
-  return pair2(__uint_as_float(r0), __uint_as_float(r1));
-}
-
 __device__ __forceinline__ bool wait_raw(uint64_t* bar, uint32_t parity,
                                          unsigned long long limit) {
   const unsigned long long t0 = clock64();
