@@ -125,11 +125,12 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(tk=None, trace=None):
+    def step(tk=None, trace=None, xin=None):
+        xi = x if xin is None else xin
         if trace is not None:
             att.plan.set_trace_events(trace)
-        att.plan.zone_stats(x["V"], x["a2v"], att.stats)
-        att.plan.assign_and_permute(att.stats, x["Q"], x["K"], x["V"], att.perm_out)
+        att.plan.zone_stats(xi["V"], xi["a2v"], att.stats)
+        att.plan.assign_and_permute(att.stats, xi["Q"], xi["K"], xi["V"], att.perm_out)
         o = att.perm_out
         att.plan.block_select(o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"], o["n_valid"],
                               att.ws, att.lists)
@@ -140,7 +141,7 @@ def run_ours(args, w):
         if tk is not None:
             tk[1].record(stream)
         att.plan.unpermute(o["inv"], att.Op, att.O)
-        att.plan.permute(o["perm"], x["dO"], att.dOp)
+        att.plan.permute(o["perm"], xi["dO"], att.dOp)
         if tk is not None:
             tk[2].record(stream)
         att.plan.sparse_attn_bwd(o["Qp"], o["Kp"], o["Vp"], att.Op, att.dOp, att.lse, o["n_valid"],
@@ -158,6 +159,14 @@ def run_ours(args, w):
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
     pairs = int(att.lists["row_ptr"][-1].item())
+    # load balance: selected key blocks per query block (real query blocks)
+    rp = att.lists["row_ptr"].cpu().numpy().astype(np.int64)
+    lens = np.diff(rp)
+    real = att.perm_out["n_valid"].reshape(-1).cpu().numpy() > 0
+    lens = lens[real]
+    list_lengths = {"min": int(lens.min()), "p50": int(np.median(lens)),
+                    "p99": int(np.percentile(lens, 99)), "max": int(lens.max()),
+                    "mean": round(float(lens.mean()), 1)}
     amb = int(att.ws[4:8].view(torch.int32).item())
     flop = pairs * (FWD_PAIR_FLOP + BWD_PAIR_FLOP)
 
@@ -197,25 +206,53 @@ def run_ours(args, w):
         flop_all = float(flop)
     st = att.status()
 
-    # ---- end to end through host buffers (pinned), H2D inputs, D2H outputs ----
+    # ---- end to end through host buffers (pinned): every step's inputs are
+    # copied host -> device and its outputs device -> host inside the timed
+    # region, pipelined over two device buffer sets on two copy streams, so
+    # the copies of one step overlap the compute of its neighbours ----
     names_in = ["Q", "K", "V", "a2v", "dO"]
+    names_out = ("O", "dQ", "dK", "dV")
     host_in = {k: x[k].cpu().pin_memory() for k in names_in}
     host_out = {k: torch.empty(x["Q"].shape, dtype=torch.bfloat16).pin_memory()
-                for k in ("O", "dQ", "dK", "dV")}
+                for k in names_out}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    e_steps = max(1, min(args.steps, 3))
+    xb = [x, {k: torch.empty_like(x[k]) for k in names_in}]
+    ob = [{k: torch.empty_like(att.O) for k in names_out} for _ in range(2)]
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+    e_steps = max(1, args.steps)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     e0, e1 = ev(), ev()
     e0.record(stream)
-    for _ in range(e_steps):
-        for k in names_in:
-            x[k].copy_(host_in[k], non_blocking=True)
-        step()
-        for k, src in (("O", att.O), ("dQ", att.dQ), ("dK", att.dK), ("dV", att.dV)):
-            host_out[k].copy_(src, non_blocking=True)
+    s_h2d.wait_stream(stream)
+    s_d2h.wait_stream(stream)
+    for k in range(e_steps):
+        b = k % 2
+        with torch.cuda.stream(s_h2d):
+            if k >= 2:
+                s_h2d.wait_event(comp_done[b])  # step k-2 has finished reading buffer b
+            for n in names_in:
+                xb[b][n].copy_(host_in[n], non_blocking=True)
+            in_ready[b].record(s_h2d)
+        stream.wait_event(in_ready[b])
+        if k >= 2:
+            stream.wait_event(out_free[b])  # step k-2's outputs have left buffer b
+        step(xin=xb[b])
+        for n, src in zip(names_out, (att.O, att.dQ, att.dK, att.dV)):
+            ob[b][n].copy_(src, non_blocking=True)
+        comp_done[b].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(comp_done[b])
+            for n in names_out:
+                host_out[n].copy_(ob[b][n], non_blocking=True)
+            out_free[b].record(s_d2h)
+    stream.wait_stream(s_d2h)
+    stream.wait_stream(s_h2d)
     e1.record(stream)
     torch.cuda.synchronize()
     e_ms = e0.elapsed_time(e1) / e_steps
@@ -252,7 +289,8 @@ def run_ours(args, w):
                    "l2": "inputs larger than L2 (no flush needed)",
                    "selected_pairs": pairs,
                    "block_density": round(pairs / (w.B * w.H * w.n_blocks ** 2), 4),
-                   "rows_decided_exactly": amb},
+                   "rows_decided_exactly": amb,
+                   "selected_per_query_block": list_lengths},
         "attn_ms": {"fwd": round(fwd_ms, 3), "bwd": round(bwd_ms, 3),
                     "other": round(ms - fwd_ms - bwd_ms, 3)},
         "attn_tflops": {"fwd": round(fwd_achieved, 1), "bwd": round(bwd_achieved, 1)},
@@ -269,7 +307,9 @@ def run_ours(args, w):
                      "flop_per_launch": pairs * kern_flop[dom], "traffic": None},
         "e2e": {"value": round(flop_all / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "steps": e_steps,
+                "copies": "pinned host buffers, two device buffer sets, copy streams "
+                          "overlapped with the neighbouring steps' compute"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk.summary(),
         "device_status": st,
@@ -386,8 +426,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="2k", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dense", action="store_true",
+                    help="Top-p = 1: every valid key block (the dense comparison)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.dense:
+        w = w.with_(topp=1.0, name=w.name + "-dense")
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)
