@@ -290,7 +290,8 @@ def run_ours(args, w):
                    "selected_pairs": pairs,
                    "block_density": round(pairs / (w.B * w.H * w.n_blocks ** 2), 4),
                    "rows_decided_exactly": amb,
-                   "selected_per_query_block": list_lengths},
+                   "selected_per_query_block": list_lengths,
+                   "key_ranges": att.plan.sz.key_chunks},
         "attn_ms": {"fwd": round(fwd_ms, 3), "bwd": round(bwd_ms, 3),
                     "other": round(ms - fwd_ms - bwd_ms, 3)},
         "attn_tflops": {"fwd": round(fwd_achieved, 1), "bwd": round(bwd_achieved, 1)},
@@ -310,7 +311,7 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
                 "copies": "pinned host buffers, two device buffer sets, copy streams "
                           "overlapped with the neighbouring steps' compute"},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (2 if att.plan.sz.key_chunks > 1 else 0)) * args.steps,
         "clocks": clk.summary(),
         "device_status": st,
     }

@@ -36,11 +36,16 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
                                 const float* D, const int32_t* n_valid, const int32_t* col_ptr,
                                 const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
                                 uint8_t* ws, cudaStream_t st);
+cudaError_t launch_fwd_combine(const Plan& p, const int32_t* row_ptr, const int32_t* col_idx,
+                               const int32_t* n_valid, const uint8_t* ws, uint16_t* Op, float* lse,
+                               cudaStream_t st);
+cudaError_t launch_dq_combine(const Plan& p, const int32_t* row_ptr, const int32_t* col_idx,
+                              const uint8_t* ws, uint16_t* dQp, cudaStream_t st);
 cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
                               const float* D, const int32_t* n_valid, const int32_t* row_ptr,
                               const int32_t* col_idx, float scale, uint16_t* dQp, uint8_t* ws,
-                              cudaStream_t st);
+                              uint16_t* dqpart, cudaStream_t st);
 }  // namespace prism
 
 namespace {
@@ -105,7 +110,8 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
       c.zH < 1 || c.zW < 1 || c.block_tokens < 1 || c.Ca < 1 || c.topk_floor < 0 ||
       !(c.topp >= 0.f) || c.n_shapes < 1 || c.n_shapes > PRISM_MAX_SHAPES ||
       !(c.alpha == c.alpha) || !(c.eps >= 0.0) ||
-      (c.fault_inject != 0 && c.fault_inject != PRISM_FAULT_STARVE_LOADS))
+      (c.fault_inject != 0 && c.fault_inject != PRISM_FAULT_STARVE_LOADS) ||
+      c.key_chunk_blocks < 0)
     return PRISM_ERR_ARG;
   if (c.d % 32 != 0 || c.d > 128) return PRISM_ERR_UNSUPPORTED;
   const int lS = ilog2_exact(c.block_tokens);
@@ -167,7 +173,29 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   p.off_scores = off; off = align256(off + 2 * rows * nb * 4);
   p.off_D = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
   p.off_lse2 = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
-  p.off_dq = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * c.d * 4);
+  p.off_dq = off;
+  if (!z.tensor_core_bwd) off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * c.d * 4);
+  // key ranges of at most 512 blocks (32 MB of K and V per head) once a head's
+  // K and V outgrow L2; the partial results are capped at 32 GB
+  z.key_chunks = 1;
+  const int kcb = c.key_chunk_blocks > 0 ? c.key_chunk_blocks : (z.nb > 1024 ? 512 : z.nb);
+  if (z.tensor_core_fwd && kcb < z.nb) {
+    long long C = (z.nb + kcb - 1) / kcb;
+    if (C > 64) C = 64;
+    const long long per = static_cast<long long>(rows) * (c.block_tokens * c.d * 2 +
+                                                          c.block_tokens * 8);
+    const long long cap = (32LL << 30) / per;
+    if (C > cap) C = cap < 1 ? 1 : cap;
+    z.key_chunks = static_cast<int>(C);
+  }
+  z.chunk_blocks = (z.nb + z.key_chunks - 1) / z.key_chunks;
+  p.off_part = off;
+  p.off_ml = off;
+  if (z.key_chunks > 1) {
+    off = align256(off + static_cast<size_t>(rows) * z.key_chunks * c.block_tokens * c.d * 2);
+    p.off_ml = off;
+    off = align256(off + static_cast<size_t>(rows) * z.key_chunks * c.block_tokens * 8);
+  }
   z.ws_bytes = off;
   prism_plan* h = static_cast<prism_plan*>(malloc(sizeof(prism_plan)));
   if (h == nullptr) return PRISM_ERR_ARG;
@@ -285,6 +313,9 @@ int prism_sparse_attn_fwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
     PRISM_TRACED(PRISM_TRACE_ATTN_FWD,
                  prism::launch_attn_fwd_tc(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op,
                                            lse, static_cast<uint8_t*>(ws), st));
+    if (p.sz.key_chunks > 1)
+      PRISM_CUDA(prism::launch_fwd_combine(p, row_ptr, col_idx, n_valid,
+                                           static_cast<const uint8_t*>(ws), Op, lse, st));
   } else {
     PRISM_TRACED(PRISM_TRACE_ATTN_FWD,
                  prism::launch_attn_fwd_simt(p, Qp, Kp, Vp, n_valid, row_ptr, col_idx, scale, Op,
@@ -325,9 +356,12 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
     PRISM_TRACED(PRISM_TRACE_ATTN_DKDV,
                  prism::launch_attn_dkdv_tc(p, Qp, Kp, Vp, dOp, lse2, D, n_valid, col_ptr,
                                             row_idx, scale, dKp, dVp, w, st));
+    const bool ranges = p.sz.key_chunks > 1;
     PRISM_TRACED(PRISM_TRACE_ATTN_DQ,
-                 prism::launch_attn_dq_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx,
-                                          scale, dQp, w, st));
+                 prism::launch_attn_dq_tc(
+                     p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx, scale, dQp, w,
+                     ranges ? reinterpret_cast<uint16_t*>(w + p.off_part) : nullptr, st));
+    if (ranges) PRISM_CUDA(prism::launch_dq_combine(p, row_ptr, col_idx, w, dQp, st));
   } else {
     float* dq = reinterpret_cast<float*>(w + p.off_dq);
     PRISM_TRACED(PRISM_TRACE_BWD_PRE,

@@ -57,7 +57,7 @@ struct FwdShared {
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full, s_free, p_full[2], p_empty[2], q_ready, final_bar;  // p_*: per column half
   uint64_t work_full[2], work_empty[2];
-  int work_row[2], work_beg[2], work_end[2], work_nvq[2];
+  int work_row[2], work_beg[2], work_end[2], work_nvq[2], work_chunk[2];
   float xm[2][128];       // [column half][row]: running max at the end of a query block
   float xl[2][128];       // [column half][row]: row sum at the end of a query block
   int xok[2][2][4];       // [exchange parity][column half][lane quarter]: still on track
@@ -74,8 +74,13 @@ struct FwdParams {
   float* lse;
   uint32_t* status;
   long long rows;
+  long long items;    // rows * chunks
   long long Np;
   int nb;
+  int chunks;         // key ranges per head (1: no split)
+  int chunk_blocks;   // key blocks per range
+  uint16_t* Opart;    // chunks > 1: normalised partial O per (row, range)
+  float* ml;          // chunks > 1: (max in log2 units, row sum) per (row, range, query row)
   float scale_log2;
   unsigned long long limit;
   int starve;  // fault injection (test only): the producer issues no loads
@@ -128,21 +133,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (uint32_t it = 0;; ++it) {
         const int ws = it & 1;
         if (!W.wait(&sm.work_empty[ws], ((it >> 1) & 1) ^ 1, 1)) break;
-        const long long row = atomicAdd(queue, 1u);
-        if (row >= P.rows) {
+        const long long item = atomicAdd(queue, 1u);
+        if (item >= P.items) {
           sm.work_row[ws] = -1;
           mbar_arrive(&sm.work_full[ws]);
           break;
         }
-        const int beg = P.row_ptr[row], end = P.row_ptr[row + 1];
+        // item -> (b, h), key range c, query block i: within a head all query
+        // blocks take range 0, then range 1, ... so the K / V tiles in use
+        // stay in L2
+        const long long per_bh = static_cast<long long>(P.chunks) * P.nb;
+        const long long bh = item / per_bh;
+        const int rem = static_cast<int>(item - bh * per_bh);
+        const int c = rem / P.nb;
+        const long long row = bh * P.nb + (rem - c * P.nb);
+        int beg = P.row_ptr[row], end = P.row_ptr[row + 1];
+        if (P.chunks > 1) {
+          const int lo = c * P.chunk_blocks;
+          beg = lower_bound_i32(P.col_idx, beg, end, lo);
+          end = lower_bound_i32(P.col_idx, beg, end, lo + P.chunk_blocks);
+        }
         const int nvq = P.n_valid[row];
         sm.work_row[ws] = static_cast<int>(row);
+        sm.work_chunk[ws] = c;
         sm.work_beg[ws] = beg;
         sm.work_end[ws] = nvq > 0 ? end : beg;
         sm.work_nvq[ws] = nvq;
         mbar_arrive(&sm.work_full[ws]);
         if (nvq == 0) continue;
-        const long long bh = row / P.nb;
         bool ok = true;
         for (int t = beg; t < end; ++t) {
           const int j = P.col_idx[t];
@@ -282,14 +300,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int row = sm.work_row[ws];
       if (row < 0) break;
       const int beg = sm.work_beg[ws], n = sm.work_end[ws] - beg, nvq = sm.work_nvq[ws];
+      const int chunk = sm.work_chunk[ws];
       const long long bh = row / P.nb;
       const int i = row % P.nb;
       const long long grow = bh * P.Np + static_cast<long long>(i) * kS + r;
-      uint4* orow = reinterpret_cast<uint4*>(P.Op + grow * kD) + half * 8;
+      // output row: the final O, or this key range's normalised partial O
+      const long long prow = (static_cast<long long>(row) * P.chunks + chunk) * kS + r;
+      uint4* orow = reinterpret_cast<uint4*>(P.chunks > 1 ? P.Opart + prow * kD : P.Op + grow * kD) +
+                    half * 8;
       if (n == 0) {
+        // (with key ranges, the combining kernel handles empty ranges)
+        if (P.chunks == 1) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
-        if (half == 0) P.lse[grow] = 0.f;
+          for (int q = 0; q < 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
+          if (half == 0) P.lse[grow] = 0.f;
+        }
         mbar_arrive(&sm.work_empty[ws]);
         continue;
       }
@@ -447,7 +472,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             orow[c * 4 + q] = u;
           }
         }
-        if (half == 0) P.lse[grow] = real ? (M + log2f(lt)) * 0.69314718055994531f : 0.f;
+        if (half == 0) {
+          if (P.chunks == 1)
+            P.lse[grow] = real ? (M + log2f(lt)) * 0.69314718055994531f : 0.f;
+          else
+            reinterpret_cast<float2*>(P.ml)[prow] = make_float2(M, lt);
+        }
       }
       // both halves have read O_0, O_1, xm and xl before either moves on
       ok = meet(ok);
@@ -526,8 +556,13 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   a.lse = lse;
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.rows = static_cast<long long>(c.B) * c.H * p.sz.nb;
+  a.items = a.rows * p.sz.key_chunks;
   a.Np = p.sz.Np;
   a.nb = p.sz.nb;
+  a.chunks = p.sz.key_chunks;
+  a.chunk_blocks = p.sz.chunk_blocks;
+  a.Opart = reinterpret_cast<uint16_t*>(ws + p.off_part);
+  a.ml = reinterpret_cast<float*>(ws + p.off_ml);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
   a.starve = c.fault_inject == PRISM_FAULT_STARVE_LOADS ? 1 : 0;
@@ -537,7 +572,7 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long g = a.rows < sm_count() ? a.rows : sm_count();
+  const long long g = a.items < sm_count() ? a.items : sm_count();
   attn_fwd_tc_kernel<<<static_cast<unsigned>(g), kFwdThreads, smem, st>>>(tmK, tmV, a);
   return cudaGetLastError();
 }

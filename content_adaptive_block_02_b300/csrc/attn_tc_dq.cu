@@ -45,7 +45,7 @@ struct DqBars {
   uint64_t s_full, dp_full, s_free, dp_free, ds_ready[2], ds_empty[2];
   uint64_t dq_done, dq_free, final_bar;
   uint64_t work_full[2], work_empty[2];
-  int work_row[2], work_beg[2], work_end[2], work_nvq[2];
+  int work_row[2], work_beg[2], work_end[2], work_nvq[2], work_chunk[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -58,10 +58,14 @@ struct DqParams {
   const int32_t* row_ptr;
   const int32_t* col_idx;
   uint16_t* dQp;
+  uint16_t* dqpart;  // chunks > 1: partial dQ (scaled, bf16) per (row, key range)
   uint32_t* status;
-  long long rows;  // B*H*nb work items
+  long long rows;    // B*H*nb query blocks
+  long long items;   // rows * chunks work items
   long long Np;
   int nb;
+  int chunks;        // key ranges per head (1: no split)
+  int chunk_blocks;  // key blocks per range
   float scale, scale_log2;
   unsigned long long limit;
   int starve;  // fault injection (test only): the producer issues no loads
@@ -122,15 +126,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t it = 0; ok; ++it) {
         const int ws = it & 1;
         if (!W.wait(&sm.work_empty[ws], ((it >> 1) & 1) ^ 1, 61)) break;
-        const long long row = atomicAdd(P.status + WS_DQ_QUEUE, 1u);
-        if (row >= P.rows) {
+        const long long item = atomicAdd(P.status + WS_DQ_QUEUE, 1u);
+        if (item >= P.items) {
           sm.work_row[ws] = -1;
           mbar_arrive(&sm.work_full[ws]);
           break;
         }
-        const int beg = P.row_ptr[row], end = P.row_ptr[row + 1];
+        // item -> (b, h), key range c, query block i (ranges outermost within
+        // a head, so the K / V tiles in use stay in L2)
+        const long long per_bh = static_cast<long long>(P.chunks) * P.nb;
+        const long long bhi = item / per_bh;
+        const int rem = static_cast<int>(item - bhi * per_bh);
+        const int c = rem / P.nb;
+        const long long row = bhi * P.nb + (rem - c * P.nb);
+        int beg = P.row_ptr[row], end = P.row_ptr[row + 1];
+        if (P.chunks > 1) {
+          const int lo = c * P.chunk_blocks;
+          beg = lower_bound_i32(P.col_idx, beg, end, lo);
+          end = lower_bound_i32(P.col_idx, beg, end, lo + P.chunk_blocks);
+        }
         const int nvq = P.n_valid[row];
         sm.work_row[ws] = static_cast<int>(row);
+        sm.work_chunk[ws] = c;
         sm.work_beg[ws] = beg;
         sm.work_end[ws] = nvq > 0 ? end : beg;
         sm.work_nvq[ws] = nvq;
@@ -269,10 +286,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long bh = row / P.nb;
       const int i = row % P.nb;
       const long long grow = bh * P.Np + static_cast<long long>(i) * kS + r;
-      uint4* drow = reinterpret_cast<uint4*>(P.dQp + grow * kD) + half * 8;
+      // output row: the final dQ, or this key range's partial dQ
+      const long long prow =
+          (static_cast<long long>(row) * P.chunks + sm.work_chunk[ws]) * kS + r;
+      uint4* drow =
+          reinterpret_cast<uint4*>(P.chunks > 1 ? P.dqpart + prow * kD : P.dQp + grow * kD) +
+          half * 8;
       if (n == 0) {
+        // (with key ranges, the combining kernel handles empty ranges)
+        if (P.chunks == 1) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) drow[q] = make_uint4(0, 0, 0, 0);
+          for (int q = 0; q < 8; ++q) drow[q] = make_uint4(0, 0, 0, 0);
+        }
         mbar_arrive(&sm.work_empty[ws]);
         continue;
       }
@@ -385,7 +410,7 @@ cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t*
                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
                               const float* D, const int32_t* n_valid, const int32_t* row_ptr,
                               const int32_t* col_idx, float scale, uint16_t* dQp, uint8_t* ws,
-                              cudaStream_t st) {
+                              uint16_t* dqpart, cudaStream_t st) {
   const prism_config_t& c = p.cfg;
   const long long rows_total = static_cast<long long>(c.B) * c.H * p.sz.Np;
   CUtensorMap tmQ, tmK, tmV, tmdO;
@@ -401,6 +426,10 @@ cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t*
   a.dQp = dQp;
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.rows = static_cast<long long>(c.B) * c.H * p.sz.nb;
+  a.dqpart = dqpart;
+  a.chunks = dqpart != nullptr ? p.sz.key_chunks : 1;
+  a.chunk_blocks = a.chunks > 1 ? p.sz.chunk_blocks : p.sz.nb;
+  a.items = a.rows * a.chunks;
   a.Np = p.sz.Np;
   a.nb = p.sz.nb;
   a.scale = scale;
@@ -412,7 +441,7 @@ cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t*
   e = cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const long long g = a.rows < sm_count() ? a.rows : sm_count();
+  const long long g = a.items < sm_count() ? a.items : sm_count();
   attn_dq_tc_kernel<<<static_cast<unsigned>(g), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO,
                                                                              a);
   return cudaGetLastError();

@@ -19,6 +19,7 @@ struct Plan {
   double log2_S;
   // workspace offsets (bytes), each region 256-aligned
   size_t off_rowcnt, off_colcnt, off_amb, off_bitmask, off_scores, off_D, off_lse2, off_dq;
+  size_t off_part, off_ml;  // key-range partial results (key_chunks > 1)
 };
 
 // Workspace layout (bytes from the start of ws, each region 256-aligned):
@@ -31,6 +32,11 @@ struct Plan {
 //   off_D           fp32  [B*H*Np]       rowsum(dO * O) for the backward
 //   off_lse2        fp32  [B*H*Np]       LSE * log2(e) for the backward
 //   off_dq          fp32  [B*H*Np*d]     dQ accumulator of the CUDA-core backward
+//                                        (empty for a tensor-core plan)
+//   off_part        bf16  [B*H*nb, C, S, d] per key range: the forward's normalised
+//                                        partial O, later the dQ kernel's partial dQ
+//   off_ml          fp32  [B*H*nb, C, S, 2] per key range: running max (log2 units)
+//                                        and row sum of the forward
 enum : int {
   WS_STATUS = 0,      // uint32: first device error code (0 = none)
   WS_AMB_COUNT = 1,   // uint32: number of ambiguous rows appended by the select kernel
@@ -97,6 +103,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// First position in col[lo, hi) holding a value >= key (col ascending).
+__device__ __forceinline__ int lower_bound_i32(const int32_t* col, int lo, int hi, int key) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (col[mid] < key)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
 }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {

@@ -49,7 +49,7 @@ class Config(ctypes.Structure):
         ("per_head", ctypes.c_int), ("use_video", ctypes.c_int), ("use_audio", ctypes.c_int),
         ("topk_floor", ctypes.c_int), ("topp", ctypes.c_float),
         ("timeout_cycles", ctypes.c_ulonglong), ("attn_kernel", ctypes.c_int),
-        ("fault_inject", ctypes.c_int),
+        ("fault_inject", ctypes.c_int), ("key_chunk_blocks", ctypes.c_int),
     ]
 
 
@@ -68,6 +68,7 @@ class Sizes(ctypes.Structure):
         ("n_admissible", ctypes.c_int), ("admissible", ctypes.c_int * MAX_SHAPES),
         ("max_pairs", ctypes.c_longlong), ("ws_bytes", ctypes.c_size_t),
         ("tensor_core_fwd", ctypes.c_int), ("tensor_core_bwd", ctypes.c_int),
+        ("key_chunks", ctypes.c_int), ("chunk_blocks", ctypes.c_int),
     ]
 
 
@@ -142,7 +143,7 @@ def _stream():
 
 
 def make_config(w, timeout_cycles: int = 0, attn_kernel: int = 0,
-                fault_inject: int = 0) -> Config:
+                fault_inject: int = 0, key_chunk_blocks: int = 0) -> Config:
     """Config from a workload description (``synth.Workload``-like object)."""
     c = Config()
     c.B, c.H, c.d = w.B, w.H, w.d
@@ -162,15 +163,17 @@ def make_config(w, timeout_cycles: int = 0, attn_kernel: int = 0,
     c.timeout_cycles = timeout_cycles
     c.attn_kernel = attn_kernel
     c.fault_inject = fault_inject
+    c.key_chunk_blocks = key_chunk_blocks
     return c
 
 
 class Plan:
     """Host plan of one problem size (prism_plan_create / prism_plan_query)."""
 
-    def __init__(self, w, timeout_cycles: int = 0, attn_kernel: int = 0, fault_inject: int = 0):
+    def __init__(self, w, timeout_cycles: int = 0, attn_kernel: int = 0, fault_inject: int = 0,
+                 key_chunk_blocks: int = 0):
         self.w = w
-        self.cfg = make_config(w, timeout_cycles, attn_kernel, fault_inject)
+        self.cfg = make_config(w, timeout_cycles, attn_kernel, fault_inject, key_chunk_blocks)
         h = ctypes.c_void_p()
         _check(lib().prism_plan_create(ctypes.byref(self.cfg), ctypes.byref(h)), "prism_plan_create")
         self.h = h
@@ -350,10 +353,10 @@ class PrismAttention:
     reused across calls."""
 
     def __init__(self, w, device="cuda", attn_kernel: int = 0, timeout_cycles: int = 0,
-                 fault_inject: int = 0):
+                 fault_inject: int = 0, key_chunk_blocks: int = 0):
         self.w = w
         self.plan = Plan(w, timeout_cycles=timeout_cycles, attn_kernel=attn_kernel,
-                         fault_inject=fault_inject)
+                         fault_inject=fault_inject, key_chunk_blocks=key_chunk_blocks)
         self.device = torch.device(device)
         self.scale = 1.0 / math.sqrt(w.d)
         self.ws = self.plan.ws(self.device)

@@ -81,6 +81,11 @@ typedef struct prism_config {
                              kernels free their tensor memory and return, and the
                              status word reads PRISM_ERR_DEVICE_TIMEOUT.  No copy
                              is in flight when they return.                       */
+  int key_chunk_blocks;   /* key blocks per range of the tensor-core forward / dQ
+                             kernels (prism_sizes_t.key_chunks): 0 = automatic
+                             (ranges of 512 blocks once a head has more than 1024
+                             key blocks, else one range); > 0 = ranges of this
+                             many blocks (at most 64 ranges)                      */
 } prism_config_t;
 
 #define PRISM_FAULT_STARVE_LOADS 1
@@ -100,6 +105,13 @@ typedef struct prism_sizes {
                              prism_sparse_attn_fwd and prism_sparse_attn_bwd */
   int tensor_core_fwd;    /* 1 when the forward attention runs on tcgen05 kernels */
   int tensor_core_bwd;    /* 1 when the backward attention runs on tcgen05 kernels */
+  int key_chunks;         /* the tensor-core forward and dQ kernels split each head's
+                             key blocks into this many ranges of chunk_blocks and
+                             walk them range by range (all query blocks of a head
+                             for one range, then the next), so that the K / V tiles
+                             in use fit in L2; partial results are combined per
+                             query block afterwards.  1 = no split. */
+  int chunk_blocks;       /* key blocks per range (nb when key_chunks == 1) */
 } prism_sizes_t;
 
 typedef struct prism_plan prism_plan_t;

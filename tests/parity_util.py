@@ -31,10 +31,10 @@ def f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(w, inputs, attn_kernel=0, shape_id=None):
+def run_gpu(w, inputs, attn_kernel=0, shape_id=None, key_chunk_blocks=0):
     dev = torch.device("cuda")
     x = {k: inputs[k].to(dev) for k in ("Q", "K", "V", "a2v", "dO")}
-    att = prism.PrismAttention(w, dev, attn_kernel=attn_kernel)
+    att = prism.PrismAttention(w, dev, attn_kernel=attn_kernel, key_chunk_blocks=key_chunk_blocks)
     sid = None if shape_id is None else torch.as_tensor(shape_id, dtype=torch.uint8).to(dev)
     O = att.forward(x["Q"], x["K"], x["V"], x["a2v"], shape_id=sid)
     dQ, dK, dV = att.backward(x["dO"])
@@ -69,13 +69,15 @@ def rel_err(a, b):
 
 
 def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=None,
-            attn_kernel=0, shape_id=None):
+            attn_kernel=0, shape_id=None, key_chunk_blocks=0):
     """Run both sides on the seeded inputs of `w`; assert the contract.
     heads / rows / key_blocks restrict the oracle's attention work (a sample
     of the (b, h), query blocks and key blocks).  shape_id ([B, H, Z] ints):
     block shapes given to both sides instead of the statistics and Eq. 7."""
     inputs = synth.generate(w, "cpu")
-    att, g = run_gpu(w, inputs, attn_kernel, shape_id)
+    att, g = run_gpu(w, inputs, attn_kernel, shape_id, key_chunk_blocks)
+    rep_ = {} if report is None else report
+    rep_["key_chunks"] = att.plan.sz.key_chunks
     nb = att.plan.nb
     X = {k: f64(inputs[k]) for k in ("Q", "K", "V", "a2v", "dO")}
     rep = {} if report is None else report

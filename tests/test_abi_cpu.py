@@ -46,6 +46,14 @@ def test_2k_sizes_are_the_documented_ones(L):
     p = prism.Plan(synth.WORKLOADS["2k"])
     assert (p.sz.Np, p.sz.Z, p.sz.nb) == (322_560, 420, 2520)
     assert p.sz.tensor_core_fwd == 1
+    # key ranges of at most 512 blocks once a head's K / V outgrow L2
+    assert (p.sz.key_chunks, p.sz.chunk_blocks) == (5, 504)
+    assert prism.Plan(synth.WORKLOADS["720p"]).sz.key_chunks == 1
+    assert prism.Plan(synth.WORKLOADS["1080p"]).sz.key_chunks == 4
+    small = synth.WORKLOADS["720p"].with_(T=6, Hg=40, W=48, H=2)
+    q = prism.Plan(small, key_chunk_blocks=16)
+    assert (q.sz.nb, q.sz.key_chunks, q.sz.chunk_blocks) == (108, 7, 16)
+    assert prism.Plan(small, key_chunk_blocks=16, attn_kernel=1).sz.key_chunks == 1
     p1 = prism.Plan(synth.WORKLOADS["2k"], attn_kernel=1)
     assert p1.sz.tensor_core_fwd == 0 and p1.sz.tensor_core_bwd == 0
     assert prism.Plan(synth.WORKLOADS["tiny"]).sz.tensor_core_fwd == 0

@@ -72,6 +72,16 @@ def test_128_blocks_both_kernels(attn_kernel):
     assert rep["O_max_rel"] <= pu.O_TOL
 
 
+@pytest.mark.parametrize("kw", [dict(), dict(topp=1.0), dict(topp=0.5, topk_floor=2)])
+def test_128_blocks_key_ranges(kw):
+    """The tensor-core forward and dQ kernels walking the key blocks in ranges
+    of 16 (7 ranges over 108 blocks, many (query block, range) items empty),
+    with the per-range partial results combined afterwards."""
+    rep = {}
+    pu.compare(_w128(**kw), key_chunk_blocks=16, report=rep)
+    assert rep["key_chunks"] == 7
+
+
 def test_128_blocks_wide_zone():
     """3 x 8 x 32 zones: wider than the register-pencil statistics kernel
     handles (16 tokens per line), so the general statistics kernel runs."""
