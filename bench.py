@@ -311,7 +311,7 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
                 "copies": "pinned host buffers, two device buffer sets, copy streams "
                           "overlapped with the neighbouring steps' compute"},
-        "gpu_launches": (KERNELS_PER_STEP + (2 if att.plan.sz.key_chunks > 1 else 0)) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (4 if att.plan.sz.key_chunks > 1 else 0)) * args.steps,
         "clocks": clk.summary(),
         "device_status": st,
     }

@@ -35,12 +35,12 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
                                 const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
                                 const float* D, const int32_t* n_valid, const int32_t* col_ptr,
                                 const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
-                                uint8_t* ws, cudaStream_t st);
+                                uint8_t* ws, uint16_t* dkvpart, cudaStream_t st);
 cudaError_t launch_fwd_combine(const Plan& p, const int32_t* row_ptr, const int32_t* col_idx,
                                const int32_t* n_valid, const uint8_t* ws, uint16_t* Op, float* lse,
                                cudaStream_t st);
-cudaError_t launch_dq_combine(const Plan& p, const int32_t* row_ptr, const int32_t* col_idx,
-                              const uint8_t* ws, uint16_t* dQp, cudaStream_t st);
+cudaError_t launch_sum_combine(const Plan& p, const int32_t* ptr, const int32_t* idx,
+                               const uint16_t* part, uint16_t* out, cudaStream_t st);
 cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
                               const float* D, const int32_t* n_valid, const int32_t* row_ptr,
@@ -182,7 +182,7 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   if (z.tensor_core_fwd && kcb < z.nb) {
     long long C = (z.nb + kcb - 1) / kcb;
     if (C > 64) C = 64;
-    const long long per = static_cast<long long>(rows) * (c.block_tokens * c.d * 2 +
+    const long long per = static_cast<long long>(rows) * (2 * c.block_tokens * c.d * 2 +
                                                           c.block_tokens * 8);
     const long long cap = (32LL << 30) / per;
     if (C > cap) C = cap < 1 ? 1 : cap;
@@ -192,7 +192,8 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   p.off_part = off;
   p.off_ml = off;
   if (z.key_chunks > 1) {
-    off = align256(off + static_cast<size_t>(rows) * z.key_chunks * c.block_tokens * c.d * 2);
+    // two bf16 tiles per (block, range): dK and dV partials (O and dQ use the first)
+    off = align256(off + 2 * static_cast<size_t>(rows) * z.key_chunks * c.block_tokens * c.d * 2);
     p.off_ml = off;
     off = align256(off + static_cast<size_t>(rows) * z.key_chunks * c.block_tokens * 8);
   }
@@ -353,15 +354,24 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
     float* lse2 = reinterpret_cast<float*>(w + p.off_lse2);
     PRISM_TRACED(PRISM_TRACE_BWD_PRE,
                  prism::launch_bwd_pre(p, Op, dOp, lse, D, lse2, nullptr, st));
+    const bool ranges = p.sz.key_chunks > 1;
+    uint16_t* part = reinterpret_cast<uint16_t*>(w + p.off_part);
     PRISM_TRACED(PRISM_TRACE_ATTN_DKDV,
                  prism::launch_attn_dkdv_tc(p, Qp, Kp, Vp, dOp, lse2, D, n_valid, col_ptr,
-                                            row_idx, scale, dKp, dVp, w, st));
-    const bool ranges = p.sz.key_chunks > 1;
+                                            row_idx, scale, dKp, dVp, w, ranges ? part : nullptr,
+                                            st));
+    if (ranges) {
+      // dK partials first, then dV partials (one tile per key block and range)
+      const size_t tiles = static_cast<size_t>(p.cfg.B) * p.cfg.H * p.sz.nb * p.sz.key_chunks;
+      PRISM_CUDA(prism::launch_sum_combine(p, col_ptr, row_idx, part, dKp, st));
+      PRISM_CUDA(prism::launch_sum_combine(p, col_ptr, row_idx, part + tiles * 128 * 128, dVp,
+                                           st));
+    }
     PRISM_TRACED(PRISM_TRACE_ATTN_DQ,
                  prism::launch_attn_dq_tc(
                      p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx, scale, dQp, w,
-                     ranges ? reinterpret_cast<uint16_t*>(w + p.off_part) : nullptr, st));
-    if (ranges) PRISM_CUDA(prism::launch_dq_combine(p, row_ptr, col_idx, w, dQp, st));
+                     ranges ? part : nullptr, st));
+    if (ranges) PRISM_CUDA(prism::launch_sum_combine(p, row_ptr, col_idx, part, dQp, st));
   } else {
     float* dq = reinterpret_cast<float*>(w + p.off_dq);
     PRISM_TRACED(PRISM_TRACE_BWD_PRE,

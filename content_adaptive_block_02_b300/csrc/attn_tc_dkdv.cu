@@ -51,7 +51,7 @@ struct BwdBars {
   uint64_t s_full, dp_full, dp_free, p_ready, ds_ready, ds_empty;
   uint64_t kv_done, kv_free, final_bar;
   uint64_t work_full[2], work_empty[2];
-  int work_col[2], work_beg[2], work_end[2], work_nvk[2];
+  int work_col[2], work_beg[2], work_end[2], work_nvk[2], work_chunk[2];
   int stage_i[2], stage_nvq[2];  // query block of each Q / dO stage and its real rows
   int xok[2][2][4];  // [meeting parity][column half][lane quarter]: still on track
   uint32_t tmem_base;
@@ -67,10 +67,15 @@ struct BwdParams {
   const int32_t* row_idx;
   uint16_t* dKp;
   uint16_t* dVp;
+  uint16_t* dkpart;  // chunks > 1: partial dK (scaled) / dV per (key block, query range)
+  uint16_t* dvpart;
   uint32_t* status;
-  long long cols;  // B*H*nb work items
+  long long cols;    // B*H*nb key blocks
+  long long items;   // cols * chunks work items
   long long Np;
   int nb;
+  int chunks;        // query ranges per head (1: no split)
+  int chunk_blocks;  // query blocks per range
   float scale, scale_log2;
   unsigned long long limit;
   int starve;  // fault injection (test only): the producer issues no loads
@@ -133,14 +138,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t it = 0; ok; ++it) {
         const int ws = it & 1;
         if (!W.wait(&sm.work_empty[ws], ((it >> 1) & 1) ^ 1, 21)) break;
-        const long long col = atomicAdd(P.status + WS_BWD_QUEUE, 1u);
-        if (col >= P.cols) {
+        const long long item = atomicAdd(P.status + WS_BWD_QUEUE, 1u);
+        if (item >= P.items) {
           sm.work_col[ws] = -1;
           mbar_arrive(&sm.work_full[ws]);
           break;
         }
-        const int beg = P.col_ptr[col], end = P.col_ptr[col + 1];
+        // item -> (b, h), query range c, key block j (ranges outermost within
+        // a head, so the Q / dO tiles in use stay in L2)
+        const long long per_bh = static_cast<long long>(P.chunks) * P.nb;
+        const long long bhi = item / per_bh;
+        const int rem = static_cast<int>(item - bhi * per_bh);
+        const int c = rem / P.nb;
+        const long long col = bhi * P.nb + (rem - c * P.nb);
+        int beg = P.col_ptr[col], end = P.col_ptr[col + 1];
+        if (P.chunks > 1) {
+          const int lo = c * P.chunk_blocks;
+          beg = lower_bound_i32(P.row_idx, beg, end, lo);
+          end = lower_bound_i32(P.row_idx, beg, end, lo + P.chunk_blocks);
+        }
         sm.work_col[ws] = static_cast<int>(col);
+        sm.work_chunk[ws] = c;
         sm.work_beg[ws] = beg;
         sm.work_end[ws] = end;
         sm.work_nvk[ws] = P.n_valid[col];
@@ -304,11 +322,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long bh = col / P.nb;
       const int j = static_cast<int>(col % P.nb);
       const long long krow = bh * P.Np + static_cast<long long>(j) * kS + r;
-      uint4* dkrow = reinterpret_cast<uint4*>(P.dKp + krow * kD) + half * 8;
-      uint4* dvrow = reinterpret_cast<uint4*>(P.dVp + krow * kD) + half * 8;
+      // output rows: the final dK / dV, or this query range's partial ones
+      const long long prow =
+          (static_cast<long long>(col) * P.chunks + sm.work_chunk[ws]) * kS + r;
+      uint4* dkrow =
+          reinterpret_cast<uint4*>(P.chunks > 1 ? P.dkpart + prow * kD : P.dKp + krow * kD) +
+          half * 8;
+      uint4* dvrow =
+          reinterpret_cast<uint4*>(P.chunks > 1 ? P.dvpart + prow * kD : P.dVp + krow * kD) +
+          half * 8;
       if (n == 0) {
+        // (with query ranges, the combining kernel handles empty ranges)
+        if (P.chunks == 1) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dkrow[q] = dvrow[q] = make_uint4(0, 0, 0, 0);
+          for (int q = 0; q < 8; ++q) dkrow[q] = dvrow[q] = make_uint4(0, 0, 0, 0);
+        }
         mbar_arrive(&sm.work_empty[ws]);
         continue;
       }
@@ -446,7 +474,7 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
                                 const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
                                 const float* D, const int32_t* n_valid, const int32_t* col_ptr,
                                 const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
-                                uint8_t* ws, cudaStream_t st) {
+                                uint8_t* ws, uint16_t* dkvpart, cudaStream_t st) {
   const prism_config_t& c = p.cfg;
   const long long rows_total = static_cast<long long>(c.B) * c.H * p.sz.Np;
   CUtensorMap tmQ, tmK, tmV, tmdO;
@@ -463,6 +491,12 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
   a.dVp = dVp;
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.cols = static_cast<long long>(c.B) * c.H * p.sz.nb;
+  a.chunks = dkvpart != nullptr ? p.sz.key_chunks : 1;
+  a.chunk_blocks = a.chunks > 1 ? p.sz.chunk_blocks : p.sz.nb;
+  a.items = a.cols * a.chunks;
+  // dK partials, then dV partials
+  a.dkpart = dkvpart;
+  a.dvpart = dkvpart != nullptr ? dkvpart + a.items * kS * kD : nullptr;
   a.Np = p.sz.Np;
   a.nb = p.sz.nb;
   a.scale = scale;
@@ -474,7 +508,7 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
   e = cudaFuncSetAttribute(attn_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const long long g = a.cols < sm_count() ? a.cols : sm_count();
+  const long long g = a.items < sm_count() ? a.items : sm_count();
   attn_dkdv_tc_kernel<<<static_cast<unsigned>(g), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmdO,
                                                                             a);
   return cudaGetLastError();

@@ -1,18 +1,21 @@
-// Combination of the per-key-range partial results of the tensor-core forward
-// and dQ kernels (plans with key_chunks > 1).
+// Combination of the per-range partial results of the tensor-core attention
+// kernels (plans with key_chunks > 1).
 //
 // Prism (arXiv 2610.05416), Fig. 2 caption: a query block attends to the
 // union of its selected key blocks.  The kernels walk each head's key blocks
 // range by range; a query block's selected blocks in range c give a partial
 // softmax state (normalised O_c, running max m_c in log2 units, row sum l_c)
-// and a partial dQ_c.  Exact combination:
+// and a partial dQ_c; the dK / dV kernel walks the query blocks that
+// selected a key block range by range in the same way (partial dK_c, dV_c).
+// Exact combination:
 //   M = max_c m_c,  w_c = l_c 2^(m_c - M),  O = sum_c w_c O_c / sum_c w_c,
-//   LSE = (M + log2 sum_c w_c) ln 2,        dQ = sum_c dQ_c,
-// over the ranges that hold at least one selected block.
+//   LSE = (M + log2 sum_c w_c) ln 2,   dQ = sum_c dQ_c,  dK = sum_c dK_c, ...
+// over the ranges that hold at least one entry of the block's list.
 //
-// One CTA per query block (256 threads): the ranges that hold entries are
-// found by binary search in the block's ascending CSR list; half-warps then
-// take one query row each, 16 lanes x 16 bytes = one 256-byte row.
+// One CTA per block (256 threads; a query block for O and dQ, a key block
+// for dK and dV): the ranges that hold entries are found by binary search in
+// the block's ascending list (CSR or CSC); half-warps then take one token row
+// each, 16 lanes x 16 bytes = one 256-byte row.
 #include "prism_internal.cuh"
 
 namespace prism {
@@ -86,13 +89,15 @@ __global__ void __launch_bounds__(kCombThreads) fwd_combine_kernel(
   }
 }
 
-__global__ void __launch_bounds__(kCombThreads) dq_combine_kernel(
-    int nb, long long Np, int C, int kc, const int32_t* __restrict__ row_ptr,
-    const int32_t* __restrict__ col_idx, const uint16_t* __restrict__ dqpart,
-    uint16_t* __restrict__ dQp) {
+// out tile = sum over the ranges holding entries of the block's list
+// (CSR for dQ, CSC for dK and dV) of the bf16 partial tiles.
+__global__ void __launch_bounds__(kCombThreads) sum_combine_kernel(
+    int nb, long long Np, int C, int kc, const int32_t* __restrict__ ptr,
+    const int32_t* __restrict__ idx, const uint16_t* __restrict__ part,
+    uint16_t* __restrict__ out) {
   __shared__ int flag[kMaxChunks];
   const long long row = blockIdx.x;
-  range_flags(row_ptr, col_idx, row, C, kc, flag);
+  range_flags(ptr, idx, row, C, kc, flag);
   const long long bh = row / nb;
   const int i = static_cast<int>(row % nb);
   const int q = threadIdx.x & 15;
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(kCombThreads) dq_combine_kernel(
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int c = 0; c < C; ++c) {
       if (!flag[c]) continue;
-      const uint4 u = ldg_nc_v4(dqpart + ((row * C + c) * 128 + r) * 128 + q * 8);
+      const uint4 u = ldg_nc_v4(part + ((row * C + c) * 128 + r) * 128 + q * 8);
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(kCombThreads) dq_combine_kernel(
     o.y = pack_bf16x2(acc[2], acc[3]);
     o.z = pack_bf16x2(acc[4], acc[5]);
     o.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(dQp + grow * 128 + q * 8) = o;
+    *reinterpret_cast<uint4*>(out + grow * 128 + q * 8) = o;
   }
 }
 
@@ -133,14 +138,13 @@ cudaError_t launch_fwd_combine(const Plan& p, const int32_t* row_ptr, const int3
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_combine(const Plan& p, const int32_t* row_ptr, const int32_t* col_idx,
-                              const uint8_t* ws, uint16_t* dQp, cudaStream_t st) {
+cudaError_t launch_sum_combine(const Plan& p, const int32_t* ptr, const int32_t* idx,
+                               const uint16_t* part, uint16_t* out, cudaStream_t st) {
   const long long rows = static_cast<long long>(p.cfg.B) * p.cfg.H * p.sz.nb;
   if (p.sz.key_chunks > kMaxChunks || p.cfg.block_tokens != 128 || p.cfg.d != 128)
     return cudaErrorInvalidValue;
-  dq_combine_kernel<<<static_cast<unsigned>(rows), kCombThreads, 0, st>>>(
-      p.sz.nb, p.sz.Np, p.sz.key_chunks, p.sz.chunk_blocks, row_ptr, col_idx,
-      reinterpret_cast<const uint16_t*>(ws + p.off_part), dQp);
+  sum_combine_kernel<<<static_cast<unsigned>(rows), kCombThreads, 0, st>>>(
+      p.sz.nb, p.sz.Np, p.sz.key_chunks, p.sz.chunk_blocks, ptr, idx, part, out);
   return cudaGetLastError();
 }
 

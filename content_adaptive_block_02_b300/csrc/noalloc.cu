@@ -32,7 +32,7 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
                                 const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
                                 const float* D, const int32_t* n_valid, const int32_t* col_ptr,
                                 const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
-                                uint8_t* ws, cudaStream_t st);
+                                uint8_t* ws, uint16_t* dkvpart, cudaStream_t st);
 cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
                               const uint16_t* Vp, const uint16_t* dOp, const float* lse,
                               const float* D, const int32_t* n_valid, const int32_t* row_ptr,
@@ -110,7 +110,7 @@ extern "C" int prism_sparse_attn_bwd_noalloc(
     if (prism::launch_bwd_pre(p, Op, dOp, lse, D, x, nullptr, st) != cudaSuccess)
       return PRISM_ERR_CUDA;
     if (prism::launch_attn_dkdv_tc(p, Qp, Kp, Vp, dOp, x, D, n_valid, col_ptr, row_idx, scale,
-                                   dKp, dVp, base, st) != cudaSuccess)
+                                   dKp, dVp, base, nullptr, st) != cudaSuccess)
       return PRISM_ERR_CUDA;
     // the whole key range in one pass (no partial-result scratch here)
     if (prism::launch_attn_dq_tc(p, Qp, Kp, Vp, dOp, lse, D, n_valid, row_ptr, col_idx, scale,

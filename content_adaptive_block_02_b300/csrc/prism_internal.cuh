@@ -33,8 +33,10 @@ struct Plan {
 //   off_lse2        fp32  [B*H*Np]       LSE * log2(e) for the backward
 //   off_dq          fp32  [B*H*Np*d]     dQ accumulator of the CUDA-core backward
 //                                        (empty for a tensor-core plan)
-//   off_part        bf16  [B*H*nb, C, S, d] per key range: the forward's normalised
-//                                        partial O, later the dQ kernel's partial dQ
+//   off_part        bf16  2 x [B*H*nb, C, S, d] per key / query range: the forward's
+//                                        normalised partial O, later the dK and dV
+//                                        kernel's partial dK and dV, then the dQ
+//                                        kernel's partial dQ (first half)
 //   off_ml          fp32  [B*H*nb, C, S, 2] per key range: running max (log2 units)
 //                                        and row sum of the forward
 enum : int {
