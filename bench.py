@@ -41,6 +41,12 @@ BWD_PAIR_FLOP = 10 * 128 * 128 * 128         # S, dP, dV, dK, dQ
 DKDV_PAIR_FLOP = 8 * 128 * 128 * 128         # the dK/dV kernel: S^T, dP^T, dV, dK
 DQ_PAIR_FLOP = 6 * 128 * 128 * 128           # the dQ kernel: S, dP (recomputed), dQ
 KERNELS_PER_STEP = 22
+# DRAM bytes (read + written) per launch of the attention kernels on the 2K-like
+# workload, from one ncu capture of these kernel versions (dram__bytes_read.sum +
+# dram__bytes_write.sum, 1 pass; profiles/dram_traffic_2k_attention.md).  Only
+# reported for that workload; to be refreshed whenever the kernels change.
+TRAFFIC_2K = {"attn_fwd_tc_kernel": 12.50e9 + 8.07e9, "attn_dkdv_tc_kernel": 26.09e9 + 19.80e9,
+              "attn_dq_tc_kernel": 20.80e9 + 7.74e9}
 
 
 def peaks():
@@ -305,7 +311,8 @@ def run_ours(args, w):
                      "peak_kind": f"bf16 sustained ({pk['src']})", "unit": "TFLOP/s",
                      "frac": round(kern_tf[dom] / pk["bf16_sus"], 4),
                      "frac_burst": round(kern_tf[dom] / pk["bf16"], 4),
-                     "flop_per_launch": pairs * kern_flop[dom], "traffic": None},
+                     "flop_per_launch": pairs * kern_flop[dom],
+                     "traffic": (TRAFFIC_2K.get(dom_name) if w.name == "2k" else None)},
         "e2e": {"value": round(flop_all / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
