@@ -116,6 +116,31 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_workload(w, rank: int):
+    """The problem of replica `rank`: the same workload with its own seeds, so
+    that N replicas process N independent problems (every head of every batch
+    is independent through all steps; no data-path exchange)."""
+    return w.with_(seed_base=w.seed_base + 100 * rank)
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Slowest rank's value (timings are bracketed by barriers on every rank)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, device) -> float:
+    """Whole-job total of a per-rank count (the units all ranks processed)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------- ours ----
 
 def run_ours(args, w):
@@ -125,7 +150,7 @@ def run_ours(args, w):
     if ws > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     build.build()
-    wr = w.with_(seed_base=w.seed_base + 100 * rank)     # an independent problem per replica
+    wr = replica_workload(w, rank)     # an independent problem per replica
     x = synth.generate(wr, dev)
     att = prism.PrismAttention(wr, dev)
     stream = torch.cuda.current_stream()
@@ -201,15 +226,8 @@ def run_ours(args, w):
     bwd_ms = statistics.mean(m[2].elapsed_time(m[3]) for m in marks)
     kern_ms = {s: statistics.mean(tr[s][0].elapsed_time(tr[s][1]) for tr in traces)
                for s in prism.Plan.TRACE_SLOTS}
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        f = torch.tensor([float(flop)], device=dev)
-        torch.distributed.all_reduce(f)
-        flop_all = float(f.item())
-    else:
-        flop_all = float(flop)
+    ms = max_over_ranks(ms, dev)
+    flop_all = sum_over_ranks(flop, dev)
     st = att.status()
 
     # ---- end to end through host buffers (pinned): every step's inputs are
@@ -261,11 +279,7 @@ def run_ours(args, w):
     stream.wait_stream(s_h2d)
     e1.record(stream)
     torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / e_steps
-    if ws > 1:
-        t = torch.tensor([e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
 
     pk = peaks()
     bwd_achieved = pairs * BWD_PAIR_FLOP / (bwd_ms * 1e-3) / 1e12
@@ -401,7 +415,10 @@ def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
-    x = synth.generate(w, "cpu")
+    # the seeded inputs (untimed setup): made by the generator's torch ops on the
+    # device when there is one, then held in host memory for the oracle
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    x = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in synth.generate(w, gen).items()}
     X = _head_inputs(x)
     for _ in range(args.warmup):
         oracle_sample(w, X, rows_sample=2)
