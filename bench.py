@@ -453,8 +453,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dense", action="store_true",
                     help="Top-p = 1: every valid key block (the dense comparison)")
+    ap.add_argument("--stress", choices=["white", "onesrc", "skew"], default=None,
+                    help="stress inputs: white field / one dominant audio source / skewed noise")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.stress is not None:
+        w = synth.stress(args.workload, args.stress, w.topp)
     if args.dense:
         w = w.with_(topp=1.0, name=w.name + "-dense")
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)

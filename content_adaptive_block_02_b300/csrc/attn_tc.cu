@@ -7,9 +7,11 @@
 // real tokens of the selected key blocks, scale `scale`, natural-log LSE.
 //
 // Design (one persistent CTA per SM, 352 threads, warp-specialised):
-//   warp 8  producer: takes the next query block from a global work counter,
+//   warp 8  producer: takes the next work item -- a query block and one
+//           range of the head's key blocks (the whole range unless the plan
+//           splits it; see combine.cu) -- from a global work counter,
 //           publishes it in a 2-slot work ring, and streams the K and V tiles
-//           of its selected key blocks into a 3-stage shared-memory ring (one
+//           of its selected key blocks in that range into a 3-stage ring (one
 //           K + V pair per stage) with TMA (128-byte swizzle, 2 boxes of
 //           64 x 128 per tile).
 //   warp 9  S issuer (one thread): S = Q K^T with Q held in tensor memory

@@ -8,7 +8,9 @@
 // runs in its own kernel (attn_tc_dq.cu), so that no partial sum leaves an SM.
 //
 // Work item = one key block j of one (b, h) with the ascending list of query
-// blocks i that selected it (CSC).  For each i, four 128x128x128 products:
+// blocks i that selected it (CSC), restricted to one range of query blocks
+// when the plan walks them in ranges (partial dK / dV per range, summed in
+// combine.cu).  For each i, four 128x128x128 products:
 //   (1) S^T  = K_j Q_i^T           A = K_j (smem),  B = Q_i (smem)   -> TMEM S
 //   (2) dP^T = V_j dO_i^T          A = V_j (smem),  B = dO_i (smem)  -> TMEM dP
 //       P^T = exp(S^T * scale - LSE_i)     (row = key, column = query)

@@ -9,7 +9,9 @@
 // in tensor memory and written once, in bf16, deterministically.
 //
 // Work item = one query block (b, h, i) with its ascending list of key
-// blocks (CSR).  Per key block j, three 128x128x128 products:
+// blocks (CSR), restricted to one range of key blocks when the plan walks
+// them in ranges (partial dQ per range, summed in combine.cu).  Per key block
+// j, three 128x128x128 products:
 //   S  = Q_i K_j^T     A = Q_i (smem),  B = K_j (smem)        -> TMEM S
 //   dP = dO_i V_j^T    A = dO_i (smem), B = V_j (smem)        -> TMEM dP
 //   dQ += dS K_j       A = dS (TMEM, bf16), B = K_j (MN-major) -> TMEM dQ

@@ -125,3 +125,15 @@ def test_key_feature_variance_variant():
     for k in range(8):
         scale = max(1e-30, np.abs(ref[..., k]).max())
         assert np.abs(got[..., k] - ref[..., k]).max() / scale <= 2e-5, k
+
+
+@pytest.mark.parametrize("variant,topp", [("white", 0.9), ("onesrc", 0.9), ("skew", 0.9),
+                                          ("white", 0.5), ("onesrc", 0.99), ("skew", 0.99)])
+def test_stress_variants(variant, topp):
+    """The stress inputs on a small 128-token-block grid: (a) an isotropic
+    white field with no anisotropic noise, (b) one audio source zone carrying
+    90 % of the A2V norm mass, (c) per-zone noise with a 100:1:1 variance
+    ratio along the axes; Top-p 0.5 / 0.9 / 0.99."""
+    kw = dict(white=dict(field="white", noise="none"), onesrc=dict(n_src=1, src_mass=0.9),
+              skew=dict(noise="skew"))[variant]
+    pu.compare(_w128(topp=topp, **kw))
