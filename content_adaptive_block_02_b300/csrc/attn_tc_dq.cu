@@ -5,8 +5,9 @@
 // caption).  dQ_i = scale * sum over the key blocks j selected by query
 // block i of dS_ij K_j, with P_ij = exp(Q_i K_j^T * scale - LSE_i) and
 // dS_ij = P_ij * (dO_i V_j^T - D_i).  The key-block side (dK, dV) runs in a
-// separate kernel, so no partial sum of dQ ever leaves the SM: dQ is summed
-// in tensor memory and written once, in bf16, deterministically.
+// separate kernel, so dQ needs no atomics: it is summed in tensor memory over
+// the key blocks of a range and written once per range, in bf16 (once in all
+// when the plan does not split the keys), deterministically.
 //
 // Work item = one query block (b, h, i) with its ascending list of key
 // blocks (CSR), restricted to one range of key blocks when the plan walks
