@@ -5,7 +5,7 @@
 // caption: trainable methods replace video self-attention during training).
 // The backward is the softmax-attention VJP restricted to the selected
 // (query block, key block) pairs; the selection itself is a constant.  dQ
-// runs in its own kernel (attn_tc_dq.cu), so that no partial sum leaves an SM.
+// runs in its own kernel (attn_tc_dq.cu), so that no gradient needs atomics.
 //
 // Work item = one key block j of one (b, h) with the ascending list of query
 // blocks i that selected it (CSC), restricted to one range of query blocks
