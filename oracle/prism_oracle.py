@@ -446,12 +446,31 @@ def attn_fwd(w, Qp, Kp, Vp, n_valid, lists, scale):
     return Op, lse
 
 
-def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale):
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even: 8 significant bits),
+    returned as float64.  Done on the float64 bit pattern: keep the sign, the
+    exponent and the top 7 fraction bits, rounding on the 45 bits below."""
+    u = np.ascontiguousarray(a, dtype=f64).view(np.uint64)
+    low = u & np.uint64((1 << 45) - 1)
+    keep = u >> np.uint64(45)
+    half = np.uint64(1 << 44)
+    up = (low > half) | ((low == half) & ((keep & np.uint64(1)) == np.uint64(1)))
+    r = (keep + up.astype(np.uint64)) << np.uint64(45)
+    return r.view(f64).reshape(np.shape(a))
+
+
+def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf16=False):
     """VJP of ``attn_fwd_row`` (Prism trains through this attention: Table 2
     caption -- it replaces video self-attention during training).  Gradients
     flow only through the attention; the discrete steps are constants.
     Returns (dq [S, d], dk [rows, d], dv [rows, d]) with dk/dv in the order of
-    ``_gather_keys``."""
+    ``_gather_keys``.
+
+    The VJP's row term D = rowsum(dO * O) (equal to sum_j P_ij dP_ij) is formed
+    from O itself.  READING of the boundary: the backward entry point takes
+    the forward's output O as the forward stores it, in bf16; with
+    ``o_bf16`` D is formed from O rounded to bf16, which is what a backward
+    given that stored O computes.  The default (exact O) is the plain VJP."""
     q = Qp_bh[i * S:(i + 1) * S].astype(f64)
     k = _gather_keys(Kp_bh, n_valid_bh, sel, S).astype(f64)
     v = _gather_keys(Vp_bh, n_valid_bh, sel, S).astype(f64)
@@ -464,7 +483,7 @@ def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale):
     o = P @ v
     dv = P.T @ do
     dP = do @ v.T
-    Dr = (do * o).sum(axis=1, keepdims=True)
+    Dr = (do * (round_bf16(o) if o_bf16 else o)).sum(axis=1, keepdims=True)
     dS = P * (dP - Dr)
     dq = (dS @ k) * scale
     dk = (dS.T @ q) * scale
@@ -472,10 +491,11 @@ def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale):
     return dq, dk, dv
 
 
-def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None):
+def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None, o_bf16=False):
     """Backward over every (b, h, query block) in ``lists``; returns permuted
     dQp, dKp, dVp [B, H, Np, d] (float64).  ``rows_only`` restricts the query
-    blocks that are processed (dK/dV then hold partial sums)."""
+    blocks that are processed (dK/dV then hold partial sums); ``o_bf16`` as
+    in ``attn_bwd_row``."""
     B, H, Np, d = Qp.shape
     S = w.block
     dQ = np.zeros((B, H, Np, d), dtype=f64)
@@ -488,7 +508,7 @@ def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None):
             if rows_only is not None and i not in rows_only:
                 continue
             dq, dk, dv = attn_bwd_row(Qp[b, h], Kp[b, h], Vp[b, h], dOp[b, h], n_valid[b, h],
-                                      i, sel, S, scale)
+                                      i, sel, S, scale, o_bf16)
             dQ[b, h, i * S:(i + 1) * S] += dq
             off = 0
             for j in sel:

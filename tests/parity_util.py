@@ -11,7 +11,10 @@ Contract (checked per step):
     near ties (then the CUDA list is carried into the oracle);
   * CSC lists: exactly the transpose of the CSR lists;
   * attention: max|gpu - ref| / max|ref| per head <= 2e-2 for O and <= 5e-2
-    for dQ, dK, dV (bf16 tensor-core arithmetic against fp64).
+    for dQ, dK, dV (bf16 tensor-core arithmetic against fp64).  The oracle's
+    backward forms its row term D = rowsum(dO * O) from its own O rounded to
+    bf16 (o_bf16): the backward entry point receives O as the forward stores
+    it, in bf16.
 """
 from __future__ import annotations
 
@@ -195,7 +198,8 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
     dOp_o = orc.permute(X["dO"][:, :, hs], perm_o)
     assert np.array_equal(f64(g["dOp"])[:, hs], dOp_o)
     if key_blocks is None and rows is None:
-        dQ_o, dK_o, dV_o = orc.attn_bwd(w_h, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, L_use, scale)
+        dQ_o, dK_o, dV_o = orc.attn_bwd(w_h, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, L_use, scale,
+                                        o_bf16=True)
         for name, got, ref in (("dQ", g["dQp"], dQ_o), ("dK", g["dKp"], dK_o),
                                ("dV", g["dVp"], dV_o)):
             got = f64(got)[:, hs]
@@ -211,7 +215,7 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
         S = w.block
         if rows is not None:
             dQ_o, _, _ = orc.attn_bwd(w_h, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, L_use, scale,
-                                      rows_only=set(rows))
+                                      rows_only=set(rows), o_bf16=True)
             got = f64(g["dQp"])[:, hs]
             e = 0.0
             for b in range(w.B):
@@ -230,7 +234,7 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
                             w_h, Qp_o[b:b + 1, hi:hi + 1], Kp_o[b:b + 1, hi:hi + 1],
                             Vp_o[b:b + 1, hi:hi + 1], dOp_o[b:b + 1, hi:hi + 1],
                             nval_o[b:b + 1, hi:hi + 1], {(0, 0): L_use[(b, hi)]}, scale,
-                            rows_only=qs)
+                            rows_only=qs, o_bf16=True)
                         sl = slice(j * S, (j + 1) * S)
                         for nm, ref in (("dKp", dK_o), ("dVp", dV_o)):
                             got = f64(g[nm])[b, hs[hi], sl]
@@ -321,7 +325,7 @@ def compare_sampled(w, heads, n_rows=6, n_key_blocks=1, seed=0, report=None):
             Lrows = {(0, 0): [Lg[i] if i in rows else None for i in range(nb)]}
             Op_o, lse_o = orc.attn_fwd(w1, Qp_o, Kp_o, Vp_o, nval_o, Lrows, scale)
             dQ_o, _, _ = orc.attn_bwd(w1, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, Lfull, scale,
-                                      rows_only=set(rows))
+                                      rows_only=set(rows), o_bf16=True)
             Op_g, lse_g, dQp_g = f64(att.Op[sl]), f64(att.lse[sl]), f64(att.dQp[sl])
             # the contract is per tensor (per head): max |err| / max |ref|; on a
             # sample the maxima run over the sampled rows (a smaller, stricter
@@ -349,7 +353,8 @@ def compare_sampled(w, heads, n_rows=6, n_key_blocks=1, seed=0, report=None):
             for j in rng.choice(realk, size=min(n_key_blocks, len(realk)), replace=False):
                 j = int(j)
                 _, dK_o, dV_o = orc.attn_bwd(w1, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, Lfull, scale,
-                                             rows_only=set(int(i) for i in cols[j]))
+                                             rows_only=set(int(i) for i in cols[j]),
+                                             o_bf16=True)
                 r = slice(j * S, (j + 1) * S)
                 for nm, ref in (("dKp", dK_o), ("dVp", dV_o)):
                     got = f64(getattr(att, nm)[sl])[0, 0, r]

@@ -449,3 +449,39 @@ def test_lse_is_log_sum_exp_of_selected_scores():
         want = max(s) + math.log(math.fsum(math.exp(v - max(s)) for v in s))
         slot = r["inv"][0, h, n]
         assert abs(r["lse"][0, h, slot] - want) < 1e-12
+
+
+# ------------------------------------------------------- bf16 rounding ------
+
+def test_round_bf16_matches_the_library_conversion_and_ties_to_even():
+    rng = np.random.default_rng(3)
+    # values exactly representable in fp32, so the library's conversion has a
+    # single rounding too
+    x = rng.standard_normal(20000).astype(np.float32).astype(np.float64) * 10.0 ** rng.integers(-8, 8, 20000)
+    x = x.astype(np.float32).astype(np.float64)
+    ref = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(orc.round_bf16(x), ref)
+    # exact ties: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 (even: 1);
+    # 1 + 3 * 2^-8 halfway between 1 + 2^-7 and 1 + 2^-6 (even: 1 + 2^-6)
+    t = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 0.0, -0.0])
+    assert orc.round_bf16(t).tolist() == [1.0, 1 + 2.0 ** -6, -1.0, 0.0, -0.0]
+
+
+def test_backward_from_stored_bf16_output_differs_by_the_rounding_of_o_only():
+    """o_bf16 changes only D = rowsum(dO * O): dV is unchanged and dQ moves by
+    at most scale * max|K| * 2^-8 * sum_c |dO_c| |O_c| per row (each P row sums
+    to one; bf16 rounding is within 2^-8 relative)."""
+    rng = np.random.default_rng(5)
+    S, d, nb = 8, 16, 4
+    Qp = rng.standard_normal((nb * S, d)); Kp = rng.standard_normal((nb * S, d))
+    Vp = rng.standard_normal((nb * S, d)); dOp = rng.standard_normal((nb * S, d))
+    nv = np.full(nb, S)
+    sel = np.array([0, 2, 3])
+    scale = 1 / math.sqrt(d)
+    dq0, dk0, dv0 = orc.attn_bwd_row(Qp, Kp, Vp, dOp, nv, 1, sel, S, scale)
+    dq1, dk1, dv1 = orc.attn_bwd_row(Qp, Kp, Vp, dOp, nv, 1, sel, S, scale, o_bf16=True)
+    assert np.array_equal(dv0, dv1)
+    o, _ = orc.attn_fwd_row(Qp, Kp, Vp, nv, 1, sel, S, scale)
+    bound = scale * np.abs(Kp).max() * 2.0 ** -8 * (np.abs(dOp[S:2 * S]) * np.abs(o)).sum(1)
+    assert np.all(np.abs(dq1 - dq0).max(1) <= bound + 1e-15)
+    assert np.abs(dq1 - dq0).max() > 0
