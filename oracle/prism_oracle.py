@@ -459,7 +459,8 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     return r.view(f64).reshape(np.shape(a))
 
 
-def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf16=False):
+def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf16=False,
+                 abs_terms=False):
     """VJP of ``attn_fwd_row`` (Prism trains through this attention: Table 2
     caption -- it replaces video self-attention during training).  Gradients
     flow only through the attention; the discrete steps are constants.
@@ -470,7 +471,13 @@ def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf
     from O itself.  READING of the boundary: the backward entry point takes
     the forward's output O as the forward stores it, in bf16; with
     ``o_bf16`` D is formed from O rounded to bf16, which is what a backward
-    given that stored O computes.  The default (exact O) is the plain VJP."""
+    given that stored O computes.  The default (exact O) is the plain VJP.
+
+    ``abs_terms`` also returns the sizes to which a relative error eps in D
+    carries into dq and dk, divided by eps: with a_i = sum_c |dO_ic| |O_ic|
+    (the bound on |D_i| error per unit eps), scale * (P * a) |K| and
+    scale * (P * a)^T |Q|.  Rows whose softmax is nearly one-hot make dq and
+    dk cancel to about this size times the rounding of O."""
     q = Qp_bh[i * S:(i + 1) * S].astype(f64)
     k = _gather_keys(Kp_bh, n_valid_bh, sel, S).astype(f64)
     v = _gather_keys(Vp_bh, n_valid_bh, sel, S).astype(f64)
@@ -488,34 +495,51 @@ def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf
     dq = (dS @ k) * scale
     dk = (dS.T @ q) * scale
     dq[nv:] = 0.0
+    if abs_terms:
+        pa = P * (np.abs(do) * np.abs(o)).sum(axis=1, keepdims=True)
+        dq_abs = (pa @ np.abs(k)) * scale
+        dq_abs[nv:] = 0.0
+        return dq, dk, dv, dq_abs, (pa.T @ np.abs(q)) * scale
     return dq, dk, dv
 
 
-def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None, o_bf16=False):
+def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None, o_bf16=False,
+             abs_terms=False):
     """Backward over every (b, h, query block) in ``lists``; returns permuted
     dQp, dKp, dVp [B, H, Np, d] (float64).  ``rows_only`` restricts the query
-    blocks that are processed (dK/dV then hold partial sums); ``o_bf16`` as
-    in ``attn_bwd_row``."""
+    blocks that are processed (dK/dV then hold partial sums); ``o_bf16`` and
+    ``abs_terms`` as in ``attn_bwd_row`` (with ``abs_terms`` two more arrays,
+    the summed sizes of the dQ and dK terms, are returned)."""
     B, H, Np, d = Qp.shape
     S = w.block
     dQ = np.zeros((B, H, Np, d), dtype=f64)
     dK = np.zeros((B, H, Np, d), dtype=f64)
     dV = np.zeros((B, H, Np, d), dtype=f64)
+    if abs_terms:
+        aQ = np.zeros((B, H, Np, d), dtype=f64)
+        aK = np.zeros((B, H, Np, d), dtype=f64)
     for (b, h), L in lists.items():
         for i, sel in enumerate(L):
             if sel is None or len(sel) == 0:
                 continue
             if rows_only is not None and i not in rows_only:
                 continue
-            dq, dk, dv = attn_bwd_row(Qp[b, h], Kp[b, h], Vp[b, h], dOp[b, h], n_valid[b, h],
-                                      i, sel, S, scale, o_bf16)
+            r = attn_bwd_row(Qp[b, h], Kp[b, h], Vp[b, h], dOp[b, h], n_valid[b, h],
+                             i, sel, S, scale, o_bf16, abs_terms)
+            dq, dk, dv = r[:3]
             dQ[b, h, i * S:(i + 1) * S] += dq
+            if abs_terms:
+                aQ[b, h, i * S:(i + 1) * S] += r[3]
             off = 0
             for j in sel:
                 nv = int(n_valid[b, h, j])
                 dK[b, h, j * S: j * S + nv] += dk[off: off + nv]
                 dV[b, h, j * S: j * S + nv] += dv[off: off + nv]
+                if abs_terms:
+                    aK[b, h, j * S: j * S + nv] += r[4][off: off + nv]
                 off += nv
+    if abs_terms:
+        return dQ, dK, dV, aQ, aK
     return dQ, dK, dV
 
 

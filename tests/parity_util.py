@@ -72,11 +72,15 @@ def rel_err(a, b):
 
 
 def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=None,
-            attn_kernel=0, shape_id=None, key_chunk_blocks=0):
+            attn_kernel=0, shape_id=None, key_chunk_blocks=0, grad_scale="result"):
     """Run both sides on the seeded inputs of `w`; assert the contract.
     heads / rows / key_blocks restrict the oracle's attention work (a sample
     of the (b, h), query blocks and key blocks).  shape_id ([B, H, Z] ints):
-    block shapes given to both sides instead of the statistics and Eq. 7."""
+    block shapes given to both sides instead of the statistics and Eq. 7.
+    grad_scale "terms" adds to the dQ / dK tolerance the error that a 2^-7
+    relative error in D = rowsum(dO * O) carries into them (two bf16
+    roundings of O: the forward's and the stored value's), for inputs whose
+    softmax rows are nearly one-hot, where dQ and dK cancel to that size."""
     inputs = synth.generate(w, "cpu")
     att, g = run_gpu(w, inputs, attn_kernel, shape_id, key_chunk_blocks)
     rep_ = {} if report is None else report
@@ -91,7 +95,7 @@ def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=No
         sid_use = np.asarray(shape_id, dtype=np.int64)[:, hs]
         assert np.array_equal(g["shape_id"].numpy().astype(np.int64)[:, hs], sid_use)
         return _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd,
-                                    rep, heads)
+                                    rep, heads, grad_scale)
 
     # ---- step 1: zone statistics ----
     Vs = X["V"][:, :, hs, :]
@@ -116,11 +120,11 @@ def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=No
     rep["shape_ties_taken"] = int(mism.sum())
     sid_use = np.where(mism, sid_g, sid_o)
     return _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd, rep,
-                                heads)
+                                heads, grad_scale)
 
 
 def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd, rep,
-                         heads):
+                         heads, grad_scale="result"):
     """Steps 2 (permutation, pooling) to 5b of ``compare`` for given shapes."""
     perm_o, inv_o, nval_o = orc.build_permutation(w_h, sid_use)
     assert np.array_equal(g["perm"].numpy()[:, hs], perm_o)
@@ -198,12 +202,18 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
     dOp_o = orc.permute(X["dO"][:, :, hs], perm_o)
     assert np.array_equal(f64(g["dOp"])[:, hs], dOp_o)
     if key_blocks is None and rows is None:
-        dQ_o, dK_o, dV_o = orc.attn_bwd(w_h, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, L_use, scale,
-                                        o_bf16=True)
-        for name, got, ref in (("dQ", g["dQp"], dQ_o), ("dK", g["dKp"], dK_o),
-                               ("dV", g["dVp"], dV_o)):
+        dQ_o, dK_o, dV_o, aQ_o, aK_o = orc.attn_bwd(w_h, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, L_use,
+                                                    scale, o_bf16=True, abs_terms=True)
+        for name, got, ref, terms in (("dQ", g["dQp"], dQ_o, aQ_o), ("dK", g["dKp"], dK_o, aK_o),
+                                      ("dV", g["dVp"], dV_o, None)):
             got = f64(got)[:, hs]
-            e = max(rel_err(got[b, hi], ref[b, hi]) for b in range(w.B) for hi in range(len(hs)))
+            if grad_scale == "terms" and terms is not None:
+                e = max(np.abs(got[b, hi] - ref[b, hi]).max() /
+                        (np.abs(ref[b, hi]).max() + 2.0 ** -7 * terms[b, hi].max() / G_TOL)
+                        for b in range(w.B) for hi in range(len(hs)))
+            else:
+                e = max(rel_err(got[b, hi], ref[b, hi]) for b in range(w.B)
+                        for hi in range(len(hs)))
             rep[name + "_max_rel"] = e
             assert e <= G_TOL, (name, e)
         if heads is None:

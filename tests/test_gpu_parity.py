@@ -136,4 +136,7 @@ def test_stress_variants(variant, topp):
     ratio along the axes; Top-p 0.5 / 0.9 / 0.99."""
     kw = dict(white=dict(field="white", noise="none"), onesrc=dict(n_src=1, src_mass=0.9),
               skew=dict(noise="skew"))[variant]
-    pu.compare(_w128(topp=topp, **kw))
+    # the white field's source zone gives nearly one-hot softmax rows (logits
+    # up to ~110): there dQ and dK cancel to the size of their terms' rounding
+    # and are measured against the size of the terms
+    pu.compare(_w128(topp=topp, **kw), grad_scale="terms" if variant == "white" else "result")
