@@ -103,7 +103,8 @@ MENU_TINY = ((1, 4, 4), (2, 2, 4), (2, 4, 2), (1, 2, 8), (1, 8, 2))
 MENU_128 = ((1, 8, 16), (1, 16, 8), (2, 8, 8), (4, 4, 8), (4, 8, 4), (2, 4, 16), (2, 16, 4))
 
 # Block-mean field gain: chosen once so that the 720p-like grid at Top-p 0.9,
-# Top-k floor 8 lands in the 85-90 % block-sparsity band.
+# Top-k floor 8 lands in the 85-90 % block-sparsity band (88.6 % measured on
+# head 0 by the oracle), then frozen.
 GAMMA = 1.95
 
 WORKLOADS = {
