@@ -152,7 +152,7 @@ def run_ours(args, w):
     build.build()
     wr = replica_workload(w, rank)     # an independent problem per replica
     x = synth.generate(wr, dev)
-    att = prism.PrismAttention(wr, dev)
+    att = prism.PrismAttention(wr, dev, key_chunk_blocks=args.key_chunk_blocks)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
@@ -326,7 +326,8 @@ def run_ours(args, w):
                      "frac": round(kern_tf[dom] / pk["bf16_sus"], 4),
                      "frac_burst": round(kern_tf[dom] / pk["bf16"], 4),
                      "flop_per_launch": pairs * kern_flop[dom],
-                     "traffic": (TRAFFIC_2K.get(dom_name) if w.name == "2k" else None)},
+                     "traffic": (TRAFFIC_2K.get(dom_name)
+                                 if w.name == "2k" and args.key_chunk_blocks == 0 else None)},
         "e2e": {"value": round(flop_all / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
@@ -453,6 +454,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dense", action="store_true",
                     help="Top-p = 1: every valid key block (the dense comparison)")
+    ap.add_argument("--key-chunk-blocks", type=int, default=0,
+                    help="key / query range size of the attention kernels (0: automatic)")
     ap.add_argument("--stress", choices=["white", "onesrc", "skew"], default=None,
                     help="stress inputs: white field / one dominant audio source / skewed noise")
     args = ap.parse_args()
