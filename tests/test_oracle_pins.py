@@ -485,3 +485,67 @@ def test_backward_from_stored_bf16_output_differs_by_the_rounding_of_o_only():
     bound = scale * np.abs(Kp).max() * 2.0 ** -8 * (np.abs(dOp[S:2 * S]) * np.abs(o)).sum(1)
     assert np.all(np.abs(dq1 - dq0).max(1) <= bound + 1e-15)
     assert np.abs(dq1 - dq0).max() > 0
+
+
+# ------------------------------------------------- library and structure ----
+
+def test_masked_attention_vjp_equals_torch_autograd():
+    """The reference masked attention's VJP (used by the brute-force pin)
+    against torch's autograd of the same masked softmax attention in fp64."""
+    rng = np.random.default_rng(11)
+    N, d = 40, 12
+    Q, K, V, dO = (rng.standard_normal((N, d)) for _ in range(4))
+    mask = rng.random((N, N)) < 0.3
+    mask[np.arange(N), rng.integers(0, N, N)] = True          # every row keeps a key
+    scale = 1 / math.sqrt(d)
+    O, dQ, dK, dV = orc.masked_attention(Q, K, V, mask, scale, dO=dO)
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (Q, K, V))
+    s = (tq @ tk.T * scale).masked_fill(~torch.tensor(mask), float("-inf"))
+    to = torch.softmax(s, dim=-1) @ tv
+    to.backward(torch.tensor(dO, dtype=torch.float64))
+    assert np.abs(O - to.detach().numpy()).max() <= 1e-12
+    for got, ref in ((dQ, tq.grad), (dK, tk.grad), (dV, tv.grad)):
+        assert np.abs(got - ref.numpy()).max() <= 1e-12
+
+
+def test_csc_is_the_transpose_of_the_lists():
+    rng = np.random.default_rng(2)
+    nb = 23
+    L = [None if i % 7 == 3 else np.sort(rng.choice(nb, rng.integers(0, 9), replace=False))
+         for i in range(nb)]
+    cols = orc.csc_from_lists(L, nb)
+    pairs_rows = {(i, int(j)) for i, s in enumerate(L) if s is not None for j in s}
+    pairs_cols = {(int(i), j) for j, c in enumerate(cols) for i in c}
+    assert pairs_rows == pairs_cols
+    assert all(np.all(np.diff(c) > 0) for c in cols)
+
+
+def test_block_scores_are_bilinear_and_scaled():
+    rng = np.random.default_rng(4)
+    d = 16
+    Qb, Kb = rng.standard_normal((5, d)), rng.standard_normal((7, d))
+    S = orc.block_scores(Qb, Kb, d)
+    assert np.allclose(orc.block_scores(3.0 * Qb, Kb, d), 3.0 * S, rtol=0, atol=1e-12)
+    e = np.eye(d) * d ** 0.25                                   # e_i . e_i / sqrt(d) = 1
+    assert np.allclose(orc.block_scores(e[:4], e[:4], d), np.eye(4), rtol=0, atol=1e-14)
+    assert np.allclose(orc.block_scores(e[:2], e[2:4], d), 0.0, rtol=0, atol=0)
+
+
+def test_select_blocks_applies_the_row_rule_and_skips_empty_blocks():
+    w = synth.WORKLOADS["tiny"].with_(B=1, H=2, topk_floor=2, topp=0.7)
+    rng = np.random.default_rng(9)
+    nb, d = 16, w.d
+    Qb, Kb = rng.standard_normal((1, 2, nb, d)), rng.standard_normal((1, 2, nb, d))
+    nv = np.full((1, 2, nb), 16)
+    nv[0, 0, [3, 11]] = 0                                       # blocks without real tokens
+    L, F = orc.select_blocks(w, Qb, Kb, nv)
+    for h in range(2):
+        S = orc.block_scores(Qb[0, h], Kb[0, h], d)
+        valid = nv[0, h] > 0
+        for i in range(nb):
+            if not valid[i]:
+                assert len(L[(0, h)][i]) == 0
+                continue
+            ref, flag = orc.hybrid_select_row(S[i], valid, w.topk_floor, w.topp)
+            assert np.array_equal(L[(0, h)][i], ref) and F[(0, h)][i] == flag
+            assert not np.isin(L[(0, h)][i], np.flatnonzero(~valid)).any()
