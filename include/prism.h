@@ -105,13 +105,15 @@ typedef struct prism_sizes {
                              prism_sparse_attn_fwd and prism_sparse_attn_bwd */
   int tensor_core_fwd;    /* 1 when the forward attention runs on tcgen05 kernels */
   int tensor_core_bwd;    /* 1 when the backward attention runs on tcgen05 kernels */
-  int key_chunks;         /* the tensor-core forward and dQ kernels split each head's
-                             key blocks into this many ranges of chunk_blocks and
-                             walk them range by range (all query blocks of a head
-                             for one range, then the next), so that the K / V tiles
-                             in use fit in L2; partial results are combined per
-                             query block afterwards.  1 = no split. */
-  int chunk_blocks;       /* key blocks per range (nb when key_chunks == 1) */
+  int key_chunks;         /* the tensor-core attention kernels split each head's
+                             blocks into this many ranges of chunk_blocks and walk
+                             them range by range (the forward and dQ kernels: key
+                             blocks, for all query blocks of a head one range at a
+                             time; the dK / dV kernel: query blocks, likewise), so
+                             that the tiles in use fit in L2; partial results are
+                             combined per block afterwards (their room is part of
+                             ws_bytes).  1 = no split. */
+  int chunk_blocks;       /* blocks per range (nb when key_chunks == 1) */
 } prism_sizes_t;
 
 typedef struct prism_plan prism_plan_t;

@@ -113,3 +113,16 @@ def test_permute_shapes_rejects_null_pointers(L):
     p = prism.Plan(synth.WORKLOADS["tiny"])
     args = [p.h] + [None] * 16
     assert L.prism_permute_shapes(*args) == -1
+
+
+def test_key_range_setting_is_validated_and_sized(L):
+    w = synth.WORKLOADS["720p"].with_(T=6, Hg=40, W=48, H=2)
+    with pytest.raises(prism.PrismError) as e:
+        prism.Plan(w, key_chunk_blocks=-1)
+    assert e.value.code == -1
+    # at most 64 ranges; every block falls in one range
+    p = prism.Plan(w, key_chunk_blocks=1)
+    assert p.sz.key_chunks == 64 and p.sz.key_chunks * p.sz.chunk_blocks >= p.sz.nb
+    # ranges larger than the head: one range, no partial-result workspace
+    q = prism.Plan(w, key_chunk_blocks=10_000)
+    assert q.sz.key_chunks == 1 and q.sz.ws_bytes < p.sz.ws_bytes
