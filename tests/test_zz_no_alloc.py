@@ -30,12 +30,18 @@ def _small128():
     return synth.WORKLOADS["720p"].with_(T=6, Hg=40, W=48, H=2, n_src=1, name="small128")
 
 
-@pytest.mark.parametrize("w", [synth.WORKLOADS["tiny"], _small128()], ids=["tiny", "small128"])
-def test_noalloc_backward_matches_workspace_backward(w):
+@pytest.mark.parametrize("w,kcb", [(synth.WORKLOADS["tiny"], 0), (_small128(), 0),
+                                   (_small128(), 16)],
+                         ids=["tiny", "small128", "small128-key-ranges"])
+def test_noalloc_backward_matches_workspace_backward(w, kcb):
+    """kcb > 0: a plan whose attention kernels walk the blocks in ranges (the
+    workspace backward combines per-range partials; the workspace-free one
+    walks each list in one pass)."""
     fn = _fn()
     dev = torch.device("cuda")
     x = {k: v.to(dev) for k, v in synth.generate(w, "cpu").items() if torch.is_tensor(v)}
-    att = prism.PrismAttention(w, dev)
+    att = prism.PrismAttention(w, dev, key_chunk_blocks=kcb)
+    assert att.plan.sz.key_chunks == (7 if kcb else 1) or w.block != 128
     att.forward(x["Q"], x["K"], x["V"], x["a2v"])
     att.backward(x["dO"])
     torch.cuda.synchronize()
