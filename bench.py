@@ -198,6 +198,13 @@ def run_ours(args, w):
     list_lengths = {"min": int(lens.min()), "p50": int(np.median(lens)),
                     "p99": int(np.percentile(lens, 99)), "max": int(lens.max()),
                     "mean": round(float(lens.mean()), 1)}
+    # shapes chosen per (b, h, zone) (cf. Table 11) and the near ties of both decisions
+    sid = att.perm_out["shape_id"].reshape(-1).cpu().numpy().astype(np.int64)
+    counts = np.bincount(sid, minlength=len(wr.menu))
+    shape_hist = {"x".join(str(e) for e in wr.menu[k]): int(counts[k])
+                  for k in range(len(wr.menu)) if counts[k] > 0}
+    zone_ties = int(att.perm_out["shape_tie"].sum().item())
+    sel_ties = int(att.lists["sel_tie"].sum().item())
     amb = int(att.ws[4:8].view(torch.int32).item())
     flop = pairs * (FWD_PAIR_FLOP + BWD_PAIR_FLOP)
 
@@ -311,6 +318,8 @@ def run_ours(args, w):
                    "block_density": round(pairs / (w.B * w.H * w.n_blocks ** 2), 4),
                    "rows_decided_exactly": amb,
                    "selected_per_query_block": list_lengths,
+                   "shapes_chosen": shape_hist,
+                   "near_ties": {"zone_shapes": zone_ties, "selection_rows": sel_ties},
                    "key_ranges": att.plan.sz.key_chunks},
         "attn_ms": {"fwd": round(fwd_ms, 3), "bwd": round(bwd_ms, 3),
                     "other": round(ms - fwd_ms - bwd_ms, 3)},
