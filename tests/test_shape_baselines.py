@@ -4,6 +4,8 @@ Shape", "Fixed 4^3"): the zones' block shapes are given by the caller
 selection, attention forward and backward -- runs through the same kernels.
 Both sides get the same shapes; the contract is that of the other parity
 tests."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -74,3 +76,24 @@ def test_shape_that_does_not_tile_the_zone_is_reported():
         assert ref.status() == 0
         assert torch.equal(att.perm_out["perm"], ref.perm_out["perm"])
         assert torch.equal(att.O, ref.O)
+
+
+def _table11_class(tokens):
+    path = os.path.join(os.path.dirname(__file__), "golden", "table11_shape_names.txt")
+    for line in open(path):
+        f = line.split()
+        if f and not line.startswith("#") and int(f[0]) == tokens:
+            return tuple(tuple(int(c) for c in name) for name in f[1:])
+    raise KeyError(tokens)
+
+
+def test_only_c64_menu():
+    """"Only C64" (Table 9): the 64-token class of Table 11 as the menu, with
+    the zones' shapes from the statistics and Eq. 7 (4 x 16 x 16 zones admit
+    five of its seven shapes); 64-token blocks run on the CUDA-core attention."""
+    menu = _table11_class(64)
+    w = synth.WORKLOADS["720p"].with_(T=8, Hg=32, W=48, H=2, n_src=1, zone=(4, 16, 16),
+                                      block=64, menu=menu, name="only_c64")
+    assert len(orc.admissible_shapes(w.menu, w.zone)) == 5
+    rep = pu.compare(w)
+    assert rep["O_max_rel"] <= pu.O_TOL
