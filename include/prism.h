@@ -228,7 +228,11 @@ int prism_block_select(const prism_plan_t* plan, const float* Qbar, const float*
 
 /* Step 5a -- block-sparse attention forward (Fig. 2 caption).
  * For every query block i and every key block j in its list, exact softmax
- * over the real tokens of the listed key blocks, scale `scale`.
+ * over the real tokens of the listed key blocks, scale `scale`.  With
+ * prism_sizes_t.key_chunks > 1 the key blocks are walked in ranges and the
+ * per-range partial results, kept in `ws`, are combined before the call's
+ * last kernel writes Op and lse; prism_sparse_attn_bwd does the same for dQ,
+ * dK and dV.  The results do not depend on the split beyond rounding.
  *   Qp, Kp, Vp [B, H, Np, d] bf16 in; n_valid, row_ptr, col_idx as above
  *   Op  [B, H, Np, d] bf16 out (padding rows 0)
  *   lse [B, H, Np] fp32 out: natural-log log-sum-exp per row (padding 0) */

@@ -264,6 +264,42 @@ def test_permutation_is_a_blockwise_bijection():
             assert np.all(np.diff(seg[:nv]) > 0)
 
 
+def test_permutation_orders_zones_then_blocks_in_raster_order():
+    """Reading 7: zones in raster (zt, zh, zw) order, and inside a zone its
+    blocks in raster order of the zone's block grid: block k lies in zone
+    k // blocks_per_zone, at grid position k % blocks_per_zone."""
+    w = _small()
+    sid = _random_shapes(w, 8)
+    perm, inv, nval = orc.build_permutation(w, sid)
+    S = w.block
+    zT, zH, zW = w.zone
+    Tp, Hp, Wp = orc.padded_grid(w.T, w.Hg, w.W, w.zone)
+    nzH, nzW = Hp // zH, Wp // zW
+    bpz = (zT * zH * zW) // S
+    for h in range(w.H):
+        for blk in range(w.n_blocks):
+            nv = int(nval[0, h, blk])
+            if nv == 0:
+                continue
+            Z, local = divmod(blk, bpz)
+            zt, rest = divmod(Z, nzH * nzW)
+            zh, zw = divmod(rest, nzW)
+            bT, bH, bW = w.menu[sid[0, h, Z]]
+            it, rest = divmod(local, (zH // bH) * (zW // bW))
+            ih, iw = divmod(rest, zW // bW)
+            t0, y0, x0 = zt * zT + it * bT, zh * zH + ih * bH, zw * zW + iw * bW
+            seg = perm[0, h, blk * S: blk * S + nv]
+            t, r = np.divmod(seg, w.Hg * w.W)
+            y, x = np.divmod(r, w.W)
+            assert t.min() >= t0 and t.max() < t0 + bT, (h, blk)
+            assert y.min() >= y0 and y.max() < y0 + bH, (h, blk)
+            assert x.min() >= x0 and x.max() < x0 + bW, (h, blk)
+            # every real token of that box is in the block
+            box = [(tt * w.Hg + yy) * w.W + xx for tt in range(t0, min(t0 + bT, w.T))
+                   for yy in range(y0, min(y0 + bH, w.Hg)) for xx in range(x0, min(x0 + bW, w.W))]
+            assert sorted(box) == seg.tolist()
+
+
 def test_permute_unpermute_identity():
     w = _small()
     sid = _random_shapes(w, 4)
