@@ -172,15 +172,20 @@ def _zone_index(w: Workload, device) -> torch.Tensor:
     return (t.view(-1, 1, 1) * nzh + h.view(1, -1, 1)) * nzw + x.view(1, 1, -1)
 
 
-def generate(w: Workload, device="cpu", want_dO: bool = True) -> dict:
-    """Return a dict of bf16 tensors Q, K, V, dO [B, N, H, d], a2v [B, N, Ca]
-    and audio [B, Na, Ca], plus the source-zone ids (for reports)."""
+def generate(w: Workload, device="cpu", want_dO: bool = True, a2v_f32: bool = False) -> dict:
+    """Return a dict of bf16 tensors Q, K, V, dO [B, N, H, d], a2v [B, N, Ca],
+    the A2V queries qa [B, N, Ca] (the head-mean of Q, rounded to bf16) and
+    audio [B, Na, Ca], plus the source-zone ids (for reports).  a2v is
+    computed from qa and audio as they are stored (bf16); with ``a2v_f32``
+    its fp32 value before that rounding is returned too, as a2v_f32."""
     dev = torch.device(device)
     kern = _gauss_kernel(device=dev)
     zid = _zone_index(w, dev)                       # [T,Hg,W]
     out = {k: torch.empty(w.B, w.N, w.H, w.d, dtype=torch.bfloat16, device=dev)
            for k in (["Q", "K", "V"] + (["dO"] if want_dO else []))}
     a2v = torch.empty(w.B, w.N, w.Ca, dtype=torch.bfloat16, device=dev)
+    qa_all = torch.empty(w.B, w.N, w.Ca, dtype=torch.bfloat16, device=dev)
+    a2v32 = torch.empty(w.B, w.N, w.Ca, dtype=torch.float32, device=dev) if a2v_f32 else None
     audio_all = torch.empty(w.B, w.Na, w.Ca, dtype=torch.bfloat16, device=dev)
     src_zones_all = []
     for b in range(w.B):
@@ -220,7 +225,11 @@ def generate(w: Workload, device="cpu", want_dO: bool = True) -> dict:
             if want_dO:
                 out["dO"][b, :, h, :] = torch.randn(w.N, w.d, generator=g, device=dev).bfloat16()
         qbar = (qsum / w.H).reshape(w.N, w.d)
-        att = torch.softmax(qbar[:, : w.Ca] @ A.t() / math.sqrt(w.Ca), dim=-1)
+        qa = torch.zeros(w.N, w.Ca, device=dev)
+        qa[:, : min(w.Ca, w.d)] = qbar[:, : w.Ca]
+        qa = qa.bfloat16()
+        qa_all[b] = qa
+        att = torch.softmax(qa.float() @ A.t() / math.sqrt(w.Ca), dim=-1)
         a2 = att @ A                                                          # [N, Ca]
         if w.src_mass is not None:
             n = a2.norm(dim=-1)
@@ -229,7 +238,12 @@ def generate(w: Workload, device="cpu", want_dO: bool = True) -> dict:
             f = w.src_mass / (1.0 - w.src_mass) * m_out / m_in
             a2[inz] *= f
         a2v[b] = a2.bfloat16()
+        if a2v32 is not None:
+            a2v32[b] = a2
     out["a2v"] = a2v
+    out["qa"] = qa_all
+    if a2v32 is not None:
+        out["a2v_f32"] = a2v32
     out["audio"] = audio_all
     out["src_zones"] = src_zones_all
     return out

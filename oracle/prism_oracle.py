@@ -101,26 +101,54 @@ def line_variance(g: np.ndarray, m: np.ndarray, axis: int) -> np.ndarray:
     return np.where(cnt > 0, num / np.maximum(cnt, 1.0), 0.0)
 
 
+def a2v_norms(Qa: np.ndarray, Ka: np.ndarray, Va: np.ndarray) -> np.ndarray:
+    """Per-token norm of the audio-to-video (A2V) cross-attention output
+    (Prism, Abstract: the zone signals use feature norms from the
+    audio-to-video cross-attention).
+
+    READING (the pages give no formula): one attention head in which every
+    video token's cross-attention query Qa_i attends to the audio tokens'
+    keys Ka and values Va with scale 1/sqrt(Ca) and a softmax over the audio
+    tokens; n_i = ||softmax(Qa_i Ka^T / sqrt(Ca)) Va||_2.
+    Qa [B, N, Ca], Ka / Va [B, Na, Ca] (any float dtype) -> n [B, N] float64."""
+    B, N, Ca = Qa.shape
+    out = np.zeros((B, N), dtype=f64)
+    for b in range(B):
+        s = (Qa[b].astype(f64) @ Ka[b].astype(f64).T) / math.sqrt(Ca)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        P = e / e.sum(axis=1, keepdims=True)
+        out[b] = np.sqrt(((P @ Va[b].astype(f64)) ** 2).sum(axis=1))
+    return out
+
+
 def zone_stats(w, V: np.ndarray, a2v: np.ndarray) -> np.ndarray:
+    """Per (b, h, zone) statistics, [B, H, Z, 8] float64:
+    (var_v_T, var_v_H, var_v_W, var_n_T, var_n_H, var_n_W, nbar, n_valid),
+    from the value features V [B, N, H, d] and the A2V cross-attention output
+    a2v [B, N, Ca] (its per-token norms n_i = ||a2v_i||_2; see
+    ``zone_stats_from_norms``)."""
+    return zone_stats_from_norms(w, V, np.sqrt((a2v.astype(f64) ** 2).sum(axis=-1)))
+
+
+def zone_stats_from_norms(w, V: np.ndarray, n: np.ndarray) -> np.ndarray:
     """Per (b, h, zone) statistics, [B, H, Z, 8] float64:
     (var_v_T, var_v_H, var_v_W, var_n_T, var_n_H, var_n_W, nbar, n_valid).
 
     * var_v_d: directional variance of the VALUE features of head h
       (Prism, Table 9 caption: the default uses value features; the query/key
       variants are ablations) -- ``line_variance`` along d.
-    * n_i = ||a2v_i||_2: per-token norm of the audio-to-video cross-attention
-      output (Prism, Abstract: feature norms from the A2V cross-attention).
+    * n [B, N]: per-token norm of the audio-to-video cross-attention output
+      (Prism, Abstract: feature norms from the A2V cross-attention).
       var_n_d: the same directional variance of the scalar map n (READING of
       the audio directional variance v_hat_{a,d} of Table 9's caption).
       nbar: mean of n over the zone's valid tokens (READING of the audio
       coupling gate's input, Table 9 caption).
-    V: [B, N, H, d], a2v: [B, N, Ca] (any float dtype; used as float64).
+    V: [B, N, H, d] (any float dtype; used as float64).
     """
     B, N, H, d = V.shape
     out = []
     for b in range(B):
-        n_tok = np.sqrt((a2v[b].astype(f64) ** 2).sum(axis=-1))          # [N]
-        gn, m = _grid_views(n_tok[:, None], w, 1)
+        gn, m = _grid_views(np.asarray(n[b], dtype=f64)[:, None], w, 1)
         sn = np.stack([line_variance(gn, m, a) for a in range(3)], -1)    # [Zt,Zh,Zw,3]
         mf = m.astype(f64)
         cnt = mf.sum(axis=(1, 3, 5))
@@ -143,8 +171,12 @@ def zone_stats(w, V: np.ndarray, a2v: np.ndarray) -> np.ndarray:
 # token dominates the cross-attention) have no directional variance; what any
 # arithmetic returns for them is round-off, and its ratios are meaningless.
 # A directional variance whose sum is at most AUDIO_VAR_FLOOR * nbar^2 counts
-# as zero (round-off of a constant map is ~1e-30 nbar^2 in fp64).
-AUDIO_VAR_FLOOR = 1e-20
+# as zero: a spread of the norms below 1e-5 of their size, which a norm map
+# computed in fp32 (relative error ~1e-7, variance ~1e-14 nbar^2 from
+# rounding alone) cannot resolve.  Round-off of a constant map is ~1e-30
+# nbar^2 in fp64; the zones of the synthetic grids that do vary have at least
+# ~1e-3 nbar^2.
+AUDIO_VAR_FLOOR = 1e-10
 
 
 def guidance(w, st: np.ndarray, nbar_max: float) -> np.ndarray:
@@ -214,6 +246,93 @@ def assign_shapes(w, stats: np.ndarray):
                     srt = np.sort(costs)
                     tie[b, h, z] = (srt[1] - srt[0]) < SHAPE_TIE
     return sid, tie
+
+
+def line_variance_bound(g: np.ndarray, m: np.ndarray, axis: int, tau: float) -> np.ndarray:
+    """How far ``line_variance`` of a scalar map (C = 1) can move when every
+    value n_i is replaced by n_i (1 + e_i) with |e_i| <= tau.
+
+    On a line of L values with mean mu the variance moves by
+    (2/L) sum_i (n_i - mu) n_i e_i + (1/L) sum_i (n_i e_i)^2 - (mean of n_i e_i)^2,
+    so by at most (2 tau / L) sum_i |n_i - mu| n_i + (tau^2 / L) sum_i n_i^2;
+    the zone's statistic is the mean over its qualifying lines, and so is the
+    bound.  Returns [Zt, Zh, Zw]."""
+    inner = (1, 3, 5)[axis]
+    mf = m.astype(f64)[..., None]
+    n = mf.sum(axis=inner, keepdims=True)
+    mean = (g * mf).sum(axis=inner, keepdims=True) / np.maximum(n, 1.0)
+    lin = (mf * np.abs(g - mean) * np.abs(g)).sum(axis=inner, keepdims=True)
+    sq = (mf * g * g).sum(axis=inner, keepdims=True)
+    bnd = (2.0 * tau * lin + tau * tau * sq) / np.maximum(n, 1.0)
+    ok = (n >= 2.0)
+    bnd = np.where(ok, bnd, 0.0)
+    other = tuple(a for a in (1, 3, 5) if a != inner)
+    num = bnd.sum(axis=(inner,) + other + (6,))
+    cnt = ok.astype(f64).sum(axis=(inner,) + other) * g.shape[6]
+    cnt = cnt[..., 0] if cnt.ndim == num.ndim + 1 else cnt
+    return np.where(cnt > 0, num / np.maximum(cnt, 1.0), 0.0)
+
+
+def _shape_decision_reachable(w, st: np.ndarray, nmax: float, dvar: np.ndarray,
+                              tau: float) -> bool:
+    """True when the shape chosen from the statistics row ``st`` could change
+    if the audio statistics came from norms off by at most tau relative:
+    var_n_d by at most dvar[d], nbar and the zones' max nbar by at most tau
+    relative.  Every bound below is a worst case over that box (first order
+    where the quantity is linear in the perturbation, exact otherwise)."""
+    if not w.use_audio:
+        return False
+    sv, sn, nbar = st[0:3], st[3:6], st[6]
+    ssv, ssn, dss = sv.sum(), sn.sum(), dvar.sum()
+    # the audio-direction floor: the decision "no direction" must be the same
+    # everywhere in the box
+    fl_lo = AUDIO_VAR_FLOOR * (nbar * (1.0 - tau)) ** 2
+    fl_hi = AUDIO_VAR_FLOOR * (nbar * (1.0 + tau)) ** 2
+    if ssn - dss > fl_hi:
+        vh = sn / ssn
+        dvh = (dvar + vh * dss) / (ssn - dss)
+    elif ssn + dss <= fl_lo:
+        vh, dvh = np.full(3, 1.0 / 3.0), np.zeros(3)
+    else:
+        return True
+    abar = nbar / nmax if nmax > 0 else 0.0
+    dab = abar * 2.0 * tau / (1.0 - tau)
+    r = sv / ssv if ssv > 0 else np.full(3, 1.0 / 3.0)
+    uv = 1.0 if w.use_video else 0.0
+    g = uv * r + abar * vh + w.eps
+    dg = dab * (vh + dvh) + abar * dvh
+    if np.any(dg >= g):
+        return True
+    dL = np.log2(g / (g - dg))                         # largest move of log2 g_d
+    dl = abs(w.alpha) * (dL.sum() / 3.0 + dL / 3.0)    # of log2 b*_d: |mean - own|
+    costs, idx = shape_costs(w, g)
+    kb = int(np.argmin(costs))
+    lb = np.array([[math.log2(e) for e in w.menu[k]] for k in idx])
+    for q in range(len(idx)):
+        if q == kb:
+            continue
+        reach = 2.0 * (np.abs(lb[q] - lb[kb]) * dl).sum()
+        if costs[q] - costs[kb] < SHAPE_TIE + reach:
+            return True
+    return False
+
+
+def norm_sensitive_zones(w, n: np.ndarray, stats: np.ndarray, tau: float) -> np.ndarray:
+    """Zones whose block shape could change if every A2V norm n_i [B, N] were
+    off by up to tau * n_i (a norm map computed in another precision): the
+    near ties of a path whose norms carry that error.  stats [B, H, Z, 8] are
+    the statistics from n itself.  Returns bool [B, H, Z]."""
+    B, H, Z, _ = stats.shape
+    flags = np.zeros((B, H, Z), dtype=bool)
+    for b in range(B):
+        gn, m = _grid_views(np.asarray(n[b], dtype=f64)[:, None], w, 1)
+        dv = np.stack([line_variance_bound(gn, m, a, tau) for a in range(3)], -1).reshape(-1, 3)
+        for h in range(H):
+            st_h = stats[b, h] if w.per_head else stats[b].mean(axis=0)
+            nmax = st_h[:, 6].max()
+            for z in range(Z):
+                flags[b, h, z] = _shape_decision_reachable(w, st_h[z], nmax, dv[z], tau)
+    return flags
 
 
 def build_permutation(w, shape_id: np.ndarray):
@@ -460,7 +579,7 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
 
 
 def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf16=False,
-                 abs_terms=False):
+                 abs_terms=False, o_given=None):
     """VJP of ``attn_fwd_row`` (Prism trains through this attention: Table 2
     caption -- it replaces video self-attention during training).  Gradients
     flow only through the attention; the discrete steps are constants.
@@ -471,13 +590,19 @@ def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf
     from O itself.  READING of the boundary: the backward entry point takes
     the forward's output O as the forward stores it, in bf16; with
     ``o_bf16`` D is formed from O rounded to bf16, which is what a backward
-    given that stored O computes.  The default (exact O) is the plain VJP.
+    given that stored O computes; ``o_given`` ([S, d]) forms D from that O
+    instead (a backward handed some other forward output).  The default
+    (exact O) is the plain VJP.
 
-    ``abs_terms`` also returns the sizes to which a relative error eps in D
-    carries into dq and dk, divided by eps: with a_i = sum_c |dO_ic| |O_ic|
-    (the bound on |D_i| error per unit eps), scale * (P * a) |K| and
-    scale * (P * a)^T |Q|.  Rows whose softmax is nearly one-hot make dq and
-    dk cancel to about this size times the rounding of O."""
+    ``abs_terms`` also returns how far dq and dk move, per element, when the O
+    that D is formed from carries the errors of a forward that rounds to bf16
+    (unit roundoff u): P rounded before the P V product moves O_ic by at most
+    u (P |V|)_ic, and storing O moves it by at most u |O_ic|, so D_i moves by
+    at most u b_i with b_i = sum_c |dO_ic| (|O_ic| + (P |V|)_ic).  D enters
+    dq_i as -scale D_i (P K)_i and dk_j as -scale sum_i D_i P_ij Q_i, so the
+    returned sizes (per unit u) are scale b_i |(P K)_ic| for dq and
+    scale sum_i b_i P_ij |Q_ic| for dk.  Rows whose softmax is nearly one-hot
+    make dq and dk cancel to about these sizes times u."""
     q = Qp_bh[i * S:(i + 1) * S].astype(f64)
     k = _gather_keys(Kp_bh, n_valid_bh, sel, S).astype(f64)
     v = _gather_keys(Vp_bh, n_valid_bh, sel, S).astype(f64)
@@ -490,16 +615,20 @@ def attn_bwd_row(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, i, sel, S, scale, o_bf
     o = P @ v
     dv = P.T @ do
     dP = do @ v.T
-    Dr = (do * (round_bf16(o) if o_bf16 else o)).sum(axis=1, keepdims=True)
+    if o_given is not None:
+        o_used = np.asarray(o_given, dtype=f64)
+    else:
+        o_used = round_bf16(o) if o_bf16 else o
+    Dr = (do * o_used).sum(axis=1, keepdims=True)
     dS = P * (dP - Dr)
     dq = (dS @ k) * scale
     dk = (dS.T @ q) * scale
     dq[nv:] = 0.0
     if abs_terms:
-        pa = P * (np.abs(do) * np.abs(o)).sum(axis=1, keepdims=True)
-        dq_abs = (pa @ np.abs(k)) * scale
+        b = (np.abs(do) * (np.abs(o) + P @ np.abs(v))).sum(axis=1, keepdims=True)
+        dq_abs = scale * b * np.abs(P @ k)
         dq_abs[nv:] = 0.0
-        return dq, dk, dv, dq_abs, (pa.T @ np.abs(q)) * scale
+        return dq, dk, dv, dq_abs, scale * ((P * b).T @ np.abs(q))
     return dq, dk, dv
 
 
@@ -541,6 +670,42 @@ def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None, o_bf16=F
     if abs_terms:
         return dQ, dK, dV, aQ, aK
     return dQ, dK, dV
+
+
+def attn_bwd_key_blocks(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, L, key_blocks, S, scale,
+                        o_bf16=False):
+    """dK and dV of the key blocks ``key_blocks`` of one (b, h): the same VJP
+    as ``attn_bwd_row`` summed over every query block whose list L[i] holds
+    one of them, with only those key blocks' columns formed in full (each
+    query row still needs its whole softmax for P and its whole O for D).
+    Returns {j: (dK_j [S, d], dV_j [S, d])}, rows past n_valid[j] zero."""
+    d = Qp_bh.shape[1]
+    want = set(int(j) for j in key_blocks)
+    out = {j: (np.zeros((S, d)), np.zeros((S, d))) for j in want}
+    for i, sel in enumerate(L):
+        if sel is None or len(sel) == 0 or not want.intersection(int(j) for j in sel):
+            continue
+        q = Qp_bh[i * S:(i + 1) * S].astype(f64)
+        k = _gather_keys(Kp_bh, n_valid_bh, sel, S).astype(f64)
+        v = _gather_keys(Vp_bh, n_valid_bh, sel, S).astype(f64)
+        do = dOp_bh[i * S:(i + 1) * S].astype(f64).copy()
+        do[int(n_valid_bh[i]):] = 0.0
+        s = (q @ k.T) * scale
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        P = e / e.sum(axis=1, keepdims=True)
+        o = P @ v
+        Dr = (do * (round_bf16(o) if o_bf16 else o)).sum(axis=1, keepdims=True)
+        off = 0
+        for j in sel:
+            nv = int(n_valid_bh[j])
+            j = int(j)
+            if j in want:
+                Pj = P[:, off:off + nv]
+                dSj = Pj * (do @ v[off:off + nv].T - Dr)
+                out[j][0][:nv] += (dSj.T @ q) * scale
+                out[j][1][:nv] += Pj.T @ do
+            off += nv
+    return out
 
 
 def csc_from_lists(L, nb: int):

@@ -201,10 +201,11 @@ def test_guidance_zero_statistics_is_isotropic():
 
 def test_audio_guidance_of_a_constant_norm_map_is_isotropic():
     """A zone whose A2V norms are all equal has no audio direction: round-off
-    variances (any size up to 1e-20 nbar^2) give v_hat = 1/3 each, while a
-    small real variance keeps its direction."""
+    variances (any size up to 1e-10 nbar^2: a norm spread below 1e-5, which
+    fp32 norms do not resolve) give v_hat = 1/3 each, while a small real
+    variance keeps its direction."""
     w = synth.WORKLOADS["2k"]
-    for noise in ([3e-30, 1e-31, 0.0], [0.0, 9e-13 / 1e9, 0.0]):
+    for noise in ([3e-30, 1e-31, 0.0], [0.0, 9e-13 / 1e9, 0.0], [5e-9, 3e-9, 4e-9]):
         st = np.array([1.0, 2.0, 3.0] + noise + [11.0, 768.0])
         g = orc.guidance(w, st, 11.0)
         np.testing.assert_allclose(g, np.array([1, 2, 3]) / 6.0 + 1.0 / 3.0 + w.eps)
@@ -224,6 +225,101 @@ def test_assign_shapes_follow_directional_variance():
     assert w.menu[sid[0, 0, 0]] == (1, 16, 8)          # fine along W
     assert w.menu[sid[0, 0, 1]] == (1, 8, 16)          # fine along H
     assert not tie.any()
+
+
+# ------------------------------------------------ A2V cross-attention -------
+
+def test_a2v_norms_special_cases():
+    """One audio token: every output is that token's value; equal logits (zero
+    keys): the output is the mean of the values; a dominant key: its value."""
+    rng = np.random.default_rng(7)
+    B, N, Na, Ca = 2, 9, 5, 8
+    Qa = rng.standard_normal((B, N, Ca))
+    Va = rng.standard_normal((B, Na, Ca))
+    n1 = orc.a2v_norms(Qa, rng.standard_normal((B, 1, Ca)), Va[:, :1])
+    np.testing.assert_allclose(n1, np.linalg.norm(Va[:, 0], axis=-1)[:, None].repeat(N, 1),
+                               rtol=1e-14)
+    n0 = orc.a2v_norms(Qa, np.zeros((B, Na, Ca)), Va)
+    np.testing.assert_allclose(n0, np.linalg.norm(Va.mean(axis=1), axis=-1)[:, None].repeat(N, 1),
+                               rtol=1e-14)
+    Ka = np.zeros((B, Na, Ca))
+    Ka[:, 3] = 1e3 * Qa[:, 0] / np.linalg.norm(Qa[:, 0], axis=-1, keepdims=True)
+    nd = orc.a2v_norms(Qa[:, :1], Ka, Va)
+    np.testing.assert_allclose(nd[:, 0], np.linalg.norm(Va[:, 3], axis=-1), rtol=1e-12)
+
+
+def test_a2v_norms_match_the_generators_cross_attention():
+    """The generator's stand-in for the model's A2V layer (torch, fp32, from
+    the same bf16 queries and audio tokens) against the oracle's norms."""
+    w = synth.WORKLOADS["tiny"]
+    x = synth.generate(w, "cpu", a2v_f32=True)
+    n_ref = np.linalg.norm(x["a2v_f32"].double().numpy(), axis=-1)
+    qa = x["qa"].float().numpy()
+    au = x["audio"].float().numpy()
+    n = orc.a2v_norms(qa, au, au)
+    np.testing.assert_allclose(n, n_ref, rtol=2e-5)
+    # and zone statistics from the norms equal those from the output itself
+    a2v = x["a2v_f32"].double().numpy()
+    V = x["V"].float().numpy()
+    np.testing.assert_allclose(orc.zone_stats_from_norms(w, V, np.linalg.norm(a2v, axis=-1)),
+                               orc.zone_stats(w, V, a2v), rtol=1e-12, atol=1e-300)
+
+
+def test_line_variance_bound_holds_and_is_reached():
+    """Brute force: relative perturbations of a scalar map within tau move
+    every zone's line variance by at most the bound; perturbing each line's
+    values away from its mean (sign of n - mean) comes within O(tau^2) of it."""
+    w = _small()
+    rng = np.random.default_rng(9)
+    n = 3.0 + rng.random(w.N)
+    tau = 1e-3
+    g, m = orc._grid_views(n[:, None], w, 1)
+    for axis in range(3):
+        v0 = orc.line_variance(g, m, axis)
+        bnd = orc.line_variance_bound(g, m, axis, tau)
+        for _ in range(30):
+            gp, _ = orc._grid_views((n * (1 + rng.uniform(-tau, tau, n.shape)))[:, None], w, 1)
+            assert np.all(np.abs(orc.line_variance(gp, m, axis) - v0) <= bnd * (1 + 1e-9))
+    # the extreme perturbation of the W lines: e_i = tau sign(n_i - line mean)
+    inner = 5
+    mean = (g * m[..., None]).sum(axis=inner, keepdims=True) / m[..., None].sum(axis=inner, keepdims=True).clip(1)
+    gp = g * (1 + tau * np.sign(g - mean))
+    lin = orc.line_variance_bound(g, m, 2, tau) - orc.line_variance_bound(g, m, 2, 0.0)
+    move = orc.line_variance(gp, m, 2) - orc.line_variance(g, m, 2)
+    np.testing.assert_allclose(move, lin, rtol=1e-2, atol=1e-12)
+
+
+def test_norm_sensitive_zones_cover_every_flip_under_bounded_norm_errors():
+    """Brute force over norm maps perturbed within tau (relative): every zone
+    whose shape changes is flagged (as a near tie or as norm-sensitive); tau
+    = 0 flags nothing beyond the near ties; one zone with a constant norm map
+    (audio floor) is flagged once tau can lift it over the floor."""
+    w = _small(H=2, d=4)
+    rng = np.random.default_rng(21)
+    t, y, x = np.meshgrid(np.arange(w.T), np.arange(w.Hg), np.arange(w.W), indexing="ij")
+    n = (4.0 + np.sin(0.9 * x + 0.3 * t) + 0.6 * np.cos(0.7 * y) + 0.3 * rng.random(x.shape))
+    n[:2, :4, :4] = 2.5                                  # zone 0: a constant map
+    n = n.reshape(1, -1)
+    V = rng.standard_normal((1, w.N, w.H, w.d))
+    st = orc.zone_stats_from_norms(w, V, n)
+    sid, tie = orc.assign_shapes(w, st)
+    assert np.array_equal(orc.norm_sensitive_zones(w, n, st, 0.0) | tie, tie)
+    seen_flip = False
+    for tau in (1e-4, 3e-3, 1e-2):
+        flags = orc.norm_sensitive_zones(w, n, st, tau) | tie
+        assert not flags.all()
+        for trial in range(60):
+            if trial % 3 == 0:
+                e = tau * rng.choice([-1.0, 1.0], size=n.shape)
+            else:
+                e = rng.uniform(-tau, tau, n.shape)
+            s2, _ = orc.assign_shapes(w, orc.zone_stats_from_norms(w, V, n * (1 + e)))
+            flips = s2 != sid
+            seen_flip |= bool(flips.any())
+            assert not (flips & ~flags).any(), (tau, np.nonzero(flips & ~flags))
+        if tau >= 3e-3:
+            assert flags[0, :, 0].all()                    # the constant zone
+    assert seen_flip
 
 
 # ------------------------------------------------------------ permutation ---
@@ -521,6 +617,98 @@ def test_backward_from_stored_bf16_output_differs_by_the_rounding_of_o_only():
     bound = scale * np.abs(Kp).max() * 2.0 ** -8 * (np.abs(dOp[S:2 * S]) * np.abs(o)).sum(1)
     assert np.all(np.abs(dq1 - dq0).max(1) <= bound + 1e-15)
     assert np.abs(dq1 - dq0).max() > 0
+
+
+def _bwd_case(seed=11, positive=()):
+    rng = np.random.default_rng(seed)
+    S, d, nb = 8, 4, 4
+    X = {k: rng.standard_normal((nb * S, d)) for k in ("Q", "K", "V", "dO")}
+    for k in positive:
+        X[k] = np.abs(X[k])
+    nv = np.array([S, 5, S, S])                       # query block 1 partly real
+    return X, nv, S, d, np.array([0, 1, 3]), 1 / math.sqrt(d)
+
+
+def _dq_dk_at(X, nv, S, sel, scale, o_given, i=1):
+    dq, dk, _ = orc.attn_bwd_row(X["Q"], X["K"], X["V"], X["dO"], nv, i, sel, S, scale,
+                                 o_given=o_given)
+    return dq, dk
+
+
+def test_bound_terms_are_the_worst_case_over_bf16_output_errors_brute_force():
+    """abs_terms: the per-element sizes by which dq and dk move when the O
+    that D is formed from carries bf16 forward errors (|dO_ic| <= u (|O_ic| +
+    (P|V|)_ic)).  Brute force over perturbations of O: every one of the 2^d
+    extreme sign patterns of a query row, and random interior ones, stays
+    within u * terms; the worst pattern reaches it for dq exactly, and, with
+    Q >= 0 (no cancellation over rows), for dk too."""
+    u = 2.0 ** -9
+    i = 1
+    for positive in ((), ("Q",)):
+        X, nv, S, d, sel, scale = _bwd_case(positive=positive)
+        o, _ = orc.attn_fwd_row(X["Q"], X["K"], X["V"], nv, i, sel, S, scale)
+        _, _, _, aq, ak = orc.attn_bwd_row(X["Q"], X["K"], X["V"], X["dO"], nv, i, sel, S,
+                                           scale, abs_terms=True)
+        dq0, dk0 = _dq_dk_at(X, nv, S, sel, scale, o)
+        # the allowed size of the error of each element of O
+        k = np.concatenate([X["K"][j * S:j * S + nv[j]] for j in sel])
+        v = np.concatenate([X["V"][j * S:j * S + nv[j]] for j in sel])
+        s = X["Q"][i * S:(i + 1) * S] @ k.T * scale
+        P = np.exp(s - s.max(1, keepdims=True))
+        P /= P.sum(1, keepdims=True)
+        room = u * (np.abs(o) + P @ np.abs(v))
+        worst_q = np.zeros_like(dq0)
+        for signs in itertools.product((-1.0, 1.0), repeat=d):
+            dq, dk = _dq_dk_at(X, nv, S, sel, scale, o + room * np.array(signs))
+            worst_q = np.maximum(worst_q, np.abs(dq - dq0))
+            assert np.all(np.abs(dq - dq0) <= u * aq * (1 + 1e-9) + 1e-300)
+            assert np.all(np.abs(dk - dk0) <= u * ak * (1 + 1e-9) + 1e-300)
+        rng = np.random.default_rng(2)
+        for _ in range(50):
+            dq, dk = _dq_dk_at(X, nv, S, sel, scale, o + room * rng.uniform(-1, 1, o.shape))
+            assert np.all(np.abs(dq - dq0) <= u * aq * (1 + 1e-9) + 1e-300)
+            assert np.all(np.abs(dk - dk0) <= u * ak * (1 + 1e-9) + 1e-300)
+        np.testing.assert_allclose(worst_q, u * aq, rtol=1e-9, atol=1e-300)
+        assert np.all(aq[nv[i]:] == 0) and aq[:nv[i]].min() > 0
+        if positive:
+            # every D_i moved up by u b_i at once (signs of dO): dk's terms align
+            dq, dk = _dq_dk_at(X, nv, S, sel, scale, o + room * np.sign(X["dO"][i * S:(i + 1) * S]))
+            np.testing.assert_allclose(np.abs(dk - dk0), u * ak, rtol=1e-9, atol=1e-300)
+
+
+def test_bound_terms_vanish_without_upstream_gradient():
+    """A query row with zero upstream gradient has nothing to move: its dq
+    sizes are zero, and a query block whose dO is zero throughout adds nothing
+    to the dk sizes."""
+    X, nv, S, d, sel, scale = _bwd_case(seed=4)
+    X["dO"][1 * S:1 * S + 2] = 0.0
+    _, _, _, aq, ak = orc.attn_bwd_row(X["Q"], X["K"], X["V"], X["dO"], nv, 1, sel, S, scale,
+                                       abs_terms=True)
+    assert np.all(aq[:2] == 0)
+    # dk collects over the rows of the query block: a block whose dO is all
+    # zero contributes nothing
+    X["dO"][1 * S:2 * S] = 0.0
+    _, _, _, aq0, ak0 = orc.attn_bwd_row(X["Q"], X["K"], X["V"], X["dO"], nv, 1, sel, S, scale,
+                                         abs_terms=True)
+    assert np.all(aq0 == 0) and np.all(ak0 == 0)
+
+
+def test_key_block_gradients_equal_the_full_backward():
+    """attn_bwd_key_blocks is attn_bwd restricted to some key blocks."""
+    w = _small(H=1, d=6, Ca=6, topp=0.6, topk_floor=2)
+    x = _tiny_inputs(w, seed=5)
+    r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"], dO=x["dO"])
+    S, L = w.block, r["lists"][(0, 0)]
+    for o_bf16 in (False, True):
+        _, dK, dV = orc.attn_bwd(w, r["Qp"], r["Kp"], r["Vp"], r["dOp"], r["n_valid"], r["lists"],
+                                 r["scale"], o_bf16=o_bf16)
+        kb = [j for j in range(len(L)) if r["n_valid"][0, 0, j] > 0][::3]
+        got = orc.attn_bwd_key_blocks(r["Qp"][0, 0], r["Kp"][0, 0], r["Vp"][0, 0], r["dOp"][0, 0],
+                                      r["n_valid"][0, 0], L, kb, S, r["scale"], o_bf16=o_bf16)
+        for j in kb:
+            np.testing.assert_allclose(got[j][0], dK[0, 0, j * S:(j + 1) * S], atol=1e-13)
+            np.testing.assert_allclose(got[j][1], dV[0, 0, j * S:(j + 1) * S], atol=1e-13)
+        assert max(np.abs(got[j][0]).max() for j in kb) > 0
 
 
 # ------------------------------------------------- library and structure ----
