@@ -36,17 +36,36 @@ import torch  # noqa: E402
 from content_adaptive_block_02_b300 import build, prism, synth  # noqa: E402
 
 METRIC = "sparse-attn fwd+bwd ms & effective TFLOP/s at 2K grid; % of bf16 tensor peak"
-FWD_PAIR_FLOP = 4 * 128 * 128 * 128          # S = QK^T and O = PV per 128x128 pair
-BWD_PAIR_FLOP = 10 * 128 * 128 * 128         # S, dP, dV, dK, dQ
-DKDV_PAIR_FLOP = 8 * 128 * 128 * 128         # the dK/dV kernel: S^T, dP^T, dV, dK
-DQ_PAIR_FLOP = 6 * 128 * 128 * 128           # the dQ kernel: S, dP (recomputed), dQ
 KERNELS_PER_STEP = 22
+
+
+def pair_flops(w):
+    """Flops per selected (query block, key block) pair of S-token blocks:
+    forward 4 S^2 d, backward 10 S^2 d (algorithmic), and what the dK/dV
+    (8 S^2 d) and dQ (6 S^2 d, S and dP recomputed) kernels compute."""
+    u = w.block * w.block * w.d
+    return {"fwd": 4 * u, "bwd": 10 * u, "attn_fwd": 4 * u, "attn_dkdv": 8 * u, "attn_dq": 6 * u}
 # DRAM bytes (read + written) per launch of the attention kernels on the 2K-like
-# workload, from one ncu capture of these kernel versions (dram__bytes_read.sum +
-# dram__bytes_write.sum, 1 pass; profiles/dram_traffic_2k_attention.md).  Only
-# reported for that workload; to be refreshed whenever the kernels change.
-TRAFFIC_2K = {"attn_fwd_tc_kernel": 12.50e9 + 8.07e9, "attn_dkdv_tc_kernel": 26.09e9 + 19.80e9,
-              "attn_dq_tc_kernel": 20.80e9 + 7.74e9}
+# workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum,
+# 1 pass) of the kernel sources whose SHA-256 prefix is given; reported only for
+# that workload, and as null once the kernel's source file has changed since.
+TRAFFIC_2K = {
+    "attn_fwd_tc_kernel": ("attn_tc.cu", None, 12.50e9 + 8.07e9),
+    "attn_dkdv_tc_kernel": ("attn_tc_dkdv.cu", None, 26.09e9 + 19.80e9),
+    "attn_dq_tc_kernel": ("attn_tc_dq.cu", None, 20.80e9 + 7.74e9),
+}
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` if its source is still the captured one."""
+    ent = TRAFFIC_2K.get(kernel)
+    if ent is None or ent[1] is None:
+        return None
+    import hashlib
+    path = os.path.join(ROOT, "content_adaptive_block_02_b300", "csrc", ent[0])
+    with open(path, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return ent[2] if sha == ent[1] else None
 
 
 def peaks():
@@ -143,6 +162,172 @@ def sum_over_ranks(x: float, device) -> float:
 
 # ----------------------------------------------------------------- ours ----
 
+CALLS = ("a2v_norms", "zone_stats", "assign_permute", "block_select", "attn_fwd_call",
+         "unpermute_O", "permute_dO", "attn_bwd_call", "unpermute_dQ", "unpermute_dK",
+         "unpermute_dV")
+
+
+def call_bytes(w, plan, fused: bool):
+    """Algorithmic HBM bytes of the memory-bound calls: every tensor read or
+    written once at its stored size (a [B, N, H, d] bf16 tensor is
+    B*N*H*d*2 bytes; block-order tensors hold Np rows, padding included)."""
+    B, N, H, d, Np, nb = w.B, w.N, w.H, w.d, plan.Np, plan.nb
+    tok = B * N * H * d * 2                 # one model-side bf16 tensor
+    ptok = B * H * Np * d * 2               # one block-order bf16 tensor
+    out = {
+        "zone_stats": tok + (B * N * 4 if fused else B * N * w.Ca * 2),
+        "assign_permute": 3 * tok + 3 * ptok + 4 * B * H * nb * d * 4 + B * H * (Np + N) * 4
+                          + B * H * nb * 4,
+        "permute_dO": tok + ptok + B * H * Np * 4,
+        "unpermute_O": 2 * tok + B * H * N * 4,
+        "bwd_pre": 2 * ptok + B * H * Np * 4 * 3,
+    }
+    for k in ("unpermute_dQ", "unpermute_dK", "unpermute_dV"):
+        out[k] = out["unpermute_O"]
+    if fused:
+        out["a2v_norms"] = B * N * w.Ca * 2 + B * N * 4
+    return out
+
+
+class Runner:
+    """One Prism attention layer (forward + backward) on the device through
+    the C ABI, with optional CUDA events around every call."""
+
+    def __init__(self, w, dev, key_chunk_blocks=0, fused=True, x=None):
+        self.w, self.dev, self.fused = w, dev, fused
+        self.x = synth.generate(w, dev) if x is None else x
+        self.att = prism.PrismAttention(w, dev, key_chunk_blocks=key_chunk_blocks)
+        self.stream = torch.cuda.current_stream()
+        self.nrm = torch.empty(w.B, w.N, dtype=torch.float32, device=dev)
+
+    def step(self, ev=None, trace=None, xin=None):
+        att, p, st = self.att, self.att.plan, self.stream
+        xi = self.x if xin is None else xin
+        if trace is not None:
+            p.set_trace_events(trace)
+
+        def mark(k):
+            if ev is not None:
+                ev[k].record(st)
+        o = att.perm_out
+        mark(0)
+        if self.fused:
+            p.a2v_norms(xi["qa"], xi["audio"], xi["audio"], att.ws, self.nrm)
+            mark(1)
+            p.zone_stats_norms(xi["V"], self.nrm, att.stats)
+        else:
+            mark(1)
+            p.zone_stats(xi["V"], xi["a2v"], att.stats)
+        mark(2)
+        p.assign_and_permute(att.stats, xi["Q"], xi["K"], xi["V"], o)
+        mark(3)
+        p.block_select(o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"], o["n_valid"], att.ws,
+                       att.lists)
+        mark(4)
+        p.sparse_attn_fwd(o["Qp"], o["Kp"], o["Vp"], o["n_valid"], att.lists["row_ptr"],
+                          att.lists["col_idx"], att.scale, att.ws, att.Op, att.lse)
+        mark(5)
+        p.unpermute(o["inv"], att.Op, att.O)
+        mark(6)
+        p.permute(o["perm"], xi["dO"], att.dOp)
+        mark(7)
+        p.sparse_attn_bwd(o["Qp"], o["Kp"], o["Vp"], att.Op, att.dOp, att.lse, o["n_valid"],
+                          att.lists, att.scale, att.ws, att.dQp, att.dKp, att.dVp)
+        mark(8)
+        p.unpermute(o["inv"], att.dQp, att.dQ)
+        mark(9)
+        p.unpermute(o["inv"], att.dKp, att.dK)
+        mark(10)
+        p.unpermute(o["inv"], att.dVp, att.dV)
+        mark(11)
+
+    def selection_summary(self):
+        att, w = self.att, self.w
+        nb = att.plan.nb
+        rp = att.lists["row_ptr"]
+        pairs = int(rp[-1].item())
+        counts = (rp[1:] - rp[:-1]).long()
+        nv = att.perm_out["n_valid"].reshape(-1).long()
+        rows = torch.repeat_interleave(torch.arange(counts.numel(), device=rp.device), counts)
+        cols = att.lists["col_idx"][:pairs].long()
+        # token pairs actually attended (real query rows x real key rows)
+        tok_pairs = int((nv[rows] * nv[(rows // nb) * nb + cols]).sum().item())
+        lens = counts[nv > 0].cpu().numpy()
+        sid = att.perm_out["shape_id"].reshape(-1).cpu().numpy().astype(np.int64)
+        hist = np.bincount(sid, minlength=len(w.menu))
+        return dict(
+            pairs=pairs, tok_pairs=tok_pairs,
+            lengths={"min": int(lens.min()), "p50": int(np.median(lens)),
+                     "p99": int(np.percentile(lens, 99)), "max": int(lens.max()),
+                     "mean": round(float(lens.mean()), 1)},
+            shapes={"x".join(str(e) for e in w.menu[k]): int(hist[k])
+                    for k in range(len(w.menu)) if hist[k] > 0},
+            ties={"zone_shapes": int(att.perm_out["shape_tie"].sum().item()),
+                  "selection_rows": int(att.lists["sel_tie"].sum().item())},
+            amb=int(att.ws[4:8].view(torch.int32).item()))
+
+    def measure(self, steps, warmup, barrier=lambda: None, clock_dev=None):
+        """W untimed steps, then K steps between events; per-call and
+        per-kernel times from events recorded on the launching stream."""
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        st = self.att.status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} after warm-up")
+        calls = [[ev() for _ in range(len(CALLS) + 1)] for _ in range(steps)]
+        # per-kernel marks recorded by the library around each attention
+        # kernel; every event is recorded once here so that its handle exists
+        traces = [{s: (ev(), ev()) for s in prism.Plan.TRACE_SLOTS} for _ in range(steps)]
+        for tr in traces:
+            for pair in tr.values():
+                for e in pair:
+                    e.record(self.stream)
+        barrier()
+        torch.cuda.synchronize()
+        t0, t1 = ev(), ev()
+        clk = Clocks(clock_dev) if clock_dev is not None else None
+        if clk is not None:
+            clk.__enter__()
+        t0.record(self.stream)
+        for k in range(steps):
+            self.step(calls[k], traces[k])
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        if clk is not None:
+            clk.__exit__(None, None, None)
+        self.att.plan.set_trace_events(None)
+        mean = lambda f: statistics.mean(f(k) for k in range(steps))
+        call_ms = {c: mean(lambda k, i=i: calls[k][i].elapsed_time(calls[k][i + 1]))
+                   for i, c in enumerate(CALLS)}
+        kern_ms = {s: mean(lambda k, s=s: traces[k][s][0].elapsed_time(traces[k][s][1]))
+                   for s in prism.Plan.TRACE_SLOTS}
+        return dict(ms=t0.elapsed_time(t1) / steps, call_ms=call_ms, kern_ms=kern_ms,
+                    clocks=clk.summary() if clk is not None else None,
+                    status=self.att.status())
+
+
+def hbm_summary(w, plan, fused, call_ms, kern_ms, pk):
+    """GB/s of the memory-bound calls from their algorithmic bytes."""
+    by = call_bytes(w, plan, fused)
+    t = dict(call_ms)
+    t["bwd_pre"] = kern_ms["bwd_pre"]
+    out = {}
+    for k, b in by.items():
+        ms = t[k]
+        if ms > 0:
+            gbs = b / (ms * 1e-3) / 1e9
+            out[k] = {"ms": round(ms, 3), "bytes": b, "gbs": round(gbs, 1),
+                      "frac": round(gbs / pk["hbm"], 3)}
+    return out
+
+
+def workload_desc(w):
+    return (f"{w.name}: {w.T}x{w.Hg}x{w.W} grid, {w.H} heads, d={w.d}, zones {w.zone}, "
+            f"{w.block}-token blocks, top-k {w.topk_floor}, top-p {w.topp}")
+
+
 def run_ours(args, w):
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -150,98 +335,33 @@ def run_ours(args, w):
     if ws > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     build.build()
+    fused = not args.a2v_input
     wr = replica_workload(w, rank)     # an independent problem per replica
-    x = synth.generate(wr, dev)
-    att = prism.PrismAttention(wr, dev, key_chunk_blocks=args.key_chunk_blocks)
-    stream = torch.cuda.current_stream()
+    R = Runner(wr, dev, args.key_chunk_blocks, fused)
+    att, stream = R.att, R.stream
     ev = lambda: torch.cuda.Event(enable_timing=True)
-
-    def step(tk=None, trace=None, xin=None):
-        xi = x if xin is None else xin
-        if trace is not None:
-            att.plan.set_trace_events(trace)
-        att.plan.zone_stats(xi["V"], xi["a2v"], att.stats)
-        att.plan.assign_and_permute(att.stats, xi["Q"], xi["K"], xi["V"], att.perm_out)
-        o = att.perm_out
-        att.plan.block_select(o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"], o["n_valid"],
-                              att.ws, att.lists)
-        if tk is not None:
-            tk[0].record(stream)
-        att.plan.sparse_attn_fwd(o["Qp"], o["Kp"], o["Vp"], o["n_valid"], att.lists["row_ptr"],
-                                 att.lists["col_idx"], att.scale, att.ws, att.Op, att.lse)
-        if tk is not None:
-            tk[1].record(stream)
-        att.plan.unpermute(o["inv"], att.Op, att.O)
-        att.plan.permute(o["perm"], xi["dO"], att.dOp)
-        if tk is not None:
-            tk[2].record(stream)
-        att.plan.sparse_attn_bwd(o["Qp"], o["Kp"], o["Vp"], att.Op, att.dOp, att.lse, o["n_valid"],
-                                 att.lists, att.scale, att.ws, att.dQp, att.dKp, att.dVp)
-        if tk is not None:
-            tk[3].record(stream)
-        att.plan.unpermute(o["inv"], att.dQp, att.dQ)
-        att.plan.unpermute(o["inv"], att.dKp, att.dK)
-        att.plan.unpermute(o["inv"], att.dVp, att.dV)
-
+    barrier = (lambda: torch.distributed.barrier()) if ws > 1 else (lambda: None)
     for _ in range(args.warmup):
-        step()
+        R.step()
     torch.cuda.synchronize()
-    st = att.status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} after warm-up")
-    pairs = int(att.lists["row_ptr"][-1].item())
-    # load balance: selected key blocks per query block (real query blocks)
-    rp = att.lists["row_ptr"].cpu().numpy().astype(np.int64)
-    lens = np.diff(rp)
-    real = att.perm_out["n_valid"].reshape(-1).cpu().numpy() > 0
-    lens = lens[real]
-    list_lengths = {"min": int(lens.min()), "p50": int(np.median(lens)),
-                    "p99": int(np.percentile(lens, 99)), "max": int(lens.max()),
-                    "mean": round(float(lens.mean()), 1)}
-    # shapes chosen per (b, h, zone) (cf. Table 11) and the near ties of both decisions
-    sid = att.perm_out["shape_id"].reshape(-1).cpu().numpy().astype(np.int64)
-    counts = np.bincount(sid, minlength=len(wr.menu))
-    shape_hist = {"x".join(str(e) for e in wr.menu[k]): int(counts[k])
-                  for k in range(len(wr.menu)) if counts[k] > 0}
-    zone_ties = int(att.perm_out["shape_tie"].sum().item())
-    sel_ties = int(att.lists["sel_tie"].sum().item())
-    amb = int(att.ws[4:8].view(torch.int32).item())
-    flop = pairs * (FWD_PAIR_FLOP + BWD_PAIR_FLOP)
-
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    marks = [[ev() for _ in range(4)] for _ in range(args.steps)]
-    # per-kernel marks recorded by the library around each attention kernel;
-    # every event is recorded once here so that its CUDA handle exists
-    traces = [{s: (ev(), ev()) for s in prism.Plan.TRACE_SLOTS} for _ in range(args.steps)]
-    for tr in traces:
-        for pair in tr.values():
-            for e in pair:
-                e.record(stream)
-    torch.cuda.synchronize()
-    t0, t1 = ev(), ev()
-    with Clocks(local) as clk:
-        t0.record(stream)
-        for k in range(args.steps):
-            step(marks[k], traces[k])
-        t1.record(stream)
-        torch.cuda.synchronize()
-    att.plan.set_trace_events(None)
-    ms = t0.elapsed_time(t1) / args.steps
-    fwd_ms = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
-    bwd_ms = statistics.mean(m[2].elapsed_time(m[3]) for m in marks)
-    kern_ms = {s: statistics.mean(tr[s][0].elapsed_time(tr[s][1]) for tr in traces)
-               for s in prism.Plan.TRACE_SLOTS}
-    ms = max_over_ranks(ms, dev)
+    sel = R.selection_summary()
+    pairs = sel["pairs"]
+    PF = pair_flops(wr)
+    flop = pairs * (PF["fwd"] + PF["bwd"])
+    real_flop = sel["tok_pairs"] * 14 * wr.d           # 4 d forward + 10 d backward per token pair
+    m = R.measure(args.steps, 0, barrier, clock_dev=local)
+    ms = max_over_ranks(m["ms"], dev)
     flop_all = sum_over_ranks(flop, dev)
-    st = att.status()
+    real_all = sum_over_ranks(real_flop, dev)
+    kern_ms, call_ms = m["kern_ms"], m["call_ms"]
+    fwd_ms, bwd_ms = call_ms["attn_fwd_call"], call_ms["attn_bwd_call"]
 
     # ---- end to end through host buffers (pinned): every step's inputs are
     # copied host -> device and its outputs device -> host inside the timed
     # region, pipelined over two device buffer sets on two copy streams, so
     # the copies of one step overlap the compute of its neighbours ----
-    names_in = ["Q", "K", "V", "a2v", "dO"]
+    x = R.x
+    names_in = ["Q", "K", "V", "dO"] + (["qa", "audio"] if fused else ["a2v"])
     names_out = ("O", "dQ", "dK", "dV")
     host_in = {k: x[k].cpu().pin_memory() for k in names_in}
     host_out = {k: torch.empty(x["Q"].shape, dtype=torch.bfloat16).pin_memory()
@@ -255,8 +375,7 @@ def run_ours(args, w):
     comp_done = [torch.cuda.Event() for _ in range(2)]
     out_free = [torch.cuda.Event() for _ in range(2)]
     e_steps = max(1, args.steps)
-    if ws > 1:
-        torch.distributed.barrier()
+    barrier()
     torch.cuda.synchronize()
     e0, e1 = ev(), ev()
     e0.record(stream)
@@ -273,7 +392,7 @@ def run_ours(args, w):
         stream.wait_event(in_ready[b])
         if k >= 2:
             stream.wait_event(out_free[b])  # step k-2's outputs have left buffer b
-        step(xin=xb[b])
+        R.step(xin=xb[b])
         for n, src in zip(names_out, (att.O, att.dQ, att.dK, att.dV)):
             ob[b][n].copy_(src, non_blocking=True)
         comp_done[b].record(stream)
@@ -289,9 +408,8 @@ def run_ours(args, w):
     e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
 
     pk = peaks()
-    bwd_achieved = pairs * BWD_PAIR_FLOP / (bwd_ms * 1e-3) / 1e12
-    fwd_achieved = pairs * FWD_PAIR_FLOP / (fwd_ms * 1e-3) / 1e12
-    kern_flop = {"attn_fwd": FWD_PAIR_FLOP, "attn_dkdv": DKDV_PAIR_FLOP, "attn_dq": DQ_PAIR_FLOP}
+    clk_sum = m["clocks"]
+    kern_flop = {k: PF[k] for k in ("attn_fwd", "attn_dkdv", "attn_dq")}
     kern_tf = {s: round(pairs * f / (kern_ms[s] * 1e-3) / 1e12, 1) for s, f in kern_flop.items()}
     dom = max(kern_flop, key=lambda s: kern_ms[s])     # the longest attention kernel
     dom_name = {"attn_fwd": "attn_fwd_tc_kernel", "attn_dkdv": "attn_dkdv_tc_kernel",
@@ -309,73 +427,161 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.T}x{w.Hg}x{w.W} grid, {w.H} heads, d={w.d}, "
-                               f"zones {w.zone}, {w.block}-token blocks, top-k {w.topk_floor}, "
-                               f"top-p {w.topp}",
+        "real_token_tflops": round(real_all / (ms * 1e-3) / 1e12, 2),
+        "config": {"workload": workload_desc(w),
                    "global_batch": w.B * ws, "tokens": w.N, "parallelism": f"replicas x{ws}",
+                   "a2v": ("norms computed on the device from the A2V queries and the "
+                           f"{w.Na} audio tokens" if fused else "A2V output given"),
                    "l2": "inputs larger than L2 (no flush needed)",
                    "selected_pairs": pairs,
-                   "block_density": round(pairs / (w.B * w.H * w.n_blocks ** 2), 4),
-                   "rows_decided_exactly": amb,
-                   "selected_per_query_block": list_lengths,
-                   "shapes_chosen": shape_hist,
-                   "near_ties": {"zone_shapes": zone_ties, "selection_rows": sel_ties},
+                   "real_token_pairs": sel["tok_pairs"],
+                   "block_density": round(pairs / (w.B * w.H * att.plan.nb ** 2), 4),
+                   "rows_decided_exactly": sel["amb"],
+                   "selected_per_query_block": sel["lengths"],
+                   "shapes_chosen": sel["shapes"],
+                   "near_ties": sel["ties"],
                    "key_ranges": att.plan.sz.key_chunks},
         "attn_ms": {"fwd": round(fwd_ms, 3), "bwd": round(bwd_ms, 3),
                     "other": round(ms - fwd_ms - bwd_ms, 3)},
-        "attn_tflops": {"fwd": round(fwd_achieved, 1), "bwd": round(bwd_achieved, 1)},
-        "dense_equiv_tflops": round(w.B * w.H * (w.n_blocks ** 2) *
-                                    (FWD_PAIR_FLOP + BWD_PAIR_FLOP) / (ms * 1e-3) / 1e12 * ws, 1),
+        "attn_tflops": {"fwd": round(pairs * PF["fwd"] / (fwd_ms * 1e-3) / 1e12, 1),
+                        "bwd": round(pairs * PF["bwd"] / (bwd_ms * 1e-3) / 1e12, 1)},
+        "dense_equiv_tflops": round(w.B * w.H * (att.plan.nb ** 2) *
+                                    (PF["fwd"] + PF["bwd"]) / (ms * 1e-3) / 1e12 * ws, 1),
+        "call_ms": {c: round(v, 3) for c, v in call_ms.items()},
         "kernel_ms": {s: round(v, 3) for s, v in kern_ms.items()},
         "kernel_tflops": kern_tf,
+        "hbm_kernels": hbm_summary(wr, att.plan, fused, call_ms, kern_ms, pk),
         "roofline": {"bound": "tensor",
                      "kernel": f"{dom_name} (library-recorded events around the launch)",
-                     "achieved": kern_tf[dom], "peak": pk["bf16_sus"],
-                     "peak_kind": f"bf16 sustained ({pk['src']})", "unit": "TFLOP/s",
-                     "frac": round(kern_tf[dom] / pk["bf16_sus"], 4),
-                     "frac_burst": round(kern_tf[dom] / pk["bf16"], 4),
+                     "achieved": kern_tf[dom], "peak": pk["bf16"],
+                     "peak_kind": f"bf16 dense burst ({pk['src']})", "unit": "TFLOP/s",
+                     "frac": round(kern_tf[dom] / pk["bf16"], 4),
+                     "frac_sustained": round(kern_tf[dom] / pk["bf16_sus"], 4),
+                     # the burst peak scaled to the SM clock sampled in the timed
+                     # region (the burst GEMM taken to run at the maximum clock)
+                     "frac_at_run_clock": (round(kern_tf[dom] / (pk["bf16"] * clk_sum["sm_mhz"] /
+                                                                 clk_sum["sm_max_mhz"]), 4)
+                                           if clk_sum.get("sm_mhz") else None),
                      "flop_per_launch": pairs * kern_flop[dom],
-                     "traffic": (TRAFFIC_2K.get(dom_name)
+                     "traffic": (measured_traffic(dom_name)
                                  if w.name == "2k" and args.key_chunk_blocks == 0 else None)},
         "e2e": {"value": round(flop_all / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
                 "copies": "pinned host buffers, two device buffer sets, copy streams "
                           "overlapped with the neighbouring steps' compute"},
-        "gpu_launches": (KERNELS_PER_STEP + (4 if att.plan.sz.key_chunks > 1 else 0)) * args.steps,
-        "clocks": clk.summary(),
-        "device_status": st,
+        "gpu_launches": (KERNELS_PER_STEP + (1 if fused else 0) +
+                         (4 if att.plan.sz.key_chunks > 1 else 0)) * args.steps,
+        "clocks": clk_sum,
+        "device_status": m["status"],
     }
+    del xb, ob, host_in, host_out
+    if rank == 0 and ws == 1 and not args.no_dense:
+        line["dense"] = dense_run(wr, dev, args, R.x, fused)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, x)
+        line["cpu_baseline"] = cpu_baseline(w, R.x, fused)
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return line if rank == 0 else None
 
 
+def dense_run(w, dev, args, x, fused, steps=2, warmup=1):
+    """The same kernels with every valid key block selected (Top-p = 1), on
+    the same inputs: the dense-attention reference timed next to the sparse
+    step (fewer steps: a dense 2K step is several seconds)."""
+    wd = w.with_(topp=1.0, name=w.name + "-dense")
+    R = Runner(wd, dev, args.key_chunk_blocks, fused, x=x)
+    for _ in range(warmup):
+        R.step()
+    torch.cuda.synchronize()
+    pairs = int(R.att.lists["row_ptr"][-1].item())
+    m = R.measure(steps, 0)
+    out = {"steps": steps, "warmup": warmup, "ms_per_step": round(m["ms"], 1),
+           "selected_pairs": pairs,
+           "value": round(pairs * (pair_flops(w)["fwd"] + pair_flops(w)["bwd"]) /
+                          (m["ms"] * 1e-3) / 1e12, 1),
+           "unit": "TFLOP/s",
+           "kernel_ms": {s: round(v, 2) for s, v in m["kern_ms"].items()},
+           "device_status": m["status"]}
+    del R
+    torch.cuda.empty_cache()
+    return out
+
+
+def sweep(args):
+    """One line per workload of the measurement plan: the 720p, 1080p and 2K
+    grids, the 41-frame grid, and the 2K stress inputs (white field, one
+    dominant source, skewed noise) at Top-p 0.5 / 0.9 / 0.99."""
+    cases = [synth.WORKLOADS[n] for n in ("720p", "1080p", "2k", "2k_long")]
+    for v in ("white", "onesrc", "skew"):
+        for p in (0.5, 0.9, 0.99):
+            cases.append(synth.stress("2k", v, p))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    pk = peaks()
+    for w in cases:
+        # the one-source stress input scales the A2V output itself: it runs
+        # with the A2V output given
+        fused = not args.a2v_input and w.src_mass is None
+        R = Runner(w, dev, args.key_chunk_blocks, fused)
+        for _ in range(args.warmup):
+            R.step()
+        torch.cuda.synchronize()
+        sel = R.selection_summary()
+        m = R.measure(args.steps, 0, clock_dev=0)
+        pairs = sel["pairs"]
+        PF = pair_flops(w)
+        kern_tf = {s: round(pairs * PF[s] / (m["kern_ms"][s] * 1e-3) / 1e12, 1)
+                   for s in ("attn_fwd", "attn_dkdv", "attn_dq")}
+        print(json.dumps({
+            "workload": workload_desc(w), "a2v_on_device": fused, "ms_per_step": round(m["ms"], 2),
+            "value": round(pairs * (PF["fwd"] + PF["bwd"]) / (m["ms"] * 1e-3) / 1e12, 1),
+            "unit": "TFLOP/s", "real_token_tflops":
+                round(sel["tok_pairs"] * 14 * w.d / (m["ms"] * 1e-3) / 1e12, 1),
+            "block_density": round(pairs / (w.B * w.H * R.att.plan.nb ** 2), 4),
+            "selected_per_query_block": sel["lengths"], "near_ties": sel["ties"],
+            "kernel_tflops": kern_tf, "frac_burst_dkdv": round(kern_tf["attn_dkdv"] / pk["bf16"], 3),
+            "hbm_kernels": {k: v["gbs"] for k, v in
+                            hbm_summary(w, R.att.plan, fused, m["call_ms"], m["kern_ms"], pk).items()},
+            "key_ranges": R.att.plan.sz.key_chunks, "clocks": m["clocks"],
+            "device_status": m["status"]}), flush=True)
+        del R
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------ oracle leg ----
+# The oracle is timed as it stands, one process per head with one BLAS thread
+# each (every head is independent through every step), started with `spawn`
+# (never forked from a process that holds a CUDA context).
 
-def _threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info()]
-        return max(n) if n else 1
-    except Exception:
-        return os.cpu_count() or 1
+_ONE_THREAD = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
 
 
-def oracle_sample(w, inputs_f64, rows_sample=8, head=0):
-    """Time the fp64 oracle on one head (statistics, shapes, permutation,
-    pooling, selection) and on `rows_sample` query blocks of attention
-    forward + backward; extrapolate to the whole workload.  Returns
-    (seconds for the whole workload, pair flop of the whole workload,
-    description)."""
+def _bits(t):
+    """bf16 tensor -> its uint16 bit patterns as a numpy array (exact)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _oracle_head(job):
+    """One head of the oracle (runs in a spawned worker): steps 1-4 in full,
+    attention forward + backward on `rows` sampled query blocks.  Returns
+    (seconds of steps 1-4, selected pairs of the head, pairs sampled,
+    seconds of the sampled attention)."""
+    shared, own, w, rows_sample, fused, seed = job
     from oracle import prism_oracle as orc
-    X = inputs_f64
+    f = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    S_, O_ = np.load(shared), np.load(own)
+    X = {k: f(O_[k]) for k in O_.files}
+    A = {k: f(S_[k]) for k in S_.files}
     w1 = w.with_(H=1)
     t0 = time.perf_counter()
-    st = orc.zone_stats(w1, X["V"], X["a2v"])
+    if fused:
+        n = orc.a2v_norms(A["qa"], A["audio"], A["audio"])
+        st = orc.zone_stats_from_norms(w1, X["V"], n)
+    else:
+        st = orc.zone_stats(w1, X["V"], A["a2v"])
     sid, _ = orc.assign_shapes(w1, st)
     perm, inv, nval = orc.build_permutation(w1, sid)
     Qp, Kp, Vp = orc.permute(X["Q"], perm), orc.permute(X["K"], perm), orc.permute(X["V"], perm)
@@ -383,8 +589,8 @@ def oracle_sample(w, inputs_f64, rows_sample=8, head=0):
     lists, _ = orc.select_blocks(w1, Qb, Kb, nval)
     t1 = time.perf_counter()
     L = lists[(0, 0)]
-    pairs_head = sum(len(s) for s in L if s is not None)
-    rng = np.random.default_rng(0)
+    pairs = sum(len(s) for s in L if s is not None)
+    rng = np.random.default_rng(seed)
     cand = [i for i in range(len(L)) if L[i] is not None and len(L[i]) > 0]
     rows = rng.choice(cand, size=min(rows_sample, len(cand)), replace=False)
     dOp = orc.permute(X["dO"], perm)
@@ -396,29 +602,82 @@ def oracle_sample(w, inputs_f64, rows_sample=8, head=0):
         orc.attn_bwd_row(Qp[0, 0], Kp[0, 0], Vp[0, 0], dOp[0, 0], nval[0, 0], int(i), L[i],
                          w.block, scale)
         sp += len(L[i])
-    t3 = time.perf_counter()
-    per_pair = (t3 - t2) / max(sp, 1)
-    pairs_all = pairs_head * w.H * w.B
-    total = (t1 - t0) * w.H * w.B + per_pair * pairs_all
-    desc = (f"oracle on head {head}: steps 1-4 timed in full ({t1 - t0:.1f} s, x{w.H * w.B} heads); "
-            f"attention fwd+bwd timed on {len(rows)} query blocks ({sp} pairs, {t3 - t2:.1f} s), "
-            f"extrapolated per pair to the oracle's {pairs_all} pairs")
-    return total, pairs_all * (FWD_PAIR_FLOP + BWD_PAIR_FLOP), desc, (t3 - t0)
+    return t1 - t0, pairs, sp, time.perf_counter() - t2
 
 
-def _head_inputs(x, head=0):
-    f = lambda t: t.detach().float().cpu().numpy().astype(np.float64)
-    return {"Q": f(x["Q"][:, :, head:head + 1]), "K": f(x["K"][:, :, head:head + 1]),
-            "V": f(x["V"][:, :, head:head + 1]), "dO": f(x["dO"][:, :, head:head + 1]),
-            "a2v": f(x["a2v"])}
+class OracleSampler:
+    """The oracle on the host cores: P = min(heads, cores) heads at once,
+    one spawned process (one thread) per head."""
+
+    def __init__(self, w, x, fused):
+        import multiprocessing as mp
+        import tempfile
+        self.w, self.fused = w, fused
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (
+            os.cpu_count() or 1)
+        self.P = max(1, min(w.H * w.B, self.cores))
+        self.dir = tempfile.mkdtemp(prefix="prism_oracle_")
+        self.shared = os.path.join(self.dir, "shared.npz")
+        if fused:
+            np.savez(self.shared, qa=_bits(x["qa"]), audio=_bits(x["audio"]))
+        else:
+            np.savez(self.shared, a2v=_bits(x["a2v"]))
+        self.own = []
+        for h in range(self.P):
+            path = os.path.join(self.dir, f"head{h}.npz")
+            np.savez(path, **{k: _bits(x[k][:, :, h:h + 1]) for k in ("Q", "K", "V", "dO")})
+            self.own.append(path)
+        saved = {k: os.environ.get(k) for k in _ONE_THREAD}
+        os.environ.update(_ONE_THREAD)
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.P)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def sample(self, rows_sample, seed=0):
+        """Seconds the oracle needs for one whole step of the workload,
+        extrapolated from one wave of P heads; and the description."""
+        w = self.w
+        jobs = [(self.shared, self.own[h], w, rows_sample, self.fused, seed + h)
+                for h in range(self.P)]
+        t0 = time.perf_counter()
+        res = self.pool.map(_oracle_head, jobs)
+        wall = time.perf_counter() - t0
+        t14 = max(r[0] for r in res)
+        per_pair = sum(r[3] for r in res) / max(1, sum(r[2] for r in res))
+        pairs_head = statistics.mean(r[1] for r in res)
+        heads = w.H * w.B
+        waves = -(-heads // self.P)
+        pairs_all = pairs_head * heads
+        total = waves * t14 + per_pair * pairs_all / self.P
+        desc = (f"oracle, one process and thread per head, {self.P} heads at once on "
+                f"{self.cores} host cores: steps 1-4 timed in full on {self.P} heads (slowest "
+                f"{t14:.1f} s, {waves} wave(s) for {heads} heads); attention fwd+bwd timed on "
+                f"{rows_sample} query block(s) per head ({sum(r[2] for r in res)} pairs, "
+                f"{per_pair * 1e3:.2f} ms per pair per thread), extrapolated to "
+                f"{pairs_all:.0f} pairs over {self.P} threads")
+        return total, pairs_all * 14 * w.block * w.block * w.d, desc, wall
+
+    def close(self):
+        import shutil
+        self.pool.close()
+        self.pool.join()
+        shutil.rmtree(self.dir, ignore_errors=True)
 
 
-def cpu_baseline(w, x):
-    X = _head_inputs(x)
-    total, flop, desc, spent = oracle_sample(w, X)
-    return {"value": round(flop / total / 1e12, 6), "unit": "TFLOP/s", "cores": _threads(),
-            "kind": "oracle", "sample": desc, "seconds_spent": round(spent, 1),
-            "extrapolated_s_per_step": round(total, 1)}
+def cpu_baseline(w, x, fused, rows_sample=3):
+    smp = OracleSampler(w, x, fused)
+    try:
+        total, flop, desc, wall = smp.sample(rows_sample)
+    finally:
+        smp.close()
+    return {"value": round(flop / total / 1e12, 6), "unit": "TFLOP/s", "cores": smp.P,
+            "host_cores": smp.cores, "kind": "oracle", "sample": desc,
+            "seconds_spent": round(wall, 1), "extrapolated_s_per_step": round(total, 1)}
 
 
 def run_reference(args, w):
@@ -429,25 +688,30 @@ def run_reference(args, w):
     # device when there is one, then held in host memory for the oracle
     gen = "cuda" if torch.cuda.is_available() else "cpu"
     x = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in synth.generate(w, gen).items()}
-    X = _head_inputs(x)
-    for _ in range(args.warmup):
-        oracle_sample(w, X, rows_sample=2)
-    vals, descs, spent = [], [], 0.0
-    for _ in range(args.steps):
-        total, flop, desc, s = oracle_sample(w, X, rows_sample=2)
-        vals.append(total)
-        descs.append(desc)
-        spent += s
+    fused = not args.a2v_input
+    smp = OracleSampler(w, x, fused)
+    try:
+        for k in range(args.warmup):
+            smp.sample(1, seed=1000 * (k + 1))
+        vals, descs, spent = [], [], 0.0
+        for k in range(args.steps):
+            total, flop, desc, wall = smp.sample(1, seed=k)
+            vals.append(total)
+            descs.append(desc)
+            spent += wall
+    finally:
+        smp.close()
     total = statistics.mean(vals)
     v = flop / total / 1e12
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total * 1e3, 1), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{w.name}: {w.T}x{w.Hg}x{w.W} grid, {w.H} heads, d={w.d}",
-                       "global_batch": w.B, "tokens": w.N},
-            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": _threads(),
-                             "kind": "oracle", "sample": descs[-1]},
+            "config": {"workload": workload_desc(w), "global_batch": w.B, "tokens": w.N,
+                       "a2v": ("norms computed from the A2V queries and the audio tokens"
+                               if fused else "A2V output given")},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": smp.P,
+                             "host_cores": smp.cores, "kind": "oracle", "sample": descs[-1]},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "seconds_spent": round(spent, 1)}
@@ -467,12 +731,23 @@ def main():
                     help="key / query range size of the attention kernels (0: automatic)")
     ap.add_argument("--stress", choices=["white", "onesrc", "skew"], default=None,
                     help="stress inputs: white field / one dominant audio source / skewed noise")
+    ap.add_argument("--a2v-input", action="store_true",
+                    help="take the A2V output as an input instead of computing its norms")
+    ap.add_argument("--no-dense", action="store_true",
+                    help="skip the all-blocks dense run timed next to the sparse step")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one line per workload of the measurement plan (not the contract line)")
     args = ap.parse_args()
+    if args.sweep:
+        sweep(args)
+        return
     w = synth.WORKLOADS[args.workload]
     if args.stress is not None:
         w = synth.stress(args.workload, args.stress, w.topp)
     if args.dense:
         w = w.with_(topp=1.0, name=w.name + "-dense")
+    if args.stress == "onesrc":
+        args.a2v_input = True   # this input scales the A2V output itself
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)

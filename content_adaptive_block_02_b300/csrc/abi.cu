@@ -239,7 +239,31 @@ int prism_zone_stats(const prism_plan_t* plan, const uint16_t* V, const uint16_t
   PRISM_CHECK_PTR(V);
   PRISM_CHECK_PTR(a2v);
   PRISM_CHECK_PTR(stats);
-  PRISM_CUDA(prism::launch_zone_stats(plan->p, V, a2v, stats, static_cast<cudaStream_t>(stream)));
+  PRISM_CUDA(prism::launch_zone_stats(plan->p, V, a2v, nullptr, stats,
+                                      static_cast<cudaStream_t>(stream)));
+  return PRISM_OK;
+}
+
+int prism_a2v_norms(const prism_plan_t* plan, const uint16_t* Qa, const uint16_t* Ka,
+                    const uint16_t* Va, int Na, float* n, void* ws, void* stream) {
+  if (plan == nullptr || Na < 1) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(Qa); PRISM_CHECK_PTR(Ka); PRISM_CHECK_PTR(Va);
+  PRISM_CHECK_PTR(n); PRISM_CHECK_PTR(ws);
+  const prism_config_t& c = plan->p.cfg;
+  if (c.Ca % 64 != 0 || c.Ca > 128 || Na > 256) return PRISM_ERR_UNSUPPORTED;
+  PRISM_CUDA(prism::launch_a2v_norms(plan->p, Qa, Ka, Va, Na, n, static_cast<uint8_t*>(ws),
+                                     static_cast<cudaStream_t>(stream)));
+  return PRISM_OK;
+}
+
+int prism_zone_stats_norms(const prism_plan_t* plan, const uint16_t* V, const float* n,
+                           float* stats, void* stream) {
+  if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(V);
+  PRISM_CHECK_PTR(n);
+  PRISM_CHECK_PTR(stats);
+  PRISM_CUDA(prism::launch_zone_stats(plan->p, V, nullptr, n, stats,
+                                      static_cast<cudaStream_t>(stream)));
   return PRISM_OK;
 }
 

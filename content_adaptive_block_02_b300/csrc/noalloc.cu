@@ -14,7 +14,8 @@
 // cleared at the start of each call.  Two calls whose kernels overlap on the
 // GPU (different streams, or different threads without ordering) race on the
 // array and give wrong results.  Device-side wait timeouts of this variant are
-// recorded only in the array's own status word and are not reported back.
+// recorded in the array's own status word, which prism_noalloc_device_status
+// reads back.
 #include <mutex>
 
 #include "prism_internal.cuh"
@@ -58,7 +59,9 @@ std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
 // Device address of the scratch on the current device (set up on the first
-// call on that device).
+// call on that device).  The cached address belongs to the device's primary
+// context as it was then: after cudaDeviceReset (or with another context
+// current on that device) it is no longer valid.
 cudaError_t scratch_address(uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -124,5 +127,18 @@ extern "C" int prism_sparse_attn_bwd_noalloc(
       return PRISM_ERR_CUDA;
     if (prism::launch_dq_convert(p, x, scale, dQp, st) != cudaSuccess) return PRISM_ERR_CUDA;
   }
+  return PRISM_OK;
+}
+
+extern "C" int prism_noalloc_device_status(void* stream) {
+  uint8_t* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return PRISM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, base, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PRISM_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PRISM_ERR_CUDA;
+  if (word == prism::DEV_ERR_TIMEOUT) return PRISM_ERR_DEVICE_TIMEOUT;
+  if (word != 0) return PRISM_ERR_DEVICE_BOUNDS;
   return PRISM_OK;
 }

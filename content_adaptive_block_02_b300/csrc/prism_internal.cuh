@@ -53,8 +53,12 @@ enum : uint32_t { DEV_ERR_TIMEOUT = 1, DEV_ERR_BOUNDS = 2 };
 // --------------------------------------------------------- launchers ------
 // Each returns cudaGetLastError() after enqueueing.
 
+// nrm: when not null, the A2V norms [B, N] (fp32) are read instead of a2v
 cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* a2v,
-                              float* stats, cudaStream_t st);
+                              const float* nrm, float* stats, cudaStream_t st);
+cudaError_t launch_a2v_norms(const Plan& p, const uint16_t* Qa, const uint16_t* Ka,
+                             const uint16_t* Va, int Na, float* n, uint8_t* ws, cudaStream_t st);
+size_t a2v_smem_bytes(int Ca, int Na);
 cudaError_t launch_assign(const Plan& p, const float* stats, uint8_t* shape_id,
                           uint8_t* shape_tie, cudaStream_t st);
 // status: when not null, a shape id that is not admissible is recorded there

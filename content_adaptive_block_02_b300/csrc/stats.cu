@@ -116,8 +116,8 @@ __device__ __forceinline__ float lines_variance(const uint32_t* tile, int na, in
 // norms and ~350 lines per zone.  Written to slots 3..7 of every head's
 // record.
 __device__ void audio_zone_stats(const prism_config_t& c, const ZoneGeom& g, int b, int z, int Z,
-                                 const uint16_t* __restrict__ a2v, float* __restrict__ stats,
-                                 uint8_t* smem) {
+                                 const uint16_t* __restrict__ a2v, const float* __restrict__ nrm,
+                                 float* __restrict__ stats, uint8_t* smem) {
   const int vol = g.vt * g.vy * g.vx;
   const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
   double* nmap = reinterpret_cast<double*>(smem);
@@ -125,13 +125,17 @@ __device__ void audio_zone_stats(const prism_config_t& c, const ZoneGeom& g, int
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // one token per thread: the squares of bf16 values are exact in fp32 and
   // are summed as a double-float (TwoSum), so n^2 carries ~1e-11 relative
-  // error before the fp64 square root -- far below the 1e-20 nbar^2 floor on
+  // error before the fp64 square root -- far below the 1e-10 nbar^2 floor on
   // the directional variance, at FP32 rather than FP64 throughput
   const bool vec = (c.Ca % 8) == 0;
   for (int li = threadIdx.x; li < vol; li += blockDim.x) {
     const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
     const long long n =
         (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
+    if (nrm != nullptr) {  // norms given (computed by the A2V kernel)
+      nmap[li] = static_cast<double>(nrm[static_cast<long long>(b) * N + n]);
+      continue;
+    }
     const uint16_t* row = a2v + (static_cast<long long>(b) * N + n) * c.Ca;
     float hi = 0.f, lo = 0.f;
     auto add = [&](float v) {
@@ -214,7 +218,7 @@ __device__ void audio_zone_stats(const prism_config_t& c, const ZoneGeom& g, int
 
 __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
     prism_config_t c, int nzH, int nzW, int Z, const uint16_t* __restrict__ V,
-    const uint16_t* __restrict__ a2v, float* __restrict__ stats) {
+    const uint16_t* __restrict__ a2v, const float* __restrict__ nrm, float* __restrict__ stats) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float red[32 * 4];
   const int z = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -267,7 +271,7 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
         o[a] = len[a] >= 2 ? acc[a] / (nl[a] * static_cast<float>(c.d)) : 0.f;
     }
   } else {
-    audio_zone_stats(c, g, b, z, Z, a2v, stats, smem);
+    audio_zone_stats(c, g, b, z, Z, a2v, nrm, stats, smem);
   }
 }
 
@@ -404,13 +408,13 @@ __device__ __forceinline__ void pencil_chunk(const uint32_t* __restrict__ tile, 
 
 __global__ void __launch_bounds__(kStatsThreads, 2) zone_stats_pencil_kernel(
     prism_config_t c, int nzH, int nzW, int Z, const uint16_t* __restrict__ V,
-    const uint16_t* __restrict__ a2v, float* __restrict__ stats) {
+    const uint16_t* __restrict__ a2v, const float* __restrict__ nrm, float* __restrict__ stats) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float red[32 * 4];
   const int h = blockIdx.x, z = blockIdx.y, b = blockIdx.z;
   const ZoneGeom g = zone_geom(c, nzH, nzW, z);
   if (h == c.H) {
-    audio_zone_stats(c, g, b, z, Z, a2v, stats, smem);
+    audio_zone_stats(c, g, b, z, Z, a2v, nrm, stats, smem);
     return;
   }
   const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
@@ -516,8 +520,9 @@ __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, Me
     const double ssv = sv[0] + sv[1] + sv[2];
     const double ssn = sn[0] + sn[1] + sn[2];
     // no audio direction when the norm map's variance is round-off (a
-    // constant map): at most 1e-20 nbar^2
-    const bool no_var = !(ssn > 1e-20 * nbar * nbar);
+    // constant map, or one whose spread is below what fp32 norms resolve):
+    // at most 1e-10 nbar^2
+    const bool no_var = !(ssn > 1e-10 * nbar * nbar);
     const double abar = nmax > 0.0 ? nbar / nmax : 0.0;
     const double uv = c.use_video ? 1.0 : 0.0, ua = c.use_audio ? 1.0 : 0.0;
     double lg[3];
@@ -556,7 +561,7 @@ __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, Me
 }  // namespace
 
 cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* a2v,
-                              float* stats, cudaStream_t st) {
+                              const float* nrm, float* stats, cudaStream_t st) {
   const prism_config_t& c = p.cfg;
   const int vol = c.zT * c.zH * c.zW;
   const size_t smem_video = 2ull * vol * kChunk * 2;
@@ -571,7 +576,7 @@ cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* 
                                          static_cast<int>(sm));
     if (e != cudaSuccess) return e;
     zone_stats_pencil_kernel<<<dim3(c.H + 1, p.sz.Z, c.B), kStatsThreads, sm, st>>>(
-        c, p.sz.nzH, p.sz.nzW, p.sz.Z, V, a2v, stats);
+        c, p.sz.nzH, p.sz.nzW, p.sz.Z, V, a2v, nrm, stats);
     return cudaGetLastError();
   }
   cudaError_t e = cudaFuncSetAttribute(zone_stats_kernel,
@@ -580,7 +585,7 @@ cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* 
   if (e != cudaSuccess) return e;
   dim3 grid(p.sz.Z, c.H + 1, c.B);
   zone_stats_kernel<<<grid, kStatsThreads, smem, st>>>(c, p.sz.nzH, p.sz.nzW, p.sz.Z, V, a2v,
-                                                      stats);
+                                                      nrm, stats);
   return cudaGetLastError();
 }
 

@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
         "prism_unpermute": [P, P, P, P, P],
         "prism_plan_set_trace_events": [P, P],
         "prism_permute_shapes": [P] * 17,
+        "prism_a2v_norms": [P, P, P, P, ctypes.c_int, P, P, P],
+        "prism_zone_stats_norms": [P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -244,6 +246,26 @@ class Plan:
                "prism_zone_stats")
         return stats
 
+    def a2v_norms(self, Qa, Ka, Va, ws, n=None):
+        """prism_a2v_norms: per-token norms [B, N] (fp32) of the A2V
+        cross-attention output, from the queries Qa [B, N, Ca] and the audio
+        keys / values Ka, Va [B, Na, Ca] (bf16)."""
+        w = self.w
+        if n is None:
+            n = torch.empty(w.B, w.N, dtype=torch.float32, device=Qa.device)
+        _check(lib().prism_a2v_norms(self.h, _ptr(Qa), _ptr(Ka), _ptr(Va), int(Ka.shape[1]),
+                                     _ptr(n), _ptr(ws), _stream()), "prism_a2v_norms")
+        return n
+
+    def zone_stats_norms(self, V, n, stats=None):
+        """prism_zone_stats_norms: zone statistics from the A2V norms n [B, N]."""
+        w = self.w
+        if stats is None:
+            stats = torch.empty(w.B, w.H, self.Z, 8, dtype=torch.float32, device=V.device)
+        _check(lib().prism_zone_stats_norms(self.h, _ptr(V), _ptr(n), _ptr(stats), _stream()),
+               "prism_zone_stats_norms")
+        return stats
+
     def alloc_permuted(self, device):
         w = self.w
         e = dict(device=device)
@@ -370,13 +392,21 @@ class PrismAttention:
         self.dQp, self.dKp, self.dVp = (torch.empty_like(self.Op) for _ in range(3))
         self.dQ, self.dK, self.dV = (torch.empty_like(self.O) for _ in range(3))
 
-    def forward(self, Q, K, V, a2v, shape_id=None):
-        """``shape_id`` ([B, H, Z] uint8, optional): block shapes given by the
-        caller (fixed / random baselines) instead of the zone statistics and
-        Eq. 7; ``a2v`` is then unused."""
+    def forward(self, Q, K, V, a2v=None, shape_id=None, qa=None, audio=None):
+        """The A2V signal is either the cross-attention output ``a2v``
+        [B, N, Ca], or its queries ``qa`` [B, N, Ca] and the audio tokens
+        ``audio`` [B, Na, Ca] (keys and values), from which the norms are
+        computed on the device (prism_a2v_norms).  ``shape_id`` ([B, H, Z]
+        uint8, optional): block shapes given by the caller (fixed / random
+        baselines) instead of the zone statistics and Eq. 7; the A2V signal is
+        then unused."""
         p, o = self.plan, self.perm_out
         if shape_id is None:
-            p.zone_stats(V, a2v, self.stats)
+            if qa is not None:
+                self.nrm = p.a2v_norms(qa, audio, audio, self.ws, getattr(self, "nrm", None))
+                p.zone_stats_norms(V, self.nrm, self.stats)
+            else:
+                p.zone_stats(V, a2v, self.stats)
             p.assign_and_permute(self.stats, Q, K, V, o)
         else:
             p.permute_shapes(shape_id, Q, K, V, self.ws, o)

@@ -169,6 +169,29 @@ int prism_plan_set_trace_events(prism_plan_t* plan, void* const* events);
 int prism_zone_stats(const prism_plan_t* plan, const uint16_t* V, const uint16_t* a2v,
                      float* stats, void* stream);
 
+/* Step 1a -- the per-token norms of the audio-to-video (A2V) cross-attention
+ * output, computed on the device (Prism Abstract: the zone signals use
+ * "feature norms from the audio-to-video cross-attention").  Reading: one
+ * attention head, softmax over the audio tokens, scale 1/sqrt(Ca):
+ *   n_i = || softmax(Qa_i Ka^T / sqrt(Ca)) Va ||_2
+ *   Qa  [B, N, Ca] bf16  the video tokens' cross-attention queries
+ *   Ka  [B, Na, Ca] bf16 the audio tokens' keys
+ *   Va  [B, Na, Ca] bf16 the audio tokens' values (may alias Ka); |Va| < 65504
+ *   Na  audio tokens per batch entry, 1..256
+ *   n   [B, N] fp32 out
+ *   ws  workspace (status word: bounded waits, a value out of range)
+ * Tensor cores (tcgen05) for Qa Ka^T and for P Va, with P split into two
+ * fp16 terms; n carries a relative error of about 1e-6 (fp32 logits).
+ * Errors: PRISM_ERR_UNSUPPORTED unless Ca is 64 or 128 and Na <= 256. */
+int prism_a2v_norms(const prism_plan_t* plan, const uint16_t* Qa, const uint16_t* Ka,
+                    const uint16_t* Va, int Na, float* n, void* ws, void* stream);
+
+/* Step 1 with the A2V norms given (as prism_a2v_norms writes them) instead of
+ * the A2V output: the same statistics as prism_zone_stats, with n [B, N] fp32
+ * in place of ||a2v||. */
+int prism_zone_stats_norms(const prism_plan_t* plan, const uint16_t* V, const float* n,
+                           float* stats, void* stream);
+
 /* Step 2 -- block shape per zone (Eq. 7 quantisation, Table 10 caption) and
  * the token permutation into zone / block order, fused with block pooling.
  *   stats      [B, H, Z, 8] fp32 in
@@ -262,22 +285,33 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
  * memory when they run it (for example code confined to a memory pool it does
  * not own, or a runtime that forbids cudaMalloc / cudaFree after start-up).
  * The paper has no counterpart: this is a library convenience.  Arguments and
- * results are those of prism_sparse_attn_bwd minus ws; the scratch (rowsum D
- * and LSE * log2 e, 8*B*H*Np bytes plus 512, on the tensor-core path; D and the
- * fp32 dQ accumulator, 4*B*H*Np*(d+1) bytes plus 512, on the CUDA-core path)
- * lives in a 32 MiB array inside the library, held on every GPU that loads
- * the library until the process exits.  Larger problems return
+ * results are those of prism_sparse_attn_bwd minus ws.  The scratch lives in a
+ * 32 MiB array inside the library, held on every GPU that loads the library
+ * until the process exits.  With R = B*H*Np, the call needs
+ *   256 + round_up(4*R, 256) + 4*R*X  <=  32 MiB   (33554432 bytes),
+ * X = 1 on the tensor-core path (rowsum D, then LSE * log2 e) and X = d on the
+ * CUDA-core path (D, then the fp32 dQ accumulator); larger problems return
  * PRISM_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
- * device looks the array's address up (make that first call before any stream
- * capture).  All calls share the array: calls whose kernels overlap on the GPU
- * race and give wrong results.  Device-side wait timeouts are not reported by
- * this variant. */
+ * device looks the array's address up and keeps it: make that first call
+ * before any stream capture, and do not use the entry point across a
+ * cudaDeviceReset of that device (the kept address belongs to the context
+ * that was current at the first call).  All calls share the array: calls
+ * whose kernels overlap on the GPU race and give wrong results.  Device-side
+ * wait timeouts go to the array's status word, cleared at the start of each
+ * call; read it with prism_noalloc_device_status. */
 int prism_sparse_attn_bwd_noalloc(const prism_plan_t* plan, const uint16_t* Qp,
                                   const uint16_t* Kp, const uint16_t* Vp, const uint16_t* Op,
                                   const uint16_t* dOp, const float* lse, const int32_t* n_valid,
                                   const int32_t* row_ptr, const int32_t* col_idx,
                                   const int32_t* col_ptr, const int32_t* row_idx, float scale,
                                   uint16_t* dQp, uint16_t* dKp, uint16_t* dVp, void* stream);
+
+/* Status word of the workspace-free backward's scratch on the current device:
+ * waits for `stream`, then returns PRISM_OK or the first device error of the
+ * last prism_sparse_attn_bwd_noalloc call on this device
+ * (PRISM_ERR_DEVICE_TIMEOUT / PRISM_ERR_DEVICE_BOUNDS).  The paper has no
+ * counterpart.  Allocates nothing. */
+int prism_noalloc_device_status(void* stream);
 
 /* Inverse permutation: X[b,n,h] = Xp[b,h,inv[n]].  Xp [B, H, Np, d] bf16 ->
  * X [B, N, H, d] bf16. */

@@ -28,23 +28,42 @@ from oracle import prism_oracle as orc
 
 O_TOL = 2e-2
 G_TOL = 5e-2
+# bf16 unit roundoff 2^-9, twice: the forward rounds P before the P V product
+# and O when it stores it (u |O| + u P|V|, the oracle's bound terms), and a
+# forward that walks the keys in ranges also rounds each range's partial O
+# (another u P|V|)
+TERMS_U = 2.0 ** -8
+# relative tolerance of dQ and dK on inputs whose softmax rows are nearly
+# one-hot (grad_scale "terms"): there dQ and dK cancel to about 1e-6 of their
+# ingredients, and the forward's bf16 roundings of P and O, carried through
+# D = rowsum(dO * O), leave them with errors of several percent (8 % measured
+# for dK, 4 % for dQ on the white-field stress input)
+ILL_COND_TOL = 0.15
+# relative error allowed on the A2V norms the device computes (fp32 logits
+# and softmax, P V with P in two fp16 terms)
+TAU_N = 4e-6
 
 
 def f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(w, inputs, attn_kernel=0, shape_id=None, key_chunk_blocks=0):
+def run_gpu(w, inputs, attn_kernel=0, shape_id=None, key_chunk_blocks=0, fused_a2v=False):
     dev = torch.device("cuda")
-    x = {k: inputs[k].to(dev) for k in ("Q", "K", "V", "a2v", "dO")}
+    x = {k: inputs[k].to(dev) for k in ("Q", "K", "V", "a2v", "dO", "qa", "audio")}
     att = prism.PrismAttention(w, dev, attn_kernel=attn_kernel, key_chunk_blocks=key_chunk_blocks)
     sid = None if shape_id is None else torch.as_tensor(shape_id, dtype=torch.uint8).to(dev)
-    O = att.forward(x["Q"], x["K"], x["V"], x["a2v"], shape_id=sid)
+    if fused_a2v:
+        O = att.forward(x["Q"], x["K"], x["V"], qa=x["qa"], audio=x["audio"], shape_id=sid)
+    else:
+        O = att.forward(x["Q"], x["K"], x["V"], x["a2v"], shape_id=sid)
     dQ, dK, dV = att.backward(x["dO"])
     torch.cuda.synchronize()
     assert att.status() == 0, "device status word set"
     g = {k: v.cpu() for k, v in att.perm_out.items()}
     g.update({k: v.cpu() for k, v in att.lists.items()})
+    if fused_a2v:
+        g["nrm"] = att.nrm.cpu()
     g.update(stats=att.stats.cpu(), Op=att.Op.cpu(), lse=att.lse.cpu(), O=O.cpu(),
              dQ=dQ.cpu(), dK=dK.cpu(), dV=dV.cpu(), dQp=att.dQp.cpu(), dKp=att.dKp.cpu(),
              dVp=att.dVp.cpu(), dOp=att.dOp.cpu())
@@ -72,17 +91,25 @@ def rel_err(a, b):
 
 
 def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=None,
-            attn_kernel=0, shape_id=None, key_chunk_blocks=0, grad_scale="result"):
+            attn_kernel=0, shape_id=None, key_chunk_blocks=0, grad_scale="result",
+            fused_a2v=False):
     """Run both sides on the seeded inputs of `w`; assert the contract.
     heads / rows / key_blocks restrict the oracle's attention work (a sample
     of the (b, h), query blocks and key blocks).  shape_id ([B, H, Z] ints):
     block shapes given to both sides instead of the statistics and Eq. 7.
-    grad_scale "terms" adds to the dQ / dK tolerance the error that a 2^-7
-    relative error in D = rowsum(dO * O) carries into them (two bf16
-    roundings of O: the forward's and the stored value's), for inputs whose
-    softmax rows are nearly one-hot, where dQ and dK cancel to that size."""
+    grad_scale "terms" (inputs whose softmax rows are nearly one-hot, where
+    dQ and dK cancel to the size of the forward's bf16 roundings): dQ and dK
+    within ILL_COND_TOL relative, and element by element within G_TOL *
+    max|ref| plus what those roundings can move the element by through
+    D = rowsum(dO * O) (the oracle's bound terms times TERMS_U; the largest
+    ratio of error to allowance is reported as <name>_bound_use).
+    fused_a2v: the device computes the A2V norms from the cross-attention
+    queries and the audio tokens (prism_a2v_norms) instead of taking the A2V
+    output; the norms are held to TAU_N relative, the audio statistics to
+    what TAU_N can move them by, and a shape may differ from the oracle's on
+    zones whose decision that error can reach (orc.norm_sensitive_zones)."""
     inputs = synth.generate(w, "cpu")
-    att, g = run_gpu(w, inputs, attn_kernel, shape_id, key_chunk_blocks)
+    att, g = run_gpu(w, inputs, attn_kernel, shape_id, key_chunk_blocks, fused_a2v)
     rep_ = {} if report is None else report
     rep_["key_chunks"] = att.plan.sz.key_chunks
     nb = att.plan.nb
@@ -99,14 +126,26 @@ def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=No
 
     # ---- step 1: zone statistics ----
     Vs = X["V"][:, :, hs, :]
-    st_o = orc.zone_stats(w_h, Vs, X["a2v"])
+    if fused_a2v:
+        n_o = orc.a2v_norms(f64(inputs["qa"]), f64(inputs["audio"]), f64(inputs["audio"]))
+        n_g = f64(g["nrm"])
+        rep["a2v_norm_max_rel"] = float((np.abs(n_g - n_o) / n_o).max())
+        assert rep["a2v_norm_max_rel"] <= TAU_N, rep["a2v_norm_max_rel"]
+        st_o = orc.zone_stats_from_norms(w_h, Vs, n_o)
+        slack = audio_stats_slack(w, n_o, TAU_N)
+    else:
+        st_o = orc.zone_stats(w_h, Vs, X["a2v"])
+        slack = None
     st_g = f64(g["stats"])[:, hs]
     for k in range(8):
         scale = max(1e-30, np.abs(st_o[..., k]).max())
-        err = np.abs(st_g[..., k] - st_o[..., k]).max() / scale
-        assert err <= 2e-5, (k, err)
+        err = np.abs(st_g[..., k] - st_o[..., k])
+        if slack is not None and 3 <= k <= 6:
+            err = np.maximum(err - slack[:, None, :, k - 3], 0.0)
+        assert err.max() / scale <= 2e-5, (k, err.max() / scale)
     if not w.per_head:
-        st_o = orc.zone_stats(w, X["V"], X["a2v"])
+        st_o = (orc.zone_stats_from_norms(w, X["V"], n_o) if fused_a2v else
+                orc.zone_stats(w, X["V"], X["a2v"]))
 
     # ---- step 2: shapes, permutation, pooling ----
     if w.per_head:
@@ -115,12 +154,33 @@ def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=No
         sid_o, tie_o = orc.assign_shapes(w, st_o)
         sid_o, tie_o = sid_o[:, hs], tie_o[:, hs]
     sid_g = g["shape_id"].numpy().astype(np.int64)[:, hs]
+    if fused_a2v:
+        sens = orc.norm_sensitive_zones(w, n_o, st_o, TAU_N)
+        if not w.per_head:                   # st_o holds every head here
+            sens = sens[:, hs]
+        tie_o = tie_o | sens
+        rep["zones_norm_sensitive"] = int(sens.sum())
     mism = sid_g != sid_o
     assert not (mism & ~tie_o).any(), "shape id differs on a zone that is not a near tie"
     rep["shape_ties_taken"] = int(mism.sum())
     sid_use = np.where(mism, sid_g, sid_o)
     return _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd, rep,
                                 heads, grad_scale)
+
+
+def audio_stats_slack(w, n, tau):
+    """How far the audio statistics (var_n_T, var_n_H, var_n_W, nbar) of every
+    (b, zone) can move when the norms n [B, N] are off by tau relative:
+    [B, Z, 4] (the oracle's line-variance bound; tau nbar for the mean)."""
+    out = []
+    for b in range(n.shape[0]):
+        gn, m = orc._grid_views(n[b][:, None], w, 1)
+        dv = np.stack([orc.line_variance_bound(gn, m, a, tau) for a in range(3)], -1).reshape(-1, 3)
+        mf = m.astype(np.float64)
+        cnt = mf.sum(axis=(1, 3, 5))
+        nbar = np.where(cnt > 0, (gn[..., 0] * mf).sum(axis=(1, 3, 5)) / np.maximum(cnt, 1), 0.0)
+        out.append(np.concatenate([dv, tau * nbar.reshape(-1, 1)], -1))
+    return np.stack(out)
 
 
 def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd, rep,
@@ -207,15 +267,27 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
         for name, got, ref, terms in (("dQ", g["dQp"], dQ_o, aQ_o), ("dK", g["dKp"], dK_o, aK_o),
                                       ("dV", g["dVp"], dV_o, None)):
             got = f64(got)[:, hs]
-            if grad_scale == "terms" and terms is not None:
-                e = max(np.abs(got[b, hi] - ref[b, hi]).max() /
-                        (np.abs(ref[b, hi]).max() + 2.0 ** -7 * terms[b, hi].max() / G_TOL)
-                        for b in range(w.B) for hi in range(len(hs)))
-            else:
-                e = max(rel_err(got[b, hi], ref[b, hi]) for b in range(w.B)
-                        for hi in range(len(hs)))
+            e = max(rel_err(got[b, hi], ref[b, hi]) for b in range(w.B)
+                    for hi in range(len(hs)))
             rep[name + "_max_rel"] = e
-            assert e <= G_TOL, (name, e)
+            if grad_scale == "terms" and terms is not None:
+                # (1) a guard, element by element: the contract's share of the
+                # head's largest value plus what the forward's bf16 roundings
+                # of O can move this element by through D (TERMS_U per unit of
+                # the oracle's sizes); (2) the relative error within
+                # ILL_COND_TOL, the error those roundings leave once dQ and dK
+                # have cancelled to their size
+                use = 0.0
+                for b in range(w.B):
+                    for hi in range(len(hs)):
+                        allow = G_TOL * np.abs(ref[b, hi]).max() + TERMS_U * terms[b, hi]
+                        err = np.abs(got[b, hi] - ref[b, hi])
+                        use = max(use, float((err / np.maximum(allow, 1e-300)).max()))
+                rep[name + "_bound_use"] = use
+                assert use <= 1.0, (name, use)
+                assert e <= ILL_COND_TOL, (name, e)
+            else:
+                assert e <= G_TOL, (name, e)
         if heads is None:
             for name, ref in (("dQ", dQ_o), ("dK", dK_o), ("dV", dV_o)):
                 assert rel_err(f64(g[name]), orc.unpermute(ref, inv_o)) <= G_TOL, name
@@ -254,123 +326,170 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
     return rep
 
 
-def compare_sampled(w, heads, n_rows=6, n_key_blocks=1, seed=0, report=None):
-    """Full-size check on a sample.  Inputs are generated on the device; for
-    each sampled head the oracle runs every step of that head (statistics,
-    shapes, permutation, pooling), the selection on `n_rows` sampled query
-    blocks (always including one partially real block when there is one),
-    attention forward and dQ on those rows, and dK / dV on `n_key_blocks`
-    sampled key blocks (every query block that selected them contributes).
-    Only the sampled slices are copied to the host."""
+def _head_slices(att, w, b, h, nb):
+    """What the sampled comparison reads back of one (b, h): host copies."""
+    sl = (slice(b, b + 1), slice(h, h + 1))
+    o, L = att.perm_out, att.lists
+    rp = L["row_ptr"].cpu().numpy().astype(np.int64)
+    cp = L["col_ptr"].cpu().numpy().astype(np.int64)
+    base = (b * w.H + h) * nb
+    lo_, hi_ = int(rp[base]), int(rp[base + nb])
+    ci = L["col_idx"][lo_:hi_].cpu().numpy().astype(np.int64)
+    c_lo, c_hi = int(cp[base]), int(cp[base + nb])
+    ri = L["row_idx"][c_lo:c_hi].cpu().numpy().astype(np.int64)
+    g = dict(
+        stats=f64(att.stats[sl]),
+        shape_id=o["shape_id"][sl].cpu().numpy().astype(np.int64),
+        perm=o["perm"][sl].cpu().numpy(), inv=o["inv"][sl].cpu().numpy(),
+        n_valid=o["n_valid"][sl].cpu().numpy(),
+        Qbar=f64(o["Qbar"][sl]) + f64(o["Qbar_lo"][sl]),
+        Kbar=f64(o["Kbar"][sl]) + f64(o["Kbar_lo"][sl]),
+        lists=[ci[int(rp[base + i]) - lo_:int(rp[base + i + 1]) - lo_] for i in range(nb)],
+        csc=[ri[int(cp[base + j]) - c_lo:int(cp[base + j + 1]) - c_lo] for j in range(nb)],
+        sel_tie=L["sel_tie"][sl].cpu().numpy())
+    for nm in ("Qp", "Kp", "Vp"):
+        g[nm] = f64(o[nm][sl])
+    for nm in ("Op", "lse", "dQp", "dKp", "dVp", "dOp"):
+        g[nm] = f64(getattr(att, nm)[sl])
+    for nm in ("O", "dQ"):
+        g[nm] = f64(getattr(att, nm)[b:b + 1, :, h:h + 1])
+    return g
+
+
+def compare_sampled(w, heads, n_rows=6, key_clusters=2, cluster_len=4, seed=0, report=None,
+                    key_chunk_blocks=(0,)):
+    """Full-size check on a sample, in the launch configuration bench.py
+    times.  Inputs are generated on the device.  For each sampled head the
+    oracle runs every step of that head (statistics, shapes, permutation,
+    pooling) and the selection of EVERY query block of the head; attention
+    forward and dQ run on `n_rows` sampled query blocks (always including one
+    partially real block when there is one, and the block with the longest
+    list), and dK / dV on `key_clusters` runs of `cluster_len` consecutive
+    key blocks (every query block that selected them contributes).
+
+    key_chunk_blocks: the attention kernels' range settings to run (0 =
+    automatic, as the bench; a value >= nb = one pass over each list); each
+    setting is run on the device and compared with the same oracle results,
+    and its errors are reported under rep["runs"]."""
     assert w.per_head, "sampled comparison needs per-head shapes"
     rep = {} if report is None else report
     dev = torch.device("cuda")
     x = synth.generate(w, dev)
-    att = prism.PrismAttention(w, dev)
-    att.forward(x["Q"], x["K"], x["V"], x["a2v"])
-    att.backward(x["dO"])
-    torch.cuda.synchronize()
-    assert att.status() == 0, "device status word set"
-    nb, S = att.plan.nb, w.block
+    runs = []
+    for kcb in key_chunk_blocks:
+        att = prism.PrismAttention(w, dev, key_chunk_blocks=kcb)
+        att.forward(x["Q"], x["K"], x["V"], x["a2v"])
+        att.backward(x["dO"])
+        torch.cuda.synchronize()
+        assert att.status() == 0, "device status word set"
+        nb = att.plan.nb
+        grab = {(b, h): _head_slices(att, w, b, h, nb) for b in range(w.B) for h in heads}
+        rp_all = att.lists["row_ptr"].cpu().numpy()
+        runs.append(dict(key_chunks=att.plan.sz.key_chunks, g=grab,
+                         density=float(rp_all[-1]) / (w.B * w.H * nb * nb)))
+        del att
+        torch.cuda.empty_cache()
+    S = w.block
     w1 = w.with_(H=1)
     scale = 1.0 / math.sqrt(w.d)
     rng = np.random.default_rng(seed)
     a2v = f64(x["a2v"])
-    o, L = att.perm_out, att.lists
-    rp_all = L["row_ptr"].cpu().numpy()
-    cp_all = L["col_ptr"].cpu().numpy()
-    errs = dict(O=0.0, dQ=0.0, dKV=0.0)
+    errs = [dict(key_chunks=r["key_chunks"], O=0.0, dQ=0.0, dKV=0.0, lse=0.0) for r in runs]
+    rep.update(select_rows_compared=0, select_rows_flagged=0,
+               select_rows_differing_on_near_ties=0, key_blocks_compared=0)
     for b in range(w.B):
         for h in heads:
-            sl = (slice(b, b + 1), slice(h, h + 1))
+            g0 = runs[0]["g"][(b, h)]
             X = {k: f64(x[k][b:b + 1, :, h:h + 1]) for k in ("Q", "K", "V", "dO")}
+            # the discrete steps do not depend on the attention kernels' ranges
+            for r in runs[1:]:
+                gr = r["g"][(b, h)]
+                for nm in ("shape_id", "perm", "n_valid"):
+                    assert np.array_equal(gr[nm], g0[nm]), nm
+                assert all(np.array_equal(a, c) for a, c in zip(gr["lists"], g0["lists"]))
             # ---- statistics, shapes, permutation, pooling (whole head) ----
             st_o = orc.zone_stats(w1, X["V"], a2v[b:b + 1])
-            st_g = f64(att.stats[sl])
             for k in range(8):
                 sc = max(1e-30, np.abs(st_o[..., k]).max())
-                assert np.abs(st_g[..., k] - st_o[..., k]).max() / sc <= 2e-5, ("stats", k)
+                assert np.abs(g0["stats"][..., k] - st_o[..., k]).max() / sc <= 2e-5, ("stats", k)
             sid_o, tie_o = orc.assign_shapes(w1, st_o)
-            sid_g = o["shape_id"][sl].cpu().numpy().astype(np.int64)
-            mism = sid_g != sid_o
+            mism = g0["shape_id"] != sid_o
             assert not (mism & ~tie_o).any(), "shape id differs on a zone that is not a near tie"
-            sid_use = np.where(mism, sid_g, sid_o)
+            sid_use = np.where(mism, g0["shape_id"], sid_o)
             perm_o, inv_o, nval_o = orc.build_permutation(w1, sid_use)
-            assert np.array_equal(o["perm"][sl].cpu().numpy(), perm_o)
-            assert np.array_equal(o["inv"][sl].cpu().numpy(), inv_o)
-            assert np.array_equal(o["n_valid"][sl].cpu().numpy(), nval_o)
+            assert np.array_equal(g0["perm"], perm_o)
+            assert np.array_equal(g0["inv"], inv_o)
+            assert np.array_equal(g0["n_valid"], nval_o)
+            nb = nval_o.shape[2]
             Qp_o, Kp_o = orc.permute(X["Q"], perm_o), orc.permute(X["K"], perm_o)
             Vp_o, dOp_o = orc.permute(X["V"], perm_o), orc.permute(X["dO"], perm_o)
-            for nm, ref in (("Qp", Qp_o), ("Kp", Kp_o), ("Vp", Vp_o)):
-                assert np.array_equal(f64(o[nm][sl]), ref), nm
-            assert np.array_equal(f64(att.dOp[sl]), dOp_o)
+            for nm, ref in (("Qp", Qp_o), ("Kp", Kp_o), ("Vp", Vp_o), ("dOp", dOp_o)):
+                assert np.array_equal(g0[nm], ref), nm
             Qb_o, Kb_o = orc.pool(Qp_o, nval_o, S), orc.pool(Kp_o, nval_o, S)
-            Qb_g = f64(o["Qbar"][sl]) + f64(o["Qbar_lo"][sl])
-            Kb_g = f64(o["Kbar"][sl]) + f64(o["Kbar_lo"][sl])
-            assert np.abs(Qb_g - Qb_o).max() <= 1e-11 * max(1.0, np.abs(Qb_o).max())
-            assert np.abs(Kb_g - Kb_o).max() <= 1e-11 * max(1.0, np.abs(Kb_o).max())
-            # ---- the head's CSR lists from the device ----
-            base = (b * w.H + h) * nb
-            lo_, hi_ = int(rp_all[base]), int(rp_all[base + nb])
-            ci = L["col_idx"][lo_:hi_].cpu().numpy().astype(np.int64)
-            Lg = [ci[int(rp_all[base + i]) - lo_:int(rp_all[base + i + 1]) - lo_] for i in range(nb)]
-            c_lo, c_hi = int(cp_all[base]), int(cp_all[base + nb])
-            ri = L["row_idx"][c_lo:c_hi].cpu().numpy().astype(np.int64)
-            cols = orc.csc_from_lists(Lg, nb)
-            for j in range(nb):
-                got = ri[int(cp_all[base + j]) - c_lo:int(cp_all[base + j + 1]) - c_lo]
-                assert np.array_equal(got, cols[j]), ("csc", j)
-            # ---- sampled query blocks: selection, O, LSE, dQ ----
-            realq = np.nonzero(nval_o[0, 0] > 0)[0]
-            partial = [i for i in realq if nval_o[0, 0, i] < S]
-            rows = list(rng.choice(realq, size=min(n_rows, len(realq)), replace=False))
-            if partial and not any(i in partial for i in rows):
-                rows[0] = int(rng.choice(partial))
-            rows = sorted(int(i) for i in rows)
-            Lo, Fo = orc.select_blocks(w1, Qb_o, Kb_o, nval_o, rows=rows)
-            for i in rows:
+            assert np.abs(g0["Qbar"] - Qb_o).max() <= 1e-11 * max(1.0, np.abs(Qb_o).max())
+            assert np.abs(g0["Kbar"] - Kb_o).max() <= 1e-11 * max(1.0, np.abs(Kb_o).max())
+            # ---- selection: every query block of the head ----
+            Lg = g0["lists"]
+            Lo, Fo = orc.select_blocks(w1, Qb_o, Kb_o, nval_o)
+            for i in range(nb):
+                rep["select_rows_compared"] += 1
+                rep["select_rows_flagged"] += int(Fo[(0, 0)][i])
                 if not np.array_equal(Lg[i], Lo[(0, 0)][i]):
                     assert Fo[(0, 0)][i], f"list differs on an unflagged row (b={b}, h={h}, i={i})"
+                    rep["select_rows_differing_on_near_ties"] += 1
+            cols = orc.csc_from_lists(Lg, nb)
+            for j in range(nb):
+                assert np.array_equal(g0["csc"][j], cols[j]), ("csc", j)
+            # ---- sampled query blocks: O, LSE, dQ ----
+            realq = np.nonzero(nval_o[0, 0] > 0)[0]
+            partial = [i for i in realq if nval_o[0, 0, i] < S]
+            rows = [int(i) for i in rng.choice(realq, size=min(n_rows, len(realq)), replace=False)]
+            if partial and not any(i in partial for i in rows):
+                rows[0] = int(rng.choice(partial))
+            longest = int(max(realq, key=lambda i: len(Lg[i])))
+            if longest not in rows:
+                rows[-1] = longest
+            rows = sorted(set(rows))
             Lfull = {(0, 0): Lg}
             Lrows = {(0, 0): [Lg[i] if i in rows else None for i in range(nb)]}
             Op_o, lse_o = orc.attn_fwd(w1, Qp_o, Kp_o, Vp_o, nval_o, Lrows, scale)
             dQ_o, _, _ = orc.attn_bwd(w1, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, Lfull, scale,
                                       rows_only=set(rows), o_bf16=True)
-            Op_g, lse_g, dQp_g = f64(att.Op[sl]), f64(att.lse[sl]), f64(att.dQp[sl])
-            # the contract is per tensor (per head): max |err| / max |ref|; on a
-            # sample the maxima run over the sampled rows (a smaller, stricter
-            # denominator than the whole head's)
             rr = np.concatenate([np.arange(i * S, (i + 1) * S) for i in rows])
-            eo = rel_err(Op_g[0, 0, rr], Op_o[0, 0, rr])
-            eq = rel_err(dQp_g[0, 0, rr], dQ_o[0, 0, rr])
-            assert eo <= O_TOL, ("O", b, h, eo)
-            assert eq <= G_TOL, ("dQ", b, h, eq)
-            assert np.abs(lse_g[0, 0, rr] - lse_o[0, 0, rr]).max() <= 2e-2
-            errs["O"], errs["dQ"] = max(errs["O"], eo), max(errs["dQ"], eq)
-            for i in rows:  # per-block figures, reported only
-                r = slice(i * S, (i + 1) * S)
-                rep.setdefault("dQ_worst_block_rel", 0.0)
-                rep["dQ_worst_block_rel"] = max(rep["dQ_worst_block_rel"],
-                                                rel_err(dQp_g[0, 0, r], dQ_o[0, 0, r]))
-                # model order: the unpermuted outputs carry the same rows
-                toks = perm_o[0, 0, r]
-                real = toks >= 0
-                for nm, got in (("O", Op_g), ("dQ", dQp_g)):
-                    mo = f64(getattr(att, nm)[b:b + 1, :, h:h + 1])
-                    assert np.array_equal(mo[0, toks[real], 0], got[0, 0, r][real]), nm
             # ---- sampled key blocks: dK, dV over every query block that selected them ----
             realk = [j for j in range(nb) if len(cols[j]) > 0]
-            for j in rng.choice(realk, size=min(n_key_blocks, len(realk)), replace=False):
-                j = int(j)
-                _, dK_o, dV_o = orc.attn_bwd(w1, Qp_o, Kp_o, Vp_o, dOp_o, nval_o, Lfull, scale,
-                                             rows_only=set(int(i) for i in cols[j]),
-                                             o_bf16=True)
-                r = slice(j * S, (j + 1) * S)
-                for nm, ref in (("dKp", dK_o), ("dVp", dV_o)):
-                    got = f64(getattr(att, nm)[sl])[0, 0, r]
-                    e = rel_err(got, ref[0, 0, r])  # one key block: its own maximum
-                    assert e <= G_TOL, (nm, b, h, j, e)
-                    errs["dKV"] = max(errs["dKV"], e)
-    rep.update(errs)
-    rep["block_density"] = float(rp_all[-1]) / (w.B * w.H * nb * nb)
+            kbs = []
+            for _ in range(key_clusters):
+                j0 = int(rng.integers(0, max(1, len(realk) - cluster_len + 1)))
+                kbs += [j for j in realk[j0:j0 + cluster_len] if j not in kbs]
+            kv_o = orc.attn_bwd_key_blocks(Qp_o[0, 0], Kp_o[0, 0], Vp_o[0, 0], dOp_o[0, 0],
+                                           nval_o[0, 0], Lg, kbs, S, scale, o_bf16=True)
+            rep["key_blocks_compared"] += len(kbs)
+            for r, er in zip(runs, errs):
+                gr = r["g"][(b, h)]
+                # the contract is per tensor (per head): max |err| / max |ref|; on a
+                # sample the maxima run over the sampled rows (a smaller, stricter
+                # denominator than the whole head's)
+                eo = rel_err(gr["Op"][0, 0, rr], Op_o[0, 0, rr])
+                eq = rel_err(gr["dQp"][0, 0, rr], dQ_o[0, 0, rr])
+                el = np.abs(gr["lse"][0, 0, rr] - lse_o[0, 0, rr]).max()
+                assert eo <= O_TOL, ("O", r["key_chunks"], b, h, eo)
+                assert eq <= G_TOL, ("dQ", r["key_chunks"], b, h, eq)
+                assert el <= 2e-2, ("lse", r["key_chunks"], b, h, el)
+                er["O"], er["dQ"], er["lse"] = max(er["O"], eo), max(er["dQ"], eq), max(er["lse"], el)
+                for i in rows:  # model order: the unpermuted outputs carry the same rows
+                    rs = slice(i * S, (i + 1) * S)
+                    toks = perm_o[0, 0, rs]
+                    real = toks >= 0
+                    for nm, got in (("O", gr["Op"]), ("dQ", gr["dQp"])):
+                        assert np.array_equal(gr[nm][0, toks[real], 0], got[0, 0, rs][real]), nm
+                for j in kbs:
+                    rs = slice(j * S, (j + 1) * S)
+                    for nm, ref in (("dKp", kv_o[j][0]), ("dVp", kv_o[j][1])):
+                        e = rel_err(gr[nm][0, 0, rs], ref)   # one key block: its own maximum
+                        assert e <= G_TOL, (nm, r["key_chunks"], b, h, j, e)
+                        er["dKV"] = max(er["dKV"], e)
+    rep["runs"] = errs
+    rep.update({k: errs[0][k] for k in ("O", "dQ", "dKV")})
+    rep["block_density"] = runs[0]["density"]
     return rep

@@ -17,7 +17,7 @@ def L():
 
 def test_exports_every_declared_function(L):
     names = prism.declared_functions()
-    assert len(names) == 16
+    assert len(names) == 19
     for n in names:
         assert hasattr(L, n), n
 

@@ -62,6 +62,50 @@ def test_noalloc_backward_matches_workspace_backward(w, kcb):
             assert pu.rel_err(pu.f64(g), pu.f64(r)) <= pu.G_TOL
 
 
+def _status_fn():
+    fn = prism.lib().prism_noalloc_device_status
+    fn.argtypes = [P]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def test_noalloc_reports_a_device_timeout_and_recovers():
+    """A bounded wait that runs out inside the workspace-free backward is
+    read back by prism_noalloc_device_status; the next call clears it.  The
+    failure is made without a fault: a plan with PRISM_FAULT_STARVE_LOADS
+    (producer warps issue no loads) and a short wait bound."""
+    fn, status = _fn(), _status_fn()
+    dev = torch.device("cuda")
+    w = _small128()
+    x = synth.generate(w, dev)
+    good = prism.PrismAttention(w, dev)
+    good.forward(x["Q"], x["K"], x["V"], x["a2v"])
+    good.backward(x["dO"])
+    torch.cuda.synchronize()
+    want = [t.clone() for t in (good.dQp, good.dKp, good.dVp)]
+    bad = prism.Plan(w, timeout_cycles=2_000_000, fault_inject=prism.FAULT_STARVE_LOADS)
+    o, ptr = good.perm_out, prism._ptr
+
+    def call(plan):
+        got = [torch.zeros_like(t) for t in want]
+        rc = fn(plan.h, ptr(o["Qp"]), ptr(o["Kp"]), ptr(o["Vp"]), ptr(good.Op), ptr(good.dOp),
+                ptr(good.lse), ptr(o["n_valid"]), ptr(good.lists["row_ptr"]),
+                ptr(good.lists["col_idx"]), ptr(good.lists["col_ptr"]),
+                ptr(good.lists["row_idx"]), good.scale, ptr(got[0]), ptr(got[1]), ptr(got[2]),
+                prism._stream())
+        assert rc == 0
+        return got, status(prism._stream())
+
+    _, st = call(good.plan)
+    assert st == prism.PRISM_OK
+    _, st = call(bad)
+    assert st == prism.PRISM_ERR_DEVICE_TIMEOUT
+    got, st = call(good.plan)
+    assert st == prism.PRISM_OK
+    for g, r in zip(got, want):
+        assert pu.rel_err(pu.f64(g), pu.f64(r)) <= pu.G_TOL
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     fn = _fn()
     plan = prism.Plan(synth.WORKLOADS["2k"])
