@@ -73,6 +73,9 @@ class Workload:
     per_head: bool = True
     use_video: bool = True
     use_audio: bool = True
+    # block-size class thresholds, descending, one per boundary between the
+    # menu's token-count classes (empty for a single-class menu)
+    class_tau: Tuple[float, ...] = ()
 
     @property
     def N(self) -> int:
@@ -101,6 +104,12 @@ class Workload:
 
 MENU_TINY = ((1, 4, 4), (2, 2, 4), (2, 4, 2), (1, 2, 8), (1, 8, 2))
 MENU_128 = ((1, 8, 16), (1, 16, 8), (2, 8, 8), (4, 4, 8), (4, 8, 4), (2, 4, 16), (2, 16, 4))
+# 256-token class: Table 11's 488 and the other power-of-two shapes that fit a
+# 16 x 16 frame patch
+MENU_256 = ((4, 8, 8), (2, 8, 16), (2, 16, 8), (4, 4, 16), (4, 16, 4), (1, 16, 16))
+# threshold between the 128- and 256-token classes (zone complexity; about
+# half the zones of the smooth-field grids fall below it)
+TAU_256 = 0.9
 
 # Block-mean field gain: chosen once so that the 720p-like grid at Top-p 0.9,
 # Top-k floor 8 lands in the 85-90 % block-sparsity band (88.6 % measured on
@@ -124,6 +133,13 @@ WORKLOADS = {
                         block=128, menu=MENU_128, Na=200, Ca=128, topk_floor=8, topp=0.9,
                         n_src=3, gamma=GAMMA, seed_base=4),
 }
+# Mixed block-size classes (Table 11: C_128 and C_256 in one head, thresholds
+# tau): the 2K grid with 128- and 256-token blocks; 3 x 16 x 16 zones admit
+# (1,8,16), (1,16,8) and (1,16,16), 4 x 16 x 16 zones every shape of both menus.
+WORKLOADS["2k_mc"] = WORKLOADS["2k"].with_(name="2k_mc", menu=MENU_128 + MENU_256,
+                                           class_tau=(TAU_256,))
+WORKLOADS["2k_mc4"] = WORKLOADS["2k"].with_(name="2k_mc4", zone=(4, 16, 16),
+                                            menu=MENU_128 + MENU_256, class_tau=(TAU_256,))
 
 
 def stress(base: str, variant: str, topp: float) -> Workload:

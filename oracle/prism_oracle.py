@@ -201,50 +201,104 @@ def guidance(w, st: np.ndarray, nbar_max: float) -> np.ndarray:
     return uv * r + ua * abar * vh + w.eps
 
 
-def shape_costs(w, g: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+def menu_classes(menu: Sequence[Sequence[int]]) -> List[int]:
+    """The block-size classes of a menu: its distinct token counts bT bH bW,
+    ascending (Prism, Table 11: classes C_64, C_128, C_256 by token count)."""
+    return sorted(set(int(b[0] * b[1] * b[2]) for b in menu))
+
+
+def class_admissible(w, S: int) -> List[int]:
+    """Admissible menu shapes of the class of S tokens."""
+    return [k for k in admissible_shapes(w.menu, w.zone)
+            if w.menu[k][0] * w.menu[k][1] * w.menu[k][2] == S]
+
+
+def shape_costs(w, g: np.ndarray, S: int = None) -> Tuple[np.ndarray, np.ndarray]:
     """Eq. 7 (Prism, Table 10 caption: b*_d is proportional to g_d^-alpha).
 
-    READING: with the token count fixed at S = bT bH bW, the continuous optimum
-    is log2 b*_d = log2(S)/3 + alpha (mean_d log2 g_d - log2 g_d).  Each
-    admissible menu shape is scored by sum_d (log2 b_d - log2 b*_d)^2.
-    Returns (costs over the admissible shapes, their menu indices)."""
-    S = w.block
+    READING: with the token count fixed at S = bT bH bW (the zone's class;
+    the workload's block size for a single-class menu), the continuous
+    optimum is log2 b*_d = log2(S)/3 + alpha (mean_d log2 g_d - log2 g_d).
+    Each admissible menu shape of that class is scored by
+    sum_d (log2 b_d - log2 b*_d)^2.
+    Returns (costs over those shapes, their menu indices)."""
+    S = w.block if S is None else S
     lg = np.log2(g)
     lstar = math.log2(S) / 3.0 + w.alpha * (lg.mean() - lg)
-    idx = admissible_shapes(w.menu, w.zone)
+    idx = class_admissible(w, S)
     costs = np.array([sum((math.log2(w.menu[k][dd]) - lstar[dd]) ** 2 for dd in range(3))
                       for k in idx], dtype=f64)
     return costs, np.array(idx)
 
 
 SHAPE_TIE = 1e-4
+CLASS_TIE = 1e-5
+
+
+def zone_complexity(w, st_h: np.ndarray) -> np.ndarray:
+    """Per-zone complexity c_z that picks the block-size class, for one
+    (b, h): st_h [Z, 8] statistics rows.
+
+    READING (Table 10 caption: thresholds tau_128 / tau_256 assign a block
+    size class; Abstract: fine blocks where the content varies fast and
+    couples strongly to the audio; the pages print no formula):
+      c_z = u_v V_z / mean_z' V_z' + u_a a_bar_z,
+    with V_z = sum_d var_v_d(z) (0 / 0 -> 0) and a_bar_z the audio gate."""
+    V = st_h[:, 0:3].sum(axis=1)
+    Vm = V.mean()
+    nmax = st_h[:, 6].max()
+    uv = 1.0 if w.use_video else 0.0
+    ua = 1.0 if w.use_audio else 0.0
+    rel = V / Vm if Vm > 0 else np.zeros_like(V)
+    abar = st_h[:, 6] / nmax if nmax > 0 else np.zeros_like(V)
+    return uv * rel + ua * abar
+
+
+def zone_class(c: float, taus: Sequence[float]) -> int:
+    """Class index (into menu_classes, ascending block size) of a zone of
+    complexity c: the number of thresholds c is below, taus descending
+    (tau_128 > tau_256: c >= tau_128 -> C_64, tau_256 <= c < tau_128 ->
+    C_128, c < tau_256 -> C_256)."""
+    return sum(1 for t in taus if c < t)
 
 
 def assign_shapes(w, stats: np.ndarray):
     """Shape id per (b, h, zone) -> (shape_id [B,H,Z] int, near_tie [B,H,Z] bool).
 
-    The admissible shape of least cost wins; an exact tie goes to the lowest
-    menu index.  A zone whose best and second-best costs differ by less than
-    SHAPE_TIE is flagged as a near tie (either shape is then accepted).
-    With per_head False, the video statistics are averaged over heads first and
-    every head gets the same shape (Prism, Table 10 caption ablates per-head
-    shapes)."""
+    A menu with several block-size classes first gives each zone its class
+    (``zone_complexity`` against the thresholds ``w.class_tau``); then, in
+    the class, the admissible shape of least Eq. 7 cost wins; an exact tie
+    goes to the lowest menu index.  A zone whose best and second-best costs
+    differ by less than SHAPE_TIE, or whose complexity lies within CLASS_TIE
+    (relative) of a threshold, is flagged as a near tie (either decision is
+    then accepted).  With per_head False, the video statistics are averaged
+    over heads first and every head gets the same shape (Prism, Table 10
+    caption ablates per-head shapes)."""
     B, H, Z, _ = stats.shape
-    if not admissible_shapes(w.menu, w.zone):
-        raise ValueError("no admissible shape for this zone")
+    classes = menu_classes(w.menu)
+    taus = tuple(getattr(w, "class_tau", ()) or ())
+    if len(taus) != len(classes) - 1:
+        raise ValueError("one threshold per class boundary expected")
+    for S in classes:
+        if not class_admissible(w, S):
+            raise ValueError("no admissible shape for this zone")
     sid = np.zeros((B, H, Z), dtype=np.int64)
     tie = np.zeros((B, H, Z), dtype=bool)
     for b in range(B):
         for h in range(H):
             st_h = stats[b, h] if w.per_head else stats[b].mean(axis=0)
             nmax = st_h[:, 6].max()
+            cz = zone_complexity(w, st_h) if taus else np.zeros(Z)
             for z in range(Z):
-                costs, idx = shape_costs(w, guidance(w, st_h[z], nmax))
+                S = classes[zone_class(cz[z], taus)]
+                costs, idx = shape_costs(w, guidance(w, st_h[z], nmax), S)
                 k = int(np.argmin(costs))            # first minimum = lowest menu index
                 sid[b, h, z] = idx[k]
                 if len(costs) > 1:
                     srt = np.sort(costs)
                     tie[b, h, z] = (srt[1] - srt[0]) < SHAPE_TIE
+                for t in taus:
+                    tie[b, h, z] |= abs(cz[z] - t) <= CLASS_TIE * max(1.0, abs(t))
     return sid, tie
 
 
@@ -274,7 +328,7 @@ def line_variance_bound(g: np.ndarray, m: np.ndarray, axis: int, tau: float) -> 
 
 
 def _shape_decision_reachable(w, st: np.ndarray, nmax: float, dvar: np.ndarray,
-                              tau: float) -> bool:
+                              tau: float, S: int = None, cz: float = 0.0) -> bool:
     """True when the shape chosen from the statistics row ``st`` could change
     if the audio statistics came from norms off by at most tau relative:
     var_n_d by at most dvar[d], nbar and the zones' max nbar by at most tau
@@ -297,6 +351,10 @@ def _shape_decision_reachable(w, st: np.ndarray, nmax: float, dvar: np.ndarray,
         return True
     abar = nbar / nmax if nmax > 0 else 0.0
     dab = abar * 2.0 * tau / (1.0 - tau)
+    # the class: the complexity moves with the gate only
+    for t in tuple(getattr(w, "class_tau", ()) or ()):
+        if abs(cz - t) <= dab + CLASS_TIE * max(1.0, abs(t)):
+            return True
     r = sv / ssv if ssv > 0 else np.full(3, 1.0 / 3.0)
     uv = 1.0 if w.use_video else 0.0
     g = uv * r + abar * vh + w.eps
@@ -305,7 +363,7 @@ def _shape_decision_reachable(w, st: np.ndarray, nmax: float, dvar: np.ndarray,
         return True
     dL = np.log2(g / (g - dg))                         # largest move of log2 g_d
     dl = abs(w.alpha) * (dL.sum() / 3.0 + dL / 3.0)    # of log2 b*_d: |mean - own|
-    costs, idx = shape_costs(w, g)
+    costs, idx = shape_costs(w, g, S)
     kb = int(np.argmin(costs))
     lb = np.array([[math.log2(e) for e in w.menu[k]] for k in idx])
     for q in range(len(idx)):
@@ -327,39 +385,52 @@ def norm_sensitive_zones(w, n: np.ndarray, stats: np.ndarray, tau: float) -> np.
     for b in range(B):
         gn, m = _grid_views(np.asarray(n[b], dtype=f64)[:, None], w, 1)
         dv = np.stack([line_variance_bound(gn, m, a, tau) for a in range(3)], -1).reshape(-1, 3)
+        classes = menu_classes(w.menu)
+        taus = tuple(getattr(w, "class_tau", ()) or ())
         for h in range(H):
             st_h = stats[b, h] if w.per_head else stats[b].mean(axis=0)
             nmax = st_h[:, 6].max()
+            cz = zone_complexity(w, st_h) if taus else np.zeros(Z)
             for z in range(Z):
-                flags[b, h, z] = _shape_decision_reachable(w, st_h[z], nmax, dv[z], tau)
+                S = classes[zone_class(cz[z], taus)]
+                flags[b, h, z] = _shape_decision_reachable(w, st_h[z], nmax, dv[z], tau, S,
+                                                           cz[z])
     return flags
 
 
-def build_permutation(w, shape_id: np.ndarray):
+def build_permutation(w, shape_id: np.ndarray, table: bool = False):
     """Token order for every (b, h): zones in raster (zt, zh, zw) order, the
     zone's blocks in raster order of its chosen shape, and inside a block its
     valid tokens first in (t, h, w) raster order, then its padding slots.
 
     READING (Prism, Abstract: tokens inside a block stay together; the pages do
-    not give an order).  Returns perm [B,H,Np] (slot -> real token, -1 for a
-    padding slot), inv [B,H,N] (token -> slot), n_valid [B,H,nb]."""
+    not give an order).  A block of S tokens fills S / w.block consecutive
+    tiles of w.block slots (one tile when the menu has a single class of
+    w.block tokens).  Returns perm [B,H,Np] (slot -> real token, -1 for a
+    padding slot), inv [B,H,N] (token -> slot), n_valid [B,H,nb] (real tokens
+    in each tile: a block's real tokens sit at its start, so they fill its
+    first tiles); with ``table`` also tiles [B,H,nb] (a block's tile count at
+    its first tile, 0 on the tiles that continue it) and n_block [B,H,nb] (a
+    block's real tokens at its first tile, 0 elsewhere)."""
     B, H, Z = shape_id.shape
     Tp, Hp, Wp = padded_grid(w.T, w.Hg, w.W, w.zone)
     zT, zH, zW = w.zone
     nzT, nzH, nzW = Tp // zT, Hp // zH, Wp // zW
-    S = w.block
+    T_ = w.block
     Np = Tp * Hp * Wp
-    nb = Np // S
+    nb = Np // T_
     perm = np.full((B, H, Np), -1, dtype=np.int64)
     inv = np.full((B, H, w.N), -1, dtype=np.int64)
     nvalid = np.zeros((B, H, nb), dtype=np.int64)
+    tiles = np.zeros((B, H, nb), dtype=np.int64)
+    nblock = np.zeros((B, H, nb), dtype=np.int64)
     for b in range(B):
         for h in range(H):
             slot = 0
-            blk = 0
             for z in range(Z):
                 zt, zh, zw = z // (nzH * nzW), (z // nzW) % nzH, z % nzW
                 bT, bH, bW = w.menu[int(shape_id[b, h, z])]
+                S = bT * bH * bW
                 for it in range(zT // bT):
                     for ih in range(zH // bH):
                         for iw in range(zW // bW):
@@ -375,10 +446,49 @@ def build_permutation(w, shape_id: np.ndarray):
                             for k, n in enumerate(toks):
                                 perm[b, h, slot + k] = n
                                 inv[b, h, n] = slot + k
-                            nvalid[b, h, blk] = len(toks)
+                            t0 = slot // T_
+                            tiles[b, h, t0] = S // T_
+                            nblock[b, h, t0] = len(toks)
+                            for q in range(S // T_):
+                                nvalid[b, h, t0 + q] = min(T_, max(0, len(toks) - q * T_))
                             slot += S
-                            blk += 1
+    if table:
+        return perm, inv, nvalid, tiles, nblock
     return perm, inv, nvalid
+
+
+def pool_blocks(Xp: np.ndarray, tiles: np.ndarray, n_block: np.ndarray, T_: int) -> np.ndarray:
+    """Block-level feature of blocks that span one or more tiles: the mean of
+    the block's real tokens (its first n_block slots), stored at its first
+    tile; 0 on continuation tiles and for blocks without real tokens."""
+    B, H, Np, d = Xp.shape
+    nb = Np // T_
+    out = np.zeros((B, H, nb, d), dtype=f64)
+    for b in range(B):
+        for h in range(H):
+            for i in range(nb):
+                nv = int(n_block[b, h, i])
+                if tiles[b, h, i] > 0 and nv > 0:
+                    out[b, h, i] = Xp[b, h, i * T_:i * T_ + nv].sum(axis=0) / nv
+    return out
+
+
+def expand_lists(L, tiles: np.ndarray):
+    """Block lists over first tiles -> lists over tiles: every tile of a
+    query block gets the tiles of every key block its block selected,
+    ascending.  L [nb] (lists at first tiles; other entries ignored),
+    tiles [nb] (one (b, h))."""
+    nb = len(tiles)
+    out = [np.zeros(0, dtype=np.int64) for _ in range(nb)]
+    for i in range(nb):
+        n = int(tiles[i])
+        if n == 0 or L[i] is None:
+            continue
+        sel = np.concatenate([np.arange(int(j), int(j) + int(tiles[int(j)])) for j in L[i]]
+                             ) if len(L[i]) else np.zeros(0, dtype=np.int64)
+        for q in range(n):
+            out[i + q] = sel.astype(np.int64)
+    return out
 
 
 def permute(X: np.ndarray, perm: np.ndarray) -> np.ndarray:
@@ -761,17 +871,22 @@ def masked_attention(Q, K, V, mask, scale, dO=None):
 def run(w, Q, K, V, a2v, dO=None, heads=None):
     """The whole hot path on one batch, every step in the pages' order.
     Inputs in [B, N, H, d] / [B, N, Ca] (any float dtype); returns a dict of
-    every intermediate and output in float64 / int64."""
+    every intermediate and output in float64 / int64.  Blocks of a class
+    larger than w.block span several tiles: selection runs over blocks
+    (their first tiles), and the attention over the tiles of the selected
+    blocks (``expand_lists``)."""
     stats = zone_stats(w, V, a2v)
     sid, stie = assign_shapes(w, stats)
-    perm, inv, nval = build_permutation(w, sid)
+    perm, inv, nval, tiles, nblk = build_permutation(w, sid, table=True)
     Qp, Kp, Vp = permute(Q, perm), permute(K, perm), permute(V, perm)
-    Qb, Kb = pool(Qp, nval, w.block), pool(Kp, nval, w.block)
-    lists, flags = select_blocks(w, Qb, Kb, nval, heads=heads)
+    Qb, Kb = pool_blocks(Qp, tiles, nblk, w.block), pool_blocks(Kp, tiles, nblk, w.block)
+    blists, flags = select_blocks(w, Qb, Kb, nblk, heads=heads)
+    lists = {(b, h): expand_lists(L, tiles[b, h]) for (b, h), L in blists.items()}
     scale = 1.0 / math.sqrt(w.d)
     Op, lse = attn_fwd(w, Qp, Kp, Vp, nval, lists, scale)
     res = dict(stats=stats, shape_id=sid, shape_tie=stie, perm=perm, inv=inv, n_valid=nval,
-               Qp=Qp, Kp=Kp, Vp=Vp, Qbar=Qb, Kbar=Kb, lists=lists, flags=flags, Op=Op, lse=lse,
+               tiles=tiles, n_block=nblk, Qp=Qp, Kp=Kp, Vp=Vp, Qbar=Qb, Kbar=Kb,
+               block_lists=blists, lists=lists, flags=flags, Op=Op, lse=lse,
                O=unpermute(Op, inv), scale=scale)
     if dO is not None:
         dOp = permute(dO, perm)

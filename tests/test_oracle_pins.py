@@ -227,6 +227,105 @@ def test_assign_shapes_follow_directional_variance():
     assert not tie.any()
 
 
+# ----------------------------------------------------- block-size classes ---
+
+def _tiny_mc(**kw):
+    """tiny with a second class: 32-token blocks (2,4,4) next to the 16-token
+    menu; about half the zones fall below the threshold."""
+    return synth.WORKLOADS["tiny"].with_(menu=synth.MENU_TINY + ((2, 4, 4),),
+                                         class_tau=(1.4,), **kw)
+
+
+def test_single_class_block_table_is_trivial():
+    w = _small()
+    sid = _random_shapes(w, 4)
+    perm, inv, nval = orc.build_permutation(w, sid)
+    p2, i2, nv2, tiles, nblk = orc.build_permutation(w, sid, table=True)
+    assert np.array_equal(perm, p2) and np.array_equal(nval, nv2)
+    assert np.all(tiles == 1) and np.array_equal(nblk, nval)
+    X = np.random.default_rng(0).standard_normal((w.B, w.N, w.H, w.d))
+    Xp = orc.permute(X, perm)
+    assert np.array_equal(orc.pool_blocks(Xp, tiles, nblk, w.block), orc.pool(Xp, nval, w.block))
+    L = [np.array([0, 3]), np.array([1]), np.zeros(0, dtype=np.int64)] + \
+        [np.zeros(0, dtype=np.int64)] * (len(tiles[0, 0]) - 3)
+    out = orc.expand_lists(L, tiles[0, 0])
+    assert all(np.array_equal(a, b) for a, b in zip(out, L))
+
+
+def test_classes_follow_the_thresholds():
+    """Complexity above the threshold keeps the smaller class, below it the
+    larger; exactly at it the larger is not taken (c >= tau stays fine), and
+    a complexity within CLASS_TIE of it is flagged."""
+    assert orc.menu_classes(_tiny_mc().menu) == [16, 32]
+    taus = (1.5, 0.8)
+    assert [orc.zone_class(c, taus) for c in (2.0, 1.5, 1.0, 0.8, 0.1)] == [0, 0, 1, 1, 2]
+    w = _tiny_mc(T=4, Hg=4, W=8, H=1, d=4)      # two zones
+    st = np.zeros((1, 1, 2, 8))
+    st[0, 0, 0, :3] = [2.0, 0.7, 0.3]           # V = 3 (relative 1.5 + gate 1.0)
+    st[0, 0, 1, :3] = [0.5, 0.25, 0.25]         # V = 1 (relative 0.5 + gate 1.0)
+    st[0, 0, :, 6] = 1.0
+    st[0, 0, :, 7] = 32
+    sid, tie = orc.assign_shapes(w.with_(class_tau=(1.9,)), st)
+    assert [int(np.prod(w.menu[k])) for k in sid[0, 0]] == [16, 32]
+    assert not tie.any()
+    _, tie = orc.assign_shapes(w.with_(class_tau=(1.5 + 1e-7,)), st)
+    assert tie[0, 0, 1] and not tie[0, 0, 0]
+
+
+def test_multi_tile_blocks_tile_their_zones():
+    w = _tiny_mc(T=5, Hg=7, W=9, H=2, d=8, Ca=8, Na=4)
+    sid = _random_shapes(w, 6)
+    perm, inv, nval, tiles, nblk = orc.build_permutation(w, sid, table=True)
+    T_ = w.block
+    for b in range(w.B):
+        for h in range(w.H):
+            assert sorted(perm[b, h][perm[b, h] >= 0]) == list(range(w.N))
+            assert np.array_equal(perm[b, h, inv[b, h]], np.arange(w.N))
+            i = 0
+            while i < len(tiles[b, h]):
+                n = int(tiles[b, h, i])
+                assert n in (1, 2)
+                assert nblk[b, h, i] == nval[b, h, i:i + n].sum()
+                # the block's real tokens come first: full tiles, then the rest
+                for q in range(n):
+                    assert nval[b, h, i + q] == min(T_, max(0, nblk[b, h, i] - q * T_))
+                    assert np.all(perm[b, h, (i + q) * T_:(i + q) * T_ + nval[b, h, i + q]] >= 0)
+                assert np.all(tiles[b, h, i + 1:i + n] == 0)
+                i += n
+    assert (tiles == 2).any() and (tiles == 1).any()
+
+
+def test_mixed_class_path_equals_brute_force_masked_attention():
+    """Blocks of two sizes in one head: the tile-level attention over the
+    expanded lists equals masked attention whose token mask is built from the
+    BLOCK lists (a query token sees every real token of every block its
+    block selected), forward and backward, in the original token order."""
+    w = _tiny_mc()
+    x = _tiny_inputs(w)
+    r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"], dO=x["dO"])
+    assert (r["tiles"] == 2).any() and (r["tiles"] == 1).any()
+    T_ = w.block
+    for h in range(w.H):
+        perm, tiles, L = r["perm"][0, h], r["tiles"][0, h], r["block_lists"][(0, h)]
+        blk_of = np.zeros(w.N, dtype=np.int64)           # token -> first tile of its block
+        i = 0
+        while i < len(tiles):
+            n = int(tiles[i])
+            toks = perm[i * T_:(i + n) * T_]
+            blk_of[toks[toks >= 0]] = i
+            i += n
+        mask = np.zeros((w.N, w.N), bool)
+        for q in range(w.N):
+            sel = L[blk_of[q]]
+            mask[q] = np.isin(blk_of, sel)
+        O, dQ, dK, dV = orc.masked_attention(x["Q"][0, :, h], x["K"][0, :, h], x["V"][0, :, h],
+                                             mask, r["scale"], dO=x["dO"][0, :, h])
+        assert np.abs(O - r["O"][0, :, h]).max() <= 1e-12
+        assert np.abs(dQ - r["dQ"][0, :, h]).max() <= 1e-11
+        assert np.abs(dK - r["dK"][0, :, h]).max() <= 1e-11
+        assert np.abs(dV - r["dV"][0, :, h]).max() <= 1e-11
+
+
 # ------------------------------------------------ A2V cross-attention -------
 
 def test_a2v_norms_special_cases():
