@@ -193,8 +193,9 @@ class Runner:
     """One Prism attention layer (forward + backward) on the device through
     the C ABI, with optional CUDA events around every call."""
 
-    def __init__(self, w, dev, key_chunk_blocks=0, fused=True, x=None):
+    def __init__(self, w, dev, key_chunk_blocks=0, fused=True, x=None, shape_id=None):
         self.w, self.dev, self.fused = w, dev, fused
+        self.shape_id = shape_id   # [B, H, Z] uint8: given shapes (Table 9 baselines)
         self.x = synth.generate(w, dev) if x is None else x
         self.att = prism.PrismAttention(w, dev, key_chunk_blocks=key_chunk_blocks)
         self.stream = torch.cuda.current_stream()
@@ -211,18 +212,23 @@ class Runner:
                 ev[k].record(st)
         o = att.perm_out
         mark(0)
-        if self.fused:
-            p.a2v_norms(xi["qa"], xi["audio"], xi["audio"], att.ws, self.nrm)
+        if self.shape_id is not None:
             mark(1)
-            p.zone_stats_norms(xi["V"], self.nrm, att.stats)
+            mark(2)
+            p.permute_shapes(self.shape_id, xi["Q"], xi["K"], xi["V"], att.ws, o)
         else:
-            mark(1)
-            p.zone_stats(xi["V"], xi["a2v"], att.stats)
-        mark(2)
-        p.assign_and_permute(att.stats, xi["Q"], xi["K"], xi["V"], o)
+            if self.fused:
+                p.a2v_norms(xi["qa"], xi["audio"], xi["audio"], att.ws, self.nrm)
+                mark(1)
+                p.zone_stats_norms(xi["V"], self.nrm, att.stats)
+            else:
+                mark(1)
+                p.zone_stats(xi["V"], xi["a2v"], att.stats)
+            mark(2)
+            p.assign_and_permute(att.stats, xi["Q"], xi["K"], xi["V"], o)
         mark(3)
-        p.block_select(o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"], o["n_valid"], att.ws,
-                       att.lists)
+        p.block_select(o["shape_id"], o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"],
+                       o["n_valid"], att.ws, att.lists)
         mark(4)
         p.sparse_attn_fwd(o["Qp"], o["Kp"], o["Vp"], o["n_valid"], att.lists["row_ptr"],
                           att.lists["col_idx"], att.scale, att.ws, att.Op, att.lse)
@@ -511,21 +517,38 @@ def dense_run(w, dev, args, x, fused, steps=2, warmup=1):
 
 def sweep(args):
     """One line per workload of the measurement plan: the 720p, 1080p and 2K
-    grids, the 41-frame grid, and the 2K stress inputs (white field, one
-    dominant source, skewed noise) at Top-p 0.5 / 0.9 / 0.99."""
-    cases = [synth.WORKLOADS[n] for n in ("720p", "1080p", "2k", "2k_long")]
+    grids, the 41-frame grid, the 2K grid with 128- and 256-token blocks mixed
+    (3 x 16 x 16 and 4 x 16 x 16 zones), the 2K stress inputs (white field,
+    one dominant source, skewed noise) at Top-p 0.5 / 0.9 / 0.99, and the
+    block-shape baselines of Table 9 on the 2K grid."""
+    cases = [(synth.WORKLOADS[n], None) for n in ("720p", "1080p", "2k", "2k_long", "2k_mc",
+                                                  "2k_mc4")]
     for v in ("white", "onesrc", "skew"):
         for p in (0.5, 0.9, 0.99):
-            cases.append(synth.stress("2k", v, p))
+            cases.append((synth.stress("2k", v, p), None))
+    # the block-shape baselines of Table 9 on the 2K grid, shapes given to
+    # every zone: Random (seeded, over the admissible 128-token shapes), Fixed
+    # (1,8,16), Fixed 8^3 (8x16x16 zones, 512-token blocks), Only C256
+    # (4x16x16 zones, the 256-token menu through Eq. 7)
+    w2 = synth.WORKLOADS["2k"]
+    rng = np.random.default_rng(9)
+    Zc = w2.n_zones
+    cases.append((w2.with_(name="2k_random_shapes"),
+                  rng.choice([0, 1], size=(w2.B, w2.H, Zc)).astype(np.uint8)))
+    cases.append((w2.with_(name="2k_fixed_1x8x16"), np.zeros((w2.B, w2.H, Zc), np.uint8)))
+    w8 = w2.with_(name="2k_fixed_8cubed", zone=(8, 16, 16), menu=((8, 8, 8),))
+    cases.append((w8, np.zeros((w8.B, w8.H, w8.n_zones), np.uint8)))
+    cases.append((w2.with_(name="2k_only_c256", zone=(4, 16, 16), menu=synth.MENU_256), None))
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     build.build()
     pk = peaks()
-    for w in cases:
+    for w, sid in cases:
         # the one-source stress input scales the A2V output itself: it runs
         # with the A2V output given
         fused = not args.a2v_input and w.src_mass is None
-        R = Runner(w, dev, args.key_chunk_blocks, fused)
+        sid_t = None if sid is None else torch.as_tensor(sid).to(dev)
+        R = Runner(w, dev, args.key_chunk_blocks, fused, shape_id=sid_t)
         for _ in range(args.warmup):
             R.step()
         torch.cuda.synchronize()
@@ -536,7 +559,8 @@ def sweep(args):
         kern_tf = {s: round(pairs * PF[s] / (m["kern_ms"][s] * 1e-3) / 1e12, 1)
                    for s in ("attn_fwd", "attn_dkdv", "attn_dq")}
         print(json.dumps({
-            "workload": workload_desc(w), "a2v_on_device": fused, "ms_per_step": round(m["ms"], 2),
+            "workload": workload_desc(w), "a2v_on_device": fused and sid is None,
+            "shapes": "given" if sid is not None else "Eq. 7", "ms_per_step": round(m["ms"], 2),
             "value": round(pairs * (PF["fwd"] + PF["bwd"]) / (m["ms"] * 1e-3) / 1e12, 1),
             "unit": "TFLOP/s", "real_token_tflops":
                 round(sel["tok_pairs"] * 14 * w.d / (m["ms"] * 1e-3) / 1e12, 1),
@@ -544,7 +568,8 @@ def sweep(args):
             "selected_per_query_block": sel["lengths"], "near_ties": sel["ties"],
             "kernel_tflops": kern_tf, "frac_burst_dkdv": round(kern_tf["attn_dkdv"] / pk["bf16"], 3),
             "hbm_kernels": {k: v["gbs"] for k, v in
-                            hbm_summary(w, R.att.plan, fused, m["call_ms"], m["kern_ms"], pk).items()},
+                            hbm_summary(w, R.att.plan, fused, m["call_ms"], m["kern_ms"], pk).items()
+                            if sid is None or k not in ("zone_stats", "a2v_norms")},
             "key_ranges": R.att.plan.sz.key_chunks, "clocks": m["clocks"],
             "device_status": m["status"]}), flush=True)
         del R
@@ -735,6 +760,8 @@ def main():
                     help="take the A2V output as an input instead of computing its norms")
     ap.add_argument("--no-dense", action="store_true",
                     help="skip the all-blocks dense run timed next to the sparse step")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override the workload's head count (smaller cases for profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="one line per workload of the measurement plan (not the contract line)")
     args = ap.parse_args()
@@ -742,6 +769,8 @@ def main():
         sweep(args)
         return
     w = synth.WORKLOADS[args.workload]
+    if args.heads > 0:
+        w = w.with_(H=args.heads, name=f"{w.name}-h{args.heads}")
     if args.stress is not None:
         w = synth.stress(args.workload, args.stress, w.topp)
     if args.dense:

@@ -117,11 +117,29 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   const int lS = ilog2_exact(c.block_tokens);
   if (lS < 2 || c.block_tokens > 128) return PRISM_ERR_UNSUPPORTED;
   if (c.d * c.block_tokens > 16384) return PRISM_ERR_UNSUPPORTED;
+  // block-size classes: the menu's token counts, each 1, 2 or 4 tiles
+  int classes[PRISM_MAX_CLASSES];
+  int n_classes = 0;
   for (int k = 0; k < c.n_shapes; ++k) {
     const int* s = c.shapes[k];
     if (s[0] < 1 || s[1] < 1 || s[2] < 1) return PRISM_ERR_ARG;
-    if (s[0] * s[1] * s[2] != c.block_tokens) return PRISM_ERR_UNSUPPORTED;
+    const int t = s[0] * s[1] * s[2];
+    if (t != c.block_tokens && t != 2 * c.block_tokens && t != 4 * c.block_tokens)
+      return PRISM_ERR_UNSUPPORTED;
+    bool seen = false;
+    for (int q = 0; q < n_classes; ++q) seen |= classes[q] == t;
+    if (!seen) classes[n_classes++] = t;
   }
+  for (int a = 1; a < n_classes; ++a)  // ascending
+    for (int q = a; q > 0 && classes[q - 1] > classes[q]; --q) {
+      const int tmp = classes[q];
+      classes[q] = classes[q - 1];
+      classes[q - 1] = tmp;
+    }
+  for (int q = 1; q + 1 < n_classes; ++q)
+    if (!(c.class_tau[q - 1] > c.class_tau[q])) return PRISM_ERR_ARG;  // descending
+  for (int q = 0; q + 1 < n_classes; ++q)
+    if (!(c.class_tau[q] == c.class_tau[q])) return PRISM_ERR_ARG;
   const long long vol = static_cast<long long>(c.zT) * c.zH * c.zW;
   if (vol > 3072) return PRISM_ERR_UNSUPPORTED;
   Plan p;
@@ -143,6 +161,17 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
       z.admissible[z.n_admissible++] = k;
   }
   if (z.n_admissible == 0) return PRISM_ERR_NO_ADMISSIBLE_SHAPE;
+  z.n_classes = n_classes;
+  for (int q = 0; q < n_classes; ++q) {
+    z.class_tokens[q] = classes[q];
+    bool any = false;
+    for (int a = 0; a < z.n_admissible; ++a) {
+      const int* s = c.shapes[z.admissible[a]];
+      any |= s[0] * s[1] * s[2] == classes[q];
+    }
+    if (!any) return PRISM_ERR_NO_ADMISSIBLE_SHAPE;
+  }
+  z.multi_tile = classes[n_classes - 1] > c.block_tokens ? 1 : 0;
   z.blocks_per_zone = static_cast<int>(vol / c.block_tokens);
   const long long nb = z.Np / c.block_tokens;
   if (nb > 8192 || z.Np >= (1LL << 31) || z.N >= (1LL << 31)) return PRISM_ERR_UNSUPPORTED;
@@ -175,6 +204,14 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   p.off_lse2 = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
   p.off_dq = off;
   if (!z.tensor_core_bwd) off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * c.d * 4);
+  // multi-tile blocks: real tokens per block at its first tile, first tile of
+  // every tile's block, and the tile-level selection bitmask
+  p.off_nsel = p.off_bstart = p.off_tbitmask = off;
+  if (z.multi_tile) {
+    p.off_nsel = off; off = align256(off + rows * 4);
+    p.off_bstart = off; off = align256(off + rows * 4);
+    p.off_tbitmask = off; off = align256(off + rows * nwords * 4);
+  }
   // key ranges of at most 512 blocks (32 MB of K and V per head) once a head's
   // K and V outgrow L2; the partial results are capped at 32 GB
   z.key_chunks = 1;
@@ -307,18 +344,21 @@ int prism_permute_shapes(const prism_plan_t* plan, const uint8_t* shape_id, cons
   return PRISM_OK;
 }
 
-int prism_block_select(const prism_plan_t* plan, const float* Qbar, const float* Qbar_lo,
-                       const float* Kbar, const float* Kbar_lo, const int32_t* n_valid,
-                       int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr, int32_t* row_idx,
-                       uint8_t* sel_tie, void* ws, void* stream) {
+int prism_block_select(const prism_plan_t* plan, const uint8_t* shape_id, const float* Qbar,
+                       const float* Qbar_lo, const float* Kbar, const float* Kbar_lo,
+                       const int32_t* n_valid, int32_t* row_ptr, int32_t* col_idx,
+                       int32_t* col_ptr, int32_t* row_idx, uint8_t* sel_tie, void* ws,
+                       void* stream) {
   if (plan == nullptr) return PRISM_ERR_ARG;
+  PRISM_CHECK_PTR(shape_id);
   PRISM_CHECK_PTR(Qbar); PRISM_CHECK_PTR(Qbar_lo);
   PRISM_CHECK_PTR(Kbar); PRISM_CHECK_PTR(Kbar_lo);
   PRISM_CHECK_PTR(n_valid);
   PRISM_CHECK_PTR(row_ptr); PRISM_CHECK_PTR(col_idx);
   PRISM_CHECK_PTR(col_ptr); PRISM_CHECK_PTR(row_idx);
   PRISM_CHECK_PTR(sel_tie); PRISM_CHECK_PTR(ws);
-  PRISM_CUDA(prism::launch_select(plan->p, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid, sel_tie,
+  PRISM_CUDA(prism::launch_select(plan->p, shape_id, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid,
+                                  sel_tie,
                                   row_ptr, col_idx, col_ptr, row_idx,
                                   static_cast<uint8_t*>(ws), static_cast<cudaStream_t>(stream)));
   return PRISM_OK;

@@ -27,9 +27,9 @@ struct BlockGeom {
   int t0, y0, x0, et, ey, ex;
 };
 
+// Geometry of block `local` (raster order of the zone's shape) of zone z.
 __device__ __forceinline__ BlockGeom block_geom(const prism_config_t& c, int nzH, int nzW,
-                                                int bpz, const Menu& menu, int sid, int blk) {
-  const int z = blk / bpz, local = blk % bpz;
+                                                const Menu& menu, int sid, int z, int local) {
   const int zt = z / (nzH * nzW), zh = (z / nzW) % nzH, zw = z % nzW;
   const int bT = menu.ext[sid][0], bH = menu.ext[sid][1], bW = menu.ext[sid][2];
   const int nbh = c.zH / bH, nbw = c.zW / bW;
@@ -53,9 +53,12 @@ __device__ __forceinline__ long long slot_token(const prism_config_t& c, const B
 
 constexpr int kPermThreads = 256;
 
-// One CTA per (block, head, batch): gather Q, K, V rows of the block's
-// tokens into contiguous block order, write perm / inv / n_valid, and the
-// block means of Q and K.  The means are carried in double-float (hi + lo
+// One CTA per (tile, head, batch).  A tile that starts a block gathers the
+// Q, K, V rows of the whole block (1, 2 or 4 tiles of S slots: its class's
+// token count) into contiguous block order, writes perm / inv, the real-token
+// count of each of its tiles, and the block means of Q and K at its first
+// tile (zeros at the tiles that continue it); a continuation tile's CTA
+// returns at once.  The means are carried in double-float (hi + lo
 // fp32): per-thread compensated sums (two_sum) over the thread's tokens, a
 // fixed-order double-float reduction over the token groups, and a
 // double-float division by the real-token count -- about 46 significant
@@ -71,26 +74,30 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
   extern __shared__ __align__(16) float2 red2[];
   const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;  // heads fastest: the heads
                                                                  // of a block share token rows
-  const int S = c.block_tokens, d = c.d, P = d / 8;
+  const int S = c.block_tokens, d = c.d, P = d / 8;  // S: tile slots
   const int G = kPermThreads / P;  // tokens handled per pass
   const int q = threadIdx.x % P, grp = threadIdx.x / P;
   const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
   const long long bh = static_cast<long long>(b) * c.H + h;
-  int sid = shape_id[bh * Z + blk / bpz];
+  const int z = blk / bpz, lt = blk % bpz;  // bpz: tiles per zone
+  int sid = shape_id[bh * Z + z];
   if (sid >= PRISM_MAX_SHAPES || !((menu.adm_mask >> sid) & 1u)) {
     // a caller-given shape that does not tile the zone: report, fall back
-    if (status != nullptr && threadIdx.x == 0 && blk % bpz == 0)
+    if (status != nullptr && threadIdx.x == 0 && lt == 0)
       dev_error(status, DEV_ERR_BOUNDS, 0x5A1, static_cast<uint32_t>(sid));
     sid = menu.first_adm;
   }
-  const BlockGeom g = block_geom(c, nzH, nzW, bpz, menu, sid, blk);
+  const int SB = menu.ext[sid][0] * menu.ext[sid][1] * menu.ext[sid][2];  // block tokens
+  const int tpb = SB / S;                                                   // tiles per block
+  if (lt % tpb != 0) return;  // written by the CTA of the block's first tile
+  const BlockGeom g = block_geom(c, nzH, nzW, menu, sid, z, lt / tpb);
   const int nv = g.et * g.ey * g.ex;
   df sq[8], sk[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) sq[k] = sk[k] = df{0.f, 0.f};
   const long long slot0 = static_cast<long long>(blk) * S;
   constexpr int U = 4;  // tokens per thread in flight
-  for (int k0 = grp; k0 < S; k0 += U * G) {
+  for (int k0 = grp; k0 < SB; k0 += U * G) {
     uint4 vq[U], vk[U], vv[U];
     long long nn[U];
 #pragma unroll
@@ -98,7 +105,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
       const int k = k0 + u * G;
       vq[u] = vk[u] = vv[u] = make_uint4(0, 0, 0, 0);
       nn[u] = -1;
-      if (k < nv) {  // nv <= S
+      if (k < nv) {  // nv <= SB
         nn[u] = slot_token(c, g, k);
         const long long src = ((static_cast<long long>(b) * N + nn[u]) * c.H + h) * d + q * 8;
         vq[u] = ldg_nc_v4(Q + src);
@@ -109,7 +116,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int k = k0 + u * G;
-      if (k >= S) break;
+      if (k >= SB) break;
       const long long dst = (bh * Np + slot0 + k) * d + q * 8;
       if (nn[u] >= 0) {
         const uint32_t wq[4] = {vq[u].x, vq[u].y, vq[u].z, vq[u].w};
@@ -148,16 +155,20 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
     df s = {0.f, 0.f};
     for (int j = 0; j < G; ++j) s = df_add(s, df{r[j * d + cc].x, r[j * d + cc].y});
     const df mean = nv > 0 ? df_div_int(s, nv) : df{0.f, 0.f};
-    const long long o = (bh * nb + blk) * d + cc;
-    if (ch < d) {
-      Qh[o] = mean.hi;
-      Ql[o] = mean.lo;
-    } else {
-      Kh[o] = mean.hi;
-      Kl[o] = mean.lo;
+    for (int t = 0; t < tpb; ++t) {
+      const long long o = (bh * nb + blk + t) * d + cc;
+      const df v = t == 0 ? mean : df{0.f, 0.f};
+      if (ch < d) {
+        Qh[o] = v.hi;
+        Ql[o] = v.lo;
+      } else {
+        Kh[o] = v.hi;
+        Kl[o] = v.lo;
+      }
     }
   }
-  if (threadIdx.x == 0) n_valid[bh * nb + blk] = nv;
+  if (threadIdx.x < tpb)
+    n_valid[bh * nb + blk + threadIdx.x] = min(S, max(0, nv - static_cast<int>(threadIdx.x) * S));
 }
 
 // Xp[b,h,s,:] = X[b,perm[s],h,:] (zeros on padding slots).  One thread per

@@ -20,6 +20,7 @@ struct Plan {
   // workspace offsets (bytes), each region 256-aligned
   size_t off_rowcnt, off_colcnt, off_amb, off_bitmask, off_scores, off_D, off_lse2, off_dq;
   size_t off_part, off_ml;  // key-range partial results (key_chunks > 1)
+  size_t off_nsel, off_bstart, off_tbitmask;  // multi-tile blocks (sz.multi_tile)
 };
 
 // Workspace layout (bytes from the start of ws, each region 256-aligned):
@@ -33,6 +34,10 @@ struct Plan {
 //   off_lse2        fp32  [B*H*Np]       LSE * log2(e) for the backward
 //   off_dq          fp32  [B*H*Np*d]     dQ accumulator of the CUDA-core backward
 //                                        (empty for a tensor-core plan)
+//   off_nsel        int32 [B*H*nb]       (multi-tile blocks) real tokens of the block
+//                                        starting at each tile, 0 on continuations
+//   off_bstart      int32 [B*H*nb]       (multi-tile blocks) first tile of each tile's block
+//   off_tbitmask    u32   [B*H*nb*nw]    (multi-tile blocks) tile-level selection bitmask
 //   off_part        bf16  2 x [B*H*nb, C, S, d] per key / query range: the forward's
 //                                        normalised partial O, later the dK and dV
 //                                        kernel's partial dK and dV, then the dQ
@@ -74,8 +79,9 @@ cudaError_t launch_unpermute(const Plan& p, const int32_t* inv, const uint16_t* 
                              cudaStream_t st);
 cudaError_t launch_dq_convert(const Plan& p, const float* dq, float scale, uint16_t* dQp,
                               cudaStream_t st);
-cudaError_t launch_select(const Plan& p, const float* Qh, const float* Ql, const float* Kh,
-                          const float* Kl, const int32_t* n_valid, uint8_t* sel_tie,
+cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Qh,
+                          const float* Ql, const float* Kh, const float* Kl,
+                          const int32_t* n_valid, uint8_t* sel_tie,
                           int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
                           int32_t* row_idx, uint8_t* ws, cudaStream_t st);
 

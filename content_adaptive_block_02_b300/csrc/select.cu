@@ -616,10 +616,71 @@ __global__ void csc_fill_kernel(int nb, int nwords, long long units,
   }
 }
 
+// ------------------------------------------------- multi-tile blocks -----
+// Block table from the zones' shapes: for every tile, the first tile of its
+// block, and at a block's first tile the block's real-token count (the sum
+// of its tiles' counts; 0 on the tiles that continue a block).
+struct ShapeTokens {
+  int32_t t[PRISM_MAX_SHAPES];  // token count of every menu shape
+};
+
+__global__ void block_table_kernel(long long rows, int nb, int bpz, int Z, int S,
+                                   ShapeTokens ext_tokens,
+                                   const uint8_t* __restrict__ shape_id,
+                                   const int32_t* __restrict__ n_valid,
+                                   int32_t* __restrict__ n_sel, int32_t* __restrict__ bstart) {
+  const long long r = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (r >= rows) return;
+  const long long bh = r / nb;
+  const int t = static_cast<int>(r % nb);
+  const int z = t / bpz, lt = t % bpz;
+  const int sid = shape_id[bh * Z + z];
+  const int tpb = sid < PRISM_MAX_SHAPES ? max(1, ext_tokens.t[sid] / S) : 1;
+  const int first = t - lt % tpb;
+  bstart[r] = first;
+  int nv = 0;
+  if (first == t)
+    for (int q = 0; q < tpb; ++q) nv += n_valid[r + q];
+  n_sel[r] = nv;
+}
+
+// Tile-level selection: tile u is selected for tile t when the block that
+// starts u's block was selected for the block that starts t's block.  One
+// thread per (tile row, 32-tile word); also the row's count.
+__global__ void expand_bitmask_kernel(long long rows, int nb, int nwords,
+                                      const uint32_t* __restrict__ bm_block,
+                                      const int32_t* __restrict__ bstart,
+                                      uint32_t* __restrict__ bm_tile,
+                                      int32_t* __restrict__ rowcnt) {
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long r = i / 32;
+  const int lane = static_cast<int>(i % 32);
+  if (r >= rows) return;
+  const long long bh = r / nb;
+  const long long rs = bh * nb + bstart[r];           // the row of its block
+  const uint32_t* src = bm_block + rs * nwords;
+  const int32_t* bs = bstart + bh * nb;
+  int cnt = 0;
+  for (int w = lane; w < nwords; w += 32) {
+    uint32_t out = 0u;
+    for (int k = 0; k < 32; ++k) {
+      const int u = w * 32 + k;
+      if (u >= nb) break;
+      const int j = bs[u];
+      out |= ((src[j >> 5] >> (j & 31)) & 1u) << k;
+    }
+    bm_tile[r * nwords + w] = out;
+    cnt += __popc(out);
+  }
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) rowcnt[r] = cnt;
+}
+
 }  // namespace
 
-cudaError_t launch_select(const Plan& p, const float* Qh, const float* Ql, const float* Kh,
-                          const float* Kl, const int32_t* n_valid, uint8_t* sel_tie,
+cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Qh,
+                          const float* Ql, const float* Kh, const float* Kl,
+                          const int32_t* n_valid, uint8_t* sel_tie,
                           int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
                           int32_t* row_idx, uint8_t* ws, cudaStream_t st) {
   const prism_config_t& c = p.cfg;
@@ -639,6 +700,19 @@ cudaError_t launch_select(const Plan& p, const float* Qh, const float* Ql, const
   isd_df.lo = static_cast<float>(isd - static_cast<double>(isd_df.hi));
   cudaError_t e = cudaMemsetAsync(status + WS_AMB_COUNT, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
+  int32_t* bstart = reinterpret_cast<int32_t*>(ws + p.off_bstart);
+  if (p.sz.multi_tile) {
+    // blocks span several tiles: select over blocks (their first tiles), with
+    // each block's real-token count in place of the tile counts
+    ShapeTokens ext;
+    for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
+      ext.t[k] = k < c.n_shapes ? c.shapes[k][0] * c.shapes[k][1] * c.shapes[k][2] : c.block_tokens;
+    int32_t* n_sel = reinterpret_cast<int32_t*>(ws + p.off_nsel);
+    block_table_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(
+        rows, nb, p.sz.blocks_per_zone, p.sz.Z, c.block_tokens, ext, shape_id, n_valid,
+        n_sel, bstart);
+    n_valid = n_sel;
+  }
   dim3 g((nb + kTJ - 1) / kTJ, (nb + kTI - 1) / kTI, c.B * c.H);
   score_dot2_kernel<<<g, 256, 0, st>>>(nb, c.d, Qh, Ql, Kh, Kl, Shi, Slo);
   SelParams sp;
@@ -687,6 +761,14 @@ cudaError_t launch_select(const Plan& p, const float* Qh, const float* Ql, const
                            static_cast<int>(fsm));
   if (e != cudaSuccess) return e;
   select_fallback_kernel<<<296, 256, fsm, st>>>(fp);
+  if (p.sz.multi_tile) {
+    // block lists -> tile lists: every tile of a query block gets every tile
+    // of every key block its block selected
+    uint32_t* tbm = reinterpret_cast<uint32_t*>(ws + p.off_tbitmask);
+    expand_bitmask_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(
+        rows, nb, nwords, bitmask, bstart, tbm, rowcnt);
+    bitmask = tbm;
+  }
   scan_kernel<<<1, 1024, 0, st>>>(rows, rowcnt, row_ptr);
   csr_fill_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(
       rows, nwords, bitmask, row_ptr, col_idx);

@@ -8,11 +8,14 @@
 // v_hat_{a,d}); Table 10 caption gives the Eq. 7 quantisation
 // b*_d ~ g_d^-alpha with alpha = 1 the best setting.
 //
-// zone_stats: one CTA per (zone, head) for the value variance and one CTA
-// per zone for the A2V norm statistics.  The zone's real tokens are staged in
+// zone_stats (zones wider than 4 x 16 x 16): one CTA per (zone, head) for
+// the value variance and one CTA per zone for the A2V norm statistics.  The zone's real tokens are staged in
 // shared memory 32 channels at a time (cp.async, 16-byte rows pieces, two
 // stages so the next chunk loads while this one is reduced), then every line
 // along every axis is reduced exactly with a two-pass mean / variance.
+#include <cooperative_groups.h>
+#include <string.h>
+
 #include "prism_internal.cuh"
 
 namespace prism {
@@ -276,17 +279,11 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
 }
 
 // Zones of at most kPT x kPH x kPW tokens (the 3 x 16 x 16 zones of the
-// latent grids, and smaller ones).  One CTA per (head, zone), heads fastest
-// so that the heads of one zone read the same token rows at the same time.
-// The zone is staged 32 channels at a time (two cp.async stages); each token
-// row (t, y) of the stage is padded by 64 bytes so that both register
-// passes below are free of bank conflicts.  Thread (cp, j): cp = channel
-// pair of the stage (16), j = y in pass A and x in pass B (16).
-//   pass A holds the pencil (t, y = j, all x): lines along W (over x) and
-//          along T (over t) are reduced in registers;
-//   pass B holds the pencil (t, all y, x = j): lines along H (over y).
-// Every line is reduced with a two-pass mean / variance in fp32, so each
-// staged element is read from shared memory twice in all.
+// latent grids, and smaller ones) take the cluster kernel below; each token
+// row (t, y) of a staged 32-channel slice is padded by 64 bytes so that the
+// register passes are free of bank conflicts.  Thread (cp, j): cp = channel
+// pair of the slice (16), j = y or x (16).  Every line is reduced with a
+// two-pass mean / variance in fp32.
 constexpr int kPT = 4, kPH = 16, kPW = 16;
 
 // Packed pairs of fp32 (the two channels of a bf16x2 word) for the fp32x2
@@ -349,131 +346,145 @@ __device__ __forceinline__ float line_ss(const f32x2 (&v)[M], int n) {
   return hsum2(s);
 }
 
-// One staged chunk (32 channels) of one zone.  MT x MH x MW bound the zone's
-// real extents; with EXACT the extents are exactly those (a full zone) and
-// the runtime extents are ignored.
+// The lines of one staged 32-channel slice, one line set at a time so that
+// a thread holds at most one line (16 words) in registers: along W the
+// (t, y = j) rows, along T the (y = j, x) columns, along H the (t, x = j)
+// columns.  Each staged element is read three times from shared memory.
 template <int MT, int MH, int MW, bool EXACT>
-__device__ __forceinline__ void pencil_chunk(const uint32_t* __restrict__ tile, int rs, int vt_,
-                                             int vy_, int vx_, int cp, int j, float (&acc)[3]) {
+__device__ __forceinline__ void lines_chunk(const uint32_t* __restrict__ tile, int rs, int vt_,
+                                            int vy_, int vx_, int cp, int j, float (&acc)[3]) {
   const int vt = EXACT ? MT : vt_, vy = EXACT ? MH : vy_, vx = EXACT ? MW : vx_;
   constexpr int P = kChunk / 2;  // words per token in a stage
   if (j < vy) {
-    // ---- pass A: pencil (t, y = j, all x): lines along W and along T ----
-    uint32_t w[MT][MW];
-#pragma unroll
-    for (int t = 0; t < MT; ++t)
-#pragma unroll
-      for (int x = 0; x < MW; ++x)
-        w[t][x] = (t < vt && x < vx) ? tile[(t * vy + j) * rs + x * P + cp] : 0u;
     if (vx >= 2) {
       const float inv = 1.f / static_cast<float>(vx);
+#pragma unroll 1
+      for (int t = 0; t < vt; ++t) {
+        f32x2 v[MW];
 #pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        if (t < vt) {
-          f32x2 v[MW];
-#pragma unroll
-          for (int x = 0; x < MW; ++x) v[x] = unpack2(w[t][x]);
-          acc[2] += line_ss(v, vx) * inv;
-        }
+        for (int x = 0; x < MW; ++x)
+          v[x] = unpack2(x < vx ? tile[(t * vy + j) * rs + x * P + cp] : 0u);
+        acc[2] += line_ss(v, vx) * inv;
       }
     }
     if (vt >= 2) {
       const float inv = 1.f / static_cast<float>(vt);
+#pragma unroll 1
+      for (int x = 0; x < vx; ++x) {
+        f32x2 v[MT];
 #pragma unroll
-      for (int x = 0; x < MW; ++x) {
-        if (x < vx) {
-          f32x2 v[MT];
-#pragma unroll
-          for (int t = 0; t < MT; ++t) v[t] = unpack2(w[t][x]);
-          acc[0] += line_ss(v, vt) * inv;
-        }
+        for (int t = 0; t < MT; ++t)
+          v[t] = unpack2(t < vt ? tile[(t * vy + j) * rs + x * P + cp] : 0u);
+        acc[0] += line_ss(v, vt) * inv;
       }
     }
   }
   if (j < vx && vy >= 2) {
-    // ---- pass B: pencil (t, all y, x = j): lines along H ----
     const float inv = 1.f / static_cast<float>(vy);
+#pragma unroll 1
+    for (int t = 0; t < vt; ++t) {
+      f32x2 v[MH];
 #pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      if (t < vt) {
-        f32x2 v[MH];
-#pragma unroll
-        for (int y = 0; y < MH; ++y)
-          v[y] = unpack2(y < vy ? tile[(t * vy + y) * rs + j * P + cp] : 0u);
-        acc[1] += line_ss(v, vy) * inv;
-      }
+      for (int y = 0; y < MH; ++y)
+        v[y] = unpack2(y < vy ? tile[(t * vy + y) * rs + j * P + cp] : 0u);
+      acc[1] += line_ss(v, vy) * inv;
     }
   }
 }
 
-__global__ void __launch_bounds__(kStatsThreads, 2) zone_stats_pencil_kernel(
+// Same statistics with the channels split over a thread-block cluster: the
+// d / 32 CTAs of a cluster take one 32-channel slice each of the same
+// (zone, head), stage it in shared memory in one go (all loads issued at
+// once, no chunk loop), reduce their lines as above, and the cluster's
+// first CTA sums the slices' partial sums in fixed order through distributed
+// shared memory (deterministic).  Up to four clusters' CTAs share an SM, so
+// many more loads are in flight than with one CTA walking the channel
+// chunks of a (zone, head) in turn.  The audio statistics take the first CTA
+// of the cluster of the extra head slot h == H.
+__global__ void __launch_bounds__(kStatsThreads, 4) zone_stats_cluster_kernel(
     prism_config_t c, int nzH, int nzW, int Z, const uint16_t* __restrict__ V,
     const uint16_t* __restrict__ a2v, const float* __restrict__ nrm, float* __restrict__ stats) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float red[32 * 4];
-  const int h = blockIdx.x, z = blockIdx.y, b = blockIdx.z;
+  __shared__ float part[3];
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int ncl = static_cast<int>(cluster.num_blocks());       // channel slices
+  const int slice = static_cast<int>(cluster.block_rank());
+  const int h = blockIdx.x / ncl, z = blockIdx.y, b = blockIdx.z;
   const ZoneGeom g = zone_geom(c, nzH, nzW, z);
-  if (h == c.H) {
-    audio_zone_stats(c, g, b, z, Z, a2v, nrm, stats, smem);
+  if (h == c.H) {  // uniform over the cluster: no cluster barrier on this path
+    if (slice == 0) audio_zone_stats(c, g, b, z, Z, a2v, nrm, stats, smem);
     return;
   }
   const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
   const int vol = g.vt * g.vy * g.vx;
   const int rs = g.vx * (kChunk / 2) + 16;  // words per padded token row (t, y)
-  const size_t stage_words = static_cast<size_t>(c.zT) * c.zH * (c.zW * (kChunk / 2) + 16);
-  uint32_t* st0 = reinterpret_cast<uint32_t*>(smem);
-  const int nchunk = c.d / kChunk;
-  auto load_chunk = [&](int ch, int stage) {
-    uint32_t* dst = st0 + stage * stage_words;
+  uint32_t* tile = reinterpret_cast<uint32_t*>(smem);
+  {
+    // one 16-byte piece per thread and pass: piece i = (token, quarter);
+    // full 16 x 16 frames take their token coordinates by shifts
+    const uint16_t* vb = V + (static_cast<long long>(b) * N * c.H + h) * c.d + slice * kChunk;
+    const long long tok_stride = static_cast<long long>(c.H) * c.d;  // elements per token
     const int pieces = vol * (kChunk / 8);
-    for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
-      const int li = i >> 2, q = i & 3;
-      const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
-      const long long n = (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
-      const uint16_t* src =
-          V + ((static_cast<long long>(b) * N + n) * c.H + h) * c.d + ch * kChunk + q * 8;
-      cp_async16(dst + (t * g.vy + y) * rs + x * (kChunk / 2) + q * 4, src);
+    if (g.vy == 16 && g.vx == 16) {
+#pragma unroll 4
+      for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+        const int li = i >> 2, q = i & 3;
+        const int x = li & 15, y = (li >> 4) & 15, t = li >> 8;
+        const long long n = (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
+        cp_async16(tile + (t * 16 + y) * rs + x * (kChunk / 2) + q * 4, vb + n * tok_stride + q * 8);
+      }
+    } else {
+      for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+        const int li = i >> 2, q = i & 3;
+        const int x = li % g.vx, y = (li / g.vx) % g.vy, t = li / (g.vx * g.vy);
+        const long long n =
+            (static_cast<long long>(g.t0 + t) * c.Hg + (g.y0 + y)) * c.W + (g.x0 + x);
+        cp_async16(tile + (t * g.vy + y) * rs + x * (kChunk / 2) + q * 4, vb + n * tok_stride + q * 8);
+      }
     }
     cp_async_commit();
-  };
-  const int cp = threadIdx.x & 15, j = threadIdx.x >> 4;
-  float acc[3] = {0.f, 0.f, 0.f};  // sums of line variances along T, H, W
-  load_chunk(0, 0);
-  for (int ch = 0; ch < nchunk; ++ch) {
-    if (ch + 1 < nchunk) {
-      load_chunk(ch + 1, (ch + 1) & 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t* tile = st0 + (ch & 1) * stage_words;
-    if (g.vt == 3 && g.vy == 16 && g.vx == 16)
-      pencil_chunk<3, 16, 16, true>(tile, rs, 3, 16, 16, cp, j, acc);
-    else if (g.vt == 4 && g.vy == 16 && g.vx == 16)
-      pencil_chunk<4, 16, 16, true>(tile, rs, 4, 16, 16, cp, j, acc);
-    else
-      pencil_chunk<kPT, kPH, kPW, false>(tile, rs, g.vt, g.vy, g.vx, cp, j, acc);
-    __syncthreads();
+    cp_async_wait<0>();
   }
+  __syncthreads();
+  const int cp = threadIdx.x & 15, j = threadIdx.x >> 4;
+  float acc[3] = {0.f, 0.f, 0.f};
+  if (g.vt == 3 && g.vy == 16 && g.vx == 16)
+    lines_chunk<3, 16, 16, true>(tile, rs, 3, 16, 16, cp, j, acc);
+  else if (g.vt == 4 && g.vy == 16 && g.vx == 16)
+    lines_chunk<4, 16, 16, true>(tile, rs, 4, 16, 16, cp, j, acc);
+  else
+    lines_chunk<kPT, kPH, kPW, false>(tile, rs, g.vt, g.vy, g.vx, cp, j, acc);
   block_sum<3>(acc, red);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0)
+    for (int a = 0; a < 3; ++a) part[a] = acc[a];
+  cluster.sync();
+  if (slice == 0 && threadIdx.x == 0) {
+    float tot[3] = {0.f, 0.f, 0.f};
+    for (int r = 0; r < ncl; ++r) {
+      const float* pr = cluster.map_shared_rank(part, r);
+      for (int a = 0; a < 3; ++a) tot[a] += pr[a];
+    }
     const float nl[3] = {static_cast<float>(g.vy * g.vx), static_cast<float>(g.vt * g.vx),
                          static_cast<float>(g.vt * g.vy)};
     const int len[3] = {g.vt, g.vy, g.vx};
     float* o = stats + ((static_cast<long long>(b) * c.H + h) * Z + z) * 8;
     for (int a = 0; a < 3; ++a)
-      o[a] = len[a] >= 2 ? acc[a] / (nl[a] * static_cast<float>(c.d)) : 0.f;
+      o[a] = len[a] >= 2 ? tot[a] / (nl[a] * static_cast<float>(c.d)) : 0.f;
   }
+  cluster.sync();  // the partial sums stay readable until the first CTA has them
 }
 
 // ------------------------------------------------------------ assign ------
 
 struct MenuConst {
   double log2_ext[PRISM_MAX_SHAPES][3];
-  int adm[PRISM_MAX_SHAPES];
-  int n_adm;
-  double log2_S;
+  int adm[PRISM_MAX_CLASSES][PRISM_MAX_SHAPES];  // admissible menu shapes per class
+  int n_adm[PRISM_MAX_CLASSES];
+  double log2_S[PRISM_MAX_CLASSES];             // log2 of each class's token count
+  double tau[PRISM_MAX_CLASSES - 1];            // class thresholds, descending
+  int n_classes;
 };
 
 // Eq. 7 (Table 10 caption) in log space: with bT*bH*bW = S fixed, the
@@ -483,38 +494,65 @@ struct MenuConst {
 // Guidance g_d = u_v r_{v,d} + u_a a_bar v_hat_{a,d} + eps, with
 // r_{v,d} = var_v_d / sum var_v, v_hat_{a,d} = var_n_d / sum var_n (1/3 each
 // when the sum is 0) and a_bar = nbar / max over the zones of nbar.
+// With several block-size classes (Table 10 caption: thresholds
+// tau_128 / tau_256), S is the zone's class: the number of thresholds its
+// complexity c = u_v V_z / mean_z V + u_a a_bar is below, V_z = sum_d var_v_d.
 __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, MenuConst menu,
                                                      const float* __restrict__ stats,
                                                      uint8_t* __restrict__ shape_id,
                                                      uint8_t* __restrict__ shape_tie) {
-  __shared__ double red[32];
+  __shared__ double red[32], red2[32];
   const int h = blockIdx.x, b = blockIdx.y;
   const float* sb = stats + static_cast<long long>(b) * c.H * Z * 8;
   const float* sh = sb + static_cast<long long>(h) * Z * 8;
-  // max over zones of nbar (the audio statistics are the same for every head)
-  double mx = 0.0;
-  for (int z = threadIdx.x; z < Z; z += blockDim.x) mx = fmax(mx, static_cast<double>(sh[z * 8 + 6]));
-  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double m = 0.0;
-    for (int w = 0; w < (blockDim.x >> 5); ++w) m = fmax(m, red[w]);
-    red[0] = m;
-  }
-  __syncthreads();
-  const double nmax = red[0];
-  for (int z = threadIdx.x; z < Z; z += blockDim.x) {
-    double sv[3], sn[3], nbar;
+  // the zone's video statistics (this head's, or the mean over heads)
+  auto video = [&](int z, double (&sv)[3]) {
     if (c.per_head) {
       for (int a = 0; a < 3; ++a) sv[a] = sh[z * 8 + a];
     } else {
       for (int a = 0; a < 3; ++a) {
         double s = 0.0;
-        for (int hh = 0; hh < c.H; ++hh) s += static_cast<double>(sb[(static_cast<long long>(hh) * Z + z) * 8 + a]);
+        for (int hh = 0; hh < c.H; ++hh)
+          s += static_cast<double>(sb[(static_cast<long long>(hh) * Z + z) * 8 + a]);
         sv[a] = s / c.H;
       }
     }
+  };
+  // max over zones of nbar (the audio statistics are the same for every head)
+  // and, for the class rule, the sum over zones of V_z (fixed order)
+  double mx = 0.0, vs = 0.0;
+  for (int z = threadIdx.x; z < Z; z += blockDim.x) {
+    mx = fmax(mx, static_cast<double>(sh[z * 8 + 6]));
+    if (menu.n_classes > 1) {
+      double sv[3];
+      video(z, sv);
+      vs += sv[0] + sv[1] + sv[2];
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    vs += __shfl_xor_sync(0xffffffffu, vs, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = mx;
+    red2[threadIdx.x >> 5] = vs;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double m = 0.0, v = 0.0;
+    for (int w = 0; w < (blockDim.x >> 5); ++w) {
+      m = fmax(m, red[w]);
+      v += red2[w];
+    }
+    red[0] = m;
+    red2[0] = v / Z;
+  }
+  __syncthreads();
+  const double nmax = red[0], vmean = red2[0];
+  const double uv = c.use_video ? 1.0 : 0.0, ua = c.use_audio ? 1.0 : 0.0;
+  for (int z = threadIdx.x; z < Z; z += blockDim.x) {
+    double sv[3], sn[3], nbar;
+    video(z, sv);
     for (int a = 0; a < 3; ++a) sn[a] = sh[z * 8 + 3 + a];
     nbar = sh[z * 8 + 6];
     const double ssv = sv[0] + sv[1] + sv[2];
@@ -524,7 +562,16 @@ __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, Me
     // at most 1e-10 nbar^2
     const bool no_var = !(ssn > 1e-10 * nbar * nbar);
     const double abar = nmax > 0.0 ? nbar / nmax : 0.0;
-    const double uv = c.use_video ? 1.0 : 0.0, ua = c.use_audio ? 1.0 : 0.0;
+    // block-size class
+    int cls = 0;
+    bool class_tie = false;
+    if (menu.n_classes > 1) {
+      const double cz = uv * (vmean > 0.0 ? ssv / vmean : 0.0) + ua * abar;
+      for (int q = 0; q + 1 < menu.n_classes; ++q) {
+        cls += cz < menu.tau[q] ? 1 : 0;
+        class_tie |= fabs(cz - menu.tau[q]) <= 1e-5 * fmax(1.0, fabs(menu.tau[q]));
+      }
+    }
     double lg[3];
     for (int a = 0; a < 3; ++a) {
       const double r = ssv > 0.0 ? sv[a] / ssv : 1.0 / 3.0;
@@ -534,11 +581,11 @@ __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, Me
     }
     const double mean = (lg[0] + lg[1] + lg[2]) / 3.0;
     double lstar[3];
-    for (int a = 0; a < 3; ++a) lstar[a] = menu.log2_S / 3.0 + c.alpha * (mean - lg[a]);
+    for (int a = 0; a < 3; ++a) lstar[a] = menu.log2_S[cls] / 3.0 + c.alpha * (mean - lg[a]);
     double best = 1e300, second = 1e300;
-    int bk = menu.adm[0];
-    for (int q = 0; q < menu.n_adm; ++q) {
-      const int k = menu.adm[q];
+    int bk = menu.adm[cls][0];
+    for (int q = 0; q < menu.n_adm[cls]; ++q) {
+      const int k = menu.adm[cls][q];
       double cost = 0.0;
       for (int a = 0; a < 3; ++a) {
         const double e = menu.log2_ext[k][a] - lstar[a];
@@ -554,7 +601,7 @@ __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, Me
     }
     const long long o = (static_cast<long long>(b) * c.H + h) * Z + z;
     shape_id[o] = static_cast<uint8_t>(bk);
-    shape_tie[o] = (menu.n_adm > 1 && (second - best) < 1e-4) ? 1 : 0;
+    shape_tie[o] = ((menu.n_adm[cls] > 1 && (second - best) < 1e-4) || class_tie) ? 1 : 0;
   }
 }
 
@@ -568,15 +615,28 @@ cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* 
   const size_t smem_audio = static_cast<size_t>(vol) * sizeof(double);
   const size_t smem = smem_video > smem_audio ? smem_video : smem_audio;
   if (c.zT <= kPT && c.zH <= kPH && c.zW <= kPW && p.sz.Z <= 65535) {
-    const size_t stage_words = static_cast<size_t>(c.zT) * c.zH * (c.zW * (kChunk / 2) + 16);
-    const size_t sv = 2 * stage_words * 4;
+    const int ncl = c.d / kChunk;  // channel slices = CTAs per cluster (d <= 128: <= 4)
+    const size_t sv = static_cast<size_t>(c.zT) * c.zH * (c.zW * (kChunk / 2) + 16) * 4;
     const size_t sm = sv > smem_audio ? sv : smem_audio;
-    cudaError_t e = cudaFuncSetAttribute(zone_stats_pencil_kernel,
+    cudaError_t e = cudaFuncSetAttribute(zone_stats_cluster_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sm));
     if (e != cudaSuccess) return e;
-    zone_stats_pencil_kernel<<<dim3(c.H + 1, p.sz.Z, c.B), kStatsThreads, sm, st>>>(
-        c, p.sz.nzH, p.sz.nzW, p.sz.Z, V, a2v, nrm, stats);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((c.H + 1) * ncl, p.sz.Z, c.B);
+    cfg.blockDim = dim3(kStatsThreads, 1, 1);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ncl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, zone_stats_cluster_kernel, c, p.sz.nzH, p.sz.nzW, p.sz.Z, V,
+                           a2v, nrm, stats);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
   cudaError_t e = cudaFuncSetAttribute(zone_stats_kernel,
@@ -592,11 +652,20 @@ cudaError_t launch_zone_stats(const Plan& p, const uint16_t* V, const uint16_t* 
 cudaError_t launch_assign(const Plan& p, const float* stats, uint8_t* shape_id,
                           uint8_t* shape_tie, cudaStream_t st) {
   MenuConst m;
+  memset(&m, 0, sizeof(m));
+  const prism_config_t& c = p.cfg;
   for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
     for (int a = 0; a < 3; ++a) m.log2_ext[k][a] = p.log2_ext[k][a];
-  for (int q = 0; q < PRISM_MAX_SHAPES; ++q) m.adm[q] = p.sz.admissible[q];
-  m.n_adm = p.sz.n_admissible;
-  m.log2_S = p.log2_S;
+  m.n_classes = p.sz.n_classes;
+  for (int q = 0; q < p.sz.n_classes; ++q) {
+    m.log2_S[q] = log2(static_cast<double>(p.sz.class_tokens[q]));
+    for (int a = 0; a < p.sz.n_admissible; ++a) {
+      const int k = p.sz.admissible[a];
+      if (c.shapes[k][0] * c.shapes[k][1] * c.shapes[k][2] == p.sz.class_tokens[q])
+        m.adm[q][m.n_adm[q]++] = k;
+    }
+    if (q + 1 < p.sz.n_classes) m.tau[q] = c.class_tau[q];
+  }
   assign_kernel<<<dim3(p.cfg.H, p.cfg.B), 256, 0, st>>>(p.cfg, p.sz.Z, m, stats, shape_id,
                                                         shape_tie);
   return cudaGetLastError();

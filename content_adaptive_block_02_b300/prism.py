@@ -24,6 +24,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libprism.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "prism.h")
 MAX_SHAPES = 16
+MAX_CLASSES = 3
 
 ERRORS = {
     0: "PRISM_OK", -1: "PRISM_ERR_ARG", -2: "PRISM_ERR_ALIGN", -3: "PRISM_ERR_UNSUPPORTED",
@@ -50,6 +51,7 @@ class Config(ctypes.Structure):
         ("topk_floor", ctypes.c_int), ("topp", ctypes.c_float),
         ("timeout_cycles", ctypes.c_ulonglong), ("attn_kernel", ctypes.c_int),
         ("fault_inject", ctypes.c_int), ("key_chunk_blocks", ctypes.c_int),
+        ("class_tau", ctypes.c_double * (MAX_CLASSES - 1)),
     ]
 
 
@@ -69,6 +71,8 @@ class Sizes(ctypes.Structure):
         ("max_pairs", ctypes.c_longlong), ("ws_bytes", ctypes.c_size_t),
         ("tensor_core_fwd", ctypes.c_int), ("tensor_core_bwd", ctypes.c_int),
         ("key_chunks", ctypes.c_int), ("chunk_blocks", ctypes.c_int),
+        ("n_classes", ctypes.c_int), ("class_tokens", ctypes.c_int * MAX_CLASSES),
+        ("multi_tile", ctypes.c_int),
     ]
 
 
@@ -99,7 +103,7 @@ def lib() -> ctypes.CDLL:
         "prism_strerror": [ctypes.c_int],
         "prism_zone_stats": [P, P, P, P, P],
         "prism_assign_and_permute": [P] + [P] * 17,
-        "prism_block_select": [P] + [P] * 12,
+        "prism_block_select": [P] + [P] * 13,
         "prism_sparse_attn_fwd": [P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P],
         "prism_permute": [P, P, P, P, P],
         "prism_sparse_attn_bwd": [P] + [P] * 11 + [ctypes.c_float] + [P] * 5,
@@ -166,6 +170,8 @@ def make_config(w, timeout_cycles: int = 0, attn_kernel: int = 0,
     c.attn_kernel = attn_kernel
     c.fault_inject = fault_inject
     c.key_chunk_blocks = key_chunk_blocks
+    for q, t in enumerate(tuple(getattr(w, "class_tau", ()) or ())[:MAX_CLASSES - 1]):
+        c.class_tau[q] = t
     return c
 
 
@@ -317,10 +323,11 @@ class Plan:
             sel_tie=torch.empty(w.B, w.H, self.nb, dtype=torch.uint8, device=device),
         )
 
-    def block_select(self, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid, ws, out=None):
+    def block_select(self, shape_id, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid, ws, out=None):
         o = out if out is not None else self.alloc_lists(Qbar.device)
         _check(lib().prism_block_select(
-            self.h, _ptr(Qbar), _ptr(Qbar_lo), _ptr(Kbar), _ptr(Kbar_lo), _ptr(n_valid),
+            self.h, _ptr(shape_id), _ptr(Qbar), _ptr(Qbar_lo), _ptr(Kbar), _ptr(Kbar_lo),
+            _ptr(n_valid),
             _ptr(o["row_ptr"]), _ptr(o["col_idx"]), _ptr(o["col_ptr"]), _ptr(o["row_idx"]),
             _ptr(o["sel_tie"]), _ptr(ws), _stream()), "prism_block_select")
         return o
@@ -410,8 +417,8 @@ class PrismAttention:
             p.assign_and_permute(self.stats, Q, K, V, o)
         else:
             p.permute_shapes(shape_id, Q, K, V, self.ws, o)
-        p.block_select(o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"], o["n_valid"], self.ws,
-                       self.lists)
+        p.block_select(o["shape_id"], o["Qbar"], o["Qbar_lo"], o["Kbar"], o["Kbar_lo"],
+                       o["n_valid"], self.ws, self.lists)
         p.sparse_attn_fwd(o["Qp"], o["Kp"], o["Vp"], o["n_valid"], self.lists["row_ptr"],
                           self.lists["col_idx"], self.scale, self.ws, self.Op, self.lse)
         p.unpermute(o["inv"], self.Op, self.O)

@@ -41,6 +41,7 @@ extern "C" {
 #endif
 
 #define PRISM_MAX_SHAPES 16
+#define PRISM_MAX_CLASSES 3
 
 enum {
   PRISM_OK = 0,
@@ -86,6 +87,18 @@ typedef struct prism_config {
                              (ranges of 512 blocks once a head has more than 1024
                              key blocks, else one range); > 0 = ranges of this
                              many blocks (at most 64 ranges)                      */
+  double class_tau[PRISM_MAX_CLASSES - 1];
+                          /* block-size classes (Table 10 caption: thresholds
+                             tau_128 / tau_256; Table 11: classes C_64, C_128,
+                             C_256).  The menu's distinct token counts are the
+                             classes, ascending; each must be block_tokens,
+                             2 block_tokens or 4 block_tokens (a block then spans
+                             1, 2 or 4 consecutive tiles of block_tokens slots).
+                             A zone of complexity c = V_z / mean V + a_bar
+                             (V_z: its summed directional video variance, a_bar
+                             its audio gate; each term only when that guidance is
+                             on) takes class k = number of thresholds c is below;
+                             thresholds descending, the first n_classes - 1 used. */
 } prism_config_t;
 
 #define PRISM_FAULT_STARVE_LOADS 1
@@ -95,8 +108,9 @@ typedef struct prism_sizes {
   int Tp, Hp, Wp;         /* padded grid */
   int nzT, nzH, nzW;      /* zones per axis */
   int Z;                  /* zones = nzT * nzH * nzW */
-  int nb;                 /* blocks per (b, h) = Np / S */
-  int blocks_per_zone;
+  int nb;                 /* tiles per (b, h) = Np / S (S = block_tokens); one block
+                             per tile for a single class of S tokens */
+  int blocks_per_zone;    /* tiles per zone */
   long long N, Np;        /* real and padded tokens */
   int n_admissible;       /* menu shapes that tile the zone */
   int admissible[PRISM_MAX_SHAPES];
@@ -114,13 +128,19 @@ typedef struct prism_sizes {
                              combined per block afterwards (their room is part of
                              ws_bytes).  1 = no split. */
   int chunk_blocks;       /* blocks per range (nb when key_chunks == 1) */
+  int n_classes;          /* block-size classes of the menu */
+  int class_tokens[PRISM_MAX_CLASSES]; /* their token counts, ascending */
+  int multi_tile;         /* 1 when some block spans several tiles: nb, n_valid
+                             and the block lists then count tiles (a block's
+                             mean is stored at its first tile) */
 } prism_sizes_t;
 
 typedef struct prism_plan prism_plan_t;
 
-/* Validate `cfg` and build a host plan.  Errors: PRISM_ERR_ARG (sizes),
- * PRISM_ERR_UNSUPPORTED (menu with unequal token counts, d, S),
- * PRISM_ERR_NO_ADMISSIBLE_SHAPE (no menu shape divides the zone). */
+/* Validate `cfg` and build a host plan.  Errors: PRISM_ERR_ARG (sizes,
+ * thresholds not descending), PRISM_ERR_UNSUPPORTED (a menu token count that
+ * is not 1, 2 or 4 times block_tokens, d, S), PRISM_ERR_NO_ADMISSIBLE_SHAPE
+ * (a class with no menu shape that divides the zone). */
 int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out);
 void prism_plan_destroy(prism_plan_t* plan);
 int prism_plan_query(const prism_plan_t* plan, prism_sizes_t* out);
@@ -205,8 +225,10 @@ int prism_zone_stats_norms(const prism_plan_t* plan, const uint16_t* V, const fl
  *              block's real tokens as a double-float pair: Qbar is the fp32
  *              rounding of the mean and Qbar_lo the fp32 rounding of the rest
  *              (Qbar + Qbar_lo carries about 46 significant bits); 0 for a
- *              block without real tokens
- *   n_valid    [B, H, nb] int32 out: real tokens in the block (first in it) */
+ *              block without real tokens; a block that spans several tiles
+ *              has its mean at its first tile and 0 at the others
+ *   n_valid    [B, H, nb] int32 out: real tokens in each tile (a block's real
+ *              tokens come first in it, so they fill its first tiles) */
 int prism_assign_and_permute(const prism_plan_t* plan, const float* stats,
                              const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                              uint8_t* shape_id, uint8_t* shape_tie, int32_t* perm,
@@ -233,6 +255,11 @@ int prism_permute_shapes(const prism_plan_t* plan, const uint8_t* shape_id, cons
 /* Step 3+4 -- block scores Qbar Kbar^T / sqrt(d) and hybrid Top-k / Top-p
  * selection (Table 7 caption; Abstract: per-query sparsity), then the
  * block lists in both directions.
+ *   shape_id    [B, H, Z] uint8 in: the zones' shapes (as step 2 wrote or was
+ *               given them); with blocks that span several tiles
+ *               (prism_sizes_t.multi_tile) the selection runs over blocks and
+ *               every list below is over tiles: each tile of a query block
+ *               lists every tile of every key block its block selected
  *   Qbar, Qbar_lo, Kbar, Kbar_lo [B, H, nb, d] fp32 in (as written above)
  *   n_valid     [B, H, nb] int32 in
  *   row_ptr     [B*H*nb + 1] int32 out: CSR offsets over all (b, h, i)
@@ -240,14 +267,15 @@ int prism_permute_shapes(const prism_plan_t* plan, const uint8_t* shape_id, cons
  *   col_ptr     [B*H*nb + 1] int32 out: CSC offsets over all (b, h, j)
  *   row_idx     [max_pairs] int32 out: query blocks of each key block, ascending
  *   sel_tie     [B, H, nb] uint8 out: 1 where the decision sat within 1e-6 of
- *               a boundary (score gap or cumulative mass)
+ *               a boundary (score gap or cumulative mass), at a block's first tile
  *   ws          workspace of ws_bytes
  * Query blocks with no real token select nothing; candidates are the key
  * blocks with at least one real token. */
-int prism_block_select(const prism_plan_t* plan, const float* Qbar, const float* Qbar_lo,
-                       const float* Kbar, const float* Kbar_lo, const int32_t* n_valid,
-                       int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
-                       int32_t* row_idx, uint8_t* sel_tie, void* ws, void* stream);
+int prism_block_select(const prism_plan_t* plan, const uint8_t* shape_id, const float* Qbar,
+                       const float* Qbar_lo, const float* Kbar, const float* Kbar_lo,
+                       const int32_t* n_valid, int32_t* row_ptr, int32_t* col_idx,
+                       int32_t* col_ptr, int32_t* row_idx, uint8_t* sel_tie, void* ws,
+                       void* stream);
 
 /* Step 5a -- block-sparse attention forward (Fig. 2 caption).
  * For every query block i and every key block j in its list, exact softmax

@@ -48,8 +48,18 @@ int main(void) {
   /* rejections before any launch */
   c = cfg_2k(); c.d = 96 + 1;
   CHECK(prism_plan_create(&c, &plan) == PRISM_ERR_UNSUPPORTED && plan == NULL);
-  c = cfg_2k(); c.shapes[0][0] = 2;           /* 2 x 8 x 16 = 256 tokens */
+  c = cfg_2k(); c.shapes[0][0] = 4; c.shapes[0][1] = 16;  /* 4 x 16 x 16: 8 tiles */
   CHECK(prism_plan_create(&c, &plan) == PRISM_ERR_UNSUPPORTED);
+  c = cfg_2k(); c.shapes[0][0] = 2;           /* a 256-token class that fits no 3-frame zone */
+  CHECK(prism_plan_create(&c, &plan) == PRISM_ERR_NO_ADMISSIBLE_SHAPE);
+  /* two block-size classes: (1,16,16) next to the 128-token menu */
+  c = cfg_2k(); c.n_shapes = 8; c.shapes[7][0] = 1; c.shapes[7][1] = 16; c.shapes[7][2] = 16;
+  c.class_tau[0] = 0.9;
+  CHECK(prism_plan_create(&c, &plan) == PRISM_OK);
+  CHECK(prism_plan_query(plan, &z) == PRISM_OK);
+  CHECK(z.n_classes == 2 && z.class_tokens[0] == 128 && z.class_tokens[1] == 256);
+  CHECK(z.multi_tile == 1 && z.nb == 2520 && z.blocks_per_zone == 6);
+  prism_plan_destroy(plan);
   c = cfg_2k(); c.zT = 5;                     /* no menu shape divides 5 x 16 x 16 ... */
   c.n_shapes = 2; c.shapes[0][0] = 2; c.shapes[1][0] = 2;
   c.shapes[0][1] = 8; c.shapes[0][2] = 8; c.shapes[1][1] = 4; c.shapes[1][2] = 16;

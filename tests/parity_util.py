@@ -186,7 +186,7 @@ def audio_stats_slack(w, n, tau):
 def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_bwd, rep,
                          heads, grad_scale="result"):
     """Steps 2 (permutation, pooling) to 5b of ``compare`` for given shapes."""
-    perm_o, inv_o, nval_o = orc.build_permutation(w_h, sid_use)
+    perm_o, inv_o, nval_o, tiles_o, nblk_o = orc.build_permutation(w_h, sid_use, table=True)
     assert np.array_equal(g["perm"].numpy()[:, hs], perm_o)
     assert np.array_equal(g["inv"].numpy()[:, hs], inv_o)
     assert np.array_equal(g["n_valid"].numpy()[:, hs], nval_o)
@@ -196,30 +196,43 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
     assert np.array_equal(f64(g["Qp"])[:, hs], Qp_o)
     assert np.array_equal(f64(g["Kp"])[:, hs], Kp_o)
     assert np.array_equal(f64(g["Vp"])[:, hs], Vp_o)
-    Qb_o = orc.pool(Qp_o, nval_o, w.block)
-    Kb_o = orc.pool(Kp_o, nval_o, w.block)
+    Qb_o = orc.pool_blocks(Qp_o, tiles_o, nblk_o, w.block)
+    Kb_o = orc.pool_blocks(Kp_o, tiles_o, nblk_o, w.block)
     Qb_g = (f64(g["Qbar"]) + f64(g["Qbar_lo"]))[:, hs]
     Kb_g = (f64(g["Kbar"]) + f64(g["Kbar_lo"]))[:, hs]
     assert np.abs(Qb_g - Qb_o).max() <= 1e-11 * max(1.0, np.abs(Qb_o).max())
     assert np.abs(Kb_g - Kb_o).max() <= 1e-11 * max(1.0, np.abs(Kb_o).max())
+    rep["multi_tile_blocks"] = int((tiles_o > 1).sum())
 
-    # ---- step 3+4: selection ----
+    # ---- step 3+4: selection (over blocks: their first tiles) ----
     Lg_all = gpu_lists(w, g, nb)
-    Lo, Fo = orc.select_blocks(w_h, Qb_o, Kb_o, nval_o, rows=rows)
+    Lo, Fo = orc.select_blocks(w_h, Qb_o, Kb_o, nblk_o, rows=rows)
     diff_rows = 0
     flagged = 0
     # The CUDA lists (equal to the oracle's on every unflagged row checked
-    # here) are the ones the attention steps of both sides use.
-    L_use = {(b, hi): Lg_all[(b, h)] for b in range(w.B) for hi, h in enumerate(hs)}
+    # here) are the ones the attention steps of both sides use.  With blocks
+    # that span several tiles the device lists are over tiles: the block list
+    # of a query block is read off its first tile (the first tiles of the
+    # listed tiles) and must expand back to the device list of every one of
+    # its tiles.
+    L_use = {}
     for b in range(w.B):
         for hi, h in enumerate(hs):
-            Lg = Lg_all[(b, h)]
+            Lg, tl = Lg_all[(b, h)], tiles_o[b, hi]
+            Lb = [None] * nb
+            for i in range(nb):
+                if tl[i] > 0:
+                    Lb[i] = Lg[i][tl[Lg[i]] > 0]
+            exp = orc.expand_lists(Lb, tl)
+            for i in range(nb):
+                assert np.array_equal(exp[i], Lg[i]), ("tile lists", b, h, i)
+            L_use[(b, hi)] = Lg
             lo_, fo = Lo[(b, hi)], Fo[(b, hi)]
             for i in range(nb):
-                if lo_[i] is None:
+                if lo_[i] is None or tl[i] == 0:
                     continue
                 flagged += int(fo[i])
-                if not np.array_equal(Lg[i], lo_[i]):
+                if not np.array_equal(Lb[i], lo_[i]):
                     assert fo[i], f"list differs on an unflagged row (b={b}, h={h}, i={i})"
                     diff_rows += 1
     L_fwd = {k: [L[i] if (rows is None or i in rows) else None for i in range(nb)]

@@ -194,3 +194,32 @@ def test_fused_a2v_pipeline(w):
     rep = {}
     pu.compare(w, fused_a2v=True, report=rep)
     print(w.name, rep)
+
+
+# --------------------------------------------------------------------------
+# block-size classes in one head (Table 11: C_128 and C_256; thresholds tau)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kw,kcb", [(dict(), 0), (dict(zone=(4, 16, 16), T=8), 0),
+                                    (dict(zone=(4, 16, 16), T=8), 16),
+                                    (dict(zone=(4, 16, 16), T=8, topp=0.5, topk_floor=2), 0)],
+                         ids=["3x16x16", "4x16x16", "4x16x16-key-ranges", "4x16x16-p0.5"])
+def test_mixed_block_classes(kw, kcb):
+    """128- and 256-token blocks mixed within each head, the class of every
+    zone from its complexity and the threshold, the shape from Eq. 7 in the
+    class; selection over blocks, attention over their tiles."""
+    # the small grid's zones sit higher (one source zone: large audio gates
+    # everywhere); 1.25 puts about half of them below the threshold
+    w = _w128(menu=synth.MENU_128 + synth.MENU_256, class_tau=(1.25,), **kw)
+    rep = {}
+    pu.compare(w, key_chunk_blocks=kcb, report=rep)
+    print(kw, kcb, rep)
+    assert rep["multi_tile_blocks"] > 0
+
+
+def test_mixed_block_classes_cuda_cores():
+    """The same on the CUDA-core kernels: 16- and 32-token blocks, d = 64."""
+    w = synth.WORKLOADS["tiny"].with_(menu=synth.MENU_TINY + ((2, 4, 4),), class_tau=(1.4,))
+    rep = {}
+    pu.compare(w, report=rep)
+    assert rep["multi_tile_blocks"] > 0

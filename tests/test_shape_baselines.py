@@ -97,3 +97,32 @@ def test_only_c64_menu():
     assert len(orc.admissible_shapes(w.menu, w.zone)) == 5
     rep = pu.compare(w)
     assert rep["O_max_rel"] <= pu.O_TOL
+
+
+def test_fixed_8cubed_512_token_blocks():
+    """Fixed 8^3 (Table 9): the single 512-token shape (8, 8, 8) on 8 x 16 x 16
+    zones; every block spans four 128-slot tiles of the tensor-core kernels."""
+    w = synth.WORKLOADS["720p"].with_(T=8, Hg=32, W=48, H=2, n_src=1, zone=(8, 16, 16),
+                                      menu=((8, 8, 8),), name="fixed8")
+    plan = prism.Plan(w)
+    assert plan.sz.tensor_core_fwd == 1 and plan.sz.multi_tile == 1
+    rep = pu.compare(w, shape_id=np.zeros((w.B, w.H, w.n_zones), np.uint8))
+    assert rep["multi_tile_blocks"] > 0
+
+
+def test_only_c256_menu():
+    """"Only C256" (Table 9): the 256-token class as the menu, shapes from the
+    statistics and Eq. 7 on 4 x 16 x 16 zones (two tiles per block)."""
+    w = synth.WORKLOADS["720p"].with_(T=8, Hg=40, W=48, H=2, n_src=1, zone=(4, 16, 16),
+                                      menu=synth.MENU_256, name="only_c256")
+    rep = pu.compare(w)
+    assert rep["multi_tile_blocks"] > 0
+
+
+def test_random_shapes_across_classes():
+    """Random shapes drawn from both the 128- and the 256-token menus: blocks
+    of one and of two tiles side by side in every head."""
+    w = _w_menu128(menu=synth.MENU_128 + synth.MENU_256, class_tau=(synth.TAU_256,))
+    sid = _random_shapes(w, 11)
+    rep = pu.compare(w, shape_id=sid)
+    assert rep["multi_tile_blocks"] > 0
