@@ -262,6 +262,19 @@ def zone_class(c: float, taus: Sequence[float]) -> int:
     return sum(1 for t in taus if c < t)
 
 
+def zone_class_tokens(w, classes, cz: float, taus, n_real: float) -> int:
+    """Token count of a zone's class.  READING: a class smaller than the
+    tile (w.block, the tensor cores' row tile; two such blocks share one) is
+    taken only by zones without padding, so that both halves of every shared
+    tile are real; a zone with padding takes the smallest class of at least
+    a tile instead."""
+    S = classes[zone_class(cz, taus)]
+    vol = w.zone[0] * w.zone[1] * w.zone[2]
+    if S < w.block and n_real < vol:
+        S = min(c for c in classes if c >= w.block)
+    return S
+
+
 def assign_shapes(w, stats: np.ndarray):
     """Shape id per (b, h, zone) -> (shape_id [B,H,Z] int, near_tie [B,H,Z] bool).
 
@@ -290,7 +303,7 @@ def assign_shapes(w, stats: np.ndarray):
             nmax = st_h[:, 6].max()
             cz = zone_complexity(w, st_h) if taus else np.zeros(Z)
             for z in range(Z):
-                S = classes[zone_class(cz[z], taus)]
+                S = zone_class_tokens(w, classes, cz[z], taus, st_h[z][7])
                 costs, idx = shape_costs(w, guidance(w, st_h[z], nmax), S)
                 k = int(np.argmin(costs))            # first minimum = lowest menu index
                 sid[b, h, z] = idx[k]
@@ -392,10 +405,16 @@ def norm_sensitive_zones(w, n: np.ndarray, stats: np.ndarray, tau: float) -> np.
             nmax = st_h[:, 6].max()
             cz = zone_complexity(w, st_h) if taus else np.zeros(Z)
             for z in range(Z):
-                S = classes[zone_class(cz[z], taus)]
+                S = zone_class_tokens(w, classes, cz[z], taus, st_h[z][7])
                 flags[b, h, z] = _shape_decision_reachable(w, st_h[z], nmax, dv[z], tau, S,
                                                            cz[z])
     return flags
+
+
+def slot_tokens(w) -> int:
+    """Granularity of the block table: the tile (w.block), or half of it when
+    the menu has a class of half a tile."""
+    return min([w.block] + menu_classes(w.menu))
 
 
 def build_permutation(w, shape_id: np.ndarray, table: bool = False):
@@ -406,24 +425,27 @@ def build_permutation(w, shape_id: np.ndarray, table: bool = False):
     READING (Prism, Abstract: tokens inside a block stay together; the pages do
     not give an order).  A block of S tokens fills S / w.block consecutive
     tiles of w.block slots (one tile when the menu has a single class of
-    w.block tokens).  Returns perm [B,H,Np] (slot -> real token, -1 for a
-    padding slot), inv [B,H,N] (token -> slot), n_valid [B,H,nb] (real tokens
-    in each tile: a block's real tokens sit at its start, so they fill its
-    first tiles); with ``table`` also tiles [B,H,nb] (a block's tile count at
-    its first tile, 0 on the tiles that continue it) and n_block [B,H,nb] (a
-    block's real tokens at its first tile, 0 elsewhere)."""
+    w.block tokens; two blocks of half a tile share one).  Returns perm
+    [B,H,Np] (slot -> real token, -1 for a padding slot), inv [B,H,N]
+    (token -> slot), n_valid [B,H,nb] (real tokens in each tile: a block's
+    real tokens sit at its start, so they fill its first tiles); with
+    ``table`` also, per unit of ``slot_tokens(w)`` tokens, units [B,H,nu]
+    (a block's unit count at its first unit, 0 on the units that continue
+    it) and n_block [B,H,nu] (a block's real tokens at its first unit, 0
+    elsewhere)."""
     B, H, Z = shape_id.shape
     Tp, Hp, Wp = padded_grid(w.T, w.Hg, w.W, w.zone)
     zT, zH, zW = w.zone
     nzT, nzH, nzW = Tp // zT, Hp // zH, Wp // zW
     T_ = w.block
+    U = slot_tokens(w)
     Np = Tp * Hp * Wp
     nb = Np // T_
     perm = np.full((B, H, Np), -1, dtype=np.int64)
     inv = np.full((B, H, w.N), -1, dtype=np.int64)
     nvalid = np.zeros((B, H, nb), dtype=np.int64)
-    tiles = np.zeros((B, H, nb), dtype=np.int64)
-    nblock = np.zeros((B, H, nb), dtype=np.int64)
+    units = np.zeros((B, H, Np // U), dtype=np.int64)
+    nblock = np.zeros((B, H, Np // U), dtype=np.int64)
     for b in range(B):
         for h in range(H):
             slot = 0
@@ -446,21 +468,21 @@ def build_permutation(w, shape_id: np.ndarray, table: bool = False):
                             for k, n in enumerate(toks):
                                 perm[b, h, slot + k] = n
                                 inv[b, h, n] = slot + k
-                            t0 = slot // T_
-                            tiles[b, h, t0] = S // T_
-                            nblock[b, h, t0] = len(toks)
-                            for q in range(S // T_):
-                                nvalid[b, h, t0 + q] = min(T_, max(0, len(toks) - q * T_))
+                            units[b, h, slot // U] = S // U
+                            nblock[b, h, slot // U] = len(toks)
                             slot += S
+            for t in range(nb):
+                nvalid[b, h, t] = int((perm[b, h, t * T_:(t + 1) * T_] >= 0).sum())
     if table:
-        return perm, inv, nvalid, tiles, nblock
+        return perm, inv, nvalid, units, nblock
     return perm, inv, nvalid
 
 
 def pool_blocks(Xp: np.ndarray, tiles: np.ndarray, n_block: np.ndarray, T_: int) -> np.ndarray:
-    """Block-level feature of blocks that span one or more tiles: the mean of
-    the block's real tokens (its first n_block slots), stored at its first
-    tile; 0 on continuation tiles and for blocks without real tokens."""
+    """Block-level feature of blocks that span one or more units of T_
+    slots: the mean of the block's real tokens (its first n_block slots),
+    stored at its first unit; 0 on continuation units and for blocks without
+    real tokens."""
     B, H, Np, d = Xp.shape
     nb = Np // T_
     out = np.zeros((B, H, nb, d), dtype=f64)
@@ -471,6 +493,95 @@ def pool_blocks(Xp: np.ndarray, tiles: np.ndarray, n_block: np.ndarray, T_: int)
                 if tiles[b, h, i] > 0 and nv > 0:
                     out[b, h, i] = Xp[b, h, i * T_:i * T_ + nv].sum(axis=0) / nv
     return out
+
+
+def expand_lists_masked(L, units: np.ndarray, U: int, T_: int):
+    """Block lists over first units (of U slots) -> lists over tiles of T_ =
+    2U slots with, per entry, a 4-bit mask of the sub-tile pairs that are NOT
+    selected: bit 2 qh + kh for the query tile's half qh and the key tile's
+    half kh (0: the whole tile pair is selected).  A tile pair is listed when
+    any of its four halves is selected."""
+    per = T_ // U
+    nu = len(units)
+    nt = nu // per
+    start = np.zeros(nu, dtype=np.int64)                 # first unit of every unit's block
+    i = 0
+    while i < nu:
+        n = max(1, int(units[i]))
+        start[i:i + n] = i
+        i += n
+    sel = [set() if L[int(start[u])] is None else set(int(j) for j in L[int(start[u])])
+           for u in range(nu)]
+    lists, masks = [], []
+    for t in range(nt):
+        cols, ms = [], []
+        for v in range(nt):
+            bits = 0
+            for qh in range(per):
+                for kh in range(per):
+                    if int(start[v * per + kh]) in sel[t * per + qh]:
+                        bits |= 1 << (qh * per + kh)
+            if bits:
+                cols.append(v)
+                ms.append((~bits) & ((1 << (per * per)) - 1))
+        lists.append(np.array(cols, dtype=np.int64))
+        masks.append(np.array(ms, dtype=np.int64))
+    return lists, masks
+
+
+def _rows_of(Xp_bh, blocks, U, n_block_bh):
+    """Real rows of the given blocks (first units), concatenated in order."""
+    return np.concatenate([Xp_bh[int(j) * U: int(j) * U + int(n_block_bh[int(j)])] for j in blocks],
+                          axis=0)
+
+
+def attn_blocks(Qp, Kp, Vp, units, n_block, L, U, scale, dOp=None, o_bf16=False):
+    """Block-sparse attention at block level for blocks of any size (units of
+    U slots): every real query token of block i attends to every real token of
+    the blocks in L[(b, h)][i] (Prism, Fig. 2 caption; readings as
+    ``attn_fwd_row``), and with dOp its VJP (as ``attn_bwd_row``; ``o_bf16``
+    forms D from O rounded to bf16).  Returns (Op, lse) or
+    (Op, lse, dQp, dKp, dVp), all in the permuted layout."""
+    B, H, Np, d = Qp.shape
+    Op = np.zeros((B, H, Np, d), dtype=f64)
+    lse = np.zeros((B, H, Np), dtype=f64)
+    if dOp is not None:
+        dQ, dK, dV = (np.zeros((B, H, Np, d), dtype=f64) for _ in range(3))
+    for (b, h), Lbh in L.items():
+        nb_ = n_block[b, h]
+        for i, sel in enumerate(Lbh):
+            if sel is None or len(sel) == 0 or units[b, h, i] == 0 or nb_[i] == 0:
+                continue
+            r0, nq = i * U, int(nb_[i])
+            q = Qp[b, h, r0:r0 + nq].astype(f64)
+            k = _rows_of(Kp[b, h], sel, U, nb_).astype(f64)
+            v = _rows_of(Vp[b, h], sel, U, nb_).astype(f64)
+            s = (q @ k.T) * scale
+            mx = s.max(axis=1, keepdims=True)
+            e = np.exp(s - mx)
+            l = e.sum(axis=1, keepdims=True)
+            P = e / l
+            o = P @ v
+            Op[b, h, r0:r0 + nq] = o
+            lse[b, h, r0:r0 + nq] = (mx + np.log(l))[:, 0]
+            if dOp is None:
+                continue
+            do = dOp[b, h, r0:r0 + nq].astype(f64)
+            dv = P.T @ do
+            dP = do @ v.T
+            Dr = (do * (round_bf16(o) if o_bf16 else o)).sum(axis=1, keepdims=True)
+            dS = P * (dP - Dr)
+            dQ[b, h, r0:r0 + nq] = (dS @ k) * scale
+            dk = (dS.T @ q) * scale
+            off = 0
+            for j in sel:
+                nv = int(nb_[int(j)])
+                dK[b, h, int(j) * U:int(j) * U + nv] += dk[off:off + nv]
+                dV[b, h, int(j) * U:int(j) * U + nv] += dv[off:off + nv]
+                off += nv
+    if dOp is None:
+        return Op, lse
+    return Op, lse, dQ, dK, dV
 
 
 def expand_lists(L, tiles: np.ndarray):
@@ -874,23 +985,39 @@ def run(w, Q, K, V, a2v, dO=None, heads=None):
     every intermediate and output in float64 / int64.  Blocks of a class
     larger than w.block span several tiles: selection runs over blocks
     (their first tiles), and the attention over the tiles of the selected
-    blocks (``expand_lists``)."""
+    blocks (``expand_lists``).  With a class of half a tile the block table
+    is kept per half tile, the attention runs at block level
+    (``attn_blocks``) and ``lists`` holds the tile lists with their sub-tile
+    masks (``expand_lists_masked``)."""
     stats = zone_stats(w, V, a2v)
     sid, stie = assign_shapes(w, stats)
     perm, inv, nval, tiles, nblk = build_permutation(w, sid, table=True)
+    U = slot_tokens(w)
     Qp, Kp, Vp = permute(Q, perm), permute(K, perm), permute(V, perm)
-    Qb, Kb = pool_blocks(Qp, tiles, nblk, w.block), pool_blocks(Kp, tiles, nblk, w.block)
+    Qb, Kb = pool_blocks(Qp, tiles, nblk, U), pool_blocks(Kp, tiles, nblk, U)
     blists, flags = select_blocks(w, Qb, Kb, nblk, heads=heads)
-    lists = {(b, h): expand_lists(L, tiles[b, h]) for (b, h), L in blists.items()}
     scale = 1.0 / math.sqrt(w.d)
-    Op, lse = attn_fwd(w, Qp, Kp, Vp, nval, lists, scale)
+    if U < w.block:
+        # blocks of half a tile: attention at block level; the tile lists with
+        # their sub-tile masks are what the tensor-core kernels walk
+        lists = {(b, h): expand_lists_masked(L, tiles[b, h], U, w.block)
+                 for (b, h), L in blists.items()}
+        dOp = permute(dO, perm) if dO is not None else None
+        r = attn_blocks(Qp, Kp, Vp, tiles, nblk, blists, U, scale, dOp=dOp)
+        Op, lse = r[0], r[1]
+    else:
+        lists = {(b, h): expand_lists(L, tiles[b, h]) for (b, h), L in blists.items()}
+        Op, lse = attn_fwd(w, Qp, Kp, Vp, nval, lists, scale)
     res = dict(stats=stats, shape_id=sid, shape_tie=stie, perm=perm, inv=inv, n_valid=nval,
                tiles=tiles, n_block=nblk, Qp=Qp, Kp=Kp, Vp=Vp, Qbar=Qb, Kbar=Kb,
                block_lists=blists, lists=lists, flags=flags, Op=Op, lse=lse,
                O=unpermute(Op, inv), scale=scale)
     if dO is not None:
-        dOp = permute(dO, perm)
-        dQp, dKp, dVp = attn_bwd(w, Qp, Kp, Vp, dOp, nval, lists, scale)
+        if U < w.block:
+            dQp, dKp, dVp = r[2], r[3], r[4]
+        else:
+            dOp = permute(dO, perm)
+            dQp, dKp, dVp = attn_bwd(w, Qp, Kp, Vp, dOp, nval, lists, scale)
         res.update(dOp=dOp, dQp=dQp, dKp=dKp, dVp=dVp, dQ=unpermute(dQp, inv),
                    dK=unpermute(dKp, inv), dV=unpermute(dVp, inv))
     return res

@@ -326,6 +326,90 @@ def test_mixed_class_path_equals_brute_force_masked_attention():
         assert np.abs(dV - r["dV"][0, :, h]).max() <= 1e-11
 
 
+def _tiny_mc3(**kw):
+    """tiny with three classes: 8-token blocks (half a 16-slot tile), the
+    16-token menu and (2,4,4); the 4 x 8 x 8 grid has no padding."""
+    half = ((1, 2, 4), (2, 2, 2), (1, 4, 2), (2, 1, 4), (2, 4, 1))
+    return synth.WORKLOADS["tiny"].with_(menu=half + synth.MENU_TINY + ((2, 4, 4),),
+                                         class_tau=(1.6, 1.3), **kw)
+
+
+def test_block_level_attention_equals_tile_level_attention():
+    """attn_blocks (blocks of any size, at block level) equals the tile-level
+    forward and backward over the expanded lists, for one class and for
+    blocks of one and two tiles."""
+    for w in (synth.WORKLOADS["tiny"], _tiny_mc()):
+        x = _tiny_inputs(w)
+        r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"], dO=x["dO"])
+        U = orc.slot_tokens(w)
+        assert U == w.block
+        Op, lse, dQ, dK, dV = orc.attn_blocks(r["Qp"], r["Kp"], r["Vp"], r["tiles"], r["n_block"],
+                                              r["block_lists"], U, r["scale"], dOp=r["dOp"])
+        for a, b_ in ((Op, r["Op"]), (dQ, r["dQp"]), (dK, r["dKp"]), (dV, r["dVp"])):
+            np.testing.assert_allclose(a, b_, atol=1e-12)
+        np.testing.assert_allclose(lse, r["lse"], atol=1e-12)
+
+
+def test_half_tile_blocks_equal_brute_force_masked_attention():
+    """Three classes, one of them half a tile: the block-level path equals
+    masked attention whose token mask comes from the block lists (forward and
+    backward, original order), and the masked tile lists describe the same
+    token pairs."""
+    w = _tiny_mc3()
+    x = _tiny_inputs(w)
+    r = orc.run(w, x["Q"], x["K"], x["V"], x["a2v"], dO=x["dO"])
+    U, T_ = orc.slot_tokens(w), w.block
+    assert U == T_ // 2
+    sizes = set((r["tiles"] * U)[r["tiles"] > 0].tolist())
+    assert sizes == {8, 16, 32}, sizes
+    for h in range(w.H):
+        perm, units, L = r["perm"][0, h], r["tiles"][0, h], r["block_lists"][(0, h)]
+        blk_of = np.zeros(w.N, dtype=np.int64)           # token -> first unit of its block
+        i = 0
+        while i < len(units):
+            n = int(units[i])
+            toks = perm[i * U:(i + n) * U]
+            blk_of[toks[toks >= 0]] = i
+            i += n
+        mask = np.zeros((w.N, w.N), bool)
+        for q in range(w.N):
+            mask[q] = np.isin(blk_of, L[blk_of[q]])
+        O, dQ, dK, dV = orc.masked_attention(x["Q"][0, :, h], x["K"][0, :, h], x["V"][0, :, h],
+                                             mask, r["scale"], dO=x["dO"][0, :, h])
+        assert np.abs(O - r["O"][0, :, h]).max() <= 1e-12
+        assert np.abs(dQ - r["dQ"][0, :, h]).max() <= 1e-11
+        assert np.abs(dK - r["dK"][0, :, h]).max() <= 1e-11
+        assert np.abs(dV - r["dV"][0, :, h]).max() <= 1e-11
+        # tile lists with masks: (tile t half qh, tile v half kh) is selected
+        # exactly when a token there may attend a token there
+        tl, tm = r["lists"][(0, h)]
+        tok_slot = np.zeros(w.N, dtype=np.int64)
+        tok_slot[perm[perm >= 0]] = np.nonzero(perm >= 0)[0]
+        for t in range(len(tl)):
+            for v, mbits in zip(tl[t], tm[t]):
+                for qh in range(2):
+                    for kh in range(2):
+                        qs = perm[t * T_ + qh * U:t * T_ + (qh + 1) * U]
+                        ks = perm[v * T_ + kh * U:v * T_ + (kh + 1) * U]
+                        qs, ks = qs[qs >= 0], ks[ks >= 0]
+                        want = bool(mask[np.ix_(qs, ks)].any()) if len(qs) and len(ks) else False
+                        assert want == (not (mbits >> (qh * 2 + kh)) & 1), (t, v, qh, kh)
+        nsel = sum(len(a) for a in tl)
+        assert nsel > 0 and any((m > 0).any() for m in tm if len(m))
+
+
+def test_padded_zones_skip_the_half_tile_class():
+    """A zone with padding never takes a class smaller than the tile."""
+    w = _tiny_mc3(T=5, Hg=7, W=9)
+    x = _tiny_inputs(w)
+    st = orc.zone_stats(w, x["V"], x["a2v"])
+    sid, _ = orc.assign_shapes(w, st)
+    vol = w.zone[0] * w.zone[1] * w.zone[2]
+    small = np.array([np.prod(w.menu[k]) < w.block for k in sid.ravel()]).reshape(sid.shape)
+    assert small.any()
+    assert not (small & (st[..., 7] < vol)).any()
+
+
 # ------------------------------------------------ A2V cross-attention -------
 
 def test_a2v_norms_special_cases():
