@@ -118,17 +118,21 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   if (lS < 2 || c.block_tokens > 128) return PRISM_ERR_UNSUPPORTED;
   if (c.d * c.block_tokens > 16384) return PRISM_ERR_UNSUPPORTED;
   // block-size classes: the menu's token counts, each 1, 2 or 4 tiles
-  int classes[PRISM_MAX_CLASSES];
+  int classes[PRISM_MAX_CLASSES + 1];
   int n_classes = 0;
   for (int k = 0; k < c.n_shapes; ++k) {
     const int* s = c.shapes[k];
     if (s[0] < 1 || s[1] < 1 || s[2] < 1) return PRISM_ERR_ARG;
     const int t = s[0] * s[1] * s[2];
-    if (t != c.block_tokens && t != 2 * c.block_tokens && t != 4 * c.block_tokens)
+    if (2 * t != c.block_tokens && t != c.block_tokens && t != 2 * c.block_tokens &&
+        t != 4 * c.block_tokens)
       return PRISM_ERR_UNSUPPORTED;
     bool seen = false;
     for (int q = 0; q < n_classes; ++q) seen |= classes[q] == t;
-    if (!seen) classes[n_classes++] = t;
+    if (!seen) {
+      if (n_classes == PRISM_MAX_CLASSES) return PRISM_ERR_UNSUPPORTED;
+      classes[n_classes++] = t;
+    }
   }
   for (int a = 1; a < n_classes; ++a)  // ascending
     for (int q = a; q > 0 && classes[q - 1] > classes[q]; --q) {
@@ -171,19 +175,24 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
     }
     if (!any) return PRISM_ERR_NO_ADMISSIBLE_SHAPE;
   }
-  z.multi_tile = classes[n_classes - 1] > c.block_tokens ? 1 : 0;
+  z.half_tile = 2 * classes[0] == c.block_tokens ? 1 : 0;
+  z.multi_tile = (classes[n_classes - 1] > c.block_tokens || z.half_tile) ? 1 : 0;
+  z.slot_tokens = z.half_tile ? c.block_tokens / 2 : c.block_tokens;
   z.blocks_per_zone = static_cast<int>(vol / c.block_tokens);
   const long long nb = z.Np / c.block_tokens;
   if (nb > 8192 || z.Np >= (1LL << 31) || z.N >= (1LL << 31)) return PRISM_ERR_UNSUPPORTED;
   z.nb = static_cast<int>(nb);
+  z.nslots = static_cast<int>(z.Np / z.slot_tokens);
   const long long rows = static_cast<long long>(c.B) * c.H * nb;
+  const long long srows = static_cast<long long>(c.B) * c.H * z.nslots;  // selection rows
   z.max_pairs = rows * nb;
-  if (z.max_pairs >= (1LL << 31)) return PRISM_ERR_UNSUPPORTED;
+  if (z.max_pairs >= (1LL << 31) || srows * z.nslots >= (1LL << 31)) return PRISM_ERR_UNSUPPORTED;
   {
     const bool tc_shape = c.block_tokens == 128 && c.d == 128 && c.attn_kernel == 0;
     z.tensor_core_fwd = tc_shape ? 1 : 0;
     z.tensor_core_bwd = tc_shape ? 1 : 0;
   }
+  if (z.half_tile && !z.tensor_core_fwd) return PRISM_ERR_UNSUPPORTED;
   if (c.attn_kernel < 0 || c.attn_kernel > 1) return PRISM_ERR_ARG;
   for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
     for (int a = 0; a < 3; ++a) {
@@ -192,14 +201,15 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
       p.log2_ext[k][a] = l >= 0 ? static_cast<double>(l) : log2(static_cast<double>(e));
     }
   p.log2_S = static_cast<double>(lS);
-  // workspace layout
+  // workspace layout (the selection runs over slots: tiles, or half tiles)
   const int nwords = (z.nb + 31) / 32;
+  const int swords = (z.nslots + 31) / 32;
   size_t off = 256;
-  p.off_rowcnt = off; off = align256(off + rows * 4);
-  p.off_colcnt = off; off = align256(off + rows * 4);
-  p.off_amb = off; off = align256(off + rows * 4);
-  p.off_bitmask = off; off = align256(off + rows * nwords * 4);
-  p.off_scores = off; off = align256(off + 2 * rows * nb * 4);
+  p.off_rowcnt = off; off = align256(off + srows * 4);
+  p.off_colcnt = off; off = align256(off + srows * 4);
+  p.off_amb = off; off = align256(off + srows * 4);
+  p.off_bitmask = off; off = align256(off + srows * swords * 4);
+  p.off_scores = off; off = align256(off + 2 * srows * z.nslots * 4);
   p.off_D = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
   p.off_lse2 = off; off = align256(off + static_cast<size_t>(c.B) * c.H * z.Np * 4);
   p.off_dq = off;
@@ -207,10 +217,16 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
   // multi-tile blocks: real tokens per block at its first tile, first tile of
   // every tile's block, and the tile-level selection bitmask
   p.off_nsel = p.off_bstart = p.off_tbitmask = off;
+  z.ws_csr_mask = z.ws_csc_mask = 0;
   if (z.multi_tile) {
-    p.off_nsel = off; off = align256(off + rows * 4);
-    p.off_bstart = off; off = align256(off + rows * 4);
+    p.off_nsel = off; off = align256(off + srows * 4);
+    p.off_bstart = off; off = align256(off + srows * 4);
     p.off_tbitmask = off; off = align256(off + rows * nwords * 4);
+  }
+  if (z.half_tile) {
+    // sub-tile masks of the tile lists (one byte per CSR / CSC entry)
+    z.ws_csr_mask = off; off = align256(off + static_cast<size_t>(z.max_pairs));
+    z.ws_csc_mask = off; off = align256(off + static_cast<size_t>(z.max_pairs));
   }
   // key ranges of at most 512 blocks (32 MB of K and V per head) once a head's
   // K and V outgrow L2; the partial results are capped at 32 GB

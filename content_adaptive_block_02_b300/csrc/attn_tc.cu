@@ -86,6 +86,7 @@ struct FwdParams {
   float scale_log2;
   unsigned long long limit;
   int starve;  // fault injection (test only): the producer issues no loads
+  const uint8_t* mask;  // blocks of half a tile: sub-tile mask per CSR entry (else null)
 };
 
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -341,11 +342,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int32_t* cols = P.col_idx + beg;
       int nvk_next = nvb[cols[0]];
       int j_next2 = n > 1 ? cols[1] : 0;
+      // blocks of half a tile: bit 2 qh + kh of an entry's mask set = this
+      // row half (qh) does not attend that key half (kh = this column half)
+      const int mbit = (quarter >> 1) * 2 + half;
       for (int jj = 0; jj < n; ++jj) {
         const int nvk = nvk_next;
         if (jj + 1 < n) nvk_next = nvb[j_next2];
         if (jj + 2 < n) j_next2 = cols[jj + 2];
-        const int lim = nvk - c0;  // columns of this half that hold real keys
+        const bool act = P.mask == nullptr || !((P.mask[beg + jj] >> mbit) & 1);
+        const int lim = act ? nvk - c0 : 0;  // columns of this half that hold real keys
         // wait results are made warp-uniform: the TMEM loads and stores
         // below are warp-collective
         ok = __all_sync(0xffffffffu, ok && (s_ready || W.wait(&sm.s_full, sidx & 1, 11)));
@@ -447,11 +452,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (ok) {
         fence_after();
         const float m0 = sm.xm[0][r], m1 = sm.xm[1][r];
-        const float M = fmaxf(m0, m1);  // finite: half 0 holds a real key of every block
-        const float a0 = ex2(m0 - M), a1 = ex2(m1 - M);
+        const float M = fmaxf(m0, m1);
+        // no key at all for this row in this item (possible only with
+        // sub-tile masks, within one key range): O = 0, weight 0
+        const bool none = !(M > -INFINITY);
+        const float a0 = none ? 0.f : ex2(m0 - M), a1 = none ? 0.f : ex2(m1 - M);
         const float lt = sm.xl[0][r] * a0 + sm.xl[1][r] * a1;
         const bool real = r < nvq;
-        const float inv = real ? 1.f / lt : 0.f;
+        const float inv = (real && !none) ? 1.f / lt : 0.f;
         const float w0 = a0 * inv, w1 = a1 * inv;
         const uint32_t tO0 = tmem + lane_base + TM_O0 + c0, tO1 = tmem + lane_base + TM_O1 + c0;
 #pragma unroll
@@ -476,9 +484,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         if (half == 0) {
           if (P.chunks == 1)
-            P.lse[grow] = real ? (M + log2f(lt)) * 0.69314718055994531f : 0.f;
+            P.lse[grow] = (real && !none) ? (M + log2f(lt)) * 0.69314718055994531f : 0.f;
           else
-            reinterpret_cast<float2*>(P.ml)[prow] = make_float2(M, lt);
+            reinterpret_cast<float2*>(P.ml)[prow] = make_float2(M, none ? 0.f : lt);
         }
       }
       // both halves have read O_0, O_1, xm and xl before either moves on
@@ -568,6 +576,7 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   a.scale_log2 = scale * 1.4426950408889634f;
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
   a.starve = c.fault_inject == PRISM_FAULT_STARVE_LOADS ? 1 : 0;
+  a.mask = p.sz.half_tile ? ws + p.sz.ws_csr_mask : nullptr;
   cudaError_t e = cudaMemsetAsync(a.status + WS_FWD_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   const size_t smem = 2ull * kStages * kTile + 1024;  // K + V per stage

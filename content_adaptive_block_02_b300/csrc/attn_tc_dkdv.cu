@@ -81,6 +81,7 @@ struct BwdParams {
   float scale, scale_log2;
   unsigned long long limit;
   int starve;  // fault injection (test only): the producer issues no loads
+  const uint8_t* mask;  // blocks of half a tile: sub-tile mask per CSC entry (else null)
 };
 
 // 14 warps: 3-4 per SM sub-partition, so at most 128 registers per thread.
@@ -346,7 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s_ = (use + k) & 1;
         // LSE_i and D_i arrive with Q_i / dO_i on the stage's barrier
         ok = ok && W.wait(&sm.qdo_full[s_], ((use + k) >> 1) & 1, 40);
-        const int lim = (r < nvk) ? sm.stage_nvq[s_] - q0 : 0;  // real query columns here
+        // blocks of half a tile: bit 2 qh + kh of an entry's mask set = the
+        // query half qh (this column half) does not attend the key half kh
+        // (this row's half)
+        const bool act =
+            P.mask == nullptr || !((P.mask[beg + k] >> (half * 2 + (quarter >> 1))) & 1);
+        const int lim = (r < nvk && act) ? sm.stage_nvq[s_] - q0 : 0;  // real query columns here
         const float4* lse4 = reinterpret_cast<const float4*>(stage(s_) + 2 * kTile) + half * 16;
         const float4* D4 = lse4 + 32;
         // ---- P^T = exp(S^T * scale - LSE) on this half of the queries ----
@@ -505,6 +511,7 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
   a.scale_log2 = scale * 1.4426950408889634f;
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
   a.starve = c.fault_inject == PRISM_FAULT_STARVE_LOADS ? 1 : 0;
+  a.mask = (p.sz.half_tile && ws != nullptr) ? ws + p.sz.ws_csc_mask : nullptr;
   cudaError_t e = cudaMemsetAsync(a.status + WS_BWD_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -72,6 +72,7 @@ struct DqParams {
   float scale, scale_log2;
   unsigned long long limit;
   int starve;  // fault injection (test only): the producer issues no loads
+  const uint8_t* mask;  // blocks of half a tile: sub-tile mask per CSR entry (else null)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -313,12 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* cols = P.col_idx + beg;
       int nvk_next = nvb[cols[0]];
       int j_next2 = n > 1 ? cols[1] : 0;
+      // blocks of half a tile: bit 2 qh + kh of an entry's mask set = this
+      // row half (qh) does not attend that key half (kh = this column half)
+      const int mbit = (quarter >> 1) * 2 + half;
       bool ok = true;
       for (int jj = 0; jj < n; ++jj) {
         const int nvk = nvk_next;
         if (jj + 1 < n) nvk_next = nvb[j_next2];
         if (jj + 2 < n) j_next2 = cols[jj + 2];
-        const int lim = real ? nvk - c0 : 0;  // real key columns of this half
+        const bool act = P.mask == nullptr || !((P.mask[beg + jj] >> mbit) & 1);
+        const int lim = (real && act) ? nvk - c0 : 0;  // real key columns of this half
         // wait results are made warp-uniform: TMEM loads and stores are
         // warp-collective
         if (!__all_sync(0xffffffffu, W.wait(&sm.s_full, sidx & 1, 82))) { ok = false; break; }
@@ -439,6 +444,7 @@ cudaError_t launch_attn_dq_tc(const Plan& p, const uint16_t* Qp, const uint16_t*
   a.scale_log2 = scale * 1.4426950408889634f;
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
   a.starve = c.fault_inject == PRISM_FAULT_STARVE_LOADS ? 1 : 0;
+  a.mask = (p.sz.half_tile && ws != nullptr) ? ws + p.sz.ws_csr_mask : nullptr;
   cudaError_t e = cudaMemsetAsync(a.status + WS_DQ_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -96,6 +96,8 @@ extern "C" int prism_sparse_attn_bwd_noalloc(
     if (!al16(q)) return PRISM_ERR_ALIGN;
   }
   const prism::Plan& p = plan->p;
+  // blocks of half a tile: the sub-tile masks live in the plan's workspace
+  if (p.sz.half_tile) return PRISM_ERR_UNSUPPORTED;
   // layout inside the scratch: status words, D, then LSE * log2(e) for the
   // tensor-core kernels or the fp32 dQ accumulator for the CUDA-core ones
   const size_t rows = static_cast<size_t>(p.cfg.B) * p.cfg.H * p.sz.Np;

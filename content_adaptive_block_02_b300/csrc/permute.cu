@@ -64,8 +64,8 @@ constexpr int kPermThreads = 256;
 // double-float division by the real-token count -- about 46 significant
 // bits, without fp64 arithmetic.
 __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
-    prism_config_t c, int nzH, int nzW, int bpz, int Z, int nb, long long Np, Menu menu,
-    const uint8_t* __restrict__ shape_id, const uint16_t* __restrict__ Q,
+    prism_config_t c, int nzH, int nzW, int bpz, int Z, int nb, int nslots, int U, long long Np,
+    Menu menu, const uint8_t* __restrict__ shape_id, const uint16_t* __restrict__ Q,
     const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, uint16_t* __restrict__ Qp, uint16_t* __restrict__ Kp,
     uint16_t* __restrict__ Vp, float* __restrict__ Qh, float* __restrict__ Ql,
@@ -74,34 +74,37 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
   extern __shared__ __align__(16) float2 red2[];
   const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;  // heads fastest: the heads
                                                                  // of a block share token rows
-  const int S = c.block_tokens, d = c.d, P = d / 8;  // S: tile slots
+  const int S = c.block_tokens, d = c.d, P = d / 8;  // S: tile slots; U: table unit slots
   const int G = kPermThreads / P;  // tokens handled per pass
   const int q = threadIdx.x % P, grp = threadIdx.x / P;
   const long long N = static_cast<long long>(c.T) * c.Hg * c.W;
   const long long bh = static_cast<long long>(b) * c.H + h;
-  const int z = blk / bpz, lt = blk % bpz;  // bpz: tiles per zone
+  const int z = blk / bpz, lu = blk % bpz;  // bpz: units per zone
   int sid = shape_id[bh * Z + z];
   if (sid >= PRISM_MAX_SHAPES || !((menu.adm_mask >> sid) & 1u)) {
     // a caller-given shape that does not tile the zone: report, fall back
-    if (status != nullptr && threadIdx.x == 0 && lt == 0)
+    if (status != nullptr && threadIdx.x == 0 && lu == 0)
       dev_error(status, DEV_ERR_BOUNDS, 0x5A1, static_cast<uint32_t>(sid));
     sid = menu.first_adm;
   }
   const int SB = menu.ext[sid][0] * menu.ext[sid][1] * menu.ext[sid][2];  // block tokens
-  const int tpb = SB / S;                                                   // tiles per block
-  if (lt % tpb != 0) return;  // written by the CTA of the block's first tile
-  const BlockGeom g = block_geom(c, nzH, nzW, menu, sid, z, lt / tpb);
+  const int upb = SB / U;                                                   // units per block
+  if (lu % upb != 0) return;  // written by the CTA of the block's first unit
+  const BlockGeom g = block_geom(c, nzH, nzW, menu, sid, z, lu / upb);
   const int nv = g.et * g.ey * g.ex;
+  if (SB < S && nv < SB && status != nullptr && threadIdx.x == 0)
+    // a block of half a tile must be full (its tile's halves are both real)
+    dev_error(status, DEV_ERR_BOUNDS, 0x5A2, static_cast<uint32_t>(sid));
   df sq[8], sk[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) sq[k] = sk[k] = df{0.f, 0.f};
-  const long long slot0 = static_cast<long long>(blk) * S;
-  constexpr int U = 4;  // tokens per thread in flight
-  for (int k0 = grp; k0 < SB; k0 += U * G) {
-    uint4 vq[U], vk[U], vv[U];
-    long long nn[U];
+  const long long slot0 = static_cast<long long>(blk) * U;
+  constexpr int IF = 4;  // tokens per thread in flight
+  for (int k0 = grp; k0 < SB; k0 += IF * G) {
+    uint4 vq[IF], vk[IF], vv[IF];
+    long long nn[IF];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < IF; ++u) {
       const int k = k0 + u * G;
       vq[u] = vk[u] = vv[u] = make_uint4(0, 0, 0, 0);
       nn[u] = -1;
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < IF; ++u) {
       const int k = k0 + u * G;
       if (k >= SB) break;
       const long long dst = (bh * Np + slot0 + k) * d + q * 8;
@@ -155,8 +158,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
     df s = {0.f, 0.f};
     for (int j = 0; j < G; ++j) s = df_add(s, df{r[j * d + cc].x, r[j * d + cc].y});
     const df mean = nv > 0 ? df_div_int(s, nv) : df{0.f, 0.f};
-    for (int t = 0; t < tpb; ++t) {
-      const long long o = (bh * nb + blk + t) * d + cc;
+    for (int t = 0; t < upb; ++t) {
+      const long long o = (bh * nslots + blk + t) * d + cc;
       const df v = t == 0 ? mean : df{0.f, 0.f};
       if (ch < d) {
         Qh[o] = v.hi;
@@ -167,8 +170,15 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
       }
     }
   }
-  if (threadIdx.x < tpb)
-    n_valid[bh * nb + blk + threadIdx.x] = min(S, max(0, nv - static_cast<int>(threadIdx.x) * S));
+  // real tokens per tile: a block of one or more tiles fills its first tiles;
+  // two blocks of half a tile share one (both full), written by the first
+  const long long t0 = slot0 / S;
+  if (SB >= S) {
+    if (threadIdx.x < SB / S)
+      n_valid[bh * nb + t0 + threadIdx.x] = min(S, max(0, nv - static_cast<int>(threadIdx.x) * S));
+  } else if (threadIdx.x == 0 && slot0 % S == 0) {
+    n_valid[bh * nb + t0] = S;
+  }
 }
 
 // Xp[b,h,s,:] = X[b,perm[s],h,:] (zeros on padding slots).  One thread per
@@ -258,9 +268,12 @@ cudaError_t launch_permute_pool(const Plan& p, const uint8_t* shape_id, const ui
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (p.sz.nb > 65535) return cudaErrorInvalidValue;
-  dim3 grid(c.H, p.sz.nb, c.B);
+  if (p.sz.nslots > 65535) return cudaErrorInvalidValue;
+  const int U = p.sz.slot_tokens;
+  const int upz = c.zT * c.zH * c.zW / U;  // table units per zone
+  dim3 grid(c.H, p.sz.nslots, c.B);
   permute_pool_kernel<<<grid, kPermThreads, smem, st>>>(
-      c, p.sz.nzH, p.sz.nzW, p.sz.blocks_per_zone, p.sz.Z, p.sz.nb, p.sz.Np, m, shape_id, Q, K,
+      c, p.sz.nzH, p.sz.nzW, upz, p.sz.Z, p.sz.nb, p.sz.nslots, U, p.sz.Np, m, shape_id, Q, K,
       V, perm, inv, Qp, Kp, Vp, Qh, Ql, Kh, Kl, n_valid, status);
   return cudaGetLastError();
 }

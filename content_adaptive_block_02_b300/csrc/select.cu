@@ -624,31 +624,58 @@ struct ShapeTokens {
   int32_t t[PRISM_MAX_SHAPES];  // token count of every menu shape
 };
 
-__global__ void block_table_kernel(long long rows, int nb, int bpz, int Z, int S,
+__global__ void block_table_kernel(long long rows, int nu, int upz, int Z, int U, int T,
                                    ShapeTokens ext_tokens,
                                    const uint8_t* __restrict__ shape_id,
                                    const int32_t* __restrict__ n_valid,
                                    int32_t* __restrict__ n_sel, int32_t* __restrict__ bstart) {
+  // units of U slots (a tile, or half a tile); rows = B*H*nu
   const long long r = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   if (r >= rows) return;
-  const long long bh = r / nb;
-  const int t = static_cast<int>(r % nb);
-  const int z = t / bpz, lt = t % bpz;
+  const long long bh = r / nu;
+  const int u = static_cast<int>(r % nu);
+  const int z = u / upz, lu = u % upz;
   const int sid = shape_id[bh * Z + z];
-  const int tpb = sid < PRISM_MAX_SHAPES ? max(1, ext_tokens.t[sid] / S) : 1;
-  const int first = t - lt % tpb;
+  const int SB = sid < PRISM_MAX_SHAPES ? ext_tokens.t[sid] : T;
+  const int upb = max(1, SB / U);
+  const int first = u - lu % upb;
   bstart[r] = first;
   int nv = 0;
-  if (first == t)
-    for (int q = 0; q < tpb; ++q) nv += n_valid[r + q];
+  if (first == u) {
+    const int nt = nu / (T / U);                      // tiles per (b, h)
+    const long long t0 = bh * nt + static_cast<long long>(u) * U / T;
+    if (SB >= T) {
+      for (int q = 0; q < SB / T; ++q) nv += n_valid[t0 + q];
+    } else {  // half a tile: this block's part of its tile's real tokens
+      const int hb = (u * U) % T / SB;
+      nv = min(SB, max(0, n_valid[t0] - hb * SB));
+    }
+  }
   n_sel[r] = nv;
 }
 
-// Tile-level selection: tile u is selected for tile t when the block that
-// starts u's block was selected for the block that starts t's block.  One
-// thread per (tile row, 32-tile word); also the row's count.
-__global__ void expand_bitmask_kernel(long long rows, int nb, int nwords,
-                                      const uint32_t* __restrict__ bm_block,
+// Tile-level selection: tile u is selected for tile t when some block of t
+// (one, or two of half a tile each) selected some block of u.  One thread
+// per (tile row, 32-tile word); also the row's count.  per = table units per
+// tile (1 or 2); bm_unit is the selection bitmask over units (uwords words
+// per row), bstart the first unit of every unit's block.
+__device__ __forceinline__ uint32_t pair_bits(const uint32_t* __restrict__ bm_unit, int uwords,
+                                              const int32_t* __restrict__ bs, long long bh, int nu,
+                                              int per, int qt, int kt) {
+  uint32_t bits = 0u;
+  for (int qh = 0; qh < per; ++qh) {
+    const long long row = bh * nu + bs[qt * per + qh];
+    const uint32_t* src = bm_unit + row * uwords;
+    for (int kh = 0; kh < per; ++kh) {
+      const int j = bs[kt * per + kh];
+      bits |= ((src[j >> 5] >> (j & 31)) & 1u) << (qh * per + kh);
+    }
+  }
+  return bits;
+}
+
+__global__ void expand_bitmask_kernel(long long rows, int nb, int nwords, int nu, int uwords,
+                                      int per, const uint32_t* __restrict__ bm_unit,
                                       const int32_t* __restrict__ bstart,
                                       uint32_t* __restrict__ bm_tile,
                                       int32_t* __restrict__ rowcnt) {
@@ -657,23 +684,44 @@ __global__ void expand_bitmask_kernel(long long rows, int nb, int nwords,
   const int lane = static_cast<int>(i % 32);
   if (r >= rows) return;
   const long long bh = r / nb;
-  const long long rs = bh * nb + bstart[r];           // the row of its block
-  const uint32_t* src = bm_block + rs * nwords;
-  const int32_t* bs = bstart + bh * nb;
+  const int t = static_cast<int>(r % nb);
+  const int32_t* bs = bstart + bh * nu;
   int cnt = 0;
   for (int w = lane; w < nwords; w += 32) {
     uint32_t out = 0u;
     for (int k = 0; k < 32; ++k) {
       const int u = w * 32 + k;
       if (u >= nb) break;
-      const int j = bs[u];
-      out |= ((src[j >> 5] >> (j & 31)) & 1u) << k;
+      out |= (pair_bits(bm_unit, uwords, bs, bh, nu, per, t, u) != 0u ? 1u : 0u) << k;
     }
     bm_tile[r * nwords + w] = out;
     cnt += __popc(out);
   }
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
   if (lane == 0) rowcnt[r] = cnt;
+}
+
+// Sub-tile masks of the tile lists (blocks of half a tile): for every entry
+// of the CSR (rows = query tiles) or CSC (rows = key tiles) lists, bit
+// 2 qh + kh set when the query tile's half qh does not attend the key tile's
+// half kh.  One warp per row, lanes over its entries.
+__global__ void list_mask_kernel(long long rows, int nb, int nu, int uwords, int per, int csc,
+                                 const int32_t* __restrict__ ptr, const int32_t* __restrict__ idx,
+                                 const uint32_t* __restrict__ bm_unit,
+                                 const int32_t* __restrict__ bstart, uint8_t* __restrict__ mask) {
+  const long long r = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const long long bh = r / nb;
+  const int me = static_cast<int>(r % nb);
+  const int32_t* bs = bstart + bh * nu;
+  const uint32_t full = (1u << (per * per)) - 1u;
+  for (int e = ptr[r] + lane; e < ptr[r + 1]; e += 32) {
+    const int other = idx[e];
+    const uint32_t bits = csc ? pair_bits(bm_unit, uwords, bs, bh, nu, per, other, me)
+                              : pair_bits(bm_unit, uwords, bs, bh, nu, per, me, other);
+    mask[e] = static_cast<uint8_t>(~bits & full);
+  }
 }
 
 }  // namespace
@@ -684,7 +732,12 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
                           int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
                           int32_t* row_idx, uint8_t* ws, cudaStream_t st) {
   const prism_config_t& c = p.cfg;
-  const int nb = p.sz.nb;
+  // the selection runs over the block table's units (tiles, or half tiles);
+  // the lists handed on are over tiles
+  const int nt = p.sz.nb;
+  const long long trows = static_cast<long long>(c.B) * c.H * nt;
+  const int twords = (nt + 31) / 32;
+  const int nb = p.sz.nslots;
   const long long rows = static_cast<long long>(c.B) * c.H * nb;
   const int nwords = (nb + 31) / 32;
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
@@ -701,16 +754,17 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
   cudaError_t e = cudaMemsetAsync(status + WS_AMB_COUNT, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   int32_t* bstart = reinterpret_cast<int32_t*>(ws + p.off_bstart);
+  const int per = c.block_tokens / p.sz.slot_tokens;  // table units per tile
   if (p.sz.multi_tile) {
-    // blocks span several tiles: select over blocks (their first tiles), with
-    // each block's real-token count in place of the tile counts
+    // blocks span several tiles or share one: select over blocks (their first
+    // units), with each block's real-token count in place of the tile counts
     ShapeTokens ext;
     for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
       ext.t[k] = k < c.n_shapes ? c.shapes[k][0] * c.shapes[k][1] * c.shapes[k][2] : c.block_tokens;
     int32_t* n_sel = reinterpret_cast<int32_t*>(ws + p.off_nsel);
     block_table_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(
-        rows, nb, p.sz.blocks_per_zone, p.sz.Z, c.block_tokens, ext, shape_id, n_valid,
-        n_sel, bstart);
+        rows, nb, c.zT * c.zH * c.zW / p.sz.slot_tokens, p.sz.Z, p.sz.slot_tokens,
+        c.block_tokens, ext, shape_id, n_valid, n_sel, bstart);
     n_valid = n_sel;
   }
   dim3 g((nb + kTJ - 1) / kTJ, (nb + kTI - 1) / kTI, c.B * c.H);
@@ -761,23 +815,33 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
                            static_cast<int>(fsm));
   if (e != cudaSuccess) return e;
   select_fallback_kernel<<<296, 256, fsm, st>>>(fp);
+  uint32_t* bm_unit = bitmask;
   if (p.sz.multi_tile) {
     // block lists -> tile lists: every tile of a query block gets every tile
     // of every key block its block selected
     uint32_t* tbm = reinterpret_cast<uint32_t*>(ws + p.off_tbitmask);
-    expand_bitmask_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(
-        rows, nb, nwords, bitmask, bstart, tbm, rowcnt);
+    expand_bitmask_kernel<<<static_cast<unsigned>((trows * 32 + 255) / 256), 256, 0, st>>>(
+        trows, nt, twords, nb, nwords, per, bitmask, bstart, tbm, rowcnt);
     bitmask = tbm;
   }
-  scan_kernel<<<1, 1024, 0, st>>>(rows, rowcnt, row_ptr);
-  csr_fill_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(
-      rows, nwords, bitmask, row_ptr, col_idx);
-  const long long units = static_cast<long long>(c.B) * c.H * nwords;
+  scan_kernel<<<1, 1024, 0, st>>>(trows, rowcnt, row_ptr);
+  csr_fill_kernel<<<static_cast<unsigned>((trows * 32 + 255) / 256), 256, 0, st>>>(
+      trows, twords, bitmask, row_ptr, col_idx);
+  const long long units = static_cast<long long>(c.B) * c.H * twords;
   csc_count_kernel<<<static_cast<unsigned>((units * 32 + 255) / 256), 256, 0, st>>>(
-      nb, nwords, units, bitmask, colcnt);
-  scan_kernel<<<1, 1024, 0, st>>>(rows, colcnt, col_ptr);
+      nt, twords, units, bitmask, colcnt);
+  scan_kernel<<<1, 1024, 0, st>>>(trows, colcnt, col_ptr);
   csc_fill_kernel<<<static_cast<unsigned>((units * 32 + 255) / 256), 256, 0, st>>>(
-      nb, nwords, units, bitmask, col_ptr, row_idx);
+      nt, twords, units, bitmask, col_ptr, row_idx);
+  if (p.sz.half_tile) {
+    uint8_t* mcsr = ws + p.sz.ws_csr_mask;
+    uint8_t* mcsc = ws + p.sz.ws_csc_mask;
+    const unsigned gm = static_cast<unsigned>((trows * 32 + 255) / 256);
+    list_mask_kernel<<<gm, 256, 0, st>>>(trows, nt, nb, nwords, per, 0, row_ptr, col_idx, bm_unit,
+                                         bstart, mcsr);
+    list_mask_kernel<<<gm, 256, 0, st>>>(trows, nt, nb, nwords, per, 1, col_ptr, row_idx, bm_unit,
+                                         bstart, mcsc);
+  }
   return cudaGetLastError();
 }
 

@@ -485,6 +485,8 @@ struct MenuConst {
   double log2_S[PRISM_MAX_CLASSES];             // log2 of each class's token count
   double tau[PRISM_MAX_CLASSES - 1];            // class thresholds, descending
   int n_classes;
+  int half_tile;                                // class 0 is half a tile
+  int zone_volume;
 };
 
 // Eq. 7 (Table 10 caption) in log space: with bT*bH*bW = S fixed, the
@@ -571,6 +573,9 @@ __global__ void __launch_bounds__(256) assign_kernel(prism_config_t c, int Z, Me
         cls += cz < menu.tau[q] ? 1 : 0;
         class_tie |= fabs(cz - menu.tau[q]) <= 1e-5 * fmax(1.0, fabs(menu.tau[q]));
       }
+      // a zone with padding takes no class smaller than a tile
+      if (menu.half_tile && cls == 0 && sh[z * 8 + 7] < static_cast<float>(menu.zone_volume))
+        cls = 1;
     }
     double lg[3];
     for (int a = 0; a < 3; ++a) {
@@ -657,6 +662,8 @@ cudaError_t launch_assign(const Plan& p, const float* stats, uint8_t* shape_id,
   for (int k = 0; k < PRISM_MAX_SHAPES; ++k)
     for (int a = 0; a < 3; ++a) m.log2_ext[k][a] = p.log2_ext[k][a];
   m.n_classes = p.sz.n_classes;
+  m.half_tile = p.sz.half_tile;
+  m.zone_volume = c.zT * c.zH * c.zW;
   for (int q = 0; q < p.sz.n_classes; ++q) {
     m.log2_S[q] = log2(static_cast<double>(p.sz.class_tokens[q]));
     for (int a = 0; a < p.sz.n_admissible; ++a) {

@@ -23,7 +23,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libprism.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "prism.h")
-MAX_SHAPES = 16
+MAX_SHAPES = 32
 MAX_CLASSES = 3
 
 ERRORS = {
@@ -72,7 +72,9 @@ class Sizes(ctypes.Structure):
         ("tensor_core_fwd", ctypes.c_int), ("tensor_core_bwd", ctypes.c_int),
         ("key_chunks", ctypes.c_int), ("chunk_blocks", ctypes.c_int),
         ("n_classes", ctypes.c_int), ("class_tokens", ctypes.c_int * MAX_CLASSES),
-        ("multi_tile", ctypes.c_int),
+        ("multi_tile", ctypes.c_int), ("slot_tokens", ctypes.c_int), ("nslots", ctypes.c_int),
+        ("half_tile", ctypes.c_int), ("ws_csr_mask", ctypes.c_size_t),
+        ("ws_csc_mask", ctypes.c_size_t),
     ]
 
 
@@ -283,10 +285,10 @@ class Plan:
             Qp=torch.empty(w.B, w.H, self.Np, w.d, dtype=torch.bfloat16, **e),
             Kp=torch.empty(w.B, w.H, self.Np, w.d, dtype=torch.bfloat16, **e),
             Vp=torch.empty(w.B, w.H, self.Np, w.d, dtype=torch.bfloat16, **e),
-            Qbar=torch.empty(w.B, w.H, self.nb, w.d, dtype=torch.float32, **e),
-            Qbar_lo=torch.empty(w.B, w.H, self.nb, w.d, dtype=torch.float32, **e),
-            Kbar=torch.empty(w.B, w.H, self.nb, w.d, dtype=torch.float32, **e),
-            Kbar_lo=torch.empty(w.B, w.H, self.nb, w.d, dtype=torch.float32, **e),
+            Qbar=torch.empty(w.B, w.H, self.sz.nslots, w.d, dtype=torch.float32, **e),
+            Qbar_lo=torch.empty(w.B, w.H, self.sz.nslots, w.d, dtype=torch.float32, **e),
+            Kbar=torch.empty(w.B, w.H, self.sz.nslots, w.d, dtype=torch.float32, **e),
+            Kbar_lo=torch.empty(w.B, w.H, self.sz.nslots, w.d, dtype=torch.float32, **e),
             n_valid=torch.empty(w.B, w.H, self.nb, dtype=torch.int32, **e),
         )
 
@@ -320,7 +322,7 @@ class Plan:
         return dict(
             row_ptr=torch.empty(rows + 1, **e), col_idx=torch.empty(max(self.sz.max_pairs, 4), **e),
             col_ptr=torch.empty(rows + 1, **e), row_idx=torch.empty(max(self.sz.max_pairs, 4), **e),
-            sel_tie=torch.empty(w.B, w.H, self.nb, dtype=torch.uint8, device=device),
+            sel_tie=torch.empty(w.B, w.H, self.sz.nslots, dtype=torch.uint8, device=device),
         )
 
     def block_select(self, shape_id, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid, ws, out=None):

@@ -107,9 +107,14 @@ MENU_128 = ((1, 8, 16), (1, 16, 8), (2, 8, 8), (4, 4, 8), (4, 8, 4), (2, 4, 16),
 # 256-token class: Table 11's 488 and the other power-of-two shapes that fit a
 # 16 x 16 frame patch
 MENU_256 = ((4, 8, 8), (2, 8, 16), (2, 16, 8), (4, 4, 16), (4, 16, 4), (1, 16, 16))
+# 64-token class: Table 11's shapes whose extents fit a 4 x 16 x 16 zone
+MENU_64 = ((4, 4, 4), (2, 4, 8), (2, 8, 4), (4, 2, 8), (4, 8, 2))
 # threshold between the 128- and 256-token classes (zone complexity; about
 # half the zones of the smooth-field grids fall below it)
 TAU_256 = 0.9
+# threshold between the 64- and 128-token classes (about the top fifth of the
+# smooth-field grids' zones lie above it)
+TAU_128 = 1.3
 
 # Block-mean field gain: chosen once so that the 720p-like grid at Top-p 0.9,
 # Top-k floor 8 lands in the 85-90 % block-sparsity band (88.6 % measured on
@@ -140,6 +145,11 @@ WORKLOADS["2k_mc"] = WORKLOADS["2k"].with_(name="2k_mc", menu=MENU_128 + MENU_25
                                            class_tau=(TAU_256,))
 WORKLOADS["2k_mc4"] = WORKLOADS["2k"].with_(name="2k_mc4", zone=(4, 16, 16),
                                             menu=MENU_128 + MENU_256, class_tau=(TAU_256,))
+# all three classes of Table 11 (C_64, C_128, C_256) on 4 x 16 x 16 zones; two
+# 64-token blocks share one 128-row tensor-core tile
+WORKLOADS["2k_mc3"] = WORKLOADS["2k"].with_(name="2k_mc3", zone=(4, 16, 16),
+                                            menu=MENU_64 + MENU_128 + MENU_256,
+                                            class_tau=(TAU_128, TAU_256))
 
 
 def stress(base: str, variant: str, topp: float) -> Workload:

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PRISM_MAX_SHAPES 16
+#define PRISM_MAX_SHAPES 32
 #define PRISM_MAX_CLASSES 3
 
 enum {
@@ -91,14 +91,18 @@ typedef struct prism_config {
                           /* block-size classes (Table 10 caption: thresholds
                              tau_128 / tau_256; Table 11: classes C_64, C_128,
                              C_256).  The menu's distinct token counts are the
-                             classes, ascending; each must be block_tokens,
-                             2 block_tokens or 4 block_tokens (a block then spans
-                             1, 2 or 4 consecutive tiles of block_tokens slots).
+                             classes, ascending; each must be block_tokens / 2
+                             (tensor-core plans only: two such blocks share one
+                             tile), block_tokens, 2 block_tokens or
+                             4 block_tokens (a block then spans 1, 2 or 4
+                             consecutive tiles of block_tokens slots).
                              A zone of complexity c = V_z / mean V + a_bar
                              (V_z: its summed directional video variance, a_bar
                              its audio gate; each term only when that guidance is
                              on) takes class k = number of thresholds c is below;
-                             thresholds descending, the first n_classes - 1 used. */
+                             thresholds descending, the first n_classes - 1 used.
+                             A zone with padding takes no class smaller than a
+                             tile. */
 } prism_config_t;
 
 #define PRISM_FAULT_STARVE_LOADS 1
@@ -130,9 +134,21 @@ typedef struct prism_sizes {
   int chunk_blocks;       /* blocks per range (nb when key_chunks == 1) */
   int n_classes;          /* block-size classes of the menu */
   int class_tokens[PRISM_MAX_CLASSES]; /* their token counts, ascending */
-  int multi_tile;         /* 1 when some block spans several tiles: nb, n_valid
-                             and the block lists then count tiles (a block's
-                             mean is stored at its first tile) */
+  int multi_tile;         /* 1 when some block spans several tiles or shares one:
+                             n_valid and the block lists then count tiles, and
+                             the block means sit at a block's first slot */
+  int slot_tokens;        /* granularity of the block table: block_tokens, or half
+                             of it when the menu has a class of half a tile (two
+                             such blocks share one tile; tensor-core plans only) */
+  int nslots;             /* slots per (b, h) = Np / slot_tokens: the length of the
+                             Qbar / Kbar / sel_tie rows (nb unless half_tile) */
+  int half_tile;          /* 1 when the menu has a class of half a tile */
+  size_t ws_csr_mask;     /* half_tile: workspace offset of the uint8 sub-tile masks
+                             of the CSR entries (one per col_idx entry), written by
+                             prism_block_select and read by the attention calls:
+                             bit 2 qh + kh set = the query tile's half qh does NOT
+                             attend the key tile's half kh (0: the whole pair) */
+  size_t ws_csc_mask;     /* half_tile: likewise for the CSC entries (row_idx) */
 } prism_sizes_t;
 
 typedef struct prism_plan prism_plan_t;
@@ -221,12 +237,12 @@ int prism_zone_stats_norms(const prism_plan_t* plan, const uint16_t* V, const fl
  *   perm       [B, H, Np] int32 out: slot -> token, -1 for a padding slot
  *   inv        [B, H, N]  int32 out: token -> slot
  *   Qp, Kp, Vp [B, H, Np, d] bf16 out
- *   Qbar, Qbar_lo, Kbar, Kbar_lo [B, H, nb, d] fp32 out: mean over the
+ *   Qbar, Qbar_lo, Kbar, Kbar_lo [B, H, nslots, d] fp32 out: mean over the
  *              block's real tokens as a double-float pair: Qbar is the fp32
  *              rounding of the mean and Qbar_lo the fp32 rounding of the rest
  *              (Qbar + Qbar_lo carries about 46 significant bits); 0 for a
  *              block without real tokens; a block that spans several tiles
- *              has its mean at its first tile and 0 at the others
+ *              has its mean at its first slot and 0 at the slots that continue it
  *   n_valid    [B, H, nb] int32 out: real tokens in each tile (a block's real
  *              tokens come first in it, so they fill its first tiles) */
 int prism_assign_and_permute(const prism_plan_t* plan, const float* stats,
@@ -260,14 +276,15 @@ int prism_permute_shapes(const prism_plan_t* plan, const uint8_t* shape_id, cons
  *               (prism_sizes_t.multi_tile) the selection runs over blocks and
  *               every list below is over tiles: each tile of a query block
  *               lists every tile of every key block its block selected
- *   Qbar, Qbar_lo, Kbar, Kbar_lo [B, H, nb, d] fp32 in (as written above)
+ *   Qbar, Qbar_lo, Kbar, Kbar_lo [B, H, nslots, d] fp32 in (as written above)
  *   n_valid     [B, H, nb] int32 in
  *   row_ptr     [B*H*nb + 1] int32 out: CSR offsets over all (b, h, i)
  *   col_idx     [max_pairs] int32 out: key blocks of each query block, ascending
  *   col_ptr     [B*H*nb + 1] int32 out: CSC offsets over all (b, h, j)
  *   row_idx     [max_pairs] int32 out: query blocks of each key block, ascending
- *   sel_tie     [B, H, nb] uint8 out: 1 where the decision sat within 1e-6 of
- *               a boundary (score gap or cumulative mass), at a block's first tile
+ *   sel_tie     [B, H, nslots] uint8 out: 1 where the decision sat within 1e-6
+ *               of a boundary (score gap or cumulative mass), at a block's
+ *               first slot
  *   ws          workspace of ws_bytes
  * Query blocks with no real token select nothing; candidates are the key
  * blocks with at least one real token. */
@@ -283,7 +300,9 @@ int prism_block_select(const prism_plan_t* plan, const uint8_t* shape_id, const 
  * prism_sizes_t.key_chunks > 1 the key blocks are walked in ranges and the
  * per-range partial results, kept in `ws`, are combined before the call's
  * last kernel writes Op and lse; prism_sparse_attn_bwd does the same for dQ,
- * dK and dV.  The results do not depend on the split beyond rounding.
+ * dK and dV.  The results do not depend on the split beyond rounding.  With
+ * blocks of half a tile (prism_sizes_t.half_tile) both calls read the
+ * sub-tile masks that prism_block_select left in `ws` for these lists.
  *   Qp, Kp, Vp [B, H, Np, d] bf16 in; n_valid, row_ptr, col_idx as above
  *   Op  [B, H, Np, d] bf16 out (padding rows 0)
  *   lse [B, H, Np] fp32 out: natural-log log-sum-exp per row (padding 0) */
@@ -326,7 +345,9 @@ int prism_sparse_attn_bwd(const prism_plan_t* plan, const uint16_t* Qp, const ui
  * that was current at the first call).  All calls share the array: calls
  * whose kernels overlap on the GPU race and give wrong results.  Device-side
  * wait timeouts go to the array's status word, cleared at the start of each
- * call; read it with prism_noalloc_device_status. */
+ * call; read it with prism_noalloc_device_status.  Plans with blocks of half a
+ * tile (prism_sizes_t.half_tile) return PRISM_ERR_UNSUPPORTED: their sub-tile
+ * masks live in the workspace. */
 int prism_sparse_attn_bwd_noalloc(const prism_plan_t* plan, const uint16_t* Qp,
                                   const uint16_t* Kp, const uint16_t* Vp, const uint16_t* Op,
                                   const uint16_t* dOp, const float* lse, const int32_t* n_valid,

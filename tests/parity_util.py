@@ -64,6 +64,12 @@ def run_gpu(w, inputs, attn_kernel=0, shape_id=None, key_chunk_blocks=0, fused_a
     g.update({k: v.cpu() for k, v in att.lists.items()})
     if fused_a2v:
         g["nrm"] = att.nrm.cpu()
+    sz = att.plan.sz
+    if sz.half_tile:
+        # the sub-tile masks prism_block_select left in the workspace
+        nnz = int(att.lists["row_ptr"][-1].item())
+        g["csr_mask"] = att.ws[sz.ws_csr_mask:sz.ws_csr_mask + nnz].cpu()
+        g["csc_mask"] = att.ws[sz.ws_csc_mask:sz.ws_csc_mask + nnz].cpu()
     g.update(stats=att.stats.cpu(), Op=att.Op.cpu(), lse=att.lse.cpu(), O=O.cpu(),
              dQ=dQ.cpu(), dK=dK.cpu(), dV=dV.cpu(), dQp=att.dQp.cpu(), dKp=att.dKp.cpu(),
              dVp=att.dVp.cpu(), dOp=att.dOp.cpu())
@@ -168,6 +174,89 @@ def compare(w, heads=None, rows=None, key_blocks=None, check_bwd=True, report=No
                                 heads, grad_scale)
 
 
+def _compare_half_tile(w, w_h, hs, g, X, nb, perm_o, inv_o, units_o, nblk_o, Qp_o, Kp_o, Vp_o,
+                       Qb_o, Kb_o, check_bwd, rep):
+    """Steps 3+ of ``compare`` for plans with blocks of half a tile: the
+    device's tile lists and sub-tile masks are read back as block lists (a
+    query block of half tile qh selects the key blocks of the halves kh its
+    mask leaves on), compared with the oracle's selection, checked to expand
+    back exactly (``orc.expand_lists_masked``), and the attention is compared
+    with the oracle's block-level attention."""
+    U, T_ = orc.slot_tokens(w), w.block
+    per = T_ // U
+    nu = units_o.shape[2]
+    Lg_all = gpu_lists(w, g, nb)
+    rp = g["row_ptr"].numpy()
+    cm = g["csr_mask"].numpy().astype(np.int64)
+    cp, ri = g["col_ptr"].numpy(), g["row_idx"].numpy()
+    ccm = g["csc_mask"].numpy().astype(np.int64)
+    Lo, Fo = orc.select_blocks(w_h, Qb_o, Kb_o, nblk_o)
+    L_use = {}
+    diff_rows = flagged = 0
+    for b in range(w.B):
+        for hi, h in enumerate(hs):
+            ul = units_o[b, hi]
+            start = np.zeros(nu, dtype=np.int64)
+            i = 0
+            while i < nu:
+                n = max(1, int(ul[i]))
+                start[i:i + n] = i
+                i += n
+            Lg = Lg_all[(b, h)]
+            masks = [cm[rp[(b * w.H + h) * nb + t]:rp[(b * w.H + h) * nb + t + 1]] for t in range(nb)]
+            Lb = [None] * nu
+            for t in range(nb):
+                for qh in range(per):
+                    i = t * per + qh
+                    if ul[i] == 0:
+                        continue
+                    sel = set()
+                    for v, m in zip(Lg[t], masks[t]):
+                        for kh in range(per):
+                            if not (m >> (qh * per + kh)) & 1:
+                                sel.add(int(start[int(v) * per + kh]))
+                    Lb[i] = np.array(sorted(sel), dtype=np.int64)
+            el, em = orc.expand_lists_masked(Lb, ul, U, T_)
+            for t in range(nb):
+                assert np.array_equal(el[t], Lg[t]), ("tile list", b, h, t)
+                assert np.array_equal(em[t], masks[t]), ("sub-tile mask", b, h, t)
+            # CSC: the transpose, each entry with the same mask
+            cols = orc.csc_from_lists(Lg, nb)
+            for j in range(nb):
+                r = (b * w.H + h) * nb + j
+                assert np.array_equal(ri[cp[r]:cp[r + 1]], cols[j]), ("csc", b, h, j)
+                for e, t in zip(range(cp[r], cp[r + 1]), ri[cp[r]:cp[r + 1]]):
+                    k = int(np.searchsorted(Lg[t], j))
+                    assert ccm[e] == masks[t][k], ("csc mask", b, h, j, t)
+            lo_, fo = Lo[(b, hi)], Fo[(b, hi)]
+            for i in range(nu):
+                if Lb[i] is None:
+                    continue
+                flagged += int(fo[i])
+                if not np.array_equal(Lb[i], lo_[i]):
+                    assert fo[i], f"list differs on an unflagged row (b={b}, h={h}, unit {i})"
+                    diff_rows += 1
+            L_use[(b, hi)] = Lb
+    rep["select_rows_differing_on_near_ties"] = diff_rows
+    rep["select_rows_flagged"] = flagged
+    rep["masked_entries"] = int((cm > 0).sum())
+    scale = 1.0 / math.sqrt(w.d)
+    dOp_o = orc.permute(X["dO"][:, :, hs], perm_o)
+    assert np.array_equal(f64(g["dOp"])[:, hs], dOp_o)
+    Op_o, lse_o, dQ_o, dK_o, dV_o = orc.attn_blocks(Qp_o, Kp_o, Vp_o, units_o, nblk_o, L_use, U,
+                                                    scale, dOp=dOp_o, o_bf16=True)
+    for name, got, ref, tol in (("O", g["Op"], Op_o, O_TOL), ("dQ", g["dQp"], dQ_o, G_TOL),
+                                ("dK", g["dKp"], dK_o, G_TOL), ("dV", g["dVp"], dV_o, G_TOL)):
+        if name != "O" and not check_bwd:
+            continue
+        got = f64(got)[:, hs]
+        e = max(rel_err(got[b, hi], ref[b, hi]) for b in range(w.B) for hi in range(len(hs)))
+        rep[name + "_max_rel"] = e
+        assert e <= tol, (name, e)
+    assert np.abs(f64(g["lse"])[:, hs] - lse_o).max() <= 2e-2
+    return rep
+
+
 def audio_stats_slack(w, n, tau):
     """How far the audio statistics (var_n_T, var_n_H, var_n_W, nbar) of every
     (b, zone) can move when the norms n [B, N] are off by tau relative:
@@ -196,13 +285,19 @@ def _compare_from_shapes(w, w_h, hs, g, X, nb, sid_use, rows, key_blocks, check_
     assert np.array_equal(f64(g["Qp"])[:, hs], Qp_o)
     assert np.array_equal(f64(g["Kp"])[:, hs], Kp_o)
     assert np.array_equal(f64(g["Vp"])[:, hs], Vp_o)
-    Qb_o = orc.pool_blocks(Qp_o, tiles_o, nblk_o, w.block)
-    Kb_o = orc.pool_blocks(Kp_o, tiles_o, nblk_o, w.block)
+    U = orc.slot_tokens(w)
+    Qb_o = orc.pool_blocks(Qp_o, tiles_o, nblk_o, U)
+    Kb_o = orc.pool_blocks(Kp_o, tiles_o, nblk_o, U)
     Qb_g = (f64(g["Qbar"]) + f64(g["Qbar_lo"]))[:, hs]
     Kb_g = (f64(g["Kbar"]) + f64(g["Kbar_lo"]))[:, hs]
     assert np.abs(Qb_g - Qb_o).max() <= 1e-11 * max(1.0, np.abs(Qb_o).max())
     assert np.abs(Kb_g - Kb_o).max() <= 1e-11 * max(1.0, np.abs(Kb_o).max())
     rep["multi_tile_blocks"] = int((tiles_o > 1).sum())
+    if U < w.block:
+        assert rows is None and key_blocks is None, "half-tile blocks: whole heads only"
+        rep["half_tile_blocks"] = int((tiles_o == 1).sum())
+        return _compare_half_tile(w, w_h, hs, g, X, nb, perm_o, inv_o, tiles_o, nblk_o, Qp_o, Kp_o,
+                                  Vp_o, Qb_o, Kb_o, check_bwd, rep)
 
     # ---- step 3+4: selection (over blocks: their first tiles) ----
     Lg_all = gpu_lists(w, g, nb)

@@ -223,3 +223,20 @@ def test_mixed_block_classes_cuda_cores():
     rep = {}
     pu.compare(w, report=rep)
     assert rep["multi_tile_blocks"] > 0
+
+
+@pytest.mark.parametrize("kw,kcb", [(dict(Hg=32), 0), (dict(Hg=40), 0), (dict(Hg=32), 8),
+                                    (dict(Hg=32, topp=0.5, topk_floor=2), 0)],
+                         ids=["no-padding", "padding", "key-ranges", "p0.5"])
+def test_half_tile_block_classes(kw, kcb):
+    """All three classes of Table 11: 64-token blocks (two share a 128-row
+    tensor-core tile, with a sub-tile mask per listed tile pair), 128 and 256
+    on 4 x 16 x 16 zones; with padding, padded zones skip the 64-token class."""
+    w = _w128(zone=(4, 16, 16), T=8, menu=synth.MENU_64 + synth.MENU_128 + synth.MENU_256,
+              class_tau=(1.3, 1.15), **kw)
+    plan = prism.Plan(w)
+    assert plan.sz.half_tile == 1 and plan.sz.slot_tokens == 64
+    rep = {}
+    pu.compare(w, key_chunk_blocks=kcb, report=rep)
+    print(kw, kcb, rep)
+    assert rep["half_tile_blocks"] > 0 and rep["masked_entries"] > 0
