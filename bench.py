@@ -36,7 +36,10 @@ import torch  # noqa: E402
 from content_adaptive_block_02_b300 import build, prism, synth  # noqa: E402
 
 METRIC = "sparse-attn fwd+bwd ms & effective TFLOP/s at 2K grid; % of bf16 tensor peak"
-KERNELS_PER_STEP = 22
+# kernels one step launches: statistics, assign, permute_pool, score, select
+# fast / fallback, 2 scans, CSR fill, CSC count and fill, forward, unpermute
+# (O), permute (dO), bwd_pre, dK/dV, dQ, unpermute (dQ, dK, dV)
+KERNELS_PER_STEP = 20
 
 
 def pair_flops(w):
@@ -47,8 +50,8 @@ def pair_flops(w):
     return {"fwd": 4 * u, "bwd": 10 * u, "attn_fwd": 4 * u, "attn_dkdv": 8 * u, "attn_dq": 6 * u}
 # DRAM bytes (read + written) per launch of the attention kernels on the 2K-like
 # workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum,
-# 1 pass) of the kernel sources whose SHA-256 prefix is given; reported only for
-# that workload, and as null once the kernel's source file has changed since.
+# 1 pass) of the kernel code whose digest (source_digest) is given; reported
+# only for that workload, and as null once the kernel's code has changed since.
 TRAFFIC_2K = {
     "attn_fwd_tc_kernel": ("attn_tc.cu", None, 12.50e9 + 8.07e9),
     "attn_dkdv_tc_kernel": ("attn_tc_dkdv.cu", None, 26.09e9 + 19.80e9),
@@ -56,16 +59,23 @@ TRAFFIC_2K = {
 }
 
 
+def source_digest(name: str) -> str:
+    """SHA-256 prefix of a kernel source file's code lines (comments and blank
+    lines dropped, so that a comment edit keeps a capture valid)."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "content_adaptive_block_02_b300", "csrc", name)
+    with open(path) as f:
+        code = [re.sub(r"//.*$", "", line).strip() for line in f]
+    return hashlib.sha256("\n".join(c for c in code if c).encode()).hexdigest()[:16]
+
+
 def measured_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` if its source is still the captured one."""
+    """DRAM bytes per launch of `kernel` if its code is still the captured one."""
     ent = TRAFFIC_2K.get(kernel)
     if ent is None or ent[1] is None:
         return None
-    import hashlib
-    path = os.path.join(ROOT, "content_adaptive_block_02_b300", "csrc", ent[0])
-    with open(path, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    return ent[2] if sha == ent[1] else None
+    return ent[2] if source_digest(ent[0]) == ent[1] else None
 
 
 def peaks():
@@ -477,7 +487,9 @@ def run_ours(args, w):
                 "copies": "pinned host buffers, two device buffer sets, copy streams "
                           "overlapped with the neighbouring steps' compute"},
         "gpu_launches": (KERNELS_PER_STEP + (1 if fused else 0) +
-                         (4 if att.plan.sz.key_chunks > 1 else 0)) * args.steps,
+                         (4 if att.plan.sz.key_chunks > 1 else 0) +
+                         (2 if att.plan.sz.multi_tile else 0) +
+                         (2 if att.plan.sz.half_tile else 0)) * args.steps,
         "clocks": clk_sum,
         "device_status": m["status"],
     }
