@@ -22,7 +22,9 @@
 //              -> bf16 pairs in TMEM (two buffers); epilogue dQ * scale -> bf16.
 //              No exchange between the halves is needed: LSE and D are known.
 //   warp 8     producer: work counter, TMA loads of Q_i and dO_i (once per
-//              item) and of K_j, V_j (2-stage ring).
+//              item) and of K_j (3-stage ring) and V_j (2-stage ring).  V_j
+//              is free as soon as dP_j is done, K_j only after dQ += dS K_j,
+//              so the two rings are separate and K is fetched further ahead.
 //   warp 9     issuer A: S_j then dP_j, as soon as the compute warps have
 //              read the previous S / dP tiles.
 //   warp 10    issuer B: dQ += dS_j K_j.
@@ -36,15 +38,16 @@ using namespace tc;
 
 constexpr int kS = 128, kD = 128;
 constexpr int kTile = kS * kD * 2;  // 32 KB
-constexpr int kStages = 2;
+constexpr int kKStages = 3, kVStages = 2;
 constexpr int kThreads = 352;
 constexpr int kCompute = 256;
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_DS0 = 384, TM_DS1 = 448;
-constexpr int kOffQ = 0, kOffDO = kTile, kOffKV = 2 * kTile;
-constexpr int kOffBar = kOffKV + kStages * 2 * kTile;
+constexpr int kOffQ = 0, kOffDO = kTile, kOffK = 2 * kTile, kOffV = kOffK + kKStages * kTile;
+constexpr int kOffBar = kOffV + kVStages * kTile;
 
 struct DqBars {
-  uint64_t qd_full, qd_empty, kv_full[kStages], kv_empty[kStages];
+  uint64_t qd_full, qd_empty, k_full[kKStages], k_empty[kKStages], v_full[kVStages],
+      v_empty[kVStages];
   uint64_t s_full, dp_full, s_free, dp_free, ds_ready[2], ds_empty[2];
   uint64_t dq_done, dq_free, final_bar;
   uint64_t work_full[2], work_empty[2];
@@ -53,6 +56,7 @@ struct DqBars {
   int abort;
 };
 constexpr size_t kSmemBytes = kOffBar + sizeof(DqBars);
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the per-CTA limit");
 
 struct DqParams {
   const float* lse;
@@ -90,9 +94,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.qd_full, 1);
     mbar_init(&sm.qd_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 2);  // K is read by both issuers
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 2);  // K is read by both issuers
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
@@ -116,7 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   const uint32_t tmem = sm.tmem_base;
   const Waiter W{&sm.abort, P.status, P.limit};
-  uint8_t* kvbuf = dsm + kOffKV;  // stage s: K at s * 2 * kTile, V right after
+  uint8_t* kbuf = dsm + kOffK;  // K stage s at s * kTile
+  uint8_t* vbuf = dsm + kOffV;  // V stage s at s * kTile
 
   if (warp == 8) {
     // ------------------------------------------------------ producer ----
@@ -173,15 +182,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = beg; t < end; ++t) {
           const int j = P.col_idx[t];
           const int y = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
-          const int st = use % kStages;
-          if (!W.wait(&sm.kv_empty[st], ((use / kStages) & 1) ^ 1, 63)) { ok = false; break; }
-          uint8_t* kb = kvbuf + st * 2 * kTile;
+          const int ks = use % kKStages, vs = use % kVStages;
+          if (!W.wait(&sm.k_empty[ks], ((use / kKStages) & 1) ^ 1, 63)) { ok = false; break; }
+          uint8_t* kb = kbuf + ks * kTile;
           if (!P.starve) {  // fault injection: no loads, consumers time out
-            mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
-            tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
-            tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
-            tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
-            tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+            mbar_expect_tx(&sm.k_full[ks], kTile);
+            tma_load_2d(kb, &tmK, &sm.k_full[ks], 0, y);
+            tma_load_2d(kb + kTile / 2, &tmK, &sm.k_full[ks], 64, y);
+          }
+          if (!W.wait(&sm.v_empty[vs], ((use / kVStages) & 1) ^ 1, 60)) { ok = false; break; }
+          uint8_t* vb = vbuf + vs * kTile;
+          if (!P.starve) {
+            mbar_expect_tx(&sm.v_full[vs], kTile);
+            tma_load_2d(vb, &tmV, &sm.v_full[vs], 0, y);
+            tma_load_2d(vb + kTile / 2, &tmV, &sm.v_full[vs], 64, y);
           }
           ++use;
         }
@@ -208,23 +222,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!W.wait(&sm.qd_full, items & 1, 65)) break;
           ++items;
           for (int jj = 0; jj < n; ++jj) {
-            const int st = use % kStages;
-            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 66)) { ok = false; break; }
-            const uint64_t kd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile), 16, 1024);
-            const uint64_t vd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile + kTile), 16, 1024);
+            const int ks = use % kKStages, vs = use % kVStages;
+            if (!W.wait(&sm.k_full[ks], (use / kKStages) & 1, 66)) { ok = false; break; }
+            const uint64_t kd = sdesc_sw128(smem_u32(kbuf + ks * kTile), 16, 1024);
+            const uint64_t vd = sdesc_sw128(smem_u32(vbuf + vs * kTile), 16, 1024);
             if (sidx > 0 && !W.wait(&sm.s_free, (sidx - 1) & 1, 67)) { ok = false; break; }
             fence_after();
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               mma_ss(tmem + TM_S, qd + koff(kk), kd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
             commit(&sm.s_full);
+            commit(&sm.k_empty[ks]);
             if (sidx > 0 && !W.wait(&sm.dp_free, (sidx - 1) & 1, 68)) { ok = false; break; }
+            if (!W.wait(&sm.v_full[vs], (use / kVStages) & 1, 69)) { ok = false; break; }
             fence_after();
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               mma_ss(tmem + TM_DP, dod + koff(kk), vd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
             commit(&sm.dp_full);
-            commit(&sm.kv_empty[st]);
+            commit(&sm.v_empty[vs]);
             ++use;
             ++sidx;
           }
@@ -253,17 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < n; ++jj) {
             const uint32_t b = gidx & 1;
             if (!W.wait(&sm.ds_ready[b], (gidx >> 1) & 1, 73)) { ok = false; break; }
-            const int st = use % kStages;
-            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 74)) { ok = false; break; }
+            const int ks = use % kKStages;
+            if (!W.wait(&sm.k_full[ks], (use / kKStages) & 1, 74)) { ok = false; break; }
             fence_after();
-            const uint64_t kd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile), kTile / 2, 1024);
+            const uint64_t kd = sdesc_sw128(smem_u32(kbuf + ks * kTile), kTile / 2, 1024);
             const uint32_t a = tmem + (b ? TM_DS1 : TM_DS0);
 #pragma unroll
             for (int kk = 0; kk < kS / 16; ++kk)
               mma_ts(tmem + TM_DQ, a + kk * 8, kd + static_cast<uint64_t>((kk * 2048) >> 4), id_kn,
                      (jj > 0 || kk > 0) ? 1u : 0u);
             commit(&sm.ds_empty[b]);
-            commit(&sm.kv_empty[st]);
+            commit(&sm.k_empty[ks]);
             ++use;
             ++gidx;
           }
