@@ -11,13 +11,16 @@
 //           range of the head's key blocks (the whole range unless the plan
 //           splits it; see combine.cu) -- from a global work counter,
 //           publishes it in a 2-slot work ring, and streams the K and V tiles
-//           of its selected key blocks in that range into a 3-stage ring (one
-//           K + V pair per stage) with TMA (128-byte swizzle, 2 boxes of
-//           64 x 128 per tile).
+//           of its selected key blocks in that range into two 3-stage rings
+//           with TMA (128-byte swizzle, 2 boxes of 64 x 128 per tile).  A K
+//           tile is free once its score tile is done, long before the V tile
+//           of the same key block, so the rings are separate.
 //   warp 9  S issuer (one thread): S = Q K^T with Q held in tensor memory
 //           (A from TMEM, B = K tile from smem), as soon as the softmax warps
 //           have read the previous S tile, so the next score tile is on the
-//           tensor pipe while they work on this one.
+//           tensor pipe while they work on this one.  (Two 128 x 64 score
+//           tiles, one per column half, would let the halves drift apart, but
+//           N = 64 products issue at about the same cost as N = 128 ones.)
 //   warp 10 PV issuer (one thread): O_h += P_h V_h for each column half h
 //           (keys 64h..64h+63; A = P from TMEM, B = V rows from smem,
 //           MN-major), as soon as that half's P is in.  Two issuing threads
@@ -31,7 +34,9 @@
 //           channels), so the halves never wait for each other inside a query
 //           block and the exp work of one overlaps the loads, maxima and
 //           waits of the other.  Online softmax in the log2 domain with lazy
-//           rescaling (O_h is rescaled only when m_h grows by more than 2^8).
+//           rescaling: O_h is rescaled only when m_h grows by more than
+//           kRescaleLog2 (P stays below 2^kRescaleLog2, far inside the bf16
+//           and fp32 ranges).
 //           At the end of the query block the halves meet once and combine:
 //           O = (O_0 2^(m_0-M) + O_1 2^(m_1-M)) / (l_0 2^(m_0-M) + l_1 2^(m_1-M)),
 //           M = max(m_0, m_1); each half writes 64 of the output channels.
@@ -50,13 +55,14 @@ using namespace tc;
 constexpr int kS = 128;
 constexpr int kD = 128;
 constexpr int kTile = kS * kD * 2;  // 32 KB
-constexpr int kStages = 3;
+constexpr int kKStages = 3, kVStages = 3;
 constexpr int kFwdThreads = 352;
+constexpr float kRescaleLog2 = 16.f;
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t TM_S = 0, TM_O0 = 128, TM_O1 = 256, TM_Q = 384, TM_P = 448;
 
 struct FwdShared {
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full, s_free, p_full[2], p_empty[2], q_ready, final_bar;  // p_*: per column half
   uint64_t work_full[2], work_empty[2];
   int work_row[2], work_beg[2], work_end[2], work_nvq[2], work_chunk[2];
@@ -96,13 +102,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __shared__ FwdShared sm;
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* kvbuf = dsm;  // stage s: K at s * 2 * kTile, V right after
+  uint8_t* kbuf = dsm;                     // K stage s at s * kTile
+  uint8_t* vbuf = dsm + kKStages * kTile;  // V stage s at s * kTile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 2);  // released by the S and the PV issuer
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);  // released by the S issuer
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);  // released by the PV issuer
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, kSoftmaxThreads);
@@ -168,15 +179,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int t = beg; t < end; ++t) {
           const int j = P.col_idx[t];
           const int y = static_cast<int>(bh * P.Np + static_cast<long long>(j) * kS);
-          const int st = use % kStages;
-          if (!W.wait(&sm.kv_empty[st], ((use / kStages) & 1) ^ 1, 2)) { ok = false; break; }
-          uint8_t* kb = kvbuf + st * 2 * kTile;
+          const int ks = use % kKStages, vs = use % kVStages;
+          if (!W.wait(&sm.k_empty[ks], ((use / kKStages) & 1) ^ 1, 2)) { ok = false; break; }
+          uint8_t* kb = kbuf + ks * kTile;
           if (!P.starve) {  // fault injection: no loads, consumers time out
-            mbar_expect_tx(&sm.kv_full[st], 2 * kTile);
-            tma_load_2d(kb, &tmK, &sm.kv_full[st], 0, y);
-            tma_load_2d(kb + kTile / 2, &tmK, &sm.kv_full[st], 64, y);
-            tma_load_2d(kb + kTile, &tmV, &sm.kv_full[st], 0, y);
-            tma_load_2d(kb + kTile + kTile / 2, &tmV, &sm.kv_full[st], 64, y);
+            mbar_expect_tx(&sm.k_full[ks], kTile);
+            tma_load_2d(kb, &tmK, &sm.k_full[ks], 0, y);
+            tma_load_2d(kb + kTile / 2, &tmK, &sm.k_full[ks], 64, y);
+          }
+          if (!W.wait(&sm.v_empty[vs], ((use / kVStages) & 1) ^ 1, 3)) { ok = false; break; }
+          uint8_t* vb = vbuf + vs * kTile;
+          if (!P.starve) {
+            mbar_expect_tx(&sm.v_full[vs], kTile);
+            tma_load_2d(vb, &tmV, &sm.v_full[vs], 0, y);
+            tma_load_2d(vb + kTile / 2, &tmV, &sm.v_full[vs], 64, y);
           }
           ++use;
         }
@@ -200,17 +216,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ++qcnt;
           for (int jj = 0; jj < n; ++jj) {
             if (jj > 0 && !W.wait(&sm.s_free, (sidx - 1) & 1, 6)) { ok = false; break; }
-            const int st = use % kStages;
-            if (!W.wait(&sm.kv_full[st], (use / kStages) & 1, 9)) { ok = false; break; }
+            const int ks = use % kKStages;
+            if (!W.wait(&sm.k_full[ks], (use / kKStages) & 1, 9)) { ok = false; break; }
             fence_after();
-            const uint64_t kd = sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile), 16, 1024);
+            const uint64_t kd = sdesc_sw128(smem_u32(kbuf + ks * kTile), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               mma_ts(tmem + TM_S, tmem + TM_Q + kk * 8,
                      kd + static_cast<uint64_t>(((kk >> 2) * (kTile / 2) + (kk & 3) * 32) >> 4), idS,
                      kk > 0 ? 1u : 0u);
             commit(&sm.s_full);
-            commit(&sm.kv_empty[st]);
+            commit(&sm.k_empty[ks]);
             ++use;
             ++sidx;
           }
@@ -236,12 +252,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!W.wait(&sm.q_ready, qcnt & 1, 15)) break;
           ++qcnt;
           for (int jj = 0; jj < n; ++jj) {
-            const int st = use % kStages;
-            const uint64_t vd =
-                sdesc_sw128(smem_u32(kvbuf + st * 2 * kTile + kTile), kTile / 2, 1024);
+            const int vs = use % kVStages;
+            const uint64_t vd = sdesc_sw128(smem_u32(vbuf + vs * kTile), kTile / 2, 1024);
             for (int h = 0; h < 2; ++h) {
               if (!W.wait(&sm.p_full[h], pidx & 1, 7)) { ok = false; break; }
-              if (h == 0 && !W.wait(&sm.kv_full[st], (use / kStages) & 1, 8)) { ok = false; break; }
+              if (h == 0 && !W.wait(&sm.v_full[vs], (use / kVStages) & 1, 8)) { ok = false; break; }
               fence_after();
               const uint32_t o = tmem + (h ? TM_O1 : TM_O0);
 #pragma unroll
@@ -253,7 +268,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               commit(&sm.p_empty[h]);
             }
             if (!ok) break;
-            commit(&sm.kv_empty[st]);
+            commit(&sm.v_empty[vs]);
             ++use;
             ++pidx;
           }
@@ -383,7 +398,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(s[c][e]));
         }
         mx *= P.scale_log2;
-        const bool resc = mx > m + 8.f;
+        const bool resc = mx > m + kRescaleLog2;
         const float m_new = resc ? mx : m;
         const float corr = resc ? ex2(m - m_new) : 1.f;
         // this half's P buffer and O_h are free once its previous PV is done
@@ -579,7 +594,7 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
   a.mask = p.sz.half_tile ? ws + p.sz.ws_csr_mask : nullptr;
   cudaError_t e = cudaMemsetAsync(a.status + WS_FWD_QUEUE, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  const size_t smem = 2ull * kStages * kTile + 1024;  // K + V per stage
+  const size_t smem = static_cast<size_t>(kKStages + kVStages) * kTile + 1024;  // K, V rings
   e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
