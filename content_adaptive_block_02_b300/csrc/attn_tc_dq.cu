@@ -16,7 +16,7 @@
 //   S  = Q_i K_j^T     A = Q_i (smem),  B = K_j (smem)        -> TMEM S
 //   dP = dO_i V_j^T    A = dO_i (smem), B = V_j (smem)        -> TMEM dP
 //   dQ += dS K_j       A = dS (TMEM, bf16), B = K_j (MN-major) -> TMEM dQ
-// Roles (352 threads, one persistent CTA per SM):
+// Roles (384 threads, one persistent CTA per SM):
 //   warps 0-7  compute: thread = query row; warps w and w+4 split the key
 //              columns in halves.  P = exp2(S*c - LSE*log2 e), dS = P (dP - D)
 //              -> bf16 pairs in TMEM (two buffers); epilogue dQ * scale -> bf16.
@@ -25,9 +25,14 @@
 //              item) and of K_j (3-stage ring) and V_j (2-stage ring).  V_j
 //              is free as soon as dP_j is done, K_j only after dQ += dS K_j,
 //              so the two rings are separate and K is fetched further ahead.
-//   warp 9     issuer A: S_j then dP_j, as soon as the compute warps have
-//              read the previous S / dP tiles.
-//   warp 10    issuer B: dQ += dS_j K_j.
+//   warp 9     S issuer: S_j, as soon as the compute warps have read the
+//              previous S tile.
+//   warp 11    dP issuer: dP_j, as soon as they have read the previous dP.
+//   warp 10    dQ issuer: dQ += dS_j K_j.
+//   One thread issues a tcgen05.mma only every ~120 cycles, about twice the
+//   time the tensor pipe needs for a 128 x 128 x 16 product, so each of the
+//   three products has its own issuing thread (on its own SM sub-partition)
+//   and the three streams overlap on the pipe.
 // Tensor memory: S [0,128), dP [128,256), dQ [256,384), dS0 [384,448),
 // dS1 [448,512).
 #include "tc_common.cuh"
@@ -39,7 +44,7 @@ using namespace tc;
 constexpr int kS = 128, kD = 128;
 constexpr int kTile = kS * kD * 2;  // 32 KB
 constexpr int kKStages = 3, kVStages = 2;
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kCompute = 256;
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_DS0 = 384, TM_DS1 = 448;
 constexpr int kOffQ = 0, kOffDO = kTile, kOffK = 2 * kTile, kOffV = kOffK + kKStages * kTile;
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(&sm.qd_full, 1);
-    mbar_init(&sm.qd_empty, 1);
+    mbar_init(&sm.qd_empty, 2);  // the S and the dP issuer
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 2);  // K is read by both issuers
@@ -110,11 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.ds_ready[b], kCompute);
       mbar_init(&sm.ds_empty[b], 1);
       mbar_init(&sm.work_full[b], 1);
-      mbar_init(&sm.work_empty[b], 2 + kCompute);
+      mbar_init(&sm.work_empty[b], 3 + kCompute);
     }
     mbar_init(&sm.dq_done, 1);
     mbar_init(&sm.dq_free, kCompute);
-    mbar_init(&sm.final_bar, 2);
+    mbar_init(&sm.final_bar, 3);
     sm.abort = 0;
     mbar_init_fence();
   }
@@ -202,47 +207,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------ issuer A: S, dP ----
+  } else if (warp == 9 || warp == 11) {
+    // ------------------------------------------------ S issuer, dP issuer ----
     if (lane == 0) {
+      const bool is_s = warp == 9;
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);
-      const uint64_t qd = sdesc_sw128(smem_u32(dsm + kOffQ), 16, 1024);
-      const uint64_t dod = sdesc_sw128(smem_u32(dsm + kOffDO), 16, 1024);
+      // S = Q K^T reads Q and K; dP = dO V^T reads dO and V
+      const uint64_t ad = sdesc_sw128(smem_u32(dsm + (is_s ? kOffQ : kOffDO)), 16, 1024);
+      uint8_t* bbuf = is_s ? kbuf : vbuf;
+      const int nst = is_s ? kKStages : kVStages;
+      uint64_t* full = is_s ? sm.k_full : sm.v_full;
+      uint64_t* empty = is_s ? sm.k_empty : sm.v_empty;
+      uint64_t* done = is_s ? &sm.s_full : &sm.dp_full;
+      uint64_t* freed = is_s ? &sm.s_free : &sm.dp_free;
+      const uint32_t dt = tmem + (is_s ? TM_S : TM_DP);
+      const uint32_t wbase = is_s ? 64 : 90;  // wait-site codes
       auto koff = [](int kk) {
         return static_cast<uint64_t>(((kk >> 2) * (kTile / 2) + (kk & 3) * 32) >> 4);
       };
-      uint32_t use = 0, items = 0, sidx = 0;
+      uint32_t use = 0, items = 0, idx = 0;
       bool ok = true;
       for (uint32_t it = 0; ok; ++it) {
         const int ws = it & 1;
-        if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, 64)) break;
+        if (!W.wait(&sm.work_full[ws], (it >> 1) & 1, wbase)) break;
         if (sm.work_row[ws] < 0) break;
         const int n = sm.work_end[ws] - sm.work_beg[ws];
         if (n > 0) {
-          if (!W.wait(&sm.qd_full, items & 1, 65)) break;
+          if (!W.wait(&sm.qd_full, items & 1, wbase + 1)) break;
           ++items;
           for (int jj = 0; jj < n; ++jj) {
-            const int ks = use % kKStages, vs = use % kVStages;
-            if (!W.wait(&sm.k_full[ks], (use / kKStages) & 1, 66)) { ok = false; break; }
-            const uint64_t kd = sdesc_sw128(smem_u32(kbuf + ks * kTile), 16, 1024);
-            const uint64_t vd = sdesc_sw128(smem_u32(vbuf + vs * kTile), 16, 1024);
-            if (sidx > 0 && !W.wait(&sm.s_free, (sidx - 1) & 1, 67)) { ok = false; break; }
+            const int st = use % nst;
+            if (!W.wait(&full[st], (use / nst) & 1, wbase + 2)) { ok = false; break; }
+            // the compute warps have read this product's previous tile
+            if (idx > 0 && !W.wait(freed, (idx - 1) & 1, wbase + 3)) { ok = false; break; }
             fence_after();
+            const uint64_t bd = sdesc_sw128(smem_u32(bbuf + st * kTile), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              mma_ss(tmem + TM_S, qd + koff(kk), kd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
-            commit(&sm.s_full);
-            commit(&sm.k_empty[ks]);
-            if (sidx > 0 && !W.wait(&sm.dp_free, (sidx - 1) & 1, 68)) { ok = false; break; }
-            if (!W.wait(&sm.v_full[vs], (use / kVStages) & 1, 69)) { ok = false; break; }
-            fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-              mma_ss(tmem + TM_DP, dod + koff(kk), vd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
-            commit(&sm.dp_full);
-            commit(&sm.v_empty[vs]);
+              mma_ss(dt, ad + koff(kk), bd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
+            commit(done);
+            commit(&empty[st]);
             ++use;
-            ++sidx;
+            ++idx;
           }
           if (ok) commit(&sm.qd_empty);
         }
