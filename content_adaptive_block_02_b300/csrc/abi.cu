@@ -16,7 +16,7 @@ struct prism_plan {
 
 namespace prism {
 cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp,
-                           const float* lse, float* D, float* lse2, float* dQacc,
+                           const float* lse, float* D, float* nlse2, float* dQacc,
                            cudaStream_t st);
 cudaError_t launch_attn_fwd_simt(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
                                  const uint16_t* Vp, const int32_t* n_valid,
@@ -32,7 +32,7 @@ cudaError_t launch_attn_fwd_tc(const Plan& p, const uint16_t* Qp, const uint16_t
                                const int32_t* col_idx, float scale, uint16_t* Op, float* lse,
                                uint8_t* ws, cudaStream_t st);
 cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
-                                const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
+                                const uint16_t* Vp, const uint16_t* dOp, const float* nlse2,
                                 const float* D, const int32_t* n_valid, const int32_t* col_ptr,
                                 const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
                                 uint8_t* ws, uint16_t* dkvpart, cudaStream_t st);

@@ -223,13 +223,13 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(BwdArgs a) {
 
 }  // namespace
 
-// D[b,h,s] = sum_c dOp * Op (fp32); when lse2 is given, also
-// lse2 = lse * log2(e); when dQacc is given, that row of the accumulator is
+// D[b,h,s] = sum_c dOp * Op (fp32); when nlse2 is given, also
+// nlse2 = -lse * log2(e); when dQacc is given, that row of the accumulator is
 // cleared.  Four lanes per row of d channels (d <= 128: at most four 16-byte
 // pieces of O and of dO per lane, all loads issued before the first use).
 __global__ void bwd_pre_kernel(long long rows, int d, const uint16_t* __restrict__ Op,
                                const uint16_t* __restrict__ dOp, const float* __restrict__ lse,
-                               float* __restrict__ D, float* __restrict__ lse2,
+                               float* __restrict__ D, float* __restrict__ nlse2,
                                float* __restrict__ dQacc) {
   const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   const long long row = tid >> 2;
@@ -272,16 +272,16 @@ __global__ void bwd_pre_kernel(long long rows, int d, const uint16_t* __restrict
   s += __shfl_xor_sync(0xffffffffu, s, 2);
   if (live && sub == 0) {
     D[row] = s;
-    if (lse2 != nullptr) lse2[row] = lse[row] * 1.4426950408889634f;
+    if (nlse2 != nullptr) nlse2[row] = -lse[row] * 1.4426950408889634f;
   }
 }
 
 cudaError_t launch_bwd_pre(const Plan& p, const uint16_t* Op, const uint16_t* dOp,
-                           const float* lse, float* D, float* lse2, float* dQacc,
+                           const float* lse, float* D, float* nlse2, float* dQacc,
                            cudaStream_t st) {
   const long long rows = static_cast<long long>(p.cfg.B) * p.cfg.H * p.sz.Np;
   bwd_pre_kernel<<<static_cast<unsigned>((rows * 4 + 255) / 256), 256, 0, st>>>(
-      rows, p.cfg.d, Op, dOp, lse, D, lse2, dQacc);
+      rows, p.cfg.d, Op, dOp, lse, D, nlse2, dQacc);
   return cudaGetLastError();
 }
 

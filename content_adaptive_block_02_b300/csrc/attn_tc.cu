@@ -426,16 +426,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float lsum = 0.f;
         uint32_t pk[32];
         if (lim >= 64) {
-          float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+          // two keys per fp32x2 instruction: x = s * c - m, partial row sums
+          const f32x2 c2 = pack2(P.scale_log2, P.scale_log2), nm2 = pack2(-m, -m);
+          f32x2 ls2[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int k0 = 2 * e;
-            const float p0 = ex2(fmaf(__uint_as_float(s[k0 >> 5][k0 & 31]), P.scale_log2, -m));
-            const float p1 = ex2(fmaf(__uint_as_float(s[(k0 + 1) >> 5][(k0 + 1) & 31]), P.scale_log2, -m));
-            ls4[e & 3] += p0 + p1;
+            const f32x2 x2 = fma2(pack2(__uint_as_float(s[k0 >> 5][k0 & 31]),
+                                        __uint_as_float(s[(k0 + 1) >> 5][(k0 + 1) & 31])),
+                                  c2, nm2);
+            float x0, x1;
+            unpack2(x2, x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            ls2[e & 1] = add2(ls2[e & 1], pack2(p0, p1));
             pk[e] = pack_bf16x2(p0, p1);
           }
-          lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+          float a0, a1, b0, b1;
+          unpack2(ls2[0], a0, a1);
+          unpack2(ls2[1], b0, b1);
+          lsum = (a0 + b0) + (a1 + b1);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {

@@ -24,7 +24,7 @@
 //              query columns in halves; P^T, dS^T, epilogue dK * scale, dV
 //              -> bf16 (the halves split the 128 channels there).
 //   warp 8     producer: work counter, TMA loads of K_j, V_j (once per item)
-//              and of Q_i, dO_i, LSE_i * log2 e, D_i (2-stage ring) plus the
+//              and of Q_i, dO_i, -LSE_i * log2 e, D_i (2-stage ring) plus the
 //              stage's query-block real-token count.
 //   warp 9     issuer A: (1) and (3), which share the S/P columns, in the
 //              order 1_0 3_0 1_1 3_1 ...
@@ -62,7 +62,7 @@ struct BwdBars {
 constexpr size_t kSmemBytes = kOffBar + sizeof(BwdBars);
 
 struct BwdParams {
-  const float* lse2;  // LSE * log2(e)
+  const float* nlse2;  // -LSE * log2(e)
   const float* D;
   const int32_t* n_valid;
   const int32_t* col_ptr;
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + kTile / 2, &tmQ, &sm.qdo_full[s], 64, static_cast<int>(yq));
             tma_load_2d(st + kTile, &tmdO, &sm.qdo_full[s], 0, static_cast<int>(yq));
             tma_load_2d(st + kTile + kTile / 2, &tmdO, &sm.qdo_full[s], 64, static_cast<int>(yq));
-            bulk_load(st + 2 * kTile, P.lse2 + yq, 512, &sm.qdo_full[s]);
+            bulk_load(st + 2 * kTile, P.nlse2 + yq, 512, &sm.qdo_full[s]);
             bulk_load(st + 2 * kTile + 512, P.D + yq, 512, &sm.qdo_full[s]);
           }
           ++use;
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int k = 0; k < n; ++k) {
         const int s_ = (use + k) & 1;
-        // LSE_i and D_i arrive with Q_i / dO_i on the stage's barrier
+        // -LSE_i log2 e and D_i arrive with Q_i / dO_i on the stage's barrier
         ok = ok && W.wait(&sm.qdo_full[s_], ((use + k) >> 1) & 1, 40);
         // blocks of half a tile: bit 2 qh + kh of an entry's mask set = the
         // query half qh (this column half) does not attend the key half kh
@@ -366,15 +366,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sv[32];
             tmem_ld32(tmem + lb + TM_S + q0 + c * 32, sv);
             tmem_ld_wait();
+            // two queries per fp32x2 instruction: x = s * c - LSE log2 e
+            const f32x2 c2 = pack2(P.scale_log2, P.scale_log2);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
               const float4 L = lse4[c * 8 + g];
-              const float lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int q = c * 32 + g * 4 + e;
-                const float x = fmaf(__uint_as_float(sv[g * 4 + e]), P.scale_log2, -lv[e]);
-                p[q] = q < lim ? ex2(x) : 0.f;
+              for (int e = 0; e < 2; ++e) {
+                const int q = c * 32 + g * 4 + 2 * e;
+                const f32x2 x2 = fma2(pack2(__uint_as_float(sv[g * 4 + 2 * e]),
+                                            __uint_as_float(sv[g * 4 + 2 * e + 1])),
+                                      c2, e ? pack2(L.z, L.w) : pack2(L.x, L.y));
+                float x0, x1;
+                unpack2(x2, x0, x1);
+                p[q] = q < lim ? ex2(x0) : 0.f;
+                p[q + 1] = q + 1 < lim ? ex2(x1) : 0.f;
               }
             }
           }
@@ -413,13 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk
               const int ql = c * 32 + g * 8;  // local query index in this half
               const float4 da = D4[ql / 4], db4 = D4[ql / 4 + 1];
-              const float dv[8] = {da.x, da.y, da.z, da.w, db4.x, db4.y, db4.z, db4.w};
+              const f32x2 dv2[4] = {pack2(da.x, da.y), pack2(da.z, da.w), pack2(db4.x, db4.y),
+                                    pack2(db4.z, db4.w)};
               uint32_t w4[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float x0 = p[ql + 2 * e] * (__uint_as_float(dp[g * 8 + 2 * e]) - dv[2 * e]);
-                const float x1 =
-                    p[ql + 2 * e + 1] * (__uint_as_float(dp[g * 8 + 2 * e + 1]) - dv[2 * e + 1]);
+              for (int e = 0; e < 4; ++e) {  // two queries per fp32x2 instruction
+                const f32x2 ds2 = mul2(pack2(p[ql + 2 * e], p[ql + 2 * e + 1]),
+                                       sub2(pack2(__uint_as_float(dp[g * 8 + 2 * e]),
+                                                  __uint_as_float(dp[g * 8 + 2 * e + 1])),
+                                            dv2[e]));
+                float x0, x1;
+                unpack2(ds2, x0, x1);
                 w4[e] = pack_bf16x2(x0, x1);
               }
               const int chunk = ql >> 3;
@@ -479,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_t* Kp,
-                                const uint16_t* Vp, const uint16_t* dOp, const float* lse2,
+                                const uint16_t* Vp, const uint16_t* dOp, const float* nlse2,
                                 const float* D, const int32_t* n_valid, const int32_t* col_ptr,
                                 const int32_t* row_idx, float scale, uint16_t* dKp, uint16_t* dVp,
                                 uint8_t* ws, uint16_t* dkvpart, cudaStream_t st) {
@@ -490,7 +500,7 @@ cudaError_t launch_attn_dkdv_tc(const Plan& p, const uint16_t* Qp, const uint16_
       !make_tile_map(&tmV, Vp, rows_total) || !make_tile_map(&tmdO, dOp, rows_total))
     return cudaErrorInvalidValue;
   BwdParams a;
-  a.lse2 = lse2;
+  a.nlse2 = nlse2;
   a.D = D;
   a.n_valid = n_valid;
   a.col_ptr = col_ptr;

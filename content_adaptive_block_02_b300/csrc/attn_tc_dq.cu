@@ -366,13 +366,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++sidx;
         uint32_t pk[32];
         if (lim >= 64) {
+          // two keys per fp32x2 instruction: x = s * c - LSE log2 e, dS = P (dP - D)
+          const f32x2 c2 = pack2(P.scale_log2, P.scale_log2), nl2 = pack2(-lse2, -lse2);
+          const f32x2 D2 = pack2(Dr, Dr);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int k0 = 2 * e, k1 = k0 + 1;
-            const float p0 = ex2(fmaf(__uint_as_float(sv[k0 >> 5][k0 & 31]), P.scale_log2, -lse2));
-            const float p1 = ex2(fmaf(__uint_as_float(sv[k1 >> 5][k1 & 31]), P.scale_log2, -lse2));
-            pk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[k0 >> 5][k0 & 31]) - Dr),
-                                p1 * (__uint_as_float(dp[k1 >> 5][k1 & 31]) - Dr));
+            const f32x2 x2 = fma2(pack2(__uint_as_float(sv[k0 >> 5][k0 & 31]),
+                                        __uint_as_float(sv[k1 >> 5][k1 & 31])),
+                                  c2, nl2);
+            float x0, x1;
+            unpack2(x2, x0, x1);
+            const f32x2 ds2 = mul2(pack2(ex2(x0), ex2(x1)),
+                                   sub2(pack2(__uint_as_float(dp[k0 >> 5][k0 & 31]),
+                                              __uint_as_float(dp[k1 >> 5][k1 & 31])),
+                                        D2));
+            float d0, d1;
+            unpack2(ds2, d0, d1);
+            pk[e] = pack_bf16x2(d0, d1);
           }
         } else {
 #pragma unroll

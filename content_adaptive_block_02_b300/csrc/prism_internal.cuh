@@ -31,7 +31,7 @@ struct Plan {
 //   off_bitmask     u32   [B*H*nb*nw]    selection bitmask, nw = ceil(nb/32)
 //   off_scores      fp32  [2*B*H*nb*nb]  block scores (unscaled dots), hi then lo
 //   off_D           fp32  [B*H*Np]       rowsum(dO * O) for the backward
-//   off_lse2        fp32  [B*H*Np]       LSE * log2(e) for the backward
+//   off_lse2        fp32  [B*H*Np]       -LSE * log2(e) for the backward
 //   off_dq          fp32  [B*H*Np*d]     dQ accumulator of the CUDA-core backward
 //                                        (empty for a tensor-core plan)
 //   off_nsel        int32 [B*H*nb]       (multi-tile blocks) real tokens of the block
