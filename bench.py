@@ -325,10 +325,15 @@ class Runner:
 
 
 def hbm_summary(w, plan, fused, call_ms, kern_ms, pk):
-    """GB/s of the memory-bound calls from their algorithmic bytes."""
+    """GB/s of the memory-bound kernels from their algorithmic bytes, timed by
+    the library's own events around each kernel where it has a slot (zone
+    statistics, permutation + pooling, bwd_pre), else around the call."""
     by = call_bytes(w, plan, fused)
     t = dict(call_ms)
     t["bwd_pre"] = kern_ms["bwd_pre"]
+    t["zone_stats"] = kern_ms.get("zone_stats", t["zone_stats"])
+    by["permute_pool"] = by.pop("assign_permute")
+    t["permute_pool"] = kern_ms.get("permute_pool", t["assign_permute"])
     out = {}
     for k, b in by.items():
         ms = t[k]

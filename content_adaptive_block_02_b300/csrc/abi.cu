@@ -292,8 +292,9 @@ int prism_zone_stats(const prism_plan_t* plan, const uint16_t* V, const uint16_t
   PRISM_CHECK_PTR(V);
   PRISM_CHECK_PTR(a2v);
   PRISM_CHECK_PTR(stats);
-  PRISM_CUDA(prism::launch_zone_stats(plan->p, V, a2v, nullptr, stats,
-                                      static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PRISM_TRACED(PRISM_TRACE_ZONE_STATS,
+               prism::launch_zone_stats(plan->p, V, a2v, nullptr, stats, st));
   return PRISM_OK;
 }
 
@@ -315,8 +316,9 @@ int prism_zone_stats_norms(const prism_plan_t* plan, const uint16_t* V, const fl
   PRISM_CHECK_PTR(V);
   PRISM_CHECK_PTR(n);
   PRISM_CHECK_PTR(stats);
-  PRISM_CUDA(prism::launch_zone_stats(plan->p, V, nullptr, n, stats,
-                                      static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PRISM_TRACED(PRISM_TRACE_ZONE_STATS,
+               prism::launch_zone_stats(plan->p, V, nullptr, n, stats, st));
   return PRISM_OK;
 }
 
@@ -336,8 +338,9 @@ int prism_assign_and_permute(const prism_plan_t* plan, const float* stats, const
   PRISM_CHECK_PTR(n_valid);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   PRISM_CUDA(prism::launch_assign(plan->p, stats, shape_id, shape_tie, st));
-  PRISM_CUDA(prism::launch_permute_pool(plan->p, shape_id, Q, K, V, perm, inv, Qp, Kp, Vp, Qbar,
-                                        Qbar_lo, Kbar, Kbar_lo, n_valid, nullptr, st));
+  PRISM_TRACED(PRISM_TRACE_PERMUTE_POOL,
+               prism::launch_permute_pool(plan->p, shape_id, Q, K, V, perm, inv, Qp, Kp, Vp,
+                                          Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid, nullptr, st));
   return PRISM_OK;
 }
 
@@ -353,10 +356,11 @@ int prism_permute_shapes(const prism_plan_t* plan, const uint8_t* shape_id, cons
   PRISM_CHECK_PTR(Qbar); PRISM_CHECK_PTR(Qbar_lo);
   PRISM_CHECK_PTR(Kbar); PRISM_CHECK_PTR(Kbar_lo);
   PRISM_CHECK_PTR(n_valid); PRISM_CHECK_PTR(ws);
-  PRISM_CUDA(prism::launch_permute_pool(plan->p, shape_id, Q, K, V, perm, inv, Qp, Kp, Vp, Qbar,
-                                        Qbar_lo, Kbar, Kbar_lo, n_valid,
-                                        static_cast<uint32_t*>(ws),
-                                        static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PRISM_TRACED(PRISM_TRACE_PERMUTE_POOL,
+               prism::launch_permute_pool(plan->p, shape_id, Q, K, V, perm, inv, Qp, Kp, Vp,
+                                          Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid,
+                                          static_cast<uint32_t*>(ws), st));
   return PRISM_OK;
 }
 
@@ -373,10 +377,13 @@ int prism_block_select(const prism_plan_t* plan, const uint8_t* shape_id, const 
   PRISM_CHECK_PTR(row_ptr); PRISM_CHECK_PTR(col_idx);
   PRISM_CHECK_PTR(col_ptr); PRISM_CHECK_PTR(row_idx);
   PRISM_CHECK_PTR(sel_tie); PRISM_CHECK_PTR(ws);
-  PRISM_CUDA(prism::launch_select(plan->p, shape_id, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid,
-                                  sel_tie,
-                                  row_ptr, col_idx, col_ptr, row_idx,
-                                  static_cast<uint8_t*>(ws), static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PRISM_TRACED(PRISM_TRACE_SELECT,
+               prism::launch_select(plan->p, shape_id, Qbar, Qbar_lo, Kbar, Kbar_lo, n_valid,
+                                    sel_tie, row_ptr, col_idx, col_ptr, row_idx,
+                                    static_cast<uint8_t*>(ws), st,
+                                    plan->trace[2 * PRISM_TRACE_SCORE],
+                                    plan->trace[2 * PRISM_TRACE_SCORE + 1]));
   return PRISM_OK;
 }
 

@@ -63,7 +63,9 @@ constexpr int kPermThreads = 256;
 // fixed-order double-float reduction over the token groups, and a
 // double-float division by the real-token count -- about 46 significant
 // bits, without fp64 arithmetic.
-__global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
+// Three CTAs per SM (80 registers) with two tokens in flight per thread
+// move more bytes at once than two CTAs with four (128 registers).
+__global__ void __launch_bounds__(kPermThreads, 3) permute_pool_kernel(
     prism_config_t c, int nzH, int nzW, int bpz, int Z, int nb, int nslots, int U, long long Np,
     Menu menu, const uint8_t* __restrict__ shape_id, const uint16_t* __restrict__ Q,
     const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int32_t* __restrict__ perm,
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_pool_kernel(
 #pragma unroll
   for (int k = 0; k < 8; ++k) sq[k] = sk[k] = df{0.f, 0.f};
   const long long slot0 = static_cast<long long>(blk) * U;
-  constexpr int IF = 4;  // tokens per thread in flight
+  constexpr int IF = 2;  // tokens per thread in flight
   for (int k0 = grp; k0 < SB; k0 += IF * G) {
     uint4 vq[IF], vk[IF], vv[IF];
     long long nn[IF];

@@ -83,7 +83,8 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
                           const float* Ql, const float* Kh, const float* Kl,
                           const int32_t* n_valid, uint8_t* sel_tie,
                           int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
-                          int32_t* row_idx, uint8_t* ws, cudaStream_t st);
+                          int32_t* row_idx, uint8_t* ws, cudaStream_t st,
+                          cudaEvent_t score_begin = nullptr, cudaEvent_t score_end = nullptr);
 
 // ----------------------------------------------------- device helpers -----
 
@@ -141,6 +142,39 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 // A value carried as an unevaluated sum hi + lo of two fp32 numbers
 // (|lo| <= ulp(hi)/2).  Every operation below uses explicitly rounded
 // intrinsics so that the compiler cannot contract them into FMAs.
+// Packed pairs of fp32 for the fp32x2 fma / add / sub / mul of sm_100-class
+// SMs: one instruction for two lanes, each rounded exactly as the scalar
+// operation would be.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 struct df {
   float hi, lo;
 };

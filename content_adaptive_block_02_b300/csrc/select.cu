@@ -730,7 +730,8 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
                           const float* Ql, const float* Kh, const float* Kl,
                           const int32_t* n_valid, uint8_t* sel_tie,
                           int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
-                          int32_t* row_idx, uint8_t* ws, cudaStream_t st) {
+                          int32_t* row_idx, uint8_t* ws, cudaStream_t st,
+                          cudaEvent_t score_begin, cudaEvent_t score_end) {
   const prism_config_t& c = p.cfg;
   // the selection runs over the block table's units (tiles, or half tiles);
   // the lists handed on are over tiles
@@ -768,7 +769,10 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
     n_valid = n_sel;
   }
   dim3 g((nb + kTJ - 1) / kTJ, (nb + kTI - 1) / kTI, c.B * c.H);
+  // optional timing marks around the score kernel alone
+  if (score_begin != nullptr && (e = cudaEventRecord(score_begin, st)) != cudaSuccess) return e;
   score_dot2_kernel<<<g, 256, 0, st>>>(nb, c.d, Qh, Ql, Kh, Kl, Shi, Slo);
+  if (score_end != nullptr && (e = cudaEventRecord(score_end, st)) != cudaSuccess) return e;
   SelParams sp;
   sp.nb = nb;
   sp.nwords = nwords;

@@ -287,9 +287,7 @@ __global__ void __launch_bounds__(kStatsThreads) zone_stats_kernel(
 constexpr int kPT = 4, kPH = 16, kPW = 16;
 
 // Packed pairs of fp32 (the two channels of a bf16x2 word) for the fp32x2
-// add / sub / fma of sm_100-class SMs: one instruction for both channels,
-// each rounded exactly as the scalar operation would be.
-typedef unsigned long long f32x2;
+// arithmetic of sm_100-class SMs (add2 / sub2 / mul2 / fma2, shared helpers).
 __device__ __forceinline__ f32x2 unpack2(uint32_t u) {  // bf16x2 -> (lo, hi) fp32
   f32x2 r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(u << 16), "r"(u & 0xffff0000u));
@@ -298,26 +296,6 @@ __device__ __forceinline__ f32x2 unpack2(uint32_t u) {  // bf16x2 -> (lo, hi) fp
 __device__ __forceinline__ f32x2 splat2(float a) {
   f32x2 r;
   asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(a));
-  return r;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
 __device__ __forceinline__ float hsum2(f32x2 a) {

@@ -223,7 +223,8 @@ class Plan:
     def device_status(self, ws: torch.Tensor) -> int:
         return lib().prism_device_status(self.h, _ptr(ws), _stream())
 
-    TRACE_SLOTS = ("attn_fwd", "bwd_pre", "attn_dkdv", "attn_dq")
+    TRACE_SLOTS = ("attn_fwd", "bwd_pre", "attn_dkdv", "attn_dq", "zone_stats", "permute_pool",
+                   "score", "select")
 
     def set_trace_events(self, events=None):
         """prism_plan_set_trace_events: `events` maps a slot name of

@@ -169,26 +169,36 @@ int prism_device_status(const prism_plan_t* plan, const void* ws, void* stream);
 const char* prism_strerror(int code);
 
 /* Kernel timing hooks.  The paper has no counterpart: this lets a caller
- * time each attention kernel on its own with CUDA events, without a
+ * time each kernel of the path on its own with CUDA events, without a
  * profiler.  Slots:
- *   PRISM_TRACE_ATTN_FWD   the forward attention kernel
- *   PRISM_TRACE_BWD_PRE    rowsum(dO * O) (and log2-scaled LSE) before the backward
- *   PRISM_TRACE_ATTN_DKDV  the dK/dV kernel (tensor cores) or the CUDA-core backward
- *   PRISM_TRACE_ATTN_DQ    the dQ kernel (tensor cores) or the dQ conversion
+ *   PRISM_TRACE_ATTN_FWD      the forward attention kernel
+ *   PRISM_TRACE_BWD_PRE       rowsum(dO * O) (and -LSE log2 e) before the backward
+ *   PRISM_TRACE_ATTN_DKDV     the dK/dV kernel (tensor cores) or the CUDA-core backward
+ *   PRISM_TRACE_ATTN_DQ       the dQ kernel (tensor cores) or the dQ conversion
+ *   PRISM_TRACE_ZONE_STATS    the zone-statistics kernel (prism_zone_stats,
+ *                             prism_zone_stats_norms)
+ *   PRISM_TRACE_PERMUTE_POOL  the permutation + pooling kernel
+ *                             (prism_assign_and_permute, prism_permute_shapes)
+ *   PRISM_TRACE_SCORE         the block-score kernel inside prism_block_select
+ *   PRISM_TRACE_SELECT        every kernel of prism_block_select
  * events: NULL (clears every slot) or an array of 2 * PRISM_TRACE_SLOTS
  * cudaEvent_t handles, begin then end for each slot; a NULL handle leaves
  * that mark out.  The handles are copied into the plan and stay owned by the
  * caller, who must keep them alive while the plan records into them.  While
- * set, prism_sparse_attn_fwd / prism_sparse_attn_bwd record the begin event
- * on the call's stream just before the slot's kernel is enqueued and the end
- * event just after.  Not synchronised with other threads using the same plan.
+ * set, the calls above record the begin event on the call's stream just
+ * before the slot's kernels are enqueued and the end event just after.  Not
+ * synchronised with other threads using the same plan.
  * Errors: PRISM_ERR_ARG (plan NULL). */
-#define PRISM_TRACE_SLOTS 4
+#define PRISM_TRACE_SLOTS 8
 enum {
   PRISM_TRACE_ATTN_FWD = 0,
   PRISM_TRACE_BWD_PRE = 1,
   PRISM_TRACE_ATTN_DKDV = 2,
-  PRISM_TRACE_ATTN_DQ = 3
+  PRISM_TRACE_ATTN_DQ = 3,
+  PRISM_TRACE_ZONE_STATS = 4,
+  PRISM_TRACE_PERMUTE_POOL = 5,
+  PRISM_TRACE_SCORE = 6,
+  PRISM_TRACE_SELECT = 7
 };
 int prism_plan_set_trace_events(prism_plan_t* plan, void* const* events);
 
