@@ -228,10 +228,13 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
     z.ws_csr_mask = off; off = align256(off + static_cast<size_t>(z.max_pairs));
     z.ws_csc_mask = off; off = align256(off + static_cast<size_t>(z.max_pairs));
   }
-  // key ranges of at most 512 blocks (32 MB of K and V per head) once a head's
-  // K and V outgrow L2; the partial results are capped at 32 GB
+  // once a head has more than 1024 key blocks, equal key ranges of at most
+  // 900 blocks (56 MB of K and V per head: a range of the head stays in L2);
+  // the partial results are capped at 32 GB
   z.key_chunks = 1;
-  const int kcb = c.key_chunk_blocks > 0 ? c.key_chunk_blocks : (z.nb > 1024 ? 512 : z.nb);
+  const int kcb = c.key_chunk_blocks > 0
+                      ? c.key_chunk_blocks
+                      : (z.nb > 1024 ? (z.nb + (z.nb + 899) / 900 - 1) / ((z.nb + 899) / 900) : z.nb);
   if (z.tensor_core_fwd && kcb < z.nb) {
     long long C = (z.nb + kcb - 1) / kcb;
     if (C > 64) C = 64;

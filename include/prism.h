@@ -84,9 +84,9 @@ typedef struct prism_config {
                              is in flight when they return.                       */
   int key_chunk_blocks;   /* key blocks per range of the tensor-core forward / dQ
                              kernels (prism_sizes_t.key_chunks): 0 = automatic
-                             (ranges of 512 blocks once a head has more than 1024
-                             key blocks, else one range); > 0 = ranges of this
-                             many blocks (at most 64 ranges)                      */
+                             (ceil(nb / 900) equal ranges once a head has more
+                             than 1024 key blocks, else one range); > 0 = ranges
+                             of this many blocks (at most 64 ranges)              */
   double class_tau[PRISM_MAX_CLASSES - 1];
                           /* block-size classes (Table 10 caption: thresholds
                              tau_128 / tau_256; Table 11: classes C_64, C_128,
