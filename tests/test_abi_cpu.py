@@ -46,10 +46,11 @@ def test_2k_sizes_are_the_documented_ones(L):
     p = prism.Plan(synth.WORKLOADS["2k"])
     assert (p.sz.Np, p.sz.Z, p.sz.nb) == (322_560, 420, 2520)
     assert p.sz.tensor_core_fwd == 1
-    # key ranges of at most 512 blocks once a head's K / V outgrow L2
-    assert (p.sz.key_chunks, p.sz.chunk_blocks) == (5, 504)
+    # ceil(nb / 900) equal key ranges once a head has more than 1024 key blocks
+    assert (p.sz.key_chunks, p.sz.chunk_blocks) == (3, 840)
     assert prism.Plan(synth.WORKLOADS["720p"]).sz.key_chunks == 1
-    assert prism.Plan(synth.WORKLOADS["1080p"]).sz.key_chunks == 4
+    assert (prism.Plan(synth.WORKLOADS["1080p"]).sz.key_chunks,
+            prism.Plan(synth.WORKLOADS["1080p"]).sz.chunk_blocks) == (2, 840)
     small = synth.WORKLOADS["720p"].with_(T=6, Hg=40, W=48, H=2)
     q = prism.Plan(small, key_chunk_blocks=16)
     assert (q.sz.nb, q.sz.key_chunks, q.sz.chunk_blocks) == (108, 7, 16)
