@@ -40,7 +40,7 @@ int main(void) {
   CHECK(prism_plan_query(plan, &z) == PRISM_OK);
   CHECK(z.Np == 322560 && z.Z == 420 && z.nb == 2520);
   CHECK(z.n_admissible == 2 && z.admissible[0] == 0 && z.admissible[1] == 1);
-  CHECK(z.tensor_core_fwd == 1 && z.key_chunks == 5 && z.chunk_blocks == 504);
+  CHECK(z.tensor_core_fwd == 1 && z.key_chunks == 3 && z.chunk_blocks == 840);
   CHECK(z.ws_bytes > 0);
   CHECK(prism_plan_set_trace_events(plan, NULL) == PRISM_OK);
   prism_plan_destroy(plan);
