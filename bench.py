@@ -50,12 +50,13 @@ def pair_flops(w):
     return {"fwd": 4 * u, "bwd": 10 * u, "attn_fwd": 4 * u, "attn_dkdv": 8 * u, "attn_dq": 6 * u}
 # DRAM bytes (read + written) per launch of the attention kernels on the 2K-like
 # workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum,
-# 1 pass) of the kernel code whose digest (source_digest) is given; reported
-# only for that workload, and as null once the kernel's code has changed since.
+# 1 pass) of the kernel code whose digest (source_digest) is given, with the
+# plan's number of key ranges; reported only for that workload and range count,
+# and as null once the kernel's code has changed since.
 TRAFFIC_2K = {
-    "attn_fwd_tc_kernel": ("attn_tc.cu", None, 12.50e9 + 8.07e9),
-    "attn_dkdv_tc_kernel": ("attn_tc_dkdv.cu", None, 26.09e9 + 19.80e9),
-    "attn_dq_tc_kernel": ("attn_tc_dq.cu", None, 20.80e9 + 7.74e9),
+    "attn_fwd_tc_kernel": ("attn_tc.cu", "e62fc53d1541ffef", 3, 24.23e9 + 5.50e9),
+    "attn_dkdv_tc_kernel": ("attn_tc_dkdv.cu", "d1fc1f9843f34902", 3, 20.39e9 + 11.89e9),
+    "attn_dq_tc_kernel": ("attn_tc_dq.cu", "667fec371cf742e6", 3, 33.01e9 + 4.98e9),
 }
 
 
@@ -70,12 +71,13 @@ def source_digest(name: str) -> str:
     return hashlib.sha256("\n".join(c for c in code if c).encode()).hexdigest()[:16]
 
 
-def measured_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` if its code is still the captured one."""
+def measured_traffic(kernel: str, key_ranges: int):
+    """DRAM bytes per launch of `kernel` if its code and the plan's key ranges
+    are still the captured ones."""
     ent = TRAFFIC_2K.get(kernel)
-    if ent is None or ent[1] is None:
+    if ent is None or ent[1] is None or ent[2] != key_ranges:
         return None
-    return ent[2] if source_digest(ent[0]) == ent[1] else None
+    return ent[3] if source_digest(ent[0]) == ent[1] else None
 
 
 def peaks():
@@ -484,8 +486,8 @@ def run_ours(args, w):
                                                                  clk_sum["sm_max_mhz"]), 4)
                                            if clk_sum.get("sm_mhz") else None),
                      "flop_per_launch": pairs * kern_flop[dom],
-                     "traffic": (measured_traffic(dom_name)
-                                 if w.name == "2k" and args.key_chunk_blocks == 0 else None)},
+                     "traffic": (measured_traffic(dom_name, att.plan.sz.key_chunks)
+                                 if w.name == "2k" else None)},
         "e2e": {"value": round(flop_all / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
