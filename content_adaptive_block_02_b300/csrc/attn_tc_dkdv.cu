@@ -32,7 +32,8 @@
 //              as soon as the compute warps have read this one.
 //   A tcgen05.mma issue blocks while the tensor pipe's queue is full; with two
 //   issuing threads, one thread's barrier waits overlap the other's MMAs.
-// Tensor memory: S/P [0,128), dP [128,256), dV [256,384), dK [384,512).
+// Tensor memory: S/P [0,128) (P^T of query half h as bf16 pairs in
+// [64h, 64h + 32)), dP [128,256), dV [256,384), dK [384,512).
 #include "tc_common.cuh"
 
 namespace prism {
@@ -248,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               fence_after();
 #pragma unroll
               for (int kk = 0; kk < kS / 16; ++kk)
-                mma_ts(tmem + TM_DV, tmem + TM_S + kk * 8, dod_n + noff(kk), id_kn,
+                mma_ts(tmem + TM_DV, tmem + TM_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                       dod_n + noff(kk), id_kn,
                        (k > 0 || kk > 0) ? 1u : 0u);
               commit(&sm.qdo_empty[st]);
             } else {
@@ -299,11 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // key row == TMEM lane
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
     const int q0 = half * 64;  // first query column (and first channel) of this half
-    // Warps w and w+4 meet at a named barrier (64 threads) once per query
-    // block and once per work item.  A named barrier has no time limit, so
-    // the two never leave a loop on their own: every bounded wait only clears
-    // `ok`, the flags are exchanged at each meeting, and both warps leave
-    // together at the first meeting after either of them failed.
+    // Warps w and w+4 meet at a named barrier (64 threads) once per work
+    // item.  A named barrier has no time limit, so the two never leave the
+    // item loop on their own: a failed bounded wait clears `ok` and ends the
+    // query-block loop (every later wait of the other warp then fails at
+    // once on the abort flag), the flags are exchanged at each meeting, and
+    // both warps leave together at the first meeting after either failed.
     uint32_t xpar = 0;
     auto meet = [&](bool mine) -> bool {
       mine = __all_sync(0xffffffffu, mine);  // one flag per warp
@@ -358,8 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- P^T = exp(S^T * scale - LSE) on this half of the queries ----
         ok = __all_sync(0xffffffffu, ok && W.wait(&sm.s_full, scnt & 1, 42));
         ++scnt;
+        if (!ok) break;
         float p[64];
-        if (ok) {
+        {
           fence_after();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -385,15 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // both halves have read S^T before P^T (half as wide) is written over it
-        ok = meet(ok);
-        if (!ok) break;
+        // P^T (bf16 pairs) over the first 32 of this half's own 64 S^T
+        // columns, which only this thread's row has read: no wait for the
+        // other half
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[h * 32 + 2 * e], p[h * 32 + 2 * e + 1]);
-          tmem_st16(tmem + lb + TM_S + half * 32 + h * 16, pk);
+          tmem_st16(tmem + lb + TM_S + q0 + h * 16, pk);
         }
         tmem_st_wait();
         fence_before();
