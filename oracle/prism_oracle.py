@@ -894,15 +894,19 @@ def attn_bwd(w, Qp, Kp, Vp, dOp, n_valid, lists, scale, rows_only=None, o_bf16=F
 
 
 def attn_bwd_key_blocks(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, L, key_blocks, S, scale,
-                        o_bf16=False):
+                        o_bf16=False, abs_terms=False):
     """dK and dV of the key blocks ``key_blocks`` of one (b, h): the same VJP
     as ``attn_bwd_row`` summed over every query block whose list L[i] holds
     one of them, with only those key blocks' columns formed in full (each
     query row still needs its whole softmax for P and its whole O for D).
-    Returns {j: (dK_j [S, d], dV_j [S, d])}, rows past n_valid[j] zero."""
+    Returns {j: (dK_j [S, d], dV_j [S, d])}, rows past n_valid[j] zero; with
+    ``abs_terms`` {j: (dK_j, dV_j, dK_abs_j)}, dK_abs_j the sizes of
+    ``attn_bwd_row`` (scale sum_i b_i P_ij |Q_i|, per unit roundoff of the O
+    that D is formed from) over the same query blocks."""
     d = Qp_bh.shape[1]
     want = set(int(j) for j in key_blocks)
-    out = {j: (np.zeros((S, d)), np.zeros((S, d))) for j in want}
+    out = {j: (np.zeros((S, d)), np.zeros((S, d))) + ((np.zeros((S, d)),) if abs_terms else ())
+           for j in want}
     for i, sel in enumerate(L):
         if sel is None or len(sel) == 0 or not want.intersection(int(j) for j in sel):
             continue
@@ -916,6 +920,8 @@ def attn_bwd_key_blocks(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, L, key_blocks, 
         P = e / e.sum(axis=1, keepdims=True)
         o = P @ v
         Dr = (do * (round_bf16(o) if o_bf16 else o)).sum(axis=1, keepdims=True)
+        if abs_terms:
+            b = (np.abs(do) * (np.abs(o) + P @ np.abs(v))).sum(axis=1, keepdims=True)
         off = 0
         for j in sel:
             nv = int(n_valid_bh[j])
@@ -925,6 +931,8 @@ def attn_bwd_key_blocks(Qp_bh, Kp_bh, Vp_bh, dOp_bh, n_valid_bh, L, key_blocks, 
                 dSj = Pj * (do @ v[off:off + nv].T - Dr)
                 out[j][0][:nv] += (dSj.T @ q) * scale
                 out[j][1][:nv] += Pj.T @ do
+                if abs_terms:
+                    out[j][2][:nv] += ((Pj * b).T @ np.abs(q)) * scale
             off += nv
     return out
 

@@ -108,16 +108,19 @@ def test_128_blocks_selection_settings(kw):
                                             ("2k", [7], (0, 10 ** 6))])
 def test_full_size_sampled(name, heads, kcb):
     """Every query block's list of the sampled heads, O / LSE / dQ on sampled
-    query blocks, dK / dV on 8 sampled key blocks.  At 2K the attention
-    kernels run twice, with the key ranges of the bench (5 ranges, bf16
-    partial results combined afterwards) and with one pass over each list, and
-    both are held to the contract; the report gives the error of each."""
+    query blocks, dK / dV on 8 sampled key blocks (dK held element by element
+    to the contract plus its sensitivity to the forward's bf16 O, see
+    parity_util.compare_sampled).  At 2K the attention kernels run twice,
+    with the key ranges of the bench (bf16 partial results combined
+    afterwards) and with one pass over each list, and both are held to the
+    contract; the report gives the error of each."""
     rep = pu.compare_sampled(synth.WORKLOADS[name], heads, key_chunk_blocks=kcb)
     print(name, rep)
-    assert rep["O"] <= pu.O_TOL and rep["dQ"] <= pu.G_TOL and rep["dKV"] <= pu.G_TOL
+    assert rep["O"] <= pu.O_TOL and rep["dQ"] <= pu.G_TOL and rep["dKV"] <= pu.ILL_COND_TOL
     assert rep["key_blocks_compared"] >= 8 * len(heads)
     if name == "2k":
-        assert [r["key_chunks"] for r in rep["runs"]] == [5, 1]
+        ranges = prism.Plan(synth.WORKLOADS[name]).sz.key_chunks
+        assert ranges > 1 and [r["key_chunks"] for r in rep["runs"]] == [ranges, 1]
 
 
 def test_key_feature_variance_variant():

@@ -892,6 +892,16 @@ def test_key_block_gradients_equal_the_full_backward():
             np.testing.assert_allclose(got[j][0], dK[0, 0, j * S:(j + 1) * S], atol=1e-13)
             np.testing.assert_allclose(got[j][1], dV[0, 0, j * S:(j + 1) * S], atol=1e-13)
         assert max(np.abs(got[j][0]).max() for j in kb) > 0
+    # the dK sizes (per unit roundoff of the O behind D) are the full
+    # backward's, whose per-row terms the brute-force pin above holds
+    _, _, _, _, aK = orc.attn_bwd(w, r["Qp"], r["Kp"], r["Vp"], r["dOp"], r["n_valid"],
+                                  r["lists"], r["scale"], o_bf16=True, abs_terms=True)
+    got = orc.attn_bwd_key_blocks(r["Qp"][0, 0], r["Kp"][0, 0], r["Vp"][0, 0], r["dOp"][0, 0],
+                                  r["n_valid"][0, 0], L, kb, S, r["scale"], o_bf16=True,
+                                  abs_terms=True)
+    for j in kb:
+        np.testing.assert_allclose(got[j][2], aK[0, 0, j * S:(j + 1) * S], rtol=1e-12, atol=1e-300)
+    assert max(got[j][2].max() for j in kb) > 0
 
 
 # ------------------------------------------------- library and structure ----
