@@ -176,6 +176,10 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
     if (!any) return PRISM_ERR_NO_ADMISSIBLE_SHAPE;
   }
   z.half_tile = 2 * classes[0] == c.block_tokens ? 1 : 0;
+  // a zone with padding cannot take the half-tile class (both halves of a
+  // shared tile must be real): it needs a class of at least a tile
+  if (z.half_tile && n_classes == 1 && (z.Tp != c.T || z.Hp != c.Hg || z.Wp != c.W))
+    return PRISM_ERR_NO_ADMISSIBLE_SHAPE;
   z.multi_tile = (classes[n_classes - 1] > c.block_tokens || z.half_tile) ? 1 : 0;
   z.slot_tokens = z.half_tile ? c.block_tokens / 2 : c.block_tokens;
   z.blocks_per_zone = static_cast<int>(vol / c.block_tokens);

@@ -11,29 +11,41 @@
 // blocks i that selected it (CSC), restricted to one range of query blocks
 // when the plan walks them in ranges (partial dK / dV per range, summed in
 // combine.cu).  For each i, four 128x128x128 products:
-//   (1) S^T  = K_j Q_i^T           A = K_j (smem),  B = Q_i (smem)   -> TMEM S
-//   (2) dP^T = V_j dO_i^T          A = V_j (smem),  B = dO_i (smem)  -> TMEM dP
+//   (1) S^T  = K_j Q_i^T           A = K_j (smem),  B = Q_i (smem)   -> TMEM
+//   (2) dP^T = V_j dO_i^T          A = V_j (smem),  B = dO_i (smem)  -> TMEM
 //       P^T = exp(S^T * scale - LSE_i)     (row = key, column = query)
 //       dS^T = P^T * (dP^T - D_i)
-//   (3) dV  += P^T dO_i            A = P^T (TMEM, written over S), B = dO_i (MN-major)
+//   (3) dV  += P^T dO_i            A = P^T (TMEM, written over S^T), B = dO_i (MN-major)
 //   (4) dK  += dS^T Q_i            A = dS^T (smem, K-major), B = Q_i (MN-major)
+// S^T and dP^T of a query block take the two 128-column regions of tensor
+// memory in turn: block g's S^T (then its P^T) goes in region g % 2, its
+// dP^T in the other.  So the next S^T goes where this block's dP^T was, as
+// soon as the compute warps have read it, without waiting for (3) to read
+// this block's P^T; the next dP^T goes where this block's P^T was, after (3).
 //
-// Roles (352 threads, one persistent CTA per SM):
+// Roles (384 threads, one persistent CTA per SM):
 //   warps 0-7  compute, two warpgroups: warps w and w+4 own the key rows of
 //              TMEM lane quarter w%4 (thread = key row) and split the 128
 //              query columns in halves; P^T, dS^T, epilogue dK * scale, dV
 //              -> bf16 (the halves split the 128 channels there).
 //   warp 8     producer: work counter, TMA loads of K_j, V_j (once per item)
 //              and of Q_i, dO_i, -LSE_i * log2 e, D_i (2-stage ring) plus the
-//              stage's query-block real-token count.
-//   warp 9     issuer A: (1) and (3), which share the S/P columns, in the
-//              order 1_0 3_0 1_1 3_1 ...
-//   warp 10    issuer B: (2) and (4); dP^T of the next query block is issued
-//              as soon as the compute warps have read this one.
-//   A tcgen05.mma issue blocks while the tensor pipe's queue is full; with two
-//   issuing threads, one thread's barrier waits overlap the other's MMAs.
-// Tensor memory: S/P [0,128) (P^T of query half h as bf16 pairs in
-// [64h, 64h + 32)), dP [128,256), dV [256,384), dK [384,512).
+//              stage's query-block real-token count.  A stage's dO part is
+//              free after (3), its Q part (with -LSE log2 e and D) only after
+//              (4), and each is reloaded as soon as it is free: the Q part's
+//              reload is on the loop that bounds the kernel (the next S^T
+//              needs it), so it carries half the bytes.
+//   warp 9     issuer of (1).
+//   warp 10    issuer of (3) and (2), in the order 2_0 3_0 2_1 3_1 2_2 ...:
+//              (2) of the next block overwrites the P^T that (3) of this
+//              block reads, and MMAs of one thread run in issue order.
+//   warp 11    issuer of (4).
+//   One thread issues a tcgen05.mma only every ~120 cycles, about twice the
+//   time the tensor pipe needs for a 128 x 128 x 16 product; three issuing
+//   threads on three SM sub-partitions keep the pipe fed.
+// Tensor memory: regions [0,128) and [128,256) (S^T / P^T of one block, dP^T
+// of the other; P^T of query half h as bf16 pairs in the region's columns
+// [64h, 64h + 32)), dV [256,384), dK [384,512).
 #include "tc_common.cuh"
 
 namespace prism {
@@ -43,15 +55,23 @@ using namespace tc;
 constexpr int kS = 128, kD = 128;
 constexpr int kTile = kS * kD * 2;           // 32 KB
 constexpr int kStage = 2 * kTile + 1024;     // Q, dO, LSE (512 B), D (512 B)
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kCompute = 256;
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
+// S^T / P^T of query block g in region tm_r(g & 1), its dP^T in the other
+__device__ __forceinline__ uint32_t tm_r(uint32_t parity) { return parity ? 128u : 0u; }
+constexpr uint32_t TM_DV = 256, TM_DK = 384;
 constexpr int kOffV = kTile, kOffStage = 2 * kTile, kOffDS = 2 * kTile + 2 * kStage;
 constexpr int kOffBar = kOffDS + kTile;
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2];
-  uint64_t s_full, dp_full, dp_free, p_ready, ds_ready, ds_empty;
+  uint64_t kv_full, kv_empty;
+  // a stage's Q, -LSE log2 e and D (read until (4)) and its dO (read until
+  // (3)) have their own barriers, so each part is reloaded as soon as it is free
+  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+  uint64_t s_full, dp_free, ds_ready, ds_empty;
+  // one barrier per block parity: with the regions alternating, the compute
+  // warps can be one block ahead of the dV issuer, never two
+  uint64_t dp_full[2], p_ready[2];
   uint64_t kv_done, kv_free, final_bar;
   uint64_t work_full[2], work_empty[2];
   int work_col[2], work_beg[2], work_end[2], work_nvk[2], work_chunk[2];
@@ -100,22 +120,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
-    mbar_init(&sm.kv_empty, 2);
+    mbar_init(&sm.kv_empty, 2);  // the S^T issuer (K) and the dP^T issuer (V)
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.qdo_full[s], 1);
-      mbar_init(&sm.qdo_empty[s], 2);  // issuers A and B
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);   // the dK issuer
+      mbar_init(&sm.do_full[s], 1);
+      mbar_init(&sm.do_empty[s], 1);  // the dV issuer
       mbar_init(&sm.work_full[s], 1);
-      mbar_init(&sm.work_empty[s], 2 + kCompute);
+      mbar_init(&sm.work_empty[s], 3 + kCompute);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.dp_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.dp_full[b], 1);
+      mbar_init(&sm.p_ready[b], kCompute);
+    }
     mbar_init(&sm.dp_free, kCompute);
-    mbar_init(&sm.p_ready, kCompute);
     mbar_init(&sm.ds_ready, kCompute);
     mbar_init(&sm.ds_empty, 1);
-    mbar_init(&sm.kv_done, 2);
+    mbar_init(&sm.kv_done, 2);  // the dV and the dK issuer
     mbar_init(&sm.kv_free, kCompute);
-    mbar_init(&sm.final_bar, 2);
+    mbar_init(&sm.final_bar, 3);
     sm.abort = 0;
     mbar_init_fence();
   }
@@ -184,28 +208,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int i = P.row_idx[t];
           const long long yq = bh * P.Np + static_cast<long long>(i) * kS;
           const int s = use & 1;
-          if (!W.wait(&sm.qdo_empty[s], ((use >> 1) & 1) ^ 1, 23)) { ok = false; break; }
+          const int nvq = P.n_valid[bh * P.nb + i];
           uint8_t* st = stage(s);
-          sm.stage_i[s] = i;
-          sm.stage_nvq[s] = P.n_valid[bh * P.nb + i];
+          // dO: free once (3) of the block two back is done
+          if (!W.wait(&sm.do_empty[s], ((use >> 1) & 1) ^ 1, 24)) { ok = false; break; }
           if (!P.starve) {  // fault injection: no loads, consumers time out
-            mbar_expect_tx(&sm.qdo_full[s], 2 * kTile + 1024);
-            tma_load_2d(st, &tmQ, &sm.qdo_full[s], 0, static_cast<int>(yq));
-            tma_load_2d(st + kTile / 2, &tmQ, &sm.qdo_full[s], 64, static_cast<int>(yq));
-            tma_load_2d(st + kTile, &tmdO, &sm.qdo_full[s], 0, static_cast<int>(yq));
-            tma_load_2d(st + kTile + kTile / 2, &tmdO, &sm.qdo_full[s], 64, static_cast<int>(yq));
-            bulk_load(st + 2 * kTile, P.nlse2 + yq, 512, &sm.qdo_full[s]);
-            bulk_load(st + 2 * kTile + 512, P.D + yq, 512, &sm.qdo_full[s]);
+            mbar_expect_tx(&sm.do_full[s], kTile);
+            tma_load_2d(st + kTile, &tmdO, &sm.do_full[s], 0, static_cast<int>(yq));
+            tma_load_2d(st + kTile + kTile / 2, &tmdO, &sm.do_full[s], 64, static_cast<int>(yq));
+          }
+          // Q, -LSE log2 e, D: free once (4) of the block two back is done
+          if (!W.wait(&sm.q_empty[s], ((use >> 1) & 1) ^ 1, 23)) { ok = false; break; }
+          sm.stage_i[s] = i;
+          sm.stage_nvq[s] = nvq;
+          if (!P.starve) {
+            mbar_expect_tx(&sm.q_full[s], kTile + 1024);
+            tma_load_2d(st, &tmQ, &sm.q_full[s], 0, static_cast<int>(yq));
+            tma_load_2d(st + kTile / 2, &tmQ, &sm.q_full[s], 64, static_cast<int>(yq));
+            bulk_load(st + 2 * kTile, P.nlse2 + yq, 512, &sm.q_full[s]);
+            bulk_load(st + 2 * kTile + 512, P.D + yq, 512, &sm.q_full[s]);
           }
           ++use;
         }
       }
     }
     __syncwarp();
-  } else if (warp == 9 || warp == 10) {
+  } else if (warp >= 9 && warp <= 11) {
     // ------------------------------------------------------ MMA issuers ----
     if (lane == 0) {
-      const bool is_a = warp == 9;
+      const int role = warp - 9;  // 0: (1) S^T, 1: (3) dV then (2) dP^T, 2: (4) dK
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // A K-major, B K-major
       constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // A K-major, B MN-major
       const uint64_t kd_k = sdesc_sw128(smem_u32(kbuf), 16, 1024);          // K, K-major
@@ -217,7 +248,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto noff = [](int kk) {  // MN-major 16-row step
         return static_cast<uint64_t>((kk * 2048) >> 4);
       };
-      uint32_t use = 0, items = 0, pcnt = 0, dscnt = 0, dpcnt = 0, kvcnt = 0;
+      // (2) dP^T of query block g (CTA-wide count) into its region; the
+      // region held P^T of block g - 1, read by (3) of g - 1, which this same
+      // thread issued before
+      auto issue_dp = [&](uint32_t g) -> bool {
+        const int sq = g & 1;
+        if (!W.wait(&sm.do_full[sq], (g >> 1) & 1, 35)) return false;
+        fence_after();
+        const uint64_t dd = sdesc_sw128(smem_u32(stage(sq) + kTile), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + tm_r((g & 1) ^ 1), vd_k + koff(kk), dd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
+        commit(&sm.dp_full[g & 1]);
+        return true;
+      };
+      uint32_t use = 0, items = 0, kvcnt = 0;
       bool ok = true;
       for (uint32_t it = 0; ok; ++it) {
         const int ws = it & 1;
@@ -225,69 +270,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sm.work_col[ws] < 0) break;
         const int n = sm.work_end[ws] - sm.work_beg[ws];
         if (n > 0) {
-          if (!W.wait(&sm.kv_full, items & 1, 32)) break;
+          if (role != 2 && !W.wait(&sm.kv_full, items & 1, 32)) break;
           ++items;
-          // the previous item's dK / dV have been read out
-          if (kvcnt > 0 && !W.wait(&sm.kv_free, (kvcnt - 1) & 1, 33)) break;
           fence_after();
-          for (int k = 0; k < n; ++k) {
-            const int st = (use + k) & 1;
-            if (!W.wait(&sm.qdo_full[st], ((use + k) >> 1) & 1, 34)) { ok = false; break; }
-            fence_after();
-            const uint64_t qd_k = sdesc_sw128(smem_u32(stage(st)), 16, 1024);
-            const uint64_t qd_n = sdesc_sw128(smem_u32(stage(st)), kTile / 2, 1024);
-            const uint64_t dod_n = sdesc_sw128(smem_u32(stage(st) + kTile), kTile / 2, 1024);
-            if (is_a) {
+          if (role == 0) {
+            for (int k = 0; k < n; ++k) {
+              const uint32_t g = use + k;
+              const int st = g & 1;
+              if (!W.wait(&sm.q_full[st], (g >> 1) & 1, 34)) { ok = false; break; }
+              // S^T of block g goes where dP^T of block g - 1 was: the compute
+              // warps have read it
+              if (g > 0 && !W.wait(&sm.dp_free, (g - 1) & 1, 38)) { ok = false; break; }
+              fence_after();
+              const uint64_t qd_k = sdesc_sw128(smem_u32(stage(st)), 16, 1024);
               // (1) S^T = K Q^T
 #pragma unroll
               for (int kk = 0; kk < kD / 16; ++kk)
-                mma_ss(tmem + TM_S, kd_k + koff(kk), qd_k + koff(kk), id_kk, kk > 0 ? 1u : 0u);
+                mma_ss(tmem + tm_r(g & 1), kd_k + koff(kk), qd_k + koff(kk), id_kk,
+                       kk > 0 ? 1u : 0u);
               commit(&sm.s_full);
-              // (3) dV += P^T dO, once P^T has replaced S^T
-              if (!W.wait(&sm.p_ready, pcnt & 1, 36)) { ok = false; break; }
-              ++pcnt;
+            }
+            if (!ok) break;
+            commit(&sm.kv_empty);
+          } else if (role == 1) {
+            if (!issue_dp(use)) break;
+            // the previous item's dK / dV have been read out
+            if (kvcnt > 0 && !W.wait(&sm.kv_free, (kvcnt - 1) & 1, 33)) break;
+            for (int k = 0; k < n; ++k) {
+              const uint32_t g = use + k;
+              const int st = g & 1;
+              // (3) dV += P^T dO, once P^T has replaced S^T in block g's region
+              if (!W.wait(&sm.p_ready[g & 1], (g >> 1) & 1, 36)) { ok = false; break; }
               fence_after();
+              const uint64_t dod_n = sdesc_sw128(smem_u32(stage(st) + kTile), kTile / 2, 1024);
 #pragma unroll
               for (int kk = 0; kk < kS / 16; ++kk)
-                mma_ts(tmem + TM_DV, tmem + TM_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                       dod_n + noff(kk), id_kn,
-                       (k > 0 || kk > 0) ? 1u : 0u);
-              commit(&sm.qdo_empty[st]);
-            } else {
-              // (2) dP^T of this query block was issued in the previous step
-              // (or just below for the first one); (2) of the next one goes
-              // out as soon as the compute warps have read this dP^T
-              auto issue_dp = [&](uint32_t kq) -> bool {
-                const int sq = (use + kq) & 1;
-                if (kq > 0 && !W.wait(&sm.qdo_full[sq], ((use + kq) >> 1) & 1, 35)) return false;
-                if (dpcnt > 0 && !W.wait(&sm.dp_free, (dpcnt - 1) & 1, 38)) return false;
-                fence_after();
-                const uint64_t dd = sdesc_sw128(smem_u32(stage(sq) + kTile), 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                  mma_ss(tmem + TM_DP, vd_k + koff(kk), dd + koff(kk), id_kk, kk > 0 ? 1u : 0u);
-                commit(&sm.dp_full);
-                ++dpcnt;
-                return true;
-              };
-              if (k == 0 && !issue_dp(0)) { ok = false; break; }
-              if (k + 1 < n && !issue_dp(k + 1)) { ok = false; break; }
+                mma_ts(tmem + TM_DV, tmem + tm_r(g & 1) + (kk >> 2) * 64 + (kk & 3) * 8,
+                       dod_n + noff(kk), id_kn, (k > 0 || kk > 0) ? 1u : 0u);
+              commit(&sm.do_empty[st]);
+              if (k + 1 < n && !issue_dp(g + 1)) { ok = false; break; }
+            }
+            if (!ok) break;
+            commit(&sm.kv_done);
+            commit(&sm.kv_empty);
+          } else {
+            if (kvcnt > 0 && !W.wait(&sm.kv_free, (kvcnt - 1) & 1, 39)) break;
+            for (int k = 0; k < n; ++k) {
+              const uint32_t g = use + k;
+              const int st = g & 1;
               // (4) dK += dS^T Q
-              if (!W.wait(&sm.ds_ready, dscnt & 1, 37)) { ok = false; break; }
-              ++dscnt;
+              if (!W.wait(&sm.ds_ready, g & 1, 37)) { ok = false; break; }
+              if (!W.wait(&sm.q_full[st], (g >> 1) & 1, 30)) { ok = false; break; }
               fence_after();
+              const uint64_t qd_n = sdesc_sw128(smem_u32(stage(st)), kTile / 2, 1024);
 #pragma unroll
               for (int kk = 0; kk < kS / 16; ++kk)
                 mma_ss(tmem + TM_DK, dsd_k + koff(kk), qd_n + noff(kk), id_kn,
                        (k > 0 || kk > 0) ? 1u : 0u);
               commit(&sm.ds_empty);
-              commit(&sm.qdo_empty[st]);
+              commit(&sm.q_empty[st]);
             }
+            if (!ok) break;
+            commit(&sm.kv_done);
           }
-          if (!ok) break;
           use += n;
-          commit(&sm.kv_done);
-          commit(&sm.kv_empty);
           ++kvcnt;
         }
         mbar_arrive(&sm.work_empty[ws]);
@@ -348,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int k = 0; k < n; ++k) {
         const int s_ = (use + k) & 1;
-        // -LSE_i log2 e and D_i arrive with Q_i / dO_i on the stage's barrier
-        ok = ok && W.wait(&sm.qdo_full[s_], ((use + k) >> 1) & 1, 40);
+        // -LSE_i log2 e and D_i arrive with Q_i on the stage's Q barrier
+        ok = ok && W.wait(&sm.q_full[s_], ((use + k) >> 1) & 1, 40);
         // blocks of half a tile: bit 2 qh + kh of an entry's mask set = the
         // query half qh (this column half) does not attend the key half kh
         // (this row's half)
@@ -368,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t sv[32];
-            tmem_ld32(tmem + lb + TM_S + q0 + c * 32, sv);
+            tmem_ld32(tmem + lb + tm_r((use + k) & 1) + q0 + c * 32, sv);
             tmem_ld_wait();
             // two queries per fp32x2 instruction: x = s * c - LSE log2 e
             const f32x2 c2 = pack2(P.scale_log2, P.scale_log2);
@@ -397,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[h * 32 + 2 * e], p[h * 32 + 2 * e + 1]);
-          tmem_st16(tmem + lb + TM_S + q0 + h * 16, pk);
+          tmem_st16(tmem + lb + tm_r((use + k) & 1) + q0 + h * 16, pk);
         }
         tmem_st_wait();
         fence_before();
-        mbar_arrive(&sm.p_ready);
+        mbar_arrive(&sm.p_ready[(use + k) & 1]);
         // ---- dS^T = P^T * (dP^T - D) -> smem panel `half` (128-byte swizzle) ----
-        ok = ok && W.wait(&sm.dp_full, dpcnt & 1, 43);
+        ok = ok && W.wait(&sm.dp_full[dpcnt & 1], (dpcnt >> 1) & 1, 43);
         ++dpcnt;
         if (dsidx > 0) ok = ok && W.wait(&sm.ds_empty, (dsidx - 1) & 1, 44);
         ok = __all_sync(0xffffffffu, ok);
@@ -413,11 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t dp[32];
-            tmem_ld32(tmem + lb + TM_DP + q0 + c * 32, dp);
+            tmem_ld32(tmem + lb + tm_r(((use + k) & 1) ^ 1) + q0 + c * 32, dp);
             tmem_ld_wait();
             if (c == 1) {
               fence_before();
-              mbar_arrive(&sm.dp_free);  // issuer B may start the next dP^T
+              mbar_arrive(&sm.dp_free);  // the next S^T may be written here
             }
 #pragma unroll
             for (int g = 0; g < 4; ++g) {  // 8 queries = one 16-byte chunk

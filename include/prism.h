@@ -156,7 +156,9 @@ typedef struct prism_plan prism_plan_t;
 /* Validate `cfg` and build a host plan.  Errors: PRISM_ERR_ARG (sizes,
  * thresholds not descending), PRISM_ERR_UNSUPPORTED (a menu token count that
  * is not 1, 2 or 4 times block_tokens, d, S), PRISM_ERR_NO_ADMISSIBLE_SHAPE
- * (a class with no menu shape that divides the zone). */
+ * (a class with no menu shape that divides the zone, or a menu whose only
+ * class is half a tile on a grid with padded zones: a padded zone needs a
+ * class of at least a tile). */
 int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out);
 void prism_plan_destroy(prism_plan_t* plan);
 int prism_plan_query(const prism_plan_t* plan, prism_sizes_t* out);

@@ -127,3 +127,18 @@ def test_key_range_setting_is_validated_and_sized(L):
     # ranges larger than the head: one range, no partial-result workspace
     q = prism.Plan(w, key_chunk_blocks=10_000)
     assert q.sz.key_chunks == 1 and q.sz.ws_bytes < p.sz.ws_bytes
+
+
+def test_half_tile_only_menu_needs_a_grid_without_padding(L):
+    """Only C64 (Table 9) on the tensor cores: 64-token blocks share 128-row
+    tiles, so every zone must be full; on a grid without padding the plan
+    takes the tensor-core path, on the 2K grid (H = 90, T = 21: padded
+    zones) it is rejected, since a padded zone needs a class of at least a
+    tile."""
+    small = synth.WORKLOADS["720p"].with_(T=8, Hg=32, W=48, H=2, zone=(4, 16, 16),
+                                          menu=synth.MENU_64, class_tau=(), name="only_c64_tc")
+    p = prism.Plan(small)
+    assert (p.sz.half_tile, p.sz.n_classes, p.sz.tensor_core_fwd, p.sz.tensor_core_bwd) == (1, 1, 1, 1)
+    with pytest.raises(prism.PrismError) as e:
+        prism.Plan(synth.WORKLOADS["2k"].with_(menu=synth.MENU_64, zone=(4, 16, 16), class_tau=()))
+    assert prism.ERRORS[e.value.code] == "PRISM_ERR_NO_ADMISSIBLE_SHAPE"

@@ -99,6 +99,20 @@ def test_only_c64_menu():
     assert rep["O_max_rel"] <= pu.O_TOL
 
 
+def test_only_c64_on_tensor_cores():
+    """"Only C64" (Table 9) on the tensor cores: the 64-token menu with a
+    128-row tile, so two 64-token blocks share every tile and each listed tile
+    pair carries a sub-tile mask; the grid has no padding (a padded zone would
+    need a class of at least a tile)."""
+    w = synth.WORKLOADS["720p"].with_(T=8, Hg=32, W=48, H=2, n_src=1, zone=(4, 16, 16),
+                                      menu=_table11_class(64), class_tau=(), name="only_c64_tc")
+    plan = prism.Plan(w)
+    assert plan.sz.half_tile == 1 and plan.sz.tensor_core_fwd == 1 and plan.sz.tensor_core_bwd == 1
+    rep = pu.compare(w)
+    assert rep["half_tile_blocks"] > 0 and rep["masked_entries"] > 0
+    assert rep["O_max_rel"] <= pu.O_TOL
+
+
 def test_fixed_8cubed_512_token_blocks():
     """Fixed 8^3 (Table 9): the single 512-token shape (8, 8, 8) on 8 x 16 x 16
     zones; every block spans four 128-slot tiles of the tensor-core kernels."""
