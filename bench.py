@@ -54,9 +54,9 @@ def pair_flops(w):
 # plan's number of key ranges; reported only for that workload and range count,
 # and as null once the kernel's code has changed since.
 TRAFFIC_2K = {
-    "attn_fwd_tc_kernel": ("attn_tc.cu", "e62fc53d1541ffef", 3, 24.18e9 + 5.50e9),
-    "attn_dkdv_tc_kernel": ("attn_tc_dkdv.cu", "280e701045147215", 3, 20.39e9 + 11.89e9),
-    "attn_dq_tc_kernel": ("attn_tc_dq.cu", "667fec371cf742e6", 3, 32.84e9 + 4.98e9),
+    "attn_fwd_tc_kernel": ("attn_tc.cu", "e62fc53d1541ffef", 3, 24.24e9 + 5.50e9),
+    "attn_dkdv_tc_kernel": ("attn_tc_dkdv.cu", "779df76c79c99244", 3, 20.39e9 + 11.89e9),
+    "attn_dq_tc_kernel": ("attn_tc_dq.cu", "667fec371cf742e6", 3, 32.88e9 + 4.98e9),
 }
 
 
