@@ -53,6 +53,18 @@ def test_fixed_4cubed_64_token_blocks():
     pu.compare(w, shape_id=np.zeros((w.B, w.H, w.n_zones), np.uint8))
 
 
+def test_fixed_4cubed_on_tensor_cores():
+    """Fixed 4^3 on the tensor cores: the single 64-token shape with a 128-row
+    tile, so two blocks share every tile (sub-tile masks); shapes given by the
+    caller, grid without padding."""
+    w = synth.WORKLOADS["720p"].with_(T=8, Hg=32, W=48, H=2, n_src=1, zone=(4, 16, 16),
+                                      menu=((4, 4, 4),), class_tau=(), name="fixed4_tc")
+    plan = prism.Plan(w)
+    assert plan.sz.half_tile == 1 and plan.sz.tensor_core_fwd == 1
+    rep = pu.compare(w, shape_id=np.zeros((w.B, w.H, w.n_zones), np.uint8))
+    assert rep["half_tile_blocks"] > 0 and rep["O_max_rel"] <= pu.O_TOL
+
+
 def test_shape_that_does_not_tile_the_zone_is_reported():
     """3 x 16 x 16 zones admit only (1, 8, 16) and (1, 16, 8); a given
     (2, 8, 8) or an index past the menu is reported in the status word and
