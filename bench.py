@@ -558,6 +558,17 @@ def sweep(args):
     w8 = w2.with_(name="2k_fixed_8cubed", zone=(8, 16, 16), menu=((8, 8, 8),))
     cases.append((w8, np.zeros((w8.B, w8.H, w8.n_zones), np.uint8)))
     cases.append((w2.with_(name="2k_only_c256", zone=(4, 16, 16), menu=synth.MENU_256), None))
+    # the 64-token baselines (Only C64, Fixed 4^3) share 128-row tiles between
+    # two blocks, which needs zones without padding: a 2K-wide grid of 24 x 96
+    # x 160 tokens (4 x 16 x 16 zones, 24 heads), with the 128-token menu on
+    # the same grid beside them
+    w96 = w2.with_(name="2k96_c128", T=24, Hg=96, zone=(4, 16, 16))
+    cases.append((w96, None))
+    cases.append((w96.with_(name="2k96_only_c64", menu=synth.MENU_64, class_tau=()), None))
+    w4 = w96.with_(name="2k96_fixed_4cubed", menu=((4, 4, 4),), class_tau=())
+    cases.append((w4, np.zeros((w4.B, w4.H, w4.n_zones), np.uint8)))
+    if args.sweep_filter:
+        cases = [(w, sid) for w, sid in cases if args.sweep_filter in w.name]
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     build.build()
@@ -783,6 +794,8 @@ def main():
                     help="override the workload's head count (smaller cases for profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="one line per workload of the measurement plan (not the contract line)")
+    ap.add_argument("--sweep-filter", default="",
+                    help="with --sweep: only the workloads whose name contains this text")
     args = ap.parse_args()
     if args.sweep:
         sweep(args)
