@@ -36,10 +36,10 @@ import torch  # noqa: E402
 from content_adaptive_block_02_b300 import build, prism, synth  # noqa: E402
 
 METRIC = "sparse-attn fwd+bwd ms & effective TFLOP/s at 2K grid; % of bf16 tensor peak"
-# kernels one step launches: statistics, assign, permute_pool, score, select
-# fast / fallback, 2 scans, CSR fill, CSC count and fill, forward, unpermute
-# (O), permute (dO), bwd_pre, dK/dV, dQ, unpermute (dQ, dK, dV)
-KERNELS_PER_STEP = 20
+# kernels one step launches: statistics, assign, permute_pool, score digits,
+# score product, select fast / fallback, 2 scans, CSR fill, CSC count and fill,
+# forward, unpermute (O), permute (dO), bwd_pre, dK/dV, dQ, unpermute (dQ, dK, dV)
+KERNELS_PER_STEP = 21
 
 
 def pair_flops(w):

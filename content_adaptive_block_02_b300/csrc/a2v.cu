@@ -260,20 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// 2-D map over a [rows, cols] bf16 matrix (cols a multiple of 64), boxes of
-// 64 channels x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 size_t a2v_smem_bytes(int Ca, int Na) {
@@ -296,9 +282,9 @@ cudaError_t launch_a2v_norms(const Plan& p, const uint16_t* Qa, const uint16_t* 
   a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(c.Ca)));
   a.limit = c.timeout_cycles ? c.timeout_cycles : 4000000000ull;
   CUtensorMap tmQ, tmK, tmV;
-  if (!make_map(&tmQ, Qa, static_cast<long long>(c.B) * p.sz.N, c.Ca, kRows) ||
-      !make_map(&tmK, Ka, static_cast<long long>(c.B) * Na, c.Ca, a.Na_pad) ||
-      !make_map(&tmV, Va, static_cast<long long>(c.B) * Na, c.Ca, a.Na_pad))
+  if (!make_bf16_map(&tmQ, Qa, static_cast<long long>(c.B) * p.sz.N, c.Ca, kRows) ||
+      !make_bf16_map(&tmK, Ka, static_cast<long long>(c.B) * Na, c.Ca, a.Na_pad) ||
+      !make_bf16_map(&tmV, Va, static_cast<long long>(c.B) * Na, c.Ca, a.Na_pad))
     return cudaErrorInvalidValue;
   const size_t smem = a2v_smem_bytes(c.Ca, Na);
   cudaError_t e = cudaFuncSetAttribute(a2v_norm_tc_kernel,

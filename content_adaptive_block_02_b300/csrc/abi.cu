@@ -257,6 +257,10 @@ int prism_plan_create(const prism_config_t* cfg, prism_plan_t** out) {
     p.off_ml = off;
     off = align256(off + static_cast<size_t>(rows) * z.key_chunks * c.block_tokens * 8);
   }
+  // digits and exponents of the block means for the tensor-core scores
+  p.off_digits = off;
+  off = align256(off + score_digit_bytes(p));
+  z.ws_scores = p.off_scores;
   z.ws_bytes = off;
   prism_plan* h = static_cast<prism_plan*>(malloc(sizeof(prism_plan)));
   if (h == nullptr) return PRISM_ERR_ARG;

@@ -21,6 +21,7 @@ struct Plan {
   size_t off_rowcnt, off_colcnt, off_amb, off_bitmask, off_scores, off_D, off_lse2, off_dq;
   size_t off_part, off_ml;  // key-range partial results (key_chunks > 1)
   size_t off_nsel, off_bstart, off_tbitmask;  // multi-tile blocks (sz.multi_tile)
+  size_t off_digits;  // score digits and exponents of the block means
 };
 
 // Workspace layout (bytes from the start of ws, each region 256-aligned):
@@ -44,6 +45,9 @@ struct Plan {
 //                                        kernel's partial dQ (first half)
 //   off_ml          fp32  [B*H*nb, C, S, 2] per key range: running max (log2 units)
 //                                        and row sum of the forward
+//   off_digits      bf16  2 x [7, B*H*nslots, dpad] 7-bit digits of the query and
+//                                        key block means (score_tc.cu), then int32
+//                                        2 x [B*H*nslots] their exponents
 enum : int {
   WS_STATUS = 0,      // uint32: first device error code (0 = none)
   WS_AMB_COUNT = 1,   // uint32: number of ambiguous rows appended by the select kernel
@@ -85,6 +89,13 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
                           int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
                           int32_t* row_idx, uint8_t* ws, cudaStream_t st,
                           cudaEvent_t score_begin = nullptr, cudaEvent_t score_end = nullptr);
+
+// Block scores on the tensor cores (exact digit products): Shi / Slo
+// [B*H, nslots, nslots] from the double-float block means.
+cudaError_t launch_score_tc(const Plan& p, const float* Qh, const float* Ql, const float* Kh,
+                            const float* Kl, float* Shi, float* Slo, uint8_t* ws,
+                            cudaStream_t st);
+size_t score_digit_bytes(const Plan& p);  // workspace bytes at off_digits
 
 // ----------------------------------------------------- device helpers -----
 

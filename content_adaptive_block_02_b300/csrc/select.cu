@@ -13,10 +13,10 @@
 // candidates when none is, or when p >= 1).
 //
 // Precision.  The block lists must not depend on rounding.  Scores are
-// computed for every pair in double-float arithmetic (hi + lo fp32 pairs,
-// compensated dot product Dot2 of Ogita, Rump and Oishi, SIAM J. Sci. Comput.
-// 2005) from the double-float block means, which puts their error near 1e-9.
-// The selection then runs on those scores with fp32 weights exp(s - max)
+// computed for every pair as double-float (hi + lo fp32 pairs) from the
+// double-float block means by an error-free splitting of the product into
+// exact integer digit products on the tensor cores (score_tc.cu), with an
+// error near 2e-12 max|q| max|k|, below the block means' own.  The selection then runs on those scores with fp32 weights exp(s - max)
 // (CUDA expf, 2 ulp) and compensated sums, so every cumulative weight carries
 // an error below 4e-7.  A query block whose decision lies within 1e-6 of a
 // boundary (cumulative weight near p, or a score gap at the cut) is decided
@@ -37,89 +37,6 @@ __device__ __forceinline__ uint32_t fkey(float f) {
 }
 __device__ __forceinline__ float fkey_inv(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// ------------------------------------------------ Dot2 score GEMM ---------
-// S[bh][i][j] = Qbar_i . Kbar_j (unscaled) in double-float: for every term the
-// product hi*hi is split exactly (TwoProduct by FMA), the cross terms
-// hi*lo + lo*hi are added in fp32, and the running sum is kept as an
-// unevaluated pair with TwoSum.  Tile 64 (i) x 128 (j) per CTA, 256 threads
-// with a 4 x 8 register tile, channels staged 16 at a time (transposed).
-constexpr int kTI = 64, kTJ = 128, kBK = 16;
-
-__global__ void __launch_bounds__(256) score_dot2_kernel(int nb, int d,
-                                                         const float* __restrict__ Qh,
-                                                         const float* __restrict__ Ql,
-                                                         const float* __restrict__ Kh,
-                                                         const float* __restrict__ Kl,
-                                                         float* __restrict__ Shi,
-                                                         float* __restrict__ Slo) {
-  __shared__ __align__(16) float Ah[kBK][kTI + 4], Al[kBK][kTI + 4];
-  __shared__ __align__(16) float Bh[kBK][kTJ + 4], Bl[kBK][kTJ + 4];
-  const int bh = blockIdx.z;
-  const int i0 = blockIdx.y * kTI, j0 = blockIdx.x * kTJ;
-  const long long ob = static_cast<long long>(bh) * nb * d;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float sh[4][8], sc[4][8];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 8; ++b) sh[a][b] = sc[a][b] = 0.f;
-  for (int c0 = 0; c0 < d; c0 += kBK) {
-    for (int e = threadIdx.x; e < kTI * kBK; e += 256) {
-      const int r = e / kBK, cc = e % kBK, gi = i0 + r;
-      const bool ok = gi < nb;
-      const long long o = ob + static_cast<long long>(gi) * d + c0 + cc;
-      Ah[cc][r] = ok ? Qh[o] : 0.f;
-      Al[cc][r] = ok ? Ql[o] : 0.f;
-    }
-    for (int e = threadIdx.x; e < kTJ * kBK; e += 256) {
-      const int r = e / kBK, cc = e % kBK, gj = j0 + r;
-      const bool ok = gj < nb;
-      const long long o = ob + static_cast<long long>(gj) * d + c0 + cc;
-      Bh[cc][r] = ok ? Kh[o] : 0.f;
-      Bl[cc][r] = ok ? Kl[o] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int cc = 0; cc < kBK; ++cc) {
-      const float4 ah4 = *reinterpret_cast<const float4*>(&Ah[cc][ty * 4]);
-      const float4 al4 = *reinterpret_cast<const float4*>(&Al[cc][ty * 4]);
-      const float4 bh0 = *reinterpret_cast<const float4*>(&Bh[cc][tx * 4]);
-      const float4 bh1 = *reinterpret_cast<const float4*>(&Bh[cc][64 + tx * 4]);
-      const float4 bl0 = *reinterpret_cast<const float4*>(&Bl[cc][tx * 4]);
-      const float4 bl1 = *reinterpret_cast<const float4*>(&Bl[cc][64 + tx * 4]);
-      const float ah[4] = {ah4.x, ah4.y, ah4.z, ah4.w}, al[4] = {al4.x, al4.y, al4.z, al4.w};
-      const float bhv[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
-      const float blv[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 8; ++y) {
-          const float p = __fmul_rn(ah[x], bhv[y]);
-          const float pe = fmaf(ah[x], bhv[y], -p);
-          const float cross = fmaf(ah[x], blv[y], __fmul_rn(al[x], bhv[y]));
-          const df t = two_sum(sh[x][y], p);
-          sh[x][y] = t.hi;
-          sc[x][y] = __fadd_rn(sc[x][y], __fadd_rn(t.lo, __fadd_rn(pe, cross)));
-        }
-    }
-    __syncthreads();
-  }
-  const long long os = static_cast<long long>(bh) * nb * nb;
-#pragma unroll
-  for (int x = 0; x < 4; ++x) {
-    const int gi = i0 + ty * 4 + x;
-    if (gi >= nb) continue;
-#pragma unroll
-    for (int y = 0; y < 8; ++y) {
-      const int gj = j0 + (y < 4 ? tx * 4 + y : 64 + tx * 4 + y - 4);
-      if (gj >= nb) continue;
-      const df r = fast_two_sum(sh[x][y], sc[x][y]);
-      Shi[os + static_cast<long long>(gi) * nb + gj] = r.hi;
-      Slo[os + static_cast<long long>(gi) * nb + gj] = r.lo;
-    }
-  }
 }
 
 // ------------------------------------------------- fast selection ----------
@@ -768,10 +685,9 @@ cudaError_t launch_select(const Plan& p, const uint8_t* shape_id, const float* Q
         c.block_tokens, ext, shape_id, n_valid, n_sel, bstart);
     n_valid = n_sel;
   }
-  dim3 g((nb + kTJ - 1) / kTJ, (nb + kTI - 1) / kTI, c.B * c.H);
-  // optional timing marks around the score kernel alone
+  // optional timing marks around the score kernels alone
   if (score_begin != nullptr && (e = cudaEventRecord(score_begin, st)) != cudaSuccess) return e;
-  score_dot2_kernel<<<g, 256, 0, st>>>(nb, c.d, Qh, Ql, Kh, Kl, Shi, Slo);
+  if ((e = launch_score_tc(p, Qh, Ql, Kh, Kl, Shi, Slo, ws, st)) != cudaSuccess) return e;
   if (score_end != nullptr && (e = cudaEventRecord(score_end, st)) != cudaSuccess) return e;
   SelParams sp;
   sp.nb = nb;

@@ -152,6 +152,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 16 columns of 32-bit (thread i: columns [col, col+16) of lane i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -264,6 +274,9 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // Host helpers shared by the tensor-core launchers.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 bool make_tile_map(CUtensorMap* m, const void* base, long long rows);
+// 2-D map over a [rows, cols] bf16 matrix (cols a multiple of 64), boxes of
+// 64 columns x box_rows rows, 128-byte swizzle.
+bool make_bf16_map(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
 int sm_count();
 
 }  // namespace prism

@@ -74,7 +74,7 @@ class Sizes(ctypes.Structure):
         ("n_classes", ctypes.c_int), ("class_tokens", ctypes.c_int * MAX_CLASSES),
         ("multi_tile", ctypes.c_int), ("slot_tokens", ctypes.c_int), ("nslots", ctypes.c_int),
         ("half_tile", ctypes.c_int), ("ws_csr_mask", ctypes.c_size_t),
-        ("ws_csc_mask", ctypes.c_size_t),
+        ("ws_csc_mask", ctypes.c_size_t), ("ws_scores", ctypes.c_size_t),
     ]
 
 

@@ -149,6 +149,11 @@ typedef struct prism_sizes {
                              bit 2 qh + kh set = the query tile's half qh does NOT
                              attend the key tile's half kh (0: the whole pair) */
   size_t ws_csc_mask;     /* half_tile: likewise for the CSC entries (row_idx) */
+  size_t ws_scores;       /* workspace offset of the block scores that
+                             prism_block_select writes: the unscaled dots
+                             Qbar_i . Kbar_j as double-float, fp32 hi
+                             [B, H, nslots, nslots] followed by fp32 lo of the
+                             same shape (read-only for callers; tests) */
 } prism_sizes_t;
 
 typedef struct prism_plan prism_plan_t;
