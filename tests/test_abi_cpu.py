@@ -142,3 +142,19 @@ def test_half_tile_only_menu_needs_a_grid_without_padding(L):
     with pytest.raises(prism.PrismError) as e:
         prism.Plan(synth.WORKLOADS["2k"].with_(menu=synth.MENU_64, zone=(4, 16, 16), class_tau=()))
     assert prism.ERRORS[e.value.code] == "PRISM_ERR_NO_ADMISSIBLE_SHAPE"
+
+
+@pytest.mark.parametrize("name", ["tiny", "720p", "2k"])
+def test_score_region_lies_inside_the_workspace(L, name):
+    """The block scores (fp32 hi then lo, [B, H, nslots, nslots] each) sit at
+    a 256-aligned offset inside ws_bytes, and the workspace also holds the
+    scores' seven bf16 digit slices of the query and key block means (d
+    rounded up to 64 channels) and their int32 exponents after them."""
+    w = synth.WORKLOADS[name]
+    p = prism.Plan(w)
+    R = w.B * w.H * p.sz.nslots
+    score_bytes = 2 * 4 * R * p.sz.nslots
+    digit_bytes = 2 * (7 * R * ((w.d + 63) // 64 * 64) * 2 + 256) + 2 * 4 * R
+    assert p.sz.ws_scores % 256 == 0 and p.sz.ws_scores >= 256
+    assert p.sz.ws_scores + score_bytes <= p.sz.ws_bytes
+    assert p.sz.ws_bytes >= score_bytes + digit_bytes
